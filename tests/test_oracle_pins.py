@@ -1,0 +1,407 @@
+"""Pins of the CPU oracle against what the pages and mathematics fix.
+
+Each test checks an oracle function against something other than itself:
+the pages' stated acceptance semantics (golden cases), closed forms,
+invariants, brute-force loops on tiny inputs, or a library routine that the
+special case reduces to.  None of these tests needs a GPU.
+"""
+import itertools
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle as O
+from workload import get_config, make_weights, feature_rows
+from workload.gen import splitmix64_bits, f64_to_bf16_bits, bf16_bits_to_f32
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+rng = np.random.default_rng(1234)
+
+
+# ------------------------------------------------------------------ generator
+
+def test_splitmix64_published_vector():
+    # SplitMix64 reference outputs for initial state 1234567.
+    got = splitmix64_bits(1234567, np.arange(5)).tolist()
+    assert got == [6457827717110365317, 3203168211198807973, 9817491932198370423,
+                   4593380528125082431, 16408922859458223821]
+
+
+def test_bf16_rounding_nearest_even():
+    x = np.array([1.0, 1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, -2.5, 0.0, 1.0 + 2 ** -9])
+    b = f64_to_bf16_bits(x)
+    back = bf16_bits_to_f32(b).astype(np.float64)
+    # 1+2^-8 is a tie between 1 and 1+2^-7: even mantissa (1.0) wins;
+    # 1+3*2^-8 ties between 1+2^-7 and 1+2^-6 -> 1+2^-6 (even).
+    assert back.tolist() == [1.0, 1.0, 1.0 + 2 ** -6, -2.5, 0.0, 1.0]
+
+
+# ------------------------------------------------------------------ a7 accept
+
+def _brute_accept(draft, target):
+    """Scan from the block head until the first mismatch (no cumprod)."""
+    i = 0
+    while i < 15 and draft[i] == target[i]:
+        i += 1
+    return i + 1, target[i]
+
+
+def _load_accept_cases():
+    cases = []
+    with open(os.path.join(GOLDEN, "accept_cases.txt")) as f:
+        for line in f:
+            if not line.strip() or line.startswith("#"):
+                continue
+            name, d, t, tau, bonus = [s.strip() for s in line.split("|")]
+            cases.append((name, [int(x) for x in d.split()], [int(x) for x in t.split()],
+                          int(tau), int(bonus)))
+    return cases
+
+
+@pytest.mark.parametrize("case", _load_accept_cases(), ids=lambda c: c[0])
+def test_accept_golden(case):
+    _, d, t, tau, bonus = case
+    assert O.accept_longest_prefix(np.array(d), np.array(t)) == (tau, bonus)
+
+
+def test_accept_exhaustive_all_masks():
+    """All 2^15 match patterns: cumprod form == first-mismatch scan, tau in [1,16]."""
+    base = np.arange(100, 115)
+    for bits in range(1 << 15):
+        mism = np.array([(bits >> i) & 1 for i in range(15)], dtype=bool)
+        target = np.concatenate([np.where(mism, base + 1000, base), [7]])
+        tau, bonus = O.accept_longest_prefix(base, target)
+        assert (tau, bonus) == _brute_accept(base, target)
+        assert 1 <= tau <= 16
+
+
+def test_accept_mean_closed_form():
+    """With i.i.d. matches of probability p, E[tau] = (1 - p^16) / (1 - p)."""
+    p, R = 0.8, 40000
+    r = np.random.default_rng(7)
+    draft = np.arange(15)
+    taus = []
+    for _ in range(R):
+        m = r.random(16) < p
+        u = r.integers(0, 4096, 16)
+        t = O.synthetic_target(draft, m, u, 4096)
+        taus.append(O.accept_longest_prefix(draft, t)[0])
+    expect = (1 - p ** 16) / (1 - p)
+    se = np.std(taus) / np.sqrt(R)
+    assert abs(np.mean(taus) - expect) < 5 * se
+
+
+def test_synthetic_target_depends_only_on_matches():
+    V = 50
+    r = np.random.default_rng(3)
+    for _ in range(500):
+        m = r.random(16) < 0.7
+        u = r.integers(0, V, 16)
+        d1 = r.integers(0, V, 15)
+        d2 = r.integers(0, V, 15)
+        t1 = O.synthetic_target(d1, m, u, V)
+        t2 = O.synthetic_target(d2, m, u, V)
+        lead = 0
+        while lead < 15 and m[lead]:
+            lead += 1
+        assert O.accept_longest_prefix(d1, t1)[0] == lead + 1
+        assert O.accept_longest_prefix(d2, t2)[0] == lead + 1
+        for i in range(15):
+            assert (t1[i] == d1[i]) == bool(m[i])
+            assert 0 <= t1[i] < V
+
+
+# ------------------------------------------------------------------ norms, rope
+
+def test_rmsnorm_closed_form_and_library():
+    x = rng.standard_normal((7, 33)) * 3.0
+    g = 1.0 + 0.1 * rng.standard_normal(33)
+    y = O.rmsnorm(x, g, 0.0)
+    # RMS of y/g is exactly 1 with eps = 0
+    np.testing.assert_allclose(np.sqrt(np.mean((y / g) ** 2, -1)), 1.0, rtol=1e-12)
+    # scale invariance
+    np.testing.assert_allclose(O.rmsnorm(5.0 * x, g, 0.0), y, rtol=1e-12)
+    # torch's RMSNorm routine
+    ref = F.rms_norm(torch.from_numpy(x), (33,), torch.from_numpy(g), eps=1e-6).numpy()
+    np.testing.assert_allclose(O.rmsnorm(x, g, 1e-6), ref, rtol=1e-12, atol=1e-14)
+
+
+def test_rope_complex_rotation_textbook():
+    """Rotate-half RoPE == complex multiply of (x_i + j x_{i+D/2}) by exp(j p theta^(-2i/D))."""
+    D, theta = 16, 1e4
+    x = rng.standard_normal((5, 3, D))
+    pos = np.array([0, 1, 7, 100, 12345])
+    got = O.rope(x, pos, theta)
+    z = x[..., :D // 2] + 1j * x[..., D // 2:]
+    w = np.exp(1j * pos[:, None, None] * theta ** (-np.arange(D // 2) * 2.0 / D))
+    r = z * w
+    np.testing.assert_allclose(got, np.concatenate([r.real, r.imag], -1), rtol=1e-12, atol=1e-12)
+
+
+def test_rope_identity_norm_relative():
+    D, theta = 64, 1e6
+    x = rng.standard_normal((4, 2, D))
+    np.testing.assert_array_equal(O.rope(x, np.zeros(4), theta), x)
+    y = O.rope(x, np.array([3, 50, 999, 32000]), theta)
+    np.testing.assert_allclose(np.linalg.norm(y, axis=-1), np.linalg.norm(x, axis=-1), rtol=1e-12)
+    q = rng.standard_normal((1, 1, D))
+    k = rng.standard_normal((1, 1, D))
+    dots = [np.sum(O.rope(q, np.array([m + s]), theta) * O.rope(k, np.array([n + s]), theta))
+            for (m, n, s) in [(10, 3, 0), (10, 3, 500), (10, 3, 30000)]]
+    np.testing.assert_allclose(dots, dots[0], rtol=1e-9)
+
+
+# ------------------------------------------------------------------ a5 attention
+
+def _brute_attention(q, K, V):
+    S, hq, D = q.shape
+    n, hkv, _ = K.shape
+    out = np.zeros_like(q)
+    for j in range(hq):
+        kv = j // (hq // hkv)
+        for i in range(S):
+            s = [sum(q[i, j, d] * K[t, kv, d] for d in range(D)) / np.sqrt(D) for t in range(n)]
+            mx = max(s)
+            e = [np.exp(x - mx) for x in s]
+            z = sum(e)
+            for d in range(D):
+                out[i, j, d] = sum(e[t] * V[t, kv, d] for t in range(n)) / z
+    return out
+
+
+def test_attention_bruteforce_tiny():
+    q = rng.standard_normal((4, 4, 8))
+    K = rng.standard_normal((9, 2, 8))
+    V = rng.standard_normal((9, 2, 8))
+    np.testing.assert_allclose(O.block_attention(q, K, V), _brute_attention(q, K, V), rtol=1e-11)
+
+
+@pytest.mark.parametrize("L,hq,hkv", [(0, 4, 4), (0, 8, 2), (37, 8, 2), (130, 8, 1)])
+def test_attention_equals_library_sdpa_unmasked(L, hq, hkv):
+    S, D = 16, 32
+    q = rng.standard_normal((S, hq, D))
+    K = rng.standard_normal((L + S, hkv, D))
+    V = rng.standard_normal((L + S, hkv, D))
+    rep = hq // hkv
+    qt = torch.from_numpy(q).permute(1, 0, 2)
+    kt = torch.from_numpy(K).permute(1, 0, 2).repeat_interleave(rep, 0)
+    vt = torch.from_numpy(V).permute(1, 0, 2).repeat_interleave(rep, 0)
+    ref = F.scaled_dot_product_attention(qt, kt, vt, is_causal=False).permute(1, 0, 2).numpy()
+    np.testing.assert_allclose(O.block_attention(q, K, V), ref, rtol=1e-10, atol=1e-12)
+
+
+def test_attention_context_permutation_invariant():
+    q = rng.standard_normal((16, 4, 16))
+    K = rng.standard_normal((50, 2, 16))
+    V = rng.standard_normal((50, 2, 16))
+    p = rng.permutation(50)
+    np.testing.assert_allclose(O.block_attention(q, K[p], V[p]), O.block_attention(q, K, V),
+                               rtol=1e-10)
+
+
+def test_attention_block_is_not_causal():
+    """The first block row must see the last block key (no causal mask)."""
+    q = rng.standard_normal((16, 2, 8))
+    K = rng.standard_normal((16, 2, 8))
+    V = rng.standard_normal((16, 2, 8))
+    V2 = V.copy()
+    V2[15] += 10.0
+    a = O.block_attention(q, K, V)
+    b = O.block_attention(q, K, V2)
+    assert np.abs(a[0] - b[0]).max() > 1e-3
+
+
+def test_attention_rope_shift_invariance():
+    """Shifting all positions (context and block) by a constant leaves attention unchanged."""
+    D, theta = 32, 1e6
+    q = rng.standard_normal((16, 4, D))
+    k = rng.standard_normal((16 + 40, 2, D))
+    v = rng.standard_normal((16 + 40, 2, D))
+    pk = np.arange(56)
+    pq = np.arange(40, 56)
+    a = O.block_attention(O.rope(q, pq, theta), O.rope(k, pk, theta), v)
+    b = O.block_attention(O.rope(q, pq + 777, theta), O.rope(k, pk + 777, theta), v)
+    np.testing.assert_allclose(a, b, rtol=1e-8, atol=1e-10)
+
+
+# ------------------------------------------------------------------ a1 fusion
+
+def test_fusion_selects_layers_shallow_to_deep():
+    cfg = get_config("tiny").with_(gain_std=0.1)
+    w = make_weights(cfg)
+    H = cfg.hidden
+    feats = feature_rows(cfg, 0, 0, 6)
+    ff = O.bf16_to_f64(feats)
+    for layer in (0, 4):
+        fc = np.zeros((H, 5 * H))
+        fc[:, layer * H:(layer + 1) * H] = np.eye(H)
+        w2 = dict(w)
+        w2["fc"] = f64_to_bf16_bits(fc)
+        m = O.OracleModel(cfg, w2)
+        c = O.fuse_features(m, feats)
+        ref = F.rms_norm(torch.from_numpy(ff[:, layer]), (H,),
+                         torch.from_numpy(m.w("fc_norm")), eps=cfg.rms_eps).numpy()
+        np.testing.assert_allclose(c, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_fusion_feature_scale_invariance():
+    cfg = get_config("tiny")
+    m = O.OracleModel(cfg, make_weights(cfg))
+    f = O.bf16_to_f64(feature_rows(cfg, 0, 3, 4))
+    # equal up to the eps term: relative change <= eps / (2 * mean square)
+    np.testing.assert_allclose(O.fuse_features(m, 8.0 * f), O.fuse_features(m, f), rtol=1e-5)
+
+
+# ------------------------------------------------------------------ a2 inject
+
+def test_inject_k_norm_and_rope_properties():
+    cfg = get_config("tiny-gains")
+    m = O.OracleModel(cfg, make_weights(cfg))
+    c = rng.standard_normal((5, cfg.hidden))
+    k0, v0 = O.inject_kv(m, 1, c, np.zeros(5))
+    # at position 0 RoPE is the identity: the k-normed vector divided by its
+    # gain has RMS 1 (up to eps)
+    g = m.w("k_norm", 1)
+    rms = np.sqrt(np.mean((k0 / g) ** 2, -1))
+    np.testing.assert_allclose(rms, 1.0, rtol=1e-4)
+    k1, v1 = O.inject_kv(m, 1, c, np.arange(5) + 1000)
+    np.testing.assert_allclose(np.linalg.norm(k1, axis=-1), np.linalg.norm(k0, axis=-1), rtol=1e-12)
+    np.testing.assert_array_equal(v0, v1)
+    # V is the plain projection by the layer's V rows
+    D, hq, hkv = cfg.head_dim, cfg.n_q_heads, cfg.n_kv_heads
+    wv = m.w("wqkv", 1)[(hq + hkv) * D:]
+    np.testing.assert_allclose(v0.reshape(5, -1), c @ wv.T, rtol=1e-12)
+
+
+# ------------------------------------------------------------------ a4 layer
+
+def _torch_layer(m, l, h, pos, ck, cv):
+    """The same pre-norm layer assembled from torch library routines (fp64)."""
+    cfg = m.cfg
+    hq, hkv, D, I = cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, cfg.intermediate
+    T = lambda a: torch.from_numpy(np.ascontiguousarray(a))
+    h = T(h)
+    x = F.rms_norm(h, (cfg.hidden,), T(m.w("in_norm", l)), eps=cfg.rms_eps)
+    qkv = F.linear(x, T(m.w("wqkv", l)))
+    S = h.shape[0]
+    q = qkv[:, :hq * D].view(S, hq, D)
+    k = qkv[:, hq * D:(hq + hkv) * D].view(S, hkv, D)
+    v = qkv[:, (hq + hkv) * D:].view(S, hkv, D)
+    q = F.rms_norm(q, (D,), T(m.w("q_norm", l)), eps=cfg.rms_eps)
+    k = F.rms_norm(k, (D,), T(m.w("k_norm", l)), eps=cfg.rms_eps)
+
+    def rot(t, p):  # complex-number form of RoPE
+        z = torch.complex(t[..., :D // 2], t[..., D // 2:])
+        ang = T(np.asarray(p, dtype=np.float64))[:, None, None] * \
+            cfg.rope_theta ** (-torch.arange(D // 2, dtype=torch.float64) * 2.0 / D)
+        r = z * torch.polar(torch.ones_like(ang), ang)
+        return torch.cat([r.real, r.imag], -1)
+
+    q, k = rot(q, pos), rot(k, pos)
+    K = torch.cat([T(ck), k], 0).permute(1, 0, 2).repeat_interleave(hq // hkv, 0)
+    Vv = torch.cat([T(cv), v], 0).permute(1, 0, 2).repeat_interleave(hq // hkv, 0)
+    o = F.scaled_dot_product_attention(q.permute(1, 0, 2), K, Vv).permute(1, 0, 2).reshape(S, -1)
+    h = h + F.linear(o, T(m.w("wo", l)))
+    y = F.rms_norm(h, (cfg.hidden,), T(m.w("post_norm", l)), eps=cfg.rms_eps)
+    gu = F.linear(y, T(m.w("w_gate_up", l)))
+    h = h + F.linear(F.silu(gu[:, :I]) * gu[:, I:], T(m.w("w_down", l)))
+    return h.numpy()
+
+
+def test_decoder_layer_matches_library_assembly():
+    cfg = get_config("tiny-gains")
+    m = O.OracleModel(cfg, make_weights(cfg))
+    h = rng.standard_normal((16, cfg.hidden))
+    L = 21
+    ck = rng.standard_normal((L, cfg.n_kv_heads, cfg.head_dim))
+    cv = rng.standard_normal((L, cfg.n_kv_heads, cfg.head_dim))
+    pos = np.arange(L, L + 16)
+    np.testing.assert_allclose(O.decoder_layer(m, 1, h, pos, ck, cv),
+                               _torch_layer(m, 1, h, pos, ck, cv), rtol=1e-9, atol=1e-11)
+
+
+def test_decoder_layer_residual_structure():
+    """With W_o = 0 and W_down = 0 the layer is the identity on h."""
+    cfg = get_config("tiny")
+    w = make_weights(cfg)
+    w["layers"][0] = dict(w["layers"][0])
+    w["layers"][0]["wo"] = np.zeros_like(w["layers"][0]["wo"])
+    w["layers"][0]["w_down"] = np.zeros_like(w["layers"][0]["w_down"])
+    m = O.OracleModel(cfg, w)
+    h = rng.standard_normal((16, cfg.hidden))
+    ck = np.zeros((0, cfg.n_kv_heads, cfg.head_dim))
+    np.testing.assert_array_equal(O.decoder_layer(m, 0, h, np.arange(16), ck, ck), h)
+
+
+# ------------------------------------------------------------------ a6 lm_head
+
+def test_argmax_ties_go_to_lowest_id():
+    x = np.array([[0.0, 3.0, 3.0, 1.0], [-1.0, -1.0, -2.0, -1.0], [0.0, -0.0, 0.0, -5.0]])
+    assert O.argmax_first(x).tolist() == [1, 0, 0]
+
+
+def test_lm_head_chunking_is_plain_matmul():
+    cfg = get_config("tiny")
+    m = O.OracleModel(cfg, make_weights(cfg))
+    h = rng.standard_normal((15, cfg.hidden))
+    a = O.lm_head_logits(m, h, chunk=1000)
+    b = O.rmsnorm(h, m.w("final_norm"), cfg.rms_eps) @ m.w("embed").T
+    np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------------------ whole round
+
+def _run_rounds(cfg, rounds, req_id=0, keep=None):
+    from workload import match_stream, context_lengths
+    w = make_weights(cfg)
+    m = O.OracleModel(cfg, w)
+    dr = O.OracleDrafter(m)
+    L0 = int(context_lengths(cfg)[req_id])
+    req = O.OracleRequest(cfg, L0 + 16 * (rounds + 1))
+    dr.fuse_inject(req, feature_rows(cfg, req_id, 0, L0))
+    last, hist = cfg.first_token, []
+    pending = 0
+    for r in range(rounds):
+        if pending:
+            dr.fuse_inject(req, feature_rows(cfg, req_id, req.ctx_len, pending))
+        if keep is not None:
+            keep.append([k[:req.ctx_len].copy() for k in req.K])
+        out = dr.draft(req, last, want_logits=False)
+        mm, uu = match_stream(cfg, r, [req_id])
+        t = O.synthetic_target(out["draft"], mm[0], uu[0], cfg.vocab)
+        tau, bonus, conf = dr.accept_trim(req, out["draft"], t)
+        hist.append((tau, bonus, conf, out["draft"].copy()))
+        last, pending = bonus, tau
+    return req, hist
+
+
+def test_round_invariants_and_persistence():
+    cfg = get_config("tiny")
+    snaps = []
+    req, hist = _run_rounds(cfg, 5, keep=snaps)
+    L = cfg.ctx0
+    for (tau, bonus, conf, d) in hist:
+        assert 1 <= tau <= 16
+        assert conf == L + tau
+        assert d.shape == (15,) and d.min() >= 0 and d.max() < cfg.vocab
+        L = conf
+    # context K written before a round is byte-identical after later rounds
+    for i, snap in enumerate(snaps):
+        for l in range(cfg.n_layers):
+            np.testing.assert_array_equal(req.K[l][:snap[l].shape[0]], snap[l])
+
+
+def test_round_tau_independent_of_drafts():
+    """Under the stand-in verify, tau follows the match stream alone."""
+    from workload import match_stream
+    cfg = get_config("tiny")
+    _, hist = _run_rounds(cfg, 6)
+    for r, (tau, *_rest) in enumerate(hist):
+        mm, _ = match_stream(cfg, r, [0])
+        lead = 0
+        while lead < 15 and mm[0][lead]:
+            lead += 1
+        assert tau == lead + 1

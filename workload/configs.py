@@ -1,0 +1,110 @@
+"""Workload shapes: the five drafting workloads plus small test shapes.
+
+Each entry fixes the drafter's architecture (hidden size, heads, layers,
+vocabulary, RoPE base) and the synthetic serving scenario around it (batch,
+context lengths, rounds, per-position match probability of the stand-in
+target).  Mask id is the last vocabulary id; the first verified token of
+every request is id 1.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field, replace
+from typing import Optional, Tuple
+
+
+@dataclass(frozen=True)
+class DraftConfig:
+    name: str
+    hidden: int
+    n_q_heads: int
+    n_kv_heads: int
+    head_dim: int
+    intermediate: int
+    n_layers: int
+    vocab: int
+    rope_theta: float
+    batch: int
+    ctx0: Optional[int]              # prompt length per request; None -> drawn U[ctx_lo, ctx_hi]
+    rounds: int
+    match_p: Optional[float]         # None -> per-request U[p_lo, p_hi]
+    ctx_range: Tuple[int, int] = (512, 4096)
+    p_range: Tuple[float, float] = (0.6, 0.95)
+    n_fused: int = 5
+    block: int = 16
+    page_size: int = 64
+    rms_eps: float = 1e-6
+    weight_std: float = 0.02
+    gain_std: float = 0.0            # RMSNorm gains = 1 + gain_std * N(0,1); 0 -> all ones
+    first_token: int = 1
+    seed: int = 0
+    extra: dict = field(default_factory=dict, compare=False, hash=False)
+
+    @property
+    def mask_id(self) -> int:
+        return self.vocab - 1
+
+    @property
+    def fused_dim(self) -> int:
+        return self.n_fused * self.hidden
+
+    @property
+    def qkv_rows(self) -> int:
+        return (self.n_q_heads + 2 * self.n_kv_heads) * self.head_dim
+
+    def with_(self, **kw) -> "DraftConfig":
+        return replace(self, **kw)
+
+    def weight_bytes(self) -> int:
+        H, I, V, F = self.hidden, self.intermediate, self.vocab, self.fused_dim
+        per_layer = self.qkv_rows * H + H * self.n_q_heads * self.head_dim + 2 * I * H + I * H
+        return 2 * (V * H + H * F + self.n_layers * per_layer)
+
+
+CONFIGS = {
+    # 1: tiny drafter, batch 1
+    "tiny": DraftConfig(
+        name="tiny", hidden=256, n_q_heads=4, n_kv_heads=2, head_dim=64, intermediate=768,
+        n_layers=2, vocab=4096, rope_theta=1e6, batch=1, ctx0=128, rounds=8, match_p=0.8),
+    # 2: Qwen3-8B-shaped drafter, batch 1 (the headline workload)
+    "qwen3-8b": DraftConfig(
+        name="qwen3-8b", hidden=4096, n_q_heads=32, n_kv_heads=8, head_dim=128,
+        intermediate=12288, n_layers=5, vocab=151936, rope_theta=1e6, batch=1, ctx0=2048,
+        rounds=64, match_p=0.9),
+    # 3: Llama-3.1-8B-shaped drafter, batch 1
+    "llama3.1-8b": DraftConfig(
+        name="llama3.1-8b", hidden=4096, n_q_heads=32, n_kv_heads=8, head_dim=128,
+        intermediate=14336, n_layers=5, vocab=128256, rope_theta=5e5, batch=1, ctx0=8192,
+        rounds=64, match_p=0.85),
+    # 4: batched serving with ragged contexts and ragged acceptance
+    "batched-qwen3-8b": DraftConfig(
+        name="batched-qwen3-8b", hidden=4096, n_q_heads=32, n_kv_heads=8, head_dim=128,
+        intermediate=12288, n_layers=5, vocab=151936, rope_theta=1e6, batch=64, ctx0=None,
+        rounds=32, match_p=None, ctx_range=(512, 4096), p_range=(0.6, 0.95)),
+    # 5: long-reasoning 8-layer drafter, batch 4, 32K context
+    "long-8layer": DraftConfig(
+        name="long-8layer", hidden=2048, n_q_heads=32, n_kv_heads=4, head_dim=128,
+        intermediate=6144, n_layers=8, vocab=151936, rope_theta=1e6, batch=4, ctx0=32768,
+        rounds=128, match_p=0.9),
+}
+
+# Small shapes for parity tests: several tiles per GEMM, ragged vocabulary
+# tail, ragged pages, GQA group 4 and 8, head_dim 64 and 128, random gains.
+TEST_CONFIGS = {
+    "tiny-gains": CONFIGS["tiny"].with_(name="tiny-gains", gain_std=0.1),
+    "small": DraftConfig(
+        name="small", hidden=512, n_q_heads=8, n_kv_heads=2, head_dim=128, intermediate=1024,
+        n_layers=2, vocab=8000, rope_theta=1e6, batch=1, ctx0=200, rounds=4, match_p=0.85,
+        gain_std=0.1),
+    "small-batch": DraftConfig(
+        name="small-batch", hidden=512, n_q_heads=8, n_kv_heads=1, head_dim=128,
+        intermediate=768, n_layers=2, vocab=5000, rope_theta=5e5, batch=3, ctx0=None,
+        rounds=4, match_p=None, ctx_range=(30, 300), p_range=(0.5, 0.95), gain_std=0.1),
+}
+
+
+def get_config(name: str) -> DraftConfig:
+    if name in CONFIGS:
+        return CONFIGS[name]
+    if name in TEST_CONFIGS:
+        return TEST_CONFIGS[name]
+    raise KeyError(f"unknown workload {name!r}; known: {sorted(CONFIGS) + sorted(TEST_CONFIGS)}")
