@@ -1,0 +1,266 @@
+"""ctypes binding of libdflash (include/dflash.h): argument marshalling only.
+
+Every compute step runs in the CUDA library; this module turns torch tensors
+into device pointers and CUDA streams into handles.  Loading fails loudly if
+the library is missing or was built without the expected symbols -- there is
+no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import Optional
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libdflash.so")
+HEADER = os.path.join(os.path.dirname(PKG), "include", "dflash.h")
+
+OK = 0
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported shape", 3: "capacity exceeded",
+          4: "CUDA error", 5: "device-side check failed", 6: "workspace too small or misaligned"}
+DEV_TIMEOUT, DEV_NAN, DEV_PAGE, DEV_CAPACITY, DEV_ARG = 0x01, 0x02, 0x04, 0x08, 0x10
+KID_LM_HEAD, KID_GATE_UP, KID_ATTENTION, KID_DOWN, KID_QKV = 1, 2, 3, 4, 5
+
+_c_int_p = ctypes.POINTER(ctypes.c_int32)
+_vp = ctypes.c_void_p
+
+
+class DflashConfig(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "hidden", "n_q_heads", "n_kv_heads", "head_dim", "intermediate", "n_layers", "vocab",
+        "n_fused", "block", "mask_id", "page_size", "max_batch", "max_slots", "max_pages",
+        "max_pages_per_slot", "max_rows", "device")] + [("rms_eps", ctypes.c_float),
+                                                         ("rope_theta", ctypes.c_float)]
+
+
+class DflashWeights(ctypes.Structure):
+    _fields_ = [("embed", _vp), ("fc", _vp), ("fc_norm", _vp), ("final_norm", _vp)] + [
+        (n, ctypes.POINTER(_vp)) for n in (
+            "in_norm", "wqkv", "q_norm", "k_norm", "wo", "post_norm", "w_gate_up", "w_down")]
+
+
+def declared_functions(header: str = HEADER):
+    """Names of the functions include/dflash.h declares."""
+    with open(header) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"DFLASH_API\s+[\w\s\*]+?\b(dflash_\w+)\s*\(", text)))
+
+
+_SIGS = {
+    "dflash_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(DflashConfig)]),
+    "dflash_create": (ctypes.c_int, [ctypes.POINTER(DflashConfig), ctypes.POINTER(DflashWeights), _vp,
+                                     ctypes.c_size_t, ctypes.POINTER(_vp)]),
+    "dflash_destroy": (ctypes.c_int, [_vp]),
+    "dflash_fuse_inject": (ctypes.c_int, [_vp, _vp, ctypes.c_int32, _vp, ctypes.c_int32, _vp, _vp]),
+    "dflash_draft_block": (ctypes.c_int, [_vp, _vp, ctypes.c_int32, _vp, _vp, _vp]),
+    "dflash_draft_block_debug": (ctypes.c_int, [_vp, _vp, ctypes.c_int32, _vp, _vp, _vp, _vp, _vp]),
+    "dflash_accept_trim": (ctypes.c_int, [_vp, _vp, ctypes.c_int32, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "dflash_reset_slot": (ctypes.c_int, [_vp, ctypes.c_int32, _vp]),
+    "dflash_read_status": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_uint32)]),
+    "dflash_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "dflash_graph_begin": (ctypes.c_int, [_vp, _vp]),
+    "dflash_graph_end": (ctypes.c_int, [_vp, _vp, _c_int_p]),
+    "dflash_graph_launch": (ctypes.c_int, [_vp, _vp]),
+    "dflash_read_kv": (ctypes.c_int, [_vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                      _vp, _vp, _vp]),
+    "dflash_slot_lengths": (ctypes.c_int, [_vp, _vp, ctypes.c_int32, _vp, _vp]),
+    "dflash_probe_arm": (ctypes.c_int, [_vp, ctypes.c_int32, ctypes.c_int32]),
+    "dflash_probe_read": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_float), ctypes.c_int32, _c_int_p]),
+    "dflash_launch_count": (ctypes.c_uint64, [_vp]),
+    "dflash_harness_verify": (ctypes.c_int, [_vp, _vp, ctypes.c_int32, _vp, _vp, _vp, ctypes.c_int32, _vp,
+                                             _vp, _vp, ctypes.c_int32, _vp, _vp]),
+}
+
+_LIB = None
+
+
+def load(path: str = LIB_PATH):
+    """Load libdflash and declare every entry point's signature."""
+    global _LIB
+    if _LIB is not None and path == LIB_PATH:
+        return _LIB
+    if not os.path.exists(path):
+        raise RuntimeError(f"libdflash not built ({path} missing): run __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(lib, name)  # AttributeError if the symbol is missing
+        fn.restype = res
+        fn.argtypes = args
+    if path == LIB_PATH:
+        _LIB = lib
+    return lib
+
+
+class DflashError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} failed: {STATUS.get(code, code)} ({code})")
+        self.code = code
+
+
+def _check(fn: str, code: int):
+    if code != OK:
+        raise DflashError(fn, code)
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int:
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+class Drafter:
+    """One libdflash handle: drafter weights (device), workspace and slots.
+
+    `weights` follows workload.make_weights' layout with torch bf16 device
+    tensors; the handle keeps them referenced for its lifetime.
+    """
+
+    def __init__(self, cfg, weights: dict, *, max_batch: int, max_slots: int, max_pages: int,
+                 max_pages_per_slot: int, max_rows: int, device: int = 0):
+        import torch
+        self.lib = load()
+        self.cfg = cfg
+        self.device = device
+        self.w = weights
+        c = DflashConfig(hidden=cfg.hidden, n_q_heads=cfg.n_q_heads, n_kv_heads=cfg.n_kv_heads,
+                         head_dim=cfg.head_dim, intermediate=cfg.intermediate, n_layers=cfg.n_layers,
+                         vocab=cfg.vocab, n_fused=cfg.n_fused, block=cfg.block, mask_id=cfg.mask_id,
+                         page_size=cfg.page_size, max_batch=max_batch, max_slots=max_slots,
+                         max_pages=max_pages, max_pages_per_slot=max_pages_per_slot,
+                         max_rows=max_rows, device=device, rms_eps=cfg.rms_eps,
+                         rope_theta=cfg.rope_theta)
+        self.c = c
+        nbytes = self.lib.dflash_workspace_bytes(ctypes.byref(c))
+        if nbytes == 0:
+            raise DflashError("dflash_workspace_bytes", 2)
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=f"cuda:{device}")
+        L = cfg.n_layers
+
+        def arr(name):
+            a = (_vp * L)(*[weights["layers"][l][name].data_ptr() for l in range(L)])
+            return a
+
+        self._arrays = {n: arr(n) for n in ("in_norm", "wqkv", "q_norm", "k_norm", "wo", "post_norm",
+                                            "w_gate_up", "w_down")}
+        wts = DflashWeights(embed=weights["embed"].data_ptr(), fc=weights["fc"].data_ptr(),
+                            fc_norm=weights["fc_norm"].data_ptr(),
+                            final_norm=weights["final_norm"].data_ptr(),
+                            **{n: ctypes.cast(a, ctypes.POINTER(_vp)) for n, a in self._arrays.items()})
+        h = _vp()
+        _check("dflash_create", self.lib.dflash_create(ctypes.byref(c), ctypes.byref(wts),
+                                                       self.workspace.data_ptr(), nbytes,
+                                                       ctypes.byref(h)))
+        self.h = h
+        self.max_batch, self.max_rows = max_batch, max_rows
+
+    def close(self):
+        if getattr(self, "h", None):
+            self.lib.dflash_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # ---- the three calls of a round
+    def fuse_inject(self, slots, feats, rows_per_req: int, n_new, stream=None):
+        _check("dflash_fuse_inject", self.lib.dflash_fuse_inject(
+            self.h, _ptr(slots), slots.numel(), _ptr(feats), rows_per_req, _ptr(n_new), _stream(stream)))
+
+    def draft_block(self, slots, last_tok, draft, stream=None):
+        _check("dflash_draft_block", self.lib.dflash_draft_block(
+            self.h, _ptr(slots), slots.numel(), _ptr(last_tok), _ptr(draft), _stream(stream)))
+
+    def draft_block_debug(self, slots, last_tok, draft, hidden=None, logits=None, stream=None):
+        _check("dflash_draft_block_debug", self.lib.dflash_draft_block_debug(
+            self.h, _ptr(slots), slots.numel(), _ptr(last_tok), _ptr(draft), _ptr(hidden),
+            _ptr(logits), _stream(stream)))
+
+    def accept_trim(self, slots, draft, target, accept_len, bonus, ctx_len, stream=None):
+        _check("dflash_accept_trim", self.lib.dflash_accept_trim(
+            self.h, _ptr(slots), slots.numel(), _ptr(draft), _ptr(target), _ptr(accept_len),
+            _ptr(bonus), _ptr(ctx_len), _stream(stream)))
+
+    def reset_slot(self, slot: int, stream=None):
+        _check("dflash_reset_slot", self.lib.dflash_reset_slot(self.h, slot, _stream(stream)))
+
+    def read_status(self) -> int:
+        v = ctypes.c_uint32(0)
+        _check("dflash_read_status", self.lib.dflash_read_status(self.h, ctypes.byref(v)))
+        return v.value
+
+    # ---- introspection
+    def read_kv(self, layer: int, slot: int, pos0: int, n: int, stream=None):
+        import torch
+        shape = (n, self.cfg.n_kv_heads, self.cfg.head_dim)
+        k = torch.empty(shape, dtype=torch.bfloat16, device=f"cuda:{self.device}")
+        v = torch.empty_like(k)
+        _check("dflash_read_kv", self.lib.dflash_read_kv(self.h, layer, slot, pos0, n, _ptr(k), _ptr(v),
+                                                         _stream(stream)))
+        return k, v
+
+    def slot_lengths(self, slots, stream=None):
+        import torch
+        out = torch.empty(slots.numel(), dtype=torch.int32, device=slots.device)
+        _check("dflash_slot_lengths", self.lib.dflash_slot_lengths(self.h, _ptr(slots), slots.numel(),
+                                                                   _ptr(out), _stream(stream)))
+        return out
+
+    # ---- runtime
+    def graph_begin(self, stream=None):
+        _check("dflash_graph_begin", self.lib.dflash_graph_begin(self.h, _stream(stream)))
+
+    def graph_end(self, stream=None) -> int:
+        n = ctypes.c_int32(0)
+        _check("dflash_graph_end", self.lib.dflash_graph_end(self.h, _stream(stream), ctypes.byref(n)))
+        return n.value
+
+    def graph_launch(self, stream=None):
+        _check("dflash_graph_launch", self.lib.dflash_graph_launch(self.h, _stream(stream)))
+
+    def probe_arm(self, kernel_id: int, n: int):
+        _check("dflash_probe_arm", self.lib.dflash_probe_arm(self.h, kernel_id, n))
+
+    def probe_read(self, cap: int):
+        buf = (ctypes.c_float * max(cap, 1))()
+        n = ctypes.c_int32(0)
+        _check("dflash_probe_read", self.lib.dflash_probe_read(self.h, buf, cap, ctypes.byref(n)))
+        return list(buf[:n.value])
+
+    def launch_count(self) -> int:
+        return int(self.lib.dflash_launch_count(self.h))
+
+    def harness_verify(self, slots, draft, match, offs, rounds_cap: int, round_ctr, target,
+                       feat_stream=None, stream_rows: int = 0, feats_out=None, stream=None):
+        _check("dflash_harness_verify", self.lib.dflash_harness_verify(
+            self.h, _ptr(slots), slots.numel(), _ptr(draft), _ptr(match), _ptr(offs), rounds_cap,
+            _ptr(round_ctr), _ptr(target), _ptr(feat_stream), stream_rows, _ptr(feats_out),
+            _stream(stream)))
+
+
+def weights_to_device(w_np: dict, device: int = 0) -> dict:
+    """workload.make_weights output (uint16 bf16 bits) -> torch bf16 tensors on the GPU."""
+    import numpy as np
+    import torch
+
+    def t(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(
+            f"cuda:{device}")
+
+    out = {k: t(v) for k, v in w_np.items() if k != "layers"}
+    out["layers"] = [{k: t(v) for k, v in lw.items()} for lw in w_np["layers"]]
+    return out
+
+
+def bf16_host(a) -> "torch.Tensor":
+    """uint16 bf16 bit patterns (numpy) -> torch bf16 CPU tensor (no copy of values)."""
+    import numpy as np
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)

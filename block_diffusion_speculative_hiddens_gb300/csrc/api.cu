@@ -1,0 +1,700 @@
+// Host runtime behind the C ABI of include/dflash.h: configuration checks,
+// workspace layout, TMA descriptors, launch planning, CUDA-graph capture and
+// kernel timing probes.  Every entry point returns a dflash_status; nothing
+// throws across the boundary and nothing here allocates device memory (the
+// caller supplies the workspace).
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool load_encode() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+// 2-D bf16 tensor [rows, cols] row-major; box = 64 columns (128 B) x box_rows,
+// 128-byte swizzle -- the canonical K-major tcgen05 operand layout.
+bool make_tmap(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  if (!load_encode()) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct Carve {
+  size_t off = 0;
+  char* base = nullptr;
+  template <class T>
+  T* take(size_t n) {
+    off = align_up(off, 256);
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off += n * sizeof(T);
+    return p;
+  }
+};
+
+int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
+
+struct Probe {
+  int kid = 0;
+  int n = 0;
+  int next = 0;
+  std::vector<cudaEvent_t> ev;  // 2*n
+};
+
+}  // namespace
+
+struct dflash_handle {
+  dflash_config cfg;
+  int num_sms = 0;
+  int max_tok = 0;     // max_batch * block
+  int max_pos = 0;     // max_pages_per_slot * page_size
+  int attn_splits = 1;
+  int max_tiles = 0;
+  // weights
+  const bf16* embed;
+  const bf16* fc;
+  const bf16* fc_norm;
+  const bf16* final_norm;
+  const bf16* in_norm[DFL_MAX_LAYERS];
+  const bf16* q_norm[DFL_MAX_LAYERS];
+  const bf16* k_norm[DFL_MAX_LAYERS];
+  const bf16* post_norm[DFL_MAX_LAYERS];
+  // A operand descriptors
+  CUtensorMap tm_qkv[DFL_MAX_LAYERS], tm_wo[DFL_MAX_LAYERS], tm_gu[DFL_MAX_LAYERS], tm_down[DFL_MAX_LAYERS];
+  CUtensorMap tm_fc, tm_embed;
+  // cached B operand descriptors for the current token count
+  int bm_M = -1;
+  CUtensorMap tm_hg, tm_o, tm_act;
+  int bm_rows = -1;
+  CUtensorMap tm_cg;
+  // workspace
+  uint32_t* status;
+  int *ctx_len, *pos0, *n_pages, *page_table, *free_stack, *free_top, *n_eff;
+  bf16 *k_pool, *v_pool;
+  long long layer_stride;
+  float2* rope;
+  float* h;
+  bf16 *hg, *qbuf, *obuf, *act, *cg;
+  float *ss_a, *ss_c;
+  unsigned long long* keys;
+  unsigned* done_ctr;
+  float* gemm_ws;
+  unsigned* tile_ctr;
+  float* attn_ws;
+  unsigned* attn_ctr;
+  // runtime
+  bool pdl = true;
+  uint64_t launches = 0;
+  Probe probe;
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+};
+
+namespace {
+
+bool cfg_valid(const dflash_config* c) {
+  if (!c) return false;
+  if (c->hidden <= 0 || c->n_q_heads <= 0 || c->n_kv_heads <= 0 || c->head_dim <= 0 || c->intermediate <= 0 ||
+      c->n_layers <= 0 || c->vocab <= 0 || c->n_fused <= 0)
+    return false;
+  if (c->n_layers > DFL_MAX_LAYERS) return false;
+  if (c->block != DFL_BLOCK || c->page_size != DFL_PAGE) return false;
+  if (c->head_dim != 64 && c->head_dim != 128) return false;
+  if (c->hidden % 128 || c->hidden > 8192) return false;
+  if (c->intermediate % 64) return false;
+  if ((c->n_q_heads * c->head_dim) % 128 || (c->n_kv_heads * c->head_dim) % 128) return false;
+  if (c->n_q_heads % c->n_kv_heads) return false;
+  const int G = c->n_q_heads / c->n_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return false;
+  if (c->max_batch <= 0 || c->max_batch > 64 || c->max_slots <= 0 || c->max_pages <= 0 ||
+      c->max_pages_per_slot <= 0 || c->max_rows < 0)
+    return false;
+  if (c->mask_id < 0 || c->mask_id >= c->vocab) return false;
+  if (!(c->rms_eps > 0.f) || !(c->rope_theta > 1.f)) return false;
+  return true;
+}
+
+int pick_attn_splits(const dflash_config& c, int num_sms) {
+  const int pairs = c.max_batch * c.n_kv_heads;
+  int want = ceil_div(2LL * num_sms, pairs);
+  const int cap = std::max(1, c.max_pages_per_slot / 2);
+  want = std::min(want, cap);
+  want = std::min(want, 16);
+  return std::max(1, want);
+}
+
+// Lay out the workspace; with base == nullptr only sizes are computed.
+size_t carve(dflash_handle* h, const dflash_config& c, char* base, int num_sms) {
+  Carve w;
+  w.base = base;
+  const int M = c.max_batch * DFL_BLOCK;
+  const int R = std::max(c.max_rows, 1);
+  const int H = c.hidden, D = c.head_dim, hq = c.n_q_heads, hkv = c.n_kv_heads, I = c.intermediate;
+  const int max_pos = c.max_pages_per_slot * DFL_PAGE;
+  const long long blk = 64LL * hkv * D;  // elements per page per layer (K or V)
+  const long long layer_stride = (long long)c.max_pages * blk;
+  const int splits = pick_attn_splits(c, num_sms);
+  const int G = hq / hkv;
+  // split-K tile counters: the largest tile count of any split GEMM
+  const int Tmax = std::max(M, R);
+  const int t_tiles_max = ceil_div(Tmax, 16);
+  int tiles = std::max({(c.n_q_heads + 2 * hkv) * D / 128, H / 128, I / 64, c.n_layers * 2 * hkv * D / 128});
+  tiles *= t_tiles_max;
+
+  dflash_handle tmp;
+  dflash_handle* o = h ? h : &tmp;
+  o->status = w.take<uint32_t>(64);
+  o->ctx_len = w.take<int>(c.max_slots);
+  o->pos0 = w.take<int>(c.max_slots);
+  o->n_pages = w.take<int>(c.max_slots);
+  o->page_table = w.take<int>((size_t)c.max_slots * c.max_pages_per_slot);
+  o->free_stack = w.take<int>(c.max_pages);
+  o->free_top = w.take<int>(1);
+  o->n_eff = w.take<int>(c.max_batch);
+  o->k_pool = w.take<bf16>((size_t)c.n_layers * layer_stride);
+  o->v_pool = w.take<bf16>((size_t)c.n_layers * layer_stride);
+  o->layer_stride = layer_stride;
+  o->rope = w.take<float2>((size_t)max_pos * (D / 2));
+  o->h = w.take<float>((size_t)M * H);
+  o->hg = w.take<bf16>((size_t)M * H);
+  o->ss_a = w.take<float>((size_t)(H / 128) * M);
+  o->qbuf = w.take<bf16>((size_t)M * hq * D);
+  o->obuf = w.take<bf16>((size_t)M * hq * D);
+  o->act = w.take<bf16>((size_t)M * I);
+  o->keys = w.take<unsigned long long>(M);
+  o->done_ctr = w.take<unsigned>(64);
+  o->cg = w.take<bf16>((size_t)R * H);
+  o->ss_c = w.take<float>((size_t)(H / 128) * R);
+  o->gemm_ws = w.take<float>((size_t)num_sms * 2 * DFL_BN_MAX * 128);
+  o->tile_ctr = w.take<unsigned>(tiles);
+  o->attn_ws = w.take<float>((size_t)c.max_batch * hkv * splits * (G * 16) * (D + 2));
+  o->attn_ctr = w.take<unsigned>((size_t)c.max_batch * hkv);
+  if (h) {
+    h->attn_splits = splits;
+    h->max_tiles = tiles;
+    h->max_pos = max_pos;
+    h->max_tok = M;
+  }
+  return align_up(w.off, 256);
+}
+
+int device_sms(int dev) {
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+inline int cuda_err(cudaError_t e) {
+  if (e == cudaSuccess) return DFLASH_OK;
+  fprintf(stderr, "[dflash] CUDA error: %s\n", cudaGetErrorString(e));
+  return DFLASH_ERR_CUDA;
+}
+
+struct ProbeScope {
+  dflash_handle* h;
+  cudaStream_t s;
+  bool on = false;
+  int idx = 0;
+  ProbeScope(dflash_handle* h_, int kid, cudaStream_t s_) : h(h_), s(s_) {
+    if (h->probe.kid == kid && h->probe.next < h->probe.n) {
+      on = true;
+      idx = h->probe.next++;
+      cudaEventRecordWithFlags(h->probe.ev[2 * idx], s, cudaEventRecordExternal);
+    }
+  }
+  ~ProbeScope() {
+    if (on) cudaEventRecordWithFlags(h->probe.ev[2 * idx + 1], s, cudaEventRecordExternal);
+  }
+};
+
+// Plan and launch one GEMM.  N_rows: A rows covered per group; tile_rows:
+// rows per tile along N (128, or 64 features for SwiGLU).
+int run_gemm(dflash_handle* h, cudaStream_t s, int mode, const CUtensorMap* A, int groups, int n_tiles, int K,
+             const CUtensorMap& B, int M, GemmParams p, bool allow_split, int kid = 0) {
+  if (M <= 0) return DFLASH_OK;
+  TmapSet set;
+  for (int g = 0; g < groups; ++g) set.m[g] = A[g];
+  const int t_tiles = ceil_div(M, DFL_BN_MAX);
+  const int BN = ((ceil_div(M, t_tiles) + 15) / 16) * 16;
+  p.mode = mode;
+  p.M = M;
+  p.kblocks = K / 64;
+  p.n_tiles = n_tiles;
+  p.t_tiles = t_tiles;
+  p.BN = BN;
+  p.groups = groups;
+  p.total_tiles = groups * n_tiles * t_tiles;
+  p.allow_split = allow_split ? 1 : 0;
+  p.stages = gemm_pick_stages(BN);
+  int cols = 32;
+  while (cols < 2 * BN) cols *= 2;
+  p.tmem_cols = cols;
+  p.status = h->status;
+  p.ws = h->gemm_ws;
+  p.tile_ctr = h->tile_ctr;
+  p.eps = h->cfg.rms_eps;
+  p.H = h->cfg.hidden;
+  p.hq = h->cfg.n_q_heads;
+  p.hkv = h->cfg.n_kv_heads;
+  p.D = h->cfg.head_dim;
+  p.rope = h->rope;
+  p.max_pos = h->max_pos;
+  if (allow_split && p.total_tiles > h->max_tiles) return DFLASH_ERR_SHAPE;
+  const long long units = allow_split ? (long long)p.total_tiles * p.kblocks : p.total_tiles;
+  const int grid = (int)std::min<long long>(units, h->num_sms);
+  ProbeScope ps(h, kid, s);
+  h->launches++;
+  return cuda_err(gemm_launch(set, B, p, grid, s, h->pdl));
+}
+
+KVGeom kv_geom(dflash_handle* h) {
+  KVGeom g;
+  g.k_pool = h->k_pool;
+  g.v_pool = h->v_pool;
+  g.layer_stride = h->layer_stride;
+  g.page_table = h->page_table;
+  g.max_pages_per_slot = h->cfg.max_pages_per_slot;
+  g.max_pages = h->cfg.max_pages;
+  g.hkv = h->cfg.n_kv_heads;
+  g.D = h->cfg.head_dim;
+  return g;
+}
+
+int ensure_bmaps(dflash_handle* h, int M) {
+  if (h->bm_M == M) return DFLASH_OK;
+  const dflash_config& c = h->cfg;
+  const int t_tiles = ceil_div(M, DFL_BN_MAX);
+  const uint32_t BN = (uint32_t)(((ceil_div(M, t_tiles) + 15) / 16) * 16);
+  if (!make_tmap(&h->tm_hg, h->hg, M, c.hidden, BN)) return DFLASH_ERR_CUDA;
+  if (!make_tmap(&h->tm_o, h->obuf, M, (uint64_t)c.n_q_heads * c.head_dim, BN)) return DFLASH_ERR_CUDA;
+  if (!make_tmap(&h->tm_act, h->act, M, c.intermediate, BN)) return DFLASH_ERR_CUDA;
+  h->bm_M = M;
+  return DFLASH_OK;
+}
+
+int draft_impl(dflash_handle* h, const int32_t* slots, int32_t batch, const int32_t* last_tok, int32_t* draft,
+               float* hidden, float* logits, void* stream) {
+  if (!h || !slots || !last_tok || !draft) return DFLASH_ERR_INVALID_ARG;
+  if (batch < 0 || batch > h->cfg.max_batch) return DFLASH_ERR_INVALID_ARG;
+  if (batch == 0) return DFLASH_OK;
+  if (cudaSetDevice(h->cfg.device) != cudaSuccess) return DFLASH_ERR_CUDA;
+  cudaStream_t s = (cudaStream_t)stream;
+  const dflash_config& c = h->cfg;
+  const int M = batch * DFL_BLOCK;
+  const int H = c.hidden, D = c.head_dim, hq = c.n_q_heads, hkv = c.n_kv_heads, I = c.intermediate;
+  int rc = ensure_bmaps(h, M);
+  if (rc) return rc;
+  const KVGeom kv = kv_geom(h);
+
+  h->launches++;
+  rc = cuda_err(launch_embed(slots, batch, last_tok, c.mask_id, h->embed, h->in_norm[0], H, h->h, h->hg, h->ss_a,
+                             h->keys, s));
+  if (rc) return rc;
+
+  for (int l = 0; l < c.n_layers; ++l) {
+    {  // QKV projection + q/k norm + RoPE; block K/V into the cache
+      GemmParams p = {};
+      p.ss_in = h->ss_a;
+      p.ss_parts = H / 128;
+      p.out = h->qbuf;
+      p.qn_gain = h->q_norm[l];
+      p.kn_gain[0] = h->k_norm[l];
+      p.layer = l;
+      p.kv = kv;
+      p.slots = slots;
+      p.ctx_len = h->ctx_len;
+      p.rows_per_req = DFL_BLOCK;
+      p.N = (hq + 2 * hkv) * D;
+      rc = run_gemm(h, s, GM_QKV, &h->tm_qkv[l], 1, p.N / 128, H, h->tm_hg, M, p, true, DFLASH_KID_QKV);
+      if (rc) return rc;
+    }
+    {  // block attention
+      AttnParams a = {};
+      a.q = h->qbuf;
+      a.out = h->obuf;
+      a.kv = kv;
+      a.layer = l;
+      a.slots = slots;
+      a.ctx_len = h->ctx_len;
+      a.hq = hq;
+      a.hkv = hkv;
+      a.D = D;
+      a.n_splits = h->attn_splits;
+      a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
+      a.ws = h->attn_ws;
+      a.ctr = h->attn_ctr;
+      a.status = h->status;
+      ProbeScope ps(h, DFLASH_KID_ATTENTION, s);
+      h->launches++;
+      rc = cuda_err(attn_launch(a, batch, s, h->pdl));
+      if (rc) return rc;
+    }
+    {  // output projection + residual; post-attention norm inputs
+      GemmParams p = {};
+      p.h = h->h;
+      p.out = h->hg;
+      p.gain = h->post_norm[l];
+      p.ss_out = h->ss_a;
+      p.N = H;
+      rc = run_gemm(h, s, GM_RESID, &h->tm_wo[l], 1, H / 128, hq * D, h->tm_o, M, p, true);
+      if (rc) return rc;
+    }
+    {  // gate/up projection + SiLU gating
+      GemmParams p = {};
+      p.ss_in = h->ss_a;
+      p.ss_parts = H / 128;
+      p.out = h->act;
+      p.N = I;
+      p.up_off = I;
+      rc = run_gemm(h, s, GM_SWIGLU, &h->tm_gu[l], 1, I / 64, H, h->tm_hg, M, p, true, DFLASH_KID_GATE_UP);
+      if (rc) return rc;
+    }
+    {  // down projection + residual; next norm inputs
+      GemmParams p = {};
+      p.h = h->h;
+      p.out = h->hg;
+      p.gain = (l + 1 < c.n_layers) ? h->in_norm[l + 1] : h->final_norm;
+      p.ss_out = h->ss_a;
+      p.N = H;
+      rc = run_gemm(h, s, GM_RESID, &h->tm_down[l], 1, H / 128, I, h->tm_act, M, p, true, DFLASH_KID_DOWN);
+      if (rc) return rc;
+    }
+  }
+  if (hidden) {
+    rc = cuda_err(cudaMemcpyAsync(hidden, h->h, (size_t)M * H * sizeof(float), cudaMemcpyDeviceToDevice, s));
+    if (rc) return rc;
+  }
+  {  // final norm + tied lm_head + argmax
+    GemmParams p = {};
+    p.ss_in = h->ss_a;
+    p.ss_parts = H / 128;
+    p.N = c.vocab;
+    p.keys = h->keys;
+    p.logits = logits;
+    p.draft = draft;
+    p.done_ctr = h->done_ctr;
+    rc = run_gemm(h, s, GM_ARGMAX, &h->tm_embed, 1, ceil_div(c.vocab, 128), H, h->tm_hg, M, p, false,
+                  DFLASH_KID_LM_HEAD);
+    if (rc) return rc;
+  }
+  return DFLASH_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* dflash_status_string(int st) {
+  switch (st) {
+    case DFLASH_OK: return "ok";
+    case DFLASH_ERR_INVALID_ARG: return "invalid argument";
+    case DFLASH_ERR_SHAPE: return "unsupported shape";
+    case DFLASH_ERR_CAPACITY: return "capacity exceeded";
+    case DFLASH_ERR_CUDA: return "CUDA error";
+    case DFLASH_ERR_DEVICE: return "device-side check failed";
+    case DFLASH_ERR_WORKSPACE: return "workspace too small or misaligned";
+  }
+  return "unknown status";
+}
+
+size_t dflash_workspace_bytes(const dflash_config* cfg) {
+  if (!cfg_valid(cfg)) return 0;
+  int sms = device_sms(cfg->device);
+  if (sms <= 0) sms = 160;  // no device visible: size for the largest part
+  return carve(nullptr, *cfg, nullptr, sms);
+}
+
+int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* workspace, size_t bytes,
+                  dflash_handle** out) {
+  if (!out) return DFLASH_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!cfg_valid(cfg)) return DFLASH_ERR_SHAPE;
+  if (!w || !w->embed || !w->fc || !w->fc_norm || !w->final_norm || !w->in_norm || !w->wqkv || !w->q_norm ||
+      !w->k_norm || !w->wo || !w->post_norm || !w->w_gate_up || !w->w_down)
+    return DFLASH_ERR_INVALID_ARG;
+  for (int l = 0; l < cfg->n_layers; ++l)
+    if (!w->in_norm[l] || !w->wqkv[l] || !w->q_norm[l] || !w->k_norm[l] || !w->wo[l] || !w->post_norm[l] ||
+        !w->w_gate_up[l] || !w->w_down[l])
+      return DFLASH_ERR_INVALID_ARG;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255)) return DFLASH_ERR_WORKSPACE;
+  if (cudaSetDevice(cfg->device) != cudaSuccess) return DFLASH_ERR_CUDA;
+  const int sms = device_sms(cfg->device);
+  if (sms <= 0) return DFLASH_ERR_CUDA;
+  if (bytes < carve(nullptr, *cfg, nullptr, sms)) return DFLASH_ERR_WORKSPACE;
+  if (!load_encode()) return DFLASH_ERR_CUDA;
+
+  dflash_handle* h = new (std::nothrow) dflash_handle();
+  if (!h) return DFLASH_ERR_CAPACITY;
+  h->cfg = *cfg;
+  h->num_sms = sms;
+  carve(h, *cfg, static_cast<char*>(workspace), sms);
+  const dflash_config& c = *cfg;
+  const int H = c.hidden, D = c.head_dim, hq = c.n_q_heads, hkv = c.n_kv_heads, I = c.intermediate;
+  h->embed = static_cast<const bf16*>(w->embed);
+  h->fc = static_cast<const bf16*>(w->fc);
+  h->fc_norm = static_cast<const bf16*>(w->fc_norm);
+  h->final_norm = static_cast<const bf16*>(w->final_norm);
+  bool ok = make_tmap(&h->tm_embed, w->embed, c.vocab, H, 64) &&
+            make_tmap(&h->tm_fc, w->fc, H, (uint64_t)c.n_fused * H, 64);
+  for (int l = 0; l < c.n_layers && ok; ++l) {
+    h->in_norm[l] = static_cast<const bf16*>(w->in_norm[l]);
+    h->q_norm[l] = static_cast<const bf16*>(w->q_norm[l]);
+    h->k_norm[l] = static_cast<const bf16*>(w->k_norm[l]);
+    h->post_norm[l] = static_cast<const bf16*>(w->post_norm[l]);
+    ok = make_tmap(&h->tm_qkv[l], w->wqkv[l], (uint64_t)(hq + 2 * hkv) * D, H, 64) &&
+         make_tmap(&h->tm_wo[l], w->wo[l], H, (uint64_t)hq * D, 64) &&
+         make_tmap(&h->tm_gu[l], w->w_gate_up[l], 2ull * I, H, 64) &&
+         make_tmap(&h->tm_down[l], w->w_down[l], H, I, 64);
+  }
+  int rc = ok ? DFLASH_OK : DFLASH_ERR_CUDA;
+  if (!rc) rc = cuda_err(gemm_init_attributes());
+  if (!rc) rc = cuda_err(attn_init_attributes());
+  if (!rc) rc = cuda_err(cudaMemset(workspace, 0, carve(nullptr, c, nullptr, sms)));
+  if (!rc)
+    rc = cuda_err(cudaMemset(h->page_table, 0xFF, (size_t)c.max_slots * c.max_pages_per_slot * sizeof(int)));
+  if (!rc) rc = cuda_err(launch_pool_init(h->free_stack, h->free_top, c.max_pages, 0));
+  if (!rc) rc = cuda_err(launch_rope_table(h->rope, h->max_pos, D, c.rope_theta, 0));
+  if (!rc) rc = cuda_err(cudaDeviceSynchronize());
+  if (rc) {
+    delete h;
+    return rc;
+  }
+  *out = h;
+  return DFLASH_OK;
+}
+
+int dflash_destroy(dflash_handle* h) {
+  if (!h) return DFLASH_ERR_INVALID_ARG;
+  if (h->exec) cudaGraphExecDestroy(h->exec);
+  if (h->graph) cudaGraphDestroy(h->graph);
+  for (cudaEvent_t e : h->probe.ev) cudaEventDestroy(e);
+  delete h;
+  return DFLASH_OK;
+}
+
+int dflash_fuse_inject(dflash_handle* h, const int32_t* slots, int32_t batch, const void* feats,
+                       int32_t rows_per_req, const int32_t* n_new, void* stream) {
+  if (!h || !slots || !n_new) return DFLASH_ERR_INVALID_ARG;
+  if (batch < 0 || batch > h->cfg.max_batch || rows_per_req < 0) return DFLASH_ERR_INVALID_ARG;
+  if ((long long)batch * rows_per_req > h->cfg.max_rows) return DFLASH_ERR_CAPACITY;
+  if (batch == 0) return DFLASH_OK;
+  if (rows_per_req > 0 && !feats) return DFLASH_ERR_INVALID_ARG;
+  if (cudaSetDevice(h->cfg.device) != cudaSuccess) return DFLASH_ERR_CUDA;
+  cudaStream_t s = (cudaStream_t)stream;
+  const dflash_config& c = h->cfg;
+  const int H = c.hidden, D = c.head_dim, hkv = c.n_kv_heads;
+  h->launches++;
+  int rc = cuda_err(launch_page_alloc(slots, batch, n_new, rows_per_req, h->ctx_len, h->pos0, h->n_pages,
+                                      h->page_table, c.max_pages_per_slot, h->free_stack, h->free_top, h->n_eff,
+                                      c.max_slots, h->status, s));
+  if (rc || rows_per_req == 0) return rc;
+  const int R = batch * rows_per_req;
+  const int t_tiles = ceil_div(R, DFL_BN_MAX);
+  const uint32_t BN = (uint32_t)(((ceil_div(R, t_tiles) + 15) / 16) * 16);
+  CUtensorMap tm_feats;
+  if (!make_tmap(&tm_feats, feats, R, (uint64_t)c.n_fused * H, BN)) return DFLASH_ERR_INVALID_ARG;
+  if (h->bm_rows != R) {
+    if (!make_tmap(&h->tm_cg, h->cg, R, H, BN)) return DFLASH_ERR_CUDA;
+    h->bm_rows = R;
+  }
+  {  // fusion projection; RMSNorm gain folded in, its scale deferred to the consumer
+    GemmParams p = {};
+    p.out = h->cg;
+    p.gain = h->fc_norm;
+    p.ss_out = h->ss_c;
+    p.N = H;
+    rc = run_gemm(h, s, GM_FC, &h->tm_fc, 1, H / 128, c.n_fused * H, tm_feats, R, p, true);
+    if (rc) return rc;
+  }
+  {  // every layer's K/V projection of the fused feature, k-norm, RoPE, paged append
+    GemmParams p = {};
+    p.ss_in = h->ss_c;
+    p.ss_parts = H / 128;
+    p.a_row_off = c.n_q_heads * D;
+    p.N = 2 * hkv * D;
+    for (int l = 0; l < c.n_layers; ++l) p.kn_gain[l] = h->k_norm[l];
+    p.kv = kv_geom(h);
+    p.slots = slots;
+    p.pos0 = h->pos0;
+    p.n_eff = h->n_eff;
+    p.rows_per_req = rows_per_req;
+    rc = run_gemm(h, s, GM_INJECT, h->tm_qkv, c.n_layers, p.N / 128, H, h->tm_cg, R, p, true);
+    if (rc) return rc;
+  }
+  return DFLASH_OK;
+}
+
+int dflash_draft_block(dflash_handle* h, const int32_t* slots, int32_t batch, const int32_t* last_tok,
+                       int32_t* draft, void* stream) {
+  return draft_impl(h, slots, batch, last_tok, draft, nullptr, nullptr, stream);
+}
+
+int dflash_draft_block_debug(dflash_handle* h, const int32_t* slots, int32_t batch, const int32_t* last_tok,
+                             int32_t* draft, float* hidden, float* logits, void* stream) {
+  return draft_impl(h, slots, batch, last_tok, draft, hidden, logits, stream);
+}
+
+int dflash_accept_trim(dflash_handle* h, const int32_t* slots, int32_t batch, const int32_t* draft,
+                       const int32_t* target, int32_t* accept_len, int32_t* bonus, int32_t* ctx_len,
+                       void* stream) {
+  if (!h || !slots || !draft || !target || !accept_len || !bonus || !ctx_len) return DFLASH_ERR_INVALID_ARG;
+  if (batch < 0 || batch > h->cfg.max_batch) return DFLASH_ERR_INVALID_ARG;
+  if (batch == 0) return DFLASH_OK;
+  if (cudaSetDevice(h->cfg.device) != cudaSuccess) return DFLASH_ERR_CUDA;
+  h->launches++;
+  return cuda_err(launch_accept(slots, batch, draft, target, accept_len, bonus, ctx_len, h->ctx_len,
+                                h->cfg.max_slots, h->status, (cudaStream_t)stream));
+}
+
+int dflash_reset_slot(dflash_handle* h, int32_t slot, void* stream) {
+  if (!h || slot < 0 || slot >= h->cfg.max_slots) return DFLASH_ERR_INVALID_ARG;
+  if (cudaSetDevice(h->cfg.device) != cudaSuccess) return DFLASH_ERR_CUDA;
+  h->launches++;
+  return cuda_err(launch_reset_slot(slot, h->ctx_len, h->n_pages, h->page_table, h->cfg.max_pages_per_slot,
+                                    h->free_stack, h->free_top, (cudaStream_t)stream));
+}
+
+int dflash_read_status(dflash_handle* h, uint32_t* out) {
+  if (!h || !out) return DFLASH_ERR_INVALID_ARG;
+  if (cudaSetDevice(h->cfg.device) != cudaSuccess) return DFLASH_ERR_CUDA;
+  int rc = cuda_err(cudaDeviceSynchronize());
+  if (rc) return rc;
+  rc = cuda_err(cudaMemcpy(out, h->status, sizeof(uint32_t), cudaMemcpyDeviceToHost));
+  if (rc) return rc;
+  return cuda_err(cudaMemset(h->status, 0, sizeof(uint32_t)));
+}
+
+int dflash_graph_begin(dflash_handle* h, void* stream) {
+  if (!h) return DFLASH_ERR_INVALID_ARG;
+  if (cudaSetDevice(h->cfg.device) != cudaSuccess) return DFLASH_ERR_CUDA;
+  return cuda_err(cudaStreamBeginCapture((cudaStream_t)stream, cudaStreamCaptureModeThreadLocal));
+}
+
+int dflash_graph_end(dflash_handle* h, void* stream, int32_t* n_kernels) {
+  if (!h) return DFLASH_ERR_INVALID_ARG;
+  cudaGraph_t g = nullptr;
+  int rc = cuda_err(cudaStreamEndCapture((cudaStream_t)stream, &g));
+  if (rc) return rc;
+  size_t n = 0;
+  rc = cuda_err(cudaGraphGetNodes(g, nullptr, &n));
+  std::vector<cudaGraphNode_t> nodes(n);
+  if (!rc && n) rc = cuda_err(cudaGraphGetNodes(g, nodes.data(), &n));
+  int kernels = 0;
+  for (size_t i = 0; i < n && !rc; ++i) {
+    cudaGraphNodeType t;
+    if (cudaGraphNodeGetType(nodes[i], &t) == cudaSuccess && t == cudaGraphNodeTypeKernel) ++kernels;
+  }
+  cudaGraphExec_t e = nullptr;
+  if (!rc) rc = cuda_err(cudaGraphInstantiate(&e, g, 0));
+  if (rc) {
+    if (g) cudaGraphDestroy(g);
+    return rc;
+  }
+  if (h->exec) cudaGraphExecDestroy(h->exec);
+  if (h->graph) cudaGraphDestroy(h->graph);
+  h->graph = g;
+  h->exec = e;
+  if (n_kernels) *n_kernels = kernels;
+  return DFLASH_OK;
+}
+
+int dflash_graph_launch(dflash_handle* h, void* stream) {
+  if (!h || !h->exec) return DFLASH_ERR_INVALID_ARG;
+  return cuda_err(cudaGraphLaunch(h->exec, (cudaStream_t)stream));
+}
+
+int dflash_read_kv(dflash_handle* h, int32_t layer, int32_t slot, int32_t pos0, int32_t n, void* k_out,
+                   void* v_out, void* stream) {
+  if (!h || !k_out || !v_out || layer < 0 || layer >= h->cfg.n_layers || slot < 0 || slot >= h->cfg.max_slots ||
+      pos0 < 0 || n < 0 || pos0 + n > h->max_pos)
+    return DFLASH_ERR_INVALID_ARG;
+  if (cudaSetDevice(h->cfg.device) != cudaSuccess) return DFLASH_ERR_CUDA;
+  return cuda_err(launch_read_kv(kv_geom(h), layer, slot, pos0, n, static_cast<bf16*>(k_out),
+                                 static_cast<bf16*>(v_out), (cudaStream_t)stream));
+}
+
+int dflash_slot_lengths(dflash_handle* h, const int32_t* slots, int32_t batch, int32_t* out, void* stream) {
+  if (!h || !slots || !out || batch < 0) return DFLASH_ERR_INVALID_ARG;
+  if (batch == 0) return DFLASH_OK;
+  if (cudaSetDevice(h->cfg.device) != cudaSuccess) return DFLASH_ERR_CUDA;
+  return cuda_err(launch_slot_lengths(slots, batch, h->ctx_len, h->cfg.max_slots, out, (cudaStream_t)stream));
+}
+
+int dflash_probe_arm(dflash_handle* h, int32_t kernel_id, int32_t n) {
+  if (!h || n < 0) return DFLASH_ERR_INVALID_ARG;
+  if (cudaSetDevice(h->cfg.device) != cudaSuccess) return DFLASH_ERR_CUDA;
+  while ((int)h->probe.ev.size() < 2 * n) {
+    cudaEvent_t e;
+    int rc = cuda_err(cudaEventCreate(&e));
+    if (rc) return rc;
+    h->probe.ev.push_back(e);
+  }
+  h->probe.kid = kernel_id;
+  h->probe.n = n;
+  h->probe.next = 0;
+  return DFLASH_OK;
+}
+
+int dflash_probe_read(dflash_handle* h, float* ms_out, int32_t cap, int32_t* n_out) {
+  if (!h || (!ms_out && cap > 0)) return DFLASH_ERR_INVALID_ARG;
+  const int n = std::min(h->probe.next, (int)cap);
+  for (int i = 0; i < n; ++i) {
+    int rc = cuda_err(cudaEventSynchronize(h->probe.ev[2 * i + 1]));
+    if (rc) return rc;
+    rc = cuda_err(cudaEventElapsedTime(ms_out + i, h->probe.ev[2 * i], h->probe.ev[2 * i + 1]));
+    if (rc) return rc;
+  }
+  if (n_out) *n_out = n;
+  return DFLASH_OK;
+}
+
+uint64_t dflash_launch_count(dflash_handle* h) { return h ? h->launches : 0; }
+
+int dflash_harness_verify(dflash_handle* h, const int32_t* slots, int32_t batch, const int32_t* draft,
+                          const int32_t* match, const int32_t* offs, int32_t rounds_cap, int32_t* round_ctr,
+                          int32_t* target, const void* feat_stream, int32_t stream_rows, void* feats_out,
+                          void* stream) {
+  if (!h || !slots || !draft || !match || !offs || !round_ctr || !target || rounds_cap <= 0) {
+    return DFLASH_ERR_INVALID_ARG;
+  }
+  if (batch < 0 || batch > h->cfg.max_batch) return DFLASH_ERR_INVALID_ARG;
+  if (feat_stream && (!feats_out || stream_rows <= 0)) return DFLASH_ERR_INVALID_ARG;
+  if (batch == 0) return DFLASH_OK;
+  if (cudaSetDevice(h->cfg.device) != cudaSuccess) return DFLASH_ERR_CUDA;
+  h->launches++;
+  return cuda_err(launch_harness_verify(slots, batch, draft, match, offs, rounds_cap, round_ctr, target,
+                                        h->cfg.vocab, static_cast<const bf16*>(feat_stream), stream_rows,
+                                        static_cast<bf16*>(feats_out), h->cfg.n_fused * h->cfg.hidden,
+                                        h->ctx_len, h->cfg.max_slots, (cudaStream_t)stream));
+}
+
+}  // extern "C"

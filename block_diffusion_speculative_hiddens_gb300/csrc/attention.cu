@@ -1,0 +1,335 @@
+// Block attention: the 16 block queries of every query head attend, with no
+// mask, to [context K/V ; block K/V] of their KV head (grouped-query attention).
+//
+// Grid (split, kv_head, request).  One CTA owns the G = hq/hkv query heads of
+// one KV head (G warps, 16 block rows each) and a contiguous range of the
+// request's 64-position pages.  Each page of K (64 x D) and V^T (D x 64) is a
+// contiguous 2 x 8..16 KB block stored pre-swizzled in HBM, so an untiled TMA
+// bulk copy lands it in shared memory already in a bank-conflict-free layout
+// for ldmatrix.  Q.K^T and P.V run on warp MMAs (m16n8k16, bf16 in, fp32
+// accumulate), the softmax is online in the log2 domain with quad shuffles.
+// Splits write fp32 partials (O, running max, running sum); the last CTA of a
+// (request, KV head) merges them in split order -- deterministic, no waiting.
+#include "common.cuh"
+#include "internal.h"
+
+namespace {
+
+template <int D>
+struct AttnCfg {
+  static constexpr int STAGES = 3;
+  static constexpr int BLK_BYTES = 64 * D * 2;               // one K (or V) page block
+  static constexpr int STAGE_BYTES = 2 * BLK_BYTES;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + 128;    // + barriers and flag
+};
+
+template <int D, int G>
+__global__ void __launch_bounds__(G * 32) k_attn(const AttnParams p) {
+  using C = AttnCfg<D>;
+  extern __shared__ __align__(128) uint8_t sm[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + C::STAGES * C::STAGE_BYTES);
+  int* flag = reinterpret_cast<int*>(full + C::STAGES);
+
+  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, c4 = lane & 3;
+  const int rows = G * 16;
+  const int hq = p.hq, hkv = p.hkv;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) mbar_init(full + s, 1);
+    fence_mbar_init();
+  }
+  pdl_launch_dependents();
+  pdl_wait();
+  __syncthreads();
+
+  const int slot = p.slots[b];
+  const int nkeys = p.ctx_len[slot] + DFL_BLOCK;
+  const int npages = (nkeys + 63) >> 6;
+  const int per = (npages + p.n_splits - 1) / p.n_splits;
+  const int pb = split * per;
+  const int pe = min(npages, pb + per);
+  const bf16* kbase = p.kv.k_pool + (size_t)p.layer * p.kv.layer_stride;
+  const bf16* vbase = p.kv.v_pool + (size_t)p.layer * p.kv.layer_stride;
+  const int* pt = p.kv.page_table + (size_t)slot * p.kv.max_pages_per_slot;
+
+  auto issue = [&](int s, int page_idx) {
+    int pg = page_idx < p.kv.max_pages_per_slot ? pt[page_idx] : -1;
+    if (pg < 0 || pg >= p.kv.max_pages) {
+      dev_error(p.status, DFLASH_DEV_PAGE);
+      pg = 0;
+    }
+    const size_t off = ((size_t)pg * hkv + kvh) * (64 * D);
+    uint8_t* dst = sm + s * C::STAGE_BYTES;
+    mbar_arrive_expect_tx(full + s, C::STAGE_BYTES);
+    bulk_load(dst, kbase + off, C::BLK_BYTES, full + s);
+    bulk_load(dst + C::BLK_BYTES, vbase + off, C::BLK_BYTES, full + s);
+  };
+  int issued = 0;  // meaningful in thread 0 only
+  if (threadIdx.x == 0)
+    for (int i = 0; i < C::STAGES && pb + i < pe; ++i, ++issued) issue(i, pb + i);
+
+  // Q fragments of this warp's query head (16 block rows x D) in registers.
+  const int j = kvh * G + warp;
+  uint32_t qa[D / 16][4];
+  {
+    const bf16* q0 = p.q + ((size_t)(b * DFL_BLOCK) * hq + j) * D;
+    const size_t rs = (size_t)hq * D;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const int col = kk * 16 + 2 * c4;
+      qa[kk][0] = *reinterpret_cast<const uint32_t*>(q0 + g * rs + col);
+      qa[kk][1] = *reinterpret_cast<const uint32_t*>(q0 + (g + 8) * rs + col);
+      qa[kk][2] = *reinterpret_cast<const uint32_t*>(q0 + g * rs + col + 8);
+      qa[kk][3] = *reinterpret_cast<const uint32_t*>(q0 + (g + 8) * rs + col + 8);
+    }
+  }
+
+  float o[D / 8][4];
+#pragma unroll
+  for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  bool aborted = false;
+  const int mi = lane >> 3, rr = lane & 7;
+
+  int it = 0;
+  for (int pi = pb; pi < pe; ++pi, ++it) {
+    const int s = it % C::STAGES;
+    const bool ok = mbar_wait(full + s, (uint32_t)((it / C::STAGES) & 1), p.status, &aborted);
+    if (ok) {
+      const int valid = min(64, nkeys - pi * 64);
+      const uint32_t kb_addr = smem_u32(sm + s * C::STAGE_BYTES);
+      const uint32_t vb_addr = kb_addr + C::BLK_BYTES;
+      float sc[8][4];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
+      // S = Q K^T over this page's 64 keys
+#pragma unroll
+      for (int kg = 0; kg < 4; ++kg) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const int key = kg * 16 + (mi >> 1) * 8 + rr;
+          const int chunk = kk * 2 + (mi & 1);
+          const uint32_t addr =
+              kb_addr + 2u * (uint32_t)((chunk >> 3) * (64 * 64) + key * 64 + (((chunk & 7) ^ (key & 7)) << 3));
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(addr, b0, b1, b2, b3);
+          mma_bf16_16816(sc[2 * kg], qa[kk], b0, b1);
+          mma_bf16_16816(sc[2 * kg + 1], qa[kk], b2, b3);
+        }
+      }
+      // online softmax (log2 domain), rows g and g+8 of this warp
+      float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int key = nt * 8 + 2 * c4 + (e & 1);
+          float v = sc[nt][e] * p.scale_log2;
+          if (key >= valid) v = -INFINITY;
+          sc[nt][e] = v;
+        }
+        mx0 = fmaxf(mx0, fmaxf(sc[nt][0], sc[nt][1]));
+        mx1 = fmaxf(mx1, fmaxf(sc[nt][2], sc[nt][3]));
+      }
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      const float a0 = exp2f(m0 - mn0), a1 = exp2f(m1 - mn1);
+      float rs0 = 0.f, rs1 = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+        sc[nt][0] = exp2f(sc[nt][0] - mn0);
+        sc[nt][1] = exp2f(sc[nt][1] - mn0);
+        sc[nt][2] = exp2f(sc[nt][2] - mn1);
+        sc[nt][3] = exp2f(sc[nt][3] - mn1);
+        rs0 += sc[nt][0] + sc[nt][1];
+        rs1 += sc[nt][2] + sc[nt][3];
+      }
+      l0 = l0 * a0 + rs0;
+      l1 = l1 * a1 + rs1;
+      m0 = mn0;
+      m1 = mn1;
+#pragma unroll
+      for (int nd = 0; nd < D / 8; ++nd) {
+        o[nd][0] *= a0;
+        o[nd][1] *= a0;
+        o[nd][2] *= a1;
+        o[nd][3] *= a1;
+      }
+      // O += P V  (V^T page: rows = dims, 64 keys per row)
+#pragma unroll
+      for (int k2 = 0; k2 < 4; ++k2) {
+        uint32_t pa[4];
+        pa[0] = pack_bf16x2(sc[2 * k2][0], sc[2 * k2][1]);
+        pa[1] = pack_bf16x2(sc[2 * k2][2], sc[2 * k2][3]);
+        pa[2] = pack_bf16x2(sc[2 * k2 + 1][0], sc[2 * k2 + 1][1]);
+        pa[3] = pack_bf16x2(sc[2 * k2 + 1][2], sc[2 * k2 + 1][3]);
+#pragma unroll
+        for (int nd = 0; nd < D / 8; nd += 2) {
+          const int dim = (nd + (mi >> 1)) * 8 + rr;
+          const int chunk = 2 * k2 + (mi & 1);
+          const uint32_t addr = vb_addr + 2u * (uint32_t)(dim * 64 + ((chunk ^ (dim & 7)) << 3));
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(addr, b0, b1, b2, b3);
+          mma_bf16_16816(o[nd], pa, b0, b1);
+          mma_bf16_16816(o[nd + 1], pa, b2, b3);
+        }
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !aborted && pi + C::STAGES < pe) {
+      issue(s, pi + C::STAGES);
+      ++issued;
+    }
+  }
+  if (threadIdx.x == 0 && aborted) {
+    // let copies already in flight land before the CTA exits
+    for (int i = (issued > C::STAGES ? issued - C::STAGES : 0); i < issued; ++i) {
+      bool drain_abort = false;
+      mbar_wait(full + (i % C::STAGES), (uint32_t)((i / C::STAGES) & 1), p.status, &drain_abort);
+    }
+  }
+
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+  const int r0 = warp * 16 + g, r1 = r0 + 8;
+
+  if (p.n_splits == 1) {
+    const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
+    bf16* out0 = p.out + ((size_t)(b * DFL_BLOCK + g) * hq + j) * D;
+    bf16* out1 = p.out + ((size_t)(b * DFL_BLOCK + g + 8) * hq + j) * D;
+#pragma unroll
+    for (int nd = 0; nd < D / 8; ++nd) {
+      const int d = nd * 8 + 2 * c4;
+      *reinterpret_cast<uint32_t*>(out0 + d) = pack_bf16x2(o[nd][0] * i0, o[nd][1] * i0);
+      *reinterpret_cast<uint32_t*>(out1 + d) = pack_bf16x2(o[nd][2] * i1, o[nd][3] * i1);
+    }
+    return;
+  }
+
+  float* part = p.ws + (size_t)((b * hkv + kvh) * p.n_splits + split) * (size_t)(rows * (D + 2));
+#pragma unroll
+  for (int nd = 0; nd < D / 8; ++nd) {
+    const int d = nd * 8 + 2 * c4;
+    __stcg(reinterpret_cast<float2*>(part + (size_t)r0 * D + d), make_float2(o[nd][0], o[nd][1]));
+    __stcg(reinterpret_cast<float2*>(part + (size_t)r1 * D + d), make_float2(o[nd][2], o[nd][3]));
+  }
+  if (c4 == 0) {
+    __stcg(part + rows * D + r0, m0);
+    __stcg(part + rows * D + r1, m1);
+    __stcg(part + rows * D + rows + r0, l0);
+    __stcg(part + rows * D + rows + r1, l1);
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned old = atomicAdd(p.ctr + b * hkv + kvh, 1u);
+    const int last = old == (unsigned)p.n_splits - 1;
+    if (last) p.ctr[b * hkv + kvh] = 0;
+    *flag = last;
+  }
+  __syncthreads();
+  if (!*flag) return;
+  __threadfence();
+
+  // merge the splits in split order; per-split weights in shared memory
+  float* wsm = reinterpret_cast<float*>(sm);  // [n_splits][rows]
+  const float* base = p.ws + (size_t)((b * hkv + kvh) * p.n_splits) * (size_t)(rows * (D + 2));
+  const size_t pstride = (size_t)rows * (D + 2);
+  for (int r = threadIdx.x; r < rows; r += blockDim.x) {
+    float M = -INFINITY;
+    for (int s = 0; s < p.n_splits; ++s) {
+      const float ls = __ldcg(base + s * pstride + rows * D + rows + r);
+      if (ls > 0.f) M = fmaxf(M, __ldcg(base + s * pstride + rows * D + r));
+    }
+    float L = 0.f;
+    for (int s = 0; s < p.n_splits; ++s) {
+      const float ls = __ldcg(base + s * pstride + rows * D + rows + r);
+      const float w = ls > 0.f ? exp2f(__ldcg(base + s * pstride + rows * D + r) - M) : 0.f;
+      wsm[s * rows + r] = w;
+      L += w * ls;
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    for (int s = 0; s < p.n_splits; ++s) wsm[s * rows + r] *= inv;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < rows * D / 4; e += blockDim.x) {
+    const int r = (e * 4) / D, d = (e * 4) % D;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < p.n_splits; ++s) {
+      const float w = wsm[s * rows + r];
+      if (w != 0.f) {
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(base + s * pstride + (size_t)r * D + d));
+        acc.x += w * v.x;
+        acc.y += w * v.y;
+        acc.z += w * v.z;
+        acc.w += w * v.w;
+      }
+    }
+    const int wq = r / 16, t = r % 16;
+    bf16* dst = p.out + ((size_t)(b * DFL_BLOCK + t) * hq + kvh * G + wq) * D + d;
+    *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc.x, acc.y);
+    *reinterpret_cast<uint32_t*>(dst + 2) = pack_bf16x2(acc.z, acc.w);
+  }
+}
+
+template <int D, int G>
+cudaError_t launch_t(const AttnParams& p, int batch, cudaStream_t s, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)p.n_splits, (unsigned)p.hkv, (unsigned)batch);
+  cfg.blockDim = dim3(G * 32);
+  cfg.dynamicSmemBytes = AttnCfg<D>::SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k_attn<D, G>, p);
+}
+
+template <int D>
+cudaError_t launch_d(const AttnParams& p, int batch, cudaStream_t s, bool pdl) {
+  switch (p.hq / p.hkv) {
+    case 1: return launch_t<D, 1>(p, batch, s, pdl);
+    case 2: return launch_t<D, 2>(p, batch, s, pdl);
+    case 4: return launch_t<D, 4>(p, batch, s, pdl);
+    case 8: return launch_t<D, 8>(p, batch, s, pdl);
+  }
+  return cudaErrorInvalidValue;
+}
+
+template <int D>
+cudaError_t attr_d() {
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(k_attn<D, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnCfg<D>::SMEM)))
+    return e;
+  if ((e = cudaFuncSetAttribute(k_attn<D, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnCfg<D>::SMEM)))
+    return e;
+  if ((e = cudaFuncSetAttribute(k_attn<D, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnCfg<D>::SMEM)))
+    return e;
+  return cudaFuncSetAttribute(k_attn<D, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnCfg<D>::SMEM);
+}
+
+}  // namespace
+
+int attn_stages(int D) { return D == 64 ? AttnCfg<64>::STAGES : AttnCfg<128>::STAGES; }
+size_t attn_smem_bytes(int D, int) { return D == 64 ? AttnCfg<64>::SMEM : AttnCfg<128>::SMEM; }
+
+cudaError_t attn_init_attributes() {
+  cudaError_t e = attr_d<64>();
+  if (e) return e;
+  return attr_d<128>();
+}
+
+cudaError_t attn_launch(const AttnParams& p, int batch, cudaStream_t s, bool pdl) {
+  if (p.D == 64) return launch_d<64>(p, batch, s, pdl);
+  if (p.D == 128) return launch_d<128>(p, batch, s, pdl);
+  return cudaErrorInvalidValue;
+}

@@ -1,0 +1,512 @@
+// Weight-streaming GEMM on the 5th-generation tensor cores (tcgen05 + TMEM).
+//
+// out[t][n] = sum_k X[t][k] * W[n][k] for the drafter's projections.  The
+// weight matrix is the 128-row A operand ("swap-AB"): at batch 1 the block has
+// only 16 token rows, which become the MMA's N dimension (16..256), so one
+// tcgen05.mma.cta_group::1 M=128 instruction covers 128 output features x all
+// tokens, and the weights stream through shared memory exactly once.
+//
+// Pipeline per CTA (persistent, one per SM, 192 threads):
+//   warp 0  TMA producer: 128x64 weight tile (two 64-row boxes) + BNx64 token
+//           tile per stage, 128-byte swizzle, completion on an mbarrier;
+//   warp 1  TMEM allocator and single-thread MMA issuer (4 x K=16 per stage),
+//           double-buffered fp32 accumulators in TMEM;
+//   warps 2-5 epilogue: tcgen05.ld -> registers -> fused epilogue.
+//
+// Work split: the (tile, 64-wide k-block) units are divided evenly over the
+// grid (stream-K style), so every SM streams the same number of weight bytes.
+// A tile cut between CTAs writes fp32 partials; the last CTA to arrive (device
+// counter, no waiting) sums them in k order -- deterministic -- and runs the
+// epilogue.  All waits are bounded (%globaltimer) and report through the
+// status word instead of hanging.
+#include "common.cuh"
+#include "internal.h"
+
+namespace {
+
+constexpr int A_STAGE_BYTES = 128 * 128;  // 128 rows x 64 bf16
+constexpr int STG_BYTES = 32 * 128 * 4;   // epilogue staging: 32 tokens x 128 rows fp32
+constexpr int EPI_THREADS = 128;
+
+DFL_DEV long long unit_start(long long c, long long U, long long G) { return c * U / G; }
+// CTA whose unit range [unit_start(c), unit_start(c+1)) contains unit u.
+DFL_DEV long long cta_of_unit(long long u, long long U, long long G) { return ((u + 1) * G + U - 1) / U - 1; }
+
+DFL_DEV float norm_scale(const float* ss, int parts, int M, int t, int width, float eps, int lane) {
+  float s = 0.f;
+  for (int i = lane; i < parts; i += 32) s += ss[(size_t)i * M + t];
+  s = warp_sum(s);
+  return rsqrtf(s / (float)width + eps);
+}
+
+// Head RMSNorm + RoPE on the 4 values a lane holds (rows lane, lane+32,
+// lane+64, lane+96 of a 128-row tile).  D = 128: one head, RoPE pairs (0,2),
+// (1,3).  D = 64: two heads (rows 0-63, 64-127), pairs (0,1) and (2,3).
+DFL_DEV void head_norm_rope(float* x, const bf16* gain, const float2* rope_row, int D, float eps, int lane) {
+  if (D == 128) {
+    float ss = warp_sum(x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3]);
+    const float inv = rsqrtf(ss / 128.f + eps);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) x[j] *= inv * bf2f(gain[lane + 32 * j]);
+    const float2 c0 = rope_row[lane], c1 = rope_row[lane + 32];
+    const float a0 = x[0], b0 = x[2], a1 = x[1], b1 = x[3];
+    x[0] = a0 * c0.x - b0 * c0.y;
+    x[2] = b0 * c0.x + a0 * c0.y;
+    x[1] = a1 * c1.x - b1 * c1.y;
+    x[3] = b1 * c1.x + a1 * c1.y;
+  } else {  // D == 64
+    const float sa = warp_sum(x[0] * x[0] + x[1] * x[1]);
+    const float sb = warp_sum(x[2] * x[2] + x[3] * x[3]);
+    const float ia = rsqrtf(sa / 64.f + eps), ib = rsqrtf(sb / 64.f + eps);
+    const float g0 = bf2f(gain[lane]), g1 = bf2f(gain[lane + 32]);
+    x[0] *= ia * g0;
+    x[1] *= ia * g1;
+    x[2] *= ib * g0;
+    x[3] *= ib * g1;
+    const float2 c = rope_row[lane];
+    const float a0 = x[0], b0 = x[1], a1 = x[2], b1 = x[3];
+    x[0] = a0 * c.x - b0 * c.y;
+    x[1] = b0 * c.x + a0 * c.y;
+    x[2] = a1 * c.x - b1 * c.y;
+    x[3] = b1 * c.x + a1 * c.y;
+  }
+}
+
+DFL_DEV void write_k(const GemmParams& p, int layer, int slot, int pos, int kh, int d, float v) {
+  const int pg_i = pos >> 6;
+  if (pg_i >= p.kv.max_pages_per_slot) { dev_error(p.status, DFLASH_DEV_PAGE); return; }
+  const int pg = p.kv.page_table[(size_t)slot * p.kv.max_pages_per_slot + pg_i];
+  if (pg < 0 || pg >= p.kv.max_pages) { dev_error(p.status, DFLASH_DEV_PAGE); return; }
+  bf16* blk = p.kv.k_pool + (size_t)layer * p.kv.layer_stride + ((size_t)pg * p.kv.hkv + kh) * (64 * p.kv.D);
+  blk[k_swz(pos & 63, d)] = __float2bfloat16(v);
+}
+DFL_DEV void write_v(const GemmParams& p, int layer, int slot, int pos, int kh, int d, float v) {
+  const int pg_i = pos >> 6;
+  if (pg_i >= p.kv.max_pages_per_slot) { dev_error(p.status, DFLASH_DEV_PAGE); return; }
+  const int pg = p.kv.page_table[(size_t)slot * p.kv.max_pages_per_slot + pg_i];
+  if (pg < 0 || pg >= p.kv.max_pages) { dev_error(p.status, DFLASH_DEV_PAGE); return; }
+  bf16* blk = p.kv.v_pool + (size_t)layer * p.kv.layer_stride + ((size_t)pg * p.kv.hkv + kh) * (64 * p.kv.D);
+  blk[v_swz(d, pos & 63)] = __float2bfloat16(v);
+}
+
+// Final epilogue for tokens t_first .. t_first+ntok-1 of `tile`; staging
+// stg[j][r] holds the fully reduced fp32 accumulators.  Epilogue warp ew
+// handles tokens j = ew, ew+4, ...; lane holds rows lane + 32*jj.
+template <int MODE>
+DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, const float* stg, int ew, int lane) {
+  const int tt_all = tile / p.t_tiles;       // (group, n-tile)
+  const int group = tt_all / p.n_tiles;
+  const int nt = tt_all % p.n_tiles;
+  for (int j = ew; j < ntok; j += 4) {
+    const int t = t_first + j;
+    const float* row = stg + j * 128;
+    float x[4] = {row[lane], row[lane + 32], row[lane + 64], row[lane + 96]};
+
+    if (MODE == GM_RESID || MODE == GM_FC) {
+      const int n0 = nt * 128;
+      float sq = 0.f;
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        const int n = n0 + lane + 32 * jj;
+        const size_t o = (size_t)t * p.N + n;
+        float hv = x[jj];
+        if (MODE == GM_RESID) {
+          hv += p.h[o];
+          p.h[o] = hv;
+        }
+        p.out[o] = __float2bfloat16(hv * bf2f(p.gain[n]));
+        sq += hv * hv;
+      }
+      sq = warp_sum(sq);
+      if (lane == 0) p.ss_out[(size_t)nt * p.M + t] = sq;
+    } else if (MODE == GM_SWIGLU) {
+      const float s = norm_scale(p.ss_in, p.ss_parts, p.M, t, p.H, p.eps, lane);
+      const int f0 = nt * 64;
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj) {
+        const float g = x[jj] * s, u = x[jj + 2] * s;
+        const float a = g / (1.f + __expf(-g)) * u;
+        p.out[(size_t)t * p.N + f0 + lane + 32 * jj] = __float2bfloat16(a);
+      }
+    } else if (MODE == GM_ARGMAX) {
+      const float s = norm_scale(p.ss_in, p.ss_parts, p.M, t, p.H, p.eps, lane);
+      const int n0 = nt * 128;
+      unsigned long long best = 0ull;
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        const int n = n0 + lane + 32 * jj;
+        if (n < p.N) {
+          const float v = x[jj] * s;
+          if (v != v) {
+            dev_error(p.status, DFLASH_DEV_NAN);
+            continue;
+          }
+          if (p.logits) p.logits[(size_t)t * p.N + n] = v;
+          const unsigned long long k = argmax_key(v, (uint32_t)n);
+          best = k > best ? k : best;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
+        best = other > best ? other : best;
+      }
+      if (lane == 0 && best) atomicMax(p.keys + t, best);
+    } else if (MODE == GM_QKV || MODE == GM_INJECT) {
+      const int D = p.D;
+      int slot, pos, layer, kind, n0;
+      const bf16* kgain;
+      float s;
+      if (MODE == GM_QKV) {
+        const int b = t / DFL_BLOCK;
+        slot = p.slots[b];
+        pos = p.ctx_len[slot] + (t % DFL_BLOCK);
+        layer = p.layer;
+        n0 = nt * 128;
+        kind = n0 < p.hq * D ? 0 : (n0 < (p.hq + p.hkv) * D ? 1 : 2);
+        kgain = kind == 0 ? p.qn_gain : p.kn_gain[0];
+      } else {
+        const int b = t / p.rows_per_req;
+        const int i = t % p.rows_per_req;
+        if (i >= p.n_eff[b]) continue;  // warp-uniform: one token per warp
+        slot = p.slots[b];
+        pos = p.pos0[slot] + i;
+        layer = group;
+        n0 = nt * 128 + p.hq * D;  // row index in this layer's wqkv
+        kind = n0 < (p.hq + p.hkv) * D ? 1 : 2;
+        kgain = p.kn_gain[group];
+      }
+      s = norm_scale(p.ss_in, p.ss_parts, p.M, t, p.H, p.eps, lane);
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) x[jj] *= s;
+      if (pos >= p.max_pos) {
+        dev_error(p.status, DFLASH_DEV_CAPACITY);
+        continue;
+      }
+      if (kind < 2) head_norm_rope(x, kgain, p.rope + (size_t)pos * (D / 2), D, p.eps, lane);
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        const int n = n0 + lane + 32 * jj;
+        if (kind == 0) {
+          p.out[(size_t)t * (p.hq * D) + n] = __float2bfloat16(x[jj]);
+        } else if (kind == 1) {
+          const int m = n - p.hq * D;
+          write_k(p, layer, slot, pos, m / D, m % D, x[jj]);
+        } else {
+          const int m = n - (p.hq + p.hkv) * D;
+          write_v(p, layer, slot, pos, m / D, m % D, x[jj]);
+        }
+      }
+    }
+  }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
+    k_gemm(const __grid_constant__ TmapSet tmA, const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* sm = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  const int BN = p.BN;
+  const int stages = p.stages;
+  const int stage_bytes = A_STAGE_BYTES + BN * 128;
+  float* stg = reinterpret_cast<float*>(sm + (size_t)stages * stage_bytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + (size_t)stages * stage_bytes + STG_BYTES);
+  uint64_t* empty = full + stages;
+  uint64_t* tfull = empty + stages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* mdone = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mdone + 1);
+  int* flag = reinterpret_cast<int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t ncols = (uint32_t)p.tmem_cols;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, 1);
+    }
+    mbar_init(tfull + 0, 1);
+    mbar_init(tfull + 1, 1);
+    mbar_init(tempty + 0, EPI_THREADS);
+    mbar_init(tempty + 1, EPI_THREADS);
+    mbar_init(mdone, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, ncols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_launch_dependents();
+
+  const long long KB = p.kblocks;
+  const long long G = gridDim.x, c = blockIdx.x;
+  long long U, u0, u1;
+  if (p.allow_split) {
+    U = (long long)p.total_tiles * KB;
+    u0 = unit_start(c, U, G);
+    u1 = unit_start(c + 1, U, G);
+  } else {
+    U = (long long)p.total_tiles * KB;
+    u0 = unit_start(c, p.total_tiles, G) * KB;
+    u1 = unit_start(c + 1, p.total_tiles, G) * KB;
+  }
+  bool aborted = false;
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tmap(&tmB);
+      for (int g = 0; g < p.groups; ++g) prefetch_tmap(&tmA.m[g]);
+      const bool stream_w = p.t_tiles == 1;
+      const uint64_t pol = policy_evict_first();
+      auto load_a = [&](int s, long long u) {
+        const int tile = (int)(u / KB), kb = (int)(u % KB);
+        const int tt_all = tile / p.t_tiles;
+        const int g = tt_all / p.n_tiles, nt = tt_all % p.n_tiles;
+        int y0, y1;
+        if (MODE == GM_SWIGLU) {
+          y0 = p.a_row_off + nt * 64;
+          y1 = p.up_off + nt * 64;
+        } else {
+          y0 = p.a_row_off + nt * 128;
+          y1 = y0 + 64;
+        }
+        uint8_t* dst = sm + (size_t)s * stage_bytes;
+        if (stream_w) {
+          tma_load_2d_hint(dst, &tmA.m[g], full + s, kb * 64, y0, pol);
+          tma_load_2d_hint(dst + 8192, &tmA.m[g], full + s, kb * 64, y1, pol);
+        } else {
+          tma_load_2d(dst, &tmA.m[g], full + s, kb * 64, y0);
+          tma_load_2d(dst + 8192, &tmA.m[g], full + s, kb * 64, y1);
+        }
+      };
+      auto load_b = [&](int s, long long u) {
+        const int tile = (int)(u / KB), kb = (int)(u % KB);
+        const int tt = tile % p.t_tiles;
+        tma_load_2d(sm + (size_t)s * stage_bytes + A_STAGE_BYTES, &tmB, full + s, kb * 64, tt * BN);
+      };
+      // Weights do not depend on the previous kernel: fetch the first stages'
+      // weight tiles before waiting on it, then the token tiles.
+      const long long pre = (u1 - u0) < stages ? (u1 - u0) : stages;
+      for (long long i = 0; i < pre; ++i) {
+        mbar_arrive_expect_tx(full + i, stage_bytes);
+        load_a((int)i, u0 + i);
+      }
+      pdl_wait();
+      for (long long i = 0; i < pre; ++i) load_b((int)i, u0 + i);
+      long long it = pre;
+      for (long long u = u0 + pre; u < u1; ++u, ++it) {
+        const int s = (int)(it % stages);
+        const uint32_t round = (uint32_t)(it / stages);
+        if (!mbar_wait(empty + s, (round & 1u) ^ 1u, p.status, &aborted)) break;
+        mbar_arrive_expect_tx(full + s, stage_bytes);
+        load_a(s, u);
+        load_b(s, u);
+      }
+      // drain: every issued copy lands before the CTA may exit
+      const long long issued = it;
+      for (long long i = (issued > stages ? issued - stages : 0); i < issued; ++i) {
+        bool drain_abort = false;
+        mbar_wait(full + (i % stages), (uint32_t)((i / stages) & 1), p.status, &drain_abort);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(128, BN);
+      long long it = 0;
+      int seg = 0;
+      for (long long u = u0; u < u1 && !aborted; ++seg) {
+        const long long tile = u / KB;
+        const long long seg_end = (tile + 1) * KB < u1 ? (tile + 1) * KB : u1;
+        const int abuf = seg & 1;
+        const uint32_t use = (uint32_t)(seg >> 1);
+        if (!mbar_wait(tempty + abuf, (use & 1u) ^ 1u, p.status, &aborted)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(abuf * BN);
+        for (long long k = 0; u < seg_end; ++u, ++k, ++it) {
+          const int s = (int)(it % stages);
+          if (!mbar_wait(full + s, (uint32_t)((it / stages) & 1), p.status, &aborted)) break;
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(sm + (size_t)s * stage_bytes);
+          const uint64_t adesc = sdesc_sw128(a_addr);
+          const uint64_t bdesc = sdesc_sw128(a_addr + A_STAGE_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma_bf16(d, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk), idesc,
+                        (k > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(empty + s);
+        }
+        tc_commit(tfull + abuf);
+      }
+      tc_commit(mdone);
+      bool drain_abort = false;
+      mbar_wait(mdone, 0, p.status, &drain_abort);
+    }
+  } else {
+    // ------------------------------------------------ epilogue (warps 2..5)
+    pdl_wait();
+    const int q = warp & 3;
+    const int r = q * 32 + lane;  // TMEM lane = tile row
+    const int et = threadIdx.x - 64;
+    const int ew = et >> 5;
+    int seg = 0;
+    for (long long u = u0; u < u1; ++seg) {
+      const long long tile = u / KB;
+      const long long seg_end = (tile + 1) * KB < u1 ? (tile + 1) * KB : u1;
+      u = seg_end;
+      const int abuf = seg & 1;
+      const uint32_t use = (uint32_t)(seg >> 1);
+      if (!mbar_wait(tfull + abuf, use & 1u, p.status, &aborted)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(abuf * BN);
+      const int tt = (int)(tile % p.t_tiles);
+      const int t_base = tt * BN;
+      const int mt = (p.M - t_base) < BN ? (p.M - t_base) : BN;
+      long long c_first = c, c_last = c;
+      if (p.allow_split) {
+        c_first = cta_of_unit(tile * KB, U, G);
+        c_last = cta_of_unit(tile * KB + KB - 1, U, G);
+      }
+      const bool split = c_first != c_last;
+      if (split) {
+        const int my_slot = (tile == unit_start(c, U, G) / KB) ? 0 : 1;
+        float* w = p.ws + (size_t)(c * 2 + my_slot) * (DFL_BN_MAX * 128);
+        for (int col = 0; col < BN; col += 16) {
+          float v[16];
+          tmem_ld16(taddr + (uint32_t)col, v);
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if (col + i < mt) __stcg(w + (size_t)(col + i) * 128 + r, v[i]);
+        }
+        tc_fence_before();
+        mbar_arrive(tempty + abuf);
+        __threadfence();
+        named_bar_sync(1, EPI_THREADS);
+        if (et == 0) {
+          const unsigned cnt = (unsigned)(c_last - c_first + 1);
+          const unsigned old = atomicAdd(p.tile_ctr + tile, 1u);
+          const int last = old == cnt - 1;
+          if (last) p.tile_ctr[tile] = 0;
+          *flag = last;
+        }
+        named_bar_sync(1, EPI_THREADS);
+        const int last = *flag;
+        named_bar_sync(1, EPI_THREADS);
+        if (!last) continue;
+        __threadfence();
+      }
+      for (int tc0 = 0; tc0 < mt; tc0 += 32) {
+#pragma unroll
+        for (int sub = 0; sub < 2; ++sub) {
+          const int col = tc0 + 16 * sub;
+          if (col < BN) {
+            float v[16];
+            if (split) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) v[i] = 0.f;
+              for (long long cc = c_first; cc <= c_last; ++cc) {
+                const int sl = (tile == unit_start(cc, U, G) / KB) ? 0 : 1;
+                const float* w = p.ws + (size_t)(cc * 2 + sl) * (DFL_BN_MAX * 128);
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                  if (col + i < mt) v[i] += __ldcg(w + (size_t)(col + i) * 128 + r);
+              }
+            } else {
+              tmem_ld16(taddr + (uint32_t)col, v);
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) stg[(16 * sub + i) * 128 + r] = v[i];
+          }
+        }
+        named_bar_sync(1, EPI_THREADS);
+        epi_final<MODE>(p, (int)tile, t_base + tc0, (mt - tc0) < 32 ? (mt - tc0) : 32, stg, ew, lane);
+        named_bar_sync(1, EPI_THREADS);
+      }
+      if (!split) {
+        tc_fence_before();
+        mbar_arrive(tempty + abuf);
+      }
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, ncols);
+  }
+  if (MODE == GM_ARGMAX) {
+    // The last CTA to finish turns the per-token argmax keys of block rows
+    // 1..15 into draft ids and clears the keys for the next round.
+    int* done_flag = flag + 1;
+    if (threadIdx.x == 0) {
+      __threadfence();
+      const unsigned old = atomicAdd(p.done_ctr, 1u);
+      *done_flag = old == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (*done_flag) {
+      __threadfence();
+      const int batch = p.M / DFL_BLOCK;
+      for (int idx = threadIdx.x; idx < batch * (DFL_BLOCK - 1); idx += blockDim.x) {
+        const int b = idx / (DFL_BLOCK - 1), i = idx % (DFL_BLOCK - 1) + 1;
+        const unsigned long long k = __ldcg(p.keys + b * DFL_BLOCK + i);
+        p.draft[idx] = k ? (int)argmax_key_index(k) : 0;
+      }
+      __syncthreads();
+      for (int idx = threadIdx.x; idx < p.M; idx += blockDim.x) p.keys[idx] = 0ull;
+      if (threadIdx.x == 0) *p.done_ctr = 0u;
+    }
+  }
+}
+
+}  // namespace
+
+size_t gemm_smem_bytes(int BN, int stages) {
+  return 1024 + (size_t)stages * (A_STAGE_BYTES + BN * 128) + STG_BYTES + (size_t)(2 * stages + 5) * 8 + 16;
+}
+
+int gemm_pick_stages(int BN) {
+  const size_t budget = 232448 - 1024 - STG_BYTES - 512;
+  int st = (int)(budget / (size_t)(A_STAGE_BYTES + BN * 128));
+  return st > 12 ? 12 : st;
+}
+
+cudaError_t gemm_init_attributes() {
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(k_gemm<GM_QKV>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448))) return e;
+  if ((e = cudaFuncSetAttribute(k_gemm<GM_INJECT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448))) return e;
+  if ((e = cudaFuncSetAttribute(k_gemm<GM_RESID>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448))) return e;
+  if ((e = cudaFuncSetAttribute(k_gemm<GM_SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448))) return e;
+  if ((e = cudaFuncSetAttribute(k_gemm<GM_FC>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448))) return e;
+  return cudaFuncSetAttribute(k_gemm<GM_ARGMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+}
+
+cudaError_t gemm_launch(const TmapSet& A, const CUtensorMap& B, const GemmParams& p, int grid, cudaStream_t s,
+                        bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(DFL_GEMM_THREADS);
+  cfg.dynamicSmemBytes = gemm_smem_bytes(p.BN, p.stages);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  switch (p.mode) {
+    case GM_QKV: return cudaLaunchKernelEx(&cfg, k_gemm<GM_QKV>, A, B, p);
+    case GM_INJECT: return cudaLaunchKernelEx(&cfg, k_gemm<GM_INJECT>, A, B, p);
+    case GM_RESID: return cudaLaunchKernelEx(&cfg, k_gemm<GM_RESID>, A, B, p);
+    case GM_SWIGLU: return cudaLaunchKernelEx(&cfg, k_gemm<GM_SWIGLU>, A, B, p);
+    case GM_FC: return cudaLaunchKernelEx(&cfg, k_gemm<GM_FC>, A, B, p);
+    case GM_ARGMAX: return cudaLaunchKernelEx(&cfg, k_gemm<GM_ARGMAX>, A, B, p);
+  }
+  return cudaErrorInvalidValue;
+}

@@ -1,0 +1,299 @@
+// Small kernels of the round: block embedding, page allocation, acceptance,
+// slot reset, RoPE table, cache read-back and the benchmark's stand-in verify.
+#include "common.cuh"
+#include "internal.h"
+
+namespace {
+
+cudaLaunchConfig_t cfg_of(dim3 grid, dim3 block, cudaStream_t s, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t c = {};
+  c.gridDim = grid;
+  c.blockDim = block;
+  c.stream = s;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  c.attrs = attr;
+  c.numAttrs = 1;
+  return c;
+}
+
+// a3: block = [last_tok, mask x 15]; h = E[block] (fp32 residual stream),
+// hg = bf16(h * g_in0) and per-128-feature sums of squares of h, the form the
+// first layer's QKV GEMM consumes.  Also clears the argmax keys.
+__global__ void k_embed(const int* __restrict__ slots, const int* __restrict__ last_tok, int mask_id,
+                        const bf16* __restrict__ E, const bf16* __restrict__ gain, int H, int M, float* h,
+                        bf16* hg, float* ss, unsigned long long* keys) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int t = blockIdx.x;
+  const int b = t / DFL_BLOCK, i = t % DFL_BLOCK;
+  const int tok = i == 0 ? last_tok[b] : mask_id;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  const bf16* row = E + (size_t)tok * H;
+  for (int part = warp; part < H / 128; part += nw) {
+    float sq = 0.f;
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      const int n = part * 128 + lane + 32 * jj;
+      const float v = bf2f(row[n]);
+      h[(size_t)t * H + n] = v;
+      hg[(size_t)t * H + n] = __float2bfloat16(v * bf2f(gain[n]));
+      sq += v * v;
+    }
+    sq = warp_sum(sq);
+    if (lane == 0) ss[(size_t)part * M + t] = sq;
+  }
+  if (threadIdx.x == 0) keys[t] = 0ull;
+}
+
+// Page allocation for dflash_fuse_inject (one thread, requests in order, so
+// the page assignment is deterministic).  Grows each slot's page table to
+// cover ctx_len + n_new + block positions, records the first new position
+// (pos0) and the effective row count, and advances ctx_len.
+__global__ void k_page_alloc(const int* slots, int batch, const int* n_new, int rows_per_req, int* ctx_len,
+                             int* pos0, int* n_pages, int* page_table, int mpps, int* free_stack, int* free_top,
+                             int* n_eff, int max_slots, uint32_t* status) {
+  pdl_launch_dependents();
+  pdl_wait();
+  if (threadIdx.x != 0) return;
+  int top = *free_top;
+  for (int b = 0; b < batch; ++b) {
+    const int slot = slots[b];
+    if (slot < 0 || slot >= max_slots) {
+      dev_error(status, DFLASH_DEV_ARG);
+      n_eff[b] = 0;
+      continue;
+    }
+    int n = n_new[b];
+    if (n < 0 || n > rows_per_req) {
+      dev_error(status, DFLASH_DEV_ARG);
+      n = 0;
+    }
+    const int L = ctx_len[slot];
+    int need = (L + n + DFL_BLOCK + DFL_PAGE - 1) / DFL_PAGE;
+    if (need > mpps) {
+      dev_error(status, DFLASH_DEV_CAPACITY);
+      n = 0;
+      need = min(mpps, (L + DFL_BLOCK + DFL_PAGE - 1) / DFL_PAGE);
+    }
+    int np = n_pages[slot];
+    while (np < need) {
+      if (top == 0) {
+        dev_error(status, DFLASH_DEV_CAPACITY);
+        break;
+      }
+      page_table[(size_t)slot * mpps + np] = free_stack[--top];
+      ++np;
+    }
+    if (np * DFL_PAGE < L + n) n = 0;  // no room for the new rows
+    n_pages[slot] = np;
+    pos0[slot] = L;
+    ctx_len[slot] = L + n;
+    n_eff[b] = n;
+  }
+  *free_top = top;
+}
+
+// a7: one warp per request.  Lane i compares draft d_{i+1} with target t_i;
+// the ballot's lowest zero bit is the first mismatch n, so the accepted
+// prefix is the cumulative product of the matches; tau = n + 1, the bonus is
+// t_n, and the confirmed length is ctx_len + tau.
+__global__ void k_accept(const int* slots, int batch, const int* draft, const int* target, int* accept_len,
+                         int* bonus, int* ctx_out, const int* ctx_len, int max_slots, uint32_t* status) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int b = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (b >= batch) return;
+  const bool match = lane < DFL_BLOCK - 1 &&
+                     draft[b * (DFL_BLOCK - 1) + lane] == target[b * DFL_BLOCK + lane];
+  const unsigned m = __ballot_sync(0xffffffffu, match);
+  const int n = __ffs(~m) - 1;  // bits 15.. of m are 0, so n <= 15
+  if (lane == 0) {
+    const int tau = n + 1;
+    const int slot = slots[b];
+    int L = 0;
+    if (slot < 0 || slot >= max_slots)
+      dev_error(status, DFLASH_DEV_ARG);
+    else
+      L = ctx_len[slot];
+    accept_len[b] = tau;
+    bonus[b] = target[b * DFL_BLOCK + n];
+    ctx_out[b] = L + tau;
+  }
+}
+
+__global__ void k_reset_slot(int slot, int* ctx_len, int* n_pages, int* page_table, int mpps, int* free_stack,
+                             int* free_top) {
+  pdl_launch_dependents();
+  pdl_wait();
+  if (threadIdx.x != 0) return;
+  int top = *free_top;
+  const int np = n_pages[slot];
+  for (int i = np - 1; i >= 0; --i) {
+    free_stack[top++] = page_table[(size_t)slot * mpps + i];
+    page_table[(size_t)slot * mpps + i] = -1;
+  }
+  *free_top = top;
+  n_pages[slot] = 0;
+  ctx_len[slot] = 0;
+}
+
+__global__ void k_pool_init(int* free_stack, int* free_top, int max_pages) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < max_pages) free_stack[i] = max_pages - 1 - i;  // pops 0, 1, 2, ...
+  if (i == 0) *free_top = max_pages;
+}
+
+// RoPE angles pos * theta^(-2i/D) evaluated in double precision, stored as
+// float (cos, sin) pairs.
+__global__ void k_rope_table(float2* tab, int max_pos, int D, double theta) {
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const int half = D / 2;
+  if (idx >= (long long)max_pos * half) return;
+  const int pos = (int)(idx / half), i = (int)(idx % half);
+  const double inv = pow(theta, -2.0 * (double)i / (double)D);
+  const double a = (double)pos * inv;
+  tab[idx] = make_float2((float)cos(a), (float)sin(a));
+}
+
+__global__ void k_read_kv(KVGeom kv, int layer, int slot, int pos0, int n, bf16* k_out, bf16* v_out) {
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const int D = kv.D, hkv = kv.hkv;
+  if (idx >= (long long)n * hkv * D) return;
+  const int d = (int)(idx % D);
+  const int h = (int)((idx / D) % hkv);
+  const int t = (int)(idx / ((long long)D * hkv));
+  const int pos = pos0 + t;
+  const int pi = pos >> 6;
+  int pg = pi < kv.max_pages_per_slot ? kv.page_table[(size_t)slot * kv.max_pages_per_slot + pi] : -1;
+  if (pg < 0 || pg >= kv.max_pages) {
+    k_out[idx] = __float2bfloat16(0.f);
+    v_out[idx] = __float2bfloat16(0.f);
+    return;
+  }
+  const size_t blk = (size_t)layer * kv.layer_stride + ((size_t)pg * hkv + h) * (64 * D);
+  k_out[idx] = kv.k_pool[blk + k_swz(pos & 63, d)];
+  v_out[idx] = kv.v_pool[blk + v_swz(d, pos & 63)];
+}
+
+__global__ void k_slot_lengths(const int* slots, int batch, const int* ctx_len, int max_slots, int* out) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= batch) return;
+  const int s = slots[b];
+  out[b] = (s >= 0 && s < max_slots) ? ctx_len[s] : -1;
+}
+
+// Benchmark stand-in for the target's verify (not part of the method).
+// Block 0 builds the target tokens of round (*round_ctr)++; blocks 1.. copy
+// the target features of the 16 block positions from a position-indexed stream.
+__global__ void k_harness_verify(const int* slots, int batch, const int* draft, const int* match, const int* offs,
+                                 int rounds_cap, int* round_ctr, int* target, int vocab,
+                                 const bf16* feat_stream, int stream_rows, bf16* feats_out, int F,
+                                 const int* ctx_len, int max_slots) {
+  pdl_launch_dependents();
+  pdl_wait();
+  if (blockIdx.x == 0) {
+    const int r = *round_ctr;
+    const int rr = r % rounds_cap;
+    for (int idx = threadIdx.x; idx < batch * DFL_BLOCK; idx += blockDim.x) {
+      const int b = idx / DFL_BLOCK, i = idx % DFL_BLOCK;
+      const size_t o = ((size_t)rr * batch + b) * DFL_BLOCK + i;
+      const int u = offs[o];
+      int t;
+      if (i < DFL_BLOCK - 1) {
+        const int d = draft[b * (DFL_BLOCK - 1) + i];
+        t = match[o] ? d : (u == d ? (u + 1) % vocab : u);
+      } else {
+        t = u;
+      }
+      target[idx] = t;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) *round_ctr = r + 1;
+    return;
+  }
+  const int row = blockIdx.x - 1;
+  const int b = row / DFL_BLOCK, i = row % DFL_BLOCK;
+  const int slot = slots[b];
+  if (slot < 0 || slot >= max_slots) return;
+  int pos = ctx_len[slot] + i;
+  if (pos >= stream_rows) pos = stream_rows - 1;
+  const uint4* src = reinterpret_cast<const uint4*>(feat_stream + ((size_t)b * stream_rows + pos) * F);
+  uint4* dst = reinterpret_cast<uint4*>(feats_out + (size_t)row * F);
+  for (int k = threadIdx.x; k < F / 8; k += blockDim.x) dst[k] = src[k];
+}
+
+}  // namespace
+
+cudaError_t launch_embed(const int* slots, int batch, const int* last_tok, int mask_id, const bf16* embed,
+                         const bf16* gain, int H, float* h, bf16* hg, float* ss, unsigned long long* keys,
+                         cudaStream_t s) {
+  cudaLaunchAttribute a[1];
+  const int M = batch * DFL_BLOCK;
+  int threads = (H / 128) * 32;
+  if (threads > 1024) threads = 1024;
+  cudaLaunchConfig_t c = cfg_of(dim3(M), dim3(threads), s, a);
+  return cudaLaunchKernelEx(&c, k_embed, slots, last_tok, mask_id, embed, gain, H, M, h, hg, ss, keys);
+}
+
+cudaError_t launch_page_alloc(const int* slots, int batch, const int* n_new, int rows_per_req, int* ctx_len,
+                              int* pos0, int* n_pages, int* page_table, int mpps, int* free_stack, int* free_top,
+                              int* n_eff, int max_slots, uint32_t* status, cudaStream_t s) {
+  cudaLaunchAttribute a[1];
+  cudaLaunchConfig_t c = cfg_of(dim3(1), dim3(32), s, a);
+  return cudaLaunchKernelEx(&c, k_page_alloc, slots, batch, n_new, rows_per_req, ctx_len, pos0, n_pages,
+                            page_table, mpps, free_stack, free_top, n_eff, max_slots, status);
+}
+
+cudaError_t launch_accept(const int* slots, int batch, const int* draft, const int* target, int* accept_len,
+                          int* bonus, int* ctx_out, int* ctx_len, int max_slots, uint32_t* status,
+                          cudaStream_t s) {
+  cudaLaunchAttribute a[1];
+  cudaLaunchConfig_t c = cfg_of(dim3((batch + 3) / 4), dim3(128), s, a);
+  return cudaLaunchKernelEx(&c, k_accept, slots, batch, draft, target, accept_len, bonus, ctx_out,
+                            (const int*)ctx_len, max_slots, status);
+}
+
+cudaError_t launch_reset_slot(int slot, int* ctx_len, int* n_pages, int* page_table, int mpps, int* free_stack,
+                              int* free_top, cudaStream_t s) {
+  cudaLaunchAttribute a[1];
+  cudaLaunchConfig_t c = cfg_of(dim3(1), dim3(32), s, a);
+  return cudaLaunchKernelEx(&c, k_reset_slot, slot, ctx_len, n_pages, page_table, mpps, free_stack, free_top);
+}
+
+cudaError_t launch_pool_init(int* free_stack, int* free_top, int max_pages, cudaStream_t s) {
+  k_pool_init<<<(max_pages + 255) / 256, 256, 0, s>>>(free_stack, free_top, max_pages);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rope_table(float2* tab, int max_pos, int D, float theta, cudaStream_t s) {
+  const long long n = (long long)max_pos * (D / 2);
+  k_rope_table<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(tab, max_pos, D, (double)theta);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_read_kv(const KVGeom& kv, int layer, int slot, int pos0, int n, bf16* k_out, bf16* v_out,
+                           cudaStream_t s) {
+  const long long tot = (long long)n * kv.hkv * kv.D;
+  if (tot == 0) return cudaSuccess;
+  k_read_kv<<<(unsigned)((tot + 255) / 256), 256, 0, s>>>(kv, layer, slot, pos0, n, k_out, v_out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_slot_lengths(const int* slots, int batch, const int* ctx_len, int max_slots, int* out,
+                                cudaStream_t s) {
+  k_slot_lengths<<<(batch + 127) / 128, 128, 0, s>>>(slots, batch, ctx_len, max_slots, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_harness_verify(const int* slots, int batch, const int* draft, const int* match, const int* offs,
+                                  int rounds_cap, int* round_ctr, int* target, int vocab, const bf16* feat_stream,
+                                  int stream_rows, bf16* feats_out, int F, const int* ctx_len, int max_slots,
+                                  cudaStream_t s) {
+  cudaLaunchAttribute a[1];
+  const int blocks = 1 + (feat_stream ? batch * DFL_BLOCK : 0);
+  cudaLaunchConfig_t c = cfg_of(dim3(blocks), dim3(256), s, a);
+  return cudaLaunchKernelEx(&c, k_harness_verify, slots, batch, draft, match, offs, rounds_cap, round_ctr, target,
+                            vocab, feat_stream, stream_rows, feats_out, F, ctx_len, max_slots);
+}

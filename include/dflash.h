@@ -1,0 +1,235 @@
+/*
+ * dflash.h -- C ABI of libdflash: one DFlash drafting-plus-acceptance round
+ * on one NVIDIA GB300 GPU (sm_103a).
+ *
+ * A round ("DFlash原理深度剖析：块扩散如何用一次前向并行起草整块token", §三 第1-3步):
+ *   dflash_fuse_inject  fuse the hidden states of 5 target layers into one
+ *                       context feature per new position and inject it into
+ *                       every draft layer's paged KV cache;
+ *   dflash_draft_block  one forward of the draft transformer over a 16-token
+ *                       block [last verified token, 15 x mask] -> 15 drafts;
+ *   dflash_accept_trim  given the target's own token per block position,
+ *                       accept the longest matching prefix plus the bonus
+ *                       token and trim the caches to the confirmed length.
+ *
+ * Conventions for every call:
+ *   - Tensors are caller-owned DEVICE memory unless stated otherwise
+ *     (bf16 = IEEE bfloat16, row-major, densely packed).
+ *   - `stream` is a cudaStream_t passed as void*; work is enqueued on it and
+ *     the call returns without synchronising (except where stated), so every
+ *     call is legal inside CUDA stream capture.
+ *   - The return value is a dflash_status.  No exception or abort crosses the
+ *     ABI.  Host-side argument checks return an error and enqueue nothing.
+ *     Device-side checks (slot ids, row counts, page capacity, NaN logits)
+ *     never trap: they set bits in the handle's device status word, skip the
+ *     offending work, and are reported by dflash_read_status.
+ *   - Per-request state lives in "slots" (0 <= slot < max_slots).  A call on
+ *     a batch takes a DEVICE int32 array `slots[batch]` mapping batch row b
+ *     to its slot; a slot must not appear twice in one call.
+ */
+#ifndef DFLASH_H
+#define DFLASH_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DFLASH_API __attribute__((visibility("default")))
+#else
+#define DFLASH_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DFLASH_OK = 0,
+  DFLASH_ERR_INVALID_ARG = 1, /* null pointer, negative size, batch > max_batch */
+  DFLASH_ERR_SHAPE = 2,       /* shape the kernels do not support */
+  DFLASH_ERR_CAPACITY = 3,    /* rows > max_rows, or the page pool is exhausted (device) */
+  DFLASH_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
+  DFLASH_ERR_DEVICE = 5,      /* a device-side check tripped; see dflash_read_status */
+  DFLASH_ERR_WORKSPACE = 6    /* workspace null, too small or not 256-byte aligned */
+} dflash_status;
+
+/* Device status word bits (dflash_read_status). */
+#define DFLASH_DEV_TIMEOUT   0x01u /* a bounded wait inside a kernel gave up */
+#define DFLASH_DEV_NAN       0x02u /* a NaN logit was skipped by the argmax */
+#define DFLASH_DEV_PAGE      0x04u /* a page-table entry was out of range */
+#define DFLASH_DEV_CAPACITY  0x08u /* page pool or per-slot page table full */
+#define DFLASH_DEV_ARG       0x10u /* slot id or n_new out of range */
+
+/* Drafter shape and serving limits.
+ * Supported: head_dim in {64,128}; hidden, n_fused*hidden, intermediate and
+ * n_q_heads*head_dim multiples of 64; n_kv_heads*head_dim a multiple of 128;
+ * hidden a multiple of 128 and <= 8192; n_q_heads a multiple of n_kv_heads
+ * with n_q_heads/n_kv_heads <= 8; block == 16; page_size == 64; n_layers <= 8. */
+typedef struct dflash_config {
+  int32_t hidden;             /* H */
+  int32_t n_q_heads;          /* hq */
+  int32_t n_kv_heads;         /* hkv */
+  int32_t head_dim;           /* D */
+  int32_t intermediate;       /* I (SwiGLU) */
+  int32_t n_layers;           /* draft layers */
+  int32_t vocab;              /* V (tied embedding / lm_head rows) */
+  int32_t n_fused;            /* target layers fused (5) */
+  int32_t block;              /* block size (16): 1 verified token + 15 masks */
+  int32_t mask_id;            /* token id of the mask */
+  int32_t page_size;          /* positions per KV page (64) */
+  int32_t max_batch;          /* max requests per call */
+  int32_t max_slots;          /* request slots */
+  int32_t max_pages;          /* pages in the shared pool */
+  int32_t max_pages_per_slot; /* page-table length per slot */
+  int32_t max_rows;           /* max batch*rows_per_req of one dflash_fuse_inject */
+  int32_t device;             /* CUDA device ordinal */
+  float rms_eps;              /* RMSNorm epsilon (1e-6) */
+  float rope_theta;           /* RoPE base */
+} dflash_config;
+
+/* Device pointers to the drafter weights, all bf16 and row-major; the arrays
+ * of per-layer pointers are HOST arrays of n_layers entries.  The library
+ * keeps the device pointers (not copies): they must stay valid and unchanged
+ * until dflash_destroy. */
+typedef struct dflash_weights {
+  const void* embed;             /* [V, H]  tied embedding and lm_head */
+  const void* fc;                /* [H, n_fused*H] fusion projection (no bias) */
+  const void* fc_norm;           /* [H]     fusion RMSNorm gain */
+  const void* final_norm;        /* [H]     final RMSNorm gain */
+  const void* const* in_norm;    /* [H]     input RMSNorm gain */
+  const void* const* wqkv;       /* [(hq+2*hkv)*D, H] q rows, then k rows, then v rows */
+  const void* const* q_norm;     /* [D]     per-head q RMSNorm gain */
+  const void* const* k_norm;     /* [D]     per-head k RMSNorm gain */
+  const void* const* wo;         /* [H, hq*D] */
+  const void* const* post_norm;  /* [H]     post-attention RMSNorm gain */
+  const void* const* w_gate_up;  /* [2*I, H] gate rows, then up rows */
+  const void* const* w_down;     /* [H, I] */
+} dflash_weights;
+
+typedef struct dflash_handle dflash_handle;
+
+/* Bytes of device workspace dflash_create needs for `cfg` (KV page pool,
+ * page tables, activations, split-K and split-KV scratch, status word).
+ * Returns 0 if cfg is invalid. */
+DFLASH_API size_t dflash_workspace_bytes(const dflash_config* cfg);
+
+/* Create a handle.  `workspace` is caller-allocated device memory of at least
+ * dflash_workspace_bytes(cfg) bytes, 256-byte aligned, owned by the caller
+ * and used exclusively by this handle until dflash_destroy.  Synchronises
+ * the device (initialises the page pool, RoPE table and all slots to empty).
+ * Not legal inside stream capture. */
+DFLASH_API int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* workspace,
+                  size_t workspace_bytes, dflash_handle** out);
+DFLASH_API int dflash_destroy(dflash_handle* h);
+
+/* a1 + a2.  Feature fusion ("DFlash：drafter 的答案，早写在 target model 的隐层里",
+ * 设计 — Feature Fusion: five target layers shallow->deep, concatenated, one
+ * projection, RMSNorm) and KV injection (same page, 设计 — KV Injection: the
+ * fused feature is projected by every draft layer's own K/V projections,
+ * k-normed, rotated at its context positions and kept across rounds).
+ *   feats  [batch, rows_per_req, n_fused, H] bf16; request b's new rows are
+ *          its first n_new[b] rows (position order).
+ *   n_new  DEVICE int32 [batch], 0 <= n_new[b] <= rows_per_req; rows are
+ *          appended at positions ctx_len .. ctx_len+n_new-1 of the slot.
+ * Prefill is one call with rows_per_req = prompt length.  In a round,
+ * n_new is the previous round's accept_len (the same device buffer), which
+ * keeps a captured round loop free of host reads.  Requires
+ * batch*rows_per_req <= max_rows. */
+DFLASH_API int dflash_fuse_inject(dflash_handle* h, const int32_t* slots, int32_t batch, const void* feats,
+                       int32_t rows_per_req, const int32_t* n_new, void* stream);
+
+/* a3-a6.  Embed the block [last_tok[b], mask x 15] at positions
+ * ctx_len .. ctx_len+15, run every draft layer once with non-causal
+ * attention over [context KV ; block KV] ("DFlash原理深度剖析…", §二.1, §二.2),
+ * apply the final RMSNorm and the tied lm_head, and write the argmax of
+ * block rows 1..15 (ties -> lowest id; logits are never stored).
+ *   last_tok DEVICE int32 [batch]; draft DEVICE int32 [batch, 15] (out). */
+DFLASH_API int dflash_draft_block(dflash_handle* h, const int32_t* slots, int32_t batch,
+                       const int32_t* last_tok, int32_t* draft, void* stream);
+
+/* a7.  Longest-prefix acceptance (cumulative product of matches,
+ * "DFlash原理深度剖析…", §三 第3步).  draft [batch,15], target [batch,16] (the
+ * target's token after each block position).  Outputs (DEVICE int32 [batch]):
+ *   accept_len = accepted drafts + 1, in [1, 16];
+ *   bonus      = target[b][accept_len-1] (the next round's last verified token);
+ *   ctx_len    = confirmed length = ctx_len_before_round + accept_len, the length
+ *                both the draft and the target caches are trimmed to.
+ * The draft cache never keeps block K/V, so trimming it only clamps the
+ * slot's length to the confirmed one; the accept_len new features are
+ * appended by the next dflash_fuse_inject. */
+DFLASH_API int dflash_accept_trim(dflash_handle* h, const int32_t* slots, int32_t batch, const int32_t* draft,
+                       const int32_t* target, int32_t* accept_len, int32_t* bonus,
+                       int32_t* ctx_len, void* stream);
+
+/* Free a slot's pages and set its length to 0 (stream-ordered). */
+DFLASH_API int dflash_reset_slot(dflash_handle* h, int32_t slot, void* stream);
+
+/* Synchronise the device, return the device status word in *out
+ * (DFLASH_DEV_* bits, 0 = clean) and clear it. */
+DFLASH_API int dflash_read_status(dflash_handle* h, uint32_t* out);
+
+DFLASH_API const char* dflash_status_string(int status);
+
+/* ---- round graph: one CUDA graph per captured sequence of calls ---------
+ * dflash_graph_begin starts capturing `stream` (thread-local mode); every
+ * call enqueued on it until dflash_graph_end (library calls and the caller's
+ * own kernels, e.g. the target's verify) becomes one graph, instantiated and
+ * kept in the handle (replacing any previous one).  *n_kernels receives the
+ * number of kernel nodes.  dflash_graph_launch replays it on `stream`. */
+DFLASH_API int dflash_graph_begin(dflash_handle* h, void* stream);
+DFLASH_API int dflash_graph_end(dflash_handle* h, void* stream, int32_t* n_kernels);
+DFLASH_API int dflash_graph_launch(dflash_handle* h, void* stream);
+
+/* ---- introspection ------------------------------------------------------ */
+
+/* Copy K and V of `layer` for positions pos0..pos0+n-1 of `slot` into plain
+ * [n, hkv, D] bf16 DEVICE buffers (the cache itself is stored pre-swizzled). */
+DFLASH_API int dflash_read_kv(dflash_handle* h, int32_t layer, int32_t slot, int32_t pos0, int32_t n,
+                   void* k_out, void* v_out, void* stream);
+
+/* Current cache length of each slot in slots[batch] -> DEVICE int32 out[batch]. */
+DFLASH_API int dflash_slot_lengths(dflash_handle* h, const int32_t* slots, int32_t batch, int32_t* out,
+                        void* stream);
+
+/* dflash_draft_block that also writes, when non-null, the residual stream
+ * after the last layer (hidden [batch,16,H] float32) and the full logits of
+ * all 16 block rows (logits [batch,16,V] float32), from the same kernels and
+ * the same accumulators the argmax reads. */
+DFLASH_API int dflash_draft_block_debug(dflash_handle* h, const int32_t* slots, int32_t batch,
+                             const int32_t* last_tok, int32_t* draft, float* hidden,
+                             float* logits, void* stream);
+
+/* Kernel timing probe: the next n launches of kernel `kernel_id`
+ * (DFLASH_KID_*) are bracketed by CUDA events recorded on the launching
+ * stream (as event-record nodes when captured).  dflash_probe_read
+ * synchronises on them and writes up to `cap` durations in ms. */
+#define DFLASH_KID_LM_HEAD 1
+#define DFLASH_KID_GATE_UP 2
+#define DFLASH_KID_ATTENTION 3
+#define DFLASH_KID_DOWN 4
+#define DFLASH_KID_QKV 5
+DFLASH_API int dflash_probe_arm(dflash_handle* h, int32_t kernel_id, int32_t n);
+DFLASH_API int dflash_probe_read(dflash_handle* h, float* ms_out, int32_t cap, int32_t* n_out);
+
+/* Number of kernels this handle has launched (or captured) so far. */
+DFLASH_API uint64_t dflash_launch_count(dflash_handle* h);
+
+/* ---- benchmark harness: stand-in for the target's verify step -----------
+ * Not part of the method.  For round r = (*round_ctr)++ it builds the
+ * target tokens from the draft and caller-drawn random streams
+ *   match [rounds_cap, batch, 16] int32 in {0,1}, offs [rounds_cap, batch, 16]
+ *   int32 in [0, vocab):  t_i = d_{i+1} if match_i else offs_i (bumped to
+ *   (offs_i+1) mod vocab if equal to d_{i+1}), t_15 = offs_15;
+ * and, when feat_stream is non-null, copies the target features of the 16
+ * block positions ctx_len .. ctx_len+15 from feat_stream
+ * [batch, stream_rows, n_fused*H] into feats_out [batch, 16, n_fused*H]. */
+DFLASH_API int dflash_harness_verify(dflash_handle* h, const int32_t* slots, int32_t batch,
+                          const int32_t* draft, const int32_t* match, const int32_t* offs,
+                          int32_t rounds_cap, int32_t* round_ctr, int32_t* target,
+                          const void* feat_stream, int32_t stream_rows, void* feats_out,
+                          void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DFLASH_H */

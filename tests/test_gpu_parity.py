@@ -1,0 +1,210 @@
+"""CUDA path vs the CPU oracle, element by element, through the C ABI."""
+import numpy as np
+import pytest
+
+import oracle as O
+from tests.gpu_util import GpuRun, OracleRun, TOL_REL_L2, check_drafts, rel_l2, to_np
+from workload import get_config, make_weights
+
+pytestmark = pytest.mark.gpu
+
+SMALL = ["tiny", "tiny-gains", "small", "small-batch"]
+
+
+def _pair(name, rounds, **kw):
+    cfg = get_config(name)
+    w = make_weights(cfg)
+    g = GpuRun(cfg, rounds, weights_np=w, **kw)
+    o = OracleRun(cfg, rounds, weights_np=w, **kw)
+    g.prefill()
+    o.prefill()
+    return cfg, g, o
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_inject_kv_matches_oracle(lib, name):
+    cfg, g, o = _pair(name, 1)
+    for j in range(len(g.ids)):
+        L = int(g.ctx0[j])
+        for l in range(cfg.n_layers):
+            k, v = g.d.read_kv(l, j, 0, L)
+            ok, ov = o.reqs[j].ctx(l)
+            assert rel_l2(to_np(k), ok) < TOL_REL_L2, (name, j, l)
+            assert rel_l2(to_np(v), ov) < TOL_REL_L2, (name, j, l)
+            # every position, not just the aggregate
+            kk = to_np(k).reshape(L, -1)
+            err = np.linalg.norm(kk - ok.reshape(L, -1), axis=1) / np.linalg.norm(ok.reshape(L, -1), axis=1)
+            assert err.max() < 3 * TOL_REL_L2
+    assert g.d.read_status() == 0
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_draft_round_matches_oracle(lib, name):
+    cfg, g, o = _pair(name, 2)
+    for r in range(2):
+        go = g.round(debug=True)
+        oo = o.round(want_logits=True)
+        for j, od in enumerate(oo):
+            # hidden states after the last layer (all 16 block rows)
+            assert rel_l2(go["hidden"][j], od["hidden"]) < TOL_REL_L2
+            # logits of rows 1..15
+            assert rel_l2(go["logits"][j, 1:], od["logits"]) < TOL_REL_L2
+            # fused argmax == argmax of the same kernel's materialised logits
+            assert np.array_equal(go["draft"][j], np.argmax(go["logits"][j, 1:], -1))
+            check_drafts(go["draft"][j], od)
+            assert go["tau"][j] == od["tau"]
+            assert go["ctx"][j] == od["ctx"]
+            assert go["bonus"][j] == od["bonus"]
+    assert g.d.read_status() == 0
+
+
+@pytest.mark.parametrize("name,rounds", [("tiny", 8), ("small-batch", 4)])
+def test_rounds_accept_bit_exact(lib, name, rounds):
+    cfg, g, o = _pair(name, rounds)
+    for r in range(rounds):
+        go = g.round()
+        oo = o.round(want_logits=False)
+        for j, od in enumerate(oo):
+            assert 1 <= go["tau"][j] <= 16
+            assert (go["tau"][j], go["bonus"][j], go["ctx"][j]) == (od["tau"], od["bonus"], od["ctx"]), (r, j)
+            check_drafts(go["draft"][j], od)
+    lens = to_np(g.d.slot_lengths(g.state.slots))
+    # the last round's accepted features are injected by the next round
+    assert np.array_equal(lens + to_np(g.state.accept_len), [od["ctx"] for od in oo])
+
+
+def test_context_kv_unchanged_by_later_rounds(lib):
+    cfg, g, o = _pair("small", 4)
+    L = int(g.ctx0[0])
+    before = [tuple(to_np(t).copy() for t in g.d.read_kv(l, 0, 0, L)) for l in range(cfg.n_layers)]
+    for _ in range(4):
+        g.round()
+    for l in range(cfg.n_layers):
+        k, v = g.d.read_kv(l, 0, 0, L)
+        assert np.array_equal(to_np(k), before[l][0]) and np.array_equal(to_np(v), before[l][1])
+
+
+def test_graph_replay_equals_eager(lib):
+    import torch
+    from block_diffusion_speculative_hiddens_gb300.session import run_round
+    cfg = get_config("small-batch")
+    w = make_weights(cfg)
+    a = GpuRun(cfg, 4, weights_np=w)
+    b = GpuRun(cfg, 4, weights_np=w)
+    a.prefill()
+    b.prefill()
+    st = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(st):
+        b.d.graph_begin(st)
+        run_round(b.state, b.verify, st)
+        nk = b.d.graph_end(st)
+    assert nk >= 5
+    for _ in range(4):
+        ea = a.round()
+        with torch.cuda.stream(st):
+            b.d.graph_launch(st)
+        st.synchronize()
+        s = b.state
+        for key, t in (("draft", s.draft), ("tau", s.accept_len), ("bonus", s.bonus), ("ctx", s.ctx_len)):
+            assert np.array_equal(ea[key], to_np(t).astype(np.int64)), key
+
+
+def test_batch_invariance(lib):
+    """Each request of a batch behaves as the same request run alone.
+
+    Accept lengths and lengths are bit-exact; drafts follow the margin rule
+    against the oracle (the split-KV count depends on the batch size, so the
+    attention's summation order may differ between the two runs)."""
+    cfg = get_config("small-batch")
+    w = make_weights(cfg)
+    full = GpuRun(cfg, 3, weights_np=w)
+    full.prefill()
+    orc = OracleRun(cfg, 3, weights_np=w)
+    orc.prefill()
+    res_full = [full.round() for _ in range(3)]
+    res_orc = [orc.round(want_logits=False) for _ in range(3)]
+    for b in range(cfg.batch):
+        one = GpuRun(cfg, 3, weights_np=w, batch_ids=[b])
+        one.prefill()
+        for r in range(3):
+            ro = one.round()
+            assert ro["tau"][0] == res_full[r]["tau"][b] == res_orc[r][b]["tau"]
+            assert ro["ctx"][0] == res_full[r]["ctx"][b] == res_orc[r][b]["ctx"]
+            check_drafts(ro["draft"][0], res_orc[r][b])
+            check_drafts(res_full[r]["draft"][b], res_orc[r][b])
+
+
+def test_accept_trim_exhaustive_patterns(lib):
+    import torch
+    from block_diffusion_speculative_hiddens_gb300 import Drafter, weights_to_device
+    cfg = get_config("tiny")
+    d = Drafter(cfg, weights_to_device(make_weights(cfg)), max_batch=64, max_slots=64, max_pages=64,
+                max_pages_per_slot=1, max_rows=64)
+    rng = np.random.default_rng(5)
+    for rep in range(40):
+        B = 64 if rep % 2 else int(rng.integers(1, 65))
+        draft = rng.integers(0, 7, (B, 15)).astype(np.int32)
+        target = rng.integers(0, 7, (B, 16)).astype(np.int32)
+        # force structured patterns: all right, all wrong, single mismatch at k
+        for b in range(B):
+            kind = (rep * 64 + b) % 18
+            if kind == 0:
+                target[b, :15] = draft[b]
+            elif kind == 1:
+                target[b, :15] = draft[b] + 1
+            elif kind < 17:
+                target[b, :15] = draft[b]
+                target[b, kind - 2] = draft[b, kind - 2] + 1 if kind - 2 < 15 else target[b, 14]
+        dev = torch.device("cuda:0")
+        T = lambda a: torch.from_numpy(a).to(dev)
+        slots = torch.arange(B, dtype=torch.int32, device=dev)
+        acc = torch.zeros(B, dtype=torch.int32, device=dev)
+        bon = torch.zeros_like(acc)
+        ctx = torch.zeros_like(acc)
+        d.accept_trim(slots, T(draft), T(target), acc, bon, ctx)
+        acc, bon, ctx = to_np(acc), to_np(bon), to_np(ctx)
+        for b in range(B):
+            tau, bonus = O.accept_longest_prefix(draft[b], target[b])
+            assert (acc[b], bon[b], ctx[b]) == (tau, bonus, tau)
+    assert d.read_status() == 0
+
+
+def test_edge_cases_and_errors(lib):
+    import torch
+    from block_diffusion_speculative_hiddens_gb300 import Drafter, weights_to_device
+    from block_diffusion_speculative_hiddens_gb300.binding import DflashError, DEV_ARG
+    cfg = get_config("tiny")
+    d = Drafter(cfg, weights_to_device(make_weights(cfg)), max_batch=2, max_slots=2, max_pages=8,
+                max_pages_per_slot=4, max_rows=64)
+    dev = torch.device("cuda:0")
+    i32 = dict(dtype=torch.int32, device=dev)
+    empty = torch.zeros(0, **i32)
+    d.draft_block(empty, empty, torch.zeros(0, 15, **i32))       # batch 0: no-op
+    d.fuse_inject(empty, None, 0, empty)
+    with pytest.raises(DflashError) as e:                         # batch > max_batch
+        s3 = torch.arange(3, **i32)
+        d.draft_block(s3, s3, torch.zeros(3, 15, **i32))
+    assert e.value.code == 1
+    with pytest.raises(DflashError) as e:                         # rows > max_rows
+        d.fuse_inject(torch.arange(2, **i32), torch.zeros(2, 40, cfg.fused_dim, dtype=torch.bfloat16,
+                                                          device=dev), 40, torch.zeros(2, **i32))
+    assert e.value.code == 3
+    # n_new beyond rows_per_req and an out-of-range slot are device-side errors, not faults
+    feats = torch.zeros(1, 8, cfg.fused_dim, dtype=torch.bfloat16, device=dev)
+    d.fuse_inject(torch.tensor([0], **i32), feats, 8, torch.tensor([9], **i32))
+    assert d.read_status() & DEV_ARG
+    d.fuse_inject(torch.tensor([5], **i32), feats, 8, torch.tensor([1], **i32))
+    assert d.read_status() & DEV_ARG
+    assert d.read_status() == 0                                   # cleared by the read
+    # page capacity: 4 pages of 64 positions per slot
+    big = torch.zeros(1, 64, cfg.fused_dim, dtype=torch.bfloat16, device=dev)
+    for _ in range(4):
+        d.fuse_inject(torch.tensor([1], **i32), big, 64, torch.tensor([64], **i32))
+    st = d.read_status()
+    assert st & 0x08  # DEV_CAPACITY: 256 positions + a 16-token block do not fit in 4 pages
+    lens = to_np(d.slot_lengths(torch.tensor([0, 1], **i32)))
+    assert lens[1] == 192  # the 4th chunk was refused, earlier ones kept
+    d.reset_slot(1)
+    assert to_np(d.slot_lengths(torch.tensor([1], **i32)))[0] == 0
+    assert d.read_status() == 0
