@@ -303,9 +303,9 @@ int ensure_bmaps(dflash_handle* h, int M) {
 
 int draft_impl(dflash_handle* h, const int32_t* slots, int32_t batch, const int32_t* last_tok, int32_t* draft,
                float* hidden, float* logits, void* stream) {
-  if (!h || !slots || !last_tok || !draft) return DFLASH_ERR_INVALID_ARG;
-  if (batch < 0 || batch > h->cfg.max_batch) return DFLASH_ERR_INVALID_ARG;
+  if (!h || batch < 0 || batch > h->cfg.max_batch) return DFLASH_ERR_INVALID_ARG;
   if (batch == 0) return DFLASH_OK;
+  if (!slots || !last_tok || !draft) return DFLASH_ERR_INVALID_ARG;
   if (cudaSetDevice(h->cfg.device) != cudaSuccess) return DFLASH_ERR_CUDA;
   cudaStream_t s = (cudaStream_t)stream;
   const dflash_config& c = h->cfg;
@@ -503,10 +503,10 @@ int dflash_destroy(dflash_handle* h) {
 
 int dflash_fuse_inject(dflash_handle* h, const int32_t* slots, int32_t batch, const void* feats,
                        int32_t rows_per_req, const int32_t* n_new, void* stream) {
-  if (!h || !slots || !n_new) return DFLASH_ERR_INVALID_ARG;
-  if (batch < 0 || batch > h->cfg.max_batch || rows_per_req < 0) return DFLASH_ERR_INVALID_ARG;
+  if (!h || batch < 0 || batch > h->cfg.max_batch || rows_per_req < 0) return DFLASH_ERR_INVALID_ARG;
   if ((long long)batch * rows_per_req > h->cfg.max_rows) return DFLASH_ERR_CAPACITY;
   if (batch == 0) return DFLASH_OK;
+  if (!slots || !n_new) return DFLASH_ERR_INVALID_ARG;
   if (rows_per_req > 0 && !feats) return DFLASH_ERR_INVALID_ARG;
   if (cudaSetDevice(h->cfg.device) != cudaSuccess) return DFLASH_ERR_CUDA;
   cudaStream_t s = (cudaStream_t)stream;
@@ -566,9 +566,9 @@ int dflash_draft_block_debug(dflash_handle* h, const int32_t* slots, int32_t bat
 int dflash_accept_trim(dflash_handle* h, const int32_t* slots, int32_t batch, const int32_t* draft,
                        const int32_t* target, int32_t* accept_len, int32_t* bonus, int32_t* ctx_len,
                        void* stream) {
-  if (!h || !slots || !draft || !target || !accept_len || !bonus || !ctx_len) return DFLASH_ERR_INVALID_ARG;
-  if (batch < 0 || batch > h->cfg.max_batch) return DFLASH_ERR_INVALID_ARG;
+  if (!h || batch < 0 || batch > h->cfg.max_batch) return DFLASH_ERR_INVALID_ARG;
   if (batch == 0) return DFLASH_OK;
+  if (!slots || !draft || !target || !accept_len || !bonus || !ctx_len) return DFLASH_ERR_INVALID_ARG;
   if (cudaSetDevice(h->cfg.device) != cudaSuccess) return DFLASH_ERR_CUDA;
   h->launches++;
   return cuda_err(launch_accept(slots, batch, draft, target, accept_len, bonus, ctx_len, h->ctx_len,
@@ -615,6 +615,7 @@ int dflash_graph_end(dflash_handle* h, void* stream, int32_t* n_kernels) {
   }
   cudaGraphExec_t e = nullptr;
   if (!rc) rc = cuda_err(cudaGraphInstantiate(&e, g, 0));
+  if (!rc) rc = cuda_err(cudaGraphUpload(e, (cudaStream_t)stream));
   if (rc) {
     if (g) cudaGraphDestroy(g);
     return rc;
@@ -643,8 +644,9 @@ int dflash_read_kv(dflash_handle* h, int32_t layer, int32_t slot, int32_t pos0, 
 }
 
 int dflash_slot_lengths(dflash_handle* h, const int32_t* slots, int32_t batch, int32_t* out, void* stream) {
-  if (!h || !slots || !out || batch < 0) return DFLASH_ERR_INVALID_ARG;
+  if (!h || batch < 0) return DFLASH_ERR_INVALID_ARG;
   if (batch == 0) return DFLASH_OK;
+  if (!slots || !out) return DFLASH_ERR_INVALID_ARG;
   if (cudaSetDevice(h->cfg.device) != cudaSuccess) return DFLASH_ERR_CUDA;
   return cuda_err(launch_slot_lengths(slots, batch, h->ctx_len, h->cfg.max_slots, out, (cudaStream_t)stream));
 }
@@ -683,12 +685,12 @@ int dflash_harness_verify(dflash_handle* h, const int32_t* slots, int32_t batch,
                           const int32_t* match, const int32_t* offs, int32_t rounds_cap, int32_t* round_ctr,
                           int32_t* target, const void* feat_stream, int32_t stream_rows, void* feats_out,
                           void* stream) {
-  if (!h || !slots || !draft || !match || !offs || !round_ctr || !target || rounds_cap <= 0) {
+  if (!h || batch < 0 || batch > h->cfg.max_batch) return DFLASH_ERR_INVALID_ARG;
+  if (batch == 0) return DFLASH_OK;
+  if (!slots || !draft || !match || !offs || !round_ctr || !target || rounds_cap <= 0) {
     return DFLASH_ERR_INVALID_ARG;
   }
-  if (batch < 0 || batch > h->cfg.max_batch) return DFLASH_ERR_INVALID_ARG;
   if (feat_stream && (!feats_out || stream_rows <= 0)) return DFLASH_ERR_INVALID_ARG;
-  if (batch == 0) return DFLASH_OK;
   if (cudaSetDevice(h->cfg.device) != cudaSuccess) return DFLASH_ERR_CUDA;
   h->launches++;
   return cuda_err(launch_harness_verify(slots, batch, draft, match, offs, rounds_cap, round_ctr, target,

@@ -54,9 +54,10 @@ class GpuRun:
         self.dev = dev
         # feature stream: every position a request can reach
         F = cfg.fused_dim
-        fs = np.empty((B, cap, F), dtype=np.uint16)
+        fs = np.zeros((B, cap, F), dtype=np.uint16)
         for j, b in enumerate(self.ids):
-            fs[j] = feature_rows(cfg, b, 0, cap).reshape(cap, F)
+            n = min(cap, int(self.ctx0[j]) + cfg.block * (rounds + 2))
+            fs[j, :n] = feature_rows(cfg, b, 0, n).reshape(n, F)
         self.feat_stream = torch.from_numpy(fs.view(np.int16)).view(torch.bfloat16).to(dev)
         m = np.empty((max(rounds, 1), B, cfg.block), dtype=np.int32)
         u = np.empty_like(m)

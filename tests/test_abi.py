@@ -57,6 +57,7 @@ def test_null_arguments_rejected_without_device(lib):
     # host-side checks return before any CUDA call
     assert lib.dflash_destroy(None) == 1
     assert lib.dflash_draft_block(None, None, 1, None, None, None) == 1
+    assert lib.dflash_draft_block(None, None, 0, None, None, None) == 1
     assert lib.dflash_fuse_inject(None, None, 1, None, 16, None, None) == 1
     assert lib.dflash_accept_trim(None, None, 1, None, None, None, None, None, None) == 1
     assert lib.dflash_launch_count(None) == 0

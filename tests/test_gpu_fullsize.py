@@ -1,0 +1,82 @@
+"""Full-size workloads on the GPU against the oracle.
+
+The Qwen3-8B-shaped batch-1 workload runs in the launch configuration the
+benchmark times (batch 1, one slot, 16-row GEMMs); the oracle computes the
+whole round.  For the batched and long-context workloads the oracle checks a
+sample of requests (each request's round depends only on its own context).
+"""
+import numpy as np
+import pytest
+
+from tests.gpu_util import GpuRun, OracleRun, TOL_REL_L2, check_drafts, rel_l2, to_np
+from workload import get_config, make_weights
+
+pytestmark = pytest.mark.gpu
+
+
+def _check_round(go, oo, ids):
+    for j, od in zip(ids, oo):
+        assert rel_l2(go["hidden"][j], od["hidden"]) < TOL_REL_L2
+        assert rel_l2(go["logits"][j, 1:], od["logits"]) < TOL_REL_L2
+        assert np.array_equal(go["draft"][j], np.argmax(go["logits"][j, 1:], -1))
+        check_drafts(go["draft"][j], od)
+        assert (go["tau"][j], go["bonus"][j], go["ctx"][j]) == (od["tau"], od["bonus"], od["ctx"])
+
+
+def _check_kv(g, o, j_gpu, j_orc, positions, layers):
+    for l in layers:
+        for p in positions:
+            k, v = g.d.read_kv(l, j_gpu, int(p), 1)
+            assert rel_l2(to_np(k)[0], o.reqs[j_orc].K[l][p]) < TOL_REL_L2, (l, p)
+            assert rel_l2(to_np(v)[0], o.reqs[j_orc].V[l][p]) < TOL_REL_L2, (l, p)
+
+
+@pytest.mark.parametrize("name", ["qwen3-8b", "llama3.1-8b"])
+def test_batch1_workload_rounds_match_oracle(lib, name):
+    cfg = get_config(name)
+    w = make_weights(cfg)
+    g = GpuRun(cfg, 2, weights_np=w, prefill_chunk=2048)
+    g.prefill()
+    o = OracleRun(cfg, 2, weights_np=w, cache=False)
+    o.prefill()
+    L = cfg.ctx0
+    _check_kv(g, o, 0, 0, [0, 1, 63, 64, L // 2 + 5, L - 1], range(cfg.n_layers))
+    for r in range(2):
+        go = g.round(debug=True)
+        oo = o.round(want_logits=True)
+        _check_round(go, oo, [0])
+    assert g.d.read_status() == 0
+
+
+def test_batched_workload_sampled_requests(lib):
+    cfg = get_config("batched-qwen3-8b")
+    w = make_weights(cfg)
+    g = GpuRun(cfg, 2, weights_np=w, prefill_chunk=4096)
+    g.prefill()
+    sample = [0, 17, 63]
+    o = OracleRun(cfg, 2, weights_np=w, batch_ids=sample, cache=False)
+    o.prefill()
+    for jo, b in enumerate(sample):
+        L = int(g.ctx0[b])
+        _check_kv(g, o, b, jo, [0, L - 1], [0, cfg.n_layers - 1])
+    for r in range(2):
+        go = g.round(debug=True)
+        oo = o.round(want_logits=True)
+        _check_round(go, oo, sample)
+        # every request: tau in range, confirmed length advanced by tau
+        assert np.all((go["tau"] >= 1) & (go["tau"] <= 16))
+    assert g.d.read_status() == 0
+
+
+def test_long_context_workload_sampled_request(lib):
+    cfg = get_config("long-8layer")
+    w = make_weights(cfg)
+    g = GpuRun(cfg, 1, weights_np=w, prefill_chunk=4096)
+    g.prefill()
+    o = OracleRun(cfg, 1, weights_np=w, batch_ids=[2], cache=False)
+    o.prefill()
+    _check_kv(g, o, 2, 0, [0, 4095, 4096, 32767], [0, 7])
+    go = g.round(debug=True)
+    oo = o.round(want_logits=True)
+    _check_round(go, oo, [2])
+    assert g.d.read_status() == 0

@@ -405,3 +405,16 @@ def test_round_tau_independent_of_drafts():
         while lead < 15 and mm[0][lead]:
             lead += 1
         assert tau == lead + 1
+
+
+@pytest.mark.parametrize("name", ["tiny-gains", "small", "small-batch"])
+def test_test_shapes_draft_diverse_ids(name):
+    """The parity test shapes must draft varied ids (not one dominant token),
+    otherwise the token comparisons would check little."""
+    from tests.gpu_util import OracleRun
+    cfg = get_config(name)
+    o = OracleRun(cfg, 2)
+    o.prefill()
+    for _ in range(2):
+        for od in o.round(want_logits=False):
+            assert len(set(od["draft"].tolist())) >= 2

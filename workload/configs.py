@@ -89,8 +89,11 @@ CONFIGS = {
 
 # Small shapes for parity tests: several tiles per GEMM, ragged vocabulary
 # tail, ragged pages, GQA group 4 and 8, head_dim 64 and 128, random gains.
+# Projections at std 0.05 keep the layers' outputs larger than the tied
+# embedding row, so the argmax is not dominated by the mask token's own row
+# and the drafted ids are diverse.
 TEST_CONFIGS = {
-    "tiny-gains": CONFIGS["tiny"].with_(name="tiny-gains", gain_std=0.1),
+    "tiny-gains": CONFIGS["tiny"].with_(name="tiny-gains", gain_std=0.1, weight_std=0.05),
     "small": DraftConfig(
         name="small", hidden=512, n_q_heads=8, n_kv_heads=2, head_dim=128, intermediate=1024,
         n_layers=2, vocab=8000, rope_theta=1e6, batch=1, ctx0=200, rounds=4, match_p=0.85,
@@ -98,7 +101,8 @@ TEST_CONFIGS = {
     "small-batch": DraftConfig(
         name="small-batch", hidden=512, n_q_heads=8, n_kv_heads=1, head_dim=128,
         intermediate=768, n_layers=2, vocab=5000, rope_theta=5e5, batch=3, ctx0=None,
-        rounds=4, match_p=None, ctx_range=(30, 300), p_range=(0.5, 0.95), gain_std=0.1),
+        rounds=4, match_p=None, ctx_range=(30, 300), p_range=(0.5, 0.95), gain_std=0.1,
+        weight_std=0.05),
 }
 
 

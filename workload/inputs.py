@@ -12,6 +12,8 @@ per-request context lengths and match probabilities 3.
 """
 from __future__ import annotations
 
+import os
+
 import numpy as np
 
 from .gen import normal_bf16, stream_key, uniform
@@ -51,16 +53,38 @@ def _tensor(cfg, name, layer=None):
     return normal_bf16(key, 0, n, scale=cfg.weight_std).reshape(shape)
 
 
+def _arch_key(cfg) -> str:
+    fields = (cfg.hidden, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, cfg.intermediate,
+              cfg.n_layers, cfg.vocab, cfg.n_fused, cfg.weight_std, cfg.gain_std, cfg.seed, "v1")
+    return "w_" + "_".join(str(f) for f in fields)
+
+
 def make_weights(cfg):
-    """All drafter weights as bf16 bit patterns (numpy uint16).
+    """All drafter weights as bf16 bit patterns (numpy uint16), cached on disk
+    under $DFLASH_WORKLOAD_CACHE when that variable is set.
 
     Returns {"embed", "fc", "fc_norm", "final_norm", "layers": [ {per-layer} ]}.
     Layer tensors: wqkv [(hq+2hkv)*D, H] (q rows, then k rows, then v rows),
     wo [H, hq*D], w_gate_up [2I, H] (gate rows then up rows), w_down [H, I],
     in_norm/post_norm [H], q_norm/k_norm [D].
     """
-    w = {k: _tensor(cfg, k) for k in _GLOBAL_IDS}
-    w["layers"] = [{k: _tensor(cfg, k, l) for k in _LAYER_IDS} for l in range(cfg.n_layers)]
+    cache = os.environ.get("DFLASH_WORKLOAD_CACHE")
+    path = os.path.join(cache, _arch_key(cfg)) if cache else None
+
+    def get(name, layer=None):
+        if path is None:
+            return _tensor(cfg, name, layer)
+        f = os.path.join(path, name if layer is None else f"{name}.{layer}") + ".npy"
+        if os.path.exists(f):
+            return np.load(f, mmap_mode="r")
+        a = _tensor(cfg, name, layer)
+        os.makedirs(path, exist_ok=True)
+        np.save(f + ".tmp.npy", a)
+        os.replace(f + ".tmp.npy", f)
+        return a
+
+    w = {k: get(k) for k in _GLOBAL_IDS}
+    w["layers"] = [{k: get(k, l) for k in _LAYER_IDS} for l in range(cfg.n_layers)]
     return w
 
 
