@@ -19,7 +19,7 @@ HEADER = os.path.join(os.path.dirname(PKG), "include", "dflash.h")
 OK = 0
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported shape", 3: "capacity exceeded",
           4: "CUDA error", 5: "device-side check failed", 6: "workspace too small or misaligned"}
-DEV_TIMEOUT, DEV_NAN, DEV_PAGE, DEV_CAPACITY, DEV_ARG = 0x01, 0x02, 0x04, 0x08, 0x10
+DEV_TIMEOUT, DEV_NAN, DEV_PAGE, DEV_CAPACITY, DEV_ARG, DEV_RANGE = 0x01, 0x02, 0x04, 0x08, 0x10, 0x20
 KID_LM_HEAD, KID_GATE_UP, KID_ATTENTION, KID_DOWN, KID_QKV = 1, 2, 3, 4, 5
 
 _c_int_p = ctypes.POINTER(ctypes.c_int32)
@@ -117,7 +117,8 @@ class Drafter:
     """One libdflash handle: drafter weights (device), workspace and slots.
 
     `weights` follows workload.make_weights' layout with torch bf16 device
-    tensors; the handle keeps them referenced for its lifetime.
+    tensors.  dflash_create copies them into the handle's workspace, so the
+    caller may drop them afterwards.
     """
 
     def __init__(self, cfg, weights: dict, *, max_batch: int, max_slots: int, max_pages: int,
@@ -200,7 +201,7 @@ class Drafter:
     def read_kv(self, layer: int, slot: int, pos0: int, n: int, stream=None):
         import torch
         shape = (n, self.cfg.n_kv_heads, self.cfg.head_dim)
-        k = torch.empty(shape, dtype=torch.bfloat16, device=f"cuda:{self.device}")
+        k = torch.empty(shape, dtype=torch.float32, device=f"cuda:{self.device}")
         v = torch.empty_like(k)
         _check("dflash_read_kv", self.lib.dflash_read_kv(self.h, layer, slot, pos0, n, _ptr(k), _ptr(v),
                                                          _stream(stream)))

@@ -33,15 +33,17 @@ bool load_encode() {
   return g_encode != nullptr;
 }
 
-// 2-D bf16 tensor [rows, cols] row-major; box = 64 columns (128 B) x box_rows,
-// 128-byte swizzle -- the canonical K-major tcgen05 operand layout.
-bool make_tmap(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+// 2-D 16-bit tensor [rows, cols] row-major (f16 or bf16); box = 64 columns
+// (128 B) x box_rows, 128-byte swizzle -- the canonical K-major tcgen05
+// operand layout.
+bool make_tmap(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+               bool is_bf16 = false) {
   if (!load_encode()) return false;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * 2};
   cuuint32_t box[2] = {64, box_rows};
   cuuint32_t es[2] = {1, 1};
-  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+  CUresult r = g_encode(m, is_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -79,18 +81,20 @@ struct dflash_handle {
   int max_pos = 0;     // max_pages_per_slot * page_size
   int attn_splits = 1;
   int max_tiles = 0;
-  // weights
-  const bf16* embed;
-  const bf16* fc;
-  const bf16* fc_norm;
-  const bf16* final_norm;
-  const bf16* in_norm[DFL_MAX_LAYERS];
-  const bf16* q_norm[DFL_MAX_LAYERS];
-  const bf16* k_norm[DFL_MAX_LAYERS];
-  const bf16* post_norm[DFL_MAX_LAYERS];
-  // A operand descriptors
-  CUtensorMap tm_qkv[DFL_MAX_LAYERS], tm_wo[DFL_MAX_LAYERS], tm_gu[DFL_MAX_LAYERS], tm_down[DFL_MAX_LAYERS];
-  CUtensorMap tm_fc, tm_embed;
+  // weights, copied into the workspace at create: matrices packed into
+  // 128x64 blocks (f16, except the bf16 fusion projection), gains as fp32
+  f16* embed_pk;
+  bf16* fc_pk;
+  f16* wqkv_pk[DFL_MAX_LAYERS];
+  f16* wo_pk[DFL_MAX_LAYERS];
+  f16* gu_pk[DFL_MAX_LAYERS];
+  f16* down_pk[DFL_MAX_LAYERS];
+  float* fc_norm;
+  float* final_norm;
+  float* in_norm[DFL_MAX_LAYERS];
+  float* q_norm[DFL_MAX_LAYERS];
+  float* k_norm[DFL_MAX_LAYERS];
+  float* post_norm[DFL_MAX_LAYERS];
   // cached B operand descriptors for the current token count
   int bm_M = -1;
   CUtensorMap tm_hg, tm_o, tm_act;
@@ -99,11 +103,11 @@ struct dflash_handle {
   // workspace
   uint32_t* status;
   int *ctx_len, *pos0, *n_pages, *page_table, *free_stack, *free_top, *n_eff;
-  bf16 *k_pool, *v_pool;
+  f16 *k_pool, *v_pool;
   long long layer_stride;
   float2* rope;
   float* h;
-  bf16 *hg, *qbuf, *obuf, *act, *cg;
+  f16 *hg, *qbuf, *obuf, *act, *cg;
   float *ss_a, *ss_c;
   unsigned long long* keys;
   unsigned* done_ctr;
@@ -143,12 +147,13 @@ bool cfg_valid(const dflash_config* c) {
   return true;
 }
 
+// Split-KV count: about one wave of CTAs, at least 4 pages per split at full
+// slot capacity, and at most 8 splits so the last CTA's merge stays short.
 int pick_attn_splits(const dflash_config& c, int num_sms) {
   const int pairs = c.max_batch * c.n_kv_heads;
-  int want = ceil_div(2LL * num_sms, pairs);
-  const int cap = std::max(1, c.max_pages_per_slot / 2);
-  want = std::min(want, cap);
-  want = std::min(want, 16);
+  int want = ceil_div(num_sms, pairs);
+  want = std::min(want, std::max(1, c.max_pages_per_slot / 4));
+  want = std::min(want, 8);
   return std::max(1, want);
 }
 
@@ -180,19 +185,34 @@ size_t carve(dflash_handle* h, const dflash_config& c, char* base, int num_sms) 
   o->free_stack = w.take<int>(c.max_pages);
   o->free_top = w.take<int>(1);
   o->n_eff = w.take<int>(c.max_batch);
-  o->k_pool = w.take<bf16>((size_t)c.n_layers * layer_stride);
-  o->v_pool = w.take<bf16>((size_t)c.n_layers * layer_stride);
+  const size_t KBh = H / 64;
+  o->embed_pk = w.take<f16>((size_t)ceil_div(c.vocab, 128) * KBh * DFL_WBLK_ELEMS);
+  o->fc_pk = w.take<bf16>((size_t)(H / 128) * (c.n_fused * H / 64) * DFL_WBLK_ELEMS);
+  o->fc_norm = w.take<float>(H);
+  o->final_norm = w.take<float>(H);
+  for (int l = 0; l < c.n_layers; ++l) {
+    o->wqkv_pk[l] = w.take<f16>((size_t)((hq + 2 * hkv) * D / 128) * KBh * DFL_WBLK_ELEMS);
+    o->wo_pk[l] = w.take<f16>((size_t)(H / 128) * (hq * D / 64) * DFL_WBLK_ELEMS);
+    o->gu_pk[l] = w.take<f16>((size_t)(I / 64) * KBh * DFL_WBLK_ELEMS);
+    o->down_pk[l] = w.take<f16>((size_t)(H / 128) * (I / 64) * DFL_WBLK_ELEMS);
+    o->in_norm[l] = w.take<float>(H);
+    o->post_norm[l] = w.take<float>(H);
+    o->q_norm[l] = w.take<float>(D);
+    o->k_norm[l] = w.take<float>(D);
+  }
+  o->k_pool = w.take<f16>((size_t)c.n_layers * layer_stride);
+  o->v_pool = w.take<f16>((size_t)c.n_layers * layer_stride);
   o->layer_stride = layer_stride;
   o->rope = w.take<float2>((size_t)max_pos * (D / 2));
   o->h = w.take<float>((size_t)M * H);
-  o->hg = w.take<bf16>((size_t)M * H);
+  o->hg = w.take<f16>((size_t)M * H);
   o->ss_a = w.take<float>((size_t)(H / 128) * M);
-  o->qbuf = w.take<bf16>((size_t)M * hq * D);
-  o->obuf = w.take<bf16>((size_t)M * hq * D);
-  o->act = w.take<bf16>((size_t)M * I);
+  o->qbuf = w.take<f16>((size_t)M * hq * D);
+  o->obuf = w.take<f16>((size_t)M * hq * D);
+  o->act = w.take<f16>((size_t)M * I);
   o->keys = w.take<unsigned long long>(M);
   o->done_ctr = w.take<unsigned>(64);
-  o->cg = w.take<bf16>((size_t)R * H);
+  o->cg = w.take<f16>((size_t)R * H);
   o->ss_c = w.take<float>((size_t)(H / 128) * R);
   o->gemm_ws = w.take<float>((size_t)num_sms * 2 * DFL_BN_MAX * 128);
   o->tile_ctr = w.take<unsigned>(tiles);
@@ -236,13 +256,12 @@ struct ProbeScope {
   }
 };
 
-// Plan and launch one GEMM.  N_rows: A rows covered per group; tile_rows:
-// rows per tile along N (128, or 64 features for SwiGLU).
-int run_gemm(dflash_handle* h, cudaStream_t s, int mode, const CUtensorMap* A, int groups, int n_tiles, int K,
-             const CUtensorMap& B, int M, GemmParams p, bool allow_split, int kid = 0) {
+// Plan and launch one GEMM over packed A operands a[0..groups-1] (tiles
+// a_tile_off .. a_tile_off+n_tiles-1 of each) and the token operand B.
+int run_gemm(dflash_handle* h, cudaStream_t s, int mode, const void* const* a, int groups, int a_tile_off,
+             int n_tiles, int K, const CUtensorMap& B, int M, GemmParams p, bool allow_split, uint32_t ab_type,
+             int kid = 0) {
   if (M <= 0) return DFLASH_OK;
-  TmapSet set;
-  for (int g = 0; g < groups; ++g) set.m[g] = A[g];
   const int t_tiles = ceil_div(M, DFL_BN_MAX);
   const int BN = ((ceil_div(M, t_tiles) + 15) / 16) * 16;
   p.mode = mode;
@@ -252,6 +271,9 @@ int run_gemm(dflash_handle* h, cudaStream_t s, int mode, const CUtensorMap* A, i
   p.t_tiles = t_tiles;
   p.BN = BN;
   p.groups = groups;
+  for (int g = 0; g < groups; ++g) p.a[g] = a[g];
+  p.a_tile_off = a_tile_off;
+  p.ab_type = ab_type;
   p.total_tiles = groups * n_tiles * t_tiles;
   p.allow_split = allow_split ? 1 : 0;
   p.stages = gemm_pick_stages(BN);
@@ -273,7 +295,7 @@ int run_gemm(dflash_handle* h, cudaStream_t s, int mode, const CUtensorMap* A, i
   const int grid = (int)std::min<long long>(units, h->num_sms);
   ProbeScope ps(h, kid, s);
   h->launches++;
-  return cuda_err(gemm_launch(set, B, p, grid, s, h->pdl));
+  return cuda_err(gemm_launch(B, p, grid, s, h->pdl));
 }
 
 KVGeom kv_geom(dflash_handle* h) {
@@ -316,8 +338,8 @@ int draft_impl(dflash_handle* h, const int32_t* slots, int32_t batch, const int3
   const KVGeom kv = kv_geom(h);
 
   h->launches++;
-  rc = cuda_err(launch_embed(slots, batch, last_tok, c.mask_id, h->embed, h->in_norm[0], H, h->h, h->hg, h->ss_a,
-                             h->keys, s));
+  rc = cuda_err(launch_embed(slots, batch, last_tok, c.mask_id, c.vocab, h->embed_pk, h->in_norm[0], H, h->h,
+                             h->hg, h->ss_a, h->keys, h->status, s));
   if (rc) return rc;
 
   for (int l = 0; l < c.n_layers; ++l) {
@@ -334,7 +356,8 @@ int draft_impl(dflash_handle* h, const int32_t* slots, int32_t batch, const int3
       p.ctx_len = h->ctx_len;
       p.rows_per_req = DFL_BLOCK;
       p.N = (hq + 2 * hkv) * D;
-      rc = run_gemm(h, s, GM_QKV, &h->tm_qkv[l], 1, p.N / 128, H, h->tm_hg, M, p, true, DFLASH_KID_QKV);
+      const void* a = h->wqkv_pk[l];
+      rc = run_gemm(h, s, GM_QKV, &a, 1, 0, p.N / 128, H, h->tm_hg, M, p, true, 0, DFLASH_KID_QKV);
       if (rc) return rc;
     }
     {  // block attention
@@ -365,7 +388,8 @@ int draft_impl(dflash_handle* h, const int32_t* slots, int32_t batch, const int3
       p.gain = h->post_norm[l];
       p.ss_out = h->ss_a;
       p.N = H;
-      rc = run_gemm(h, s, GM_RESID, &h->tm_wo[l], 1, H / 128, hq * D, h->tm_o, M, p, true);
+      const void* a = h->wo_pk[l];
+      rc = run_gemm(h, s, GM_RESID, &a, 1, 0, H / 128, hq * D, h->tm_o, M, p, true, 0);
       if (rc) return rc;
     }
     {  // gate/up projection + SiLU gating
@@ -374,8 +398,8 @@ int draft_impl(dflash_handle* h, const int32_t* slots, int32_t batch, const int3
       p.ss_parts = H / 128;
       p.out = h->act;
       p.N = I;
-      p.up_off = I;
-      rc = run_gemm(h, s, GM_SWIGLU, &h->tm_gu[l], 1, I / 64, H, h->tm_hg, M, p, true, DFLASH_KID_GATE_UP);
+      const void* a = h->gu_pk[l];
+      rc = run_gemm(h, s, GM_SWIGLU, &a, 1, 0, I / 64, H, h->tm_hg, M, p, true, 0, DFLASH_KID_GATE_UP);
       if (rc) return rc;
     }
     {  // down projection + residual; next norm inputs
@@ -385,7 +409,8 @@ int draft_impl(dflash_handle* h, const int32_t* slots, int32_t batch, const int3
       p.gain = (l + 1 < c.n_layers) ? h->in_norm[l + 1] : h->final_norm;
       p.ss_out = h->ss_a;
       p.N = H;
-      rc = run_gemm(h, s, GM_RESID, &h->tm_down[l], 1, H / 128, I, h->tm_act, M, p, true, DFLASH_KID_DOWN);
+      const void* a = h->down_pk[l];
+      rc = run_gemm(h, s, GM_RESID, &a, 1, 0, H / 128, I, h->tm_act, M, p, true, 0, DFLASH_KID_DOWN);
       if (rc) return rc;
     }
   }
@@ -402,7 +427,8 @@ int draft_impl(dflash_handle* h, const int32_t* slots, int32_t batch, const int3
     p.logits = logits;
     p.draft = draft;
     p.done_ctr = h->done_ctr;
-    rc = run_gemm(h, s, GM_ARGMAX, &h->tm_embed, 1, ceil_div(c.vocab, 128), H, h->tm_hg, M, p, false,
+    const void* a = h->embed_pk;
+    rc = run_gemm(h, s, GM_ARGMAX, &a, 1, 0, ceil_div(c.vocab, 128), H, h->tm_hg, M, p, true, 0,
                   DFLASH_KID_LM_HEAD);
     if (rc) return rc;
   }
@@ -456,29 +482,33 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
   if (!h) return DFLASH_ERR_CAPACITY;
   h->cfg = *cfg;
   h->num_sms = sms;
-  carve(h, *cfg, static_cast<char*>(workspace), sms);
+  const size_t need = carve(h, *cfg, static_cast<char*>(workspace), sms);
+  if (cuda_err(cudaMemset(workspace, 0, need))) {
+    delete h;
+    return DFLASH_ERR_CUDA;
+  }
   const dflash_config& c = *cfg;
   const int H = c.hidden, D = c.head_dim, hq = c.n_q_heads, hkv = c.n_kv_heads, I = c.intermediate;
-  h->embed = static_cast<const bf16*>(w->embed);
-  h->fc = static_cast<const bf16*>(w->fc);
-  h->fc_norm = static_cast<const bf16*>(w->fc_norm);
-  h->final_norm = static_cast<const bf16*>(w->final_norm);
-  bool ok = make_tmap(&h->tm_embed, w->embed, c.vocab, H, 64) &&
-            make_tmap(&h->tm_fc, w->fc, H, (uint64_t)c.n_fused * H, 64);
-  for (int l = 0; l < c.n_layers && ok; ++l) {
-    h->in_norm[l] = static_cast<const bf16*>(w->in_norm[l]);
-    h->q_norm[l] = static_cast<const bf16*>(w->q_norm[l]);
-    h->k_norm[l] = static_cast<const bf16*>(w->k_norm[l]);
-    h->post_norm[l] = static_cast<const bf16*>(w->post_norm[l]);
-    ok = make_tmap(&h->tm_qkv[l], w->wqkv[l], (uint64_t)(hq + 2 * hkv) * D, H, 64) &&
-         make_tmap(&h->tm_wo[l], w->wo[l], H, (uint64_t)hq * D, 64) &&
-         make_tmap(&h->tm_gu[l], w->w_gate_up[l], 2ull * I, H, 64) &&
-         make_tmap(&h->tm_down[l], w->w_down[l], H, I, 64);
+  auto B16 = [](const void* p) { return static_cast<const bf16*>(p); };
+  cudaError_t e = launch_pack_weight(B16(w->embed), h->embed_pk, c.vocab, H, ceil_div(c.vocab, 128), 0, true, 0);
+  if (!e) e = launch_pack_weight(B16(w->fc), h->fc_pk, H, c.n_fused * H, H / 128, 0, false, 0);
+  if (!e) e = launch_gain_f32(B16(w->fc_norm), h->fc_norm, H, 0);
+  if (!e) e = launch_gain_f32(B16(w->final_norm), h->final_norm, H, 0);
+  for (int l = 0; l < c.n_layers && !e; ++l) {
+    e = launch_pack_weight(B16(w->wqkv[l]), h->wqkv_pk[l], (hq + 2 * hkv) * D, H, (hq + 2 * hkv) * D / 128, 0, true,
+                           0);
+    if (!e) e = launch_pack_weight(B16(w->wo[l]), h->wo_pk[l], H, hq * D, H / 128, 0, true, 0);
+    if (!e) e = launch_pack_weight(B16(w->w_gate_up[l]), h->gu_pk[l], 2 * I, H, I / 64, I, true, 0);
+    if (!e) e = launch_pack_weight(B16(w->w_down[l]), h->down_pk[l], H, I, H / 128, 0, true, 0);
+    if (!e) e = launch_gain_f32(B16(w->in_norm[l]), h->in_norm[l], H, 0);
+    if (!e) e = launch_gain_f32(B16(w->post_norm[l]), h->post_norm[l], H, 0);
+    if (!e) e = launch_gain_f32(B16(w->q_norm[l]), h->q_norm[l], D, 0);
+    if (!e) e = launch_gain_f32(B16(w->k_norm[l]), h->k_norm[l], D, 0);
   }
+  bool ok = e == cudaSuccess;
   int rc = ok ? DFLASH_OK : DFLASH_ERR_CUDA;
   if (!rc) rc = cuda_err(gemm_init_attributes());
   if (!rc) rc = cuda_err(attn_init_attributes());
-  if (!rc) rc = cuda_err(cudaMemset(workspace, 0, carve(nullptr, c, nullptr, sms)));
   if (!rc)
     rc = cuda_err(cudaMemset(h->page_table, 0xFF, (size_t)c.max_slots * c.max_pages_per_slot * sizeof(int)));
   if (!rc) rc = cuda_err(launch_pool_init(h->free_stack, h->free_top, c.max_pages, 0));
@@ -521,7 +551,7 @@ int dflash_fuse_inject(dflash_handle* h, const int32_t* slots, int32_t batch, co
   const int t_tiles = ceil_div(R, DFL_BN_MAX);
   const uint32_t BN = (uint32_t)(((ceil_div(R, t_tiles) + 15) / 16) * 16);
   CUtensorMap tm_feats;
-  if (!make_tmap(&tm_feats, feats, R, (uint64_t)c.n_fused * H, BN)) return DFLASH_ERR_INVALID_ARG;
+  if (!make_tmap(&tm_feats, feats, R, (uint64_t)c.n_fused * H, BN, true)) return DFLASH_ERR_INVALID_ARG;
   if (h->bm_rows != R) {
     if (!make_tmap(&h->tm_cg, h->cg, R, H, BN)) return DFLASH_ERR_CUDA;
     h->bm_rows = R;
@@ -532,14 +562,14 @@ int dflash_fuse_inject(dflash_handle* h, const int32_t* slots, int32_t batch, co
     p.gain = h->fc_norm;
     p.ss_out = h->ss_c;
     p.N = H;
-    rc = run_gemm(h, s, GM_FC, &h->tm_fc, 1, H / 128, c.n_fused * H, tm_feats, R, p, true);
+    const void* a = h->fc_pk;
+    rc = run_gemm(h, s, GM_FC, &a, 1, 0, H / 128, c.n_fused * H, tm_feats, R, p, true, 1);
     if (rc) return rc;
   }
   {  // every layer's K/V projection of the fused feature, k-norm, RoPE, paged append
     GemmParams p = {};
     p.ss_in = h->ss_c;
     p.ss_parts = H / 128;
-    p.a_row_off = c.n_q_heads * D;
     p.N = 2 * hkv * D;
     for (int l = 0; l < c.n_layers; ++l) p.kn_gain[l] = h->k_norm[l];
     p.kv = kv_geom(h);
@@ -547,7 +577,9 @@ int dflash_fuse_inject(dflash_handle* h, const int32_t* slots, int32_t batch, co
     p.pos0 = h->pos0;
     p.n_eff = h->n_eff;
     p.rows_per_req = rows_per_req;
-    rc = run_gemm(h, s, GM_INJECT, h->tm_qkv, c.n_layers, p.N / 128, H, h->tm_cg, R, p, true);
+    const void* a[DFL_MAX_LAYERS];
+    for (int l = 0; l < c.n_layers; ++l) a[l] = h->wqkv_pk[l];
+    rc = run_gemm(h, s, GM_INJECT, a, c.n_layers, c.n_q_heads * D / 128, p.N / 128, H, h->tm_cg, R, p, true, 0);
     if (rc) return rc;
   }
   return DFLASH_OK;
@@ -639,8 +671,8 @@ int dflash_read_kv(dflash_handle* h, int32_t layer, int32_t slot, int32_t pos0, 
       pos0 < 0 || n < 0 || pos0 + n > h->max_pos)
     return DFLASH_ERR_INVALID_ARG;
   if (cudaSetDevice(h->cfg.device) != cudaSuccess) return DFLASH_ERR_CUDA;
-  return cuda_err(launch_read_kv(kv_geom(h), layer, slot, pos0, n, static_cast<bf16*>(k_out),
-                                 static_cast<bf16*>(v_out), (cudaStream_t)stream));
+  return cuda_err(launch_read_kv(kv_geom(h), layer, slot, pos0, n, static_cast<float*>(k_out),
+                                 static_cast<float*>(v_out), (cudaStream_t)stream));
 }
 
 int dflash_slot_lengths(dflash_handle* h, const int32_t* slots, int32_t batch, int32_t* out, void* stream) {

@@ -6,7 +6,7 @@
 // request's 64-position pages.  Each page of K (64 x D) and V^T (D x 64) is a
 // contiguous 2 x 8..16 KB block stored pre-swizzled in HBM, so an untiled TMA
 // bulk copy lands it in shared memory already in a bank-conflict-free layout
-// for ldmatrix.  Q.K^T and P.V run on warp MMAs (m16n8k16, bf16 in, fp32
+// for ldmatrix.  Q.K^T and P.V run on warp MMAs (m16n8k16, f16 in, fp32
 // accumulate), the softmax is online in the log2 domain with quad shuffles.
 // Splits write fp32 partials (O, running max, running sum); the last CTA of a
 // (request, KV head) merges them in split order -- deterministic, no waiting.
@@ -50,8 +50,8 @@ __global__ void __launch_bounds__(G * 32) k_attn(const AttnParams p) {
   const int per = (npages + p.n_splits - 1) / p.n_splits;
   const int pb = split * per;
   const int pe = min(npages, pb + per);
-  const bf16* kbase = p.kv.k_pool + (size_t)p.layer * p.kv.layer_stride;
-  const bf16* vbase = p.kv.v_pool + (size_t)p.layer * p.kv.layer_stride;
+  const f16* kbase = p.kv.k_pool + (size_t)p.layer * p.kv.layer_stride;
+  const f16* vbase = p.kv.v_pool + (size_t)p.layer * p.kv.layer_stride;
   const int* pt = p.kv.page_table + (size_t)slot * p.kv.max_pages_per_slot;
 
   auto issue = [&](int s, int page_idx) {
@@ -74,7 +74,7 @@ __global__ void __launch_bounds__(G * 32) k_attn(const AttnParams p) {
   const int j = kvh * G + warp;
   uint32_t qa[D / 16][4];
   {
-    const bf16* q0 = p.q + ((size_t)(b * DFL_BLOCK) * hq + j) * D;
+    const f16* q0 = p.q + ((size_t)(b * DFL_BLOCK) * hq + j) * D;
     const size_t rs = (size_t)hq * D;
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
@@ -115,8 +115,8 @@ __global__ void __launch_bounds__(G * 32) k_attn(const AttnParams p) {
               kb_addr + 2u * (uint32_t)((chunk >> 3) * (64 * 64) + key * 64 + (((chunk & 7) ^ (key & 7)) << 3));
           uint32_t b0, b1, b2, b3;
           ldsm_x4(addr, b0, b1, b2, b3);
-          mma_bf16_16816(sc[2 * kg], qa[kk], b0, b1);
-          mma_bf16_16816(sc[2 * kg + 1], qa[kk], b2, b3);
+          mma_f16_16816(sc[2 * kg], qa[kk], b0, b1);
+          mma_f16_16816(sc[2 * kg + 1], qa[kk], b2, b3);
         }
       }
       // online softmax (log2 domain), rows g and g+8 of this warp
@@ -164,10 +164,10 @@ __global__ void __launch_bounds__(G * 32) k_attn(const AttnParams p) {
 #pragma unroll
       for (int k2 = 0; k2 < 4; ++k2) {
         uint32_t pa[4];
-        pa[0] = pack_bf16x2(sc[2 * k2][0], sc[2 * k2][1]);
-        pa[1] = pack_bf16x2(sc[2 * k2][2], sc[2 * k2][3]);
-        pa[2] = pack_bf16x2(sc[2 * k2 + 1][0], sc[2 * k2 + 1][1]);
-        pa[3] = pack_bf16x2(sc[2 * k2 + 1][2], sc[2 * k2 + 1][3]);
+        pa[0] = pack_f16x2(sc[2 * k2][0], sc[2 * k2][1]);
+        pa[1] = pack_f16x2(sc[2 * k2][2], sc[2 * k2][3]);
+        pa[2] = pack_f16x2(sc[2 * k2 + 1][0], sc[2 * k2 + 1][1]);
+        pa[3] = pack_f16x2(sc[2 * k2 + 1][2], sc[2 * k2 + 1][3]);
 #pragma unroll
         for (int nd = 0; nd < D / 8; nd += 2) {
           const int dim = (nd + (mi >> 1)) * 8 + rr;
@@ -175,8 +175,8 @@ __global__ void __launch_bounds__(G * 32) k_attn(const AttnParams p) {
           const uint32_t addr = vb_addr + 2u * (uint32_t)(dim * 64 + ((chunk ^ (dim & 7)) << 3));
           uint32_t b0, b1, b2, b3;
           ldsm_x4(addr, b0, b1, b2, b3);
-          mma_bf16_16816(o[nd], pa, b0, b1);
-          mma_bf16_16816(o[nd + 1], pa, b2, b3);
+          mma_f16_16816(o[nd], pa, b0, b1);
+          mma_f16_16816(o[nd + 1], pa, b2, b3);
         }
       }
     }
@@ -202,13 +202,13 @@ __global__ void __launch_bounds__(G * 32) k_attn(const AttnParams p) {
 
   if (p.n_splits == 1) {
     const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
-    bf16* out0 = p.out + ((size_t)(b * DFL_BLOCK + g) * hq + j) * D;
-    bf16* out1 = p.out + ((size_t)(b * DFL_BLOCK + g + 8) * hq + j) * D;
+    f16* out0 = p.out + ((size_t)(b * DFL_BLOCK + g) * hq + j) * D;
+    f16* out1 = p.out + ((size_t)(b * DFL_BLOCK + g + 8) * hq + j) * D;
 #pragma unroll
     for (int nd = 0; nd < D / 8; ++nd) {
       const int d = nd * 8 + 2 * c4;
-      *reinterpret_cast<uint32_t*>(out0 + d) = pack_bf16x2(o[nd][0] * i0, o[nd][1] * i0);
-      *reinterpret_cast<uint32_t*>(out1 + d) = pack_bf16x2(o[nd][2] * i1, o[nd][3] * i1);
+      *reinterpret_cast<uint32_t*>(out0 + d) = pack_f16x2(o[nd][0] * i0, o[nd][1] * i0);
+      *reinterpret_cast<uint32_t*>(out1 + d) = pack_f16x2(o[nd][2] * i1, o[nd][3] * i1);
     }
     return;
   }
@@ -261,21 +261,29 @@ __global__ void __launch_bounds__(G * 32) k_attn(const AttnParams p) {
   __syncthreads();
   for (int e = threadIdx.x; e < rows * D / 4; e += blockDim.x) {
     const int r = (e * 4) / D, d = (e * 4) % D;
+    // all splits' loads in flight before any is consumed (n_splits <= 8)
+    float4 v[8];
+#pragma unroll
+    for (int s = 0; s < 8; ++s)
+      if (s < p.n_splits)
+        v[s] = __ldcg(reinterpret_cast<const float4*>(base + s * pstride + (size_t)r * D + d));
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s = 0; s < p.n_splits; ++s) {
-      const float w = wsm[s * rows + r];
-      if (w != 0.f) {
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(base + s * pstride + (size_t)r * D + d));
-        acc.x += w * v.x;
-        acc.y += w * v.y;
-        acc.z += w * v.z;
-        acc.w += w * v.w;
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      if (s < p.n_splits) {
+        const float w = wsm[s * rows + r];
+        if (w != 0.f) {
+          acc.x += w * v[s].x;
+          acc.y += w * v[s].y;
+          acc.z += w * v[s].z;
+          acc.w += w * v[s].w;
+        }
       }
     }
     const int wq = r / 16, t = r % 16;
-    bf16* dst = p.out + ((size_t)(b * DFL_BLOCK + t) * hq + kvh * G + wq) * D + d;
-    *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc.x, acc.y);
-    *reinterpret_cast<uint32_t*>(dst + 2) = pack_bf16x2(acc.z, acc.w);
+    f16* dst = p.out + ((size_t)(b * DFL_BLOCK + t) * hq + kvh * G + wq) * D + d;
+    *reinterpret_cast<uint32_t*>(dst) = pack_f16x2(acc.x, acc.y);
+    *reinterpret_cast<uint32_t*>(dst + 2) = pack_f16x2(acc.z, acc.w);
   }
 }
 
@@ -319,8 +327,7 @@ cudaError_t attr_d() {
 
 }  // namespace
 
-int attn_stages(int D) { return D == 64 ? AttnCfg<64>::STAGES : AttnCfg<128>::STAGES; }
-size_t attn_smem_bytes(int D, int) { return D == 64 ? AttnCfg<64>::SMEM : AttnCfg<128>::SMEM; }
+size_t attn_smem_bytes(int D) { return D == 64 ? AttnCfg<64>::SMEM : AttnCfg<128>::SMEM; }
 
 cudaError_t attn_init_attributes() {
   cudaError_t e = attr_d<64>();

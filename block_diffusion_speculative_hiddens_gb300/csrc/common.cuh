@@ -1,8 +1,9 @@
 // Device primitives for sm_103a: mbarriers, TMA (tensor and bulk), tcgen05
-// (TMEM allocation, MMA, loads), legacy warp MMA, bf16 helpers, bounded waits.
+// (TMEM allocation, MMA, loads), warp MMA, f16/bf16 helpers, bounded waits.
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -11,6 +12,7 @@
 #define DFL_DEV __device__ __forceinline__
 
 typedef __nv_bfloat16 bf16;
+typedef __half f16;
 
 // Bounded waits give up after this many nanoseconds of %globaltimer.
 #define DFL_WAIT_NS 2000000000ull
@@ -97,6 +99,13 @@ DFL_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
+DFL_DEV void bulk_load_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
 DFL_DEV void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }
@@ -116,8 +125,8 @@ DFL_DEV void tmem_dealloc(uint32_t taddr, uint32_t ncols) {  // one full warp
 DFL_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 DFL_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (bf16 inputs, f32 accumulate).
-DFL_DEV void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accum) {
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (f16 or bf16 inputs, f32 accumulate).
+DFL_DEV void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accum) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
@@ -154,9 +163,10 @@ DFL_DEV uint64_t sdesc_sw128(uint32_t saddr) {
          | ((uint64_t)1 << 46)                   // descriptor version for tcgen05
          | ((uint64_t)2 << 61);                  // 128-byte swizzle
 }
-// Instruction descriptor, kind::f16: f32 accumulator, bf16 A and B, both K-major.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+// Instruction descriptor, kind::f16: f32 accumulator, A and B both bf16
+// (ab_type 1) or both f16 (ab_type 0), both K-major.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, uint32_t ab_type) {
+  return (1u << 4) | (ab_type << 7) | (ab_type << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // ------------------------------------------------------------------ named barriers
@@ -181,9 +191,21 @@ DFL_DEV void mma_bf16_16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
-DFL_DEV uint32_t pack_bf16x2(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+DFL_DEV void mma_f16_16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+DFL_DEV uint32_t pack_f16x2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+// float -> f16 activation; values beyond the f16 range set DFLASH_DEV_RANGE.
+DFL_DEV f16 to_f16(float x, uint32_t* status) {
+  if (fabsf(x) > 65504.f) dev_error(status, DFLASH_DEV_RANGE);
+  return __float2half_rn(x);
 }
 
 // ------------------------------------------------------------------ misc
@@ -202,6 +224,10 @@ DFL_DEV unsigned long long argmax_key(float v, uint32_t idx) {
   return ((unsigned long long)ord << 32) | (unsigned long long)(0xFFFFFFFFu - idx);
 }
 DFL_DEV uint32_t argmax_key_index(unsigned long long key) { return 0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull); }
+
+// Element offset of (row r, column k) inside a packed 128 x 64 weight block:
+// the 128-byte-swizzle image a TMA tiled load would produce in shared memory.
+DFL_DEV int wpack_off(int r, int k) { return r * 64 + ((((k >> 3) ^ (r & 7))) << 3) + (k & 7); }
 
 // Offsets (elements) inside one (page, kv-head) block of the pre-swizzled cache.
 //  K block: [D/64 halves][64 positions][64 dims], 16-byte chunks XOR-swizzled

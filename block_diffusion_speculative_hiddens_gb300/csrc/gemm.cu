@@ -6,9 +6,15 @@
 // tcgen05.mma.cta_group::1 M=128 instruction covers 128 output features x all
 // tokens, and the weights stream through shared memory exactly once.
 //
+// Weights are packed once at handle creation into 16 KB blocks of 128 rows x
+// 64 columns, each already laid out as the 128-byte-swizzle image tcgen05
+// reads (tiles of a matrix stored tile-major, k-blocks contiguous), so a
+// stage's weight tile is one contiguous untiled bulk copy from HBM.
+//
 // Pipeline per CTA (persistent, one per SM, 192 threads):
-//   warp 0  TMA producer: 128x64 weight tile (two 64-row boxes) + BNx64 token
-//           tile per stage, 128-byte swizzle, completion on an mbarrier;
+//   warp 0  producer: one 16 KB bulk copy for the weight block and one TMA
+//           tiled load (128-byte swizzle) for the BNx64 token tile per stage,
+//           completion on an mbarrier;
 //   warp 1  TMEM allocator and single-thread MMA issuer (4 x K=16 per stage),
 //           double-buffered fp32 accumulators in TMEM;
 //   warps 2-5 epilogue: tcgen05.ld -> registers -> fused epilogue.
@@ -24,7 +30,7 @@
 
 namespace {
 
-constexpr int A_STAGE_BYTES = 128 * 128;  // 128 rows x 64 bf16
+constexpr int A_STAGE_BYTES = 128 * 128;  // 128 rows x 64 16-bit values
 constexpr int STG_BYTES = 32 * 128 * 4;   // epilogue staging: 32 tokens x 128 rows fp32
 constexpr int EPI_THREADS = 128;
 
@@ -42,12 +48,12 @@ DFL_DEV float norm_scale(const float* ss, int parts, int M, int t, int width, fl
 // Head RMSNorm + RoPE on the 4 values a lane holds (rows lane, lane+32,
 // lane+64, lane+96 of a 128-row tile).  D = 128: one head, RoPE pairs (0,2),
 // (1,3).  D = 64: two heads (rows 0-63, 64-127), pairs (0,1) and (2,3).
-DFL_DEV void head_norm_rope(float* x, const bf16* gain, const float2* rope_row, int D, float eps, int lane) {
+DFL_DEV void head_norm_rope(float* x, const float* gain, const float2* rope_row, int D, float eps, int lane) {
   if (D == 128) {
     float ss = warp_sum(x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3]);
     const float inv = rsqrtf(ss / 128.f + eps);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) x[j] *= inv * bf2f(gain[lane + 32 * j]);
+    for (int j = 0; j < 4; ++j) x[j] *= inv * gain[lane + 32 * j];
     const float2 c0 = rope_row[lane], c1 = rope_row[lane + 32];
     const float a0 = x[0], b0 = x[2], a1 = x[1], b1 = x[3];
     x[0] = a0 * c0.x - b0 * c0.y;
@@ -58,7 +64,7 @@ DFL_DEV void head_norm_rope(float* x, const bf16* gain, const float2* rope_row, 
     const float sa = warp_sum(x[0] * x[0] + x[1] * x[1]);
     const float sb = warp_sum(x[2] * x[2] + x[3] * x[3]);
     const float ia = rsqrtf(sa / 64.f + eps), ib = rsqrtf(sb / 64.f + eps);
-    const float g0 = bf2f(gain[lane]), g1 = bf2f(gain[lane + 32]);
+    const float g0 = gain[lane], g1 = gain[lane + 32];
     x[0] *= ia * g0;
     x[1] *= ia * g1;
     x[2] *= ib * g0;
@@ -77,16 +83,16 @@ DFL_DEV void write_k(const GemmParams& p, int layer, int slot, int pos, int kh, 
   if (pg_i >= p.kv.max_pages_per_slot) { dev_error(p.status, DFLASH_DEV_PAGE); return; }
   const int pg = p.kv.page_table[(size_t)slot * p.kv.max_pages_per_slot + pg_i];
   if (pg < 0 || pg >= p.kv.max_pages) { dev_error(p.status, DFLASH_DEV_PAGE); return; }
-  bf16* blk = p.kv.k_pool + (size_t)layer * p.kv.layer_stride + ((size_t)pg * p.kv.hkv + kh) * (64 * p.kv.D);
-  blk[k_swz(pos & 63, d)] = __float2bfloat16(v);
+  f16* blk = p.kv.k_pool + (size_t)layer * p.kv.layer_stride + ((size_t)pg * p.kv.hkv + kh) * (64 * p.kv.D);
+  blk[k_swz(pos & 63, d)] = to_f16(v, p.status);
 }
 DFL_DEV void write_v(const GemmParams& p, int layer, int slot, int pos, int kh, int d, float v) {
   const int pg_i = pos >> 6;
   if (pg_i >= p.kv.max_pages_per_slot) { dev_error(p.status, DFLASH_DEV_PAGE); return; }
   const int pg = p.kv.page_table[(size_t)slot * p.kv.max_pages_per_slot + pg_i];
   if (pg < 0 || pg >= p.kv.max_pages) { dev_error(p.status, DFLASH_DEV_PAGE); return; }
-  bf16* blk = p.kv.v_pool + (size_t)layer * p.kv.layer_stride + ((size_t)pg * p.kv.hkv + kh) * (64 * p.kv.D);
-  blk[v_swz(d, pos & 63)] = __float2bfloat16(v);
+  f16* blk = p.kv.v_pool + (size_t)layer * p.kv.layer_stride + ((size_t)pg * p.kv.hkv + kh) * (64 * p.kv.D);
+  blk[v_swz(d, pos & 63)] = to_f16(v, p.status);
 }
 
 // Final epilogue for tokens t_first .. t_first+ntok-1 of `tile`; staging
@@ -114,7 +120,7 @@ DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, con
           hv += p.h[o];
           p.h[o] = hv;
         }
-        p.out[o] = __float2bfloat16(hv * bf2f(p.gain[n]));
+        p.out[o] = to_f16(hv * p.gain[n], p.status);
         sq += hv * hv;
       }
       sq = warp_sum(sq);
@@ -126,7 +132,7 @@ DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, con
       for (int jj = 0; jj < 2; ++jj) {
         const float g = x[jj] * s, u = x[jj + 2] * s;
         const float a = g / (1.f + __expf(-g)) * u;
-        p.out[(size_t)t * p.N + f0 + lane + 32 * jj] = __float2bfloat16(a);
+        p.out[(size_t)t * p.N + f0 + lane + 32 * jj] = to_f16(a, p.status);
       }
     } else if (MODE == GM_ARGMAX) {
       const float s = norm_scale(p.ss_in, p.ss_parts, p.M, t, p.H, p.eps, lane);
@@ -155,7 +161,7 @@ DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, con
     } else if (MODE == GM_QKV || MODE == GM_INJECT) {
       const int D = p.D;
       int slot, pos, layer, kind, n0;
-      const bf16* kgain;
+      const float* kgain;
       float s;
       if (MODE == GM_QKV) {
         const int b = t / DFL_BLOCK;
@@ -188,7 +194,7 @@ DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, con
       for (int jj = 0; jj < 4; ++jj) {
         const int n = n0 + lane + 32 * jj;
         if (kind == 0) {
-          p.out[(size_t)t * (p.hq * D) + n] = __float2bfloat16(x[jj]);
+          p.out[(size_t)t * (p.hq * D) + n] = to_f16(x[jj], p.status);
         } else if (kind == 1) {
           const int m = n - p.hq * D;
           write_k(p, layer, slot, pos, m / D, m % D, x[jj]);
@@ -203,7 +209,7 @@ DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, con
 
 template <int MODE>
 __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
-    k_gemm(const __grid_constant__ TmapSet tmA, const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+    k_gemm(const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* sm = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -262,29 +268,19 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
       prefetch_tmap(&tmB);
-      for (int g = 0; g < p.groups; ++g) prefetch_tmap(&tmA.m[g]);
       const bool stream_w = p.t_tiles == 1;
       const uint64_t pol = policy_evict_first();
       auto load_a = [&](int s, long long u) {
         const int tile = (int)(u / KB), kb = (int)(u % KB);
         const int tt_all = tile / p.t_tiles;
         const int g = tt_all / p.n_tiles, nt = tt_all % p.n_tiles;
-        int y0, y1;
-        if (MODE == GM_SWIGLU) {
-          y0 = p.a_row_off + nt * 64;
-          y1 = p.up_off + nt * 64;
-        } else {
-          y0 = p.a_row_off + nt * 128;
-          y1 = y0 + 64;
-        }
+        const uint16_t* src = static_cast<const uint16_t*>(p.a[g]) +
+                              ((size_t)(p.a_tile_off + nt) * p.kblocks + kb) * DFL_WBLK_ELEMS;
         uint8_t* dst = sm + (size_t)s * stage_bytes;
-        if (stream_w) {
-          tma_load_2d_hint(dst, &tmA.m[g], full + s, kb * 64, y0, pol);
-          tma_load_2d_hint(dst + 8192, &tmA.m[g], full + s, kb * 64, y1, pol);
-        } else {
-          tma_load_2d(dst, &tmA.m[g], full + s, kb * 64, y0);
-          tma_load_2d(dst + 8192, &tmA.m[g], full + s, kb * 64, y1);
-        }
+        if (stream_w)
+          bulk_load_hint(dst, src, A_STAGE_BYTES, full + s, pol);
+        else
+          bulk_load(dst, src, A_STAGE_BYTES, full + s);
       };
       auto load_b = [&](int s, long long u) {
         const int tile = (int)(u / KB), kb = (int)(u % KB);
@@ -319,7 +315,7 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(128, BN);
+      const uint32_t idesc = idesc_f16_f32(128, BN, p.ab_type);
       long long it = 0;
       int seg = 0;
       for (long long u = u0; u < u1 && !aborted; ++seg) {
@@ -339,7 +335,7 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
           const uint64_t bdesc = sdesc_sw128(a_addr + A_STAGE_BYTES);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            tc_mma_bf16(d, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk), idesc,
+            tc_mma_f16(d, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk), idesc,
                         (k > 0 || kk > 0) ? 1u : 0u);
           tc_commit(empty + s);
         }
@@ -488,8 +484,7 @@ cudaError_t gemm_init_attributes() {
   return cudaFuncSetAttribute(k_gemm<GM_ARGMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
 }
 
-cudaError_t gemm_launch(const TmapSet& A, const CUtensorMap& B, const GemmParams& p, int grid, cudaStream_t s,
-                        bool pdl) {
+cudaError_t gemm_launch(const CUtensorMap& B, const GemmParams& p, int grid, cudaStream_t s, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(DFL_GEMM_THREADS);
@@ -501,12 +496,12 @@ cudaError_t gemm_launch(const TmapSet& A, const CUtensorMap& B, const GemmParams
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   switch (p.mode) {
-    case GM_QKV: return cudaLaunchKernelEx(&cfg, k_gemm<GM_QKV>, A, B, p);
-    case GM_INJECT: return cudaLaunchKernelEx(&cfg, k_gemm<GM_INJECT>, A, B, p);
-    case GM_RESID: return cudaLaunchKernelEx(&cfg, k_gemm<GM_RESID>, A, B, p);
-    case GM_SWIGLU: return cudaLaunchKernelEx(&cfg, k_gemm<GM_SWIGLU>, A, B, p);
-    case GM_FC: return cudaLaunchKernelEx(&cfg, k_gemm<GM_FC>, A, B, p);
-    case GM_ARGMAX: return cudaLaunchKernelEx(&cfg, k_gemm<GM_ARGMAX>, A, B, p);
+    case GM_QKV: return cudaLaunchKernelEx(&cfg, k_gemm<GM_QKV>, B, p);
+    case GM_INJECT: return cudaLaunchKernelEx(&cfg, k_gemm<GM_INJECT>, B, p);
+    case GM_RESID: return cudaLaunchKernelEx(&cfg, k_gemm<GM_RESID>, B, p);
+    case GM_SWIGLU: return cudaLaunchKernelEx(&cfg, k_gemm<GM_SWIGLU>, B, p);
+    case GM_FC: return cudaLaunchKernelEx(&cfg, k_gemm<GM_FC>, B, p);
+    case GM_ARGMAX: return cudaLaunchKernelEx(&cfg, k_gemm<GM_ARGMAX>, B, p);
   }
   return cudaErrorInvalidValue;
 }

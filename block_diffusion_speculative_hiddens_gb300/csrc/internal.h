@@ -2,33 +2,37 @@
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #include "../../include/dflash.h"
 
 typedef __nv_bfloat16 bf16;
+typedef __half f16;
 
 #define DFL_MAX_LAYERS 8
 #define DFL_BLOCK 16
 #define DFL_PAGE 64
 #define DFL_BN_MAX 256
 #define DFL_GEMM_THREADS 192
+// One packed weight block: 128 rows x 64 columns of 16-bit values (16 KB).
+#define DFL_WBLK_ELEMS (128 * 64)
 
 // GEMM epilogue modes (swap-AB: weights are the 128-row A operand, tokens the N side).
 enum GemmMode : int {
   GM_QKV = 0,     // layer QKV: input-norm scale, q/k head norm, RoPE; q -> q_buf, block k/v -> cache
   GM_INJECT = 1,  // fused feature -> every layer's K/V: fusion-norm scale, k norm, RoPE, paged append
-  GM_RESID = 2,   // h += acc (fp32 residual); hg = bf16(h * next gain); per-tile sum of squares
-  GM_SWIGLU = 3,  // post-norm scale; act = silu(gate) * up
-  GM_FC = 4,      // fusion projection: cg = bf16(acc * fc gain); per-tile sum of squares
+  GM_RESID = 2,   // h += acc (fp32 residual); hg = f16(h * next gain); per-tile sum of squares
+  GM_SWIGLU = 3,  // post-norm scale; act = silu(gate) * up (tile rows 0-63 gate, 64-127 up)
+  GM_FC = 4,      // fusion projection: cg = f16(acc * fc gain); per-tile sum of squares
   GM_ARGMAX = 5   // final-norm scale; per-token argmax over the vocabulary (+ optional logits)
 };
 
 // Paged KV cache geometry (one layer's pools are at k_pool + layer*layer_stride).
 struct KVGeom {
-  bf16* k_pool;
-  bf16* v_pool;
+  f16* k_pool;
+  f16* v_pool;
   long long layer_stride;  // elements between layers' pools
   const int* page_table;   // [max_slots][max_pages_per_slot]
   int max_pages_per_slot;
@@ -36,25 +40,22 @@ struct KVGeom {
   int hkv, D;
 };
 
-struct TmapSet {
-  CUtensorMap m[DFL_MAX_LAYERS];
-};
-
 struct GemmParams {
   // problem
   int M;            // token rows of B
-  int N;            // output rows per group (A rows covered)
+  int N;            // output rows (features) per group
   int kblocks;      // K / 64
   int n_tiles;      // tiles per group along N
   int t_tiles;      // token tiles
   int BN;           // token tile (multiple of 16, <= 256)
-  int groups;       // A tensor maps used (grouped inject)
+  int groups;       // A operands used (grouped inject: one per layer)
   int total_tiles;  // groups * n_tiles * t_tiles
   int allow_split;  // 0: every tile in one CTA over the full K
   int stages;
   int tmem_cols;    // power of two >= max(32, 2*BN)
-  int a_row_off;    // first A row of the tile range (inject: hq*D)
-  int up_off;       // SwiGLU: A row offset of the up half (I)
+  uint32_t ab_type; // 0: f16 operands, 1: bf16 operands
+  const void* a[DFL_MAX_LAYERS];  // packed A blocks [tiles][kblocks][128x64] per group
+  int a_tile_off;   // first packed tile of the range (inject: hq*D/128)
   int mode;
   // shapes for epilogues
   int H;            // hidden (norm width for ss partial consumers)
@@ -67,10 +68,10 @@ struct GemmParams {
   float* ss_out;       // [n_tiles][M]
   // tensors
   float* h;             // RESID: fp32 residual [M][N]
-  bf16* out;            // QKV: q_buf [M][hq*D]; RESID: hg [M][N]; SWIGLU: act [M][I]; FC: cg [M][N]
-  const bf16* gain;     // RESID: next norm gain; FC: fusion gain
-  const bf16* qn_gain;  // QKV: q head-norm gain [D]
-  const bf16* kn_gain[DFL_MAX_LAYERS];  // per group (inject) / [0] (QKV)
+  f16* out;             // QKV: q_buf [M][hq*D]; RESID: hg [M][N]; SWIGLU: act [M][I]; FC: cg [M][N]
+  const float* gain;    // RESID: next norm gain; FC: fusion gain
+  const float* qn_gain; // QKV: q head-norm gain [D]
+  const float* kn_gain[DFL_MAX_LAYERS];  // per group (inject) / [0] (QKV)
   int layer;            // QKV: layer index for the cache
   KVGeom kv;
   const int* slots;     // [batch]
@@ -91,8 +92,8 @@ struct GemmParams {
 };
 
 struct AttnParams {
-  const bf16* q;    // [M][hq][D]
-  bf16* out;        // [M][hq][D]
+  const f16* q;     // [M][hq][D]
+  f16* out;         // [M][hq][D]
   KVGeom kv;
   int layer;
   const int* slots;
@@ -108,18 +109,21 @@ struct AttnParams {
 // host launchers (gemm.cu / attention.cu / small.cu)
 size_t gemm_smem_bytes(int BN, int stages);
 int gemm_pick_stages(int BN);
-cudaError_t gemm_launch(const TmapSet& A, const CUtensorMap& B, const GemmParams& p, int grid,
-                        cudaStream_t s, bool pdl);
+cudaError_t gemm_launch(const CUtensorMap& B, const GemmParams& p, int grid, cudaStream_t s, bool pdl);
 cudaError_t gemm_init_attributes();
 
-int attn_stages(int D);
-size_t attn_smem_bytes(int D, int stages);
+size_t attn_smem_bytes(int D);
 cudaError_t attn_launch(const AttnParams& p, int batch, cudaStream_t s, bool pdl);
 cudaError_t attn_init_attributes();
 
-cudaError_t launch_embed(const int* slots, int batch, const int* last_tok, int mask_id, const bf16* embed,
-                         const bf16* gain, int H, float* h, bf16* hg, float* ss,
-                         unsigned long long* keys, cudaStream_t s);
+// weight preparation (dflash_create)
+cudaError_t launch_pack_weight(const bf16* src, void* dst, int N, int K, int n_tiles, int swiglu_I, bool to_f16,
+                               cudaStream_t s);
+cudaError_t launch_gain_f32(const bf16* src, float* dst, int n, cudaStream_t s);
+
+cudaError_t launch_embed(const int* slots, int batch, const int* last_tok, int mask_id, int vocab,
+                         const f16* embed_pk, const float* gain, int H, float* h, f16* hg, float* ss,
+                         unsigned long long* keys, uint32_t* status, cudaStream_t s);
 cudaError_t launch_page_alloc(const int* slots, int batch, const int* n_new, int rows_per_req, int* ctx_len,
                               int* pos0, int* n_pages, int* page_table, int max_pages_per_slot,
                               int* free_stack, int* free_top, int* n_eff, int max_slots, uint32_t* status,
@@ -131,7 +135,7 @@ cudaError_t launch_reset_slot(int slot, int* ctx_len, int* n_pages, int* page_ta
                               int max_pages_per_slot, int* free_stack, int* free_top, cudaStream_t s);
 cudaError_t launch_pool_init(int* free_stack, int* free_top, int max_pages, cudaStream_t s);
 cudaError_t launch_rope_table(float2* tab, int max_pos, int D, float theta, cudaStream_t s);
-cudaError_t launch_read_kv(const KVGeom& kv, int layer, int slot, int pos0, int n, bf16* k_out, bf16* v_out,
+cudaError_t launch_read_kv(const KVGeom& kv, int layer, int slot, int pos0, int n, float* k_out, float* v_out,
                            cudaStream_t s);
 cudaError_t launch_slot_lengths(const int* slots, int batch, const int* ctx_len, int max_slots, int* out,
                                 cudaStream_t s);

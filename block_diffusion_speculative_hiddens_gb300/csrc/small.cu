@@ -1,5 +1,7 @@
 // Small kernels of the round: block embedding, page allocation, acceptance,
 // slot reset, RoPE table, cache read-back and the benchmark's stand-in verify.
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -17,27 +19,69 @@ cudaLaunchConfig_t cfg_of(dim3 grid, dim3 block, cudaStream_t s, cudaLaunchAttri
   return c;
 }
 
-// a3: block = [last_tok, mask x 15]; h = E[block] (fp32 residual stream),
-// hg = bf16(h * g_in0) and per-128-feature sums of squares of h, the form the
-// first layer's QKV GEMM consumes.  Also clears the argmax keys.
-__global__ void k_embed(const int* __restrict__ slots, const int* __restrict__ last_tok, int mask_id,
-                        const bf16* __restrict__ E, const bf16* __restrict__ gain, int H, int M, float* h,
-                        bf16* hg, float* ss, unsigned long long* keys) {
+// Weight preparation: row-major bf16 [N, K] -> packed blocks of 128 rows x 64
+// columns ([tile][k-block]), each in the 128-byte-swizzle image, converted to
+// f16 (exact for every bf16 value in the f16 normal range) or kept bf16.
+// swiglu_I > 0 packs a [2I, K] gate/up matrix so that tile t holds gate rows
+// t*64..t*64+63 then up rows I+t*64..I+t*64+63.  Rows past N are zero.
+__global__ void k_pack_weight(const bf16* __restrict__ src, uint16_t* __restrict__ dst, int N, int K, int n_tiles,
+                              int swiglu_I, int to_f16) {
+  const int KB = K / 64;
+  const long long total = (long long)n_tiles * KB * 128 * 8;  // 16-byte chunks
+  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const int c = (int)(idx & 7);
+    const int r = (int)((idx >> 3) & 127);
+    const long long blk = idx >> 10;
+    const int tile = (int)(blk / KB), kb = (int)(blk % KB);
+    const int row = swiglu_I > 0 ? (r < 64 ? tile * 64 + r : swiglu_I + tile * 64 + (r - 64)) : tile * 128 + r;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (row < N) v = *reinterpret_cast<const uint4*>(src + (size_t)row * K + kb * 64 + c * 8);
+    if (to_f16) {
+      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&v);
+      uint4 o;
+      __half2* h2 = reinterpret_cast<__half2*>(&o);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) h2[i] = __float22half2_rn(__bfloat1622float2(b2[i]));
+      v = o;
+    }
+    *reinterpret_cast<uint4*>(dst + blk * DFL_WBLK_ELEMS + r * 64 + ((c ^ (r & 7)) << 3)) = v;
+  }
+}
+
+__global__ void k_gain_f32(const bf16* __restrict__ src, float* __restrict__ dst, int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) dst[i] = __bfloat162float(src[i]);
+}
+
+// a3: block = [last_tok, mask x 15]; h = E[block] (fp32 residual stream, read
+// from the packed f16 table), hg = f16(h * g_in0) and per-128-feature sums of
+// squares of h, the form the first layer's QKV GEMM consumes.  Also clears
+// the argmax keys.
+__global__ void k_embed(const int* __restrict__ slots, const int* __restrict__ last_tok, int mask_id, int vocab,
+                        const f16* __restrict__ E, const float* __restrict__ gain, int H, int M, float* h, f16* hg,
+                        float* ss, unsigned long long* keys, uint32_t* status) {
   pdl_launch_dependents();
   pdl_wait();
   const int t = blockIdx.x;
   const int b = t / DFL_BLOCK, i = t % DFL_BLOCK;
-  const int tok = i == 0 ? last_tok[b] : mask_id;
+  int tok = i == 0 ? last_tok[b] : mask_id;
+  if (tok < 0 || tok >= vocab) {
+    if (threadIdx.x == 0) dev_error(status, DFLASH_DEV_ARG);
+    tok = mask_id;
+  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-  const bf16* row = E + (size_t)tok * H;
+  const int KB = H / 64;
+  const f16* tile = E + (size_t)(tok >> 7) * KB * DFL_WBLK_ELEMS;
+  const int r = tok & 127;
   for (int part = warp; part < H / 128; part += nw) {
     float sq = 0.f;
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) {
       const int n = part * 128 + lane + 32 * jj;
-      const float v = bf2f(row[n]);
+      const float v = __half2float(tile[(size_t)(n >> 6) * DFL_WBLK_ELEMS + wpack_off(r, n & 63)]);
       h[(size_t)t * H + n] = v;
-      hg[(size_t)t * H + n] = __float2bfloat16(v * bf2f(gain[n]));
+      hg[(size_t)t * H + n] = to_f16(v * gain[n], status);
       sq += v * v;
     }
     sq = warp_sum(sq);
@@ -157,7 +201,7 @@ __global__ void k_rope_table(float2* tab, int max_pos, int D, double theta) {
   tab[idx] = make_float2((float)cos(a), (float)sin(a));
 }
 
-__global__ void k_read_kv(KVGeom kv, int layer, int slot, int pos0, int n, bf16* k_out, bf16* v_out) {
+__global__ void k_read_kv(KVGeom kv, int layer, int slot, int pos0, int n, float* k_out, float* v_out) {
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const int D = kv.D, hkv = kv.hkv;
   if (idx >= (long long)n * hkv * D) return;
@@ -168,13 +212,13 @@ __global__ void k_read_kv(KVGeom kv, int layer, int slot, int pos0, int n, bf16*
   const int pi = pos >> 6;
   int pg = pi < kv.max_pages_per_slot ? kv.page_table[(size_t)slot * kv.max_pages_per_slot + pi] : -1;
   if (pg < 0 || pg >= kv.max_pages) {
-    k_out[idx] = __float2bfloat16(0.f);
-    v_out[idx] = __float2bfloat16(0.f);
+    k_out[idx] = 0.f;
+    v_out[idx] = 0.f;
     return;
   }
   const size_t blk = (size_t)layer * kv.layer_stride + ((size_t)pg * hkv + h) * (64 * D);
-  k_out[idx] = kv.k_pool[blk + k_swz(pos & 63, d)];
-  v_out[idx] = kv.v_pool[blk + v_swz(d, pos & 63)];
+  k_out[idx] = __half2float(kv.k_pool[blk + k_swz(pos & 63, d)]);
+  v_out[idx] = __half2float(kv.v_pool[blk + v_swz(d, pos & 63)]);
 }
 
 __global__ void k_slot_lengths(const int* slots, int batch, const int* ctx_len, int max_slots, int* out) {
@@ -226,15 +270,30 @@ __global__ void k_harness_verify(const int* slots, int batch, const int* draft, 
 
 }  // namespace
 
-cudaError_t launch_embed(const int* slots, int batch, const int* last_tok, int mask_id, const bf16* embed,
-                         const bf16* gain, int H, float* h, bf16* hg, float* ss, unsigned long long* keys,
-                         cudaStream_t s) {
+cudaError_t launch_pack_weight(const bf16* src, void* dst, int N, int K, int n_tiles, int swiglu_I, bool to_f16,
+                               cudaStream_t s) {
+  const long long total = (long long)n_tiles * (K / 64) * 128 * 8;
+  const long long blocks = std::min<long long>((total + 255) / 256, 1LL << 20);
+  k_pack_weight<<<(unsigned)blocks, 256, 0, s>>>(src, static_cast<uint16_t*>(dst), N, K, n_tiles, swiglu_I,
+                                                 to_f16 ? 1 : 0);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gain_f32(const bf16* src, float* dst, int n, cudaStream_t s) {
+  k_gain_f32<<<(n + 255) / 256, 256, 0, s>>>(src, dst, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_embed(const int* slots, int batch, const int* last_tok, int mask_id, int vocab,
+                         const f16* embed_pk, const float* gain, int H, float* h, f16* hg, float* ss,
+                         unsigned long long* keys, uint32_t* status, cudaStream_t s) {
   cudaLaunchAttribute a[1];
   const int M = batch * DFL_BLOCK;
   int threads = (H / 128) * 32;
   if (threads > 1024) threads = 1024;
   cudaLaunchConfig_t c = cfg_of(dim3(M), dim3(threads), s, a);
-  return cudaLaunchKernelEx(&c, k_embed, slots, last_tok, mask_id, embed, gain, H, M, h, hg, ss, keys);
+  return cudaLaunchKernelEx(&c, k_embed, slots, last_tok, mask_id, vocab, embed_pk, gain, H, M, h, hg, ss, keys,
+                            status);
 }
 
 cudaError_t launch_page_alloc(const int* slots, int batch, const int* n_new, int rows_per_req, int* ctx_len,
@@ -273,7 +332,7 @@ cudaError_t launch_rope_table(float2* tab, int max_pos, int D, float theta, cuda
   return cudaGetLastError();
 }
 
-cudaError_t launch_read_kv(const KVGeom& kv, int layer, int slot, int pos0, int n, bf16* k_out, bf16* v_out,
+cudaError_t launch_read_kv(const KVGeom& kv, int layer, int slot, int pos0, int n, float* k_out, float* v_out,
                            cudaStream_t s) {
   const long long tot = (long long)n * kv.hkv * kv.D;
   if (tot == 0) return cudaSuccess;

@@ -59,6 +59,7 @@ typedef enum {
 #define DFLASH_DEV_PAGE      0x04u /* a page-table entry was out of range */
 #define DFLASH_DEV_CAPACITY  0x08u /* page pool or per-slot page table full */
 #define DFLASH_DEV_ARG       0x10u /* slot id or n_new out of range */
+#define DFLASH_DEV_RANGE     0x20u /* an f16 activation or cache entry exceeded 65504 (saturated) */
 
 /* Drafter shape and serving limits.
  * Supported: head_dim in {64,128}; hidden, n_fused*hidden, intermediate and
@@ -88,9 +89,15 @@ typedef struct dflash_config {
 } dflash_config;
 
 /* Device pointers to the drafter weights, all bf16 and row-major; the arrays
- * of per-layer pointers are HOST arrays of n_layers entries.  The library
- * keeps the device pointers (not copies): they must stay valid and unchanged
- * until dflash_destroy. */
+ * of per-layer pointers are HOST arrays of n_layers entries.  They are read
+ * only during dflash_create, which copies everything into the workspace:
+ * matrices repacked into 128x64 tensor-core tiles (converted to f16, which
+ * holds every bf16 weight of magnitude >= 2^-14 exactly and the smaller ones
+ * to within 2^-25; the fusion projection stays bf16) and gains as float32.
+ * The caller may free its buffers once dflash_create returns.  Activations,
+ * the KV cache and the argmax logits are computed with f16 tensor-core
+ * operands and fp32 accumulation; an activation beyond the f16 range sets
+ * DFLASH_DEV_RANGE. */
 typedef struct dflash_weights {
   const void* embed;             /* [V, H]  tied embedding and lm_head */
   const void* fc;                /* [H, n_fused*H] fusion projection (no bias) */
@@ -183,7 +190,8 @@ DFLASH_API int dflash_graph_launch(dflash_handle* h, void* stream);
 /* ---- introspection ------------------------------------------------------ */
 
 /* Copy K and V of `layer` for positions pos0..pos0+n-1 of `slot` into plain
- * [n, hkv, D] bf16 DEVICE buffers (the cache itself is stored pre-swizzled). */
+ * [n, hkv, D] float32 DEVICE buffers (the cache itself is stored as f16,
+ * pre-swizzled). */
 DFLASH_API int dflash_read_kv(dflash_handle* h, int32_t layer, int32_t slot, int32_t pos0, int32_t n,
                    void* k_out, void* v_out, void* stream);
 
