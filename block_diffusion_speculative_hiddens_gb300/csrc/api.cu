@@ -169,10 +169,11 @@ size_t carve(dflash_handle* h, const dflash_config& c, char* base, int num_sms) 
   const long long layer_stride = (long long)c.max_pages * blk;
   const int splits = pick_attn_splits(c, num_sms);
   const int G = hq / hkv;
-  // split-K tile counters: the largest tile count of any split GEMM
-  const int Tmax = std::max(M, R);
-  const int t_tiles_max = ceil_div(Tmax, 16);
-  int tiles = std::max({(c.n_q_heads + 2 * hkv) * D / 128, H / 128, I / 64, c.n_layers * 2 * hkv * D / 128});
+  // split-K tile counters: the largest tile count of any GEMM (all of them,
+  // the lm_head included, use the balanced split)
+  const int t_tiles_max = ceil_div(std::max(M, R), DFL_BN_MAX);
+  int tiles = std::max({(c.n_q_heads + 2 * hkv) * D / 128, H / 128, I / 64, c.n_layers * 2 * hkv * D / 128,
+                        ceil_div(c.vocab, 128)});
   tiles *= t_tiles_max;
 
   dflash_handle tmp;

@@ -243,20 +243,30 @@ __global__ void __launch_bounds__(G * 32) k_attn(const AttnParams p) {
   const float* base = p.ws + (size_t)((b * hkv + kvh) * p.n_splits) * (size_t)(rows * (D + 2));
   const size_t pstride = (size_t)rows * (D + 2);
   for (int r = threadIdx.x; r < rows; r += blockDim.x) {
-    float M = -INFINITY;
-    for (int s = 0; s < p.n_splits; ++s) {
-      const float ls = __ldcg(base + s * pstride + rows * D + rows + r);
-      if (ls > 0.f) M = fmaxf(M, __ldcg(base + s * pstride + rows * D + r));
+    // every split's (max, sum) loaded at once, then combined (n_splits <= 8)
+    float mv[8], lv[8];
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      mv[s] = -INFINITY;
+      lv[s] = 0.f;
+      if (s < p.n_splits) {
+        mv[s] = __ldcg(base + s * pstride + rows * D + r);
+        lv[s] = __ldcg(base + s * pstride + rows * D + rows + r);
+      }
     }
+    float M = -INFINITY;
+#pragma unroll
+    for (int s = 0; s < 8; ++s)
+      if (lv[s] > 0.f) M = fmaxf(M, mv[s]);
     float L = 0.f;
-    for (int s = 0; s < p.n_splits; ++s) {
-      const float ls = __ldcg(base + s * pstride + rows * D + rows + r);
-      const float w = ls > 0.f ? exp2f(__ldcg(base + s * pstride + rows * D + r) - M) : 0.f;
-      wsm[s * rows + r] = w;
-      L += w * ls;
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      const float w = lv[s] > 0.f ? exp2f(mv[s] - M) : 0.f;
+      mv[s] = w;
+      L += w * lv[s];
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
-    for (int s = 0; s < p.n_splits; ++s) wsm[s * rows + r] *= inv;
+    for (int s = 0; s < p.n_splits; ++s) wsm[s * rows + r] = mv[s] * inv;
   }
   __syncthreads();
   for (int e = threadIdx.x; e < rows * D / 4; e += blockDim.x) {

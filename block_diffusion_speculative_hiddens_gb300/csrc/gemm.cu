@@ -407,12 +407,22 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
             if (split) {
 #pragma unroll
               for (int i = 0; i < 16; ++i) v[i] = 0.f;
-              for (long long cc = c_first; cc <= c_last; ++cc) {
-                const int sl = (tile == unit_start(cc, U, G) / KB) ? 0 : 1;
-                const float* w = p.ws + (size_t)(cc * 2 + sl) * (DFL_BN_MAX * 128);
+              // four contributors' loads in flight at once; summed in k order
+              for (long long cc0 = c_first; cc0 <= c_last; cc0 += 4) {
+                float tv[4][16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                  if (col + i < mt) v[i] += __ldcg(w + (size_t)(col + i) * 128 + r);
+                for (int q4 = 0; q4 < 4; ++q4) {
+                  const long long cc = cc0 + q4;
+                  const int sl = (cc <= c_last && tile == unit_start(cc, U, G) / KB) ? 0 : 1;
+                  const float* w = p.ws + (size_t)(cc * 2 + sl) * (DFL_BN_MAX * 128);
+#pragma unroll
+                  for (int i = 0; i < 16; ++i)
+                    tv[q4][i] = (cc <= c_last && col + i < mt) ? __ldcg(w + (size_t)(col + i) * 128 + r) : 0.f;
+                }
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+                  for (int i = 0; i < 16; ++i) v[i] += tv[q4][i];
               }
             } else {
               tmem_ld16(taddr + (uint32_t)col, v);
