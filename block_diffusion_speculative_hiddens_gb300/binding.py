@@ -53,6 +53,7 @@ _SIGS = {
                                      ctypes.c_size_t, ctypes.POINTER(_vp)]),
     "dflash_destroy": (ctypes.c_int, [_vp]),
     "dflash_fuse_inject": (ctypes.c_int, [_vp, _vp, ctypes.c_int32, _vp, ctypes.c_int32, _vp, _vp]),
+    "dflash_fuse_inject_noalloc": (ctypes.c_int, [_vp, _vp, ctypes.c_int32, _vp, ctypes.c_int32, _vp, _vp]),
     "dflash_draft_block": (ctypes.c_int, [_vp, _vp, ctypes.c_int32, _vp, _vp, _vp]),
     "dflash_draft_block_debug": (ctypes.c_int, [_vp, _vp, ctypes.c_int32, _vp, _vp, _vp, _vp, _vp]),
     "dflash_accept_trim": (ctypes.c_int, [_vp, _vp, ctypes.c_int32, _vp, _vp, _vp, _vp, _vp, _vp]),
@@ -173,6 +174,11 @@ class Drafter:
     # ---- the three calls of a round
     def fuse_inject(self, slots, feats, rows_per_req: int, n_new, stream=None):
         _check("dflash_fuse_inject", self.lib.dflash_fuse_inject(
+            self.h, _ptr(slots), slots.numel(), _ptr(feats), rows_per_req, _ptr(n_new), _stream(stream)))
+
+    def fuse_inject_noalloc(self, slots, feats, rows_per_req: int, n_new, stream=None):
+        """dflash_fuse_inject with the library's static scratch (at most 64 rows)."""
+        _check("dflash_fuse_inject_noalloc", self.lib.dflash_fuse_inject_noalloc(
             self.h, _ptr(slots), slots.numel(), _ptr(feats), rows_per_req, _ptr(n_new), _stream(stream)))
 
     def draft_block(self, slots, last_tok, draft, stream=None):

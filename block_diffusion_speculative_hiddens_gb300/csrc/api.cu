@@ -733,3 +733,148 @@ int dflash_harness_verify(dflash_handle* h, const int32_t* slots, int32_t batch,
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// dflash_fuse_inject_noalloc: dflash_fuse_inject with its per-call scratch in
+// a fixed array compiled into the library instead of the handle's workspace.
+//
+// The scratch is the fusion GEMM's output rows (f16) with their sums of
+// squares, and the split-K partial sums and tile counters of the two GEMMs.
+// Limits: batch * rows_per_req <= 64 rows; the GEMMs run on at most 16 CTAs.
+// Size: 16*2*256*128*4 (partials) + 64*8192*2 (rows) + 64*64*4 (sums) +
+// 4096*4 (counters) bytes, about 5.1 MB, held by every device that loads the
+// library until the process exits.
+namespace {
+constexpr int NA_MAX_ROWS = 64;
+constexpr int NA_MAX_CTAS = 16;
+constexpr size_t NA_PART_BYTES = (size_t)NA_MAX_CTAS * 2 * DFL_BN_MAX * 128 * sizeof(float);
+constexpr size_t NA_ROWS_BYTES = (size_t)NA_MAX_ROWS * 8192 * sizeof(f16);
+constexpr size_t NA_SS_BYTES = (size_t)(8192 / 128) * NA_MAX_ROWS * sizeof(float);
+constexpr int NA_MAX_TILES = 4096;
+constexpr size_t NA_CTR_BYTES = (size_t)NA_MAX_TILES * sizeof(unsigned);
+constexpr size_t NA_BYTES = NA_PART_BYTES + NA_ROWS_BYTES + NA_SS_BYTES + NA_CTR_BYTES;
+}  // namespace
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[NA_BYTES];
+
+namespace {
+std::mutex g_na_mutex;
+void* g_na_addr[64] = {};  // device address of g_noalloc_scratch, per device ordinal
+
+// Device address of the static scratch on `dev` (the current device); looked
+// up once per device.
+int noalloc_scratch(int dev, char** out) {
+  if (dev < 0 || dev >= 64) return DFLASH_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_na_mutex);
+  if (!g_na_addr[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p) return cuda_err(e == cudaSuccess ? cudaErrorInvalidSymbol : e);
+    g_na_addr[dev] = p;
+  }
+  *out = static_cast<char*>(g_na_addr[dev]);
+  return DFLASH_OK;
+}
+
+int noalloc_gemm(dflash_handle* h, cudaStream_t s, int mode, const void* const* a, int groups, int a_tile_off,
+                 int n_tiles, int K, const CUtensorMap& B, int M, GemmParams p, uint32_t ab_type, float* part,
+                 unsigned* ctr) {
+  const int BN = ((M + 15) / 16) * 16;  // M <= 64: one token tile
+  p.mode = mode;
+  p.M = M;
+  p.kblocks = K / 64;
+  p.n_tiles = n_tiles;
+  p.t_tiles = 1;
+  p.BN = BN;
+  p.groups = groups;
+  for (int g = 0; g < groups; ++g) p.a[g] = a[g];
+  p.a_tile_off = a_tile_off;
+  p.ab_type = ab_type;
+  p.total_tiles = groups * n_tiles;
+  p.allow_split = 1;
+  p.stages = gemm_pick_stages(BN);
+  int cols = 32;
+  while (cols < 2 * BN) cols *= 2;
+  p.tmem_cols = cols;
+  p.status = h->status;
+  p.ws = part;
+  p.tile_ctr = ctr;
+  p.eps = h->cfg.rms_eps;
+  p.H = h->cfg.hidden;
+  p.hq = h->cfg.n_q_heads;
+  p.hkv = h->cfg.n_kv_heads;
+  p.D = h->cfg.head_dim;
+  p.rope = h->rope;
+  p.max_pos = h->max_pos;
+  if (p.total_tiles > NA_MAX_TILES) return DFLASH_ERR_CAPACITY;
+  const long long units = (long long)p.total_tiles * p.kblocks;
+  const int grid = (int)std::min<long long>(units, NA_MAX_CTAS);
+  h->launches++;
+  return cuda_err(gemm_launch(B, p, grid, s, h->pdl));
+}
+}  // namespace
+
+extern "C" int dflash_fuse_inject_noalloc(dflash_handle* h, const int32_t* slots, int32_t batch, const void* feats,
+                                          int32_t rows_per_req, const int32_t* n_new, void* stream) {
+  if (!h || batch < 0 || batch > h->cfg.max_batch || rows_per_req < 0) return DFLASH_ERR_INVALID_ARG;
+  if ((long long)batch * rows_per_req > NA_MAX_ROWS) {
+    fprintf(stderr, "[dflash] dflash_fuse_inject_noalloc: %lld rows exceed its static scratch limit of %d\n",
+            (long long)batch * rows_per_req, NA_MAX_ROWS);
+    return DFLASH_ERR_CAPACITY;
+  }
+  if (batch == 0) return DFLASH_OK;
+  if (!slots || !n_new) return DFLASH_ERR_INVALID_ARG;
+  if (rows_per_req > 0 && !feats) return DFLASH_ERR_INVALID_ARG;
+  if (cudaSetDevice(h->cfg.device) != cudaSuccess) return DFLASH_ERR_CUDA;
+  char* base = nullptr;
+  int rc = noalloc_scratch(h->cfg.device, &base);
+  if (rc) return rc;
+  float* part = reinterpret_cast<float*>(base);
+  f16* rows = reinterpret_cast<f16*>(base + NA_PART_BYTES);
+  float* ss = reinterpret_cast<float*>(base + NA_PART_BYTES + NA_ROWS_BYTES);
+  unsigned* ctr = reinterpret_cast<unsigned*>(base + NA_PART_BYTES + NA_ROWS_BYTES + NA_SS_BYTES);
+
+  cudaStream_t s = (cudaStream_t)stream;
+  const dflash_config& c = h->cfg;
+  const int H = c.hidden, D = c.head_dim, hkv = c.n_kv_heads;
+  // tile counters must start at zero (the kernels also leave them at zero)
+  rc = cuda_err(cudaMemsetAsync(ctr, 0, NA_CTR_BYTES, s));
+  if (rc) return rc;
+  h->launches++;
+  rc = cuda_err(launch_page_alloc(slots, batch, n_new, rows_per_req, h->ctx_len, h->pos0, h->n_pages,
+                                  h->page_table, c.max_pages_per_slot, h->free_stack, h->free_top, h->n_eff,
+                                  c.max_slots, h->status, s));
+  if (rc || rows_per_req == 0) return rc;
+  const int R = batch * rows_per_req;
+  const uint32_t BN = (uint32_t)(((R + 15) / 16) * 16);
+  CUtensorMap tm_feats, tm_rows;
+  if (!make_tmap(&tm_feats, feats, R, (uint64_t)c.n_fused * H, BN, true)) return DFLASH_ERR_INVALID_ARG;
+  if (!make_tmap(&tm_rows, rows, R, H, BN)) return DFLASH_ERR_CUDA;
+  {
+    GemmParams p = {};
+    p.out = rows;
+    p.gain = h->fc_norm;
+    p.ss_out = ss;
+    p.N = H;
+    const void* a = h->fc_pk;
+    rc = noalloc_gemm(h, s, GM_FC, &a, 1, 0, H / 128, c.n_fused * H, tm_feats, R, p, 1, part, ctr);
+    if (rc) return rc;
+  }
+  {
+    GemmParams p = {};
+    p.ss_in = ss;
+    p.ss_parts = H / 128;
+    p.N = 2 * hkv * D;
+    for (int l = 0; l < c.n_layers; ++l) p.kn_gain[l] = h->k_norm[l];
+    p.kv = kv_geom(h);
+    p.slots = slots;
+    p.pos0 = h->pos0;
+    p.n_eff = h->n_eff;
+    p.rows_per_req = rows_per_req;
+    const void* a[DFL_MAX_LAYERS];
+    for (int l = 0; l < c.n_layers; ++l) a[l] = h->wqkv_pk[l];
+    rc = noalloc_gemm(h, s, GM_INJECT, a, c.n_layers, c.n_q_heads * D / 128, p.N / 128, H, tm_rows, R, p, 0, part,
+                      ctr);
+  }
+  return rc;
+}

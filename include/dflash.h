@@ -168,6 +168,28 @@ DFLASH_API int dflash_accept_trim(dflash_handle* h, const int32_t* slots, int32_
                        const int32_t* target, int32_t* accept_len, int32_t* bonus,
                        int32_t* ctx_len, void* stream);
 
+/* Same as dflash_fuse_inject, for callers that cannot set device memory
+ * aside at call time -- e.g. a workspace sized with max_rows = 0 because the
+ * process's device memory is owned by another allocator, or code that must
+ * not grow any pool while serving.  The per-call scratch (the fused feature
+ * rows, their norm statistics, the split-K partial sums and tile counters)
+ * lives in one static device array compiled into the library (about 5.1 MB,
+ * held by every GPU that loads the library until the process exits); the
+ * caller passes only the inputs and the handle whose cache receives the
+ * output.  Nothing is allocated (no cudaMalloc/cudaFree).  There is no
+ * counterpart on the pages; it is a deployment variant.
+ *   Limit: batch * rows_per_req <= 64 (a round's rows for up to 4 requests,
+ *   or a prefill fed in chunks of 64); larger calls return
+ *   DFLASH_ERR_CAPACITY and print the limit to stderr.  The two GEMMs use at
+ *   most 16 CTAs, so this variant is slower than dflash_fuse_inject.
+ *   The first call on a device looks up the array's device address; make
+ *   that first call before any stream capture.  All calls in the process
+ *   share the one array per device: calls that can overlap on the GPU (other
+ *   streams, other handles on the same device) race and must be ordered by
+ *   the caller.  The tile counters are cleared at the start of every call. */
+DFLASH_API int dflash_fuse_inject_noalloc(dflash_handle* h, const int32_t* slots, int32_t batch, const void* feats,
+                                          int32_t rows_per_req, const int32_t* n_new, void* stream);
+
 /* Free a slot's pages and set its length to 0 (stream-ordered). */
 DFLASH_API int dflash_reset_slot(dflash_handle* h, int32_t slot, void* stream);
 
