@@ -35,8 +35,13 @@ def _newer(target: str, deps) -> bool:
     return all(os.path.getmtime(d) <= t for d in deps)
 
 
-def build(verbose: bool = False, ptxas_info: bool = False, force: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, ptxas_info: bool = False, force: bool = False, defines=(),
+          out: str = None, build_dir: str = None) -> str:
+    """Compile and link libdflash.so; `defines` (e.g. "DFL_GEMM_MAX_STAGES=8")
+    with `out`/`build_dir` produce a variant library elsewhere."""
+    lib_path = out or LIB
+    bdir = build_dir or BUILD
+    os.makedirs(bdir, exist_ok=True)
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
     headers.append(os.path.join(os.path.dirname(PKG), "include", "dflash.h"))
     cc = nvcc()
@@ -44,10 +49,10 @@ def build(verbose: bool = False, ptxas_info: bool = False, force: bool = False) 
 
     def compile_one(src):
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD, src.replace(".cu", ".o"))
-        if not force and not ptxas_info and _newer(o, [s] + headers):
+        o = os.path.join(bdir, src.replace(".cu", ".o"))
+        if not force and not ptxas_info and not defines and _newer(o, [s] + headers):
             return o, ""
-        cmd = [cc, *ARCH, *FLAGS, *extra, "-c", s, "-o", o]
+        cmd = [cc, *ARCH, *FLAGS, *extra, *[f"-D{d}" for d in defines], "-c", s, "-o", o]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
@@ -60,13 +65,13 @@ def build(verbose: bool = False, ptxas_info: bool = False, force: bool = False) 
         for _, log in results:
             if log:
                 sys.stderr.write(log)
-    if force or ptxas_info or not _newer(LIB, objs):
-        cmd = [cc, *ARCH, "-shared", "-o", LIB + ".tmp", *objs]
+    if force or ptxas_info or defines or not _newer(lib_path, objs):
+        cmd = [cc, *ARCH, "-shared", "-o", lib_path + ".tmp", *objs]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(LIB + ".tmp", LIB)
-    return LIB
+        os.replace(lib_path + ".tmp", lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

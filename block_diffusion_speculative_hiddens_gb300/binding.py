@@ -20,7 +20,7 @@ OK = 0
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported shape", 3: "capacity exceeded",
           4: "CUDA error", 5: "device-side check failed", 6: "workspace too small or misaligned"}
 DEV_TIMEOUT, DEV_NAN, DEV_PAGE, DEV_CAPACITY, DEV_ARG, DEV_RANGE = 0x01, 0x02, 0x04, 0x08, 0x10, 0x20
-KID_LM_HEAD, KID_GATE_UP, KID_ATTENTION, KID_DOWN, KID_QKV = 1, 2, 3, 4, 5
+KID_LM_HEAD, KID_GATE_UP, KID_ATTENTION, KID_DOWN, KID_QKV, KID_WO, KID_FC, KID_INJECT = 1, 2, 3, 4, 5, 6, 7, 8
 
 _c_int_p = ctypes.POINTER(ctypes.c_int32)
 _vp = ctypes.c_void_p
@@ -69,6 +69,7 @@ _SIGS = {
     "dflash_probe_arm": (ctypes.c_int, [_vp, ctypes.c_int32, ctypes.c_int32]),
     "dflash_probe_read": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_float), ctypes.c_int32, _c_int_p]),
     "dflash_launch_count": (ctypes.c_uint64, [_vp]),
+    "dflash_trace_arm": (ctypes.c_int, [_vp, ctypes.c_int32, _vp, ctypes.c_int32]),
     "dflash_harness_verify": (ctypes.c_int, [_vp, _vp, ctypes.c_int32, _vp, _vp, _vp, ctypes.c_int32, _vp,
                                              _vp, _vp, ctypes.c_int32, _vp, _vp]),
 }
@@ -240,6 +241,11 @@ class Drafter:
         n = ctypes.c_int32(0)
         _check("dflash_probe_read", self.lib.dflash_probe_read(self.h, buf, cap, ctypes.byref(n)))
         return list(buf[:n.value])
+
+    def trace_arm(self, kernel_id: int, buf=None, cap_ctas: int = 0):
+        """Arm a per-CTA timeline of the next launch of a GEMM kernel; buf is an
+        int64 device tensor [cap_ctas, 8]."""
+        _check("dflash_trace_arm", self.lib.dflash_trace_arm(self.h, kernel_id, _ptr(buf), cap_ctas))
 
     def launch_count(self) -> int:
         return int(self.lib.dflash_launch_count(self.h))

@@ -72,6 +72,12 @@ struct Probe {
   std::vector<cudaEvent_t> ev;  // 2*n
 };
 
+struct Trace {
+  int kid = 0;
+  unsigned long long* buf = nullptr;
+  int cap = 0;  // CTAs the buffer holds
+};
+
 }  // namespace
 
 struct dflash_handle {
@@ -119,6 +125,7 @@ struct dflash_handle {
   bool pdl = true;
   uint64_t launches = 0;
   Probe probe;
+  Trace trace;
   cudaGraph_t graph = nullptr;
   cudaGraphExec_t exec = nullptr;
 };
@@ -240,20 +247,31 @@ inline int cuda_err(cudaError_t e) {
   return DFLASH_ERR_CUDA;
 }
 
+// Event pair around one launch: event-record nodes when the stream is being
+// captured, plain records otherwise.
 struct ProbeScope {
   dflash_handle* h;
   cudaStream_t s;
   bool on = false;
+  bool capturing = false;
   int idx = 0;
+  void record(cudaEvent_t e) {
+    if (capturing)
+      cudaEventRecordWithFlags(e, s, cudaEventRecordExternal);
+    else
+      cudaEventRecord(e, s);
+  }
   ProbeScope(dflash_handle* h_, int kid, cudaStream_t s_) : h(h_), s(s_) {
-    if (h->probe.kid == kid && h->probe.next < h->probe.n) {
+    if (kid && h->probe.kid == kid && h->probe.next < h->probe.n) {
       on = true;
       idx = h->probe.next++;
-      cudaEventRecordWithFlags(h->probe.ev[2 * idx], s, cudaEventRecordExternal);
+      cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+      capturing = cudaStreamIsCapturing(s, &st) == cudaSuccess && st == cudaStreamCaptureStatusActive;
+      record(h->probe.ev[2 * idx]);
     }
   }
   ~ProbeScope() {
-    if (on) cudaEventRecordWithFlags(h->probe.ev[2 * idx + 1], s, cudaEventRecordExternal);
+    if (on) record(h->probe.ev[2 * idx + 1]);
   }
 };
 
@@ -294,6 +312,10 @@ int run_gemm(dflash_handle* h, cudaStream_t s, int mode, const void* const* a, i
   if (allow_split && p.total_tiles > h->max_tiles) return DFLASH_ERR_SHAPE;
   const long long units = allow_split ? (long long)p.total_tiles * p.kblocks : p.total_tiles;
   const int grid = (int)std::min<long long>(units, h->num_sms);
+  if (kid && h->trace.kid == kid && h->trace.buf && grid <= h->trace.cap) {
+    p.trace = h->trace.buf;  // one launch only
+    h->trace.kid = 0;
+  }
   ProbeScope ps(h, kid, s);
   h->launches++;
   return cuda_err(gemm_launch(B, p, grid, s, h->pdl));
@@ -390,7 +412,7 @@ int draft_impl(dflash_handle* h, const int32_t* slots, int32_t batch, const int3
       p.ss_out = h->ss_a;
       p.N = H;
       const void* a = h->wo_pk[l];
-      rc = run_gemm(h, s, GM_RESID, &a, 1, 0, H / 128, hq * D, h->tm_o, M, p, true, 0);
+      rc = run_gemm(h, s, GM_RESID, &a, 1, 0, H / 128, hq * D, h->tm_o, M, p, true, 0, DFLASH_KID_WO);
       if (rc) return rc;
     }
     {  // gate/up projection + SiLU gating
@@ -564,7 +586,7 @@ int dflash_fuse_inject(dflash_handle* h, const int32_t* slots, int32_t batch, co
     p.ss_out = h->ss_c;
     p.N = H;
     const void* a = h->fc_pk;
-    rc = run_gemm(h, s, GM_FC, &a, 1, 0, H / 128, c.n_fused * H, tm_feats, R, p, true, 1);
+    rc = run_gemm(h, s, GM_FC, &a, 1, 0, H / 128, c.n_fused * H, tm_feats, R, p, true, 1, DFLASH_KID_FC);
     if (rc) return rc;
   }
   {  // every layer's K/V projection of the fused feature, k-norm, RoPE, paged append
@@ -580,7 +602,8 @@ int dflash_fuse_inject(dflash_handle* h, const int32_t* slots, int32_t batch, co
     p.rows_per_req = rows_per_req;
     const void* a[DFL_MAX_LAYERS];
     for (int l = 0; l < c.n_layers; ++l) a[l] = h->wqkv_pk[l];
-    rc = run_gemm(h, s, GM_INJECT, a, c.n_layers, c.n_q_heads * D / 128, p.N / 128, H, h->tm_cg, R, p, true, 0);
+    rc = run_gemm(h, s, GM_INJECT, a, c.n_layers, c.n_q_heads * D / 128, p.N / 128, H, h->tm_cg, R, p, true, 0,
+                  DFLASH_KID_INJECT);
     if (rc) return rc;
   }
   return DFLASH_OK;
@@ -713,6 +736,14 @@ int dflash_probe_read(dflash_handle* h, float* ms_out, int32_t cap, int32_t* n_o
 }
 
 uint64_t dflash_launch_count(dflash_handle* h) { return h ? h->launches : 0; }
+
+int dflash_trace_arm(dflash_handle* h, int32_t kernel_id, unsigned long long* buf, int32_t cap_ctas) {
+  if (!h || (kernel_id && (!buf || cap_ctas <= 0))) return DFLASH_ERR_INVALID_ARG;
+  h->trace.kid = kernel_id;
+  h->trace.buf = buf;
+  h->trace.cap = cap_ctas;
+  return DFLASH_OK;
+}
 
 int dflash_harness_verify(dflash_handle* h, const int32_t* slots, int32_t batch, const int32_t* draft,
                           const int32_t* match, const int32_t* offs, int32_t rounds_cap, int32_t* round_ctr,

@@ -28,6 +28,17 @@
 #include "common.cuh"
 #include "internal.h"
 
+// Build-time tuning knobs (the defaults are the shipped configuration).
+#ifndef DFL_GEMM_MAX_STAGES
+#define DFL_GEMM_MAX_STAGES 12
+#endif
+#ifndef DFL_GEMM_L2_HINT
+#define DFL_GEMM_L2_HINT 1
+#endif
+#ifndef DFL_GEMM_A_CHUNKS  // bulk copies per 16 KB weight block
+#define DFL_GEMM_A_CHUNKS 1
+#endif
+
 namespace {
 
 constexpr int A_STAGE_BYTES = 128 * 128;  // 128 rows x 64 16-bit values
@@ -38,23 +49,22 @@ DFL_DEV long long unit_start(long long c, long long U, long long G) { return c *
 // CTA whose unit range [unit_start(c), unit_start(c+1)) contains unit u.
 DFL_DEV long long cta_of_unit(long long u, long long U, long long G) { return ((u + 1) * G + U - 1) / U - 1; }
 
-DFL_DEV float norm_scale(const float* ss, int parts, int M, int t, int width, float eps, int lane) {
-  float s = 0.f;
-  for (int i = lane; i < parts; i += 32) s += ss[(size_t)i * M + t];
-  s = warp_sum(s);
-  return rsqrtf(s / (float)width + eps);
+// Timeline stamps (p.trace non-null): 0 entry, 1 set-up done, 2 first weight
+// stage landed, 3 last MMA issued, 4 epilogue done, 5 exit, 6 units, 7 SM id.
+DFL_DEV void trace_at(const GemmParams& p, int ev, unsigned long long v) {
+  if (p.trace) p.trace[(size_t)blockIdx.x * 8 + ev] = v;
 }
 
 // Head RMSNorm + RoPE on the 4 values a lane holds (rows lane, lane+32,
-// lane+64, lane+96 of a 128-row tile).  D = 128: one head, RoPE pairs (0,2),
-// (1,3).  D = 64: two heads (rows 0-63, 64-127), pairs (0,1) and (2,3).
-DFL_DEV void head_norm_rope(float* x, const float* gain, const float2* rope_row, int D, float eps, int lane) {
+// lane+64, lane+96 of a 128-row tile); c0/c1 are the (cos, sin) of RoPE
+// frequencies lane and lane+32.  D = 128: one head, RoPE pairs (0,2), (1,3).
+// D = 64: two heads (rows 0-63, 64-127), pairs (0,1) and (2,3), frequency lane.
+DFL_DEV void head_norm_rope(float* x, const float* gain, float2 c0, float2 c1, int D, float eps, int lane) {
   if (D == 128) {
     float ss = warp_sum(x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3]);
     const float inv = rsqrtf(ss / 128.f + eps);
 #pragma unroll
     for (int j = 0; j < 4; ++j) x[j] *= inv * gain[lane + 32 * j];
-    const float2 c0 = rope_row[lane], c1 = rope_row[lane + 32];
     const float a0 = x[0], b0 = x[2], a1 = x[1], b1 = x[3];
     x[0] = a0 * c0.x - b0 * c0.y;
     x[2] = b0 * c0.x + a0 * c0.y;
@@ -69,141 +79,210 @@ DFL_DEV void head_norm_rope(float* x, const float* gain, const float2* rope_row,
     x[1] *= ia * g1;
     x[2] *= ib * g0;
     x[3] *= ib * g1;
-    const float2 c = rope_row[lane];
     const float a0 = x[0], b0 = x[1], a1 = x[2], b1 = x[3];
-    x[0] = a0 * c.x - b0 * c.y;
-    x[1] = b0 * c.x + a0 * c.y;
-    x[2] = a1 * c.x - b1 * c.y;
-    x[3] = b1 * c.x + a1 * c.y;
+    x[0] = a0 * c0.x - b0 * c0.y;
+    x[1] = b0 * c0.x + a0 * c0.y;
+    x[2] = a1 * c0.x - b1 * c0.y;
+    x[3] = b1 * c0.x + a1 * c0.y;
   }
 }
 
-DFL_DEV void write_k(const GemmParams& p, int layer, int slot, int pos, int kh, int d, float v) {
-  const int pg_i = pos >> 6;
-  if (pg_i >= p.kv.max_pages_per_slot) { dev_error(p.status, DFLASH_DEV_PAGE); return; }
-  const int pg = p.kv.page_table[(size_t)slot * p.kv.max_pages_per_slot + pg_i];
-  if (pg < 0 || pg >= p.kv.max_pages) { dev_error(p.status, DFLASH_DEV_PAGE); return; }
-  f16* blk = p.kv.k_pool + (size_t)layer * p.kv.layer_stride + ((size_t)pg * p.kv.hkv + kh) * (64 * p.kv.D);
-  blk[k_swz(pos & 63, d)] = to_f16(v, p.status);
+// Page of position `pos` of `slot`, or -1 when it has none.
+DFL_DEV int page_of(const GemmParams& p, int slot, int pos) {
+  const int pi = pos >> 6;
+  if (pi >= p.kv.max_pages_per_slot) return -1;
+  const int pg = p.kv.page_table[(size_t)slot * p.kv.max_pages_per_slot + pi];
+  return (pg < 0 || pg >= p.kv.max_pages) ? -1 : pg;
 }
-DFL_DEV void write_v(const GemmParams& p, int layer, int slot, int pos, int kh, int d, float v) {
-  const int pg_i = pos >> 6;
-  if (pg_i >= p.kv.max_pages_per_slot) { dev_error(p.status, DFLASH_DEV_PAGE); return; }
-  const int pg = p.kv.page_table[(size_t)slot * p.kv.max_pages_per_slot + pg_i];
-  if (pg < 0 || pg >= p.kv.max_pages) { dev_error(p.status, DFLASH_DEV_PAGE); return; }
-  f16* blk = p.kv.v_pool + (size_t)layer * p.kv.layer_stride + ((size_t)pg * p.kv.hkv + kh) * (64 * p.kv.D);
-  blk[v_swz(d, pos & 63)] = to_f16(v, p.status);
-}
+
+constexpr int EPI_TOK = 4;  // tokens per warp whose inputs are gathered together
 
 // Final epilogue for tokens t_first .. t_first+ntok-1 of `tile`; staging
 // stg[j][r] holds the fully reduced fp32 accumulators.  Epilogue warp ew
-// handles tokens j = ew, ew+4, ...; lane holds rows lane + 32*jj.
+// handles tokens j = ew, ew+4, ...; lane holds rows lane + 32*jj.  Every
+// global input of a warp's next EPI_TOK tokens is loaded before any is used,
+// so the dependent-load chain costs a few round trips per tile, not per token.
 template <int MODE>
 DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, const float* stg, int ew, int lane) {
   const int tt_all = tile / p.t_tiles;       // (group, n-tile)
   const int group = tt_all / p.n_tiles;
   const int nt = tt_all % p.n_tiles;
-  for (int j = ew; j < ntok; j += 4) {
-    const int t = t_first + j;
-    const float* row = stg + j * 128;
-    float x[4] = {row[lane], row[lane + 32], row[lane + 64], row[lane + 96]};
-
-    if (MODE == GM_RESID || MODE == GM_FC) {
-      const int n0 = nt * 128;
-      float sq = 0.f;
+  for (int j0 = ew; j0 < ntok; j0 += 4 * EPI_TOK) {
+    bool ok[EPI_TOK];
+    int tq[EPI_TOK];
+    float x[EPI_TOK][4];
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        const int n = n0 + lane + 32 * jj;
-        const size_t o = (size_t)t * p.N + n;
-        float hv = x[jj];
-        if (MODE == GM_RESID) {
-          hv += p.h[o];
-          p.h[o] = hv;
+    for (int q = 0; q < EPI_TOK; ++q) {
+      const int j = j0 + 4 * q;
+      ok[q] = j < ntok;  // warp-uniform
+      tq[q] = t_first + j;
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) x[q][jj] = ok[q] ? stg[j * 128 + lane + 32 * jj] : 0.f;
+    }
+
+    if constexpr (MODE == GM_RESID || MODE == GM_FC) {
+      const int n0 = nt * 128;
+      float hv[EPI_TOK][4];
+#pragma unroll
+      for (int q = 0; q < EPI_TOK; ++q)
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj)
+          hv[q][jj] = (MODE == GM_RESID && ok[q]) ? p.h[(size_t)tq[q] * p.N + n0 + lane + 32 * jj] : 0.f;
+#pragma unroll
+      for (int q = 0; q < EPI_TOK; ++q) {
+        if (!ok[q]) continue;
+        float sq = 0.f;
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const int n = n0 + lane + 32 * jj;
+          const size_t o = (size_t)tq[q] * p.N + n;
+          const float v = x[q][jj] + hv[q][jj];
+          if (MODE == GM_RESID) p.h[o] = v;
+          p.out[o] = to_f16(v * p.gain[n], p.status);
+          sq += v * v;
         }
-        p.out[o] = to_f16(hv * p.gain[n], p.status);
-        sq += hv * hv;
+        sq = warp_sum(sq);
+        if (lane == 0) p.ss_out[(size_t)nt * p.M + tq[q]] = sq;
       }
-      sq = warp_sum(sq);
-      if (lane == 0) p.ss_out[(size_t)nt * p.M + t] = sq;
-    } else if (MODE == GM_SWIGLU) {
-      const float s = norm_scale(p.ss_in, p.ss_parts, p.M, t, p.H, p.eps, lane);
+    } else {
+    // per-token RMSNorm scale of this GEMM's input
+    float s[EPI_TOK];
+    {
+      float ssq[EPI_TOK];
+#pragma unroll
+      for (int q = 0; q < EPI_TOK; ++q) {
+        ssq[q] = 0.f;
+        if (ok[q])
+          for (int i = lane; i < p.ss_parts; i += 32) ssq[q] += p.ss_in[(size_t)i * p.M + tq[q]];
+      }
+#pragma unroll
+      for (int q = 0; q < EPI_TOK; ++q) s[q] = rsqrtf(warp_sum(ssq[q]) / (float)p.H + p.eps);
+    }
+
+    if (MODE == GM_SWIGLU) {
       const int f0 = nt * 64;
 #pragma unroll
-      for (int jj = 0; jj < 2; ++jj) {
-        const float g = x[jj] * s, u = x[jj + 2] * s;
-        const float a = g / (1.f + __expf(-g)) * u;
-        p.out[(size_t)t * p.N + f0 + lane + 32 * jj] = to_f16(a, p.status);
+      for (int q = 0; q < EPI_TOK; ++q) {
+        if (!ok[q]) continue;
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+          const float g = x[q][jj] * s[q], u = x[q][jj + 2] * s[q];
+          const float a = g / (1.f + __expf(-g)) * u;
+          p.out[(size_t)tq[q] * p.N + f0 + lane + 32 * jj] = to_f16(a, p.status);
+        }
       }
     } else if (MODE == GM_ARGMAX) {
-      const float s = norm_scale(p.ss_in, p.ss_parts, p.M, t, p.H, p.eps, lane);
       const int n0 = nt * 128;
-      unsigned long long best = 0ull;
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        const int n = n0 + lane + 32 * jj;
-        if (n < p.N) {
-          const float v = x[jj] * s;
-          if (v != v) {
-            dev_error(p.status, DFLASH_DEV_NAN);
-            continue;
+      for (int q = 0; q < EPI_TOK; ++q) {
+        if (!ok[q]) continue;
+        unsigned long long best = 0ull;
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const int n = n0 + lane + 32 * jj;
+          if (n < p.N) {
+            const float v = x[q][jj] * s[q];
+            if (v != v) {
+              dev_error(p.status, DFLASH_DEV_NAN);
+              continue;
+            }
+            if (p.logits) p.logits[(size_t)tq[q] * p.N + n] = v;
+            const unsigned long long k = argmax_key(v, (uint32_t)n);
+            best = k > best ? k : best;
           }
-          if (p.logits) p.logits[(size_t)t * p.N + n] = v;
-          const unsigned long long k = argmax_key(v, (uint32_t)n);
-          best = k > best ? k : best;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
+          best = other > best ? other : best;
+        }
+        if (lane == 0 && best) atomicMax(p.keys + tq[q], best);
+      }
+    } else if (MODE == GM_QKV || MODE == GM_INJECT) {
+      const int D = p.D;
+      int n0, kind, layer;
+      const float* kgain;
+      if (MODE == GM_QKV) {
+        n0 = nt * 128;
+        kind = n0 < p.hq * D ? 0 : (n0 < (p.hq + p.hkv) * D ? 1 : 2);
+        layer = p.layer;
+        kgain = kind == 0 ? p.qn_gain : p.kn_gain[0];
+      } else {
+        n0 = nt * 128 + p.hq * D;  // row index in this layer's wqkv
+        kind = n0 < (p.hq + p.hkv) * D ? 1 : 2;
+        layer = group;
+        kgain = p.kn_gain[group];
+      }
+      // gather: request -> slot (and row count) -> position -> RoPE row, page
+      int slot[EPI_TOK], pos[EPI_TOK], pg[EPI_TOK];
+      bool live[EPI_TOK];
+      float2 c0[EPI_TOK], c1[EPI_TOK];
+#pragma unroll
+      for (int q = 0; q < EPI_TOK; ++q) {
+        const int t = ok[q] ? tq[q] : t_first;
+        const int b = MODE == GM_QKV ? t / DFL_BLOCK : t / p.rows_per_req;
+        slot[q] = p.slots[b];
+        pos[q] = MODE == GM_QKV ? 0 : p.n_eff[b];  // inject: row count, read together with the slot
+      }
+#pragma unroll
+      for (int q = 0; q < EPI_TOK; ++q) {
+        const int t = ok[q] ? tq[q] : t_first;
+        if (MODE == GM_QKV) {
+          live[q] = ok[q];
+          pos[q] = p.ctx_len[slot[q]] + (t % DFL_BLOCK);
+        } else {
+          const int i = t % p.rows_per_req;
+          live[q] = ok[q] && i < pos[q];
+          pos[q] = p.pos0[slot[q]] + i;
+        }
+        if (live[q] && pos[q] >= p.max_pos) {
+          dev_error(p.status, DFLASH_DEV_CAPACITY);
+          live[q] = false;
         }
       }
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
-        best = other > best ? other : best;
+      for (int q = 0; q < EPI_TOK; ++q) {
+        c0[q] = c1[q] = make_float2(1.f, 0.f);
+        pg[q] = -1;
+        if (live[q]) {
+          if (kind < 2) {
+            const float2* row = p.rope + (size_t)pos[q] * (D / 2);
+            c0[q] = row[lane];
+            if (D == 128) c1[q] = row[lane + 32];
+          }
+          if (kind > 0) pg[q] = page_of(p, slot[q], pos[q]);
+        }
       }
-      if (lane == 0 && best) atomicMax(p.keys + t, best);
-    } else if (MODE == GM_QKV || MODE == GM_INJECT) {
-      const int D = p.D;
-      int slot, pos, layer, kind, n0;
-      const float* kgain;
-      float s;
-      if (MODE == GM_QKV) {
-        const int b = t / DFL_BLOCK;
-        slot = p.slots[b];
-        pos = p.ctx_len[slot] + (t % DFL_BLOCK);
-        layer = p.layer;
-        n0 = nt * 128;
-        kind = n0 < p.hq * D ? 0 : (n0 < (p.hq + p.hkv) * D ? 1 : 2);
-        kgain = kind == 0 ? p.qn_gain : p.kn_gain[0];
-      } else {
-        const int b = t / p.rows_per_req;
-        const int i = t % p.rows_per_req;
-        if (i >= p.n_eff[b]) continue;  // warp-uniform: one token per warp
-        slot = p.slots[b];
-        pos = p.pos0[slot] + i;
-        layer = group;
-        n0 = nt * 128 + p.hq * D;  // row index in this layer's wqkv
-        kind = n0 < (p.hq + p.hkv) * D ? 1 : 2;
-        kgain = p.kn_gain[group];
-      }
-      s = norm_scale(p.ss_in, p.ss_parts, p.M, t, p.H, p.eps, lane);
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj) x[jj] *= s;
-      if (pos >= p.max_pos) {
-        dev_error(p.status, DFLASH_DEV_CAPACITY);
-        continue;
-      }
-      if (kind < 2) head_norm_rope(x, kgain, p.rope + (size_t)pos * (D / 2), D, p.eps, lane);
+      for (int q = 0; q < EPI_TOK; ++q) {
+        if (!live[q]) continue;  // warp-uniform
+        float xv[4];
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        const int n = n0 + lane + 32 * jj;
+        for (int jj = 0; jj < 4; ++jj) xv[jj] = x[q][jj] * s[q];
+        if (kind < 2) head_norm_rope(xv, kgain, c0[q], c1[q], D, p.eps, lane);
         if (kind == 0) {
-          p.out[(size_t)t * (p.hq * D) + n] = to_f16(x[jj], p.status);
-        } else if (kind == 1) {
-          const int m = n - p.hq * D;
-          write_k(p, layer, slot, pos, m / D, m % D, x[jj]);
-        } else {
-          const int m = n - (p.hq + p.hkv) * D;
-          write_v(p, layer, slot, pos, m / D, m % D, x[jj]);
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj)
+            p.out[(size_t)tq[q] * (p.hq * D) + n0 + lane + 32 * jj] = to_f16(xv[jj], p.status);
+          continue;
+        }
+        if (pg[q] < 0) {
+          dev_error(p.status, DFLASH_DEV_PAGE);
+          continue;
+        }
+        const int base = (kind == 1 ? p.hq : p.hq + p.hkv) * D;
+        f16* pool = kind == 1 ? p.kv.k_pool : p.kv.v_pool;
+        const int row = pos[q] & 63;
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const int m = n0 + lane + 32 * jj - base;
+          const int kh = m / D, d = m % D;
+          f16* blk = pool + (size_t)layer * p.kv.layer_stride + ((size_t)pg[q] * p.kv.hkv + kh) * (64 * D);
+          blk[kind == 1 ? k_swz(row, d) : v_swz(d, row)] = to_f16(xv[jj], p.status);
         }
       }
     }
+    }  // not RESID/FC
   }
 }
 
@@ -227,6 +306,7 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t ncols = (uint32_t)p.tmem_cols;
+  if (threadIdx.x == 0) trace_at(p, 0, globaltimer());
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
@@ -249,6 +329,7 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   pdl_launch_dependents();
+  if (threadIdx.x == 0) trace_at(p, 1, globaltimer());
 
   const long long KB = p.kblocks;
   const long long G = gridDim.x, c = blockIdx.x;
@@ -266,48 +347,75 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer
+    // Per stage the single producer thread only bumps counters and issues
+    // two copies; every division happens once per tile.
     if (lane == 0) {
       prefetch_tmap(&tmB);
-      const bool stream_w = p.t_tiles == 1;
+      const bool hint = DFL_GEMM_L2_HINT && p.t_tiles == 1;
       const uint64_t pol = policy_evict_first();
-      auto load_a = [&](int s, long long u) {
-        const int tile = (int)(u / KB), kb = (int)(u % KB);
+      const int KBi = p.kblocks;
+      const int n_units = (int)(u1 - u0);
+      int tile = (int)(u0 / KB), kb = (int)(u0 % KB), tt = 0;
+      const uint16_t* a_ptr = nullptr;
+      auto tile_base = [&]() {
         const int tt_all = tile / p.t_tiles;
         const int g = tt_all / p.n_tiles, nt = tt_all % p.n_tiles;
-        const uint16_t* src = static_cast<const uint16_t*>(p.a[g]) +
-                              ((size_t)(p.a_tile_off + nt) * p.kblocks + kb) * DFL_WBLK_ELEMS;
-        uint8_t* dst = sm + (size_t)s * stage_bytes;
-        if (stream_w)
-          bulk_load_hint(dst, src, A_STAGE_BYTES, full + s, pol);
-        else
-          bulk_load(dst, src, A_STAGE_BYTES, full + s);
+        tt = tile % p.t_tiles;
+        a_ptr = static_cast<const uint16_t*>(p.a[g]) + ((size_t)(p.a_tile_off + nt) * KBi + kb) * DFL_WBLK_ELEMS;
       };
-      auto load_b = [&](int s, long long u) {
-        const int tile = (int)(u / KB), kb = (int)(u % KB);
-        const int tt = tile % p.t_tiles;
-        tma_load_2d(sm + (size_t)s * stage_bytes + A_STAGE_BYTES, &tmB, full + s, kb * 64, tt * BN);
+      tile_base();
+      auto advance = [&]() {
+        if (++kb == KBi) {
+          kb = 0;
+          ++tile;
+          tile_base();
+        } else {
+          a_ptr += DFL_WBLK_ELEMS;
+        }
+      };
+      auto load_a = [&](int st) {
+        uint8_t* dst = sm + (size_t)st * stage_bytes;
+        constexpr int CH = A_STAGE_BYTES / DFL_GEMM_A_CHUNKS;
+#pragma unroll
+        for (int ch = 0; ch < DFL_GEMM_A_CHUNKS; ++ch) {
+          if (hint)
+            bulk_load_hint(dst + ch * CH, a_ptr + ch * (CH / 2), CH, full + st, pol);
+          else
+            bulk_load(dst + ch * CH, a_ptr + ch * (CH / 2), CH, full + st);
+        }
+      };
+      auto load_b = [&](int st, int kb_, int tt_) {
+        tma_load_2d(sm + (size_t)st * stage_bytes + A_STAGE_BYTES, &tmB, full + st, kb_ * 64, tt_ * BN);
       };
       // Weights do not depend on the previous kernel: fetch the first stages'
       // weight tiles before waiting on it, then the token tiles.
-      const long long pre = (u1 - u0) < stages ? (u1 - u0) : stages;
-      for (long long i = 0; i < pre; ++i) {
+      const int pre = n_units < stages ? n_units : stages;
+      int pkb[DFL_GEMM_MAX_STAGES], ptt[DFL_GEMM_MAX_STAGES];
+      for (int i = 0; i < pre; ++i) {
         mbar_arrive_expect_tx(full + i, stage_bytes);
-        load_a((int)i, u0 + i);
+        load_a(i);
+        pkb[i] = kb;
+        ptt[i] = tt;
+        advance();
       }
       pdl_wait();
-      for (long long i = 0; i < pre; ++i) load_b((int)i, u0 + i);
-      long long it = pre;
-      for (long long u = u0 + pre; u < u1; ++u, ++it) {
-        const int s = (int)(it % stages);
-        const uint32_t round = (uint32_t)(it / stages);
-        if (!mbar_wait(empty + s, (round & 1u) ^ 1u, p.status, &aborted)) break;
-        mbar_arrive_expect_tx(full + s, stage_bytes);
-        load_a(s, u);
-        load_b(s, u);
+      for (int i = 0; i < pre; ++i) load_b(i, pkb[i], ptt[i]);
+      int st = pre == stages ? 0 : pre;
+      uint32_t phase = pre == stages ? 1u : 0u;  // round parity of stage st's next fill
+      int issued = pre;
+      for (; issued < n_units; ++issued) {
+        if (!mbar_wait(empty + st, phase ^ 1u, p.status, &aborted)) break;
+        mbar_arrive_expect_tx(full + st, stage_bytes);
+        load_a(st);
+        load_b(st, kb, tt);
+        advance();
+        if (++st == stages) {
+          st = 0;
+          phase ^= 1u;
+        }
       }
       // drain: every issued copy lands before the CTA may exit
-      const long long issued = it;
-      for (long long i = (issued > stages ? issued - stages : 0); i < issued; ++i) {
+      for (int i = (issued > stages ? issued - stages : 0); i < issued; ++i) {
         bool drain_abort = false;
         mbar_wait(full + (i % stages), (uint32_t)((i / stages) & 1), p.status, &drain_abort);
       }
@@ -318,6 +426,8 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
       const uint32_t idesc = idesc_f16_f32(128, BN, p.ab_type);
       long long it = 0;
       int seg = 0;
+      int s = 0;
+      uint32_t phase = 0;
       for (long long u = u0; u < u1 && !aborted; ++seg) {
         const long long tile = u / KB;
         const long long seg_end = (tile + 1) * KB < u1 ? (tile + 1) * KB : u1;
@@ -327,8 +437,14 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(abuf * BN);
         for (long long k = 0; u < seg_end; ++u, ++k, ++it) {
-          const int s = (int)(it % stages);
-          if (!mbar_wait(full + s, (uint32_t)((it / stages) & 1), p.status, &aborted)) break;
+          if (k > 0 || it > 0) {
+            if (++s == stages) {
+              s = 0;
+              phase ^= 1u;
+            }
+          }
+          if (!mbar_wait(full + s, phase, p.status, &aborted)) break;
+          if (it == 0) trace_at(p, 2, globaltimer());
           tc_fence_after();
           const uint32_t a_addr = smem_u32(sm + (size_t)s * stage_bytes);
           const uint64_t adesc = sdesc_sw128(a_addr);
@@ -341,6 +457,8 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
         }
         tc_commit(tfull + abuf);
       }
+      trace_at(p, 3, globaltimer());
+      trace_at(p, 6, (unsigned long long)(u1 - u0));
       tc_commit(mdone);
       bool drain_abort = false;
       mbar_wait(mdone, 0, p.status, &drain_abort);
@@ -440,12 +558,19 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
         mbar_arrive(tempty + abuf);
       }
     }
+    if (threadIdx.x == 64) trace_at(p, 4, globaltimer());
   }
 
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, ncols);
+  }
+  if (threadIdx.x == 0) {
+    uint32_t smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    trace_at(p, 7, smid);
+    trace_at(p, 5, globaltimer());
   }
   if (MODE == GM_ARGMAX) {
     // The last CTA to finish turns the per-token argmax keys of block rows
@@ -481,7 +606,7 @@ size_t gemm_smem_bytes(int BN, int stages) {
 int gemm_pick_stages(int BN) {
   const size_t budget = 232448 - 1024 - STG_BYTES - 512;
   int st = (int)(budget / (size_t)(A_STAGE_BYTES + BN * 128));
-  return st > 12 ? 12 : st;
+  return st > DFL_GEMM_MAX_STAGES ? DFL_GEMM_MAX_STAGES : st;
 }
 
 cudaError_t gemm_init_attributes() {

@@ -85,6 +85,8 @@ struct GemmParams {
   float* logits;             // optional [M][N] (N = vocab)
   int* draft;                // [batch][15]
   unsigned* done_ctr;
+  // optional timeline: [grid][8] %globaltimer stamps per CTA (null: off)
+  unsigned long long* trace;
   // split-K scratch
   float* ws;            // [grid][2][BN_MAX*128]
   unsigned* tile_ctr;   // [total_tiles]
