@@ -119,8 +119,6 @@ struct dflash_handle {
   unsigned* done_ctr;
   float* gemm_ws;
   unsigned* tile_ctr;
-  float* attn_ws;
-  unsigned* attn_ctr;
   // runtime
   bool pdl = true;
   uint64_t launches = 0;
@@ -175,7 +173,6 @@ size_t carve(dflash_handle* h, const dflash_config& c, char* base, int num_sms) 
   const long long blk = 64LL * hkv * D;  // elements per page per layer (K or V)
   const long long layer_stride = (long long)c.max_pages * blk;
   const int splits = pick_attn_splits(c, num_sms);
-  const int G = hq / hkv;
   // split-K tile counters: the largest tile count of any GEMM (all of them,
   // the lm_head included, use the balanced split)
   const int t_tiles_max = ceil_div(std::max(M, R), DFL_BN_MAX);
@@ -224,8 +221,6 @@ size_t carve(dflash_handle* h, const dflash_config& c, char* base, int num_sms) 
   o->ss_c = w.take<float>((size_t)(H / 128) * R);
   o->gemm_ws = w.take<float>((size_t)num_sms * 2 * DFL_BN_MAX * 128);
   o->tile_ctr = w.take<unsigned>(tiles);
-  o->attn_ws = w.take<float>((size_t)c.max_batch * hkv * splits * (G * 16) * (D + 2));
-  o->attn_ctr = w.take<unsigned>((size_t)c.max_batch * hkv);
   if (h) {
     h->attn_splits = splits;
     h->max_tiles = tiles;
@@ -396,9 +391,12 @@ int draft_impl(dflash_handle* h, const int32_t* slots, int32_t batch, const int3
       a.D = D;
       a.n_splits = h->attn_splits;
       a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
-      a.ws = h->attn_ws;
-      a.ctr = h->attn_ctr;
       a.status = h->status;
+      if (h->trace.kid == DFLASH_KID_ATTENTION && h->trace.buf &&
+          (long long)a.n_splits * hkv * batch <= h->trace.cap) {
+        a.trace = h->trace.buf;  // one launch only
+        h->trace.kid = 0;
+      }
       ProbeScope ps(h, DFLASH_KID_ATTENTION, s);
       h->launches++;
       rc = cuda_err(attn_launch(a, batch, s, h->pdl));

@@ -8,8 +8,10 @@
 // bulk copy lands it in shared memory already in a bank-conflict-free layout
 // for ldmatrix.  Q.K^T and P.V run on warp MMAs (m16n8k16, f16 in, fp32
 // accumulate), the softmax is online in the log2 domain with quad shuffles.
-// Splits write fp32 partials (O, running max, running sum); the last CTA of a
-// (request, KV head) merges them in split order -- deterministic, no waiting.
+// The splits of one (request, KV head) are one thread-block cluster; their
+// fp32 partials (O, running max, running sum) stay in shared memory and are
+// merged in split order over distributed shared memory -- deterministic, no
+// global scratch.
 #include "common.cuh"
 #include "internal.h"
 
@@ -17,18 +19,28 @@ namespace {
 
 template <int D>
 struct AttnCfg {
-  static constexpr int STAGES = 3;
+  static constexpr int STAGES = D == 128 ? 6 : 8;            // pages in flight per CTA
   static constexpr int BLK_BYTES = 64 * D * 2;               // one K (or V) page block
   static constexpr int STAGE_BYTES = 2 * BLK_BYTES;
-  static constexpr int SMEM = STAGES * STAGE_BYTES + 128;    // + barriers and flag
+  static constexpr int MAX_PIDS = 512;                       // page ids prefetched to shared memory
+  static constexpr int SMEM = STAGES * STAGE_BYTES + 128 + MAX_PIDS * 4;  // + barriers, page ids
 };
+
+// Timeline stamps (p.trace non-null), per CTA in grid order: 0 entry, 1 context
+// length known, 2 first page landed, 3 pages done, 4 partial published, 5 exit.
+DFL_DEV void atrace(const AttnParams& p, int ev) {
+  if (p.trace) {
+    const size_t cta = ((size_t)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+    p.trace[cta * 8 + ev] = globaltimer();
+  }
+}
 
 template <int D, int G>
 __global__ void __launch_bounds__(G * 32) k_attn(const AttnParams p) {
   using C = AttnCfg<D>;
   extern __shared__ __align__(128) uint8_t sm[];
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + C::STAGES * C::STAGE_BYTES);
-  int* flag = reinterpret_cast<int*>(full + C::STAGES);
+  int* pids = reinterpret_cast<int*>(sm + C::STAGES * C::STAGE_BYTES + 128);
 
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -37,12 +49,12 @@ __global__ void __launch_bounds__(G * 32) k_attn(const AttnParams p) {
   const int hq = p.hq, hkv = p.hkv;
 
   if (threadIdx.x == 0) {
+    atrace(p, 0);
     for (int s = 0; s < C::STAGES; ++s) mbar_init(full + s, 1);
     fence_mbar_init();
   }
   pdl_launch_dependents();
   pdl_wait();
-  __syncthreads();
 
   const int slot = p.slots[b];
   const int nkeys = p.ctx_len[slot] + DFL_BLOCK;
@@ -53,9 +65,15 @@ __global__ void __launch_bounds__(G * 32) k_attn(const AttnParams p) {
   const f16* kbase = p.kv.k_pool + (size_t)p.layer * p.kv.layer_stride;
   const f16* vbase = p.kv.v_pool + (size_t)p.layer * p.kv.layer_stride;
   const int* pt = p.kv.page_table + (size_t)slot * p.kv.max_pages_per_slot;
+  // this CTA's page ids, read in parallel once (not one dependent load per copy)
+  for (int i = threadIdx.x; i < pe - pb && i < C::MAX_PIDS; i += blockDim.x)
+    pids[i] = pb + i < p.kv.max_pages_per_slot ? pt[pb + i] : -1;
+  __syncthreads();
+  if (threadIdx.x == 0) atrace(p, 1);
 
   auto issue = [&](int s, int page_idx) {
-    int pg = page_idx < p.kv.max_pages_per_slot ? pt[page_idx] : -1;
+    const int li = page_idx - pb;
+    int pg = li < C::MAX_PIDS ? pids[li] : (page_idx < p.kv.max_pages_per_slot ? pt[page_idx] : -1);
     if (pg < 0 || pg >= p.kv.max_pages) {
       dev_error(p.status, DFLASH_DEV_PAGE);
       pg = 0;
@@ -97,6 +115,7 @@ __global__ void __launch_bounds__(G * 32) k_attn(const AttnParams p) {
   for (int pi = pb; pi < pe; ++pi, ++it) {
     const int s = it % C::STAGES;
     const bool ok = mbar_wait(full + s, (uint32_t)((it / C::STAGES) & 1), p.status, &aborted);
+    if (it == 0 && threadIdx.x == 0) atrace(p, 2);
     if (ok) {
       const int valid = min(64, nkeys - pi * 64);
       const uint32_t kb_addr = smem_u32(sm + s * C::STAGE_BYTES);
@@ -194,6 +213,7 @@ __global__ void __launch_bounds__(G * 32) k_attn(const AttnParams p) {
     }
   }
 
+  if (threadIdx.x == 0) atrace(p, 3);
   l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
   l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
@@ -210,84 +230,83 @@ __global__ void __launch_bounds__(G * 32) k_attn(const AttnParams p) {
       *reinterpret_cast<uint32_t*>(out0 + d) = pack_f16x2(o[nd][0] * i0, o[nd][1] * i0);
       *reinterpret_cast<uint32_t*>(out1 + d) = pack_f16x2(o[nd][2] * i1, o[nd][3] * i1);
     }
+    if (threadIdx.x == 0) atrace(p, 5);
     return;
   }
 
-  float* part = p.ws + (size_t)((b * hkv + kvh) * p.n_splits + split) * (size_t)(rows * (D + 2));
+  // Splits of one (request, KV head) form a thread-block cluster: each CTA
+  // leaves its partial (unnormalised O, running max, running sum) in its own
+  // shared memory, the cluster barrier publishes them, and CTA r merges rows
+  // r*rows/n .. of the output from all partials over distributed shared
+  // memory, in split order.  No global scratch, no counters, no waiting
+  // beyond the hardware barrier.
+  constexpr int PS = D + 4;  // padded row stride (floats) of a partial
+  float* part = reinterpret_cast<float*>(sm);  // [rows][PS], then m[rows], l[rows]
 #pragma unroll
   for (int nd = 0; nd < D / 8; ++nd) {
     const int d = nd * 8 + 2 * c4;
-    __stcg(reinterpret_cast<float2*>(part + (size_t)r0 * D + d), make_float2(o[nd][0], o[nd][1]));
-    __stcg(reinterpret_cast<float2*>(part + (size_t)r1 * D + d), make_float2(o[nd][2], o[nd][3]));
+    *reinterpret_cast<float2*>(part + r0 * PS + d) = make_float2(o[nd][0], o[nd][1]);
+    *reinterpret_cast<float2*>(part + r1 * PS + d) = make_float2(o[nd][2], o[nd][3]);
   }
   if (c4 == 0) {
-    __stcg(part + rows * D + r0, m0);
-    __stcg(part + rows * D + r1, m1);
-    __stcg(part + rows * D + rows + r0, l0);
-    __stcg(part + rows * D + rows + r1, l1);
+    part[rows * PS + r0] = m0;
+    part[rows * PS + r1] = m1;
+    part[rows * PS + rows + r0] = l0;
+    part[rows * PS + rows + r1] = l1;
   }
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const unsigned old = atomicAdd(p.ctr + b * hkv + kvh, 1u);
-    const int last = old == (unsigned)p.n_splits - 1;
-    if (last) p.ctr[b * hkv + kvh] = 0;
-    *flag = last;
-  }
-  __syncthreads();
-  if (!*flag) return;
-  __threadfence();
+  if (threadIdx.x == 0) atrace(p, 4);
+  cluster_sync_all();
 
-  // merge the splits in split order; per-split weights in shared memory
-  float* wsm = reinterpret_cast<float*>(sm);  // [n_splits][rows]
-  const float* base = p.ws + (size_t)((b * hkv + kvh) * p.n_splits) * (size_t)(rows * (D + 2));
-  const size_t pstride = (size_t)rows * (D + 2);
-  for (int r = threadIdx.x; r < rows; r += blockDim.x) {
-    // every split's (max, sum) loaded at once, then combined (n_splits <= 8)
+  const int n = p.n_splits;
+  const int rank = (int)cluster_ctarank();
+  const int rpc = (rows + n - 1) / n;           // rows merged by this CTA
+  const int rb = rank * rpc, re = min(rows, rb + rpc);
+  const uint32_t part_local = smem_u32(part);
+  float* wsm = part + rows * PS + 2 * rows;     // [n][rpc] merge weights (local)
+  for (int rr = threadIdx.x; rr < re - rb; rr += blockDim.x) {
+    const int r = rb + rr;
     float mv[8], lv[8];
 #pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      mv[s] = -INFINITY;
-      lv[s] = 0.f;
-      if (s < p.n_splits) {
-        mv[s] = __ldcg(base + s * pstride + rows * D + r);
-        lv[s] = __ldcg(base + s * pstride + rows * D + rows + r);
+    for (int sp = 0; sp < 8; ++sp) {
+      mv[sp] = -INFINITY;
+      lv[sp] = 0.f;
+      if (sp < n) {
+        const uint32_t a = dsmem_addr(part_local, (uint32_t)sp);
+        mv[sp] = ld_dsmem(a + 4u * (uint32_t)(rows * PS + r));
+        lv[sp] = ld_dsmem(a + 4u * (uint32_t)(rows * PS + rows + r));
       }
     }
     float M = -INFINITY;
 #pragma unroll
-    for (int s = 0; s < 8; ++s)
-      if (lv[s] > 0.f) M = fmaxf(M, mv[s]);
+    for (int sp = 0; sp < 8; ++sp)
+      if (lv[sp] > 0.f) M = fmaxf(M, mv[sp]);
     float L = 0.f;
 #pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      const float w = lv[s] > 0.f ? exp2f(mv[s] - M) : 0.f;
-      mv[s] = w;
-      L += w * lv[s];
+    for (int sp = 0; sp < 8; ++sp) {
+      const float w = lv[sp] > 0.f ? exp2f(mv[sp] - M) : 0.f;
+      mv[sp] = w;
+      L += w * lv[sp];
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
-    for (int s = 0; s < p.n_splits; ++s) wsm[s * rows + r] = mv[s] * inv;
+    for (int sp = 0; sp < n; ++sp) wsm[sp * rpc + rr] = mv[sp] * inv;
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < rows * D / 4; e += blockDim.x) {
-    const int r = (e * 4) / D, d = (e * 4) % D;
-    // all splits' loads in flight before any is consumed (n_splits <= 8)
+  for (int e = threadIdx.x; e < (re - rb) * (D / 4); e += blockDim.x) {
+    const int rr = e / (D / 4), d = (e % (D / 4)) * 4;
+    const int r = rb + rr;
     float4 v[8];
 #pragma unroll
-    for (int s = 0; s < 8; ++s)
-      if (s < p.n_splits)
-        v[s] = __ldcg(reinterpret_cast<const float4*>(base + s * pstride + (size_t)r * D + d));
+    for (int sp = 0; sp < 8; ++sp)
+      if (sp < n) v[sp] = ld_dsmem4(dsmem_addr(part_local, (uint32_t)sp) + 4u * (uint32_t)(r * PS + d));
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      if (s < p.n_splits) {
-        const float w = wsm[s * rows + r];
-        if (w != 0.f) {
-          acc.x += w * v[s].x;
-          acc.y += w * v[s].y;
-          acc.z += w * v[s].z;
-          acc.w += w * v[s].w;
-        }
+    for (int sp = 0; sp < 8; ++sp) {
+      if (sp < n) {
+        const float w = wsm[sp * rpc + rr];
+        acc.x += w * v[sp].x;
+        acc.y += w * v[sp].y;
+        acc.z += w * v[sp].z;
+        acc.w += w * v[sp].w;
       }
     }
     const int wq = r / 16, t = r % 16;
@@ -295,6 +314,9 @@ __global__ void __launch_bounds__(G * 32) k_attn(const AttnParams p) {
     *reinterpret_cast<uint32_t*>(dst) = pack_f16x2(acc.x, acc.y);
     *reinterpret_cast<uint32_t*>(dst + 2) = pack_f16x2(acc.z, acc.w);
   }
+  // keep this CTA's partial alive until every CTA of the cluster has read it
+  cluster_sync_all();
+  if (threadIdx.x == 0) atrace(p, 5);
 }
 
 template <int D, int G>
@@ -304,11 +326,15 @@ cudaError_t launch_t(const AttnParams& p, int batch, cudaStream_t s, bool pdl) {
   cfg.blockDim = dim3(G * 32);
   cfg.dynamicSmemBytes = AttnCfg<D>::SMEM;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;  // the splits of one KV head
+  attr[0].val.clusterDim.x = (unsigned)p.n_splits;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = pdl ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, k_attn<D, G>, p);
 }
 

@@ -27,6 +27,16 @@ DFL_DEV uint64_t globaltimer() {
 
 DFL_DEV void dev_error(uint32_t* status, uint32_t bit) { atomicOr(status, bit); }
 
+// Arrival counter with release and acquire semantics at GPU scope.  Called by
+// one thread after a CTA (or named) barrier, it publishes every write the
+// CTA made before the barrier, and the CTA that observes the final count sees
+// every other arriver's writes after its next barrier (fences are cumulative).
+DFL_DEV unsigned atomic_add_acq_rel(unsigned* addr, unsigned v) {
+  unsigned old;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
+  return old;
+}
+
 // ------------------------------------------------------------------ mbarrier
 DFL_DEV void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
@@ -167,6 +177,37 @@ DFL_DEV uint64_t sdesc_sw128(uint32_t saddr) {
 // (ab_type 1) or both f16 (ab_type 0), both K-major.
 __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, uint32_t ab_type) {
   return (1u << 4) | (ab_type << 7) | (ab_type << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// ------------------------------------------------------------------ thread-block clusters
+DFL_DEV uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA of the cluster: release this CTA's shared-memory
+// writes, wait for all CTAs, acquire theirs.
+DFL_DEV void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+DFL_DEV uint32_t dsmem_addr(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+DFL_DEV float ld_dsmem(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+DFL_DEV float4 ld_dsmem4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
 }
 
 // ------------------------------------------------------------------ named barriers

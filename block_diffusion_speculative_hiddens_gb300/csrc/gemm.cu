@@ -97,13 +97,85 @@ DFL_DEV int page_of(const GemmParams& p, int slot, int pos) {
 
 constexpr int EPI_TOK = 4;  // tokens per warp whose inputs are gathered together
 
+// Per-token epilogue inputs of one warp's EPI_TOK tokens (j0, j0+4, ...):
+// the RMSNorm scale of the GEMM's input and, for QKV/INJECT, whether the row
+// is appended, its position, RoPE (cos, sin) of frequencies lane and lane+32,
+// and the page holding it.  None depends on the accumulators, so a batch-1
+// CTA gathers them once while its main loop streams.
+struct TokCtx {
+  float s[EPI_TOK];
+  bool live[EPI_TOK];
+  int pos[EPI_TOK], pg[EPI_TOK];
+  float2 c0[EPI_TOK], c1[EPI_TOK];
+};
+
+template <int MODE>
+DFL_DEV void gather_ctx(const GemmParams& p, int t_first, int j0, int ntok, int lane, TokCtx& c) {
+  bool ok[EPI_TOK];
+  int tq[EPI_TOK];
+#pragma unroll
+  for (int q = 0; q < EPI_TOK; ++q) {
+    const int j = j0 + 4 * q;
+    ok[q] = j < ntok;  // warp-uniform
+    tq[q] = ok[q] ? t_first + j : t_first;
+  }
+  {
+    float ssq[EPI_TOK];
+#pragma unroll
+    for (int q = 0; q < EPI_TOK; ++q) {
+      ssq[q] = 0.f;
+      if (ok[q])
+        for (int i = lane; i < p.ss_parts; i += 32) ssq[q] += p.ss_in[(size_t)i * p.M + tq[q]];
+    }
+#pragma unroll
+    for (int q = 0; q < EPI_TOK; ++q) c.s[q] = rsqrtf(warp_sum(ssq[q]) / (float)p.H + p.eps);
+  }
+  if (MODE == GM_QKV || MODE == GM_INJECT) {
+    const int D = p.D;
+    int slot[EPI_TOK], ne[EPI_TOK];
+#pragma unroll
+    for (int q = 0; q < EPI_TOK; ++q) {
+      const int b = MODE == GM_QKV ? tq[q] / DFL_BLOCK : tq[q] / p.rows_per_req;
+      slot[q] = p.slots[b];
+      ne[q] = MODE == GM_QKV ? DFL_BLOCK : p.n_eff[b];
+    }
+#pragma unroll
+    for (int q = 0; q < EPI_TOK; ++q) {
+      if (MODE == GM_QKV) {
+        c.live[q] = ok[q];
+        c.pos[q] = p.ctx_len[slot[q]] + (tq[q] % DFL_BLOCK);
+      } else {
+        const int i = tq[q] % p.rows_per_req;
+        c.live[q] = ok[q] && i < ne[q];
+        c.pos[q] = p.pos0[slot[q]] + i;
+      }
+      if (c.live[q] && c.pos[q] >= p.max_pos) {
+        dev_error(p.status, DFLASH_DEV_CAPACITY);
+        c.live[q] = false;
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < EPI_TOK; ++q) {
+      c.c0[q] = c.c1[q] = make_float2(1.f, 0.f);
+      c.pg[q] = -1;
+      if (c.live[q]) {
+        const float2* row = p.rope + (size_t)c.pos[q] * (D / 2);
+        c.c0[q] = row[lane];
+        if (D == 128) c.c1[q] = row[lane + 32];
+        c.pg[q] = page_of(p, slot[q], c.pos[q]);
+      }
+    }
+  }
+}
+
 // Final epilogue for tokens t_first .. t_first+ntok-1 of `tile`; staging
 // stg[j][r] holds the fully reduced fp32 accumulators.  Epilogue warp ew
 // handles tokens j = ew, ew+4, ...; lane holds rows lane + 32*jj.  Every
 // global input of a warp's next EPI_TOK tokens is loaded before any is used,
 // so the dependent-load chain costs a few round trips per tile, not per token.
 template <int MODE>
-DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, const float* stg, int ew, int lane) {
+DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, const float* stg, int ew, int lane,
+                       const TokCtx* pre) {
   const int tt_all = tile / p.t_tiles;       // (group, n-tile)
   const int group = tt_all / p.n_tiles;
   const int nt = tt_all % p.n_tiles;
@@ -145,19 +217,15 @@ DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, con
         if (lane == 0) p.ss_out[(size_t)nt * p.M + tq[q]] = sq;
       }
     } else {
-    // per-token RMSNorm scale of this GEMM's input
-    float s[EPI_TOK];
-    {
-      float ssq[EPI_TOK];
-#pragma unroll
-      for (int q = 0; q < EPI_TOK; ++q) {
-        ssq[q] = 0.f;
-        if (ok[q])
-          for (int i = lane; i < p.ss_parts; i += 32) ssq[q] += p.ss_in[(size_t)i * p.M + tq[q]];
-      }
-#pragma unroll
-      for (int q = 0; q < EPI_TOK; ++q) s[q] = rsqrtf(warp_sum(ssq[q]) / (float)p.H + p.eps);
+    // per-token inputs: gathered at kernel start for the first 16 tokens of a
+    // single token tile, otherwise now
+    TokCtx local;
+    const TokCtx* tc = pre;
+    if (!(pre && t_first == 0 && j0 == ew)) {
+      gather_ctx<MODE>(p, t_first, j0, ntok, lane, local);
+      tc = &local;
     }
+    const float* s = tc->s;
 
     if (MODE == GM_SWIGLU) {
       const int f0 = nt * 64;
@@ -213,46 +281,11 @@ DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, con
         layer = group;
         kgain = p.kn_gain[group];
       }
-      // gather: request -> slot (and row count) -> position -> RoPE row, page
-      int slot[EPI_TOK], pos[EPI_TOK], pg[EPI_TOK];
-      bool live[EPI_TOK];
-      float2 c0[EPI_TOK], c1[EPI_TOK];
-#pragma unroll
-      for (int q = 0; q < EPI_TOK; ++q) {
-        const int t = ok[q] ? tq[q] : t_first;
-        const int b = MODE == GM_QKV ? t / DFL_BLOCK : t / p.rows_per_req;
-        slot[q] = p.slots[b];
-        pos[q] = MODE == GM_QKV ? 0 : p.n_eff[b];  // inject: row count, read together with the slot
-      }
-#pragma unroll
-      for (int q = 0; q < EPI_TOK; ++q) {
-        const int t = ok[q] ? tq[q] : t_first;
-        if (MODE == GM_QKV) {
-          live[q] = ok[q];
-          pos[q] = p.ctx_len[slot[q]] + (t % DFL_BLOCK);
-        } else {
-          const int i = t % p.rows_per_req;
-          live[q] = ok[q] && i < pos[q];
-          pos[q] = p.pos0[slot[q]] + i;
-        }
-        if (live[q] && pos[q] >= p.max_pos) {
-          dev_error(p.status, DFLASH_DEV_CAPACITY);
-          live[q] = false;
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < EPI_TOK; ++q) {
-        c0[q] = c1[q] = make_float2(1.f, 0.f);
-        pg[q] = -1;
-        if (live[q]) {
-          if (kind < 2) {
-            const float2* row = p.rope + (size_t)pos[q] * (D / 2);
-            c0[q] = row[lane];
-            if (D == 128) c1[q] = row[lane + 32];
-          }
-          if (kind > 0) pg[q] = page_of(p, slot[q], pos[q]);
-        }
-      }
+      const bool* live = tc->live;
+      const int* pos = tc->pos;
+      const int* pg = tc->pg;
+      const float2* c0 = tc->c0;
+      const float2* c1 = tc->c1;
 #pragma unroll
       for (int q = 0; q < EPI_TOK; ++q) {
         if (!live[q]) continue;  // warp-uniform
@@ -470,6 +503,12 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
     const int r = q * 32 + lane;  // TMEM lane = tile row
     const int et = threadIdx.x - 64;
     const int ew = et >> 5;
+    TokCtx pre_ctx;
+    const TokCtx* pre = nullptr;
+    if (MODE != GM_RESID && MODE != GM_FC && p.t_tiles == 1) {
+      gather_ctx<MODE>(p, 0, ew, p.M < 16 ? p.M : 16, lane, pre_ctx);
+      pre = &pre_ctx;
+    }
     int seg = 0;
     for (long long u = u0; u < u1; ++seg) {
       const long long tile = u / KB;
@@ -501,11 +540,10 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
         }
         tc_fence_before();
         mbar_arrive(tempty + abuf);
-        __threadfence();
         named_bar_sync(1, EPI_THREADS);
         if (et == 0) {
           const unsigned cnt = (unsigned)(c_last - c_first + 1);
-          const unsigned old = atomicAdd(p.tile_ctr + tile, 1u);
+          const unsigned old = atomic_add_acq_rel(p.tile_ctr + tile, 1u);
           const int last = old == cnt - 1;
           if (last) p.tile_ctr[tile] = 0;
           *flag = last;
@@ -514,7 +552,6 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
         const int last = *flag;
         named_bar_sync(1, EPI_THREADS);
         if (!last) continue;
-        __threadfence();
       }
       for (int tc0 = 0; tc0 < mt; tc0 += 32) {
 #pragma unroll
@@ -550,7 +587,8 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
           }
         }
         named_bar_sync(1, EPI_THREADS);
-        epi_final<MODE>(p, (int)tile, t_base + tc0, (mt - tc0) < 32 ? (mt - tc0) : 32, stg, ew, lane);
+        epi_final<MODE>(p, (int)tile, t_base + tc0, (mt - tc0) < 32 ? (mt - tc0) : 32, stg, ew, lane,
+                        pre);
         named_bar_sync(1, EPI_THREADS);
       }
       if (!split) {

@@ -101,11 +101,10 @@ struct AttnParams {
   const int* slots;
   const int* ctx_len;  // keys = ctx_len + 16 (block K/V already in the cache)
   int hq, hkv, D;
-  int n_splits;
+  int n_splits;        // CTAs per (request, KV head): one cluster, <= 8
   float scale_log2;    // log2(e) / sqrt(D)
-  float* ws;           // partials [batch*hkv*n_splits][rows*(D+2)]
-  unsigned* ctr;       // [batch*hkv]
   uint32_t* status;
+  unsigned long long* trace;  // optional [grid][8] timeline (null: off)
 };
 
 // host launchers (gemm.cu / attention.cu / small.cu)

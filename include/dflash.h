@@ -244,12 +244,14 @@ DFLASH_API int dflash_draft_block_debug(dflash_handle* h, const int32_t* slots, 
 DFLASH_API int dflash_probe_arm(dflash_handle* h, int32_t kernel_id, int32_t n);
 DFLASH_API int dflash_probe_read(dflash_handle* h, float* ms_out, int32_t cap, int32_t* n_out);
 
-/* Device timeline of one GEMM launch: the next launch of GEMM kernel
- * `kernel_id` (DFLASH_KID_*, not DFLASH_KID_ATTENTION) writes, per CTA, 8
- * uint64 values into the DEVICE buffer buf[cap_ctas][8]: %globaltimer (ns)
- * at entry, end of set-up, first weight stage landed, last MMA issued,
- * epilogue done and exit, then the CTA's unit count and its SM id.  Launches
- * with more CTAs than cap_ctas are not traced.  kernel_id 0 disarms. */
+/* Device timeline of one launch: the next launch of kernel `kernel_id`
+ * (DFLASH_KID_*) writes, per CTA, 8 uint64 values into the DEVICE buffer
+ * buf[cap_ctas][8].  GEMMs: %globaltimer (ns) at entry, end of set-up, first
+ * weight stage landed, last MMA issued, epilogue done and exit, then the
+ * CTA's unit count and its SM id.  Attention (CTAs in split-fastest order):
+ * entry, context length known, first page landed, pages done, partial
+ * published, exit.  Launches with more CTAs than cap_ctas are not traced.
+ * kernel_id 0 disarms. */
 DFLASH_API int dflash_trace_arm(dflash_handle* h, int32_t kernel_id, unsigned long long* buf, int32_t cap_ctas);
 
 /* Number of kernels this handle has launched (or captured) so far. */
