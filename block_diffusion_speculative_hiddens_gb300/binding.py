@@ -55,6 +55,7 @@ _SIGS = {
     "dflash_fuse_inject": (ctypes.c_int, [_vp, _vp, ctypes.c_int32, _vp, ctypes.c_int32, _vp, _vp]),
     "dflash_fuse_inject_noalloc": (ctypes.c_int, [_vp, _vp, ctypes.c_int32, _vp, ctypes.c_int32, _vp, _vp]),
     "dflash_draft_block": (ctypes.c_int, [_vp, _vp, ctypes.c_int32, _vp, _vp, _vp]),
+    "dflash_draft_round": (ctypes.c_int, [_vp, _vp, ctypes.c_int32, _vp, ctypes.c_int32, _vp, _vp, _vp, _vp]),
     "dflash_draft_block_debug": (ctypes.c_int, [_vp, _vp, ctypes.c_int32, _vp, _vp, _vp, _vp, _vp]),
     "dflash_accept_trim": (ctypes.c_int, [_vp, _vp, ctypes.c_int32, _vp, _vp, _vp, _vp, _vp, _vp]),
     "dflash_reset_slot": (ctypes.c_int, [_vp, ctypes.c_int32, _vp]),
@@ -185,6 +186,12 @@ class Drafter:
     def draft_block(self, slots, last_tok, draft, stream=None):
         _check("dflash_draft_block", self.lib.dflash_draft_block(
             self.h, _ptr(slots), slots.numel(), _ptr(last_tok), _ptr(draft), _stream(stream)))
+
+    def draft_round(self, slots, feats, rows_per_req: int, n_new, last_tok, draft, stream=None):
+        """fuse_inject + draft_block with the injection folded into the layers' QKV GEMMs."""
+        _check("dflash_draft_round", self.lib.dflash_draft_round(
+            self.h, _ptr(slots), slots.numel(), _ptr(feats), rows_per_req, _ptr(n_new), _ptr(last_tok),
+            _ptr(draft), _stream(stream)))
 
     def draft_block_debug(self, slots, last_tok, draft, hidden=None, logits=None, stream=None):
         _check("dflash_draft_block_debug", self.lib.dflash_draft_block_debug(

@@ -104,6 +104,8 @@ struct dflash_handle {
   // cached B operand descriptors for the current token count
   int bm_M = -1;
   CUtensorMap tm_hg, tm_o, tm_act;
+  int bm_MX = -1;
+  CUtensorMap tm_hgx;  // hg plus the fused-feature rows below it
   int bm_rows = -1;
   CUtensorMap tm_cg;
   // workspace
@@ -210,7 +212,7 @@ size_t carve(dflash_handle* h, const dflash_config& c, char* base, int num_sms) 
   o->layer_stride = layer_stride;
   o->rope = w.take<float2>((size_t)max_pos * (D / 2));
   o->h = w.take<float>((size_t)M * H);
-  o->hg = w.take<f16>((size_t)M * H);
+  o->hg = w.take<f16>((size_t)2 * M * H);  // [block rows ; fused-feature rows of a folded round]
   o->ss_a = w.take<float>((size_t)(H / 128) * M);
   o->qbuf = w.take<f16>((size_t)M * hq * D);
   o->obuf = w.take<f16>((size_t)M * hq * D);
@@ -280,6 +282,7 @@ int run_gemm(dflash_handle* h, cudaStream_t s, int mode, const void* const* a, i
   const int BN = ((ceil_div(M, t_tiles) + 15) / 16) * 16;
   p.mode = mode;
   p.M = M;
+  if (!p.ss_ld) p.ss_ld = M;
   p.kblocks = K / 64;
   p.n_tiles = n_tiles;
   p.t_tiles = t_tiles;
@@ -341,8 +344,12 @@ int ensure_bmaps(dflash_handle* h, int M) {
   return DFLASH_OK;
 }
 
+// Draft one block; with `feats` non-null, first fuse the new feature rows and
+// fold their K/V injection into every layer's QKV projection (rows M.. of its
+// token operand), so each layer's K/V weights stream once per round.
 int draft_impl(dflash_handle* h, const int32_t* slots, int32_t batch, const int32_t* last_tok, int32_t* draft,
-               float* hidden, float* logits, void* stream) {
+               float* hidden, float* logits, void* stream, const void* feats = nullptr, int rows_per_req = 0,
+               const int32_t* n_new = nullptr) {
   if (!h || batch < 0 || batch > h->cfg.max_batch) return DFLASH_ERR_INVALID_ARG;
   if (batch == 0) return DFLASH_OK;
   if (!slots || !last_tok || !draft) return DFLASH_ERR_INVALID_ARG;
@@ -354,6 +361,32 @@ int draft_impl(dflash_handle* h, const int32_t* slots, int32_t batch, const int3
   int rc = ensure_bmaps(h, M);
   if (rc) return rc;
   const KVGeom kv = kv_geom(h);
+  const bool fold = feats != nullptr;
+  const int R = fold ? batch * rows_per_req : 0;
+  if (fold) {
+    h->launches++;
+    rc = cuda_err(launch_page_alloc(slots, batch, n_new, rows_per_req, h->ctx_len, h->pos0, h->n_pages,
+                                    h->page_table, c.max_pages_per_slot, h->free_stack, h->free_top, h->n_eff,
+                                    c.max_slots, h->status, s));
+    if (rc) return rc;
+    const int MX = M + R;
+    const int t_tiles = ceil_div(R, DFL_BN_MAX);
+    const uint32_t BNr = (uint32_t)(((ceil_div(R, t_tiles) + 15) / 16) * 16);
+    CUtensorMap tm_feats;
+    if (!make_tmap(&tm_feats, feats, R, (uint64_t)c.n_fused * H, BNr, true)) return DFLASH_ERR_INVALID_ARG;
+    if (h->bm_MX != MX) {
+      if (!make_tmap(&h->tm_hgx, h->hg, MX, H, (uint32_t)(((MX + 15) / 16) * 16))) return DFLASH_ERR_CUDA;
+      h->bm_MX = MX;
+    }
+    GemmParams p = {};
+    p.out = h->hg + (size_t)M * H;  // fused-feature rows right below the block rows
+    p.gain = h->fc_norm;
+    p.ss_out = h->ss_c;
+    p.N = H;
+    const void* a = h->fc_pk;
+    rc = run_gemm(h, s, GM_FC, &a, 1, 0, H / 128, c.n_fused * H, tm_feats, R, p, true, 1, DFLASH_KID_FC);
+    if (rc) return rc;
+  }
 
   h->launches++;
   rc = cuda_err(launch_embed(slots, batch, last_tok, c.mask_id, c.vocab, h->embed_pk, h->in_norm[0], H, h->h,
@@ -374,8 +407,18 @@ int draft_impl(dflash_handle* h, const int32_t* slots, int32_t batch, const int3
       p.ctx_len = h->ctx_len;
       p.rows_per_req = DFL_BLOCK;
       p.N = (hq + 2 * hkv) * D;
+      if (fold) {
+        p.ss_ld = M;
+        p.inj_m0 = M;
+        p.ss_inj = h->ss_c;
+        p.inj_ld = R;
+        p.rows_per_req = rows_per_req;
+        p.pos0 = h->pos0;
+        p.n_eff = h->n_eff;
+      }
       const void* a = h->wqkv_pk[l];
-      rc = run_gemm(h, s, GM_QKV, &a, 1, 0, p.N / 128, H, h->tm_hg, M, p, true, 0, DFLASH_KID_QKV);
+      rc = run_gemm(h, s, GM_QKV, &a, 1, 0, p.N / 128, H, fold ? h->tm_hgx : h->tm_hg, fold ? M + R : M, p, true, 0,
+                    DFLASH_KID_QKV);
       if (rc) return rc;
     }
     {  // block attention
@@ -612,6 +655,22 @@ int dflash_draft_block(dflash_handle* h, const int32_t* slots, int32_t batch, co
   return draft_impl(h, slots, batch, last_tok, draft, nullptr, nullptr, stream);
 }
 
+int dflash_draft_round(dflash_handle* h, const int32_t* slots, int32_t batch, const void* feats,
+                       int32_t rows_per_req, const int32_t* n_new, const int32_t* last_tok, int32_t* draft,
+                       void* stream) {
+  if (!h || batch < 0 || batch > h->cfg.max_batch || rows_per_req < 0) return DFLASH_ERR_INVALID_ARG;
+  if (batch == 0) return DFLASH_OK;
+  // folding needs the feature rows to fit below the block rows in one token tile
+  const long long R = (long long)batch * rows_per_req;
+  if (rows_per_req == 0 || rows_per_req > DFL_BLOCK || batch * DFL_BLOCK + R > DFL_BN_MAX || R > h->cfg.max_rows) {
+    int rc = dflash_fuse_inject(h, slots, batch, feats, rows_per_req, n_new, stream);
+    if (rc) return rc;
+    return draft_impl(h, slots, batch, last_tok, draft, nullptr, nullptr, stream);
+  }
+  if (!slots || !n_new || !feats) return DFLASH_ERR_INVALID_ARG;
+  return draft_impl(h, slots, batch, last_tok, draft, nullptr, nullptr, stream, feats, rows_per_req, n_new);
+}
+
 int dflash_draft_block_debug(dflash_handle* h, const int32_t* slots, int32_t batch, const int32_t* last_tok,
                              int32_t* draft, float* hidden, float* logits, void* stream) {
   return draft_impl(h, slots, batch, last_tok, draft, hidden, logits, stream);
@@ -811,6 +870,7 @@ int noalloc_gemm(dflash_handle* h, cudaStream_t s, int mode, const void* const* 
   const int BN = ((M + 15) / 16) * 16;  // M <= 64: one token tile
   p.mode = mode;
   p.M = M;
+  if (!p.ss_ld) p.ss_ld = M;
   p.kblocks = K / 64;
   p.n_tiles = n_tiles;
   p.t_tiles = 1;

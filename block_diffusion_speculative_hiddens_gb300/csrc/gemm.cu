@@ -55,16 +55,24 @@ DFL_DEV void trace_at(const GemmParams& p, int ev, unsigned long long v) {
   if (p.trace) p.trace[(size_t)blockIdx.x * 8 + ev] = v;
 }
 
+// A lane's head-norm gains: g[j] = gain[lane + 32 j] for the rows it holds
+// (D = 64: g[0], g[1] only).
+DFL_DEV void load_head_gain(const float* gain, int D, int lane, float* g) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) g[j] = lane + 32 * j < D ? gain[lane + 32 * j] : 0.f;
+}
+
 // Head RMSNorm + RoPE on the 4 values a lane holds (rows lane, lane+32,
-// lane+64, lane+96 of a 128-row tile); c0/c1 are the (cos, sin) of RoPE
-// frequencies lane and lane+32.  D = 128: one head, RoPE pairs (0,2), (1,3).
-// D = 64: two heads (rows 0-63, 64-127), pairs (0,1) and (2,3), frequency lane.
-DFL_DEV void head_norm_rope(float* x, const float* gain, float2 c0, float2 c1, int D, float eps, int lane) {
+// lane+64, lane+96 of a 128-row tile); g from load_head_gain; c0/c1 are the
+// (cos, sin) of RoPE frequencies lane and lane+32.  D = 128: one head, RoPE
+// pairs (0,2), (1,3).  D = 64: two heads (rows 0-63, 64-127), pairs (0,1) and
+// (2,3), frequency lane.
+DFL_DEV void head_norm_rope(float* x, const float* g, float2 c0, float2 c1, int D, float eps, int lane) {
   if (D == 128) {
     float ss = warp_sum(x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3]);
     const float inv = rsqrtf(ss / 128.f + eps);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) x[j] *= inv * gain[lane + 32 * j];
+    for (int j = 0; j < 4; ++j) x[j] *= inv * g[j];
     const float a0 = x[0], b0 = x[2], a1 = x[1], b1 = x[3];
     x[0] = a0 * c0.x - b0 * c0.y;
     x[2] = b0 * c0.x + a0 * c0.y;
@@ -74,7 +82,7 @@ DFL_DEV void head_norm_rope(float* x, const float* gain, float2 c0, float2 c1, i
     const float sa = warp_sum(x[0] * x[0] + x[1] * x[1]);
     const float sb = warp_sum(x[2] * x[2] + x[3] * x[3]);
     const float ia = rsqrtf(sa / 64.f + eps), ib = rsqrtf(sb / 64.f + eps);
-    const float g0 = gain[lane], g1 = gain[lane + 32];
+    const float g0 = g[0], g1 = g[1];
     x[0] *= ia * g0;
     x[1] *= ia * g1;
     x[2] *= ib * g0;
@@ -105,6 +113,7 @@ constexpr int EPI_TOK = 4;  // tokens per warp whose inputs are gathered togethe
 struct TokCtx {
   float s[EPI_TOK];
   bool live[EPI_TOK];
+  bool inj[EPI_TOK];  // QKV: a fused-feature row (K/V appended, no Q)
   int pos[EPI_TOK], pg[EPI_TOK];
   float2 c0[EPI_TOK], c1[EPI_TOK];
 };
@@ -119,33 +128,41 @@ DFL_DEV void gather_ctx(const GemmParams& p, int t_first, int j0, int ntok, int 
     ok[q] = j < ntok;  // warp-uniform
     tq[q] = ok[q] ? t_first + j : t_first;
   }
+#pragma unroll
+  for (int q = 0; q < EPI_TOK; ++q) c.inj[q] = MODE == GM_INJECT || (MODE == GM_QKV && p.inj_m0 > 0 && tq[q] >= p.inj_m0);
   {
     float ssq[EPI_TOK];
 #pragma unroll
     for (int q = 0; q < EPI_TOK; ++q) {
       ssq[q] = 0.f;
-      if (ok[q])
-        for (int i = lane; i < p.ss_parts; i += 32) ssq[q] += p.ss_in[(size_t)i * p.M + tq[q]];
+      if (ok[q]) {
+        const bool fold = MODE == GM_QKV && c.inj[q];
+        const float* src = fold ? p.ss_inj : p.ss_in;
+        const int ld = fold ? p.inj_ld : p.ss_ld;
+        const int row = fold ? tq[q] - p.inj_m0 : tq[q];
+        for (int i = lane; i < p.ss_parts; i += 32) ssq[q] += src[(size_t)i * ld + row];
+      }
     }
 #pragma unroll
     for (int q = 0; q < EPI_TOK; ++q) c.s[q] = rsqrtf(warp_sum(ssq[q]) / (float)p.H + p.eps);
   }
   if (MODE == GM_QKV || MODE == GM_INJECT) {
     const int D = p.D;
-    int slot[EPI_TOK], ne[EPI_TOK];
+    int slot[EPI_TOK], ne[EPI_TOK], tl[EPI_TOK];
 #pragma unroll
     for (int q = 0; q < EPI_TOK; ++q) {
-      const int b = MODE == GM_QKV ? tq[q] / DFL_BLOCK : tq[q] / p.rows_per_req;
+      tl[q] = (MODE == GM_QKV && c.inj[q]) ? tq[q] - p.inj_m0 : tq[q];
+      const int b = c.inj[q] ? tl[q] / p.rows_per_req : tl[q] / DFL_BLOCK;
       slot[q] = p.slots[b];
-      ne[q] = MODE == GM_QKV ? DFL_BLOCK : p.n_eff[b];
+      ne[q] = c.inj[q] ? p.n_eff[b] : DFL_BLOCK;
     }
 #pragma unroll
     for (int q = 0; q < EPI_TOK; ++q) {
-      if (MODE == GM_QKV) {
+      if (!c.inj[q]) {
         c.live[q] = ok[q];
-        c.pos[q] = p.ctx_len[slot[q]] + (tq[q] % DFL_BLOCK);
+        c.pos[q] = p.ctx_len[slot[q]] + (tl[q] % DFL_BLOCK);
       } else {
-        const int i = tq[q] % p.rows_per_req;
+        const int i = tl[q] % p.rows_per_req;
         c.live[q] = ok[q] && i < ne[q];
         c.pos[q] = p.pos0[slot[q]] + i;
       }
@@ -173,9 +190,15 @@ DFL_DEV void gather_ctx(const GemmParams& p, int t_first, int j0, int ntok, int 
 // handles tokens j = ew, ew+4, ...; lane holds rows lane + 32*jj.  Every
 // global input of a warp's next EPI_TOK tokens is loaded before any is used,
 // so the dependent-load chain costs a few round trips per tile, not per token.
+// pre0/pre1 (use_pre): the contexts of tokens ew+4q and ew+16+4q of a chunk
+// starting at token 0, gathered at kernel start; gq/gk: QKV's q/k head-norm
+// gains (load_head_gain); hpre (use_hpre, RESID): residual values of tokens
+// ew+4q, rows lane+32jj of this tile, loaded when the tile started.  All are
+// selected by value so they stay in registers.
 template <int MODE>
 DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, const float* stg, int ew, int lane,
-                       const TokCtx* pre) {
+                       bool use_pre, const TokCtx& pre0, const TokCtx& pre1, const float* gq, const float* gk,
+                       bool use_hpre, const float (&hpre)[EPI_TOK][4]) {
   const int tt_all = tile / p.t_tiles;       // (group, n-tile)
   const int group = tt_all / p.n_tiles;
   const int nt = tt_all % p.n_tiles;
@@ -195,11 +218,14 @@ DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, con
     if constexpr (MODE == GM_RESID || MODE == GM_FC) {
       const int n0 = nt * 128;
       float hv[EPI_TOK][4];
+      const bool hp = use_hpre && t_first == 0 && j0 == ew;
 #pragma unroll
       for (int q = 0; q < EPI_TOK; ++q)
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj)
-          hv[q][jj] = (MODE == GM_RESID && ok[q]) ? p.h[(size_t)tq[q] * p.N + n0 + lane + 32 * jj] : 0.f;
+          hv[q][jj] = (MODE == GM_RESID && ok[q])
+                          ? (hp ? hpre[q][jj] : p.h[(size_t)tq[q] * p.N + n0 + lane + 32 * jj])
+                          : 0.f;
 #pragma unroll
       for (int q = 0; q < EPI_TOK; ++q) {
         if (!ok[q]) continue;
@@ -219,12 +245,12 @@ DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, con
     } else {
     // per-token inputs: gathered at kernel start for the first 16 tokens of a
     // single token tile, otherwise now
-    TokCtx local;
-    const TokCtx* tc = pre;
-    if (!(pre && t_first == 0 && j0 == ew)) {
-      gather_ctx<MODE>(p, t_first, j0, ntok, lane, local);
-      tc = &local;
-    }
+    TokCtx ctx;
+    if (use_pre && t_first == 0 && j0 - ew < 32)
+      ctx = j0 == ew ? pre0 : pre1;
+    else
+      gather_ctx<MODE>(p, t_first, j0, ntok, lane, ctx);
+    const TokCtx* tc = &ctx;
     const float* s = tc->s;
 
     if (MODE == GM_SWIGLU) {
@@ -269,19 +295,21 @@ DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, con
     } else if (MODE == GM_QKV || MODE == GM_INJECT) {
       const int D = p.D;
       int n0, kind, layer;
-      const float* kgain;
+      float g[4];
       if (MODE == GM_QKV) {
         n0 = nt * 128;
         kind = n0 < p.hq * D ? 0 : (n0 < (p.hq + p.hkv) * D ? 1 : 2);
         layer = p.layer;
-        kgain = kind == 0 ? p.qn_gain : p.kn_gain[0];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) g[j] = kind == 0 ? gq[j] : gk[j];
       } else {
         n0 = nt * 128 + p.hq * D;  // row index in this layer's wqkv
         kind = n0 < (p.hq + p.hkv) * D ? 1 : 2;
         layer = group;
-        kgain = p.kn_gain[group];
+        if (kind == 1) load_head_gain(p.kn_gain[group], D, lane, g);
       }
       const bool* live = tc->live;
+      const bool* inj = tc->inj;
       const int* pos = tc->pos;
       const int* pg = tc->pg;
       const float2* c0 = tc->c0;
@@ -289,10 +317,11 @@ DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, con
 #pragma unroll
       for (int q = 0; q < EPI_TOK; ++q) {
         if (!live[q]) continue;  // warp-uniform
+        if (kind == 0 && inj[q]) continue;  // fused-feature rows only append K/V
         float xv[4];
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) xv[jj] = x[q][jj] * s[q];
-        if (kind < 2) head_norm_rope(xv, kgain, c0[q], c1[q], D, p.eps, lane);
+        if (kind < 2) head_norm_rope(xv, g, c0[q], c1[q], D, p.eps, lane);
         if (kind == 0) {
 #pragma unroll
           for (int jj = 0; jj < 4; ++jj)
@@ -503,11 +532,21 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
     const int r = q * 32 + lane;  // TMEM lane = tile row
     const int et = threadIdx.x - 64;
     const int ew = et >> 5;
-    TokCtx pre_ctx;
-    const TokCtx* pre = nullptr;
+    TokCtx pre0, pre1;
+    bool use_pre = false;
+    float gq[4], gk[4];
+    if (MODE == GM_QKV) {
+      load_head_gain(p.qn_gain, p.D, lane, gq);
+      load_head_gain(p.kn_gain[0], p.D, lane, gk);
+    }
     if (MODE != GM_RESID && MODE != GM_FC && p.t_tiles == 1) {
-      gather_ctx<MODE>(p, 0, ew, p.M < 16 ? p.M : 16, lane, pre_ctx);
-      pre = &pre_ctx;
+      const int nt0 = p.M < 32 ? p.M : 32;  // the first chunk's tokens
+      gather_ctx<MODE>(p, 0, ew, nt0, lane, pre0);
+      if (nt0 > 16)
+        gather_ctx<MODE>(p, 0, ew + 16, nt0, lane, pre1);
+      else
+        pre1 = pre0;
+      use_pre = true;
     }
     int seg = 0;
     for (long long u = u0; u < u1; ++seg) {
@@ -516,6 +555,20 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
       u = seg_end;
       const int abuf = seg & 1;
       const uint32_t use = (uint32_t)(seg >> 1);
+      // RESID, one token tile: this tile's residual inputs for the first 16
+      // tokens, loaded while the accumulators and the split reduction finish
+      float hpre[EPI_TOK][4];
+      const bool use_hpre = MODE == GM_RESID && p.t_tiles == 1;
+      if (use_hpre) {
+        const int n0 = (int)(tile % p.n_tiles) * 128;
+#pragma unroll
+        for (int q4 = 0; q4 < EPI_TOK; ++q4)
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            const int j = ew + 4 * q4;
+            hpre[q4][jj] = j < p.M ? p.h[(size_t)j * p.N + n0 + lane + 32 * jj] : 0.f;
+          }
+      }
       if (!mbar_wait(tfull + abuf, use & 1u, p.status, &aborted)) break;
       tc_fence_after();
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(abuf * BN);
@@ -587,8 +640,8 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
           }
         }
         named_bar_sync(1, EPI_THREADS);
-        epi_final<MODE>(p, (int)tile, t_base + tc0, (mt - tc0) < 32 ? (mt - tc0) : 32, stg, ew, lane,
-                        pre);
+        epi_final<MODE>(p, (int)tile, t_base + tc0, (mt - tc0) < 32 ? (mt - tc0) : 32, stg, ew, lane, use_pre,
+                        pre0, pre1, gq, gk, use_hpre, hpre);
         named_bar_sync(1, EPI_THREADS);
       }
       if (!split) {

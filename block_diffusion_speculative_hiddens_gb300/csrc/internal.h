@@ -63,8 +63,14 @@ struct GemmParams {
   int rows_per_req; // inject: feature rows per request; QKV/ARGMAX: block (16)
   float eps;
   // norm scales
-  const float* ss_in;  // [ss_parts][M] sums of squares of the normalised input
+  const float* ss_in;  // [ss_parts][ss_ld] sums of squares of the normalised input
   int ss_parts;
+  int ss_ld;           // leading dimension of ss_in (token rows of the producer)
+  // QKV with folded KV injection: token rows >= inj_m0 are fused-feature rows
+  // (request (t-inj_m0)/rows_per_req), scaled by ss_inj [ss_parts][inj_ld]
+  int inj_m0;          // 0: no injection rows
+  const float* ss_inj;
+  int inj_ld;
   float* ss_out;       // [n_tiles][M]
   // tensors
   float* h;             // RESID: fp32 residual [M][N]

@@ -40,6 +40,11 @@ class RoundState:
     def draft_block(self, stream=None):
         self.d.draft_block(self.slots, self.bonus, self.draft, stream)
 
+    def draft_round(self, stream=None):
+        """inject + draft_block as one call (injection folded into each layer's QKV GEMM)."""
+        self.d.draft_round(self.slots, self.feats, self.d.cfg.block, self.accept_len, self.bonus, self.draft,
+                           stream)
+
     def accept(self, stream=None):
         self.d.accept_trim(self.slots, self.draft, self.target, self.accept_len, self.bonus,
                            self.ctx_len, stream)
@@ -69,9 +74,16 @@ class SyntheticVerify:
                            None if fs is None else s.feats, stream)
 
 
-def run_round(state: RoundState, verify, stream=None):
-    """One drafting-plus-acceptance round on the given stream."""
-    state.inject(stream)
-    state.draft_block(stream)
+def run_round(state: RoundState, verify, stream=None, folded: bool = True):
+    """One drafting-plus-acceptance round on the given stream.
+
+    folded=True uses dflash_draft_round (injection folded into the layers' QKV
+    projections); False issues dflash_fuse_inject and dflash_draft_block.
+    """
+    if folded:
+        state.draft_round(stream)
+    else:
+        state.inject(stream)
+        state.draft_block(stream)
     verify(stream)
     state.accept(stream)

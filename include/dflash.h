@@ -154,6 +154,17 @@ DFLASH_API int dflash_fuse_inject(dflash_handle* h, const int32_t* slots, int32_
 DFLASH_API int dflash_draft_block(dflash_handle* h, const int32_t* slots, int32_t batch,
                        const int32_t* last_tok, int32_t* draft, void* stream);
 
+/* a1-a6 in one call: exactly dflash_fuse_inject(slots, batch, feats,
+ * rows_per_req, n_new) followed by dflash_draft_block(slots, batch, last_tok,
+ * draft), with the K/V injection of the new rows computed inside each draft
+ * layer's own QKV projection (the rows ride along as extra tokens of that
+ * GEMM), so every layer's K/V weights are read once per round instead of
+ * twice.  Used when rows_per_req <= 16 and batch*(16 + rows_per_req) <= 256;
+ * otherwise it runs the two calls. */
+DFLASH_API int dflash_draft_round(dflash_handle* h, const int32_t* slots, int32_t batch, const void* feats,
+                                  int32_t rows_per_req, const int32_t* n_new, const int32_t* last_tok,
+                                  int32_t* draft, void* stream);
+
 /* a7.  Longest-prefix acceptance (cumulative product of matches,
  * "DFlash原理深度剖析…", §三 第3步).  draft [batch,15], target [batch,16] (the
  * target's token after each block position).  Outputs (DEVICE int32 [batch]):

@@ -79,7 +79,7 @@ class GpuRun:
                 feats = self.feat_stream[j:j + 1, p0:p0 + n]
                 self.d.fuse_inject(slot, feats, n, torch.tensor([n], dtype=torch.int32, device=self.dev))
 
-    def round(self, debug=False):
+    def round(self, debug=False, folded=True):
         """One round; returns dict of host arrays (draft, target, tau, bonus, ctx) and debug tensors."""
         import torch
         from block_diffusion_speculative_hiddens_gb300.session import run_round
@@ -97,7 +97,7 @@ class GpuRun:
             out["hidden"] = to_np(hidden).reshape(B, cfg.block, cfg.hidden)
             out["logits"] = to_np(logits).reshape(B, cfg.block, cfg.vocab)
         else:
-            run_round(s, self.verify)
+            run_round(s, self.verify, folded=folded)
         torch.cuda.synchronize()
         out.update(draft=to_np(s.draft).astype(np.int64), target=to_np(s.target).astype(np.int64),
                    tau=to_np(s.accept_len).astype(np.int64), bonus=to_np(s.bonus).astype(np.int64),

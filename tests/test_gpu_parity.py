@@ -73,6 +73,32 @@ def test_rounds_accept_bit_exact(lib, name, rounds):
     assert np.array_equal(lens + to_np(g.state.accept_len), [od["ctx"] for od in oo])
 
 
+@pytest.mark.parametrize("name", ["tiny-gains", "small-batch"])
+def test_folded_round_equals_separate_calls(lib, name):
+    """dflash_draft_round (K/V injection inside each layer's QKV GEMM) against
+    dflash_fuse_inject + dflash_draft_block on the same inputs: the same
+    acceptance every round, and the same injected K/V up to the fp32
+    summation order of a differently split reduction."""
+    cfg = get_config(name)
+    w = make_weights(cfg)
+    a = GpuRun(cfg, 4, weights_np=w)
+    b = GpuRun(cfg, 4, weights_np=w)
+    a.prefill()
+    b.prefill()
+    for r in range(4):
+        ea = a.round(folded=True)
+        eb = b.round(folded=False)
+        for key in ("tau", "bonus", "ctx"):
+            assert np.array_equal(ea[key], eb[key]), (r, key)
+    for j in range(len(a.ids)):
+        L = int(to_np(a.d.slot_lengths(a.state.slots))[j])
+        for l in range(cfg.n_layers):
+            ka, va = a.d.read_kv(l, j, 0, L)
+            kb, vb = b.d.read_kv(l, j, 0, L)
+            assert rel_l2(to_np(ka), to_np(kb)) < 1e-3 and rel_l2(to_np(va), to_np(vb)) < 1e-3, (j, l)
+    assert a.d.read_status() == 0 and b.d.read_status() == 0
+
+
 def test_context_kv_unchanged_by_later_rounds(lib):
     cfg, g, o = _pair("small", 4)
     L = int(g.ctx0[0])
