@@ -46,8 +46,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=25.0)
-    ap.add_argument("--separate-inject", action="store_true",
-                    help="issue dflash_fuse_inject + dflash_draft_block instead of dflash_draft_round")
+    ap.add_argument("--fold-inject", action="store_true",
+                    help="issue dflash_draft_round instead of dflash_fuse_inject + dflash_draft_block")
     return ap.parse_args()
 
 
@@ -197,7 +197,7 @@ def run_gpu(args, rank, world, local_rank):
     wst, wv = states[-1], verifies[-1]
     d.graph_begin(stream)
     for _ in range(W):
-        run_round(wst, wv, stream, folded=not args.separate_inject)
+        run_round(wst, wv, stream, folded=args.fold_inject)
     d.graph_end(stream)
     d.graph_launch(stream)
     stream.synchronize()
@@ -207,7 +207,7 @@ def run_gpu(args, rank, world, local_rank):
     n0 = d.launch_count()
     d.graph_begin(stream)
     for i in range(K):
-        run_round(states[i // R], verifies[i // R], stream, folded=not args.separate_inject)
+        run_round(states[i // R], verifies[i // R], stream, folded=args.fold_inject)
     n_kernels = d.graph_end(stream)
     launches_captured = d.launch_count() - n0
     stream.synchronize()
@@ -256,7 +256,7 @@ def run_gpu(args, rank, world, local_rank):
         u_dev = torch.zeros_like(m_dev)
         ver = SyntheticVerify(st, m_dev, u_dev, None)
         d.graph_begin(stream)
-        run_round(st, ver, stream, folded=not args.separate_inject)
+        run_round(st, ver, stream, folded=args.fold_inject)
         d.graph_end(stream)
         feats_h = torch.empty(1, 16, F, dtype=torch.bfloat16).pin_memory()
         mu_h = torch.empty(2, 16, dtype=torch.int32).pin_memory()
@@ -325,8 +325,8 @@ def run_gpu(args, rank, world, local_rank):
                                f"{cfg.head_dim}, I{cfg.intermediate}, {cfg.n_layers} layers, V{V}, fusion "
                                f"{F}->{H}, prompt {L0}, block 16, match p {cfg.match_p}",
                    "batch": B, "prompt": L0, "rounds_per_slot": R,
-                   "round_call": "dflash_fuse_inject+dflash_draft_block" if args.separate_inject
-                   else "dflash_draft_round", "slots": n_slots - 1,
+                   "round_call": "dflash_draft_round" if args.fold_inject
+                   else "dflash_fuse_inject+dflash_draft_block", "slots": n_slots - 1,
                    "l2": "inputs larger than L2 (3.3 GB of weights stream every round)",
                    "parallelism": f"replicas x{world}"},
         "gpu_launches": launches_captured,

@@ -293,7 +293,7 @@ int run_gemm(dflash_handle* h, cudaStream_t s, int mode, const void* const* a, i
   p.ab_type = ab_type;
   p.total_tiles = groups * n_tiles * t_tiles;
   p.allow_split = allow_split ? 1 : 0;
-  p.stages = gemm_pick_stages(BN);
+  p.stages = gemm_pick_stages(BN, mode);
   int cols = 32;
   while (cols < 2 * BN) cols *= 2;
   p.tmem_cols = cols;
@@ -881,7 +881,7 @@ int noalloc_gemm(dflash_handle* h, cudaStream_t s, int mode, const void* const* 
   p.ab_type = ab_type;
   p.total_tiles = groups * n_tiles;
   p.allow_split = 1;
-  p.stages = gemm_pick_stages(BN);
+  p.stages = gemm_pick_stages(BN, mode);
   int cols = 32;
   while (cols < 2 * BN) cols *= 2;
   p.tmem_cols = cols;

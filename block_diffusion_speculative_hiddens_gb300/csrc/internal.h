@@ -115,7 +115,7 @@ struct AttnParams {
 
 // host launchers (gemm.cu / attention.cu / small.cu)
 size_t gemm_smem_bytes(int BN, int stages);
-int gemm_pick_stages(int BN);
+int gemm_pick_stages(int BN, int mode);
 cudaError_t gemm_launch(const CUtensorMap& B, const GemmParams& p, int grid, cudaStream_t s, bool pdl);
 cudaError_t gemm_init_attributes();
 

@@ -74,11 +74,12 @@ class SyntheticVerify:
                            None if fs is None else s.feats, stream)
 
 
-def run_round(state: RoundState, verify, stream=None, folded: bool = True):
+def run_round(state: RoundState, verify, stream=None, folded: bool = False):
     """One drafting-plus-acceptance round on the given stream.
 
-    folded=True uses dflash_draft_round (injection folded into the layers' QKV
-    projections); False issues dflash_fuse_inject and dflash_draft_block.
+    folded=False issues dflash_fuse_inject and dflash_draft_block (the faster
+    order at batch 1 on GB300); True uses dflash_draft_round, which computes
+    the injection inside the layers' QKV projections.
     """
     if folded:
         state.draft_round(stream)

@@ -79,7 +79,7 @@ class GpuRun:
                 feats = self.feat_stream[j:j + 1, p0:p0 + n]
                 self.d.fuse_inject(slot, feats, n, torch.tensor([n], dtype=torch.int32, device=self.dev))
 
-    def round(self, debug=False, folded=True):
+    def round(self, debug=False, folded=False):
         """One round; returns dict of host arrays (draft, target, tau, bonus, ctx) and debug tensors."""
         import torch
         from block_diffusion_speculative_hiddens_gb300.session import run_round

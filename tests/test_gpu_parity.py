@@ -58,11 +58,12 @@ def test_draft_round_matches_oracle(lib, name):
     assert g.d.read_status() == 0
 
 
+@pytest.mark.parametrize("folded", [False, True], ids=["separate", "folded"])
 @pytest.mark.parametrize("name,rounds", [("tiny", 8), ("small-batch", 4)])
-def test_rounds_accept_bit_exact(lib, name, rounds):
+def test_rounds_accept_bit_exact(lib, name, rounds, folded):
     cfg, g, o = _pair(name, rounds)
     for r in range(rounds):
-        go = g.round()
+        go = g.round(folded=folded)
         oo = o.round(want_logits=False)
         for j, od in enumerate(oo):
             assert 1 <= go["tau"][j] <= 16

@@ -103,6 +103,11 @@ TEST_CONFIGS = {
         intermediate=768, n_layers=2, vocab=5000, rope_theta=5e5, batch=3, ctx0=None,
         rounds=4, match_p=None, ctx_range=(30, 300), p_range=(0.5, 0.95), gain_std=0.1,
         weight_std=0.05),
+    # Mid-size shape for detailed hardware-counter captures: the tied
+    # embedding (134 MB) is larger than L2, the whole drafter stays under 1 GB.
+    "mid": DraftConfig(
+        name="mid", hidden=2048, n_q_heads=16, n_kv_heads=4, head_dim=128, intermediate=6144,
+        n_layers=2, vocab=32768, rope_theta=1e6, batch=1, ctx0=1024, rounds=8, match_p=0.9),
 }
 
 
