@@ -2,8 +2,8 @@
 // mask, to [context K/V ; block K/V] of their KV head (grouped-query attention).
 //
 // Grid (split, kv_head, request).  One CTA owns the G = hq/hkv query heads of
-// one KV head (G warps, 16 block rows each) and a contiguous range of the
-// request's 64-position pages.  Each page of K (64 x D) and V^T (D x 64) is a
+// one KV head (16 block rows each) and a contiguous range of the request's
+// 64-position pages.  Each page of K (64 x D) and V^T (D x 64) is a
 // contiguous 2 x 8..16 KB block stored pre-swizzled in HBM, so an untiled TMA
 // bulk copy lands it in shared memory already in a bank-conflict-free layout
 // for ldmatrix.  Q.K^T and P.V run on warp MMAs (m16n8k16, f16 in, fp32
@@ -19,7 +19,10 @@ namespace {
 
 template <int D>
 struct AttnCfg {
-  static constexpr int STAGES = D == 128 ? 6 : 8;            // pages in flight per CTA
+#ifndef DFL_ATTN_STAGES
+#define DFL_ATTN_STAGES 6
+#endif
+  static constexpr int STAGES = D == 128 ? DFL_ATTN_STAGES : 8;  // pages in flight per CTA
   static constexpr int BLK_BYTES = 64 * D * 2;               // one K (or V) page block
   static constexpr int STAGE_BYTES = 2 * BLK_BYTES;
   static constexpr int MAX_PIDS = 512;                       // page ids prefetched to shared memory
@@ -35,15 +38,25 @@ DFL_DEV void atrace(const AttnParams& p, int ev) {
   }
 }
 
-template <int D, int G>
-__global__ void __launch_bounds__(G * 32) k_attn(const AttnParams p) {
+// KS warps per query head split every page's 64 keys between them (KS = 2
+// for G <= 4), each with its own online softmax, merged in shared memory at
+// the end: twice the warps in flight and half the dependent MMA chain per
+// page for the common GQA group sizes.
+template <int D, int G, int KS>
+__global__ void __launch_bounds__(G * KS * 32) k_attn(const AttnParams p) {
   using C = AttnCfg<D>;
+  constexpr int KPW = 64 / KS;   // keys of a page per warp
+  constexpr int NKG = KPW / 16;  // 16-key groups per warp
+  constexpr int PS = D + 4;      // padded row stride (floats) of a partial
   extern __shared__ __align__(128) uint8_t sm[];
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + C::STAGES * C::STAGE_BYTES);
   int* pids = reinterpret_cast<int*>(sm + C::STAGES * C::STAGE_BYTES + 128);
 
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int head0 = kvh * G;  // first query head
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int hw = warp % G;    // query head of this warp within the group
+  const int half = warp / G;  // which KPW keys of every page
   const int g = lane >> 2, c4 = lane & 3;
   const int rows = G * 16;
   const int hq = p.hq, hkv = p.hkv;
@@ -59,9 +72,8 @@ __global__ void __launch_bounds__(G * 32) k_attn(const AttnParams p) {
   const int slot = p.slots[b];
   const int nkeys = p.ctx_len[slot] + DFL_BLOCK;
   const int npages = (nkeys + 63) >> 6;
-  const int per = (npages + p.n_splits - 1) / p.n_splits;
-  const int pb = split * per;
-  const int pe = min(npages, pb + per);
+  const int pb = (int)((long long)split * npages / p.n_splits);  // balanced page ranges
+  const int pe = (int)((long long)(split + 1) * npages / p.n_splits);
   const f16* kbase = p.kv.k_pool + (size_t)p.layer * p.kv.layer_stride;
   const f16* vbase = p.kv.v_pool + (size_t)p.layer * p.kv.layer_stride;
   const int* pt = p.kv.page_table + (size_t)slot * p.kv.max_pages_per_slot;
@@ -89,7 +101,7 @@ __global__ void __launch_bounds__(G * 32) k_attn(const AttnParams p) {
     for (int i = 0; i < C::STAGES && pb + i < pe; ++i, ++issued) issue(i, pb + i);
 
   // Q fragments of this warp's query head (16 block rows x D) in registers.
-  const int j = kvh * G + warp;
+  const int j = head0 + hw;
   uint32_t qa[D / 16][4];
   {
     const f16* q0 = p.q + ((size_t)(b * DFL_BLOCK) * hq + j) * D;
@@ -120,15 +132,15 @@ __global__ void __launch_bounds__(G * 32) k_attn(const AttnParams p) {
       const int valid = min(64, nkeys - pi * 64);
       const uint32_t kb_addr = smem_u32(sm + s * C::STAGE_BYTES);
       const uint32_t vb_addr = kb_addr + C::BLK_BYTES;
-      float sc[8][4];
+      float sc[2 * NKG][4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
-      // S = Q K^T over this page's 64 keys
+      for (int i = 0; i < 2 * NKG; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
+      // S = Q K^T over this warp's keys of the page
 #pragma unroll
-      for (int kg = 0; kg < 4; ++kg) {
+      for (int kg = 0; kg < NKG; ++kg) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const int key = kg * 16 + (mi >> 1) * 8 + rr;
+          const int key = half * KPW + kg * 16 + (mi >> 1) * 8 + rr;
           const int chunk = kk * 2 + (mi & 1);
           const uint32_t addr =
               kb_addr + 2u * (uint32_t)((chunk >> 3) * (64 * 64) + key * 64 + (((chunk & 7) ^ (key & 7)) << 3));
@@ -138,13 +150,14 @@ __global__ void __launch_bounds__(G * 32) k_attn(const AttnParams p) {
           mma_f16_16816(sc[2 * kg + 1], qa[kk], b2, b3);
         }
       }
-      // online softmax (log2 domain), rows g and g+8 of this warp
+      // online softmax (log2 domain), rows g and g+8 of this warp; a row
+      // whose keys so far are all masked keeps max -inf and contributes 0
       float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
+      for (int nt = 0; nt < 2 * NKG; ++nt) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int key = nt * 8 + 2 * c4 + (e & 1);
+          const int key = half * KPW + nt * 8 + 2 * c4 + (e & 1);
           float v = sc[nt][e] * p.scale_log2;
           if (key >= valid) v = -INFINITY;
           sc[nt][e] = v;
@@ -157,14 +170,15 @@ __global__ void __launch_bounds__(G * 32) k_attn(const AttnParams p) {
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
       const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-      const float a0 = exp2f(m0 - mn0), a1 = exp2f(m1 - mn1);
+      const float ref0 = mn0 == -INFINITY ? 0.f : mn0, ref1 = mn1 == -INFINITY ? 0.f : mn1;
+      const float a0 = exp2f(m0 - ref0), a1 = exp2f(m1 - ref1);
       float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
-        sc[nt][0] = exp2f(sc[nt][0] - mn0);
-        sc[nt][1] = exp2f(sc[nt][1] - mn0);
-        sc[nt][2] = exp2f(sc[nt][2] - mn1);
-        sc[nt][3] = exp2f(sc[nt][3] - mn1);
+      for (int nt = 0; nt < 2 * NKG; ++nt) {
+        sc[nt][0] = exp2f(sc[nt][0] - ref0);
+        sc[nt][1] = exp2f(sc[nt][1] - ref0);
+        sc[nt][2] = exp2f(sc[nt][2] - ref1);
+        sc[nt][3] = exp2f(sc[nt][3] - ref1);
         rs0 += sc[nt][0] + sc[nt][1];
         rs1 += sc[nt][2] + sc[nt][3];
       }
@@ -181,7 +195,7 @@ __global__ void __launch_bounds__(G * 32) k_attn(const AttnParams p) {
       }
       // O += P V  (V^T page: rows = dims, 64 keys per row)
 #pragma unroll
-      for (int k2 = 0; k2 < 4; ++k2) {
+      for (int k2 = 0; k2 < NKG; ++k2) {
         uint32_t pa[4];
         pa[0] = pack_f16x2(sc[2 * k2][0], sc[2 * k2][1]);
         pa[1] = pack_f16x2(sc[2 * k2][2], sc[2 * k2][3]);
@@ -190,7 +204,7 @@ __global__ void __launch_bounds__(G * 32) k_attn(const AttnParams p) {
 #pragma unroll
         for (int nd = 0; nd < D / 8; nd += 2) {
           const int dim = (nd + (mi >> 1)) * 8 + rr;
-          const int chunk = 2 * k2 + (mi & 1);
+          const int chunk = 2 * (half * NKG + k2) + (mi & 1);
           const uint32_t addr = vb_addr + 2u * (uint32_t)(dim * 64 + ((chunk ^ (dim & 7)) << 3));
           uint32_t b0, b1, b2, b3;
           ldsm_x4(addr, b0, b1, b2, b3);
@@ -218,62 +232,112 @@ __global__ void __launch_bounds__(G * 32) k_attn(const AttnParams p) {
   l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-  const int r0 = warp * 16 + g, r1 = r0 + 8;
+  const int r0 = hw * 16 + g, r1 = r0 + 8;
+
+  // partial layout in shared memory: [rows][PS] unnormalised O, then the
+  // running max [rows] and running sum [rows]
+  float* part = reinterpret_cast<float*>(sm);
+  if (KS == 2) {
+    // the second key half of every head hands its state to the first
+    constexpr int PART_FLOATS = G * 16 * PS + 2 * G * 16;
+    float* xch = part + ((PART_FLOATS + 31) & ~31);
+    __syncthreads();  // every warp is past its last read of the page stages
+    if (half == 1) {
+#pragma unroll
+      for (int nd = 0; nd < D / 8; ++nd) {
+        const int d = nd * 8 + 2 * c4;
+        *reinterpret_cast<float2*>(xch + r0 * PS + d) = make_float2(o[nd][0], o[nd][1]);
+        *reinterpret_cast<float2*>(xch + r1 * PS + d) = make_float2(o[nd][2], o[nd][3]);
+      }
+      if (c4 == 0) {
+        xch[rows * PS + r0] = m0;
+        xch[rows * PS + r1] = m1;
+        xch[rows * PS + rows + r0] = l0;
+        xch[rows * PS + rows + r1] = l1;
+      }
+    }
+    __syncthreads();
+    if (half == 0) {
+      const float mb0 = xch[rows * PS + r0], mb1 = xch[rows * PS + r1];
+      const float lb0 = xch[rows * PS + rows + r0], lb1 = xch[rows * PS + rows + r1];
+      const float M0 = fmaxf(l0 > 0.f ? m0 : -INFINITY, lb0 > 0.f ? mb0 : -INFINITY);
+      const float M1 = fmaxf(l1 > 0.f ? m1 : -INFINITY, lb1 > 0.f ? mb1 : -INFINITY);
+      const float wa0 = l0 > 0.f ? exp2f(m0 - M0) : 0.f, wb0 = lb0 > 0.f ? exp2f(mb0 - M0) : 0.f;
+      const float wa1 = l1 > 0.f ? exp2f(m1 - M1) : 0.f, wb1 = lb1 > 0.f ? exp2f(mb1 - M1) : 0.f;
+#pragma unroll
+      for (int nd = 0; nd < D / 8; ++nd) {
+        const int d = nd * 8 + 2 * c4;
+        const float2 x0 = *reinterpret_cast<const float2*>(xch + r0 * PS + d);
+        const float2 x1 = *reinterpret_cast<const float2*>(xch + r1 * PS + d);
+        o[nd][0] = o[nd][0] * wa0 + x0.x * wb0;
+        o[nd][1] = o[nd][1] * wa0 + x0.y * wb0;
+        o[nd][2] = o[nd][2] * wa1 + x1.x * wb1;
+        o[nd][3] = o[nd][3] * wa1 + x1.y * wb1;
+      }
+      l0 = l0 * wa0 + lb0 * wb0;
+      l1 = l1 * wa1 + lb1 * wb1;
+      m0 = M0;
+      m1 = M1;
+    }
+  }
 
   if (p.n_splits == 1) {
-    const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
-    f16* out0 = p.out + ((size_t)(b * DFL_BLOCK + g) * hq + j) * D;
-    f16* out1 = p.out + ((size_t)(b * DFL_BLOCK + g + 8) * hq + j) * D;
+    if (half == 0) {
+      const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
+      f16* out0 = p.out + ((size_t)(b * DFL_BLOCK + g) * hq + j) * D;
+      f16* out1 = p.out + ((size_t)(b * DFL_BLOCK + g + 8) * hq + j) * D;
 #pragma unroll
-    for (int nd = 0; nd < D / 8; ++nd) {
-      const int d = nd * 8 + 2 * c4;
-      *reinterpret_cast<uint32_t*>(out0 + d) = pack_f16x2(o[nd][0] * i0, o[nd][1] * i0);
-      *reinterpret_cast<uint32_t*>(out1 + d) = pack_f16x2(o[nd][2] * i1, o[nd][3] * i1);
+      for (int nd = 0; nd < D / 8; ++nd) {
+        const int d = nd * 8 + 2 * c4;
+        *reinterpret_cast<uint32_t*>(out0 + d) = pack_f16x2(o[nd][0] * i0, o[nd][1] * i0);
+        *reinterpret_cast<uint32_t*>(out1 + d) = pack_f16x2(o[nd][2] * i1, o[nd][3] * i1);
+      }
     }
     if (threadIdx.x == 0) atrace(p, 5);
     return;
   }
 
   // Splits of one (request, KV head) form a thread-block cluster: each CTA
-  // leaves its partial (unnormalised O, running max, running sum) in its own
-  // shared memory, the cluster barrier publishes them, and CTA r merges rows
-  // r*rows/n .. of the output from all partials over distributed shared
-  // memory, in split order.  No global scratch, no counters, no waiting
-  // beyond the hardware barrier.
-  constexpr int PS = D + 4;  // padded row stride (floats) of a partial
-  float* part = reinterpret_cast<float*>(sm);  // [rows][PS], then m[rows], l[rows]
+  // leaves its partial in its own shared memory, the cluster barrier
+  // publishes them, and CTA r merges rows r*rows/n .. of the output from all
+  // partials over distributed shared memory, in split order -- every value a
+  // thread needs (each split's max, sum and O piece) loaded at once.
+  if (half == 0) {
 #pragma unroll
-  for (int nd = 0; nd < D / 8; ++nd) {
-    const int d = nd * 8 + 2 * c4;
-    *reinterpret_cast<float2*>(part + r0 * PS + d) = make_float2(o[nd][0], o[nd][1]);
-    *reinterpret_cast<float2*>(part + r1 * PS + d) = make_float2(o[nd][2], o[nd][3]);
-  }
-  if (c4 == 0) {
-    part[rows * PS + r0] = m0;
-    part[rows * PS + r1] = m1;
-    part[rows * PS + rows + r0] = l0;
-    part[rows * PS + rows + r1] = l1;
+    for (int nd = 0; nd < D / 8; ++nd) {
+      const int d = nd * 8 + 2 * c4;
+      *reinterpret_cast<float2*>(part + r0 * PS + d) = make_float2(o[nd][0], o[nd][1]);
+      *reinterpret_cast<float2*>(part + r1 * PS + d) = make_float2(o[nd][2], o[nd][3]);
+    }
+    if (c4 == 0) {
+      part[rows * PS + r0] = m0;
+      part[rows * PS + r1] = m1;
+      part[rows * PS + rows + r0] = l0;
+      part[rows * PS + rows + r1] = l1;
+    }
   }
   if (threadIdx.x == 0) atrace(p, 4);
   cluster_sync_all();
 
   const int n = p.n_splits;
   const int rank = (int)cluster_ctarank();
-  const int rpc = (rows + n - 1) / n;           // rows merged by this CTA
+  const int rpc = (rows + n - 1) / n;  // rows merged by this CTA
   const int rb = rank * rpc, re = min(rows, rb + rpc);
   const uint32_t part_local = smem_u32(part);
-  float* wsm = part + rows * PS + 2 * rows;     // [n][rpc] merge weights (local)
-  for (int rr = threadIdx.x; rr < re - rb; rr += blockDim.x) {
-    const int r = rb + rr;
+  for (int e = threadIdx.x; e < (re - rb) * (D / 4); e += blockDim.x) {
+    const int r = rb + e / (D / 4), d = (e % (D / 4)) * 4;
     float mv[8], lv[8];
+    float4 v[8];
 #pragma unroll
     for (int sp = 0; sp < 8; ++sp) {
       mv[sp] = -INFINITY;
       lv[sp] = 0.f;
+      v[sp] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (sp < n) {
         const uint32_t a = dsmem_addr(part_local, (uint32_t)sp);
         mv[sp] = ld_dsmem(a + 4u * (uint32_t)(rows * PS + r));
         lv[sp] = ld_dsmem(a + 4u * (uint32_t)(rows * PS + rows + r));
+        v[sp] = ld_dsmem4(a + 4u * (uint32_t)(r * PS + d));
       }
     }
     float M = -INFINITY;
@@ -288,21 +352,11 @@ __global__ void __launch_bounds__(G * 32) k_attn(const AttnParams p) {
       L += w * lv[sp];
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
-    for (int sp = 0; sp < n; ++sp) wsm[sp * rpc + rr] = mv[sp] * inv;
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < (re - rb) * (D / 4); e += blockDim.x) {
-    const int rr = e / (D / 4), d = (e % (D / 4)) * 4;
-    const int r = rb + rr;
-    float4 v[8];
-#pragma unroll
-    for (int sp = 0; sp < 8; ++sp)
-      if (sp < n) v[sp] = ld_dsmem4(dsmem_addr(part_local, (uint32_t)sp) + 4u * (uint32_t)(r * PS + d));
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int sp = 0; sp < 8; ++sp) {
       if (sp < n) {
-        const float w = wsm[sp * rpc + rr];
+        const float w = mv[sp] * inv;
         acc.x += w * v[sp].x;
         acc.y += w * v[sp].y;
         acc.z += w * v[sp].z;
@@ -310,7 +364,7 @@ __global__ void __launch_bounds__(G * 32) k_attn(const AttnParams p) {
       }
     }
     const int wq = r / 16, t = r % 16;
-    f16* dst = p.out + ((size_t)(b * DFL_BLOCK + t) * hq + kvh * G + wq) * D + d;
+    f16* dst = p.out + ((size_t)(b * DFL_BLOCK + t) * hq + head0 + wq) * D + d;
     *reinterpret_cast<uint32_t*>(dst) = pack_f16x2(acc.x, acc.y);
     *reinterpret_cast<uint32_t*>(dst + 2) = pack_f16x2(acc.z, acc.w);
   }
@@ -319,11 +373,17 @@ __global__ void __launch_bounds__(G * 32) k_attn(const AttnParams p) {
   if (threadIdx.x == 0) atrace(p, 5);
 }
 
+// key split per head: 2 warps per query head up to 4 heads per KV head
+template <int G>
+constexpr int attn_ks() {
+  return G <= 4 ? 2 : 1;
+}
+
 template <int D, int G>
 cudaError_t launch_t(const AttnParams& p, int batch, cudaStream_t s, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.n_splits, (unsigned)p.hkv, (unsigned)batch);
-  cfg.blockDim = dim3(G * 32);
+  cfg.blockDim = dim3(G * attn_ks<G>() * 32);
   cfg.dynamicSmemBytes = AttnCfg<D>::SMEM;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
@@ -335,7 +395,7 @@ cudaError_t launch_t(const AttnParams& p, int batch, cudaStream_t s, bool pdl) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, k_attn<D, G>, p);
+  return cudaLaunchKernelEx(&cfg, k_attn<D, G, attn_ks<G>()>, p);
 }
 
 template <int D>
@@ -352,13 +412,13 @@ cudaError_t launch_d(const AttnParams& p, int batch, cudaStream_t s, bool pdl) {
 template <int D>
 cudaError_t attr_d() {
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(k_attn<D, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnCfg<D>::SMEM)))
+  if ((e = cudaFuncSetAttribute(k_attn<D, 1, attn_ks<1>()>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnCfg<D>::SMEM)))
     return e;
-  if ((e = cudaFuncSetAttribute(k_attn<D, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnCfg<D>::SMEM)))
+  if ((e = cudaFuncSetAttribute(k_attn<D, 2, attn_ks<2>()>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnCfg<D>::SMEM)))
     return e;
-  if ((e = cudaFuncSetAttribute(k_attn<D, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnCfg<D>::SMEM)))
+  if ((e = cudaFuncSetAttribute(k_attn<D, 4, attn_ks<4>()>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnCfg<D>::SMEM)))
     return e;
-  return cudaFuncSetAttribute(k_attn<D, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnCfg<D>::SMEM);
+  return cudaFuncSetAttribute(k_attn<D, 8, attn_ks<8>()>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnCfg<D>::SMEM);
 }
 
 }  // namespace

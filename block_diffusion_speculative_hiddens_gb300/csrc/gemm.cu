@@ -62,36 +62,63 @@ DFL_DEV void load_head_gain(const float* gain, int D, int lane, float* g) {
   for (int j = 0; j < 4; ++j) g[j] = lane + 32 * j < D ? gain[lane + 32 * j] : 0.f;
 }
 
-// Head RMSNorm + RoPE on the 4 values a lane holds (rows lane, lane+32,
-// lane+64, lane+96 of a 128-row tile); g from load_head_gain; c0/c1 are the
-// (cos, sin) of RoPE frequencies lane and lane+32.  D = 128: one head, RoPE
-// pairs (0,2), (1,3).  D = 64: two heads (rows 0-63, 64-127), pairs (0,1) and
-// (2,3), frequency lane.
-DFL_DEV void head_norm_rope(float* x, const float* g, float2 c0, float2 c1, int D, float eps, int lane) {
+constexpr int EPI_TOK = 4;  // tokens per warp whose inputs are gathered together
+
+// Head RMSNorm + RoPE on the values a warp holds for EPI_TOK tokens (lane
+// holds rows lane, lane+32, lane+64, lane+96 of a 128-row tile); g from
+// load_head_gain; c0/c1[q] are token q's (cos, sin) of RoPE frequencies lane
+// and lane+32.  D = 128: one head, RoPE pairs (0,2), (1,3).  D = 64: two
+// heads (rows 0-63, 64-127), pairs (0,1) and (2,3), frequency lane.  The
+// norms' shuffle reductions of all tokens are interleaved, so the warp pays
+// one reduction latency, not one per token.
+DFL_DEV void head_norm_rope4(float (&x)[EPI_TOK][4], const float* g, const float2* c0, const float2* c1, int D,
+                             float eps) {
   if (D == 128) {
-    float ss = warp_sum(x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3]);
-    const float inv = rsqrtf(ss / 128.f + eps);
+    float ss[EPI_TOK];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) x[j] *= inv * g[j];
-    const float a0 = x[0], b0 = x[2], a1 = x[1], b1 = x[3];
-    x[0] = a0 * c0.x - b0 * c0.y;
-    x[2] = b0 * c0.x + a0 * c0.y;
-    x[1] = a1 * c1.x - b1 * c1.y;
-    x[3] = b1 * c1.x + a1 * c1.y;
+    for (int q = 0; q < EPI_TOK; ++q) ss[q] = x[q][0] * x[q][0] + x[q][1] * x[q][1] + x[q][2] * x[q][2] + x[q][3] * x[q][3];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+      for (int q = 0; q < EPI_TOK; ++q) ss[q] += __shfl_xor_sync(0xffffffffu, ss[q], o);
+#pragma unroll
+    for (int q = 0; q < EPI_TOK; ++q) {
+      const float inv = rsqrtf(ss[q] / 128.f + eps);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) x[q][j] *= inv * g[j];
+      const float a0 = x[q][0], b0 = x[q][2], a1 = x[q][1], b1 = x[q][3];
+      x[q][0] = a0 * c0[q].x - b0 * c0[q].y;
+      x[q][2] = b0 * c0[q].x + a0 * c0[q].y;
+      x[q][1] = a1 * c1[q].x - b1 * c1[q].y;
+      x[q][3] = b1 * c1[q].x + a1 * c1[q].y;
+    }
   } else {  // D == 64
-    const float sa = warp_sum(x[0] * x[0] + x[1] * x[1]);
-    const float sb = warp_sum(x[2] * x[2] + x[3] * x[3]);
-    const float ia = rsqrtf(sa / 64.f + eps), ib = rsqrtf(sb / 64.f + eps);
-    const float g0 = g[0], g1 = g[1];
-    x[0] *= ia * g0;
-    x[1] *= ia * g1;
-    x[2] *= ib * g0;
-    x[3] *= ib * g1;
-    const float a0 = x[0], b0 = x[1], a1 = x[2], b1 = x[3];
-    x[0] = a0 * c0.x - b0 * c0.y;
-    x[1] = b0 * c0.x + a0 * c0.y;
-    x[2] = a1 * c0.x - b1 * c0.y;
-    x[3] = b1 * c0.x + a1 * c0.y;
+    float sa[EPI_TOK], sb[EPI_TOK];
+#pragma unroll
+    for (int q = 0; q < EPI_TOK; ++q) {
+      sa[q] = x[q][0] * x[q][0] + x[q][1] * x[q][1];
+      sb[q] = x[q][2] * x[q][2] + x[q][3] * x[q][3];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+      for (int q = 0; q < EPI_TOK; ++q) {
+        sa[q] += __shfl_xor_sync(0xffffffffu, sa[q], o);
+        sb[q] += __shfl_xor_sync(0xffffffffu, sb[q], o);
+      }
+#pragma unroll
+    for (int q = 0; q < EPI_TOK; ++q) {
+      const float ia = rsqrtf(sa[q] / 64.f + eps), ib = rsqrtf(sb[q] / 64.f + eps);
+      x[q][0] *= ia * g[0];
+      x[q][1] *= ia * g[1];
+      x[q][2] *= ib * g[0];
+      x[q][3] *= ib * g[1];
+      const float a0 = x[q][0], b0 = x[q][1], a1 = x[q][2], b1 = x[q][3];
+      x[q][0] = a0 * c0[q].x - b0 * c0[q].y;
+      x[q][1] = b0 * c0[q].x + a0 * c0[q].y;
+      x[q][2] = a1 * c0[q].x - b1 * c0[q].y;
+      x[q][3] = b1 * c0[q].x + a1 * c0[q].y;
+    }
   }
 }
 
@@ -103,7 +130,6 @@ DFL_DEV int page_of(const GemmParams& p, int slot, int pos) {
   return (pg < 0 || pg >= p.kv.max_pages) ? -1 : pg;
 }
 
-constexpr int EPI_TOK = 4;  // tokens per warp whose inputs are gathered together
 
 // Per-token epilogue inputs of one warp's EPI_TOK tokens (j0, j0+4, ...):
 // the RMSNorm scale of the GEMM's input and, for QKV/INJECT, whether the row
@@ -226,21 +252,34 @@ DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, con
           hv[q][jj] = (MODE == GM_RESID && ok[q])
                           ? (hp ? hpre[q][jj] : p.h[(size_t)tq[q] * p.N + n0 + lane + 32 * jj])
                           : 0.f;
+      // the gain is read once, before any store (stores to h/out could alias it)
+      float gn[4];
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) gn[jj] = p.gain[n0 + lane + 32 * jj];
+      float sq[EPI_TOK];
+#pragma unroll
+      for (int q = 0; q < EPI_TOK; ++q) {
+        sq[q] = 0.f;
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          x[q][jj] += hv[q][jj];
+          sq[q] += x[q][jj] * x[q][jj];
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int q = 0; q < EPI_TOK; ++q) sq[q] += __shfl_xor_sync(0xffffffffu, sq[q], o);
 #pragma unroll
       for (int q = 0; q < EPI_TOK; ++q) {
         if (!ok[q]) continue;
-        float sq = 0.f;
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
-          const int n = n0 + lane + 32 * jj;
-          const size_t o = (size_t)tq[q] * p.N + n;
-          const float v = x[q][jj] + hv[q][jj];
-          if (MODE == GM_RESID) p.h[o] = v;
-          p.out[o] = to_f16(v * p.gain[n], p.status);
-          sq += v * v;
+          const size_t o = (size_t)tq[q] * p.N + n0 + lane + 32 * jj;
+          if (MODE == GM_RESID) p.h[o] = x[q][jj];
+          p.out[o] = to_f16(x[q][jj] * gn[jj], p.status);
         }
-        sq = warp_sum(sq);
-        if (lane == 0) p.ss_out[(size_t)nt * p.M + tq[q]] = sq;
+        if (lane == 0) p.ss_out[(size_t)nt * p.M + tq[q]] = sq[q];
       }
     } else {
     // per-token inputs: gathered at kernel start for the first 16 tokens of a
@@ -267,14 +306,14 @@ DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, con
       }
     } else if (MODE == GM_ARGMAX) {
       const int n0 = nt * 128;
+      unsigned long long best[EPI_TOK];
 #pragma unroll
       for (int q = 0; q < EPI_TOK; ++q) {
-        if (!ok[q]) continue;
-        unsigned long long best = 0ull;
+        best[q] = 0ull;
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
           const int n = n0 + lane + 32 * jj;
-          if (n < p.N) {
+          if (ok[q] && n < p.N) {
             const float v = x[q][jj] * s[q];
             if (v != v) {
               dev_error(p.status, DFLASH_DEV_NAN);
@@ -282,16 +321,20 @@ DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, con
             }
             if (p.logits) p.logits[(size_t)tq[q] * p.N + n] = v;
             const unsigned long long k = argmax_key(v, (uint32_t)n);
-            best = k > best ? k : best;
+            best[q] = k > best[q] ? k : best[q];
           }
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
-          best = other > best ? other : best;
-        }
-        if (lane == 0 && best) atomicMax(p.keys + tq[q], best);
       }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int q = 0; q < EPI_TOK; ++q) {
+          const unsigned long long other = __shfl_xor_sync(0xffffffffu, best[q], o);
+          best[q] = other > best[q] ? other : best[q];
+        }
+#pragma unroll
+      for (int q = 0; q < EPI_TOK; ++q)
+        if (ok[q] && lane == 0 && best[q]) atomicMax(p.keys + tq[q], best[q]);
     } else if (MODE == GM_QKV || MODE == GM_INJECT) {
       const int D = p.D;
       int n0, kind, layer;
@@ -315,13 +358,15 @@ DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, con
       const float2* c0 = tc->c0;
       const float2* c1 = tc->c1;
 #pragma unroll
+      for (int q = 0; q < EPI_TOK; ++q)
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) x[q][jj] *= s[q];
+      if (kind < 2) head_norm_rope4(x, g, c0, c1, D, p.eps);
+#pragma unroll
       for (int q = 0; q < EPI_TOK; ++q) {
         if (!live[q]) continue;  // warp-uniform
         if (kind == 0 && inj[q]) continue;  // fused-feature rows only append K/V
-        float xv[4];
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) xv[jj] = x[q][jj] * s[q];
-        if (kind < 2) head_norm_rope(xv, g, c0[q], c1[q], D, p.eps, lane);
+        const float* xv = x[q];
         if (kind == 0) {
 #pragma unroll
           for (int jj = 0; jj < 4; ++jj)
