@@ -310,6 +310,7 @@ int run_gemm(dflash_handle* h, cudaStream_t s, int mode, const void* const* a, i
   if (allow_split && p.total_tiles > h->max_tiles) return DFLASH_ERR_SHAPE;
   const long long units = allow_split ? (long long)p.total_tiles * p.kblocks : p.total_tiles;
   const int grid = (int)std::min<long long>(units, h->num_sms);
+  if (units * (grid + 1) >= (1LL << 31)) return DFLASH_ERR_SHAPE;  // the kernel's unit math is 32-bit
   if (kid && h->trace.kid == kid && h->trace.buf && grid <= h->trace.cap) {
     p.trace = h->trace.buf;  // one launch only
     h->trace.kid = 0;
@@ -898,6 +899,7 @@ int noalloc_gemm(dflash_handle* h, cudaStream_t s, int mode, const void* const* 
   if (p.total_tiles > NA_MAX_TILES) return DFLASH_ERR_CAPACITY;
   const long long units = (long long)p.total_tiles * p.kblocks;
   const int grid = (int)std::min<long long>(units, NA_MAX_CTAS);
+  if (units * (grid + 1) >= (1LL << 31)) return DFLASH_ERR_SHAPE;
   h->launches++;
   return cuda_err(gemm_launch(B, p, grid, s, h->pdl));
 }

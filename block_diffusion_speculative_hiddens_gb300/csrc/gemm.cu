@@ -45,9 +45,10 @@ constexpr int A_STAGE_BYTES = 128 * 128;  // 128 rows x 64 16-bit values
 constexpr int STG_BYTES = 32 * 128 * 4;   // epilogue staging: 32 tokens x 128 rows fp32
 constexpr int EPI_THREADS = 128;
 
-DFL_DEV long long unit_start(long long c, long long U, long long G) { return c * U / G; }
+// Unit arithmetic is 32-bit: the host guarantees units * grid < 2^31.
+DFL_DEV int unit_start(int c, int U, int G) { return c * U / G; }
 // CTA whose unit range [unit_start(c), unit_start(c+1)) contains unit u.
-DFL_DEV long long cta_of_unit(long long u, long long U, long long G) { return ((u + 1) * G + U - 1) / U - 1; }
+DFL_DEV int cta_of_unit(int u, int U, int G) { return ((u + 1) * G + U - 1) / U - 1; }
 
 // Timeline stamps (p.trace non-null): 0 entry, 1 set-up done, 2 first weight
 // stage landed, 3 last MMA issued, 4 epilogue done, 5 exit, 6 units, 7 SM id.
@@ -383,7 +384,7 @@ DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, con
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
           const int m = n0 + lane + 32 * jj - base;
-          const int kh = m / D, d = m % D;
+          const int kh = D == 128 ? m >> 7 : m >> 6, d = m & (D - 1);
           f16* blk = pool + (size_t)layer * p.kv.layer_stride + ((size_t)pg[q] * p.kv.hkv + kh) * (64 * D);
           blk[kind == 1 ? k_swz(row, d) : v_swz(d, row)] = to_f16(xv[jj], p.status);
         }
@@ -438,15 +439,15 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
   pdl_launch_dependents();
   if (threadIdx.x == 0) trace_at(p, 1, globaltimer());
 
-  const long long KB = p.kblocks;
-  const long long G = gridDim.x, c = blockIdx.x;
-  long long U, u0, u1;
+  const int KB = p.kblocks;
+  const int G = gridDim.x, c = blockIdx.x;
+  int U, u0, u1;
   if (p.allow_split) {
-    U = (long long)p.total_tiles * KB;
+    U = p.total_tiles * KB;
     u0 = unit_start(c, U, G);
     u1 = unit_start(c + 1, U, G);
   } else {
-    U = (long long)p.total_tiles * KB;
+    U = p.total_tiles * KB;
     u0 = unit_start(c, p.total_tiles, G) * KB;
     u1 = unit_start(c + 1, p.total_tiles, G) * KB;
   }
@@ -531,19 +532,19 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc = idesc_f16_f32(128, BN, p.ab_type);
-      long long it = 0;
+      int it = 0;
       int seg = 0;
       int s = 0;
       uint32_t phase = 0;
-      for (long long u = u0; u < u1 && !aborted; ++seg) {
-        const long long tile = u / KB;
-        const long long seg_end = (tile + 1) * KB < u1 ? (tile + 1) * KB : u1;
+      for (int u = u0; u < u1 && !aborted; ++seg) {
+        const int tile = u / KB;
+        const int seg_end = (tile + 1) * KB < u1 ? (tile + 1) * KB : u1;
         const int abuf = seg & 1;
         const uint32_t use = (uint32_t)(seg >> 1);
         if (!mbar_wait(tempty + abuf, (use & 1u) ^ 1u, p.status, &aborted)) break;
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(abuf * BN);
-        for (long long k = 0; u < seg_end; ++u, ++k, ++it) {
+        for (int k = 0; u < seg_end; ++u, ++k, ++it) {
           if (k > 0 || it > 0) {
             if (++s == stages) {
               s = 0;
@@ -594,9 +595,10 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
       use_pre = true;
     }
     int seg = 0;
-    for (long long u = u0; u < u1; ++seg) {
-      const long long tile = u / KB;
-      const long long seg_end = (tile + 1) * KB < u1 ? (tile + 1) * KB : u1;
+    const int first_tile = u0 / KB;  // this CTA's first segment's tile
+    for (int u = u0; u < u1; ++seg) {
+      const int tile = u / KB;
+      const int seg_end = (tile + 1) * KB < u1 ? (tile + 1) * KB : u1;
       u = seg_end;
       const int abuf = seg & 1;
       const uint32_t use = (uint32_t)(seg >> 1);
@@ -620,14 +622,14 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
       const int tt = (int)(tile % p.t_tiles);
       const int t_base = tt * BN;
       const int mt = (p.M - t_base) < BN ? (p.M - t_base) : BN;
-      long long c_first = c, c_last = c;
+      int c_first = c, c_last = c;
       if (p.allow_split) {
         c_first = cta_of_unit(tile * KB, U, G);
         c_last = cta_of_unit(tile * KB + KB - 1, U, G);
       }
       const bool split = c_first != c_last;
       if (split) {
-        const int my_slot = (tile == unit_start(c, U, G) / KB) ? 0 : 1;
+        const int my_slot = tile == first_tile ? 0 : 1;
         float* w = p.ws + (size_t)(c * 2 + my_slot) * (DFL_BN_MAX * 128);
         for (int col = 0; col < BN; col += 16) {
           float v[16];
@@ -652,7 +654,8 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
         if (!last) continue;
       }
       for (int tc0 = 0; tc0 < mt; tc0 += 32) {
-#pragma unroll
+        // one copy of the reduction code (run cold once per tile): not unrolled
+#pragma unroll 1
         for (int sub = 0; sub < 2; ++sub) {
           const int col = tc0 + 16 * sub;
           if (col < BN) {
@@ -660,13 +663,16 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
             if (split) {
 #pragma unroll
               for (int i = 0; i < 16; ++i) v[i] = 0.f;
-              // four contributors' loads in flight at once; summed in k order
-              for (long long cc0 = c_first; cc0 <= c_last; cc0 += 4) {
+              // four contributors' loads in flight at once; summed in k order.
+              // Every part after the first opens its CTA's range (slot 0);
+              // the first part is slot 1 unless the tile also opens c_first's.
+              const int sl_first = unit_start(c_first, U, G) == tile * KB ? 0 : 1;
+              for (int cc0 = c_first; cc0 <= c_last; cc0 += 4) {
                 float tv[4][16];
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
-                  const long long cc = cc0 + q4;
-                  const int sl = (cc <= c_last && tile == unit_start(cc, U, G) / KB) ? 0 : 1;
+                  const int cc = cc0 + q4;
+                  const int sl = cc == c_first ? sl_first : 0;
                   const float* w = p.ws + (size_t)(cc * 2 + sl) * (DFL_BN_MAX * 128);
 #pragma unroll
                   for (int i = 0; i < 16; ++i)
