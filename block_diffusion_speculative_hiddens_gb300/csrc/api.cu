@@ -118,6 +118,8 @@ struct dflash_handle {
   f16 *hg, *qbuf, *obuf, *act, *cg;
   float *ss_a, *ss_c;
   unsigned long long* keys;
+  int2* bctx;
+  float2* brope;
   unsigned* done_ctr;
   float* gemm_ws;
   unsigned* tile_ctr;
@@ -218,6 +220,8 @@ size_t carve(dflash_handle* h, const dflash_config& c, char* base, int num_sms) 
   o->obuf = w.take<f16>((size_t)M * hq * D);
   o->act = w.take<f16>((size_t)M * I);
   o->keys = w.take<unsigned long long>(M);
+  o->bctx = w.take<int2>(M);
+  o->brope = w.take<float2>((size_t)M * (D / 2));
   o->done_ctr = w.take<unsigned>(64);
   o->cg = w.take<f16>((size_t)R * H);
   o->ss_c = w.take<float>((size_t)(H / 128) * R);
@@ -390,8 +394,18 @@ int draft_impl(dflash_handle* h, const int32_t* slots, int32_t batch, const int3
   }
 
   h->launches++;
+  BlockCtx bcx;
+  bcx.ctx_len = h->ctx_len;
+  bcx.page_table = h->page_table;
+  bcx.max_pages_per_slot = c.max_pages_per_slot;
+  bcx.max_pages = c.max_pages;
+  bcx.rope = h->rope;
+  bcx.D = D;
+  bcx.max_pos = h->max_pos;
+  bcx.bctx = h->bctx;
+  bcx.brope = h->brope;
   rc = cuda_err(launch_embed(slots, batch, last_tok, c.mask_id, c.vocab, h->embed_pk, h->in_norm[0], H, h->h,
-                             h->hg, h->ss_a, h->keys, h->status, s));
+                             h->hg, h->ss_a, h->keys, bcx, h->status, s));
   if (rc) return rc;
 
   for (int l = 0; l < c.n_layers; ++l) {
@@ -406,6 +420,8 @@ int draft_impl(dflash_handle* h, const int32_t* slots, int32_t batch, const int3
       p.kv = kv;
       p.slots = slots;
       p.ctx_len = h->ctx_len;
+      p.bctx = h->bctx;
+      p.brope = h->brope;
       p.rows_per_req = DFL_BLOCK;
       p.N = (hq + 2 * hkv) * D;
       if (fold) {

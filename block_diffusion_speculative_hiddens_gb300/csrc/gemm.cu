@@ -43,6 +43,9 @@ namespace {
 
 constexpr int A_STAGE_BYTES = 128 * 128;  // 128 rows x 64 16-bit values
 constexpr int STG_BYTES = 32 * 128 * 4;   // epilogue staging: 32 tokens x 128 rows fp32
+constexpr int RED_PARTS = 4;               // split-K parts landed in shared memory at once
+constexpr int RED_CHUNK = 16 * 128;        // floats of one part's 16-column chunk (8 KB)
+constexpr int RED_BYTES = RED_PARTS * RED_CHUNK * 4;
 constexpr int EPI_THREADS = 128;
 
 // Unit arithmetic is 32-bit: the host guarantees units * grid < 2^31.
@@ -171,42 +174,77 @@ DFL_DEV void gather_ctx(const GemmParams& p, int t_first, int j0, int ntok, int 
       }
     }
 #pragma unroll
-    for (int q = 0; q < EPI_TOK; ++q) c.s[q] = rsqrtf(warp_sum(ssq[q]) / (float)p.H + p.eps);
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+      for (int q = 0; q < EPI_TOK; ++q) ssq[q] += __shfl_xor_sync(0xffffffffu, ssq[q], o);
+#pragma unroll
+    for (int q = 0; q < EPI_TOK; ++q) c.s[q] = rsqrtf(ssq[q] / (float)p.H + p.eps);
   }
   if (MODE == GM_QKV || MODE == GM_INJECT) {
     const int D = p.D;
-    int slot[EPI_TOK], ne[EPI_TOK], tl[EPI_TOK];
-#pragma unroll
-    for (int q = 0; q < EPI_TOK; ++q) {
-      tl[q] = (MODE == GM_QKV && c.inj[q]) ? tq[q] - p.inj_m0 : tq[q];
-      const int b = c.inj[q] ? tl[q] / p.rows_per_req : tl[q] / DFL_BLOCK;
-      slot[q] = p.slots[b];
-      ne[q] = c.inj[q] ? p.n_eff[b] : DFL_BLOCK;
-    }
-#pragma unroll
-    for (int q = 0; q < EPI_TOK; ++q) {
-      if (!c.inj[q]) {
-        c.live[q] = ok[q];
-        c.pos[q] = p.ctx_len[slot[q]] + (tl[q] % DFL_BLOCK);
-      } else {
-        const int i = tl[q] % p.rows_per_req;
-        c.live[q] = ok[q] && i < ne[q];
-        c.pos[q] = p.pos0[slot[q]] + i;
-      }
-      if (c.live[q] && c.pos[q] >= p.max_pos) {
-        dev_error(p.status, DFLASH_DEV_CAPACITY);
-        c.live[q] = false;
-      }
-    }
 #pragma unroll
     for (int q = 0; q < EPI_TOK; ++q) {
       c.c0[q] = c.c1[q] = make_float2(1.f, 0.f);
       c.pg[q] = -1;
-      if (c.live[q]) {
-        const float2* row = p.rope + (size_t)c.pos[q] * (D / 2);
-        c.c0[q] = row[lane];
-        if (D == 128) c.c1[q] = row[lane + 32];
-        c.pg[q] = page_of(p, slot[q], c.pos[q]);
+      c.pos[q] = 0;
+      c.live[q] = false;
+    }
+    // block rows of a QKV GEMM: position, page and RoPE row written once per
+    // round by the embedding kernel -- one load round trip
+    if (MODE == GM_QKV) {
+      int2 bc[EPI_TOK];
+      float2 r0[EPI_TOK], r1[EPI_TOK];
+#pragma unroll
+      for (int q = 0; q < EPI_TOK; ++q) {
+        const bool blk = ok[q] && !c.inj[q];
+        const float2* row = p.brope + (size_t)tq[q] * (D / 2);
+        bc[q] = blk ? p.bctx[tq[q]] : make_int2(0, -1);
+        r0[q] = blk ? row[lane] : make_float2(1.f, 0.f);
+        r1[q] = (blk && D == 128) ? row[lane + 32] : make_float2(1.f, 0.f);
+      }
+#pragma unroll
+      for (int q = 0; q < EPI_TOK; ++q) {
+        if (ok[q] && !c.inj[q]) {
+          c.pos[q] = bc[q].x;
+          c.pg[q] = bc[q].y;
+          c.live[q] = bc[q].x < p.max_pos;  // out-of-range positions were reported by the embedding
+          c.c0[q] = r0[q];
+          c.c1[q] = r1[q];
+        }
+      }
+    }
+    // fused-feature rows (INJECT, or folded into QKV): from the slot's tables
+    bool any_inj = false;
+#pragma unroll
+    for (int q = 0; q < EPI_TOK; ++q) any_inj |= ok[q] && c.inj[q];
+    if (any_inj) {
+      int slot[EPI_TOK], ne[EPI_TOK], ii[EPI_TOK];
+#pragma unroll
+      for (int q = 0; q < EPI_TOK; ++q) {
+        const int tl = MODE == GM_QKV ? tq[q] - p.inj_m0 : tq[q];
+        const int b = tl / p.rows_per_req;
+        ii[q] = tl % p.rows_per_req;
+        slot[q] = (ok[q] && c.inj[q]) ? p.slots[b] : 0;
+        ne[q] = (ok[q] && c.inj[q]) ? p.n_eff[b] : 0;
+      }
+#pragma unroll
+      for (int q = 0; q < EPI_TOK; ++q) {
+        if (!(ok[q] && c.inj[q])) continue;
+        c.live[q] = ii[q] < ne[q];
+        c.pos[q] = p.pos0[slot[q]] + ii[q];
+        if (c.live[q] && c.pos[q] >= p.max_pos) {
+          dev_error(p.status, DFLASH_DEV_CAPACITY);
+          c.live[q] = false;
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < EPI_TOK; ++q) {
+        if (ok[q] && c.inj[q] && c.live[q]) {
+          const float2* row = p.rope + (size_t)c.pos[q] * (D / 2);
+          c.c0[q] = row[lane];
+          if (D == 128) c.c1[q] = row[lane + 32];
+          c.pg[q] = page_of(p, slot[q], c.pos[q]);
+        }
       }
     }
   }
@@ -404,12 +442,14 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
   const int stages = p.stages;
   const int stage_bytes = A_STAGE_BYTES + BN * 128;
   float* stg = reinterpret_cast<float*>(sm + (size_t)stages * stage_bytes);
-  uint64_t* full = reinterpret_cast<uint64_t*>(sm + (size_t)stages * stage_bytes + STG_BYTES);
+  float* red_buf = reinterpret_cast<float*>(sm + (size_t)stages * stage_bytes + STG_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + (size_t)stages * stage_bytes + STG_BYTES + RED_BYTES);
   uint64_t* empty = full + stages;
   uint64_t* tfull = empty + stages;
   uint64_t* tempty = tfull + 2;
   uint64_t* mdone = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mdone + 1);
+  uint64_t* red = mdone + 1;  // split-K parts landed in red_buf
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red + 1);
   int* flag = reinterpret_cast<int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -426,6 +466,7 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
     mbar_init(tempty + 0, EPI_THREADS);
     mbar_init(tempty + 1, EPI_THREADS);
     mbar_init(mdone, 1);
+    mbar_init(red, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -596,6 +637,7 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
     }
     int seg = 0;
     const int first_tile = u0 / KB;  // this CTA's first segment's tile
+    uint32_t red_phase = 0;
     for (int u = u0; u < u1; ++seg) {
       const int tile = u / KB;
       const int seg_end = (tile + 1) * KB < u1 ? (tile + 1) * KB : u1;
@@ -663,25 +705,33 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
             if (split) {
 #pragma unroll
               for (int i = 0; i < 16; ++i) v[i] = 0.f;
-              // four contributors' loads in flight at once; summed in k order.
+              // Up to RED_PARTS parts' 16-column chunks land in shared memory
+              // by bulk copies (one issuing thread, one barrier: one round
+              // trip), then are added in k order by a compact loop -- this
+              // code runs cold once per tile, so it stays short.
               // Every part after the first opens its CTA's range (slot 0);
               // the first part is slot 1 unless the tile also opens c_first's.
               const int sl_first = unit_start(c_first, U, G) == tile * KB ? 0 : 1;
-              for (int cc0 = c_first; cc0 <= c_last; cc0 += 4) {
-                float tv[4][16];
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                  const int cc = cc0 + q4;
-                  const int sl = cc == c_first ? sl_first : 0;
-                  const float* w = p.ws + (size_t)(cc * 2 + sl) * (DFL_BN_MAX * 128);
-#pragma unroll
-                  for (int i = 0; i < 16; ++i)
-                    tv[q4][i] = (cc <= c_last && col + i < mt) ? __ldcg(w + (size_t)(col + i) * 128 + r) : 0.f;
+              for (int cc0 = c_first; cc0 <= c_last && !aborted; cc0 += RED_PARTS) {
+                const int nk = (c_last - cc0 + 1) < RED_PARTS ? (c_last - cc0 + 1) : RED_PARTS;
+                if (et == 0) {
+                  fence_proxy_async_global();  // parts acquired through the tile counter
+                  mbar_arrive_expect_tx(red, (uint32_t)(nk * RED_CHUNK * 4));
+#pragma unroll 1
+                  for (int k = 0; k < nk; ++k) {
+                    const int cc = cc0 + k;
+                    const int sl = cc == c_first ? sl_first : 0;
+                    bulk_load(red_buf + k * RED_CHUNK, p.ws + (size_t)(cc * 2 + sl) * (DFL_BN_MAX * 128) + col * 128,
+                              RED_CHUNK * 4, red);
+                  }
                 }
+                if (!mbar_wait(red, red_phase, p.status, &aborted)) break;
+                red_phase ^= 1u;
+#pragma unroll 1
+                for (int k = 0; k < nk; ++k)
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4)
-#pragma unroll
-                  for (int i = 0; i < 16; ++i) v[i] += tv[q4][i];
+                  for (int i = 0; i < 16; ++i) v[i] += red_buf[k * RED_CHUNK + i * 128 + r];
+                named_bar_sync(1, EPI_THREADS);  // red_buf free for the next parts
               }
             } else {
               tmem_ld16(taddr + (uint32_t)col, v);
@@ -742,7 +792,8 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
 }  // namespace
 
 size_t gemm_smem_bytes(int BN, int stages) {
-  return 1024 + (size_t)stages * (A_STAGE_BYTES + BN * 128) + STG_BYTES + (size_t)(2 * stages + 5) * 8 + 16;
+  return 1024 + (size_t)stages * (A_STAGE_BYTES + BN * 128) + STG_BYTES + RED_BYTES + (size_t)(2 * stages + 6) * 8 +
+         16;
 }
 
 // Weight-ring depth.  Six 16 KB stages per SM already keep HBM streaming at
@@ -751,7 +802,7 @@ size_t gemm_smem_bytes(int BN, int stages) {
 // is fastest at 6-7 stages, 2.5% slower at 12).  The lm_head, one long
 // stream with short tails, runs best at 8.
 int gemm_pick_stages(int BN, int mode) {
-  const size_t budget = 232448 - 1024 - STG_BYTES - 512;
+  const size_t budget = 232448 - 1024 - STG_BYTES - RED_BYTES - 512;
   int st = (int)(budget / (size_t)(A_STAGE_BYTES + BN * 128));
   const int cap = mode == GM_ARGMAX ? 8 : 6;
   st = st > cap ? cap : st;

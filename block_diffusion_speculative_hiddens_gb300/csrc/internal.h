@@ -86,6 +86,8 @@ struct GemmParams {
   const int* n_eff;     // [batch] (inject: rows appended)
   const float2* rope;   // [max_pos][D/2] (cos, sin)
   int max_pos;
+  const int2* bctx;     // QKV: block tokens' {position, page} (BlockCtx)
+  const float2* brope;  // QKV: block tokens' RoPE rows [M][D/2]
   // argmax
   unsigned long long* keys;  // [M]
   float* logits;             // optional [M][N] (N = vocab)
@@ -128,9 +130,21 @@ cudaError_t launch_pack_weight(const bf16* src, void* dst, int N, int K, int n_t
                                cudaStream_t s);
 cudaError_t launch_gain_f32(const bf16* src, float* dst, int n, cudaStream_t s);
 
+// Positions, pages and RoPE rows of a round's block tokens: the same for
+// every layer, so the embedding kernel writes them once for the layers' QKV
+// epilogues (bctx[t] = {position, page or -1}, brope[t][D/2] = (cos, sin)).
+struct BlockCtx {
+  const int* ctx_len;
+  const int* page_table;
+  int max_pages_per_slot, max_pages;
+  const float2* rope;
+  int D, max_pos;
+  int2* bctx;
+  float2* brope;
+};
 cudaError_t launch_embed(const int* slots, int batch, const int* last_tok, int mask_id, int vocab,
                          const f16* embed_pk, const float* gain, int H, float* h, f16* hg, float* ss,
-                         unsigned long long* keys, uint32_t* status, cudaStream_t s);
+                         unsigned long long* keys, const BlockCtx& bc, uint32_t* status, cudaStream_t s);
 cudaError_t launch_page_alloc(const int* slots, int batch, const int* n_new, int rows_per_req, int* ctx_len,
                               int* pos0, int* n_pages, int* page_table, int max_pages_per_slot,
                               int* free_stack, int* free_top, int* n_eff, int max_slots, uint32_t* status,

@@ -60,7 +60,7 @@ __global__ void k_gain_f32(const bf16* __restrict__ src, float* __restrict__ dst
 // the argmax keys.
 __global__ void k_embed(const int* __restrict__ slots, const int* __restrict__ last_tok, int mask_id, int vocab,
                         const f16* __restrict__ E, const float* __restrict__ gain, int H, int M, float* h, f16* hg,
-                        float* ss, unsigned long long* keys, uint32_t* status) {
+                        float* ss, unsigned long long* keys, const BlockCtx bc, uint32_t* status) {
   pdl_launch_dependents();
   pdl_wait();
   const int t = blockIdx.x;
@@ -88,6 +88,23 @@ __global__ void k_embed(const int* __restrict__ slots, const int* __restrict__ l
     if (lane == 0) ss[(size_t)part * M + t] = sq;
   }
   if (threadIdx.x == 0) keys[t] = 0ull;
+  // this token's position (block rows follow the slot's context), page and
+  // RoPE row, for every layer's QKV epilogue
+  const int slot = slots[b];
+  const int pos = bc.ctx_len[slot] + i;
+  const bool in_range = pos < bc.max_pos;
+  if (threadIdx.x == 0) {
+    int pg = -1;
+    if (!in_range) {
+      dev_error(status, DFLASH_DEV_CAPACITY);
+    } else if ((pos >> 6) < bc.max_pages_per_slot) {
+      pg = bc.page_table[(size_t)slot * bc.max_pages_per_slot + (pos >> 6)];
+      if (pg < 0 || pg >= bc.max_pages) pg = -1;
+    }
+    bc.bctx[t] = make_int2(pos, pg);
+  }
+  for (int k = threadIdx.x; k < bc.D / 2; k += blockDim.x)
+    bc.brope[(size_t)t * (bc.D / 2) + k] = in_range ? bc.rope[(size_t)pos * (bc.D / 2) + k] : make_float2(1.f, 0.f);
 }
 
 // Page allocation for dflash_fuse_inject (one thread, requests in order, so
@@ -286,13 +303,13 @@ cudaError_t launch_gain_f32(const bf16* src, float* dst, int n, cudaStream_t s) 
 
 cudaError_t launch_embed(const int* slots, int batch, const int* last_tok, int mask_id, int vocab,
                          const f16* embed_pk, const float* gain, int H, float* h, f16* hg, float* ss,
-                         unsigned long long* keys, uint32_t* status, cudaStream_t s) {
+                         unsigned long long* keys, const BlockCtx& bc, uint32_t* status, cudaStream_t s) {
   cudaLaunchAttribute a[1];
   const int M = batch * DFL_BLOCK;
   int threads = (H / 128) * 32;
   if (threads > 1024) threads = 1024;
   cudaLaunchConfig_t c = cfg_of(dim3(M), dim3(threads), s, a);
-  return cudaLaunchKernelEx(&c, k_embed, slots, last_tok, mask_id, vocab, embed_pk, gain, H, M, h, hg, ss, keys,
+  return cudaLaunchKernelEx(&c, k_embed, slots, last_tok, mask_id, vocab, embed_pk, gain, H, M, h, hg, ss, keys, bc,
                             status);
 }
 
