@@ -19,6 +19,7 @@ oracle on the host cores instead.
 from __future__ import annotations
 
 import argparse
+import re
 import json
 import math
 import os
@@ -58,6 +59,28 @@ def peaks():
         return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
     except Exception:
         return 6800.0, 1900.0, "fallback"
+
+
+def lm_head_traffic(cfg):
+    """DRAM bytes per lm_head launch from the committed ncu summary, or None
+    when the GEMM sources changed since the counters were taken (or for a
+    workload the summary does not cover)."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "lm_head_traffic_mid.md")) as f:
+            text = f.read()
+        want = re.search(r"^source_sha256: ([0-9a-f]{64})$", text, re.M).group(1)
+        traffic = int(re.search(r"^traffic_bytes_per_launch: (\d+)$", text, re.M).group(1))
+    except Exception:
+        return None
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "block_diffusion_speculative_hiddens_gb300", "csrc")
+    for name in ("gemm.cu", "common.cuh", "internal.h"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    if h.hexdigest() != want or cfg.name != "qwen3-8b":
+        return None
+    return traffic
 
 
 # ------------------------------------------------------------------ clocks
@@ -333,7 +356,7 @@ def run_gpu(args, rank, world, local_rank):
         "graph_kernel_nodes": n_kernels,
         "roofline": {"bound": "hbm", "kernel": "lm_head+argmax (tcgen05 GEMM)",
                      "achieved": round(lm_gbs, 1), "peak": hbm, "unit": "GB/s",
-                     "frac": round(lm_gbs / hbm, 4), "traffic": None, "peak_source": peak_src,
+                     "frac": round(lm_gbs / hbm, 4), "traffic": lm_head_traffic(cfg), "peak_source": peak_src,
                      "bytes_per_launch": lm_bytes, "avg_launch_us": round(lm_avg_ms * 1e3, 2)},
         "round_roofline": {"bytes_per_round": int(round_bytes), "achieved_gbs": round(
             round_bytes / (round_ms * 1e-3) / 1e9, 1), "frac": round(round_bytes / (round_ms * 1e-3) / 1e9 / hbm, 4)},
