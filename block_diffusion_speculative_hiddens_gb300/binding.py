@@ -69,6 +69,9 @@ _SIGS = {
     "dflash_slot_lengths": (ctypes.c_int, [_vp, _vp, ctypes.c_int32, _vp, _vp]),
     "dflash_probe_arm": (ctypes.c_int, [_vp, ctypes.c_int32, ctypes.c_int32]),
     "dflash_probe_read": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_float), ctypes.c_int32, _c_int_p]),
+    "dflash_marks_arm": (ctypes.c_int, [_vp, ctypes.c_int32]),
+    "dflash_mark": (ctypes.c_int, [_vp, _vp]),
+    "dflash_marks_read": (ctypes.c_int, [_vp, _vp, ctypes.c_int32, _vp]),
     "dflash_launch_count": (ctypes.c_uint64, [_vp]),
     "dflash_trace_arm": (ctypes.c_int, [_vp, ctypes.c_int32, _vp, ctypes.c_int32]),
     "dflash_harness_verify": (ctypes.c_int, [_vp, _vp, ctypes.c_int32, _vp, _vp, _vp, ctypes.c_int32, _vp,
@@ -247,6 +250,20 @@ class Drafter:
         buf = (ctypes.c_float * max(cap, 1))()
         n = ctypes.c_int32(0)
         _check("dflash_probe_read", self.lib.dflash_probe_read(self.h, buf, cap, ctypes.byref(n)))
+        return list(buf[:n.value])
+
+    def marks_arm(self, n: int):
+        _check("dflash_marks_arm", self.lib.dflash_marks_arm(self.h, n))
+
+    def mark(self, stream=None):
+        """Record the next timeline mark on the stream (a graph node when capturing)."""
+        _check("dflash_mark", self.lib.dflash_mark(self.h, _stream(stream)))
+
+    def marks_read(self, cap: int):
+        """Intervals in ms between consecutive recorded marks (synchronises)."""
+        buf = (ctypes.c_float * max(cap, 1))()
+        n = ctypes.c_int32(0)
+        _check("dflash_marks_read", self.lib.dflash_marks_read(self.h, buf, cap, ctypes.byref(n)))
         return list(buf[:n.value])
 
     def trace_arm(self, kernel_id: int, buf=None, cap_ctas: int = 0):

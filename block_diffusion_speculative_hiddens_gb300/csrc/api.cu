@@ -127,6 +127,7 @@ struct dflash_handle {
   bool pdl = true;
   uint64_t launches = 0;
   Probe probe;
+  Probe marks;  // timeline marks: ev[i] = mark i, n = capacity, next = recorded
   Trace trace;
   cudaGraph_t graph = nullptr;
   cudaGraphExec_t exec = nullptr;
@@ -156,13 +157,19 @@ bool cfg_valid(const dflash_config* c) {
   return true;
 }
 
+#ifndef DFL_ATTN_MAX_SPLITS
+#define DFL_ATTN_MAX_SPLITS 16
+#endif
+
 // Split-KV count: about one wave of CTAs, at least 4 pages per split at full
-// slot capacity, and at most 8 splits so the last CTA's merge stays short.
+// slot capacity, at most 16 (one thread-block cluster).  Above 8 (the
+// portable cluster size) dflash_create keeps it only if the GPU can hold a
+// cluster for every (request, KV head) at once.
 int pick_attn_splits(const dflash_config& c, int num_sms) {
   const int pairs = c.max_batch * c.n_kv_heads;
   int want = ceil_div(num_sms, pairs);
   want = std::min(want, std::max(1, c.max_pages_per_slot / 4));
-  want = std::min(want, 8);
+  want = std::min(want, DFL_ATTN_MAX_SPLITS);
   return std::max(1, want);
 }
 
@@ -590,6 +597,9 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
   int rc = ok ? DFLASH_OK : DFLASH_ERR_CUDA;
   if (!rc) rc = cuda_err(gemm_init_attributes());
   if (!rc) rc = cuda_err(attn_init_attributes());
+  if (!rc && h->attn_splits > 8 &&
+      attn_max_active_clusters(c.head_dim, c.n_q_heads, c.n_kv_heads, h->attn_splits) < c.max_batch * c.n_kv_heads)
+    h->attn_splits = 8;
   if (!rc)
     rc = cuda_err(cudaMemset(h->page_table, 0xFF, (size_t)c.max_slots * c.max_pages_per_slot * sizeof(int)));
   if (!rc) rc = cuda_err(launch_pool_init(h->free_stack, h->free_top, c.max_pages, 0));
@@ -608,6 +618,7 @@ int dflash_destroy(dflash_handle* h) {
   if (h->exec) cudaGraphExecDestroy(h->exec);
   if (h->graph) cudaGraphDestroy(h->graph);
   for (cudaEvent_t e : h->probe.ev) cudaEventDestroy(e);
+  for (cudaEvent_t e : h->marks.ev) cudaEventDestroy(e);
   delete h;
   return DFLASH_OK;
 }
@@ -806,6 +817,44 @@ int dflash_probe_read(dflash_handle* h, float* ms_out, int32_t cap, int32_t* n_o
     if (rc) return rc;
   }
   if (n_out) *n_out = n;
+  return DFLASH_OK;
+}
+
+int dflash_marks_arm(dflash_handle* h, int32_t n) {
+  if (!h || n < 0) return DFLASH_ERR_INVALID_ARG;
+  if (cudaSetDevice(h->cfg.device) != cudaSuccess) return DFLASH_ERR_CUDA;
+  while ((int)h->marks.ev.size() < n) {
+    cudaEvent_t e;
+    int rc = cuda_err(cudaEventCreate(&e));
+    if (rc) return rc;
+    h->marks.ev.push_back(e);
+  }
+  h->marks.n = n;
+  h->marks.next = 0;
+  return DFLASH_OK;
+}
+
+int dflash_mark(dflash_handle* h, void* stream) {
+  if (!h) return DFLASH_ERR_INVALID_ARG;
+  if (h->marks.next >= h->marks.n) return DFLASH_OK;
+  if (cudaSetDevice(h->cfg.device) != cudaSuccess) return DFLASH_ERR_CUDA;
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+  const bool capturing = cudaStreamIsCapturing(s, &st) == cudaSuccess && st == cudaStreamCaptureStatusActive;
+  cudaEvent_t e = h->marks.ev[h->marks.next++];
+  return cuda_err(capturing ? cudaEventRecordWithFlags(e, s, cudaEventRecordExternal) : cudaEventRecord(e, s));
+}
+
+int dflash_marks_read(dflash_handle* h, float* ms_out, int32_t cap, int32_t* n_out) {
+  if (!h || (!ms_out && cap > 0)) return DFLASH_ERR_INVALID_ARG;
+  const int n = std::min(h->marks.next - 1, (int)cap);
+  for (int i = 0; i < n; ++i) {
+    int rc = cuda_err(cudaEventSynchronize(h->marks.ev[i + 1]));
+    if (rc) return rc;
+    rc = cuda_err(cudaEventElapsedTime(ms_out + i, h->marks.ev[i], h->marks.ev[i + 1]));
+    if (rc) return rc;
+  }
+  if (n_out) *n_out = n < 0 ? 0 : n;
   return DFLASH_OK;
 }
 

@@ -17,6 +17,11 @@
 
 namespace {
 
+// Splits of one (request, KV head) are one thread-block cluster: up to 16
+// CTAs (a non-portable cluster size, used only where the GPU can hold the
+// clusters at once; see attn_max_active_clusters).
+constexpr int ATTN_MAX_SPLITS = 16;
+
 template <int D>
 struct AttnCfg {
 #ifndef DFL_ATTN_STAGES
@@ -326,10 +331,10 @@ __global__ void __launch_bounds__(G * KS * 32) k_attn(const AttnParams p) {
   const uint32_t part_local = smem_u32(part);
   for (int e = threadIdx.x; e < (re - rb) * (D / 4); e += blockDim.x) {
     const int r = rb + e / (D / 4), d = (e % (D / 4)) * 4;
-    float mv[8], lv[8];
-    float4 v[8];
+    float mv[ATTN_MAX_SPLITS], lv[ATTN_MAX_SPLITS];
+    float4 v[ATTN_MAX_SPLITS];
 #pragma unroll
-    for (int sp = 0; sp < 8; ++sp) {
+    for (int sp = 0; sp < ATTN_MAX_SPLITS; ++sp) {
       mv[sp] = -INFINITY;
       lv[sp] = 0.f;
       v[sp] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -342,11 +347,11 @@ __global__ void __launch_bounds__(G * KS * 32) k_attn(const AttnParams p) {
     }
     float M = -INFINITY;
 #pragma unroll
-    for (int sp = 0; sp < 8; ++sp)
+    for (int sp = 0; sp < ATTN_MAX_SPLITS; ++sp)
       if (lv[sp] > 0.f) M = fmaxf(M, mv[sp]);
     float L = 0.f;
 #pragma unroll
-    for (int sp = 0; sp < 8; ++sp) {
+    for (int sp = 0; sp < ATTN_MAX_SPLITS; ++sp) {
       const float w = lv[sp] > 0.f ? exp2f(mv[sp] - M) : 0.f;
       mv[sp] = w;
       L += w * lv[sp];
@@ -354,7 +359,7 @@ __global__ void __launch_bounds__(G * KS * 32) k_attn(const AttnParams p) {
     const float inv = L > 0.f ? 1.f / L : 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int sp = 0; sp < 8; ++sp) {
+    for (int sp = 0; sp < ATTN_MAX_SPLITS; ++sp) {
       if (sp < n) {
         const float w = mv[sp] * inv;
         acc.x += w * v[sp].x;
@@ -409,21 +414,65 @@ cudaError_t launch_d(const AttnParams& p, int batch, cudaStream_t s, bool pdl) {
   return cudaErrorInvalidValue;
 }
 
+template <int D, int G>
+cudaError_t attr_t() {
+  auto k = k_attn<D, G, attn_ks<G>()>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnCfg<D>::SMEM);
+  if (e) return e;
+  return cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+}
+
 template <int D>
 cudaError_t attr_d() {
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(k_attn<D, 1, attn_ks<1>()>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnCfg<D>::SMEM)))
-    return e;
-  if ((e = cudaFuncSetAttribute(k_attn<D, 2, attn_ks<2>()>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnCfg<D>::SMEM)))
-    return e;
-  if ((e = cudaFuncSetAttribute(k_attn<D, 4, attn_ks<4>()>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnCfg<D>::SMEM)))
-    return e;
-  return cudaFuncSetAttribute(k_attn<D, 8, attn_ks<8>()>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnCfg<D>::SMEM);
+  if ((e = attr_t<D, 1>())) return e;
+  if ((e = attr_t<D, 2>())) return e;
+  if ((e = attr_t<D, 4>())) return e;
+  return attr_t<D, 8>();
+}
+
+// Clusters of `splits` CTAs of the attention kernel for this shape that the
+// GPU can hold at once (0 when it cannot launch them at all).
+template <int D, int G>
+int max_clusters_t(int splits, int hkv) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)splits, (unsigned)hkv, 1);
+  cfg.blockDim = dim3(G * attn_ks<G>() * 32);
+  cfg.dynamicSmemBytes = AttnCfg<D>::SMEM;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)splits;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, k_attn<D, G, attn_ks<G>()>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+template <int D>
+int max_clusters_d(int splits, int G, int hkv) {
+  switch (G) {
+    case 1: return max_clusters_t<D, 1>(splits, hkv);
+    case 2: return max_clusters_t<D, 2>(splits, hkv);
+    case 4: return max_clusters_t<D, 4>(splits, hkv);
+    case 8: return max_clusters_t<D, 8>(splits, hkv);
+  }
+  return 0;
 }
 
 }  // namespace
 
 size_t attn_smem_bytes(int D) { return D == 64 ? AttnCfg<64>::SMEM : AttnCfg<128>::SMEM; }
+
+int attn_max_active_clusters(int D, int hq, int hkv, int splits) {
+  if (splits < 1 || splits > ATTN_MAX_SPLITS) return 0;
+  return D == 64 ? max_clusters_d<64>(splits, hq / hkv, hkv) : max_clusters_d<128>(splits, hq / hkv, hkv);
+}
 
 cudaError_t attn_init_attributes() {
   cudaError_t e = attr_d<64>();

@@ -109,7 +109,7 @@ struct AttnParams {
   const int* slots;
   const int* ctx_len;  // keys = ctx_len + 16 (block K/V already in the cache)
   int hq, hkv, D;
-  int n_splits;        // CTAs per (request, KV head): one cluster, <= 8
+  int n_splits;        // CTAs per (request, KV head): one cluster, <= 16
   float scale_log2;    // log2(e) / sqrt(D)
   uint32_t* status;
   unsigned long long* trace;  // optional [grid][8] timeline (null: off)
@@ -122,6 +122,8 @@ cudaError_t gemm_launch(const CUtensorMap& B, const GemmParams& p, int grid, cud
 cudaError_t gemm_init_attributes();
 
 size_t attn_smem_bytes(int D);
+// Attention clusters of `splits` CTAs the GPU can hold at once (0: cannot launch).
+int attn_max_active_clusters(int D, int hq, int hkv, int splits);
 cudaError_t attn_launch(const AttnParams& p, int batch, cudaStream_t s, bool pdl);
 cudaError_t attn_init_attributes();
 

@@ -255,6 +255,18 @@ DFLASH_API int dflash_draft_block_debug(dflash_handle* h, const int32_t* slots, 
 DFLASH_API int dflash_probe_arm(dflash_handle* h, int32_t kernel_id, int32_t n);
 DFLASH_API int dflash_probe_read(dflash_handle* h, float* ms_out, int32_t cap, int32_t* n_out);
 
+/* Timeline marks (no counterpart on the pages; measurement only).
+ * dflash_marks_arm(h, n) resets the mark list and makes room for n marks;
+ * each dflash_mark(h, stream) records the next mark event on `stream` (an
+ * external event-record node when the stream is being captured, so a graph
+ * replay records it again); marks beyond n are ignored.
+ * dflash_marks_read synchronises on the recorded marks and writes up to
+ * `cap` intervals in ms between consecutive marks (ms_out[i] = mark i ->
+ * mark i+1); *n_out = number of intervals written. */
+DFLASH_API int dflash_marks_arm(dflash_handle* h, int32_t n);
+DFLASH_API int dflash_mark(dflash_handle* h, void* stream);
+DFLASH_API int dflash_marks_read(dflash_handle* h, float* ms_out, int32_t cap, int32_t* n_out);
+
 /* Device timeline of one launch: the next launch of kernel `kernel_id`
  * (DFLASH_KID_*) writes, per CTA, 8 uint64 values into the DEVICE buffer
  * buf[cap_ctas][8].  GEMMs: %globaltimer (ns) at entry, end of set-up, first
