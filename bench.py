@@ -9,9 +9,11 @@ previous round's accepted features, draft one block, stand-in verify,
 accept/trim, all captured in one CUDA graph.  Synthetic seeded data and
 random-init weights of that architecture.
 
-Every scenario pass is 64 rounds from the 2048-token prompt; timed steps
-cycle through identically prefilled request slots, 64 rounds per slot, so K
-steps always run rounds of the stated scenario.
+Every scenario pass is the workload's round count from its prompts; timed
+steps cycle through identically prefilled groups of request slots, one pass
+per group, so K steps always run rounds of the stated scenario.  Other
+workloads (`--config llama3.1-8b | batched-qwen3-8b | long-8layer`) run the
+same way at their own batch; large feature streams are drawn on the GPU.
 
 Prints one JSON line (rank 0).  `--impl reference` times the float64 CPU
 oracle on the host cores instead.
@@ -39,7 +41,8 @@ METRIC = "drafted tok/s & draft-round latency (µs), Qwen3-8B-shape b16; % HBM r
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=512)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed rounds (default 512 at batch 1, one scenario pass of the workload otherwise)")
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="qwen3-8b")
@@ -59,6 +62,16 @@ def peaks():
         return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
     except Exception:
         return 6800.0, 1900.0, "fallback"
+
+
+def tensor_peaks():
+    """Dense bf16 tensor peaks (TFLOP/s): burst and sustained, measured else fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", p["bf16_tflops"]))
+    except Exception:
+        return 1900.0, 1700.0
 
 
 def gemm_source_hash():
@@ -186,47 +199,67 @@ def run_gpu(args, rank, world, local_rank):
     import torch
     from block_diffusion_speculative_hiddens_gb300 import Drafter, binding, weights_to_device
     from block_diffusion_speculative_hiddens_gb300.session import RoundState, SyntheticVerify, run_round
-    from workload import feature_rows, get_config, make_weights, match_stream
+    from workload import context_lengths, feature_rows, get_config, make_weights, match_stream
 
     torch.cuda.set_device(local_rank)
     dev = torch.device(f"cuda:{local_rank}")
     cfg = get_config(args.config)
-    assert cfg.batch == 1 and cfg.ctx0, "bench workload is a batch-1 scenario"
-    B = 1
+    B = cfg.batch
+    ctx = context_lengths(cfg).astype(int)               # prompt length per request
     R = args.rounds_per_slot or cfg.rounds
-    K, W = args.steps, args.warmup
-    n_slots = math.ceil(K / R) + 1                       # + one slot for warm-up
-    L0 = cfg.ctx0
-    cap = L0 + cfg.block * (max(R, W) + 2) + 64
+    K = args.steps if args.steps is not None else (512 if B == 1 else R)
+    W = args.warmup
+    n_groups = math.ceil(K / R) + 1                      # + one group of B slots for warm-up
+    n_slots = n_groups * B
+    cap = int(ctx.max()) + cfg.block * (max(R, W) + 2) + 64
     mpps = math.ceil(cap / 64) + 1
+    F = cfg.fused_dim
 
     w_dev = weights_to_device(make_weights(cfg), local_rank)
-    F = cfg.fused_dim
-    fs = feature_rows(cfg, 0, 0, cap).reshape(1, cap, F)
-    feat_stream = binding.bf16_host(fs).to(dev)
-    m = np.empty((max(R, W), 1, 16), dtype=np.int32)
+    # target features of every position a request reaches: the workload's
+    # position-keyed stream when it is small, else N(0,1) drawn on the device
+    # from a per-request seeded generator (same distribution, same shapes)
+    if B * cap * F <= 4e8:
+        fs = np.stack([feature_rows(cfg, b, 0, cap).reshape(cap, F) for b in range(B)])
+        feat_stream = binding.bf16_host(fs).to(dev)
+        feat_src = "workload generator"
+    else:
+        fs = None
+        feat_stream = torch.empty(B, cap, F, dtype=torch.bfloat16, device=dev)
+        for b in range(B):
+            g = torch.Generator(device=dev)
+            g.manual_seed(1_000_003 * (cfg.seed + 1) + b)
+            feat_stream[b].normal_(generator=g)
+        feat_src = "device generator (torch.normal_, seeded per request)"
+    m = np.empty((max(R, W), B, 16), dtype=np.int32)
     u = np.empty_like(m)
     for r in range(max(R, W)):
-        m[r], u[r] = match_stream(cfg, r, [0])
+        m[r], u[r] = match_stream(cfg, r, list(range(B)))
     match, offs = torch.from_numpy(m).to(dev), torch.from_numpy(u).to(dev)
 
     chunk = 2048
     d = Drafter(cfg, w_dev, max_batch=B, max_slots=n_slots, max_pages=mpps * n_slots,
                 max_pages_per_slot=mpps, max_rows=max(chunk, 16 * B), device=local_rank)
     stream = torch.cuda.Stream(device=dev)
+
+    def prefill(g):
+        with torch.cuda.stream(stream):
+            for b in range(B):
+                slot = torch.tensor([g * B + b], dtype=torch.int32, device=dev)
+                for p0 in range(0, int(ctx[b]), chunk):
+                    n = min(chunk, int(ctx[b]) - p0)
+                    d.fuse_inject(slot, feat_stream[b:b + 1, p0:p0 + n], n,
+                                  torch.tensor([n], dtype=torch.int32, device=dev), stream)
+
     states, verifies = [], []
-    with torch.cuda.stream(stream):
-        for j in range(n_slots):
-            st = RoundState(d, B, slots=[j], first_token=cfg.first_token)
-            for p0 in range(0, L0, chunk):
-                n = min(chunk, L0 - p0)
-                d.fuse_inject(st.slots, feat_stream[:, p0:p0 + n], n,
-                              torch.tensor([n], dtype=torch.int32, device=dev), stream)
-            states.append(st)
-            verifies.append(SyntheticVerify(st, match, offs, feat_stream))
+    for g in range(n_groups):
+        prefill(g)
+        st = RoundState(d, B, slots=[g * B + b for b in range(B)], first_token=cfg.first_token)
+        states.append(st)
+        verifies.append(SyntheticVerify(st, match, offs, feat_stream))
     stream.synchronize()
 
-    # warm-up: W rounds on the spare slot, as one graph
+    # warm-up: W rounds on the spare group, as one graph
     wst, wv = states[-1], verifies[-1]
     d.graph_begin(stream)
     for _ in range(W):
@@ -235,7 +268,7 @@ def run_gpu(args, rank, world, local_rank):
     d.graph_launch(stream)
     stream.synchronize()
 
-    # timed: K rounds, R per slot, one graph; lm_head bracketed by event probes
+    # timed: K rounds, R per group, one graph; lm_head bracketed by event probes
     d.probe_arm(binding.KID_LM_HEAD, K)
     n0 = d.launch_count()
     d.graph_begin(stream)
@@ -265,28 +298,25 @@ def run_gpu(args, rank, world, local_rank):
     lm_ms = d.probe_read(K)
     status = d.read_status()
     accepted = 0
-    for j in range(n_slots - 1):
-        rounds_j = min(R, K - j * R)
-        if rounds_j > 0:
-            accepted += int(states[j].ctx_len.item()) - L0
+    for g in range(n_groups - 1):
+        if min(R, K - g * R) > 0:
+            accepted += int((states[g].ctx_len.cpu().numpy() - ctx).sum())
     if world > 1:
         t = torch.tensor([ms], dtype=torch.float64, device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms = float(t.item())
 
     # ---- the stand-in verify on its own, and the per-round distribution: one
-    # more graph of up to R rounds on a fresh copy of the prompt, with
+    # more graph of up to R rounds on a fresh copy of the prompts, with
     # timeline marks at every round start and around the verify (the marks'
     # event nodes cost a little overlap, so the headline mean stays the
     # unmarked graph's, minus the verify's mean)
     Ki = min(R, K)
-    st_i = RoundState(d, B, slots=[n_slots - 1], first_token=cfg.first_token)
-    d.reset_slot(n_slots - 1, stream)
-    with torch.cuda.stream(stream):
-        for p0 in range(0, L0, chunk):
-            n = min(chunk, L0 - p0)
-            d.fuse_inject(st_i.slots, feat_stream[:, p0:p0 + n], n,
-                          torch.tensor([n], dtype=torch.int32, device=dev), stream)
+    gi = n_groups - 1
+    for b in range(B):
+        d.reset_slot(gi * B + b, stream)
+    prefill(gi)
+    st_i = RoundState(d, B, slots=[gi * B + b for b in range(B)], first_token=cfg.first_token)
     ver_i = SyntheticVerify(st_i, match, offs, feat_stream)
 
     def marked_verify(s_=None):
@@ -313,45 +343,50 @@ def run_gpu(args, rank, world, local_rank):
     e2e = None
     E = min(args.e2e_steps, R)
     if E > 0:
-        st = RoundState(d, B, slots=[n_slots - 1], first_token=cfg.first_token)
-        d.reset_slot(n_slots - 1, stream)
-        for p0 in range(0, L0, chunk):
-            n = min(chunk, L0 - p0)
-            d.fuse_inject(st.slots, feat_stream[:, p0:p0 + n], n,
-                          torch.tensor([n], dtype=torch.int32, device=dev), stream)
-        m_dev = torch.zeros(1, 1, 16, dtype=torch.int32, device=dev)
+        for b in range(B):
+            d.reset_slot(gi * B + b, stream)
+        prefill(gi)
+        st = RoundState(d, B, slots=[gi * B + b for b in range(B)], first_token=cfg.first_token)
+        m_dev = torch.zeros(1, B, 16, dtype=torch.int32, device=dev)
         u_dev = torch.zeros_like(m_dev)
         ver = SyntheticVerify(st, m_dev, u_dev, None)
         d.graph_begin(stream)
         run_round(st, ver, stream, folded=args.fold_inject)
         d.graph_end(stream)
-        feats_h = torch.empty(1, 16, F, dtype=torch.bfloat16).pin_memory()
-        mu_h = torch.empty(2, 16, dtype=torch.int32).pin_memory()
-        out_h = torch.empty(15 + 3, dtype=torch.int32).pin_memory()
-        fs_host = binding.bf16_host(fs[0])
+        feats_h = torch.empty(B, 16, F, dtype=torch.bfloat16).pin_memory()
+        mu_h = torch.empty(2, B, 16, dtype=torch.int32).pin_memory()
+        out_h = torch.empty(B, 15 + 3, dtype=torch.int32).pin_memory()
+        if fs is not None:
+            fs_host = binding.bf16_host(fs)
+        else:  # the device-drawn stream's first rows stand in on the host
+            fs_host = feat_stream[:, :16].cpu()
         stream.synchronize()
         # the round's inject consumes the previous round's block features
-        # (positions prev_L .. prev_L+15, the first accept_len of them)
-        prev_L = cur_L = L0
-        h2d = d2h = 0
+        # (positions prev_L .. prev_L+15 of each request, the first accept_len)
+        prev_L = ctx.copy()
+        cur_L = ctx.copy()
         t0 = time.perf_counter()
         for r in range(E):
-            feats_h.copy_(fs_host[prev_L:prev_L + 16].unsqueeze(0))
-            mu_h[0].copy_(torch.from_numpy(m[r % len(m), 0]))
-            mu_h[1].copy_(torch.from_numpy(u[r % len(u), 0]))
+            for b in range(B):
+                if fs is not None:
+                    feats_h[b].copy_(fs_host[b, prev_L[b]:prev_L[b] + 16])
+                else:
+                    feats_h[b].copy_(fs_host[b])
+            mu_h[0].copy_(torch.from_numpy(m[r % len(m)]))
+            mu_h[1].copy_(torch.from_numpy(u[r % len(u)]))
             with torch.cuda.stream(stream):
                 st.feats.copy_(feats_h, non_blocking=True)
-                m_dev[0, 0].copy_(mu_h[0], non_blocking=True)
-                u_dev[0, 0].copy_(mu_h[1], non_blocking=True)
+                m_dev[0].copy_(mu_h[0], non_blocking=True)
+                u_dev[0].copy_(mu_h[1], non_blocking=True)
                 d.graph_launch(stream)
-                out_h[:15].copy_(st.draft[0], non_blocking=True)
-                out_h[15:16].copy_(st.accept_len, non_blocking=True)
-                out_h[16:17].copy_(st.bonus, non_blocking=True)
-                out_h[17:18].copy_(st.ctx_len, non_blocking=True)
+                out_h[:, :15].copy_(st.draft, non_blocking=True)
+                out_h[:, 15].copy_(st.accept_len, non_blocking=True)
+                out_h[:, 16].copy_(st.bonus, non_blocking=True)
+                out_h[:, 17].copy_(st.ctx_len, non_blocking=True)
             stream.synchronize()
-            prev_L, cur_L = cur_L, int(out_h[17])
-            h2d = feats_h.numel() * 2 + mu_h.numel() * 4
-            d2h = out_h.numel() * 4
+            prev_L, cur_L = cur_L, out_h[:, 17].numpy().astype(int)
+        h2d = feats_h.numel() * 2 + mu_h.numel() * 4
+        d2h = out_h.numel() * 4
         t_e2e = time.perf_counter() - t0
         if world > 1:
             t = torch.tensor([t_e2e], dtype=torch.float64, device=dev)
@@ -359,20 +394,39 @@ def run_gpu(args, rank, world, local_rank):
             t_e2e = float(t.item())
         e2e = {"value": round(15 * B * E * world / t_e2e, 1), "unit": "tok/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": E,
-               "round_us": round(t_e2e / E * 1e6, 1)}
+               "round_us": round(t_e2e / E * 1e6, 1),
+               "note": "includes the stand-in verify kernel"}
 
-    # ---- roofline of the dominant kernel (lm_head + argmax) and of the round
-    hbm, bf16_tf, peak_src = peaks()
-    H, V = cfg.hidden, cfg.vocab
-    lm_bytes = V * H * 2 + 16 * B * H * 2
+    # ---- rooflines: the dominant kernel (lm_head + argmax) and the round
+    hbm, _, peak_src = peaks()
+    tf_burst, tf_sust = tensor_peaks()
+    H, V, D = cfg.hidden, cfg.vocab, cfg.head_dim
+    M = 16 * B
+    lm_bytes = V * H * 2 + M * H * 2
+    lm_flops = 2.0 * M * V * H
     lm_avg_ms = statistics.mean(lm_ms) if lm_ms else float("nan")
-    lm_gbs = lm_bytes / (lm_avg_ms * 1e-3) / 1e9
     round_ms_incl = ms / K
     round_ms = round_ms_incl - verify_ms  # the stand-in verify is not part of the round
-    wb = cfg.weight_bytes()
-    avg_ctx = L0 + accepted / max(1, (n_slots - 1)) / 2
-    kv_bytes = cfg.n_layers * (avg_ctx + 16) * cfg.n_kv_heads * cfg.head_dim * 2 * 2
-    round_bytes = wb + kv_bytes + 8 * F * 2
+    tau = accepted / (K * B)
+    avg_ctx = float(ctx.mean()) + tau * (R / 2)
+    kv_bytes = B * cfg.n_layers * (avg_ctx + 16) * cfg.n_kv_heads * D * 2 * 2
+    round_bytes = cfg.weight_bytes() + kv_bytes + B * tau * F * 2
+    layer_params = cfg.qkv_rows * H + H * cfg.n_q_heads * D + 3 * cfg.intermediate * H
+    inj_params = H * F + cfg.n_layers * 2 * cfg.n_kv_heads * D * H
+    round_flops = 2.0 * M * (cfg.n_layers * layer_params + V * H) + 2.0 * B * tau * inj_params
+    if B == 1:
+        lm_roof = {"bound": "hbm", "achieved": round(lm_bytes / (lm_avg_ms * 1e-3) / 1e9, 1), "peak": hbm,
+                   "unit": "GB/s", "frac": round(lm_bytes / (lm_avg_ms * 1e-3) / 1e9 / hbm, 4),
+                   "traffic": lm_head_traffic(cfg), "peak_source": f"{peak_src} copy bandwidth"}
+    else:
+        ach = lm_flops / (lm_avg_ms * 1e-3) / 1e12
+        lm_roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": tf_sust, "unit": "TFLOP/s",
+                   "frac": round(ach / tf_sust, 4), "traffic": None,
+                   "peak_source": "measured bf16 sustained (f16 dense rate equals bf16 on this part)"}
+    lm_roof.update({"kernel": "lm_head+argmax (tcgen05 GEMM)", "bytes_per_launch": lm_bytes,
+                    "flops_per_launch": lm_flops, "avg_launch_us": round(lm_avg_ms * 1e3, 2)})
+    ctx_desc = f"prompt {int(ctx[0])}" if cfg.ctx0 else f"prompts U[{cfg.ctx_range[0]}, {cfg.ctx_range[1]}]"
+    p_desc = f"match p {cfg.match_p}" if cfg.match_p is not None else f"match p U[{cfg.p_range[0]}, {cfg.p_range[1]}]"
     res = {
         "metric": METRIC,
         "value": round(15 * B * world / (round_ms * 1e-3), 1),
@@ -386,28 +440,29 @@ def run_gpu(args, rank, world, local_rank):
         "round_us_with_stand_in_verify": round(round_ms_incl * 1e3, 1),
         "stand_in_verify_us": round(verify_ms * 1e3, 1),
         "accepted_tok_s": round(accepted * world / (round_ms * K * 1e-3), 1),
-        "mean_tau": round(accepted / K, 3),
+        "mean_tau": round(tau, 3),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f16",
-        "data": "synthetic (seeded N(0,1) target features, N(0,0.02) random-init weights, stand-in verify)",
-        "config": {"workload": f"{cfg.name} drafter batch 1: H{H}, {cfg.n_q_heads}q/{cfg.n_kv_heads}kv x"
-                               f"{cfg.head_dim}, I{cfg.intermediate}, {cfg.n_layers} layers, V{V}, fusion "
-                               f"{F}->{H}, prompt {L0}, block 16, match p {cfg.match_p}",
-                   "batch": B, "prompt": L0, "rounds_per_slot": R,
+        "data": f"synthetic (seeded N(0,1) target features from the {feat_src}, N(0,0.02) random-init weights, "
+                "stand-in verify)",
+        "config": {"workload": f"{cfg.name} drafter batch {B}: H{H}, {cfg.n_q_heads}q/{cfg.n_kv_heads}kv x"
+                               f"{D}, I{cfg.intermediate}, {cfg.n_layers} layers, V{V}, fusion "
+                               f"{F}->{H}, {ctx_desc}, block 16, {p_desc}",
+                   "batch": B, "prompt_mean": float(ctx.mean()), "rounds_per_slot": R,
                    "round_call": "dflash_draft_round" if args.fold_inject
-                   else "dflash_fuse_inject+dflash_draft_block", "slots": n_slots - 1,
-                   "l2": "inputs larger than L2 (3.3 GB of weights stream every round)",
+                   else "dflash_fuse_inject+dflash_draft_block", "slot_groups": n_groups - 1,
+                   "l2": "inputs larger than L2 (the drafter's weights stream every round)",
                    "parallelism": f"replicas x{world}"},
         "gpu_launches": launches_captured,
         "graph_kernel_nodes": n_kernels,
-        "roofline": {"bound": "hbm", "kernel": "lm_head+argmax (tcgen05 GEMM)",
-                     "achieved": round(lm_gbs, 1), "peak": hbm, "unit": "GB/s",
-                     "frac": round(lm_gbs / hbm, 4), "traffic": lm_head_traffic(cfg), "peak_source": peak_src,
-                     "bytes_per_launch": lm_bytes, "avg_launch_us": round(lm_avg_ms * 1e3, 2)},
+        "roofline": lm_roof,
         "round_roofline": {"bytes_per_round": int(round_bytes), "achieved_gbs": round(
             round_bytes / (round_ms * 1e-3) / 1e9, 1), "frac": round(round_bytes / (round_ms * 1e-3) / 1e9 / hbm, 4)},
+        "round_tensor": {"flops_per_round": round_flops, "achieved_tflops": round(
+            round_flops / (round_ms * 1e-3) / 1e12, 1), "peak": tf_sust,
+            "frac": round(round_flops / (round_ms * 1e-3) / 1e12 / tf_sust, 4)},
         "clocks": clk,
         "status_word": status,
         "e2e": e2e,
@@ -428,7 +483,7 @@ def main():
         from workload import get_config
         cfg = get_config(args.config)
         budget = 150.0
-        times, taus = oracle_round_seconds(cfg, budget, max(1, args.steps))
+        times, taus = oracle_round_seconds(cfg, budget, max(1, args.steps or 8))
         used = times[1:] if len(times) > 1 else times
         rs = statistics.mean(used)
         val = 15 / rs
@@ -436,10 +491,12 @@ def main():
                 "n_gpus": args.gpus, "steps": len(used), "warmup": len(times) - len(used),
                 "ms_per_step": round(rs * 1e3, 1), "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": {"workload": f"{cfg.name} drafter batch 1, prompt {cfg.ctx0}, block 16"},
+                "config": {"workload": f"{cfg.name} drafter, one request of batch {cfg.batch} at a time, "
+                                       f"prompt {cfg.ctx0 or cfg.ctx_range[0]}, block 16"},
                 "cpu_baseline": {"value": round(val, 3), "unit": "tok/s", "cores": os.cpu_count(),
                                  "kind": "oracle",
-                                 "sample": f"{len(times)} rounds of request 0 after an untimed {cfg.ctx0}-token "
+                                 "sample": f"{len(times)} rounds of request 0 after an untimed "
+                                           f"{cfg.ctx0 or cfg.ctx_range[0]}-token "
                                            f"prefill, stopped after {budget:.0f} s"},
                 "e2e": {"value": round(val, 3), "unit": "tok/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
@@ -456,7 +513,7 @@ def main():
         res["cpu_baseline"] = {"value": round(15 / rs, 3), "unit": "tok/s", "cores": os.cpu_count(),
                                "kind": "oracle",
                                "sample": f"{len(times)} round(s) of the same workload (request 0) after an "
-                                         f"untimed {cfg.ctx0}-token prefill, float64 NumPy"}
+                                         f"untimed {cfg.ctx0 or cfg.ctx_range[0]}-token prefill, float64 NumPy"}
     if world > 1:
         torch.distributed.destroy_process_group()
     if rank == 0:

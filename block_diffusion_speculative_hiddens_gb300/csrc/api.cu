@@ -162,9 +162,9 @@ bool cfg_valid(const dflash_config* c) {
 #endif
 
 // Split-KV count: about one wave of CTAs, at least 4 pages per split at full
-// slot capacity, at most 16 (one thread-block cluster).  Above 8 (the
-// portable cluster size) dflash_create keeps it only if the GPU can hold a
-// cluster for every (request, KV head) at once.
+// slot capacity, at most 16 (one thread-block cluster).  dflash_create then
+// lowers it until the GPU can hold a cluster for every (request, KV head) at
+// once (clusters are placed within one GPC each).
 int pick_attn_splits(const dflash_config& c, int num_sms) {
   const int pairs = c.max_batch * c.n_kv_heads;
   int want = ceil_div(num_sms, pairs);
@@ -597,9 +597,11 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
   int rc = ok ? DFLASH_OK : DFLASH_ERR_CUDA;
   if (!rc) rc = cuda_err(gemm_init_attributes());
   if (!rc) rc = cuda_err(attn_init_attributes());
-  if (!rc && h->attn_splits > 8 &&
-      attn_max_active_clusters(c.head_dim, c.n_q_heads, c.n_kv_heads, h->attn_splits) < c.max_batch * c.n_kv_heads)
-    h->attn_splits = 8;
+  // every (request, KV head) cluster in one wave: a second wave would double
+  // the attention time, so take the most splits whose clusters all fit
+  while (!rc && h->attn_splits > 1 &&
+         attn_max_active_clusters(c.head_dim, c.n_q_heads, c.n_kv_heads, h->attn_splits) < c.max_batch * c.n_kv_heads)
+    --h->attn_splits;
   if (!rc)
     rc = cuda_err(cudaMemset(h->page_table, 0xFF, (size_t)c.max_slots * c.max_pages_per_slot * sizeof(int)));
   if (!rc) rc = cuda_err(launch_pool_init(h->free_stack, h->free_top, c.max_pages, 0));
