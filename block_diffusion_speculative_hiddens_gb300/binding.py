@@ -31,7 +31,8 @@ class DflashConfig(ctypes.Structure):
         "hidden", "n_q_heads", "n_kv_heads", "head_dim", "intermediate", "n_layers", "vocab",
         "n_fused", "block", "mask_id", "page_size", "max_batch", "max_slots", "max_pages",
         "max_pages_per_slot", "max_rows", "device")] + [("rms_eps", ctypes.c_float),
-                                                         ("rope_theta", ctypes.c_float)]
+                                                         ("rope_theta", ctypes.c_float),
+                                                         ("attn_impl", ctypes.c_int32)]
 
 
 class DflashWeights(ctypes.Structure):
@@ -128,7 +129,7 @@ class Drafter:
     """
 
     def __init__(self, cfg, weights: dict, *, max_batch: int, max_slots: int, max_pages: int,
-                 max_pages_per_slot: int, max_rows: int, device: int = 0):
+                 max_pages_per_slot: int, max_rows: int, device: int = 0, attn_impl: int = 0):
         import torch
         self.lib = load()
         self.cfg = cfg
@@ -140,7 +141,7 @@ class Drafter:
                          page_size=cfg.page_size, max_batch=max_batch, max_slots=max_slots,
                          max_pages=max_pages, max_pages_per_slot=max_pages_per_slot,
                          max_rows=max_rows, device=device, rms_eps=cfg.rms_eps,
-                         rope_theta=cfg.rope_theta)
+                         rope_theta=cfg.rope_theta, attn_impl=attn_impl)
         self.c = c
         nbytes = self.lib.dflash_workspace_bytes(ctypes.byref(c))
         if nbytes == 0:

@@ -86,6 +86,7 @@ struct dflash_handle {
   int max_tok = 0;     // max_batch * block
   int max_pos = 0;     // max_pages_per_slot * page_size
   int attn_splits = 1;
+  bool attn_tc = false;  // tcgen05 attention page loop
   int max_tiles = 0;
   // weights, copied into the workspace at create: matrices packed into
   // 128x64 blocks (f16, except the bf16 fusion projection), gains as fp32
@@ -154,6 +155,7 @@ bool cfg_valid(const dflash_config* c) {
     return false;
   if (c->mask_id < 0 || c->mask_id >= c->vocab) return false;
   if (!(c->rms_eps > 0.f) || !(c->rope_theta > 1.f)) return false;
+  if (c->attn_impl < 0 || c->attn_impl > 2) return false;
   return true;
 }
 
@@ -466,7 +468,7 @@ int draft_impl(dflash_handle* h, const int32_t* slots, int32_t batch, const int3
       }
       ProbeScope ps(h, DFLASH_KID_ATTENTION, s);
       h->launches++;
-      rc = cuda_err(attn_launch(a, batch, s, h->pdl));
+      rc = cuda_err(attn_launch(a, batch, s, h->pdl, h->attn_tc));
       if (rc) return rc;
     }
     {  // output projection + residual; post-attention norm inputs
@@ -597,10 +599,16 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
   int rc = ok ? DFLASH_OK : DFLASH_ERR_CUDA;
   if (!rc) rc = cuda_err(gemm_init_attributes());
   if (!rc) rc = cuda_err(attn_init_attributes());
+  // page loop: the tcgen05 one has the higher fixed cost per CTA and the
+  // higher rate per page, so it is chosen when a split holds 16 pages or more
+  // at full slot capacity (measured on GB300: slower at 4 and 8 pages per
+  // split, 1.3x faster on the whole round at 57)
+  h->attn_tc = c.attn_impl == 2 || (c.attn_impl == 0 && ceil_div(c.max_pages_per_slot, h->attn_splits) >= 16);
   // every (request, KV head) cluster in one wave: a second wave would double
   // the attention time, so take the most splits whose clusters all fit
   while (!rc && h->attn_splits > 1 &&
-         attn_max_active_clusters(c.head_dim, c.n_q_heads, c.n_kv_heads, h->attn_splits) < c.max_batch * c.n_kv_heads)
+         attn_max_active_clusters(c.head_dim, c.n_q_heads, c.n_kv_heads, h->attn_splits, h->attn_tc) <
+             c.max_batch * c.n_kv_heads)
     --h->attn_splits;
   if (!rc)
     rc = cuda_err(cudaMemset(h->page_table, 0xFF, (size_t)c.max_slots * c.max_pages_per_slot * sizeof(int)));

@@ -378,18 +378,385 @@ __global__ void __launch_bounds__(G * KS * 32) k_attn(const AttnParams p) {
   if (threadIdx.x == 0) atrace(p, 5);
 }
 
+// ---------------------------------------------------------------------------
+// Block attention on the 5th-generation tensor cores.  Same grid, cluster,
+// page split and merge as k_attn; per 64-key page:
+//   S = Q K^T   tcgen05.mma M=128 (the G*16 query rows, zero-padded) x N=64 keys x K=D,
+//   softmax     one query row per thread, read from TMEM, P written to shared
+//               memory in the 128-byte-swizzle K-major layout,
+//   O_p = P V   tcgen05.mma M=128 x N=D x K=64 keys, read back and folded into
+//               the row's running output (registers) with the online-softmax
+//               rescale.
+// The K page is already the K-major B operand of the first MMA and the V^T
+// page the K-major B operand of the second (pre-swizzled in HBM).  S, P and
+// O_p are double-buffered, and the next page's Q K^T is issued before this
+// page's P V, so the MMAs overlap the softmax.
+// Warps: 0 page loads (one thread), 1 TMEM allocation and MMA issue (one
+// thread), 2-5 softmax (thread = TMEM lane = query row).
+template <int D>
+struct TcCfg {
+  static constexpr int STAGES = 4;                  // pages in flight
+  static constexpr int BLK = 64 * D * 2;            // one K (or V^T) page block
+  static constexpr int STAGE = 2 * BLK;
+  static constexpr int QB = 128 * D * 2;            // Q: 128 rows x D, D/64 panels of 16 KB
+  static constexpr int PB = 128 * 64 * 2;           // P: 128 rows x 64 keys, one 16 KB panel
+  static constexpr int OFF_Q = STAGES * STAGE;
+  static constexpr int OFF_P = OFF_Q + QB;          // two P buffers
+  static constexpr int OFF_BAR = OFF_P + 2 * PB;
+  static constexpr int MAX_PIDS = 512;
+  static constexpr int OFF_PIDS = OFF_BAR + 256;
+  static constexpr int SMEM = 1024 + OFF_PIDS + MAX_PIDS * 4;  // + 1024 for aligning the base
+  static constexpr int S_COL = 0;                   // S buffers: columns [0, 128)
+  static constexpr int O_COL = 128;                 // O_p buffers: columns [128, 128 + 2D)
+  // columns allocated: exactly what the buffers use (a power of two), so two
+  // CTAs that might share an SM never wait on each other's columns
+  static constexpr uint32_t TMEM_COLS = D == 128 ? 512 : 256;
+};
+
+template <int D, int G>
+__global__ void __launch_bounds__(192, 1) k_attn_tc(const AttnParams p) {
+  using C = TcCfg<D>;
+  extern __shared__ __align__(128) uint8_t sm_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
+  uint64_t* full = bars;                    // [STAGES] page landed
+  uint64_t* empty = full + C::STAGES;       // [STAGES] page's MMAs done
+  uint64_t* s_full = empty + C::STAGES;     // [2] S in TMEM
+  uint64_t* s_empty = s_full + 2;           // [2] S read by the softmax warps
+  uint64_t* p_full = s_empty + 2;           // [2] P in shared memory
+  uint64_t* o_full = p_full + 2;            // [2] O_p in TMEM
+  uint64_t* o_empty = o_full + 2;           // [2] O_p read by the softmax warps
+  uint64_t* q_full = o_empty + 2;           // Q in shared memory
+  uint64_t* mdone = q_full + 1;             // every issued MMA complete
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mdone + 1);
+  int* pids = reinterpret_cast<int*>(sm + C::OFF_PIDS);
+
+  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rows = G * 16;
+  const int hq = p.hq, hkv = p.hkv;
+  const uint32_t idesc_s = idesc_f16_f32(128, 64, 0);
+  const uint32_t idesc_o = idesc_f16_f32(128, D, 0);
+
+  if (threadIdx.x == 0) {
+    atrace(p, 0);
+    for (int i = 0; i < C::STAGES; ++i) {
+      mbar_init(full + i, 1);
+      mbar_init(empty + i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(s_full + i, 1);
+      mbar_init(s_empty + i, 128);
+      mbar_init(p_full + i, 128);
+      mbar_init(o_full + i, 1);
+      mbar_init(o_empty + i, 128);
+    }
+    mbar_init(q_full, 128);
+    mbar_init(mdone, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_launch_dependents();
+  pdl_wait();
+
+  const int slot = p.slots[b];
+  const int nkeys = p.ctx_len[slot] + DFL_BLOCK;
+  const int npages = (nkeys + 63) >> 6;
+  const int pb = (int)((long long)split * npages / p.n_splits);  // balanced page ranges
+  const int pe = (int)((long long)(split + 1) * npages / p.n_splits);
+  const int n = pe - pb;
+  const int* pt = p.kv.page_table + (size_t)slot * p.kv.max_pages_per_slot;
+  for (int i = threadIdx.x; i < n && i < C::MAX_PIDS; i += blockDim.x)
+    pids[i] = pb + i < p.kv.max_pages_per_slot ? pt[pb + i] : -1;
+  __syncthreads();
+  if (threadIdx.x == 0) atrace(p, 1);
+  bool aborted = false;
+
+  // running state of this thread's query row (softmax warps)
+  float o[D];
+  float m_run = -INFINITY, l_run = 0.f;
+#pragma unroll
+  for (int d = 0; d < D; ++d) o[d] = 0.f;
+  const int q4 = warp & 3;
+  const int r = q4 * 32 + lane;  // TMEM lane = query row (softmax warps)
+
+  if (warp == 0) {
+    // ------------------------------------------------ page loads
+    if (lane == 0) {
+      const f16* kbase = p.kv.k_pool + (size_t)p.layer * p.kv.layer_stride;
+      const f16* vbase = p.kv.v_pool + (size_t)p.layer * p.kv.layer_stride;
+      int i = 0;
+      for (; i < n; ++i) {
+        const int s = i % C::STAGES;
+        if (i >= C::STAGES && !mbar_wait(empty + s, (uint32_t)((i / C::STAGES - 1) & 1), p.status, &aborted)) break;
+        const int page_idx = pb + i;
+        int pg = i < C::MAX_PIDS ? pids[i] : (page_idx < p.kv.max_pages_per_slot ? pt[page_idx] : -1);
+        if (pg < 0 || pg >= p.kv.max_pages) {
+          dev_error(p.status, DFLASH_DEV_PAGE);
+          pg = 0;
+        }
+        const size_t off = ((size_t)pg * hkv + kvh) * (64 * D);
+        uint8_t* dst = sm + s * C::STAGE;
+        mbar_arrive_expect_tx(full + s, C::STAGE);
+        bulk_load(dst, kbase + off, C::BLK, full + s);
+        bulk_load(dst + C::BLK, vbase + off, C::BLK, full + s);
+      }
+      // every issued copy lands before the CTA may exit
+      for (int j = (i > C::STAGES ? i - C::STAGES : 0); j < i; ++j) {
+        bool drain_abort = false;
+        mbar_wait(full + (j % C::STAGES), (uint32_t)((j / C::STAGES) & 1), p.status, &drain_abort);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issue
+    if (lane == 0 && mbar_wait(q_full, 0, p.status, &aborted)) {
+      tc_fence_after();
+      const uint32_t q_addr = smem_u32(sm + C::OFF_Q);
+      auto issue_s = [&](int i) {
+        const int s = i % C::STAGES, bb = i & 1;
+        if (!mbar_wait(full + s, (uint32_t)((i / C::STAGES) & 1), p.status, &aborted)) return false;
+        if (i >= 2 && !mbar_wait(s_empty + bb, (uint32_t)((i / 2 - 1) & 1), p.status, &aborted)) return false;
+        tc_fence_after();
+        const uint32_t k_addr = smem_u32(sm + s * C::STAGE);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t ad = sdesc_sw128(q_addr + (uint32_t)((kk >> 2) * 16384)) + (uint64_t)(2 * (kk & 3));
+          const uint64_t bd = sdesc_sw128(k_addr + (uint32_t)((kk >> 2) * 8192)) + (uint64_t)(2 * (kk & 3));
+          tc_mma_f16(tmem + (uint32_t)(C::S_COL + 64 * bb), ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(s_full + bb);
+        return true;
+      };
+      bool ok = n == 0 || issue_s(0);
+      for (int i = 0; i < n && ok; ++i) {
+        if (i + 1 < n && !issue_s(i + 1)) break;
+        const int s = i % C::STAGES, bb = i & 1;
+        if (!mbar_wait(p_full + bb, (uint32_t)((i / 2) & 1), p.status, &aborted)) break;
+        if (i >= 2 && !mbar_wait(o_empty + bb, (uint32_t)((i / 2 - 1) & 1), p.status, &aborted)) break;
+        tc_fence_after();
+        const uint32_t p_addr = smem_u32(sm + C::OFF_P + bb * C::PB);
+        const uint32_t v_addr = smem_u32(sm + s * C::STAGE + C::BLK);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t ad = sdesc_sw128(p_addr) + (uint64_t)(2 * kk);
+          const uint64_t bd = sdesc_sw128(v_addr) + (uint64_t)(2 * kk);
+          tc_mma_f16(tmem + (uint32_t)(C::O_COL + D * bb), ad, bd, idesc_o, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(o_full + bb);
+        tc_commit(empty + s);
+      }
+      // every MMA this thread issued completes before the columns are freed
+      tc_commit(mdone);
+      bool drain_abort = false;
+      mbar_wait(mdone, 0, p.status, &drain_abort);
+    }
+  } else {
+    // ------------------------------------------------ softmax (thread = query row r)
+    {  // this row's query, zero-padded to 128 rows, into the swizzled Q tile
+      const int h = r >> 4, t = r & 15;
+      const f16* src = p.q + ((size_t)(b * DFL_BLOCK + t) * hq + kvh * G + h) * D;
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c) {
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (r < rows) v = *reinterpret_cast<const uint4*>(src + c * 8);
+        uint8_t* dst = sm + C::OFF_Q + (c >> 3) * 16384 + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+        *reinterpret_cast<uint4*>(dst) = v;
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(q_full);
+    }
+    const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
+    // O_p of page i is folded in while page i+1's softmax is done: the P V
+    // MMA of one page overlaps the next page's softmax
+    auto fold = [&](int i, float alpha) {
+      const int bb = i & 1;
+      if (!mbar_wait(o_full + bb, (uint32_t)((i / 2) & 1), p.status, &aborted)) return false;
+      tc_fence_after();
+#pragma unroll
+      for (int j = 0; j < D / 16; ++j) {
+        float v[16];
+        tmem_ld16(lane_base + (uint32_t)(C::O_COL + D * bb + 16 * j), v);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) o[16 * j + e] = o[16 * j + e] * alpha + v[e];
+      }
+      tc_fence_before();
+      mbar_arrive(o_empty + bb);
+      return true;
+    };
+    float alpha_prev = 0.f;  // rescale that goes with the pending O_p
+    bool ok = true;
+    for (int i = 0; i < n && ok; ++i) {
+      const int bb = i & 1;
+      if (!mbar_wait(s_full + bb, (uint32_t)((i / 2) & 1), p.status, &aborted)) break;
+      if (i == 0 && threadIdx.x == 64) atrace(p, 2);
+      tc_fence_after();
+      float sc[64];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) tmem_ld16(lane_base + (uint32_t)(C::S_COL + 64 * bb + 16 * j), sc + 16 * j);
+      tc_fence_before();
+      mbar_arrive(s_empty + bb);
+      const int valid = min(64, nkeys - (pb + i) * 64);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < 64; ++k) {
+        sc[k] = k < valid ? sc[k] * p.scale_log2 : -INFINITY;
+        mx = fmaxf(mx, sc[k]);
+      }
+      const float mn = fmaxf(m_run, mx);
+      const float ref = mn == -INFINITY ? 0.f : mn;  // a row with only masked keys so far adds 0
+      const float alpha = exp2f(m_run - ref);
+      float rs = 0.f;
+      uint32_t pk[32];
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        const float a = exp2f(sc[2 * k] - ref), c = exp2f(sc[2 * k + 1] - ref);
+        rs += a + c;
+        pk[k] = pack_f16x2(a, c);
+      }
+      l_run = l_run * alpha + rs;
+      m_run = mn;
+      {  // P row r: 64 keys = 8 chunks of 16 bytes, swizzled like the K page rows
+        uint8_t* prow = sm + C::OFF_P + bb * C::PB + r * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(prow + (((c ^ (r & 7))) << 4)) =
+              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(p_full + bb);
+      // o holds pages < i-1 at the max before page i-1; bring in page i-1
+      if (i > 0) ok = fold(i - 1, alpha_prev);
+      alpha_prev = alpha;
+    }
+    if (ok && n > 0 && !aborted) fold(n - 1, alpha_prev);
+  }
+  if (threadIdx.x == 0) atrace(p, 3);
+  tc_fence_before();
+  __syncthreads();  // every TMEM read and MMA done, every page landed
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+
+  const int h = r >> 4, t = r & 15;
+  const bool row_out = warp >= 2 && r < rows;
+  if (p.n_splits == 1) {
+    if (row_out) {
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      f16* dst = p.out + ((size_t)(b * DFL_BLOCK + t) * hq + kvh * G + h) * D;
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c)
+        *reinterpret_cast<uint4*>(dst + c * 8) =
+            make_uint4(pack_f16x2(o[8 * c] * inv, o[8 * c + 1] * inv), pack_f16x2(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
+                       pack_f16x2(o[8 * c + 4] * inv, o[8 * c + 5] * inv), pack_f16x2(o[8 * c + 6] * inv, o[8 * c + 7] * inv));
+    }
+    if (threadIdx.x == 0) atrace(p, 5);
+    return;
+  }
+
+  // partial (unnormalised O, running max, running sum) for the cluster merge,
+  // in the page-stage area (every page is consumed)
+  constexpr int PS = D + 4;
+  float* part = reinterpret_cast<float*>(sm);
+  if (row_out) {
+#pragma unroll
+    for (int c = 0; c < D / 4; ++c)
+      *reinterpret_cast<float4*>(part + r * PS + 4 * c) = make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+    part[rows * PS + r] = m_run;
+    part[rows * PS + rows + r] = l_run;
+  }
+  if (threadIdx.x == 0) atrace(p, 4);
+  cluster_sync_all();
+
+  const int nsp = p.n_splits;
+  const int rank = (int)cluster_ctarank();
+  const int rpc = (rows + nsp - 1) / nsp;  // rows merged by this CTA
+  const int rb = rank * rpc, re = min(rows, rb + rpc);
+  const uint32_t part_local = smem_u32(part);
+  for (int e = threadIdx.x; e < (re - rb) * (D / 4); e += blockDim.x) {
+    const int rr = rb + e / (D / 4), d = (e % (D / 4)) * 4;
+    float mv[ATTN_MAX_SPLITS], lv[ATTN_MAX_SPLITS];
+    float4 v[ATTN_MAX_SPLITS];
+#pragma unroll
+    for (int sp = 0; sp < ATTN_MAX_SPLITS; ++sp) {
+      mv[sp] = -INFINITY;
+      lv[sp] = 0.f;
+      v[sp] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (sp < nsp) {
+        const uint32_t a = dsmem_addr(part_local, (uint32_t)sp);
+        mv[sp] = ld_dsmem(a + 4u * (uint32_t)(rows * PS + rr));
+        lv[sp] = ld_dsmem(a + 4u * (uint32_t)(rows * PS + rows + rr));
+        v[sp] = ld_dsmem4(a + 4u * (uint32_t)(rr * PS + d));
+      }
+    }
+    float M = -INFINITY;
+#pragma unroll
+    for (int sp = 0; sp < ATTN_MAX_SPLITS; ++sp)
+      if (lv[sp] > 0.f) M = fmaxf(M, mv[sp]);
+    float L = 0.f;
+#pragma unroll
+    for (int sp = 0; sp < ATTN_MAX_SPLITS; ++sp) {
+      const float w = lv[sp] > 0.f ? exp2f(mv[sp] - M) : 0.f;
+      mv[sp] = w;
+      L += w * lv[sp];
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int sp = 0; sp < ATTN_MAX_SPLITS; ++sp) {
+      if (sp < nsp) {
+        const float w = mv[sp] * inv;
+        acc.x += w * v[sp].x;
+        acc.y += w * v[sp].y;
+        acc.z += w * v[sp].z;
+        acc.w += w * v[sp].w;
+      }
+    }
+    const int wq = rr / 16, tt = rr % 16;
+    f16* dst = p.out + ((size_t)(b * DFL_BLOCK + tt) * hq + kvh * G + wq) * D + d;
+    *reinterpret_cast<uint32_t*>(dst) = pack_f16x2(acc.x, acc.y);
+    *reinterpret_cast<uint32_t*>(dst + 2) = pack_f16x2(acc.z, acc.w);
+  }
+  // keep this CTA's partial alive until every CTA of the cluster has read it
+  cluster_sync_all();
+  if (threadIdx.x == 0) atrace(p, 5);
+}
+
 // key split per head: 2 warps per query head up to 4 heads per KV head
 template <int G>
 constexpr int attn_ks() {
   return G <= 4 ? 2 : 1;
 }
 
+// The kernel instance, block size and shared memory of one page loop for (D, G).
+template <int D, int G, bool TC>
+struct AttnKernel;
 template <int D, int G>
+struct AttnKernel<D, G, true> {
+  static constexpr auto fn = k_attn_tc<D, G>;
+  static constexpr int threads = 192;
+  static constexpr int smem = TcCfg<D>::SMEM;
+};
+template <int D, int G>
+struct AttnKernel<D, G, false> {
+  static constexpr auto fn = k_attn<D, G, attn_ks<G>()>;
+  static constexpr int threads = G * attn_ks<G>() * 32;
+  static constexpr int smem = AttnCfg<D>::SMEM;
+};
+
+template <int D, int G, bool TC>
 cudaError_t launch_t(const AttnParams& p, int batch, cudaStream_t s, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.n_splits, (unsigned)p.hkv, (unsigned)batch);
-  cfg.blockDim = dim3(G * attn_ks<G>() * 32);
-  cfg.dynamicSmemBytes = AttnCfg<D>::SMEM;
+  cfg.blockDim = dim3(AttnKernel<D, G, TC>::threads);
+  cfg.dynamicSmemBytes = AttnKernel<D, G, TC>::smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;  // the splits of one KV head
@@ -400,45 +767,45 @@ cudaError_t launch_t(const AttnParams& p, int batch, cudaStream_t s, bool pdl) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, k_attn<D, G, attn_ks<G>()>, p);
+  return cudaLaunchKernelEx(&cfg, AttnKernel<D, G, TC>::fn, p);
 }
 
-template <int D>
+template <int D, bool TC>
 cudaError_t launch_d(const AttnParams& p, int batch, cudaStream_t s, bool pdl) {
   switch (p.hq / p.hkv) {
-    case 1: return launch_t<D, 1>(p, batch, s, pdl);
-    case 2: return launch_t<D, 2>(p, batch, s, pdl);
-    case 4: return launch_t<D, 4>(p, batch, s, pdl);
-    case 8: return launch_t<D, 8>(p, batch, s, pdl);
+    case 1: return launch_t<D, 1, TC>(p, batch, s, pdl);
+    case 2: return launch_t<D, 2, TC>(p, batch, s, pdl);
+    case 4: return launch_t<D, 4, TC>(p, batch, s, pdl);
+    case 8: return launch_t<D, 8, TC>(p, batch, s, pdl);
   }
   return cudaErrorInvalidValue;
 }
 
-template <int D, int G>
+template <int D, int G, bool TC>
 cudaError_t attr_t() {
-  auto k = k_attn<D, G, attn_ks<G>()>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnCfg<D>::SMEM);
+  auto k = AttnKernel<D, G, TC>::fn;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnKernel<D, G, TC>::smem);
   if (e) return e;
   return cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
 }
 
-template <int D>
+template <int D, bool TC>
 cudaError_t attr_d() {
   cudaError_t e;
-  if ((e = attr_t<D, 1>())) return e;
-  if ((e = attr_t<D, 2>())) return e;
-  if ((e = attr_t<D, 4>())) return e;
-  return attr_t<D, 8>();
+  if ((e = attr_t<D, 1, TC>())) return e;
+  if ((e = attr_t<D, 2, TC>())) return e;
+  if ((e = attr_t<D, 4, TC>())) return e;
+  return attr_t<D, 8, TC>();
 }
 
 // Clusters of `splits` CTAs of the attention kernel for this shape that the
 // GPU can hold at once (0 when it cannot launch them at all).
-template <int D, int G>
+template <int D, int G, bool TC>
 int max_clusters_t(int splits, int hkv) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)splits, (unsigned)hkv, 1);
-  cfg.blockDim = dim3(G * attn_ks<G>() * 32);
-  cfg.dynamicSmemBytes = AttnCfg<D>::SMEM;
+  cfg.blockDim = dim3(AttnKernel<D, G, TC>::threads);
+  cfg.dynamicSmemBytes = AttnKernel<D, G, TC>::smem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)splits;
@@ -447,41 +814,43 @@ int max_clusters_t(int splits, int hkv) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, k_attn<D, G, attn_ks<G>()>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, AttnKernel<D, G, TC>::fn, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
   return n;
 }
 
-template <int D>
+template <int D, bool TC>
 int max_clusters_d(int splits, int G, int hkv) {
   switch (G) {
-    case 1: return max_clusters_t<D, 1>(splits, hkv);
-    case 2: return max_clusters_t<D, 2>(splits, hkv);
-    case 4: return max_clusters_t<D, 4>(splits, hkv);
-    case 8: return max_clusters_t<D, 8>(splits, hkv);
+    case 1: return max_clusters_t<D, 1, TC>(splits, hkv);
+    case 2: return max_clusters_t<D, 2, TC>(splits, hkv);
+    case 4: return max_clusters_t<D, 4, TC>(splits, hkv);
+    case 8: return max_clusters_t<D, 8, TC>(splits, hkv);
   }
   return 0;
 }
 
 }  // namespace
 
-size_t attn_smem_bytes(int D) { return D == 64 ? AttnCfg<64>::SMEM : AttnCfg<128>::SMEM; }
-
-int attn_max_active_clusters(int D, int hq, int hkv, int splits) {
+int attn_max_active_clusters(int D, int hq, int hkv, int splits, bool tc) {
   if (splits < 1 || splits > ATTN_MAX_SPLITS) return 0;
-  return D == 64 ? max_clusters_d<64>(splits, hq / hkv, hkv) : max_clusters_d<128>(splits, hq / hkv, hkv);
+  const int G = hq / hkv;
+  if (D == 64) return tc ? max_clusters_d<64, true>(splits, G, hkv) : max_clusters_d<64, false>(splits, G, hkv);
+  return tc ? max_clusters_d<128, true>(splits, G, hkv) : max_clusters_d<128, false>(splits, G, hkv);
 }
 
 cudaError_t attn_init_attributes() {
-  cudaError_t e = attr_d<64>();
-  if (e) return e;
-  return attr_d<128>();
+  cudaError_t e;
+  if ((e = attr_d<64, false>())) return e;
+  if ((e = attr_d<64, true>())) return e;
+  if ((e = attr_d<128, false>())) return e;
+  return attr_d<128, true>();
 }
 
-cudaError_t attn_launch(const AttnParams& p, int batch, cudaStream_t s, bool pdl) {
-  if (p.D == 64) return launch_d<64>(p, batch, s, pdl);
-  if (p.D == 128) return launch_d<128>(p, batch, s, pdl);
+cudaError_t attn_launch(const AttnParams& p, int batch, cudaStream_t s, bool pdl, bool tc) {
+  if (p.D == 64) return tc ? launch_d<64, true>(p, batch, s, pdl) : launch_d<64, false>(p, batch, s, pdl);
+  if (p.D == 128) return tc ? launch_d<128, true>(p, batch, s, pdl) : launch_d<128, false>(p, batch, s, pdl);
   return cudaErrorInvalidValue;
 }

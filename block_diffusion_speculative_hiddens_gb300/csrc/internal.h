@@ -121,10 +121,10 @@ int gemm_pick_stages(int BN, int mode);
 cudaError_t gemm_launch(const CUtensorMap& B, const GemmParams& p, int grid, cudaStream_t s, bool pdl);
 cudaError_t gemm_init_attributes();
 
-size_t attn_smem_bytes(int D);
-// Attention clusters of `splits` CTAs the GPU can hold at once (0: cannot launch).
-int attn_max_active_clusters(int D, int hq, int hkv, int splits);
-cudaError_t attn_launch(const AttnParams& p, int batch, cudaStream_t s, bool pdl);
+// Attention clusters of `splits` CTAs the GPU can hold at once (0: cannot
+// launch); tc selects the tcgen05 page loop, else the warp-MMA one.
+int attn_max_active_clusters(int D, int hq, int hkv, int splits, bool tc);
+cudaError_t attn_launch(const AttnParams& p, int batch, cudaStream_t s, bool pdl, bool tc);
 cudaError_t attn_init_attributes();
 
 // weight preparation (dflash_create)

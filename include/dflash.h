@@ -86,6 +86,8 @@ typedef struct dflash_config {
   int32_t device;             /* CUDA device ordinal */
   float rms_eps;              /* RMSNorm epsilon (1e-6) */
   float rope_theta;           /* RoPE base */
+  int32_t attn_impl;          /* block attention page loop: 0 by capacity (tensor cores from
+                                 16 pages per split up), 1 warp MMAs, 2 tcgen05 */
 } dflash_config;
 
 /* Device pointers to the drafter weights, all bf16 and row-major; the arrays

@@ -33,7 +33,7 @@ class GpuRun:
     """CUDA-path driver: prefill every request, then rounds with the stand-in verify."""
 
     def __init__(self, cfg, rounds: int, weights_np=None, batch_ids=None, prefill_chunk=4096,
-                 ctx=None):
+                 ctx=None, attn_impl: int = 0):
         import torch
         from block_diffusion_speculative_hiddens_gb300 import Drafter, weights_to_device
         from block_diffusion_speculative_hiddens_gb300.session import RoundState, SyntheticVerify
@@ -49,7 +49,8 @@ class GpuRun:
         self.stream_rows = cap
         self.chunk = min(prefill_chunk, int(self.ctx0.max()))
         self.d = Drafter(cfg, self.w_dev, max_batch=B, max_slots=B, max_pages=mpps * B,
-                         max_pages_per_slot=mpps, max_rows=max(self.chunk, B * cfg.block))
+                         max_pages_per_slot=mpps, max_rows=max(self.chunk, B * cfg.block),
+                         attn_impl=attn_impl)
         dev = torch.device("cuda:0")
         self.dev = dev
         # feature stream: every position a request can reach

@@ -48,7 +48,7 @@ def test_workspace_sizing_accepts_every_workload(lib, name):
 
 @pytest.mark.parametrize("bad", [dict(head_dim=96), dict(block=8), dict(page_size=32), dict(n_layers=9),
                                  dict(n_kv_heads=3), dict(max_batch=65), dict(mask_id=-1),
-                                 dict(hidden=200), dict(rope_theta=0.5)])
+                                 dict(hidden=200), dict(rope_theta=0.5), dict(attn_impl=3)])
 def test_workspace_sizing_rejects_unsupported(lib, bad):
     assert lib.dflash_workspace_bytes(ctypes.byref(_cfg(CONFIGS["tiny"], **bad))) == 0
 

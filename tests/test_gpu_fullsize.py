@@ -31,11 +31,12 @@ def _check_kv(g, o, j_gpu, j_orc, positions, layers):
             assert rel_l2(to_np(v)[0], o.reqs[j_orc].V[l][p]) < TOL_REL_L2, (l, p)
 
 
-@pytest.mark.parametrize("name", ["qwen3-8b", "llama3.1-8b"])
-def test_batch1_workload_rounds_match_oracle(lib, name):
+@pytest.mark.parametrize("name,attn_impl", [("qwen3-8b", 0), ("llama3.1-8b", 0), ("qwen3-8b", 2)],
+                         ids=["qwen3-8b", "llama3.1-8b", "qwen3-8b-attn-tcgen05"])
+def test_batch1_workload_rounds_match_oracle(lib, name, attn_impl):
     cfg = get_config(name)
     w = make_weights(cfg)
-    g = GpuRun(cfg, 2, weights_np=w, prefill_chunk=2048)
+    g = GpuRun(cfg, 2, weights_np=w, prefill_chunk=2048, attn_impl=attn_impl)
     g.prefill()
     o = OracleRun(cfg, 2, weights_np=w, cache=False)
     o.prefill()

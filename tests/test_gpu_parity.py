@@ -11,10 +11,10 @@ pytestmark = pytest.mark.gpu
 SMALL = ["tiny", "tiny-gains", "small", "small-batch"]
 
 
-def _pair(name, rounds, **kw):
+def _pair(name, rounds, attn_impl=0, **kw):
     cfg = get_config(name)
     w = make_weights(cfg)
-    g = GpuRun(cfg, rounds, weights_np=w, **kw)
+    g = GpuRun(cfg, rounds, weights_np=w, attn_impl=attn_impl, **kw)
     o = OracleRun(cfg, rounds, weights_np=w, **kw)
     g.prefill()
     o.prefill()
@@ -38,9 +38,14 @@ def test_inject_kv_matches_oracle(lib, name):
     assert g.d.read_status() == 0
 
 
+# attention page loops: 1 warp MMAs, 2 tcgen05 (the default picks by capacity)
+ATTN = [pytest.param(1, id="attn-warp-mma"), pytest.param(2, id="attn-tcgen05")]
+
+
+@pytest.mark.parametrize("attn_impl", ATTN)
 @pytest.mark.parametrize("name", SMALL)
-def test_draft_round_matches_oracle(lib, name):
-    cfg, g, o = _pair(name, 2)
+def test_draft_round_matches_oracle(lib, name, attn_impl):
+    cfg, g, o = _pair(name, 2, attn_impl=attn_impl)
     for r in range(2):
         go = g.round(debug=True)
         oo = o.round(want_logits=True)
@@ -58,10 +63,11 @@ def test_draft_round_matches_oracle(lib, name):
     assert g.d.read_status() == 0
 
 
+@pytest.mark.parametrize("attn_impl", ATTN)
 @pytest.mark.parametrize("folded", [False, True], ids=["separate", "folded"])
 @pytest.mark.parametrize("name,rounds", [("tiny", 8), ("small-batch", 4)])
-def test_rounds_accept_bit_exact(lib, name, rounds, folded):
-    cfg, g, o = _pair(name, rounds)
+def test_rounds_accept_bit_exact(lib, name, rounds, folded, attn_impl):
+    cfg, g, o = _pair(name, rounds, attn_impl=attn_impl)
     for r in range(rounds):
         go = g.round(folded=folded)
         oo = o.round(want_logits=False)
