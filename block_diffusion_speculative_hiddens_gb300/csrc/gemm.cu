@@ -696,49 +696,64 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
         if (!last) continue;
       }
       for (int tc0 = 0; tc0 < mt; tc0 += 32) {
-        // one copy of the reduction code (run cold once per tile): not unrolled
-#pragma unroll 1
-        for (int sub = 0; sub < 2; ++sub) {
-          const int col = tc0 + 16 * sub;
-          if (col < BN) {
-            float v[16];
-            if (split) {
+        float v0[16], v1[16];
+        const bool two = tc0 + 16 < BN;  // a second 16-column chunk in this 32-token chunk
+        if (split) {
 #pragma unroll
-              for (int i = 0; i < 16; ++i) v[i] = 0.f;
-              // Up to RED_PARTS parts' 16-column chunks land in shared memory
-              // by bulk copies (one issuing thread, one barrier: one round
-              // trip), then are added in k order by a compact loop -- this
-              // code runs cold once per tile, so it stays short.
-              // Every part after the first opens its CTA's range (slot 0);
-              // the first part is slot 1 unless the tile also opens c_first's.
-              const int sl_first = unit_start(c_first, U, G) == tile * KB ? 0 : 1;
-              for (int cc0 = c_first; cc0 <= c_last && !aborted; cc0 += RED_PARTS) {
-                const int nk = (c_last - cc0 + 1) < RED_PARTS ? (c_last - cc0 + 1) : RED_PARTS;
-                if (et == 0) {
-                  fence_proxy_async_global();  // parts acquired through the tile counter
-                  mbar_arrive_expect_tx(red, (uint32_t)(nk * RED_CHUNK * 4));
+          for (int i = 0; i < 16; ++i) v0[i] = v1[i] = 0.f;
+          // The parts' 16-column chunks land in shared memory by bulk copies
+          // (one issuing thread, one barrier per batch) and are added in k
+          // order by a compact loop -- this code runs cold once per tile.  On
+          // the CTA's last segment every weight stage has been consumed, so
+          // the whole ring takes a batch; otherwise the RED_PARTS-chunk buffer.
+          // Every part after the first opens its CTA's range (slot 0); the
+          // first part is slot 1 unless the tile also opens c_first's.
+          const int sl_first = unit_start(c_first, U, G) == tile * KB ? 0 : 1;
+          const bool ring_free = u == u1;
+          float* land = ring_free ? reinterpret_cast<float*>(sm) : red_buf;
+          const int cap_items = ring_free ? (stages * stage_bytes) / (RED_CHUNK * 4) : RED_PARTS;
+          const int nparts = c_last - c_first + 1;
+          const int nitems = nparts * (two ? 2 : 1);  // (sub, part), part fastest
+          for (int it0 = 0; it0 < nitems && !aborted; it0 += cap_items) {
+            const int nb = (nitems - it0) < cap_items ? (nitems - it0) : cap_items;
+            if (et == 0) {
+              fence_proxy_async_global();  // parts acquired through the tile counter
+              mbar_arrive_expect_tx(red, (uint32_t)(nb * RED_CHUNK * 4));
 #pragma unroll 1
-                  for (int k = 0; k < nk; ++k) {
-                    const int cc = cc0 + k;
-                    const int sl = cc == c_first ? sl_first : 0;
-                    bulk_load(red_buf + k * RED_CHUNK, p.ws + (size_t)(cc * 2 + sl) * (DFL_BN_MAX * 128) + col * 128,
-                              RED_CHUNK * 4, red);
-                  }
-                }
-                if (!mbar_wait(red, red_phase, p.status, &aborted)) break;
-                red_phase ^= 1u;
-#pragma unroll 1
-                for (int k = 0; k < nk; ++k)
-#pragma unroll
-                  for (int i = 0; i < 16; ++i) v[i] += red_buf[k * RED_CHUNK + i * 128 + r];
-                named_bar_sync(1, EPI_THREADS);  // red_buf free for the next parts
+              for (int k = 0; k < nb; ++k) {
+                const int item = it0 + k;
+                const int sub = item >= nparts ? 1 : 0;
+                const int cc = c_first + item - sub * nparts;
+                const int sl = cc == c_first ? sl_first : 0;
+                bulk_load(land + k * RED_CHUNK,
+                          p.ws + (size_t)(cc * 2 + sl) * (DFL_BN_MAX * 128) + (tc0 + 16 * sub) * 128,
+                          RED_CHUNK * 4, red);
               }
-            } else {
-              tmem_ld16(taddr + (uint32_t)col, v);
             }
+            if (!mbar_wait(red, red_phase, p.status, &aborted)) break;
+            red_phase ^= 1u;
+#pragma unroll 1
+            for (int k = 0; k < nb; ++k) {
+              const float* src = land + k * RED_CHUNK + r;
+              if (it0 + k < nparts) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) stg[(16 * sub + i) * 128 + r] = v[i];
+                for (int i = 0; i < 16; ++i) v0[i] += src[i * 128];
+              } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v1[i] += src[i * 128];
+              }
+            }
+            named_bar_sync(1, EPI_THREADS);  // landing area free for the next batch
           }
+        } else {
+          tmem_ld16(taddr + (uint32_t)tc0, v0);
+          if (two) tmem_ld16(taddr + (uint32_t)(tc0 + 16), v1);
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) stg[i * 128 + r] = v0[i];
+        if (two) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) stg[(16 + i) * 128 + r] = v1[i];
         }
         named_bar_sync(1, EPI_THREADS);
         epi_final<MODE>(p, (int)tile, t_base + tc0, (mt - tc0) < 32 ? (mt - tc0) : 32, stg, ew, lane, use_pre,
