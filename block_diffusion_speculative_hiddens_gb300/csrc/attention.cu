@@ -392,7 +392,9 @@ __global__ void __launch_bounds__(G * KS * 32) k_attn(const AttnParams p) {
 // O_p are double-buffered, and the next page's Q K^T is issued before this
 // page's P V, so the MMAs overlap the softmax.
 // Warps: 0 page loads (one thread), 1 TMEM allocation and MMA issue (one
-// thread), 2-5 softmax (thread = TMEM lane = query row).
+// thread), 2-9 softmax: two threads per query row (TMEM lane), each taking 32
+// of a page's 64 keys and half of the output columns; the pair trades its
+// half-row maxima through shared memory once per page.
 template <int D>
 struct TcCfg {
   static constexpr int STAGES = 4;                  // pages in flight
@@ -405,7 +407,8 @@ struct TcCfg {
   static constexpr int OFF_BAR = OFF_P + 2 * PB;
   static constexpr int MAX_PIDS = 512;
   static constexpr int OFF_PIDS = OFF_BAR + 256;
-  static constexpr int SMEM = 1024 + OFF_PIDS + MAX_PIDS * 4;  // + 1024 for aligning the base
+  static constexpr int OFF_X = OFF_PIDS + MAX_PIDS * 4;  // half-row exchange: [2 parities][2 halves][128] u64
+  static constexpr int SMEM = 1024 + OFF_X + 2 * 2 * 128 * 8;  // + 1024 for aligning the base
   static constexpr int S_COL = 0;                   // S buffers: columns [0, 128)
   static constexpr int O_COL = 128;                 // O_p buffers: columns [128, 128 + 2D)
   // columns allocated: exactly what the buffers use (a power of two), so two
@@ -414,7 +417,7 @@ struct TcCfg {
 };
 
 template <int D, int G>
-__global__ void __launch_bounds__(192, 1) k_attn_tc(const AttnParams p) {
+__global__ void __launch_bounds__(320, 1) k_attn_tc(const AttnParams p) {
   using C = TcCfg<D>;
   extern __shared__ __align__(128) uint8_t sm_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
@@ -430,10 +433,16 @@ __global__ void __launch_bounds__(192, 1) k_attn_tc(const AttnParams p) {
   uint64_t* mdone = q_full + 1;             // every issued MMA complete
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mdone + 1);
   int* pids = reinterpret_cast<int*>(sm + C::OFF_PIDS);
+  // xch[tag & 1][half][row] = (tag << 32) | float bits: the half-row value a
+  // softmax thread publishes for its partner (tag = page index; n for the
+  // final sum).  A thread cannot get two tags ahead of its partner (each
+  // trade waits for the partner's same tag), so two parity slots suffice.
+  volatile unsigned long long* xch = reinterpret_cast<volatile unsigned long long*>(sm + C::OFF_X);
 
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rows = G * 16;
+  for (int i = threadIdx.x; i < 512; i += blockDim.x) xch[i] = 0xFFFFFFFF00000000ull;  // no tag yet
   const int hq = p.hq, hkv = p.hkv;
   const uint32_t idesc_s = idesc_f16_f32(128, 64, 0);
   const uint32_t idesc_o = idesc_f16_f32(128, D, 0);
@@ -446,12 +455,12 @@ __global__ void __launch_bounds__(192, 1) k_attn_tc(const AttnParams p) {
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(s_full + i, 1);
-      mbar_init(s_empty + i, 128);
-      mbar_init(p_full + i, 128);
+      mbar_init(s_empty + i, 256);
+      mbar_init(p_full + i, 256);
       mbar_init(o_full + i, 1);
-      mbar_init(o_empty + i, 128);
+      mbar_init(o_empty + i, 256);
     }
-    mbar_init(q_full, 128);
+    mbar_init(q_full, 256);
     mbar_init(mdone, 1);
     fence_mbar_init();
   }
@@ -479,26 +488,32 @@ __global__ void __launch_bounds__(192, 1) k_attn_tc(const AttnParams p) {
   if (threadIdx.x == 0) atrace(p, 1);
   bool aborted = false;
 
-  // running state of this thread's query row (softmax warps)
-  float o[D];
-  float m_run = -INFINITY, l_run = 0.f;
+  // running state of this thread's half of a query row (softmax warps)
+  constexpr int DH = D / 2;  // output columns per thread
+  float o[DH];
+  float m_run = -INFINITY, l_run = 0.f;  // l_run: this half's keys only
 #pragma unroll
-  for (int d = 0; d < D; ++d) o[d] = 0.f;
+  for (int d = 0; d < DH; ++d) o[d] = 0.f;
   const int q4 = warp & 3;
-  const int r = q4 * 32 + lane;  // TMEM lane = query row (softmax warps)
+  const int r = q4 * 32 + lane;        // TMEM lane = query row (softmax warps)
+  const int kh = warp >= 6 ? 1 : 0;    // key / output-column half
 
   if (warp == 0) {
     // ------------------------------------------------ page loads
     if (lane == 0) {
       const f16* kbase = p.kv.k_pool + (size_t)p.layer * p.kv.layer_stride;
       const f16* vbase = p.kv.v_pool + (size_t)p.layer * p.kv.layer_stride;
+      auto page_of_idx = [&](int i) {
+        const int page_idx = pb + i;
+        int pg = i < C::MAX_PIDS ? pids[i] : (page_idx < p.kv.max_pages_per_slot ? pt[page_idx] : -1);
+        return (pg < 0 || pg >= p.kv.max_pages) ? -1 : pg;
+      };
       int i = 0;
       for (; i < n; ++i) {
         const int s = i % C::STAGES;
         if (i >= C::STAGES && !mbar_wait(empty + s, (uint32_t)((i / C::STAGES - 1) & 1), p.status, &aborted)) break;
-        const int page_idx = pb + i;
-        int pg = i < C::MAX_PIDS ? pids[i] : (page_idx < p.kv.max_pages_per_slot ? pt[page_idx] : -1);
-        if (pg < 0 || pg >= p.kv.max_pages) {
+        int pg = page_of_idx(i);
+        if (pg < 0) {
           dev_error(p.status, DFLASH_DEV_PAGE);
           pg = 0;
         }
@@ -558,12 +573,32 @@ __global__ void __launch_bounds__(192, 1) k_attn_tc(const AttnParams p) {
       mbar_wait(mdone, 0, p.status, &drain_abort);
     }
   } else {
-    // ------------------------------------------------ softmax (thread = query row r)
-    {  // this row's query, zero-padded to 128 rows, into the swizzled Q tile
+    // ------------------------------------------------ softmax (threads kh=0,1 of query row r)
+    // trade a half-row value with the partner thread: publish ours under
+    // `tag`, spin (bounded) until the partner's carries the same tag
+    auto trade = [&](float mine, uint32_t tag, float* theirs) {
+      const int slot0 = (int)(tag & 1u) * 256;
+      xch[slot0 + kh * 128 + r] = ((unsigned long long)tag << 32) | __float_as_uint(mine);
+      const uint64_t t0 = globaltimer();
+      for (;;) {
+        const unsigned long long v = xch[slot0 + (1 - kh) * 128 + r];
+        if ((uint32_t)(v >> 32) == tag) {
+          *theirs = __uint_as_float((uint32_t)v);
+          return true;
+        }
+        if (globaltimer() - t0 > DFL_WAIT_NS) {
+          dev_error(p.status, DFLASH_DEV_TIMEOUT);
+          aborted = true;
+          return false;
+        }
+      }
+    };
+    {  // this row's query (half of its chunks per thread), zero-padded to 128 rows
       const int h = r >> 4, t = r & 15;
       const f16* src = p.q + ((size_t)(b * DFL_BLOCK + t) * hq + kvh * G + h) * D;
 #pragma unroll
-      for (int c = 0; c < D / 8; ++c) {
+      for (int cc = 0; cc < D / 16; ++cc) {
+        const int c = kh * (D / 16) + cc;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (r < rows) v = *reinterpret_cast<const uint4*>(src + c * 8);
         uint8_t* dst = sm + C::OFF_Q + (c >> 3) * 16384 + r * 128 + (((c & 7) ^ (r & 7)) << 4);
@@ -580,9 +615,9 @@ __global__ void __launch_bounds__(192, 1) k_attn_tc(const AttnParams p) {
       if (!mbar_wait(o_full + bb, (uint32_t)((i / 2) & 1), p.status, &aborted)) return false;
       tc_fence_after();
 #pragma unroll
-      for (int j = 0; j < D / 16; ++j) {
+      for (int j = 0; j < DH / 16; ++j) {
         float v[16];
-        tmem_ld16(lane_base + (uint32_t)(C::O_COL + D * bb + 16 * j), v);
+        tmem_ld16(lane_base + (uint32_t)(C::O_COL + D * bb + kh * DH + 16 * j), v);
 #pragma unroll
         for (int e = 0; e < 16; ++e) o[16 * j + e] = o[16 * j + e] * alpha + v[e];
       }
@@ -597,36 +632,39 @@ __global__ void __launch_bounds__(192, 1) k_attn_tc(const AttnParams p) {
       if (!mbar_wait(s_full + bb, (uint32_t)((i / 2) & 1), p.status, &aborted)) break;
       if (i == 0 && threadIdx.x == 64) atrace(p, 2);
       tc_fence_after();
-      float sc[64];
+      float sc[32];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) tmem_ld16(lane_base + (uint32_t)(C::S_COL + 64 * bb + 16 * j), sc + 16 * j);
+      for (int j = 0; j < 2; ++j)
+        tmem_ld16(lane_base + (uint32_t)(C::S_COL + 64 * bb + 32 * kh + 16 * j), sc + 16 * j);
       tc_fence_before();
       mbar_arrive(s_empty + bb);
-      const int valid = min(64, nkeys - (pb + i) * 64);
+      const int valid = min(64, nkeys - (pb + i) * 64) - 32 * kh;  // this half's unmasked keys
       float mx = -INFINITY;
 #pragma unroll
-      for (int k = 0; k < 64; ++k) {
+      for (int k = 0; k < 32; ++k) {
         sc[k] = k < valid ? sc[k] * p.scale_log2 : -INFINITY;
         mx = fmaxf(mx, sc[k]);
       }
-      const float mn = fmaxf(m_run, mx);
+      float mx_other;
+      if (!trade(mx, (uint32_t)i, &mx_other)) break;
+      const float mn = fmaxf(m_run, fmaxf(mx, mx_other));
       const float ref = mn == -INFINITY ? 0.f : mn;  // a row with only masked keys so far adds 0
       const float alpha = exp2f(m_run - ref);
       float rs = 0.f;
-      uint32_t pk[32];
+      uint32_t pk[16];
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {
+      for (int k = 0; k < 16; ++k) {
         const float a = exp2f(sc[2 * k] - ref), c = exp2f(sc[2 * k + 1] - ref);
         rs += a + c;
         pk[k] = pack_f16x2(a, c);
       }
       l_run = l_run * alpha + rs;
       m_run = mn;
-      {  // P row r: 64 keys = 8 chunks of 16 bytes, swizzled like the K page rows
+      {  // this half of P row r: 32 keys = 4 chunks of 16 bytes, swizzled like the K page rows
         uint8_t* prow = sm + C::OFF_P + bb * C::PB + r * 128;
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<uint4*>(prow + (((c ^ (r & 7))) << 4)) =
+        for (int c = 0; c < 4; ++c)
+          *reinterpret_cast<uint4*>(prow + ((((4 * kh + c) ^ (r & 7))) << 4)) =
               make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
       }
       fence_proxy_async_smem();
@@ -636,6 +674,9 @@ __global__ void __launch_bounds__(192, 1) k_attn_tc(const AttnParams p) {
       alpha_prev = alpha;
     }
     if (ok && n > 0 && !aborted) fold(n - 1, alpha_prev);
+    // the row's sum over both halves
+    float l_other = 0.f;
+    if (!aborted && trade(l_run, (uint32_t)n, &l_other)) l_run += l_other;
   }
   if (threadIdx.x == 0) atrace(p, 3);
   tc_fence_before();
@@ -650,9 +691,9 @@ __global__ void __launch_bounds__(192, 1) k_attn_tc(const AttnParams p) {
   if (p.n_splits == 1) {
     if (row_out) {
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      f16* dst = p.out + ((size_t)(b * DFL_BLOCK + t) * hq + kvh * G + h) * D;
+      f16* dst = p.out + ((size_t)(b * DFL_BLOCK + t) * hq + kvh * G + h) * D + kh * DH;
 #pragma unroll
-      for (int c = 0; c < D / 8; ++c)
+      for (int c = 0; c < DH / 8; ++c)
         *reinterpret_cast<uint4*>(dst + c * 8) =
             make_uint4(pack_f16x2(o[8 * c] * inv, o[8 * c + 1] * inv), pack_f16x2(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
                        pack_f16x2(o[8 * c + 4] * inv, o[8 * c + 5] * inv), pack_f16x2(o[8 * c + 6] * inv, o[8 * c + 7] * inv));
@@ -667,10 +708,13 @@ __global__ void __launch_bounds__(192, 1) k_attn_tc(const AttnParams p) {
   float* part = reinterpret_cast<float*>(sm);
   if (row_out) {
 #pragma unroll
-    for (int c = 0; c < D / 4; ++c)
-      *reinterpret_cast<float4*>(part + r * PS + 4 * c) = make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
-    part[rows * PS + r] = m_run;
-    part[rows * PS + rows + r] = l_run;
+    for (int c = 0; c < DH / 4; ++c)
+      *reinterpret_cast<float4*>(part + r * PS + kh * DH + 4 * c) =
+          make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+    if (kh == 0) {
+      part[rows * PS + r] = m_run;
+      part[rows * PS + rows + r] = l_run;
+    }
   }
   if (threadIdx.x == 0) atrace(p, 4);
   cluster_sync_all();
@@ -741,7 +785,7 @@ struct AttnKernel;
 template <int D, int G>
 struct AttnKernel<D, G, true> {
   static constexpr auto fn = k_attn_tc<D, G>;
-  static constexpr int threads = 192;
+  static constexpr int threads = 320;
   static constexpr int smem = TcCfg<D>::SMEM;
 };
 template <int D, int G>
