@@ -221,14 +221,17 @@ def lm_head_logits(model: OracleModel, h: np.ndarray, chunk: int = 1 << 14) -> n
 def accept_longest_prefix(draft: np.ndarray, target: np.ndarray):
     """a7: accept the longest matching prefix, then the bonus token.
 
-    draft [15]: d_1..d_15 (block positions 1..15); target [16]: t_0..t_15,
+    draft [S-1]: d_1..d_{S-1} (block positions 1..S-1); target [S]: t_0..t_{S-1},
     the target's own token after each block position.  d_{i+1} is accepted
     while it equals t_i, found with a cumulative product of the per-position
     matches ([Code walkthrough] §三 第3步); the first mismatch is replaced by
-    the target's token (the bonus).  Worst case 1 token, best case 16.
+    the target's token (the bonus).  Worst case 1 token, best case S (16 at
+    the trained block size; a smaller S at inference, [Paper walkthrough]
+    Results: a large training block generalises to smaller inference blocks).
     Returns (tau, bonus) with tau = accepted drafts + 1.
     """
-    match = (np.asarray(draft[:15]) == np.asarray(target[:15])).astype(np.int64)
+    nd = len(draft)
+    match = (np.asarray(draft[:nd]) == np.asarray(target[:nd])).astype(np.int64)
     n = int(np.cumprod(match).sum())
     return n + 1, int(target[n])
 
@@ -237,18 +240,20 @@ def synthetic_target(draft: np.ndarray, m: np.ndarray, u: np.ndarray, vocab: int
     """Stand-in for the target model's verify step (benchmark harness, not the method).
 
     t_i = d_{i+1} if m_i else a uniform id different from d_{i+1} (u_i, bumped
-    to (u_i+1) mod vocab on a collision), for i < 15; t_15 = u_15.  The
-    accepted length then depends only on m, never on the draft values.
+    to (u_i+1) mod vocab on a collision), for i < S-1; t_{S-1} = u_{S-1}, with
+    S-1 = len(draft).  The accepted length then depends only on m, never on
+    the draft values.
     """
-    t = np.empty(16, dtype=np.int64)
-    for i in range(15):
+    nd = len(draft)
+    t = np.empty(nd + 1, dtype=np.int64)
+    for i in range(nd):
         d = int(draft[i])
         if m[i]:
             t[i] = d
         else:
             x = int(u[i])
             t[i] = (x + 1) % vocab if x == d else x
-    t[15] = int(u[15])
+    t[nd] = int(u[nd])
     return t
 
 
@@ -288,10 +293,11 @@ class OracleDrafter:
         req.ctx_len += n
 
     def draft(self, req: OracleRequest, last_tok: int, want_logits: bool = True):
-        """a3-a6: one forward over [last_tok, mask x 15]; returns a dict.
+        """a3-a6: one forward over [last_tok, mask x (S-1)]; returns a dict.
 
-        Block = last verified token followed by 15 mask ids ([Code walkthrough]
-        §二.1, block size 16 = 1 known + 15 masks -> 15 candidates).
+        Block = last verified token followed by S-1 mask ids ([Code walkthrough]
+        §二.1, block size 16 = 1 known + 15 masks -> 15 candidates; S = cfg.block,
+        smaller at inference per [Paper walkthrough] Results).
         """
         cfg = self.cfg
         S = cfg.block

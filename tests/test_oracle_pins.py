@@ -44,7 +44,7 @@ def test_bf16_rounding_nearest_even():
 def _brute_accept(draft, target):
     """Scan from the block head until the first mismatch (no cumprod)."""
     i = 0
-    while i < 15 and draft[i] == target[i]:
+    while i < len(draft) and draft[i] == target[i]:
         i += 1
     return i + 1, target[i]
 
@@ -76,6 +76,22 @@ def test_accept_exhaustive_all_masks():
         tau, bonus = O.accept_longest_prefix(base, target)
         assert (tau, bonus) == _brute_accept(base, target)
         assert 1 <= tau <= 16
+
+
+@pytest.mark.parametrize("S", [2, 8, 10])
+def test_accept_exhaustive_smaller_blocks(S):
+    """Inference at a smaller block S ([Paper walkthrough] Results): all 2^(S-1)
+    match patterns against the first-mismatch scan, tau in [1, S], and the
+    stand-in target has S tokens."""
+    base = np.arange(100, 100 + S - 1)
+    for bits in range(1 << (S - 1)):
+        mism = np.array([(bits >> i) & 1 for i in range(S - 1)], dtype=bool)
+        target = np.concatenate([np.where(mism, base + 1000, base), [7]])
+        tau, bonus = O.accept_longest_prefix(base, target)
+        assert (tau, bonus) == _brute_accept(base, target)
+        assert 1 <= tau <= S
+    t = O.synthetic_target(base, np.ones(S, bool), np.zeros(S, np.int64), 4096)
+    assert t.shape == (S,) and O.accept_longest_prefix(base, t)[0] == S
 
 
 def test_accept_mean_closed_form():
