@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=25.0)
+    ap.add_argument("--block", type=int, default=None,
+                    help="inference block size S in [2, 16] (default: the workload's, 16): S-1 drafts per round")
     ap.add_argument("--fold-inject", action="store_true",
                     help="issue dflash_draft_round instead of dflash_fuse_inject + dflash_draft_block")
     return ap.parse_args()
@@ -171,7 +173,7 @@ def oracle_round_seconds(cfg, budget_s: float, max_rounds: int):
     model = O.OracleModel(cfg, w, cache=False)
     dr = O.OracleDrafter(model)
     L0 = int(cfg.ctx0 or cfg.ctx_range[0])
-    req = O.OracleRequest(cfg, L0 + 16 * (max_rounds + 2))
+    req = O.OracleRequest(cfg, L0 + cfg.block * (max_rounds + 2))
     dr.fuse_inject(req, feature_rows(cfg, 0, 0, L0))
     last, pending = cfg.first_token, 0
     times, taus = [], []
@@ -204,6 +206,9 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device(f"cuda:{local_rank}")
     cfg = get_config(args.config)
+    if args.block:
+        cfg = cfg.with_(block=args.block)
+    S = cfg.block                                        # S-1 drafts per request per round
     B = cfg.batch
     ctx = context_lengths(cfg).astype(int)               # prompt length per request
     R = args.rounds_per_slot or cfg.rounds
@@ -231,7 +236,7 @@ def run_gpu(args, rank, world, local_rank):
             g.manual_seed(1_000_003 * (cfg.seed + 1) + b)
             feat_stream[b].normal_(generator=g)
         feat_src = "device generator (torch.normal_, seeded per request)"
-    m = np.empty((max(R, W), B, 16), dtype=np.int32)
+    m = np.empty((max(R, W), B, S), dtype=np.int32)
     u = np.empty_like(m)
     for r in range(max(R, W)):
         m[r], u[r] = match_stream(cfg, r, list(range(B)))
@@ -239,7 +244,7 @@ def run_gpu(args, rank, world, local_rank):
 
     chunk = 2048
     d = Drafter(cfg, w_dev, max_batch=B, max_slots=n_slots, max_pages=mpps * n_slots,
-                max_pages_per_slot=mpps, max_rows=max(chunk, 16 * B), device=local_rank)
+                max_pages_per_slot=mpps, max_rows=max(chunk, S * B), device=local_rank)
     stream = torch.cuda.Stream(device=dev)
 
     def prefill(g):
@@ -347,29 +352,29 @@ def run_gpu(args, rank, world, local_rank):
             d.reset_slot(gi * B + b, stream)
         prefill(gi)
         st = RoundState(d, B, slots=[gi * B + b for b in range(B)], first_token=cfg.first_token)
-        m_dev = torch.zeros(1, B, 16, dtype=torch.int32, device=dev)
+        m_dev = torch.zeros(1, B, S, dtype=torch.int32, device=dev)
         u_dev = torch.zeros_like(m_dev)
         ver = SyntheticVerify(st, m_dev, u_dev, None)
         d.graph_begin(stream)
         run_round(st, ver, stream, folded=args.fold_inject)
         d.graph_end(stream)
-        feats_h = torch.empty(B, 16, F, dtype=torch.bfloat16).pin_memory()
-        mu_h = torch.empty(2, B, 16, dtype=torch.int32).pin_memory()
-        out_h = torch.empty(B, 15 + 3, dtype=torch.int32).pin_memory()
+        feats_h = torch.empty(B, S, F, dtype=torch.bfloat16).pin_memory()
+        mu_h = torch.empty(2, B, S, dtype=torch.int32).pin_memory()
+        out_h = torch.empty(B, S - 1 + 3, dtype=torch.int32).pin_memory()
         if fs is not None:
             fs_host = binding.bf16_host(fs)
         else:  # the device-drawn stream's first rows stand in on the host
-            fs_host = feat_stream[:, :16].cpu()
+            fs_host = feat_stream[:, :S].cpu()
         stream.synchronize()
         # the round's inject consumes the previous round's block features
-        # (positions prev_L .. prev_L+15 of each request, the first accept_len)
+        # (positions prev_L .. prev_L+S-1 of each request, the first accept_len)
         prev_L = ctx.copy()
         cur_L = ctx.copy()
         t0 = time.perf_counter()
         for r in range(E):
             for b in range(B):
                 if fs is not None:
-                    feats_h[b].copy_(fs_host[b, prev_L[b]:prev_L[b] + 16])
+                    feats_h[b].copy_(fs_host[b, prev_L[b]:prev_L[b] + S])
                 else:
                     feats_h[b].copy_(fs_host[b])
             mu_h[0].copy_(torch.from_numpy(m[r % len(m)]))
@@ -379,12 +384,12 @@ def run_gpu(args, rank, world, local_rank):
                 m_dev[0].copy_(mu_h[0], non_blocking=True)
                 u_dev[0].copy_(mu_h[1], non_blocking=True)
                 d.graph_launch(stream)
-                out_h[:, :15].copy_(st.draft, non_blocking=True)
-                out_h[:, 15].copy_(st.accept_len, non_blocking=True)
-                out_h[:, 16].copy_(st.bonus, non_blocking=True)
-                out_h[:, 17].copy_(st.ctx_len, non_blocking=True)
+                out_h[:, :S - 1].copy_(st.draft, non_blocking=True)
+                out_h[:, S - 1].copy_(st.accept_len, non_blocking=True)
+                out_h[:, S].copy_(st.bonus, non_blocking=True)
+                out_h[:, S + 1].copy_(st.ctx_len, non_blocking=True)
             stream.synchronize()
-            prev_L, cur_L = cur_L, out_h[:, 17].numpy().astype(int)
+            prev_L, cur_L = cur_L, out_h[:, S + 1].numpy().astype(int)
         h2d = feats_h.numel() * 2 + mu_h.numel() * 4
         d2h = out_h.numel() * 4
         t_e2e = time.perf_counter() - t0
@@ -392,7 +397,7 @@ def run_gpu(args, rank, world, local_rank):
             t = torch.tensor([t_e2e], dtype=torch.float64, device=dev)
             torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
             t_e2e = float(t.item())
-        e2e = {"value": round(15 * B * E * world / t_e2e, 1), "unit": "tok/s", "h2d_bytes_per_step": h2d,
+        e2e = {"value": round((S - 1) * B * E * world / t_e2e, 1), "unit": "tok/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": E,
                "round_us": round(t_e2e / E * 1e6, 1),
                "note": "includes the stand-in verify kernel"}
@@ -401,7 +406,7 @@ def run_gpu(args, rank, world, local_rank):
     hbm, _, peak_src = peaks()
     tf_burst, tf_sust = tensor_peaks()
     H, V, D = cfg.hidden, cfg.vocab, cfg.head_dim
-    M = 16 * B
+    M = S * B                                            # block rows the method computes
     lm_bytes = V * H * 2 + M * H * 2
     lm_flops = 2.0 * M * V * H
     lm_avg_ms = statistics.mean(lm_ms) if lm_ms else float("nan")
@@ -409,7 +414,7 @@ def run_gpu(args, rank, world, local_rank):
     round_ms = round_ms_incl - verify_ms  # the stand-in verify is not part of the round
     tau = accepted / (K * B)
     avg_ctx = float(ctx.mean()) + tau * (R / 2)
-    kv_bytes = B * cfg.n_layers * (avg_ctx + 16) * cfg.n_kv_heads * D * 2 * 2
+    kv_bytes = B * cfg.n_layers * (avg_ctx + S) * cfg.n_kv_heads * D * 2 * 2
     round_bytes = cfg.weight_bytes() + kv_bytes + B * tau * F * 2
     layer_params = cfg.qkv_rows * H + H * cfg.n_q_heads * D + 3 * cfg.intermediate * H
     inj_params = H * F + cfg.n_layers * 2 * cfg.n_kv_heads * D * H
@@ -429,7 +434,7 @@ def run_gpu(args, rank, world, local_rank):
     p_desc = f"match p {cfg.match_p}" if cfg.match_p is not None else f"match p U[{cfg.p_range[0]}, {cfg.p_range[1]}]"
     res = {
         "metric": METRIC,
-        "value": round(15 * B * world / (round_ms * 1e-3), 1),
+        "value": round((S - 1) * B * world / (round_ms * 1e-3), 1),
         "unit": "tok/s",
         "n_gpus": world,
         "steps": K,
@@ -449,7 +454,7 @@ def run_gpu(args, rank, world, local_rank):
                 "stand-in verify)",
         "config": {"workload": f"{cfg.name} drafter batch {B}: H{H}, {cfg.n_q_heads}q/{cfg.n_kv_heads}kv x"
                                f"{D}, I{cfg.intermediate}, {cfg.n_layers} layers, V{V}, fusion "
-                               f"{F}->{H}, {ctx_desc}, block 16, {p_desc}",
+                               f"{F}->{H}, {ctx_desc}, block {S}, {p_desc}",
                    "batch": B, "prompt_mean": float(ctx.mean()), "rounds_per_slot": R,
                    "round_call": "dflash_draft_round" if args.fold_inject
                    else "dflash_fuse_inject+dflash_draft_block", "slot_groups": n_groups - 1,
@@ -482,17 +487,19 @@ def main():
             return
         from workload import get_config
         cfg = get_config(args.config)
+        if args.block:
+            cfg = cfg.with_(block=args.block)
         budget = 150.0
         times, taus = oracle_round_seconds(cfg, budget, max(1, args.steps or 8))
         used = times[1:] if len(times) > 1 else times
         rs = statistics.mean(used)
-        val = 15 / rs
+        val = (cfg.block - 1) / rs
         line = {"impl": "reference", "metric": METRIC, "value": round(val, 3), "unit": "tok/s",
                 "n_gpus": args.gpus, "steps": len(used), "warmup": len(times) - len(used),
                 "ms_per_step": round(rs * 1e3, 1), "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                 "config": {"workload": f"{cfg.name} drafter, one request of batch {cfg.batch} at a time, "
-                                       f"prompt {cfg.ctx0 or cfg.ctx_range[0]}, block 16"},
+                                       f"prompt {cfg.ctx0 or cfg.ctx_range[0]}, block {cfg.block}"},
                 "cpu_baseline": {"value": round(val, 3), "unit": "tok/s", "cores": os.cpu_count(),
                                  "kind": "oracle",
                                  "sample": f"{len(times)} rounds of request 0 after an untimed "
@@ -510,7 +517,7 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         times, taus = oracle_round_seconds(cfg, args.cpu_budget_s, 4)
         rs = statistics.mean(times)
-        res["cpu_baseline"] = {"value": round(15 / rs, 3), "unit": "tok/s", "cores": os.cpu_count(),
+        res["cpu_baseline"] = {"value": round((cfg.block - 1) / rs, 3), "unit": "tok/s", "cores": os.cpu_count(),
                                "kind": "oracle",
                                "sample": f"{len(times)} round(s) of the same workload (request 0) after an "
                                          f"untimed {cfg.ctx0 or cfg.ctx_range[0]}-token prefill, float64 NumPy"}

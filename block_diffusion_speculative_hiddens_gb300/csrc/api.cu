@@ -112,6 +112,7 @@ struct dflash_handle {
   // workspace
   uint32_t* status;
   int *ctx_len, *pos0, *n_pages, *page_table, *free_stack, *free_top, *n_eff;
+  int* slots_ok;  // [max_batch] the call's slots, out-of-range ones replaced by 0 (read by GEMMs, attention)
   f16 *k_pool, *v_pool;
   long long layer_stride;
   float2* rope;
@@ -142,7 +143,9 @@ bool cfg_valid(const dflash_config* c) {
       c->n_layers <= 0 || c->vocab <= 0 || c->n_fused <= 0)
     return false;
   if (c->n_layers > DFL_MAX_LAYERS) return false;
-  if (c->block != DFL_BLOCK || c->page_size != DFL_PAGE) return false;
+  // block: the trained size is 16; inference may use a smaller block S (rows
+  // S..15 of a request are carried as padding and never become keys)
+  if (c->block < 2 || c->block > DFL_BLOCK || c->page_size != DFL_PAGE) return false;
   if (c->head_dim != 64 && c->head_dim != 128) return false;
   if (c->hidden % 128 || c->hidden > 8192) return false;
   if (c->intermediate % 64) return false;
@@ -203,6 +206,7 @@ size_t carve(dflash_handle* h, const dflash_config& c, char* base, int num_sms) 
   o->free_stack = w.take<int>(c.max_pages);
   o->free_top = w.take<int>(1);
   o->n_eff = w.take<int>(c.max_batch);
+  o->slots_ok = w.take<int>(c.max_batch);
   const size_t KBh = H / 64;
   o->embed_pk = w.take<f16>((size_t)ceil_div(c.vocab, 128) * KBh * DFL_WBLK_ELEMS);
   o->fc_pk = w.take<bf16>((size_t)(H / 128) * (c.n_fused * H / 64) * DFL_WBLK_ELEMS);
@@ -379,8 +383,8 @@ int draft_impl(dflash_handle* h, const int32_t* slots, int32_t batch, const int3
   const int R = fold ? batch * rows_per_req : 0;
   if (fold) {
     h->launches++;
-    rc = cuda_err(launch_page_alloc(slots, batch, n_new, rows_per_req, h->ctx_len, h->pos0, h->n_pages,
-                                    h->page_table, c.max_pages_per_slot, h->free_stack, h->free_top, h->n_eff,
+    rc = cuda_err(launch_page_alloc(slots, batch, h->cfg.block, n_new, rows_per_req, h->ctx_len, h->pos0, h->n_pages,
+                                    h->page_table, c.max_pages_per_slot, h->free_stack, h->free_top, h->n_eff, h->slots_ok,
                                     c.max_slots, h->status, s));
     if (rc) return rc;
     const int MX = M + R;
@@ -411,7 +415,10 @@ int draft_impl(dflash_handle* h, const int32_t* slots, int32_t batch, const int3
   bcx.rope = h->rope;
   bcx.D = D;
   bcx.max_pos = h->max_pos;
+  bcx.block = c.block;
   bcx.bctx = h->bctx;
+  bcx.slots_ok = h->slots_ok;
+  bcx.max_slots = c.max_slots;
   bcx.brope = h->brope;
   rc = cuda_err(launch_embed(slots, batch, last_tok, c.mask_id, c.vocab, h->embed_pk, h->in_norm[0], H, h->h,
                              h->hg, h->ss_a, h->keys, bcx, h->status, s));
@@ -427,7 +434,7 @@ int draft_impl(dflash_handle* h, const int32_t* slots, int32_t batch, const int3
       p.kn_gain[0] = h->k_norm[l];
       p.layer = l;
       p.kv = kv;
-      p.slots = slots;
+      p.slots = h->slots_ok;
       p.ctx_len = h->ctx_len;
       p.bctx = h->bctx;
       p.brope = h->brope;
@@ -453,12 +460,13 @@ int draft_impl(dflash_handle* h, const int32_t* slots, int32_t batch, const int3
       a.out = h->obuf;
       a.kv = kv;
       a.layer = l;
-      a.slots = slots;
+      a.slots = h->slots_ok;
       a.ctx_len = h->ctx_len;
       a.hq = hq;
       a.hkv = hkv;
       a.D = D;
       a.n_splits = h->attn_splits;
+      a.block = c.block;
       a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
       a.status = h->status;
       if (h->trace.kid == DFLASH_KID_ATTENTION && h->trace.buf &&
@@ -516,6 +524,7 @@ int draft_impl(dflash_handle* h, const int32_t* slots, int32_t batch, const int3
     p.keys = h->keys;
     p.logits = logits;
     p.draft = draft;
+    p.block = c.block;
     p.done_ctr = h->done_ctr;
     const void* a = h->embed_pk;
     rc = run_gemm(h, s, GM_ARGMAX, &a, 1, 0, ceil_div(c.vocab, 128), H, h->tm_hg, M, p, true, 0,
@@ -645,8 +654,8 @@ int dflash_fuse_inject(dflash_handle* h, const int32_t* slots, int32_t batch, co
   const dflash_config& c = h->cfg;
   const int H = c.hidden, D = c.head_dim, hkv = c.n_kv_heads;
   h->launches++;
-  int rc = cuda_err(launch_page_alloc(slots, batch, n_new, rows_per_req, h->ctx_len, h->pos0, h->n_pages,
-                                      h->page_table, c.max_pages_per_slot, h->free_stack, h->free_top, h->n_eff,
+  int rc = cuda_err(launch_page_alloc(slots, batch, h->cfg.block, n_new, rows_per_req, h->ctx_len, h->pos0, h->n_pages,
+                                      h->page_table, c.max_pages_per_slot, h->free_stack, h->free_top, h->n_eff, h->slots_ok,
                                       c.max_slots, h->status, s));
   if (rc || rows_per_req == 0) return rc;
   const int R = batch * rows_per_req;
@@ -675,7 +684,7 @@ int dflash_fuse_inject(dflash_handle* h, const int32_t* slots, int32_t batch, co
     p.N = 2 * hkv * D;
     for (int l = 0; l < c.n_layers; ++l) p.kn_gain[l] = h->k_norm[l];
     p.kv = kv_geom(h);
-    p.slots = slots;
+    p.slots = h->slots_ok;
     p.pos0 = h->pos0;
     p.n_eff = h->n_eff;
     p.rows_per_req = rows_per_req;
@@ -722,7 +731,7 @@ int dflash_accept_trim(dflash_handle* h, const int32_t* slots, int32_t batch, co
   if (!slots || !draft || !target || !accept_len || !bonus || !ctx_len) return DFLASH_ERR_INVALID_ARG;
   if (cudaSetDevice(h->cfg.device) != cudaSuccess) return DFLASH_ERR_CUDA;
   h->launches++;
-  return cuda_err(launch_accept(slots, batch, draft, target, accept_len, bonus, ctx_len, h->ctx_len,
+  return cuda_err(launch_accept(slots, batch, h->cfg.block, draft, target, accept_len, bonus, ctx_len, h->ctx_len,
                                 h->cfg.max_slots, h->status, (cudaStream_t)stream));
 }
 
@@ -890,7 +899,7 @@ int dflash_harness_verify(dflash_handle* h, const int32_t* slots, int32_t batch,
   if (feat_stream && (!feats_out || stream_rows <= 0)) return DFLASH_ERR_INVALID_ARG;
   if (cudaSetDevice(h->cfg.device) != cudaSuccess) return DFLASH_ERR_CUDA;
   h->launches++;
-  return cuda_err(launch_harness_verify(slots, batch, draft, match, offs, rounds_cap, round_ctr, target,
+  return cuda_err(launch_harness_verify(slots, batch, h->cfg.block, draft, match, offs, rounds_cap, round_ctr, target,
                                         h->cfg.vocab, static_cast<const bf16*>(feat_stream), stream_rows,
                                         static_cast<bf16*>(feats_out), h->cfg.n_fused * h->cfg.hidden,
                                         h->ctx_len, h->cfg.max_slots, (cudaStream_t)stream));
@@ -1007,8 +1016,8 @@ extern "C" int dflash_fuse_inject_noalloc(dflash_handle* h, const int32_t* slots
   rc = cuda_err(cudaMemsetAsync(ctr, 0, NA_CTR_BYTES, s));
   if (rc) return rc;
   h->launches++;
-  rc = cuda_err(launch_page_alloc(slots, batch, n_new, rows_per_req, h->ctx_len, h->pos0, h->n_pages,
-                                  h->page_table, c.max_pages_per_slot, h->free_stack, h->free_top, h->n_eff,
+  rc = cuda_err(launch_page_alloc(slots, batch, h->cfg.block, n_new, rows_per_req, h->ctx_len, h->pos0, h->n_pages,
+                                  h->page_table, c.max_pages_per_slot, h->free_stack, h->free_top, h->n_eff, h->slots_ok,
                                   c.max_slots, h->status, s));
   if (rc || rows_per_req == 0) return rc;
   const int R = batch * rows_per_req;
@@ -1033,7 +1042,7 @@ extern "C" int dflash_fuse_inject_noalloc(dflash_handle* h, const int32_t* slots
     p.N = 2 * hkv * D;
     for (int l = 0; l < c.n_layers; ++l) p.kn_gain[l] = h->k_norm[l];
     p.kv = kv_geom(h);
-    p.slots = slots;
+    p.slots = h->slots_ok;
     p.pos0 = h->pos0;
     p.n_eff = h->n_eff;
     p.rows_per_req = rows_per_req;

@@ -75,7 +75,7 @@ __global__ void __launch_bounds__(G * KS * 32) k_attn(const AttnParams p) {
   pdl_wait();
 
   const int slot = p.slots[b];
-  const int nkeys = p.ctx_len[slot] + DFL_BLOCK;
+  const int nkeys = p.ctx_len[slot] + p.block;  // context + live block rows (0..S-1)
   const int npages = (nkeys + 63) >> 6;
   const int pb = (int)((long long)split * npages / p.n_splits);  // balanced page ranges
   const int pe = (int)((long long)(split + 1) * npages / p.n_splits);
@@ -476,7 +476,7 @@ __global__ void __launch_bounds__(320, 1) k_attn_tc(const AttnParams p) {
   pdl_wait();
 
   const int slot = p.slots[b];
-  const int nkeys = p.ctx_len[slot] + DFL_BLOCK;
+  const int nkeys = p.ctx_len[slot] + p.block;  // context + live block rows (0..S-1)
   const int npages = (nkeys + 63) >> 6;
   const int pb = (int)((long long)split * npages / p.n_splits);  // balanced page ranges
   const int pe = (int)((long long)(split + 1) * npages / p.n_splits);

@@ -412,8 +412,8 @@ DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, con
             p.out[(size_t)tq[q] * (p.hq * D) + n0 + lane + 32 * jj] = to_f16(xv[jj], p.status);
           continue;
         }
-        if (pg[q] < 0) {
-          dev_error(p.status, DFLASH_DEV_PAGE);
+        if (pg[q] < 0) {  // -2: a padding row of a smaller block
+          if (pg[q] == -1) dev_error(p.status, DFLASH_DEV_PAGE);
           continue;
         }
         const int base = (kind == 1 ? p.hq : p.hq + p.hkv) * D;
@@ -781,7 +781,7 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
   }
   if (MODE == GM_ARGMAX) {
     // The last CTA to finish turns the per-token argmax keys of block rows
-    // 1..15 into draft ids and clears the keys for the next round.
+    // 1..S-1 into draft ids and clears the keys for the next round.
     int* done_flag = flag + 1;
     if (threadIdx.x == 0) {
       __threadfence();
@@ -792,8 +792,9 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
     if (*done_flag) {
       __threadfence();
       const int batch = p.M / DFL_BLOCK;
-      for (int idx = threadIdx.x; idx < batch * (DFL_BLOCK - 1); idx += blockDim.x) {
-        const int b = idx / (DFL_BLOCK - 1), i = idx % (DFL_BLOCK - 1) + 1;
+      const int nd = p.block - 1;  // drafts per request: block rows 1..S-1
+      for (int idx = threadIdx.x; idx < batch * nd; idx += blockDim.x) {
+        const int b = idx / nd, i = idx % nd + 1;
         const unsigned long long k = __ldcg(p.keys + b * DFL_BLOCK + i);
         p.draft[idx] = k ? (int)argmax_key_index(k) : 0;
       }

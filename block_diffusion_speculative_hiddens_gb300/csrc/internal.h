@@ -91,7 +91,8 @@ struct GemmParams {
   // argmax
   unsigned long long* keys;  // [M]
   float* logits;             // optional [M][N] (N = vocab)
-  int* draft;                // [batch][15]
+  int* draft;                // [batch][block-1]
+  int block;                 // ARGMAX: block size S (drafts from rows 1..S-1); 16 rows per request either way
   unsigned* done_ctr;
   // optional timeline: [grid][8] %globaltimer stamps per CTA (null: off)
   unsigned long long* trace;
@@ -107,9 +108,10 @@ struct AttnParams {
   KVGeom kv;
   int layer;
   const int* slots;
-  const int* ctx_len;  // keys = ctx_len + 16 (block K/V already in the cache)
+  const int* ctx_len;  // keys = ctx_len + block (block K/V already in the cache)
   int hq, hkv, D;
   int n_splits;        // CTAs per (request, KV head): one cluster, <= 16
+  int block;           // block size S: keys = context + S (rows S..15 of a request are padding)
   float scale_log2;    // log2(e) / sqrt(D)
   uint32_t* status;
   unsigned long long* trace;  // optional [grid][8] timeline (null: off)
@@ -141,17 +143,21 @@ struct BlockCtx {
   int max_pages_per_slot, max_pages;
   const float2* rope;
   int D, max_pos;
+  int block;  // block size S (rows S..15 of each request are padding)
+  int max_slots;
+  int* slots_ok;  // [batch] out: slots with out-of-range ones replaced by 0
   int2* bctx;
   float2* brope;
 };
 cudaError_t launch_embed(const int* slots, int batch, const int* last_tok, int mask_id, int vocab,
                          const f16* embed_pk, const float* gain, int H, float* h, f16* hg, float* ss,
                          unsigned long long* keys, const BlockCtx& bc, uint32_t* status, cudaStream_t s);
-cudaError_t launch_page_alloc(const int* slots, int batch, const int* n_new, int rows_per_req, int* ctx_len,
+cudaError_t launch_page_alloc(const int* slots, int batch, int S, const int* n_new, int rows_per_req, int* ctx_len,
                               int* pos0, int* n_pages, int* page_table, int max_pages_per_slot,
-                              int* free_stack, int* free_top, int* n_eff, int max_slots, uint32_t* status,
+                              int* free_stack, int* free_top, int* n_eff, int* slots_ok, int max_slots,
+                              uint32_t* status,
                               cudaStream_t s);
-cudaError_t launch_accept(const int* slots, int batch, const int* draft, const int* target, int* accept_len,
+cudaError_t launch_accept(const int* slots, int batch, int S, const int* draft, const int* target, int* accept_len,
                           int* bonus, int* ctx_out, int* ctx_len, int max_slots, uint32_t* status,
                           cudaStream_t s);
 cudaError_t launch_reset_slot(int slot, int* ctx_len, int* n_pages, int* page_table,
@@ -162,7 +168,7 @@ cudaError_t launch_read_kv(const KVGeom& kv, int layer, int slot, int pos0, int 
                            cudaStream_t s);
 cudaError_t launch_slot_lengths(const int* slots, int batch, const int* ctx_len, int max_slots, int* out,
                                 cudaStream_t s);
-cudaError_t launch_harness_verify(const int* slots, int batch, const int* draft, const int* match,
+cudaError_t launch_harness_verify(const int* slots, int batch, int S, const int* draft, const int* match,
                                   const int* offs, int rounds_cap, int* round_ctr, int* target, int vocab,
                                   const bf16* feat_stream, int stream_rows, bf16* feats_out, int F,
                                   const int* ctx_len, int max_slots, cudaStream_t s);

@@ -90,12 +90,25 @@ __global__ void k_embed(const int* __restrict__ slots, const int* __restrict__ l
   if (threadIdx.x == 0) keys[t] = 0ull;
   // this token's position (block rows follow the slot's context), page and
   // RoPE row, for every layer's QKV epilogue
-  const int slot = slots[b];
-  const int pos = bc.ctx_len[slot] + i;
+  // rows block..15 of a request pad a smaller block: page -2 (computed like
+  // any row, at a position clamped into the table, but never written to the
+  // cache, so they never become keys).  A request with an out-of-range slot
+  // is reported, read from slot 0 and written nowhere (all rows padding).
+  const int slot_in = slots[b];
+  const bool bad_slot = slot_in < 0 || slot_in >= bc.max_slots;
+  const int slot = bad_slot ? 0 : slot_in;
+  if (i == 0 && threadIdx.x == 0) {
+    bc.slots_ok[b] = slot;
+    if (bad_slot) dev_error(status, DFLASH_DEV_ARG);
+  }
+  const bool pad = i >= bc.block || bad_slot;
+  const int pos = pad ? min(bc.ctx_len[slot] + i, bc.max_pos - 1) : bc.ctx_len[slot] + i;
   const bool in_range = pos < bc.max_pos;
   if (threadIdx.x == 0) {
     int pg = -1;
-    if (!in_range) {
+    if (pad) {
+      pg = -2;
+    } else if (!in_range) {
       dev_error(status, DFLASH_DEV_CAPACITY);
     } else if ((pos >> 6) < bc.max_pages_per_slot) {
       pg = bc.page_table[(size_t)slot * bc.max_pages_per_slot + (pos >> 6)];
@@ -111,9 +124,9 @@ __global__ void k_embed(const int* __restrict__ slots, const int* __restrict__ l
 // the page assignment is deterministic).  Grows each slot's page table to
 // cover ctx_len + n_new + block positions, records the first new position
 // (pos0) and the effective row count, and advances ctx_len.
-__global__ void k_page_alloc(const int* slots, int batch, const int* n_new, int rows_per_req, int* ctx_len,
+__global__ void k_page_alloc(const int* slots, int batch, int S, const int* n_new, int rows_per_req, int* ctx_len,
                              int* pos0, int* n_pages, int* page_table, int mpps, int* free_stack, int* free_top,
-                             int* n_eff, int max_slots, uint32_t* status) {
+                             int* n_eff, int* slots_ok, int max_slots, uint32_t* status) {
   pdl_launch_dependents();
   pdl_wait();
   if (threadIdx.x != 0) return;
@@ -123,19 +136,21 @@ __global__ void k_page_alloc(const int* slots, int batch, const int* n_new, int 
     if (slot < 0 || slot >= max_slots) {
       dev_error(status, DFLASH_DEV_ARG);
       n_eff[b] = 0;
+      slots_ok[b] = 0;  // in bounds for the later kernels; no row of it is live
       continue;
     }
+    slots_ok[b] = slot;
     int n = n_new[b];
     if (n < 0 || n > rows_per_req) {
       dev_error(status, DFLASH_DEV_ARG);
       n = 0;
     }
     const int L = ctx_len[slot];
-    int need = (L + n + DFL_BLOCK + DFL_PAGE - 1) / DFL_PAGE;
+    int need = (L + n + S + DFL_PAGE - 1) / DFL_PAGE;
     if (need > mpps) {
       dev_error(status, DFLASH_DEV_CAPACITY);
       n = 0;
-      need = min(mpps, (L + DFL_BLOCK + DFL_PAGE - 1) / DFL_PAGE);
+      need = min(mpps, (L + S + DFL_PAGE - 1) / DFL_PAGE);
     }
     int np = n_pages[slot];
     while (np < need) {
@@ -159,17 +174,16 @@ __global__ void k_page_alloc(const int* slots, int batch, const int* n_new, int 
 // the ballot's lowest zero bit is the first mismatch n, so the accepted
 // prefix is the cumulative product of the matches; tau = n + 1, the bonus is
 // t_n, and the confirmed length is ctx_len + tau.
-__global__ void k_accept(const int* slots, int batch, const int* draft, const int* target, int* accept_len,
+__global__ void k_accept(const int* slots, int batch, int S, const int* draft, const int* target, int* accept_len,
                          int* bonus, int* ctx_out, const int* ctx_len, int max_slots, uint32_t* status) {
   pdl_launch_dependents();
   pdl_wait();
   const int b = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (b >= batch) return;
-  const bool match = lane < DFL_BLOCK - 1 &&
-                     draft[b * (DFL_BLOCK - 1) + lane] == target[b * DFL_BLOCK + lane];
+  const bool match = lane < S - 1 && draft[b * (S - 1) + lane] == target[b * S + lane];
   const unsigned m = __ballot_sync(0xffffffffu, match);
-  const int n = __ffs(~m) - 1;  // bits 15.. of m are 0, so n <= 15
+  const int n = __ffs(~m) - 1;  // bits S-1.. of m are 0, so n <= S-1
   if (lane == 0) {
     const int tau = n + 1;
     const int slot = slots[b];
@@ -179,7 +193,7 @@ __global__ void k_accept(const int* slots, int batch, const int* draft, const in
     else
       L = ctx_len[slot];
     accept_len[b] = tau;
-    bonus[b] = target[b * DFL_BLOCK + n];
+    bonus[b] = target[b * S + n];
     ctx_out[b] = L + tau;
   }
 }
@@ -247,8 +261,8 @@ __global__ void k_slot_lengths(const int* slots, int batch, const int* ctx_len, 
 
 // Benchmark stand-in for the target's verify (not part of the method).
 // Block 0 builds the target tokens of round (*round_ctr)++; blocks 1.. copy
-// the target features of the 16 block positions from a position-indexed stream.
-__global__ void k_harness_verify(const int* slots, int batch, const int* draft, const int* match, const int* offs,
+// the target features of the S block positions from a position-indexed stream.
+__global__ void k_harness_verify(const int* slots, int batch, int S, const int* draft, const int* match, const int* offs,
                                  int rounds_cap, int* round_ctr, int* target, int vocab,
                                  const bf16* feat_stream, int stream_rows, bf16* feats_out, int F,
                                  const int* ctx_len, int max_slots) {
@@ -257,13 +271,13 @@ __global__ void k_harness_verify(const int* slots, int batch, const int* draft, 
   if (blockIdx.x == 0) {
     const int r = *round_ctr;
     const int rr = r % rounds_cap;
-    for (int idx = threadIdx.x; idx < batch * DFL_BLOCK; idx += blockDim.x) {
-      const int b = idx / DFL_BLOCK, i = idx % DFL_BLOCK;
-      const size_t o = ((size_t)rr * batch + b) * DFL_BLOCK + i;
+    for (int idx = threadIdx.x; idx < batch * S; idx += blockDim.x) {
+      const int b = idx / S, i = idx % S;
+      const size_t o = ((size_t)rr * batch + b) * S + i;
       const int u = offs[o];
       int t;
-      if (i < DFL_BLOCK - 1) {
-        const int d = draft[b * (DFL_BLOCK - 1) + i];
+      if (i < S - 1) {
+        const int d = draft[b * (S - 1) + i];
         t = match[o] ? d : (u == d ? (u + 1) % vocab : u);
       } else {
         t = u;
@@ -275,7 +289,7 @@ __global__ void k_harness_verify(const int* slots, int batch, const int* draft, 
     return;
   }
   const int row = blockIdx.x - 1;
-  const int b = row / DFL_BLOCK, i = row % DFL_BLOCK;
+  const int b = row / S, i = row % S;
   const int slot = slots[b];
   if (slot < 0 || slot >= max_slots) return;
   int pos = ctx_len[slot] + i;
@@ -313,21 +327,21 @@ cudaError_t launch_embed(const int* slots, int batch, const int* last_tok, int m
                             status);
 }
 
-cudaError_t launch_page_alloc(const int* slots, int batch, const int* n_new, int rows_per_req, int* ctx_len,
+cudaError_t launch_page_alloc(const int* slots, int batch, int S, const int* n_new, int rows_per_req, int* ctx_len,
                               int* pos0, int* n_pages, int* page_table, int mpps, int* free_stack, int* free_top,
-                              int* n_eff, int max_slots, uint32_t* status, cudaStream_t s) {
+                              int* n_eff, int* slots_ok, int max_slots, uint32_t* status, cudaStream_t s) {
   cudaLaunchAttribute a[1];
   cudaLaunchConfig_t c = cfg_of(dim3(1), dim3(32), s, a);
-  return cudaLaunchKernelEx(&c, k_page_alloc, slots, batch, n_new, rows_per_req, ctx_len, pos0, n_pages,
-                            page_table, mpps, free_stack, free_top, n_eff, max_slots, status);
+  return cudaLaunchKernelEx(&c, k_page_alloc, slots, batch, S, n_new, rows_per_req, ctx_len, pos0, n_pages,
+                            page_table, mpps, free_stack, free_top, n_eff, slots_ok, max_slots, status);
 }
 
-cudaError_t launch_accept(const int* slots, int batch, const int* draft, const int* target, int* accept_len,
+cudaError_t launch_accept(const int* slots, int batch, int S, const int* draft, const int* target, int* accept_len,
                           int* bonus, int* ctx_out, int* ctx_len, int max_slots, uint32_t* status,
                           cudaStream_t s) {
   cudaLaunchAttribute a[1];
   cudaLaunchConfig_t c = cfg_of(dim3((batch + 3) / 4), dim3(128), s, a);
-  return cudaLaunchKernelEx(&c, k_accept, slots, batch, draft, target, accept_len, bonus, ctx_out,
+  return cudaLaunchKernelEx(&c, k_accept, slots, batch, S, draft, target, accept_len, bonus, ctx_out,
                             (const int*)ctx_len, max_slots, status);
 }
 
@@ -363,13 +377,13 @@ cudaError_t launch_slot_lengths(const int* slots, int batch, const int* ctx_len,
   return cudaGetLastError();
 }
 
-cudaError_t launch_harness_verify(const int* slots, int batch, const int* draft, const int* match, const int* offs,
-                                  int rounds_cap, int* round_ctr, int* target, int vocab, const bf16* feat_stream,
-                                  int stream_rows, bf16* feats_out, int F, const int* ctx_len, int max_slots,
-                                  cudaStream_t s) {
+cudaError_t launch_harness_verify(const int* slots, int batch, int S, const int* draft, const int* match,
+                                  const int* offs, int rounds_cap, int* round_ctr, int* target, int vocab,
+                                  const bf16* feat_stream, int stream_rows, bf16* feats_out, int F, const int* ctx_len,
+                                  int max_slots, cudaStream_t s) {
   cudaLaunchAttribute a[1];
-  const int blocks = 1 + (feat_stream ? batch * DFL_BLOCK : 0);
+  const int blocks = 1 + (feat_stream ? batch * S : 0);
   cudaLaunchConfig_t c = cfg_of(dim3(blocks), dim3(256), s, a);
-  return cudaLaunchKernelEx(&c, k_harness_verify, slots, batch, draft, match, offs, rounds_cap, round_ctr, target,
+  return cudaLaunchKernelEx(&c, k_harness_verify, slots, batch, S, draft, match, offs, rounds_cap, round_ctr, target,
                             vocab, feat_stream, stream_rows, feats_out, F, ctx_len, max_slots);
 }

@@ -53,7 +53,7 @@ class RoundState:
 class SyntheticVerify:
     """Benchmark stand-in for the target's verify step (see dflash_harness_verify).
 
-    match/offs: int32 [rounds, batch, 16] device tensors drawn by the workload
+    match/offs: int32 [rounds, batch, block] device tensors drawn by the workload
     generator; feat_stream: [batch, rows, n_fused*H] bf16 device tensor of the
     target features of every position (or None to leave state.feats alone).
     """

@@ -6,8 +6,9 @@
  *   dflash_fuse_inject  fuse the hidden states of 5 target layers into one
  *                       context feature per new position and inject it into
  *                       every draft layer's paged KV cache;
- *   dflash_draft_block  one forward of the draft transformer over a 16-token
- *                       block [last verified token, 15 x mask] -> 15 drafts;
+ *   dflash_draft_block  one forward of the draft transformer over a block of
+ *                       S tokens [last verified token, (S-1) x mask] -> S-1
+ *                       drafts (S = 16, the trained block, or smaller);
  *   dflash_accept_trim  given the target's own token per block position,
  *                       accept the longest matching prefix plus the bonus
  *                       token and trim the caches to the confirmed length.
@@ -58,14 +59,15 @@ typedef enum {
 #define DFLASH_DEV_NAN       0x02u /* a NaN logit was skipped by the argmax */
 #define DFLASH_DEV_PAGE      0x04u /* a page-table entry was out of range */
 #define DFLASH_DEV_CAPACITY  0x08u /* page pool or per-slot page table full */
-#define DFLASH_DEV_ARG       0x10u /* slot id or n_new out of range */
+#define DFLASH_DEV_ARG       0x10u /* slot id or n_new out of range (the request is skipped: no
+                                       cache entry written; its outputs are unspecified) */
 #define DFLASH_DEV_RANGE     0x20u /* an f16 activation or cache entry exceeded 65504 (saturated) */
 
 /* Drafter shape and serving limits.
  * Supported: head_dim in {64,128}; hidden, n_fused*hidden, intermediate and
  * n_q_heads*head_dim multiples of 64; n_kv_heads*head_dim a multiple of 128;
  * hidden a multiple of 128 and <= 8192; n_q_heads a multiple of n_kv_heads
- * with n_q_heads/n_kv_heads <= 8; block == 16; page_size == 64; n_layers <= 8. */
+ * with n_q_heads/n_kv_heads <= 8; 2 <= block <= 16; page_size == 64; n_layers <= 8. */
 typedef struct dflash_config {
   int32_t hidden;             /* H */
   int32_t n_q_heads;          /* hq */
@@ -75,7 +77,11 @@ typedef struct dflash_config {
   int32_t n_layers;           /* draft layers */
   int32_t vocab;              /* V (tied embedding / lm_head rows) */
   int32_t n_fused;            /* target layers fused (5) */
-  int32_t block;              /* block size (16): 1 verified token + 15 masks */
+  int32_t block;              /* block size S: 1 verified token + S-1 masks.  16 is the
+                                 trained size; a smaller S at inference ("DFlash：drafter
+                                 的答案…", Results: a large training block generalises to
+                                 smaller inference blocks) drafts S-1 tokens with the same
+                                 kernels, rows S..15 of each request carried as padding */
   int32_t mask_id;            /* token id of the mask */
   int32_t page_size;          /* positions per KV page (64) */
   int32_t max_batch;          /* max requests per call */
@@ -147,12 +153,12 @@ DFLASH_API int dflash_destroy(dflash_handle* h);
 DFLASH_API int dflash_fuse_inject(dflash_handle* h, const int32_t* slots, int32_t batch, const void* feats,
                        int32_t rows_per_req, const int32_t* n_new, void* stream);
 
-/* a3-a6.  Embed the block [last_tok[b], mask x 15] at positions
- * ctx_len .. ctx_len+15, run every draft layer once with non-causal
+/* a3-a6.  Embed the block [last_tok[b], mask x (S-1)] at positions
+ * ctx_len .. ctx_len+S-1, run every draft layer once with non-causal
  * attention over [context KV ; block KV] ("DFlash原理深度剖析…", §二.1, §二.2),
  * apply the final RMSNorm and the tied lm_head, and write the argmax of
- * block rows 1..15 (ties -> lowest id; logits are never stored).
- *   last_tok DEVICE int32 [batch]; draft DEVICE int32 [batch, 15] (out). */
+ * block rows 1..S-1 (ties -> lowest id; logits are never stored).
+ *   last_tok DEVICE int32 [batch]; draft DEVICE int32 [batch, S-1] (out). */
 DFLASH_API int dflash_draft_block(dflash_handle* h, const int32_t* slots, int32_t batch,
                        const int32_t* last_tok, int32_t* draft, void* stream);
 
@@ -168,9 +174,9 @@ DFLASH_API int dflash_draft_round(dflash_handle* h, const int32_t* slots, int32_
                                   int32_t* draft, void* stream);
 
 /* a7.  Longest-prefix acceptance (cumulative product of matches,
- * "DFlash原理深度剖析…", §三 第3步).  draft [batch,15], target [batch,16] (the
+ * "DFlash原理深度剖析…", §三 第3步).  draft [batch,S-1], target [batch,S] (the
  * target's token after each block position).  Outputs (DEVICE int32 [batch]):
- *   accept_len = accepted drafts + 1, in [1, 16];
+ *   accept_len = accepted drafts + 1, in [1, S];
  *   bonus      = target[b][accept_len-1] (the next round's last verified token);
  *   ctx_len    = confirmed length = ctx_len_before_round + accept_len, the length
  *                both the draft and the target caches are trimmed to.
@@ -237,7 +243,8 @@ DFLASH_API int dflash_slot_lengths(dflash_handle* h, const int32_t* slots, int32
 /* dflash_draft_block that also writes, when non-null, the residual stream
  * after the last layer (hidden [batch,16,H] float32) and the full logits of
  * all 16 block rows (logits [batch,16,V] float32), from the same kernels and
- * the same accumulators the argmax reads. */
+ * the same accumulators the argmax reads.  With block S < 16, rows S..15 of
+ * each request are padding rows (finite, not part of the method). */
 DFLASH_API int dflash_draft_block_debug(dflash_handle* h, const int32_t* slots, int32_t batch,
                              const int32_t* last_tok, int32_t* draft, float* hidden,
                              float* logits, void* stream);
@@ -285,12 +292,12 @@ DFLASH_API uint64_t dflash_launch_count(dflash_handle* h);
 /* ---- benchmark harness: stand-in for the target's verify step -----------
  * Not part of the method.  For round r = (*round_ctr)++ it builds the
  * target tokens from the draft and caller-drawn random streams
- *   match [rounds_cap, batch, 16] int32 in {0,1}, offs [rounds_cap, batch, 16]
+ *   match [rounds_cap, batch, S] int32 in {0,1}, offs [rounds_cap, batch, S]
  *   int32 in [0, vocab):  t_i = d_{i+1} if match_i else offs_i (bumped to
- *   (offs_i+1) mod vocab if equal to d_{i+1}), t_15 = offs_15;
- * and, when feat_stream is non-null, copies the target features of the 16
- * block positions ctx_len .. ctx_len+15 from feat_stream
- * [batch, stream_rows, n_fused*H] into feats_out [batch, 16, n_fused*H]. */
+ *   (offs_i+1) mod vocab if equal to d_{i+1}), t_{S-1} = offs_{S-1};
+ * and, when feat_stream is non-null, copies the target features of the S
+ * block positions ctx_len .. ctx_len+S-1 from feat_stream
+ * [batch, stream_rows, n_fused*H] into feats_out [batch, S, n_fused*H]. */
 DFLASH_API int dflash_harness_verify(dflash_handle* h, const int32_t* slots, int32_t batch,
                           const int32_t* draft, const int32_t* match, const int32_t* offs,
                           int32_t rounds_cap, int32_t* round_ctr, int32_t* target,

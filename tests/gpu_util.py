@@ -90,13 +90,14 @@ class GpuRun:
             cfg = self.cfg
             B = s.batch
             s.inject()
-            hidden = torch.empty(B * cfg.block, cfg.hidden, dtype=torch.float32, device=self.dev)
-            logits = torch.empty(B * cfg.block, cfg.vocab, dtype=torch.float32, device=self.dev)
+            # the debug outputs always hold 16 rows per request (rows S..15 pad a smaller block)
+            hidden = torch.empty(B * 16, cfg.hidden, dtype=torch.float32, device=self.dev)
+            logits = torch.empty(B * 16, cfg.vocab, dtype=torch.float32, device=self.dev)
             self.d.draft_block_debug(s.slots, s.bonus, s.draft, hidden, logits)
             self.verify()
             s.accept()
-            out["hidden"] = to_np(hidden).reshape(B, cfg.block, cfg.hidden)
-            out["logits"] = to_np(logits).reshape(B, cfg.block, cfg.vocab)
+            out["hidden"] = to_np(hidden).reshape(B, 16, cfg.hidden)[:, :cfg.block]
+            out["logits"] = to_np(logits).reshape(B, 16, cfg.vocab)[:, :cfg.block]
         else:
             run_round(s, self.verify, folded=folded)
         torch.cuda.synchronize()

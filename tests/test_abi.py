@@ -46,7 +46,7 @@ def test_workspace_sizing_accepts_every_workload(lib, name):
     assert n > 0 and n % 256 == 0
 
 
-@pytest.mark.parametrize("bad", [dict(head_dim=96), dict(block=8), dict(page_size=32), dict(n_layers=9),
+@pytest.mark.parametrize("bad", [dict(head_dim=96), dict(block=1), dict(block=17), dict(page_size=32), dict(n_layers=9),
                                  dict(n_kv_heads=3), dict(max_batch=65), dict(mask_id=-1),
                                  dict(hidden=200), dict(rope_theta=0.5), dict(attn_impl=3)])
 def test_workspace_sizing_rejects_unsupported(lib, bad):

@@ -80,6 +80,53 @@ def test_rounds_accept_bit_exact(lib, name, rounds, folded, attn_impl):
     assert np.array_equal(lens + to_np(g.state.accept_len), [od["ctx"] for od in oo])
 
 
+# inference at blocks smaller than the trained 16: S-1 drafts, acceptance over S
+SMALLER_BLOCKS = ["tiny-b8", "small-batch-b10"]
+
+
+@pytest.mark.parametrize("attn_impl", ATTN)
+@pytest.mark.parametrize("name", SMALLER_BLOCKS)
+def test_smaller_block_round_matches_oracle(lib, name, attn_impl):
+    cfg, g, o = _pair(name, 2, attn_impl=attn_impl)
+    S = cfg.block
+    assert S < 16
+    for r in range(2):
+        go = g.round(debug=True)
+        oo = o.round(want_logits=True)
+        for j, od in enumerate(oo):
+            assert go["draft"][j].shape == (S - 1,)
+            assert rel_l2(go["hidden"][j], od["hidden"]) < TOL_REL_L2
+            assert rel_l2(go["logits"][j, 1:], od["logits"]) < TOL_REL_L2
+            assert np.array_equal(go["draft"][j], np.argmax(go["logits"][j, 1:], -1))
+            check_drafts(go["draft"][j], od)
+            assert (go["tau"][j], go["bonus"][j], go["ctx"][j]) == (od["tau"], od["bonus"], od["ctx"])
+    assert g.d.read_status() == 0
+
+
+@pytest.mark.parametrize("folded", [False, True], ids=["separate", "folded"])
+@pytest.mark.parametrize("name,rounds", [("tiny-b8", 8), ("small-batch-b10", 4)])
+def test_smaller_block_rounds_and_cache(lib, name, rounds, folded):
+    """Acceptance bit-exact over several rounds, and the cache afterwards holds
+    exactly the oracle's context K/V: the padding rows of a smaller block are
+    never written to it."""
+    cfg, g, o = _pair(name, rounds)
+    for r in range(rounds):
+        go = g.round(folded=folded)
+        oo = o.round(want_logits=False)
+        for j, od in enumerate(oo):
+            assert 1 <= go["tau"][j] <= cfg.block
+            assert (go["tau"][j], go["bonus"][j], go["ctx"][j]) == (od["tau"], od["bonus"], od["ctx"]), (r, j)
+            check_drafts(go["draft"][j], od)
+    lens = to_np(g.d.slot_lengths(g.state.slots))
+    for j in range(len(g.ids)):
+        L = int(lens[j])
+        for l in range(cfg.n_layers):
+            k, v = g.d.read_kv(l, j, 0, L)
+            ok, ov = o.reqs[j].ctx(l)
+            assert rel_l2(to_np(k), ok[:L]) < TOL_REL_L2 and rel_l2(to_np(v), ov[:L]) < TOL_REL_L2, (j, l)
+    assert g.d.read_status() == 0
+
+
 @pytest.mark.parametrize("name", ["tiny-gains", "small-batch"])
 def test_folded_round_equals_separate_calls(lib, name):
     """dflash_draft_round (K/V injection inside each layer's QKV GEMM) against
@@ -168,27 +215,29 @@ def test_batch_invariance(lib):
             check_drafts(res_full[r]["draft"][b], res_orc[r][b])
 
 
-def test_accept_trim_exhaustive_patterns(lib):
+@pytest.mark.parametrize("S", [16, 10, 8, 2])
+def test_accept_trim_exhaustive_patterns(lib, S):
     import torch
     from block_diffusion_speculative_hiddens_gb300 import Drafter, weights_to_device
-    cfg = get_config("tiny")
+    cfg = get_config("tiny").with_(block=S)
     d = Drafter(cfg, weights_to_device(make_weights(cfg)), max_batch=64, max_slots=64, max_pages=64,
                 max_pages_per_slot=1, max_rows=64)
     rng = np.random.default_rng(5)
     for rep in range(40):
         B = 64 if rep % 2 else int(rng.integers(1, 65))
-        draft = rng.integers(0, 7, (B, 15)).astype(np.int32)
-        target = rng.integers(0, 7, (B, 16)).astype(np.int32)
+        draft = rng.integers(0, 7, (B, S - 1)).astype(np.int32)
+        target = rng.integers(0, 7, (B, S)).astype(np.int32)
         # force structured patterns: all right, all wrong, single mismatch at k
         for b in range(B):
-            kind = (rep * 64 + b) % 18
+            kind = (rep * 64 + b) % (S + 2)
             if kind == 0:
-                target[b, :15] = draft[b]
+                target[b, :S - 1] = draft[b]
             elif kind == 1:
-                target[b, :15] = draft[b] + 1
-            elif kind < 17:
-                target[b, :15] = draft[b]
-                target[b, kind - 2] = draft[b, kind - 2] + 1 if kind - 2 < 15 else target[b, 14]
+                target[b, :S - 1] = draft[b] + 1
+            elif kind < S + 1:
+                target[b, :S - 1] = draft[b]
+                if kind - 2 < S - 1:
+                    target[b, kind - 2] = draft[b, kind - 2] + 1
         dev = torch.device("cuda:0")
         T = lambda a: torch.from_numpy(a).to(dev)
         slots = torch.arange(B, dtype=torch.int32, device=dev)
@@ -241,3 +290,10 @@ def test_edge_cases_and_errors(lib):
     d.reset_slot(1)
     assert to_np(d.slot_lengths(torch.tensor([1], **i32)))[0] == 0
     assert d.read_status() == 0
+    # an out-of-range slot in a draft call is a device-side error too: the
+    # request is computed from slot 0's lengths and written nowhere
+    before = [to_np(t).copy() for t in d.read_kv(0, 0, 0, 64)]
+    d.draft_block(torch.tensor([7], **i32), torch.tensor([1], **i32), torch.zeros(1, 15, **i32))
+    assert d.read_status() & DEV_ARG
+    after = [to_np(t) for t in d.read_kv(0, 0, 0, 64)]
+    assert all(np.array_equal(x, y, equal_nan=True) for x, y in zip(before, after))

@@ -7,8 +7,8 @@ per-request context lengths and match probabilities 3.
   [out_features, in_features]; RMSNorm gains 1 (or 1 + gain_std*N(0,1)).
 * Features of request b at position p: row of 5*hidden N(0,1) bf16 values,
   addressed by (b, p) so the row does not depend on acceptance history.
-* Stand-in verify stream of request b in round r: 16 match bits
-  m_i ~ Bernoulli(p_b) and 16 uniform ids u_i in [0, vocab).
+* Stand-in verify stream of request b in round r: S = block match bits
+  m_i ~ Bernoulli(p_b) and S uniform ids u_i in [0, vocab).
 """
 from __future__ import annotations
 
@@ -116,7 +116,7 @@ def match_probs(cfg) -> np.ndarray:
 def match_stream(cfg, r: int, batch_ids=None):
     """Stand-in verify randomness for round r.
 
-    Returns (m, u): m int32 [B, 16] in {0,1}, u int32 [B, 16] in [0, vocab).
+    Returns (m, u): m int32 [B, S] in {0,1}, u int32 [B, S] in [0, vocab), S = cfg.block.
     """
     ids = range(cfg.batch) if batch_ids is None else batch_ids
     probs = match_probs(cfg)
