@@ -200,7 +200,7 @@ size_t carve(dflash_handle* h, const dflash_config& c, char* base, int num_sms) 
   dflash_handle* o = h ? h : &tmp;
   o->status = w.take<uint32_t>(64);
   o->ctx_len = w.take<int>(c.max_slots);
-  o->pos0 = w.take<int>(c.max_slots);
+  o->pos0 = w.take<int>(c.max_batch);
   o->n_pages = w.take<int>(c.max_slots);
   o->page_table = w.take<int>((size_t)c.max_slots * c.max_pages_per_slot);
   o->free_stack = w.take<int>(c.max_pages);

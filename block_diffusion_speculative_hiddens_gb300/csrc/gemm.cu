@@ -160,19 +160,60 @@ DFL_DEV void gather_ctx(const GemmParams& p, int t_first, int j0, int ntok, int 
   }
 #pragma unroll
   for (int q = 0; q < EPI_TOK; ++q) c.inj[q] = MODE == GM_INJECT || (MODE == GM_QKV && p.inj_m0 > 0 && tq[q] >= p.inj_m0);
+  // Every load that depends only on the token index is issued before any
+  // value is used, so the tokens' inputs arrive in one round trip (two for
+  // fused-feature rows, whose RoPE row and page follow from their position).
+  float sv[EPI_TOK][2];
+#pragma unroll
+  for (int q = 0; q < EPI_TOK; ++q) {
+    const bool fold = MODE == GM_QKV && c.inj[q];
+    const float* src = fold ? p.ss_inj : p.ss_in;
+    const int ld = fold ? p.inj_ld : p.ss_ld;
+    const int row = fold ? tq[q] - p.inj_m0 : tq[q];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int i = lane + 32 * k;
+      sv[q][k] = (ok[q] && i < p.ss_parts) ? src[(size_t)i * ld + row] : 0.f;
+    }
+  }
+  int2 bc[EPI_TOK];
+  float2 r0[EPI_TOK], r1[EPI_TOK];
+  if (MODE == GM_QKV) {  // block rows: position, page and RoPE row written by the embedding
+    const int D = p.D;
+#pragma unroll
+    for (int q = 0; q < EPI_TOK; ++q) {
+      const bool blk = ok[q] && !c.inj[q];
+      const float2* row = p.brope + (size_t)tq[q] * (D / 2);
+      bc[q] = blk ? p.bctx[tq[q]] : make_int2(0, -1);
+      r0[q] = blk ? row[lane] : make_float2(1.f, 0.f);
+      r1[q] = (blk && D == 128) ? row[lane + 32] : make_float2(1.f, 0.f);
+    }
+  }
+  int slot[EPI_TOK], ne[EPI_TOK], ii[EPI_TOK], p0[EPI_TOK];
+  bool any_inj = false;
+  if (MODE == GM_QKV || MODE == GM_INJECT) {  // fused-feature rows: the request's slot and first position
+#pragma unroll
+    for (int q = 0; q < EPI_TOK; ++q) {
+      const bool in = ok[q] && c.inj[q];
+      any_inj |= in;
+      const int tl = MODE == GM_QKV ? tq[q] - p.inj_m0 : tq[q];
+      const int b = tl / p.rows_per_req;
+      ii[q] = tl % p.rows_per_req;
+      slot[q] = in ? p.slots[b] : 0;
+      ne[q] = in ? p.n_eff[b] : 0;
+      p0[q] = in ? p.pos0[b] : 0;
+    }
+  }
   {
     float ssq[EPI_TOK];
 #pragma unroll
-    for (int q = 0; q < EPI_TOK; ++q) {
-      ssq[q] = 0.f;
-      if (ok[q]) {
+    for (int q = 0; q < EPI_TOK; ++q) ssq[q] = sv[q][0] + sv[q][1];
+    for (int i = lane + 64; i < p.ss_parts; i += 32)  // hidden sizes above 8192 only
+#pragma unroll
+      for (int q = 0; q < EPI_TOK; ++q) {
         const bool fold = MODE == GM_QKV && c.inj[q];
-        const float* src = fold ? p.ss_inj : p.ss_in;
-        const int ld = fold ? p.inj_ld : p.ss_ld;
-        const int row = fold ? tq[q] - p.inj_m0 : tq[q];
-        for (int i = lane; i < p.ss_parts; i += 32) ssq[q] += src[(size_t)i * ld + row];
+        if (ok[q]) ssq[q] += (fold ? p.ss_inj : p.ss_in)[(size_t)i * (fold ? p.inj_ld : p.ss_ld) + (fold ? tq[q] - p.inj_m0 : tq[q])];
       }
-    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
 #pragma unroll
@@ -189,19 +230,7 @@ DFL_DEV void gather_ctx(const GemmParams& p, int t_first, int j0, int ntok, int 
       c.pos[q] = 0;
       c.live[q] = false;
     }
-    // block rows of a QKV GEMM: position, page and RoPE row written once per
-    // round by the embedding kernel -- one load round trip
     if (MODE == GM_QKV) {
-      int2 bc[EPI_TOK];
-      float2 r0[EPI_TOK], r1[EPI_TOK];
-#pragma unroll
-      for (int q = 0; q < EPI_TOK; ++q) {
-        const bool blk = ok[q] && !c.inj[q];
-        const float2* row = p.brope + (size_t)tq[q] * (D / 2);
-        bc[q] = blk ? p.bctx[tq[q]] : make_int2(0, -1);
-        r0[q] = blk ? row[lane] : make_float2(1.f, 0.f);
-        r1[q] = (blk && D == 128) ? row[lane + 32] : make_float2(1.f, 0.f);
-      }
 #pragma unroll
       for (int q = 0; q < EPI_TOK; ++q) {
         if (ok[q] && !c.inj[q]) {
@@ -213,25 +242,12 @@ DFL_DEV void gather_ctx(const GemmParams& p, int t_first, int j0, int ntok, int 
         }
       }
     }
-    // fused-feature rows (INJECT, or folded into QKV): from the slot's tables
-    bool any_inj = false;
-#pragma unroll
-    for (int q = 0; q < EPI_TOK; ++q) any_inj |= ok[q] && c.inj[q];
     if (any_inj) {
-      int slot[EPI_TOK], ne[EPI_TOK], ii[EPI_TOK];
-#pragma unroll
-      for (int q = 0; q < EPI_TOK; ++q) {
-        const int tl = MODE == GM_QKV ? tq[q] - p.inj_m0 : tq[q];
-        const int b = tl / p.rows_per_req;
-        ii[q] = tl % p.rows_per_req;
-        slot[q] = (ok[q] && c.inj[q]) ? p.slots[b] : 0;
-        ne[q] = (ok[q] && c.inj[q]) ? p.n_eff[b] : 0;
-      }
 #pragma unroll
       for (int q = 0; q < EPI_TOK; ++q) {
         if (!(ok[q] && c.inj[q])) continue;
         c.live[q] = ii[q] < ne[q];
-        c.pos[q] = p.pos0[slot[q]] + ii[q];
+        c.pos[q] = p0[q] + ii[q];
         if (c.live[q] && c.pos[q] >= p.max_pos) {
           dev_error(p.status, DFLASH_DEV_CAPACITY);
           c.live[q] = false;

@@ -82,7 +82,7 @@ struct GemmParams {
   KVGeom kv;
   const int* slots;     // [batch]
   const int* ctx_len;   // [max_slots] (QKV: block starts here)
-  const int* pos0;      // [max_slots] (inject: first new position)
+  const int* pos0;      // [batch] (inject: request b's first new position)
   const int* n_eff;     // [batch] (inject: rows appended)
   const float2* rope;   // [max_pos][D/2] (cos, sin)
   int max_pos;

@@ -123,7 +123,7 @@ __global__ void k_embed(const int* __restrict__ slots, const int* __restrict__ l
 // Page allocation for dflash_fuse_inject (one thread, requests in order, so
 // the page assignment is deterministic).  Grows each slot's page table to
 // cover ctx_len + n_new + block positions, records the first new position
-// (pos0) and the effective row count, and advances ctx_len.
+// (pos0, per request) and the effective row count, and advances ctx_len.
 __global__ void k_page_alloc(const int* slots, int batch, int S, const int* n_new, int rows_per_req, int* ctx_len,
                              int* pos0, int* n_pages, int* page_table, int mpps, int* free_stack, int* free_top,
                              int* n_eff, int* slots_ok, int max_slots, uint32_t* status) {
@@ -136,6 +136,7 @@ __global__ void k_page_alloc(const int* slots, int batch, int S, const int* n_ne
     if (slot < 0 || slot >= max_slots) {
       dev_error(status, DFLASH_DEV_ARG);
       n_eff[b] = 0;
+      pos0[b] = 0;
       slots_ok[b] = 0;  // in bounds for the later kernels; no row of it is live
       continue;
     }
@@ -163,7 +164,7 @@ __global__ void k_page_alloc(const int* slots, int batch, int S, const int* n_ne
     }
     if (np * DFL_PAGE < L + n) n = 0;  // no room for the new rows
     n_pages[slot] = np;
-    pos0[slot] = L;
+    pos0[b] = L;
     ctx_len[slot] = L + n;
     n_eff[b] = n;
   }
