@@ -83,6 +83,8 @@ struct Trace {
 struct dflash_handle {
   dflash_config cfg;
   int num_sms = 0;
+  int gemm_cl = 1;       // CTAs per cluster sharing a token tile of 128+ tokens
+  int gemm_cl_ctas = 0;  // CTAs of such clusters the GPU holds at once
   int max_tok = 0;     // max_batch * block
   int max_pos = 0;     // max_pages_per_slot * page_size
   int attn_splits = 1;
@@ -289,14 +291,35 @@ struct ProbeScope {
   }
 };
 
+#ifndef DFL_GEMM_MAX_CL
+#define DFL_GEMM_MAX_CL 4
+#endif
+
+// Token tiling of an M-row GEMM operand: t_tiles tiles of BN rows; for tiles
+// of 128 tokens or more, cl CTAs of a cluster share each token tile (each
+// loads BN/cl rows into all of them), so its box is BN/cl rows.
+struct GemmShape {
+  int t_tiles, BN, cl;
+  uint32_t box() const { return (uint32_t)(BN / cl); }
+};
+GemmShape gemm_shape(const dflash_handle* h, int M) {
+  GemmShape g;
+  g.t_tiles = ceil_div(std::max(M, 1), DFL_BN_MAX);
+  g.BN = ((ceil_div(std::max(M, 1), g.t_tiles) + 15) / 16) * 16;
+  g.cl = (g.BN >= 128 && h->gemm_cl > 1) ? h->gemm_cl : 1;
+  if (g.cl == 4) g.BN = (g.BN + 31) / 32 * 32;  // each quarter whole 8-row swizzle atoms
+  return g;
+}
+
 // Plan and launch one GEMM over packed A operands a[0..groups-1] (tiles
 // a_tile_off .. a_tile_off+n_tiles-1 of each) and the token operand B.
 int run_gemm(dflash_handle* h, cudaStream_t s, int mode, const void* const* a, int groups, int a_tile_off,
              int n_tiles, int K, const CUtensorMap& B, int M, GemmParams p, bool allow_split, uint32_t ab_type,
              int kid = 0) {
   if (M <= 0) return DFLASH_OK;
-  const int t_tiles = ceil_div(M, DFL_BN_MAX);
-  const int BN = ((ceil_div(M, t_tiles) + 15) / 16) * 16;
+  const GemmShape gs = gemm_shape(h, M);
+  const int t_tiles = gs.t_tiles;
+  const int BN = gs.BN;
   p.mode = mode;
   p.M = M;
   if (!p.ss_ld) p.ss_ld = M;
@@ -309,6 +332,9 @@ int run_gemm(dflash_handle* h, cudaStream_t s, int mode, const void* const* a, i
   p.a_tile_off = a_tile_off;
   p.ab_type = ab_type;
   p.total_tiles = groups * n_tiles * t_tiles;
+  p.cl = gs.cl;
+  p.n_tg = ceil_div(n_tiles, gs.cl);
+  p.total_ctiles = groups * p.n_tg * t_tiles;
   p.allow_split = allow_split ? 1 : 0;
   p.stages = gemm_pick_stages(BN, mode);
   int cols = 32;
@@ -325,9 +351,10 @@ int run_gemm(dflash_handle* h, cudaStream_t s, int mode, const void* const* a, i
   p.rope = h->rope;
   p.max_pos = h->max_pos;
   if (allow_split && p.total_tiles > h->max_tiles) return DFLASH_ERR_SHAPE;
-  const long long units = allow_split ? (long long)p.total_tiles * p.kblocks : p.total_tiles;
-  const int grid = (int)std::min<long long>(units, h->num_sms);
-  if (units * (grid + 1) >= (1LL << 31)) return DFLASH_ERR_SHAPE;  // the kernel's unit math is 32-bit
+  const long long units = allow_split ? (long long)p.total_ctiles * p.kblocks : p.total_ctiles;
+  const int clusters = (int)std::min<long long>(units, gs.cl > 1 ? h->gemm_cl_ctas / gs.cl : h->num_sms);
+  const int grid = clusters * gs.cl;
+  if (units * (clusters + 1) >= (1LL << 31)) return DFLASH_ERR_SHAPE;  // the kernel's unit math is 32-bit
   if (kid && h->trace.kid == kid && h->trace.buf && grid <= h->trace.cap) {
     p.trace = h->trace.buf;  // one launch only
     h->trace.kid = 0;
@@ -353,8 +380,7 @@ KVGeom kv_geom(dflash_handle* h) {
 int ensure_bmaps(dflash_handle* h, int M) {
   if (h->bm_M == M) return DFLASH_OK;
   const dflash_config& c = h->cfg;
-  const int t_tiles = ceil_div(M, DFL_BN_MAX);
-  const uint32_t BN = (uint32_t)(((ceil_div(M, t_tiles) + 15) / 16) * 16);
+  const uint32_t BN = gemm_shape(h, M).box();
   if (!make_tmap(&h->tm_hg, h->hg, M, c.hidden, BN)) return DFLASH_ERR_CUDA;
   if (!make_tmap(&h->tm_o, h->obuf, M, (uint64_t)c.n_q_heads * c.head_dim, BN)) return DFLASH_ERR_CUDA;
   if (!make_tmap(&h->tm_act, h->act, M, c.intermediate, BN)) return DFLASH_ERR_CUDA;
@@ -388,12 +414,11 @@ int draft_impl(dflash_handle* h, const int32_t* slots, int32_t batch, const int3
                                     c.max_slots, h->status, s));
     if (rc) return rc;
     const int MX = M + R;
-    const int t_tiles = ceil_div(R, DFL_BN_MAX);
-    const uint32_t BNr = (uint32_t)(((ceil_div(R, t_tiles) + 15) / 16) * 16);
+    const uint32_t BNr = gemm_shape(h, R).box();
     CUtensorMap tm_feats;
     if (!make_tmap(&tm_feats, feats, R, (uint64_t)c.n_fused * H, BNr, true)) return DFLASH_ERR_INVALID_ARG;
     if (h->bm_MX != MX) {
-      if (!make_tmap(&h->tm_hgx, h->hg, MX, H, (uint32_t)(((MX + 15) / 16) * 16))) return DFLASH_ERR_CUDA;
+      if (!make_tmap(&h->tm_hgx, h->hg, MX, H, gemm_shape(h, MX).box())) return DFLASH_ERR_CUDA;
       h->bm_MX = MX;
     }
     GemmParams p = {};
@@ -608,6 +633,20 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
   int rc = ok ? DFLASH_OK : DFLASH_ERR_CUDA;
   if (!rc) rc = cuda_err(gemm_init_attributes());
   if (!rc) rc = cuda_err(attn_init_attributes());
+  // token tiles of 128+ tokens: clusters of 4 CTAs share each tile unless
+  // pairs keep clearly more SMs busy (clusters are placed within one GPC)
+  if (!rc && DFL_GEMM_MAX_CL > 1) {
+    const int st = gemm_pick_stages(DFL_BN_MAX, GM_QKV);
+    const int n2 = 2 * gemm_max_clusters(DFL_BN_MAX, st, 2);
+    const int n4 = DFL_GEMM_MAX_CL >= 4 ? 4 * gemm_max_clusters(DFL_BN_MAX, st, 4) : 0;
+    if (n4 > 0 && 10 * n4 >= 9 * n2) {
+      h->gemm_cl = 4;
+      h->gemm_cl_ctas = std::min(n4, sms);
+    } else if (n2 > 0) {
+      h->gemm_cl = 2;
+      h->gemm_cl_ctas = std::min(n2, sms);
+    }
+  }
   // page loop: the tcgen05 one has the higher fixed cost per CTA and the
   // higher rate per page, so it is chosen when a split holds 16 pages or more
   // at full slot capacity (measured on GB300: slower at 4 and 8 pages per
@@ -659,8 +698,7 @@ int dflash_fuse_inject(dflash_handle* h, const int32_t* slots, int32_t batch, co
                                       c.max_slots, h->status, s));
   if (rc || rows_per_req == 0) return rc;
   const int R = batch * rows_per_req;
-  const int t_tiles = ceil_div(R, DFL_BN_MAX);
-  const uint32_t BN = (uint32_t)(((ceil_div(R, t_tiles) + 15) / 16) * 16);
+  const uint32_t BN = gemm_shape(h, R).box();
   CUtensorMap tm_feats;
   if (!make_tmap(&tm_feats, feats, R, (uint64_t)c.n_fused * H, BN, true)) return DFLASH_ERR_INVALID_ARG;
   if (h->bm_rows != R) {
@@ -965,6 +1003,9 @@ int noalloc_gemm(dflash_handle* h, cudaStream_t s, int mode, const void* const* 
   p.a_tile_off = a_tile_off;
   p.ab_type = ab_type;
   p.total_tiles = groups * n_tiles;
+  p.cl = 1;
+  p.n_tg = n_tiles;
+  p.total_ctiles = p.total_tiles;
   p.allow_split = 1;
   p.stages = gemm_pick_stages(BN, mode);
   int cols = 32;

@@ -91,6 +91,15 @@ DFL_DEV void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x
       "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y)
       : "memory");
 }
+// The same tile load delivered to every CTA of `mask` in the cluster, at the
+// same shared-memory offsets, each landing signalled on that CTA's barrier.
+DFL_DEV void tma_load_2d_mc(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "h"(mask)
+      : "memory");
+}
 DFL_DEV void tma_load_2d_hint(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
                               uint64_t policy) {
   asm volatile(
@@ -154,6 +163,15 @@ DFL_DEV void tc_commit(uint64_t* bar) {
                : "memory");
 }
 // 32 lanes x 16 consecutive 32-bit columns; thread i of the warp gets lane (base+i).
+// Arrive on the barrier at the same offset in every CTA of `mask` once the
+// issuing thread's tensor-core operations so far have completed.
+DFL_DEV void tc_commit_mc(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(mask)
+      : "memory");
+}
 DFL_DEV void tmem_ld16(uint32_t taddr, float* v) {
   uint32_t r[16];
   asm volatile(

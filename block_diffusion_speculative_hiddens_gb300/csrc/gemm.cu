@@ -53,6 +53,17 @@ DFL_DEV int unit_start(int c, int U, int G) { return c * U / G; }
 // CTA whose unit range [unit_start(c), unit_start(c+1)) contains unit u.
 DFL_DEV int cta_of_unit(int u, int U, int G) { return ((u + 1) * G + U - 1) / U - 1; }
 
+// Work is scheduled in tiles of cl n-tiles sharing one token tile; rank cr
+// of the cluster computes n-tile (tile group * cl + cr).  Scheduled tile ct
+// -> the tile this CTA computes, or -1 for a rank past its group's last
+// n-tile (it streams a copy of the last weight tile and finalises nothing).
+// With cl = 1 the two numberings coincide.
+DFL_DEV int tile_of(const GemmParams& p, int ct, int cr) {
+  const int rest = ct / p.t_tiles;
+  const int nt = (rest % p.n_tg) * p.cl + cr;
+  return nt < p.n_tiles ? ((rest / p.n_tg) * p.n_tiles + nt) * p.t_tiles + ct % p.t_tiles : -1;
+}
+
 // Timeline stamps (p.trace non-null): 0 entry, 1 set-up done, 2 first weight
 // stage landed, 3 last MMA issued, 4 epilogue done, 5 exit, 6 units, 7 SM id.
 DFL_DEV void trace_at(const GemmParams& p, int ev, unsigned long long v) {
@@ -475,7 +486,7 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(full + s, 1);
-      mbar_init(empty + s, 1);
+      mbar_init(empty + s, p.cl);  // every cluster CTA's MMAs release the stage
     }
     mbar_init(tfull + 0, 1);
     mbar_init(tfull + 1, 1);
@@ -492,21 +503,28 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // cluster peers write into this CTA's stages and signal its barriers
+  if (p.cl > 1) cluster_sync_all();
   const uint32_t tmem = *tmem_slot;
   pdl_launch_dependents();
   if (threadIdx.x == 0) trace_at(p, 1, globaltimer());
 
+  // Units (scheduled tile, k-block) are divided over the clusters; the CTAs
+  // of a cluster run the same units in lockstep, each on its own n-tile.
   const int KB = p.kblocks;
-  const int G = gridDim.x, c = blockIdx.x;
+  const int CL = p.cl;
+  const int crank = CL > 1 ? (int)cluster_ctarank() : 0;
+  const uint16_t cmask = (uint16_t)((1u << CL) - 1u);
+  const int G = gridDim.x / CL, c = blockIdx.x / CL;
   int U, u0, u1;
   if (p.allow_split) {
-    U = p.total_tiles * KB;
+    U = p.total_ctiles * KB;
     u0 = unit_start(c, U, G);
     u1 = unit_start(c + 1, U, G);
   } else {
-    U = p.total_tiles * KB;
-    u0 = unit_start(c, p.total_tiles, G) * KB;
-    u1 = unit_start(c + 1, p.total_tiles, G) * KB;
+    U = p.total_ctiles * KB;
+    u0 = unit_start(c, p.total_ctiles, G) * KB;
+    u1 = unit_start(c + 1, p.total_ctiles, G) * KB;
   }
   bool aborted = false;
 
@@ -522,9 +540,11 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
       const int n_units = (int)(u1 - u0);
       int tile = (int)(u0 / KB), kb = (int)(u0 % KB), tt = 0;
       const uint16_t* a_ptr = nullptr;
-      auto tile_base = [&]() {
-        const int tt_all = tile / p.t_tiles;
-        const int g = tt_all / p.n_tiles, nt = tt_all % p.n_tiles;
+      auto tile_base = [&]() {  // `tile` counts scheduled tiles here
+        const int rest = tile / p.t_tiles;
+        const int g = rest / p.n_tg;
+        int nt = (rest % p.n_tg) * CL + crank;
+        if (nt >= p.n_tiles) nt = p.n_tiles - 1;
         tt = tile % p.t_tiles;
         a_ptr = static_cast<const uint16_t*>(p.a[g]) + ((size_t)(p.a_tile_off + nt) * KBi + kb) * DFL_WBLK_ELEMS;
       };
@@ -549,8 +569,15 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
             bulk_load(dst + ch * CH, a_ptr + ch * (CH / 2), CH, full + st);
         }
       };
+      // With a cluster, each CTA loads BN/CL token rows of the tile into every
+      // peer's stage (same offsets): the cluster reads each token tile once.
+      const int bq = BN / CL;
       auto load_b = [&](int st, int kb_, int tt_) {
-        tma_load_2d(sm + (size_t)st * stage_bytes + A_STAGE_BYTES, &tmB, full + st, kb_ * 64, tt_ * BN);
+        uint8_t* dst = sm + (size_t)st * stage_bytes + A_STAGE_BYTES;
+        if (CL > 1)
+          tma_load_2d_mc(dst + crank * bq * 128, &tmB, full + st, kb_ * 64, tt_ * BN + crank * bq, cmask);
+        else
+          tma_load_2d(dst, &tmB, full + st, kb_ * 64, tt_ * BN);
       };
       // Weights do not depend on the previous kernel: fetch the first stages'
       // weight tiles before waiting on it, then the token tiles.
@@ -583,6 +610,14 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
       for (int i = (issued > stages ? issued - stages : 0); i < issued; ++i) {
         bool drain_abort = false;
         mbar_wait(full + (i % stages), (uint32_t)((i / stages) & 1), p.status, &drain_abort);
+      }
+      // and every peer's last release of each stage has arrived here
+      if (CL > 1 && !aborted) {
+        for (int s2 = 0; s2 < stages && s2 < issued; ++s2) {
+          const int last_fill = (issued - 1 - s2) / stages;
+          bool drain_abort = false;
+          mbar_wait(empty + s2, (uint32_t)(last_fill & 1), p.status, &drain_abort);
+        }
       }
     }
   } else if (warp == 1) {
@@ -618,7 +653,10 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
           for (int kk = 0; kk < 4; ++kk)
             tc_mma_f16(d, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk), idesc,
                         (k > 0 || kk > 0) ? 1u : 0u);
-          tc_commit(empty + s);
+          if (CL > 1)
+            tc_commit_mc(empty + s, cmask);
+          else
+            tc_commit(empty + s);
         }
         tc_commit(tfull + abuf);
       }
@@ -652,18 +690,19 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
       use_pre = true;
     }
     int seg = 0;
-    const int first_tile = u0 / KB;  // this CTA's first segment's tile
+    const int first_tile = u0 / KB;  // this CTA's first segment's scheduled tile
     uint32_t red_phase = 0;
     for (int u = u0; u < u1; ++seg) {
-      const int tile = u / KB;
-      const int seg_end = (tile + 1) * KB < u1 ? (tile + 1) * KB : u1;
+      const int tile_s = u / KB;  // scheduled tile
+      const int seg_end = (tile_s + 1) * KB < u1 ? (tile_s + 1) * KB : u1;
       u = seg_end;
       const int abuf = seg & 1;
       const uint32_t use = (uint32_t)(seg >> 1);
+      const int tile = tile_of(p, tile_s, crank);
       // RESID, one token tile: this tile's residual inputs for the first 16
       // tokens, loaded while the accumulators and the split reduction finish
       float hpre[EPI_TOK][4];
-      const bool use_hpre = MODE == GM_RESID && p.t_tiles == 1;
+      const bool use_hpre = MODE == GM_RESID && p.t_tiles == 1 && tile >= 0;
       if (use_hpre) {
         const int n0 = (int)(tile % p.n_tiles) * 128;
 #pragma unroll
@@ -676,19 +715,24 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
       }
       if (!mbar_wait(tfull + abuf, use & 1u, p.status, &aborted)) break;
       tc_fence_after();
+      if (tile < 0) {  // a rank past its group's last n-tile
+        tc_fence_before();
+        mbar_arrive(tempty + abuf);
+        continue;
+      }
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(abuf * BN);
       const int tt = (int)(tile % p.t_tiles);
       const int t_base = tt * BN;
       const int mt = (p.M - t_base) < BN ? (p.M - t_base) : BN;
       int c_first = c, c_last = c;
       if (p.allow_split) {
-        c_first = cta_of_unit(tile * KB, U, G);
-        c_last = cta_of_unit(tile * KB + KB - 1, U, G);
+        c_first = cta_of_unit(tile_s * KB, U, G);
+        c_last = cta_of_unit(tile_s * KB + KB - 1, U, G);
       }
       const bool split = c_first != c_last;
       if (split) {
-        const int my_slot = tile == first_tile ? 0 : 1;
-        float* w = p.ws + (size_t)(c * 2 + my_slot) * (DFL_BN_MAX * 128);
+        const int my_slot = tile_s == first_tile ? 0 : 1;
+        float* w = p.ws + (size_t)((c * CL + crank) * 2 + my_slot) * (DFL_BN_MAX * 128);
         for (int col = 0; col < BN; col += 16) {
           float v[16];
           tmem_ld16(taddr + (uint32_t)col, v);
@@ -724,7 +768,7 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
           // the whole ring takes a batch; otherwise the RED_PARTS-chunk buffer.
           // Every part after the first opens its CTA's range (slot 0); the
           // first part is slot 1 unless the tile also opens c_first's.
-          const int sl_first = unit_start(c_first, U, G) == tile * KB ? 0 : 1;
+          const int sl_first = unit_start(c_first, U, G) == tile_s * KB ? 0 : 1;
           const bool ring_free = u == u1;
           float* land = ring_free ? reinterpret_cast<float*>(sm) : red_buf;
           const int cap_items = ring_free ? (stages * stage_bytes) / (RED_CHUNK * 4) : RED_PARTS;
@@ -742,7 +786,7 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
                 const int cc = c_first + item - sub * nparts;
                 const int sl = cc == c_first ? sl_first : 0;
                 bulk_load(land + k * RED_CHUNK,
-                          p.ws + (size_t)(cc * 2 + sl) * (DFL_BN_MAX * 128) + (tc0 + 16 * sub) * 128,
+                          p.ws + (size_t)((cc * CL + crank) * 2 + sl) * (DFL_BN_MAX * 128) + (tc0 + 16 * sub) * 128,
                           RED_CHUNK * 4, red);
               }
             }
@@ -785,6 +829,8 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
   }
 
   __syncthreads();
+  // no CTA leaves while a peer may still write into it or signal its barriers
+  if (p.cl > 1) cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, ncols);
@@ -851,17 +897,48 @@ cudaError_t gemm_init_attributes() {
   return cudaFuncSetAttribute(k_gemm<GM_ARGMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
 }
 
+int gemm_max_clusters(int BN, int stages, int cl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(cl * 64));
+  cfg.blockDim = dim3(DFL_GEMM_THREADS);
+  cfg.dynamicSmemBytes = gemm_smem_bytes(BN, stages);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)cl;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, k_gemm<GM_ARGMAX>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
 cudaError_t gemm_launch(const CUtensorMap& B, const GemmParams& p, int grid, cudaStream_t s, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(DFL_GEMM_THREADS);
   cfg.dynamicSmemBytes = gemm_smem_bytes(p.BN, p.stages);
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  if (p.cl > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = (unsigned)p.cl;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = (unsigned)na;
   switch (p.mode) {
     case GM_QKV: return cudaLaunchKernelEx(&cfg, k_gemm<GM_QKV>, B, p);
     case GM_INJECT: return cudaLaunchKernelEx(&cfg, k_gemm<GM_INJECT>, B, p);

@@ -50,6 +50,9 @@ struct GemmParams {
   int BN;           // token tile (multiple of 16, <= 256)
   int groups;       // A operands used (grouped inject: one per layer)
   int total_tiles;  // groups * n_tiles * t_tiles
+  int cl;           // CTAs per cluster sharing each token tile (1, or 4 for token tiles >= 128)
+  int n_tg;         // n-tile groups of cl per group: ceil(n_tiles / cl)
+  int total_ctiles; // scheduled tiles: groups * n_tg * t_tiles (the cluster's ranks take the cl n-tiles)
   int allow_split;  // 0: every tile in one CTA over the full K
   int stages;
   int tmem_cols;    // power of two >= max(32, 2*BN)
@@ -121,6 +124,8 @@ struct AttnParams {
 size_t gemm_smem_bytes(int BN, int stages);
 int gemm_pick_stages(int BN, int mode);
 cudaError_t gemm_launch(const CUtensorMap& B, const GemmParams& p, int grid, cudaStream_t s, bool pdl);
+// Clusters of `cl` GEMM CTAs (token tile BN, `stages` ring) the GPU holds at once.
+int gemm_max_clusters(int BN, int stages, int cl);
 cudaError_t gemm_init_attributes();
 
 // Attention clusters of `splits` CTAs the GPU can hold at once (0: cannot

@@ -80,6 +80,27 @@ def test_rounds_accept_bit_exact(lib, name, rounds, folded, attn_impl):
     assert np.array_equal(lens + to_np(g.state.accept_len), [od["ctx"] for od in oo])
 
 
+def test_batch16_round_matches_oracle(lib):
+    """256 block tokens: every GEMM of the round (and the prefill's fusion and
+    injection GEMMs, 128+ rows) shares its token tile across a cluster."""
+    cfg, g, o = _pair("small-b16", 2)
+    for j in range(len(g.ids)):
+        L = int(g.ctx0[j])
+        k, v = g.d.read_kv(1, j, 0, L)
+        ok, ov = o.reqs[j].ctx(1)
+        assert rel_l2(to_np(k), ok) < TOL_REL_L2 and rel_l2(to_np(v), ov) < TOL_REL_L2, j
+    for r in range(2):
+        go = g.round(debug=True)
+        oo = o.round(want_logits=True)
+        for j, od in enumerate(oo):
+            assert rel_l2(go["hidden"][j], od["hidden"]) < TOL_REL_L2, (r, j)
+            assert rel_l2(go["logits"][j, 1:], od["logits"]) < TOL_REL_L2, (r, j)
+            assert np.array_equal(go["draft"][j], np.argmax(go["logits"][j, 1:], -1))
+            check_drafts(go["draft"][j], od)
+            assert (go["tau"][j], go["bonus"][j], go["ctx"][j]) == (od["tau"], od["bonus"], od["ctx"]), (r, j)
+    assert g.d.read_status() == 0
+
+
 # inference at blocks smaller than the trained 16: S-1 drafts, acceptance over S
 SMALLER_BLOCKS = ["tiny-b8", "small-batch-b10"]
 

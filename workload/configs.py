@@ -108,6 +108,13 @@ TEST_CONFIGS = {
     "mid": DraftConfig(
         name="mid", hidden=2048, n_q_heads=16, n_kv_heads=4, head_dim=128, intermediate=6144,
         n_layers=2, vocab=32768, rope_theta=1e6, batch=1, ctx0=1024, rounds=8, match_p=0.9),
+    # Batch 16: 256 block tokens, so every GEMM of the round runs with a full
+    # 256-token tile shared by a cluster of CTAs.
+    "small-b16": DraftConfig(
+        name="small-b16", hidden=512, n_q_heads=8, n_kv_heads=2, head_dim=128,
+        intermediate=768, n_layers=2, vocab=5000, rope_theta=5e5, batch=16, ctx0=None,
+        rounds=3, match_p=None, ctx_range=(30, 200), p_range=(0.5, 0.95), gain_std=0.1,
+        weight_std=0.05),
     # Inference at blocks smaller than the trained 16 (S-1 drafts per round).
     "tiny-b8": CONFIGS["tiny"].with_(name="tiny-b8", block=8, gain_std=0.1, weight_std=0.05),
     "small-batch-b10": DraftConfig(
