@@ -52,6 +52,8 @@ def parse():
     ap.add_argument("--cpu-budget-s", type=float, default=25.0)
     ap.add_argument("--block", type=int, default=None,
                     help="inference block size S in [2, 16] (default: the workload's, 16): S-1 drafts per round")
+    ap.add_argument("--attn-impl", type=int, default=0, choices=[0, 1, 2],
+                    help="attention page loop: 0 chosen by the library, 1 warp MMAs, 2 tcgen05")
     ap.add_argument("--fold-inject", action="store_true",
                     help="issue dflash_draft_round instead of dflash_fuse_inject + dflash_draft_block")
     return ap.parse_args()
@@ -244,7 +246,7 @@ def run_gpu(args, rank, world, local_rank):
 
     chunk = 2048
     d = Drafter(cfg, w_dev, max_batch=B, max_slots=n_slots, max_pages=mpps * n_slots,
-                max_pages_per_slot=mpps, max_rows=max(chunk, S * B), device=local_rank)
+                max_pages_per_slot=mpps, max_rows=max(chunk, S * B), device=local_rank, attn_impl=args.attn_impl)
     stream = torch.cuda.Stream(device=dev)
 
     def prefill(g):
@@ -456,6 +458,7 @@ def run_gpu(args, rank, world, local_rank):
                                f"{D}, I{cfg.intermediate}, {cfg.n_layers} layers, V{V}, fusion "
                                f"{F}->{H}, {ctx_desc}, block {S}, {p_desc}",
                    "batch": B, "prompt_mean": float(ctx.mean()), "rounds_per_slot": R,
+                   "attn_impl": ["library choice", "warp MMAs", "tcgen05"][args.attn_impl],
                    "round_call": "dflash_draft_round" if args.fold_inject
                    else "dflash_fuse_inject+dflash_draft_block", "slot_groups": n_groups - 1,
                    "l2": "inputs larger than L2 (the drafter's weights stream every round)",

@@ -337,6 +337,7 @@ int run_gemm(dflash_handle* h, cudaStream_t s, int mode, const void* const* a, i
   p.total_ctiles = groups * p.n_tg * t_tiles;
   p.allow_split = allow_split ? 1 : 0;
   p.stages = gemm_pick_stages(BN, mode);
+  p.red_items = gemm_red_items(BN, p.stages);
   int cols = 32;
   while (cols < 2 * BN) cols *= 2;
   p.tmem_cols = cols;
@@ -1008,6 +1009,7 @@ int noalloc_gemm(dflash_handle* h, cudaStream_t s, int mode, const void* const* 
   p.total_ctiles = p.total_tiles;
   p.allow_split = 1;
   p.stages = gemm_pick_stages(BN, mode);
+  p.red_items = gemm_red_items(BN, p.stages);
   int cols = 32;
   while (cols < 2 * BN) cols *= 2;
   p.tmem_cols = cols;

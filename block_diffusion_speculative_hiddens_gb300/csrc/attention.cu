@@ -384,13 +384,15 @@ __global__ void __launch_bounds__(G * KS * 32) k_attn(const AttnParams p) {
 //   S = Q K^T   tcgen05.mma M=128 (the G*16 query rows, zero-padded) x N=64 keys x K=D,
 //   softmax     one query row per thread, read from TMEM, P written to shared
 //               memory in the 128-byte-swizzle K-major layout,
-//   O_p = P V   tcgen05.mma M=128 x N=D x K=64 keys, read back and folded into
-//               the row's running output (registers) with the online-softmax
-//               rescale.
+//   O += P V    tcgen05.mma M=128 x N=D x K=64 keys, accumulated in TMEM.
+// P is taken against a reference maximum that moves only when a page's row
+// maximum exceeds it by more than 2^8 (then the row's O in TMEM is rescaled
+// once), so P stays within f16 and O is read from TMEM only at the end; the
+// result is the same softmax up to rounding.
 // The K page is already the K-major B operand of the first MMA and the V^T
-// page the K-major B operand of the second (pre-swizzled in HBM).  S, P and
-// O_p are double-buffered, and the next page's Q K^T is issued before this
-// page's P V, so the MMAs overlap the softmax.
+// page the K-major B operand of the second (pre-swizzled in HBM).  S and P
+// are double-buffered, and the next page's Q K^T is issued before this page's
+// P V, so the MMAs overlap the softmax.
 // Warps: 0 page loads (one thread), 1 TMEM allocation and MMA issue (one
 // thread), 2-9 softmax: two threads per query row (TMEM lane), each taking 32
 // of a page's 64 keys and half of the output columns; the pair trades its
@@ -410,10 +412,10 @@ struct TcCfg {
   static constexpr int OFF_X = OFF_PIDS + MAX_PIDS * 4;  // half-row exchange: [2 parities][2 halves][128] u64
   static constexpr int SMEM = 1024 + OFF_X + 2 * 2 * 128 * 8;  // + 1024 for aligning the base
   static constexpr int S_COL = 0;                   // S buffers: columns [0, 128)
-  static constexpr int O_COL = 128;                 // O_p buffers: columns [128, 128 + 2D)
-  // columns allocated: exactly what the buffers use (a power of two), so two
-  // CTAs that might share an SM never wait on each other's columns
-  static constexpr uint32_t TMEM_COLS = D == 128 ? 512 : 256;
+  static constexpr int O_COL = 128;                 // O accumulator: columns [128, 128 + D)
+  // columns allocated: a power of two covering the buffers, so two CTAs that
+  // might share an SM never wait on each other's columns
+  static constexpr uint32_t TMEM_COLS = 256;
 };
 
 template <int D, int G>
@@ -427,9 +429,8 @@ __global__ void __launch_bounds__(320, 1) k_attn_tc(const AttnParams p) {
   uint64_t* s_full = empty + C::STAGES;     // [2] S in TMEM
   uint64_t* s_empty = s_full + 2;           // [2] S read by the softmax warps
   uint64_t* p_full = s_empty + 2;           // [2] P in shared memory
-  uint64_t* o_full = p_full + 2;            // [2] O_p in TMEM
-  uint64_t* o_empty = o_full + 2;           // [2] O_p read by the softmax warps
-  uint64_t* q_full = o_empty + 2;           // Q in shared memory
+  uint64_t* o_full = p_full + 2;            // [2] P V of page i (barrier i & 1) complete
+  uint64_t* q_full = o_full + 2;            // Q in shared memory
   uint64_t* mdone = q_full + 1;             // every issued MMA complete
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mdone + 1);
   int* pids = reinterpret_cast<int*>(sm + C::OFF_PIDS);
@@ -458,7 +459,6 @@ __global__ void __launch_bounds__(320, 1) k_attn_tc(const AttnParams p) {
       mbar_init(s_empty + i, 256);
       mbar_init(p_full + i, 256);
       mbar_init(o_full + i, 1);
-      mbar_init(o_empty + i, 256);
     }
     mbar_init(q_full, 256);
     mbar_init(mdone, 1);
@@ -490,10 +490,8 @@ __global__ void __launch_bounds__(320, 1) k_attn_tc(const AttnParams p) {
 
   // running state of this thread's half of a query row (softmax warps)
   constexpr int DH = D / 2;  // output columns per thread
-  float o[DH];
+  float o[DH];                           // set from TMEM after the last page
   float m_run = -INFINITY, l_run = 0.f;  // l_run: this half's keys only
-#pragma unroll
-  for (int d = 0; d < DH; ++d) o[d] = 0.f;
   const int q4 = warp & 3;
   const int r = q4 * 32 + lane;        // TMEM lane = query row (softmax warps)
   const int kh = warp >= 6 ? 1 : 0;    // key / output-column half
@@ -554,7 +552,6 @@ __global__ void __launch_bounds__(320, 1) k_attn_tc(const AttnParams p) {
         if (i + 1 < n && !issue_s(i + 1)) break;
         const int s = i % C::STAGES, bb = i & 1;
         if (!mbar_wait(p_full + bb, (uint32_t)((i / 2) & 1), p.status, &aborted)) break;
-        if (i >= 2 && !mbar_wait(o_empty + bb, (uint32_t)((i / 2 - 1) & 1), p.status, &aborted)) break;
         tc_fence_after();
         const uint32_t p_addr = smem_u32(sm + C::OFF_P + bb * C::PB);
         const uint32_t v_addr = smem_u32(sm + s * C::STAGE + C::BLK);
@@ -562,7 +559,7 @@ __global__ void __launch_bounds__(320, 1) k_attn_tc(const AttnParams p) {
         for (int kk = 0; kk < 4; ++kk) {
           const uint64_t ad = sdesc_sw128(p_addr) + (uint64_t)(2 * kk);
           const uint64_t bd = sdesc_sw128(v_addr) + (uint64_t)(2 * kk);
-          tc_mma_f16(tmem + (uint32_t)(C::O_COL + D * bb), ad, bd, idesc_o, kk > 0 ? 1u : 0u);
+          tc_mma_f16(tmem + (uint32_t)C::O_COL, ad, bd, idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
         }
         tc_commit(o_full + bb);
         tc_commit(empty + s);
@@ -608,24 +605,16 @@ __global__ void __launch_bounds__(320, 1) k_attn_tc(const AttnParams p) {
       mbar_arrive(q_full);
     }
     const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
-    // O_p of page i is folded in while page i+1's softmax is done: the P V
-    // MMA of one page overlaps the next page's softmax
-    auto fold = [&](int i, float alpha) {
-      const int bb = i & 1;
-      if (!mbar_wait(o_full + bb, (uint32_t)((i / 2) & 1), p.status, &aborted)) return false;
-      tc_fence_after();
-#pragma unroll
-      for (int j = 0; j < DH / 16; ++j) {
-        float v[16];
-        tmem_ld16(lane_base + (uint32_t)(C::O_COL + D * bb + kh * DH + 16 * j), v);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) o[16 * j + e] = o[16 * j + e] * alpha + v[e];
-      }
-      tc_fence_before();
-      mbar_arrive(o_empty + bb);
+    // P V of page i complete (o_full[i & 1]).  Waited once per page, right
+    // after P of the next page is published, so a barrier never runs two
+    // phases ahead of its waiter; also frees P buffer i & 1 for page i + 2.
+    int o_seen = -1;  // pages whose P V this thread has seen complete
+    auto wait_o = [&](int i) {
+      if (i <= o_seen) return true;
+      if (!mbar_wait(o_full + (i & 1), (uint32_t)((i / 2) & 1), p.status, &aborted)) return false;
+      o_seen = i;
       return true;
     };
-    float alpha_prev = 0.f;  // rescale that goes with the pending O_p
     bool ok = true;
     for (int i = 0; i < n && ok; ++i) {
       const int bb = i & 1;
@@ -647,9 +636,29 @@ __global__ void __launch_bounds__(320, 1) k_attn_tc(const AttnParams p) {
       }
       float mx_other;
       if (!trade(mx, (uint32_t)i, &mx_other)) break;
-      const float mn = fmaxf(m_run, fmaxf(mx, mx_other));
-      const float ref = mn == -INFINITY ? 0.f : mn;  // a row with only masked keys so far adds 0
-      const float alpha = exp2f(m_run - ref);
+      const float mx_all = fmaxf(mx, mx_other);
+      const bool move = mx_all > m_run + 8.f;  // same decision in both threads of the row
+      if (__any_sync(0xffffffffu, move)) {     // TMEM access is warp-wide
+        const float m_new = move ? mx_all : m_run;
+        if (i > 0) {  // O holds pages < i against m_run: rescale it once P V of page i-1 is done
+          if (!wait_o(i - 1)) break;
+          tc_fence_after();
+          const float alpha = move ? exp2f(m_run - m_new) : 1.f;
+#pragma unroll
+          for (int j = 0; j < DH / 16; ++j) {
+            float v[16];
+            const uint32_t ta = lane_base + (uint32_t)(C::O_COL + kh * DH + 16 * j);
+            tmem_ld16(ta, v);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] *= alpha;
+            tmem_st16(ta, v);
+          }
+          tc_fence_before();
+          l_run *= alpha;
+        }
+        m_run = m_new;
+      }
+      const float ref = m_run == -INFINITY ? 0.f : m_run;  // a row with only masked keys so far adds 0
       float rs = 0.f;
       uint32_t pk[16];
 #pragma unroll
@@ -658,8 +667,7 @@ __global__ void __launch_bounds__(320, 1) k_attn_tc(const AttnParams p) {
         rs += a + c;
         pk[k] = pack_f16x2(a, c);
       }
-      l_run = l_run * alpha + rs;
-      m_run = mn;
+      l_run += rs;
       {  // this half of P row r: 32 keys = 4 chunks of 16 bytes, swizzled like the K page rows
         uint8_t* prow = sm + C::OFF_P + bb * C::PB + r * 128;
 #pragma unroll
@@ -669,11 +677,17 @@ __global__ void __launch_bounds__(320, 1) k_attn_tc(const AttnParams p) {
       }
       fence_proxy_async_smem();
       mbar_arrive(p_full + bb);
-      // o holds pages < i-1 at the max before page i-1; bring in page i-1
-      if (i > 0) ok = fold(i - 1, alpha_prev);
-      alpha_prev = alpha;
+      if (i > 0) ok = wait_o(i - 1);
     }
-    if (ok && n > 0 && !aborted) fold(n - 1, alpha_prev);
+    // the row's output half, once every P V is done
+    if (ok && n > 0 && !aborted && wait_o(n - 1)) {
+      tc_fence_after();
+#pragma unroll
+      for (int j = 0; j < DH / 16; ++j) tmem_ld16(lane_base + (uint32_t)(C::O_COL + kh * DH + 16 * j), o + 16 * j);
+    } else {
+#pragma unroll
+      for (int d = 0; d < DH; ++d) o[d] = 0.f;
+    }
     // the row's sum over both halves
     float l_other = 0.f;
     if (!aborted && trade(l_run, (uint32_t)n, &l_other)) l_run += l_other;

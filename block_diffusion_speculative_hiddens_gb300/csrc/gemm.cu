@@ -35,6 +35,9 @@
 #ifndef DFL_GEMM_L2_HINT
 #define DFL_GEMM_L2_HINT 1
 #endif
+#ifndef DFL_GEMM_RED_MAX  // most split-K part chunks (8 KB) landed at once outside the last segment
+#define DFL_GEMM_RED_MAX 16
+#endif
 #ifndef DFL_GEMM_A_CHUNKS  // bulk copies per 16 KB weight block
 #define DFL_GEMM_A_CHUNKS 1
 #endif
@@ -43,7 +46,7 @@ namespace {
 
 constexpr int A_STAGE_BYTES = 128 * 128;  // 128 rows x 64 16-bit values
 constexpr int STG_BYTES = 32 * 128 * 4;   // epilogue staging: 32 tokens x 128 rows fp32
-constexpr int RED_PARTS = 4;               // split-K parts landed in shared memory at once
+constexpr int RED_PARTS = 4;               // fewest split-K part chunks the reduction buffer holds
 constexpr int RED_CHUNK = 16 * 128;        // floats of one part's 16-column chunk (8 KB)
 constexpr int RED_BYTES = RED_PARTS * RED_CHUNK * 4;
 constexpr int EPI_THREADS = 128;
@@ -470,7 +473,8 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
   const int stage_bytes = A_STAGE_BYTES + BN * 128;
   float* stg = reinterpret_cast<float*>(sm + (size_t)stages * stage_bytes);
   float* red_buf = reinterpret_cast<float*>(sm + (size_t)stages * stage_bytes + STG_BYTES);
-  uint64_t* full = reinterpret_cast<uint64_t*>(sm + (size_t)stages * stage_bytes + STG_BYTES + RED_BYTES);
+  uint64_t* full =
+      reinterpret_cast<uint64_t*>(sm + (size_t)stages * stage_bytes + STG_BYTES + (size_t)p.red_items * RED_CHUNK * 4);
   uint64_t* empty = full + stages;
   uint64_t* tfull = empty + stages;
   uint64_t* tempty = tfull + 2;
@@ -765,13 +769,13 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
           // (one issuing thread, one barrier per batch) and are added in k
           // order by a compact loop -- this code runs cold once per tile.  On
           // the CTA's last segment every weight stage has been consumed, so
-          // the whole ring takes a batch; otherwise the RED_PARTS-chunk buffer.
+          // the whole ring takes a batch; otherwise the p.red_items-chunk buffer.
           // Every part after the first opens its CTA's range (slot 0); the
           // first part is slot 1 unless the tile also opens c_first's.
           const int sl_first = unit_start(c_first, U, G) == tile_s * KB ? 0 : 1;
           const bool ring_free = u == u1;
           float* land = ring_free ? reinterpret_cast<float*>(sm) : red_buf;
-          const int cap_items = ring_free ? (stages * stage_bytes) / (RED_CHUNK * 4) : RED_PARTS;
+          const int cap_items = ring_free ? (stages * stage_bytes) / (RED_CHUNK * 4) : p.red_items;
           const int nparts = c_last - c_first + 1;
           const int nitems = nparts * (two ? 2 : 1);  // (sub, part), part fastest
           for (int it0 = 0; it0 < nitems && !aborted; it0 += cap_items) {
@@ -869,9 +873,17 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
 
 }  // namespace
 
+// Split-K part chunks (8 KB) the reduction lands at once while the ring is
+// still in use: whatever shared memory the ring leaves, 4 to 16.
+int gemm_red_items(int BN, int stages) {
+  const long long left = 232448LL - 1024 - (long long)stages * (A_STAGE_BYTES + BN * 128) - STG_BYTES - 512;
+  const long long n = left / (RED_CHUNK * 4);
+  return (int)(n < RED_PARTS ? RED_PARTS : (n > DFL_GEMM_RED_MAX ? DFL_GEMM_RED_MAX : n));
+}
+
 size_t gemm_smem_bytes(int BN, int stages) {
-  return 1024 + (size_t)stages * (A_STAGE_BYTES + BN * 128) + STG_BYTES + RED_BYTES + (size_t)(2 * stages + 6) * 8 +
-         16;
+  return 1024 + (size_t)stages * (A_STAGE_BYTES + BN * 128) + STG_BYTES +
+         (size_t)gemm_red_items(BN, stages) * RED_CHUNK * 4 + (size_t)(2 * stages + 6) * 8 + 16;
 }
 
 // Weight-ring depth.  Six 16 KB stages per SM already keep HBM streaming at

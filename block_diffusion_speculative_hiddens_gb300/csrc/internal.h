@@ -55,6 +55,7 @@ struct GemmParams {
   int total_ctiles; // scheduled tiles: groups * n_tg * t_tiles (the cluster's ranks take the cl n-tiles)
   int allow_split;  // 0: every tile in one CTA over the full K
   int stages;
+  int red_items;    // split-K part chunks (8 KB) the reduction buffer holds (gemm_red_items)
   int tmem_cols;    // power of two >= max(32, 2*BN)
   uint32_t ab_type; // 0: f16 operands, 1: bf16 operands
   const void* a[DFL_MAX_LAYERS];  // packed A blocks [tiles][kblocks][128x64] per group
@@ -122,6 +123,7 @@ struct AttnParams {
 
 // host launchers (gemm.cu / attention.cu / small.cu)
 size_t gemm_smem_bytes(int BN, int stages);
+int gemm_red_items(int BN, int stages);
 int gemm_pick_stages(int BN, int mode);
 cudaError_t gemm_launch(const CUtensorMap& B, const GemmParams& p, int grid, cudaStream_t s, bool pdl);
 // Clusters of `cl` GEMM CTAs (token tile BN, `stages` ring) the GPU holds at once.
