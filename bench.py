@@ -464,6 +464,7 @@ def run_gpu(args, rank, world, local_rank):
                    "l2": "inputs larger than L2 (the drafter's weights stream every round)",
                    "parallelism": f"replicas x{world}"},
         "gpu_launches": launches_captured,
+        "plan": d.plan(),
         "graph_kernel_nodes": n_kernels,
         "roofline": lm_roof,
         "round_roofline": {"bytes_per_round": int(round_bytes), "achieved_gbs": round(

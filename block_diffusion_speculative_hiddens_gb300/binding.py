@@ -74,6 +74,7 @@ _SIGS = {
     "dflash_mark": (ctypes.c_int, [_vp, _vp]),
     "dflash_marks_read": (ctypes.c_int, [_vp, _vp, ctypes.c_int32, _vp]),
     "dflash_launch_count": (ctypes.c_uint64, [_vp]),
+    "dflash_plan": (ctypes.c_int, [_vp, _vp]),
     "dflash_trace_arm": (ctypes.c_int, [_vp, ctypes.c_int32, _vp, ctypes.c_int32]),
     "dflash_harness_verify": (ctypes.c_int, [_vp, _vp, ctypes.c_int32, _vp, _vp, _vp, ctypes.c_int32, _vp,
                                              _vp, _vp, ctypes.c_int32, _vp, _vp]),
@@ -274,6 +275,13 @@ class Drafter:
 
     def launch_count(self) -> int:
         return int(self.lib.dflash_launch_count(self.h))
+
+    def plan(self) -> dict:
+        """SMs, attention splits and page loop, GEMM cluster size chosen at create."""
+        v = (ctypes.c_int32 * 4)()
+        _check("dflash_plan", self.lib.dflash_plan(self.h, v))
+        return {"sms": v[0], "attn_splits": v[1], "attn_impl": ["", "warp MMAs", "tcgen05"][v[2]],
+                "gemm_cluster": v[3]}
 
     def harness_verify(self, slots, draft, match, offs, rounds_cap: int, round_ctr, target,
                        feat_stream=None, stream_rows: int = 0, feats_out=None, stream=None):

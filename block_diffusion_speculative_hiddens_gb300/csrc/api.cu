@@ -918,6 +918,15 @@ int dflash_marks_read(dflash_handle* h, float* ms_out, int32_t cap, int32_t* n_o
 
 uint64_t dflash_launch_count(dflash_handle* h) { return h ? h->launches : 0; }
 
+int dflash_plan(dflash_handle* h, int32_t* out4) {
+  if (!h || !out4) return DFLASH_ERR_INVALID_ARG;
+  out4[0] = h->num_sms;
+  out4[1] = h->attn_splits;
+  out4[2] = h->attn_tc ? 2 : 1;
+  out4[3] = h->gemm_cl;
+  return DFLASH_OK;
+}
+
 int dflash_trace_arm(dflash_handle* h, int32_t kernel_id, unsigned long long* buf, int32_t cap_ctas) {
   if (!h || (kernel_id && (!buf || cap_ctas <= 0))) return DFLASH_ERR_INVALID_ARG;
   h->trace.kid = kernel_id;

@@ -60,6 +60,7 @@ def test_null_arguments_rejected_without_device(lib):
     assert lib.dflash_draft_block(None, None, 0, None, None, None) == 1
     assert lib.dflash_fuse_inject(None, None, 1, None, 16, None, None) == 1
     assert lib.dflash_draft_round(None, None, 1, None, 16, None, None, None, None) == 1
+    assert lib.dflash_plan(None, None) == 1
     assert lib.dflash_accept_trim(None, None, 1, None, None, None, None, None, None) == 1
     assert lib.dflash_launch_count(None) == 0
     out = ctypes.c_void_p()
