@@ -54,6 +54,9 @@ def parse():
                     help="inference block size S in [2, 16] (default: the workload's, 16): S-1 drafts per round")
     ap.add_argument("--attn-impl", type=int, default=0, choices=[0, 1, 2],
                     help="attention page loop: 0 chosen by the library, 1 warp MMAs, 2 tcgen05")
+    ap.add_argument("--temperature", type=float, default=0.0,
+                    help="draft at this temperature (> 0: each draft drawn from softmax(logits / T))")
+    ap.add_argument("--seed", type=int, default=1234, help="seed of the drafts' random streams (temperature > 0)")
     ap.add_argument("--fold-inject", action="store_true",
                     help="issue dflash_draft_round instead of dflash_fuse_inject + dflash_draft_block")
     return ap.parse_args()
@@ -264,6 +267,8 @@ def run_gpu(args, rank, world, local_rank):
         st = RoundState(d, B, slots=[g * B + b for b in range(B)], first_token=cfg.first_token)
         states.append(st)
         verifies.append(SyntheticVerify(st, match, offs, feat_stream))
+        if args.temperature > 0:
+            st.set_sampling(args.temperature, args.seed, verifies[-1].round_ctr)
     stream.synchronize()
 
     # warm-up: W rounds on the spare group, as one graph
@@ -325,6 +330,8 @@ def run_gpu(args, rank, world, local_rank):
     prefill(gi)
     st_i = RoundState(d, B, slots=[gi * B + b for b in range(B)], first_token=cfg.first_token)
     ver_i = SyntheticVerify(st_i, match, offs, feat_stream)
+    if args.temperature > 0:
+        st_i.set_sampling(args.temperature, args.seed, ver_i.round_ctr)
 
     def marked_verify(s_=None):
         d.mark(s_)
@@ -357,6 +364,8 @@ def run_gpu(args, rank, world, local_rank):
         m_dev = torch.zeros(1, B, S, dtype=torch.int32, device=dev)
         u_dev = torch.zeros_like(m_dev)
         ver = SyntheticVerify(st, m_dev, u_dev, None)
+        if args.temperature > 0:
+            st.set_sampling(args.temperature, args.seed, ver.round_ctr)
         d.graph_begin(stream)
         run_round(st, ver, stream, folded=args.fold_inject)
         d.graph_end(stream)
@@ -459,6 +468,8 @@ def run_gpu(args, rank, world, local_rank):
                                f"{F}->{H}, {ctx_desc}, block {S}, {p_desc}",
                    "batch": B, "prompt_mean": float(ctx.mean()), "rounds_per_slot": R,
                    "attn_impl": ["library choice", "warp MMAs", "tcgen05"][args.attn_impl],
+                   "drafting": (f"sampled at temperature {args.temperature} (Gumbel-max, seed {args.seed})"
+                                if args.temperature > 0 else "greedy argmax"),
                    "round_call": "dflash_draft_round" if args.fold_inject
                    else "dflash_fuse_inject+dflash_draft_block", "slot_groups": n_groups - 1,
                    "l2": "inputs larger than L2 (the drafter's weights stream every round)",

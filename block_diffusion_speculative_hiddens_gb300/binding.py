@@ -58,6 +58,8 @@ _SIGS = {
     "dflash_draft_block": (ctypes.c_int, [_vp, _vp, ctypes.c_int32, _vp, _vp, _vp]),
     "dflash_draft_round": (ctypes.c_int, [_vp, _vp, ctypes.c_int32, _vp, ctypes.c_int32, _vp, _vp, _vp, _vp]),
     "dflash_draft_block_debug": (ctypes.c_int, [_vp, _vp, ctypes.c_int32, _vp, _vp, _vp, _vp, _vp]),
+    "dflash_draft_block_sample": (ctypes.c_int, [_vp, _vp, ctypes.c_int32, _vp, ctypes.c_float, ctypes.c_uint64,
+                                                 _vp, _vp, _vp, _vp]),
     "dflash_accept_trim": (ctypes.c_int, [_vp, _vp, ctypes.c_int32, _vp, _vp, _vp, _vp, _vp, _vp]),
     "dflash_reset_slot": (ctypes.c_int, [_vp, ctypes.c_int32, _vp]),
     "dflash_read_status": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_uint32)]),
@@ -202,6 +204,13 @@ class Drafter:
         _check("dflash_draft_block_debug", self.lib.dflash_draft_block_debug(
             self.h, _ptr(slots), slots.numel(), _ptr(last_tok), _ptr(draft), _ptr(hidden),
             _ptr(logits), _stream(stream)))
+
+    def draft_block_sample(self, slots, last_tok, temperature: float, seed: int, round_ctr, draft, logits=None,
+                           stream=None):
+        """dflash_draft_block with each draft drawn from softmax(logits / temperature)."""
+        _check("dflash_draft_block_sample", self.lib.dflash_draft_block_sample(
+            self.h, _ptr(slots), slots.numel(), _ptr(last_tok), float(temperature), int(seed) & ((1 << 64) - 1),
+            _ptr(round_ctr), _ptr(draft), _ptr(logits), _stream(stream)))
 
     def accept_trim(self, slots, draft, target, accept_len, bonus, ctx_len, stream=None):
         _check("dflash_accept_trim", self.lib.dflash_accept_trim(

@@ -392,9 +392,15 @@ int ensure_bmaps(dflash_handle* h, int M) {
 // Draft one block; with `feats` non-null, first fuse the new feature rows and
 // fold their K/V injection into every layer's QKV projection (rows M.. of its
 // token operand), so each layer's K/V weights stream once per round.
+struct Sampling {
+  float temp_inv = 0.f;  // 0: greedy
+  unsigned long long seed = 0;
+  const int32_t* round = nullptr;
+};
+
 int draft_impl(dflash_handle* h, const int32_t* slots, int32_t batch, const int32_t* last_tok, int32_t* draft,
                float* hidden, float* logits, void* stream, const void* feats = nullptr, int rows_per_req = 0,
-               const int32_t* n_new = nullptr) {
+               const int32_t* n_new = nullptr, Sampling smp = Sampling()) {
   if (!h || batch < 0 || batch > h->cfg.max_batch) return DFLASH_ERR_INVALID_ARG;
   if (batch == 0) return DFLASH_OK;
   if (!slots || !last_tok || !draft) return DFLASH_ERR_INVALID_ARG;
@@ -551,6 +557,9 @@ int draft_impl(dflash_handle* h, const int32_t* slots, int32_t batch, const int3
     p.logits = logits;
     p.draft = draft;
     p.block = c.block;
+    p.temp_inv = smp.temp_inv;
+    p.seed = smp.seed;
+    p.round = smp.round;
     p.done_ctr = h->done_ctr;
     const void* a = h->embed_pk;
     rc = run_gemm(h, s, GM_ARGMAX, &a, 1, 0, ceil_div(c.vocab, 128), H, h->tm_hg, M, p, true, 0,
@@ -649,10 +658,11 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
     }
   }
   // page loop: the tcgen05 one has the higher fixed cost per CTA and the
-  // higher rate per page, so it is chosen when a split holds 16 pages or more
-  // at full slot capacity (measured on GB300: slower at 4 and 8 pages per
-  // split, 1.3x faster on the whole round at 57)
-  h->attn_tc = c.attn_impl == 2 || (c.attn_impl == 0 && ceil_div(c.max_pages_per_slot, h->attn_splits) >= 16);
+  // higher rate per page, so it is chosen when a split holds 8 pages or more
+  // at full slot capacity (measured on GB300: slower at 4-5 pages per split,
+  // faster at 11 -- 769.6 vs 775.2 us per Llama-3.1-8B-shaped round -- and at
+  // 57-86)
+  h->attn_tc = c.attn_impl == 2 || (c.attn_impl == 0 && ceil_div(c.max_pages_per_slot, h->attn_splits) >= 8);
   // every (request, KV head) cluster in one wave: a second wave would double
   // the attention time, so take the most splits whose clusters all fit
   while (!rc && h->attn_splits > 1 &&
@@ -760,6 +770,17 @@ int dflash_draft_round(dflash_handle* h, const int32_t* slots, int32_t batch, co
 int dflash_draft_block_debug(dflash_handle* h, const int32_t* slots, int32_t batch, const int32_t* last_tok,
                              int32_t* draft, float* hidden, float* logits, void* stream) {
   return draft_impl(h, slots, batch, last_tok, draft, hidden, logits, stream);
+}
+
+int dflash_draft_block_sample(dflash_handle* h, const int32_t* slots, int32_t batch, const int32_t* last_tok,
+                              float temperature, uint64_t seed, const int32_t* round, int32_t* draft, float* logits,
+                              void* stream) {
+  if (!(temperature == temperature) || temperature < 0.f) return DFLASH_ERR_INVALID_ARG;
+  Sampling smp;
+  smp.temp_inv = temperature >= 1e-6f ? 1.f / temperature : 0.f;  // below: the draw is the argmax
+  smp.seed = seed;
+  smp.round = round;
+  return draft_impl(h, slots, batch, last_tok, draft, nullptr, logits, stream, nullptr, 0, nullptr, smp);
 }
 
 int dflash_accept_trim(dflash_handle* h, const int32_t* slots, int32_t batch, const int32_t* draft,

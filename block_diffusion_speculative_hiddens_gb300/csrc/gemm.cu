@@ -67,6 +67,30 @@ DFL_DEV int tile_of(const GemmParams& p, int ct, int cr) {
   return nt < p.n_tiles ? ((rest / p.n_tg) * p.n_tiles + nt) * p.t_tiles + ct % p.t_tiles : -1;
 }
 
+// Counter-based random numbers for drafting at temperature > 0: SplitMix64
+// (Steele, Lea and Flood, OOPSLA 2014).  A stream key folds (seed, purpose 1
+// = draft, request, round, block row); element v of the stream is
+// mix(key + (v+1) * golden); its top 23 bits give u = (bits + 1/2) * 2^-23 in
+// (0, 1), exact in float32, and the Gumbel variate -ln(-ln u).
+constexpr unsigned long long SM64_GOLD = 0x9E3779B97F4A7C15ull;
+DFL_DEV unsigned long long sm64_mix(unsigned long long z) {
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+DFL_DEV unsigned long long draft_stream_key(unsigned long long seed, int b, int rnd, int row) {
+  unsigned long long k = sm64_mix(seed + SM64_GOLD);
+  k = sm64_mix(k + SM64_GOLD * 2ull);  // purpose id 1: the drafter's draws
+  k = sm64_mix(k + SM64_GOLD * (unsigned long long)(b + 1));
+  k = sm64_mix(k + SM64_GOLD * (unsigned long long)(rnd + 1));
+  return sm64_mix(k + SM64_GOLD * (unsigned long long)(row + 1));
+}
+DFL_DEV float gumbel_at(unsigned long long key, int v) {
+  const unsigned long long bits = sm64_mix(key + SM64_GOLD * (unsigned long long)(v + 1));
+  const float u = ((float)(unsigned)(bits >> 41) + 0.5f) * 1.1920928955078125e-7f;  // 2^-23
+  return -logf(-logf(u));
+}
+
 // Timeline stamps (p.trace non-null): 0 entry, 1 set-up done, 2 first weight
 // stage landed, 3 last MMA issued, 4 epilogue done, 5 exit, 6 units, 7 SM id.
 DFL_DEV void trace_at(const GemmParams& p, int ev, unsigned long long v) {
@@ -293,7 +317,7 @@ DFL_DEV void gather_ctx(const GemmParams& p, int t_first, int j0, int ntok, int 
 template <int MODE>
 DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, const float* stg, int ew, int lane,
                        bool use_pre, const TokCtx& pre0, const TokCtx& pre1, const float* gq, const float* gk,
-                       bool use_hpre, const float (&hpre)[EPI_TOK][4]) {
+                       bool use_hpre, const float (&hpre)[EPI_TOK][4], int rnd) {
   const int tt_all = tile / p.t_tiles;       // (group, n-tile)
   const int group = tt_all / p.n_tiles;
   const int nt = tt_all % p.n_tiles;
@@ -375,6 +399,17 @@ DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, con
       }
     } else if (MODE == GM_ARGMAX) {
       const int n0 = nt * 128;
+      // temperature > 0: each drafting row draws from softmax(logit / T) by
+      // the Gumbel-max rule, on its own stream
+      const float tinv = p.temp_inv;
+      bool smp[EPI_TOK];
+      unsigned long long skey[EPI_TOK];
+#pragma unroll
+      for (int q = 0; q < EPI_TOK; ++q) {
+        const int row = tq[q] % DFL_BLOCK;
+        smp[q] = tinv > 0.f && row >= 1 && row < p.block;
+        skey[q] = smp[q] ? draft_stream_key(p.seed, tq[q] / DFL_BLOCK, rnd, row) : 0ull;
+      }
       unsigned long long best[EPI_TOK];
 #pragma unroll
       for (int q = 0; q < EPI_TOK; ++q) {
@@ -389,7 +424,8 @@ DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, con
               continue;
             }
             if (p.logits) p.logits[(size_t)tq[q] * p.N + n] = v;
-            const unsigned long long k = argmax_key(v, (uint32_t)n);
+            const float sc = smp[q] ? v * tinv + gumbel_at(skey[q], n) : v;
+            const unsigned long long k = argmax_key(sc, (uint32_t)n);
             best[q] = k > best[q] ? k : best[q];
           }
         }
@@ -684,6 +720,7 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
       load_head_gain(p.qn_gain, p.D, lane, gq);
       load_head_gain(p.kn_gain[0], p.D, lane, gk);
     }
+    const int rnd = (MODE == GM_ARGMAX && p.temp_inv > 0.f && p.round) ? *p.round : 0;
     if (MODE != GM_RESID && MODE != GM_FC && p.t_tiles == 1) {
       const int nt0 = p.M < 32 ? p.M : 32;  // the first chunk's tokens
       gather_ctx<MODE>(p, 0, ew, nt0, lane, pre0);
@@ -821,7 +858,7 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
         }
         named_bar_sync(1, EPI_THREADS);
         epi_final<MODE>(p, (int)tile, t_base + tc0, (mt - tc0) < 32 ? (mt - tc0) : 32, stg, ew, lane, use_pre,
-                        pre0, pre1, gq, gk, use_hpre, hpre);
+                        pre0, pre1, gq, gk, use_hpre, hpre, rnd);
         named_bar_sync(1, EPI_THREADS);
       }
       if (!split) {

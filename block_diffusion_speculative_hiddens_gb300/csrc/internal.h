@@ -97,6 +97,9 @@ struct GemmParams {
   float* logits;             // optional [M][N] (N = vocab)
   int* draft;                // [batch][block-1]
   int block;                 // ARGMAX: block size S (drafts from rows 1..S-1); 16 rows per request either way
+  float temp_inv;            // ARGMAX: 1/temperature (0: greedy argmax)
+  unsigned long long seed;   // ARGMAX sampling: stream seed
+  const int* round;          // ARGMAX sampling: round index (device; null: 0)
   unsigned* done_ctr;
   // optional timeline: [grid][8] %globaltimer stamps per CTA (null: off)
   unsigned long long* trace;

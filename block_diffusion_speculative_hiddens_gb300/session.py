@@ -29,6 +29,16 @@ class RoundState:
         self.target = torch.zeros(batch, cfg.block, **i32)
         self.feats = torch.zeros(batch, cfg.block, cfg.n_fused * cfg.hidden, dtype=torch.bfloat16,
                                  device=dev)
+        self.temperature = 0.0     # 0: greedy drafts
+        self.seed = 0
+        self.round_ctr = None      # device int32 round index read by the sampling draft
+
+    def set_sampling(self, temperature: float, seed: int, round_ctr):
+        """Draw drafts from softmax(logits / temperature); round_ctr is a device
+        int32 the caller advances once per round (the stand-in verify does)."""
+        self.temperature = float(temperature)
+        self.seed = int(seed)
+        self.round_ctr = round_ctr
 
     def prefill(self, feats, n_new, stream=None):
         """Inject prompt features: feats [batch, rows, n_fused*H] bf16, n_new [batch] int32 (device)."""
@@ -38,7 +48,11 @@ class RoundState:
         self.d.fuse_inject(self.slots, self.feats, self.d.cfg.block, self.accept_len, stream)
 
     def draft_block(self, stream=None):
-        self.d.draft_block(self.slots, self.bonus, self.draft, stream)
+        if self.temperature > 0:
+            self.d.draft_block_sample(self.slots, self.bonus, self.temperature, self.seed, self.round_ctr,
+                                      self.draft, None, stream)
+        else:
+            self.d.draft_block(self.slots, self.bonus, self.draft, stream)
 
     def draft_round(self, stream=None):
         """inject + draft_block as one call (injection folded into each layer's QKV GEMM)."""

@@ -249,6 +249,26 @@ DFLASH_API int dflash_draft_block_debug(dflash_handle* h, const int32_t* slots, 
                              const int32_t* last_tok, int32_t* draft, float* hidden,
                              float* logits, void* stream);
 
+/* a3-a6 at temperature T > 0 ([Paper walkthrough] Results and [News summary]
+ * 用例与示例 report DFlash with sampling; [Code walkthrough] §三 第3步: the
+ * block is checked against the target's sampled tokens with the same
+ * longest-prefix rule, so dflash_accept_trim applies unchanged).  Exactly
+ * dflash_draft_block, except that block row i = 1..S-1 of request b draws its
+ * draft from softmax(logits / T) by the Gumbel-max rule,
+ * argmax_v(logit_v / T + g_v), g_v = -ln(-ln u_v) with u_v from the
+ * SplitMix64 stream (seed, 1, b, *round, i): element v is
+ * mix(key + (v+1) * 0x9E3779B97F4A7C15), u = ((bits >> 41) + 0.5) * 2^-23,
+ * where key folds seed then each id x as k = mix(k + 0x9E3779B97F4A7C15 * (x+1))
+ * starting from mix(seed + 0x9E3779B97F4A7C15) (mix: the SplitMix64
+ * finaliser).  temperature < 1e-6 (or 0) is the greedy argmax; negative or NaN
+ * is DFLASH_ERR_INVALID_ARG.  round: DEVICE int32 read by the kernels (null:
+ * round 0), so a captured round loop draws fresh numbers when the caller's
+ * counter advances.  logits: optional DEVICE float32 [batch, 16, V]
+ * receiving the unscaled logits of every block row (null: not stored). */
+DFLASH_API int dflash_draft_block_sample(dflash_handle* h, const int32_t* slots, int32_t batch,
+                                         const int32_t* last_tok, float temperature, uint64_t seed,
+                                         const int32_t* round, int32_t* draft, float* logits, void* stream);
+
 /* Kernel timing probe: the next n launches of kernel `kernel_id`
  * (DFLASH_KID_*) are bracketed by CUDA events recorded on the launching
  * stream (as event-record nodes when captured).  dflash_probe_read

@@ -8,6 +8,7 @@ import math
 import numpy as np
 
 import oracle as O
+import oracle.sampling_ref as SR
 from workload import (context_lengths, feature_rows, make_weights, match_stream)
 
 TOL_REL_L2 = 1e-2      # hidden states, logits, K/V
@@ -33,7 +34,7 @@ class GpuRun:
     """CUDA-path driver: prefill every request, then rounds with the stand-in verify."""
 
     def __init__(self, cfg, rounds: int, weights_np=None, batch_ids=None, prefill_chunk=4096,
-                 ctx=None, attn_impl: int = 0):
+                 ctx=None, attn_impl: int = 0, temperature: float = 0.0, seed: int = 0):
         import torch
         from block_diffusion_speculative_hiddens_gb300 import Drafter, weights_to_device
         from block_diffusion_speculative_hiddens_gb300.session import RoundState, SyntheticVerify
@@ -68,6 +69,8 @@ class GpuRun:
         self.offs = torch.from_numpy(u).to(dev)
         self.state = RoundState(self.d, B, first_token=cfg.first_token)
         self.verify = SyntheticVerify(self.state, self.match, self.offs, self.feat_stream)
+        if temperature > 0:
+            self.state.set_sampling(temperature, seed, self.verify.round_ctr)
 
     def prefill(self):
         import torch
@@ -93,7 +96,10 @@ class GpuRun:
             # the debug outputs always hold 16 rows per request (rows S..15 pad a smaller block)
             hidden = torch.empty(B * 16, cfg.hidden, dtype=torch.float32, device=self.dev)
             logits = torch.empty(B * 16, cfg.vocab, dtype=torch.float32, device=self.dev)
-            self.d.draft_block_debug(s.slots, s.bonus, s.draft, hidden, logits)
+            if s.temperature > 0:
+                self.d.draft_block_sample(s.slots, s.bonus, s.temperature, s.seed, s.round_ctr, s.draft, logits)
+            else:
+                self.d.draft_block_debug(s.slots, s.bonus, s.draft, hidden, logits)
             self.verify()
             s.accept()
             out["hidden"] = to_np(hidden).reshape(B, 16, cfg.hidden)[:, :cfg.block]
@@ -110,7 +116,10 @@ class GpuRun:
 # ---------------------------------------------------------------- oracle side
 
 class OracleRun:
-    def __init__(self, cfg, rounds: int, weights_np=None, batch_ids=None, ctx=None, cache=True):
+    def __init__(self, cfg, rounds: int, weights_np=None, batch_ids=None, ctx=None, cache=True,
+                 temperature: float = 0.0, seed: int = 0):
+        self.temperature = temperature
+        self.seed = seed
         self.cfg = cfg
         self.ids = list(range(cfg.batch)) if batch_ids is None else list(batch_ids)
         self.ctx0 = (context_lengths(cfg)[self.ids] if ctx is None else np.asarray(ctx)).astype(int)
@@ -134,7 +143,10 @@ class OracleRun:
             req = self.reqs[j]
             if self.pending[j]:
                 self.dr.fuse_inject(req, feature_rows(cfg, b, req.ctx_len, self.pending[j]))
-            o = self.dr.draft(req, self.last[j], want_logits=want_logits)
+            o = self.dr.draft(req, self.last[j], want_logits=want_logits or self.temperature > 0)
+            if self.temperature > 0:  # drafts drawn from softmax(logits / T); margins of the perturbed scores
+                o["draft"], o["margin"] = SR.sample_drafts(o["logits"], self.temperature, self.seed, j, self.r)
+                o["sampled"] = True
             t = O.synthetic_target(o["draft"], mm[j], uu[j], cfg.vocab)
             tau, bonus, conf = self.dr.accept_trim(req, o["draft"], t)
             o.update(target=t, tau=tau, bonus=bonus, ctx=conf)
@@ -150,7 +162,7 @@ def check_drafts(gpu_draft, o, margin=MARGIN):
     d = np.asarray(gpu_draft)
     strong = o["margin"] > margin
     assert np.array_equal(d[strong], o["draft"][strong]), (d, o["draft"], o["margin"])
-    if "logits" in o:
+    if "logits" in o and not o.get("sampled"):
         lg = o["logits"]
         top = lg.max(-1)
         got = lg[np.arange(len(d)), d]

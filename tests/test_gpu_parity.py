@@ -101,6 +101,61 @@ def test_batch16_round_matches_oracle(lib):
     assert g.d.read_status() == 0
 
 
+@pytest.mark.parametrize("T", [0.7, 1.5])
+@pytest.mark.parametrize("name", ["tiny-gains", "small-batch"])
+def test_sampled_drafts_match_oracle(lib, name, T):
+    """Temperature > 0: each draft is the Gumbel-max draw from softmax(logits / T).
+
+    The kernel's draw equals the host's Gumbel-max on the same kernel's logits
+    with the oracle's generator (an independent implementation of the same
+    published function) wherever the perturbed scores are not within float32
+    rounding of a tie, and the oracle's own draw wherever its perturbed
+    margin exceeds the logits' tolerance; acceptance stays bit-exact."""
+    import oracle.sampling_ref as SR
+    from tests.gpu_util import MARGIN
+    cfg = get_config(name)
+    w = make_weights(cfg)
+    g = GpuRun(cfg, 3, weights_np=w, temperature=T, seed=4321)
+    o = OracleRun(cfg, 3, weights_np=w, temperature=T, seed=4321)
+    g.prefill()
+    o.prefill()
+    differs = 0
+    for r in range(3):
+        go = g.round(debug=True)
+        oo = o.round(want_logits=True)
+        for j, od in enumerate(oo):
+            dh, mh = SR.sample_drafts(go["logits"][j, 1:].astype(np.float64), T, 4321, j, r)
+            sure = mh > 1e-3
+            assert np.array_equal(go["draft"][j][sure], dh[sure]), (r, j)
+            check_drafts(go["draft"][j], od, margin=MARGIN / T)
+            differs += int(np.sum(go["draft"][j] != np.argmax(go["logits"][j, 1:], -1)))
+            assert (go["tau"][j], go["bonus"][j], go["ctx"][j]) == (od["tau"], od["bonus"], od["ctx"]), (r, j)
+    assert differs > 0  # the draws are not the greedy argmax
+    assert g.d.read_status() == 0
+
+
+def test_sampling_temperature_edges(lib):
+    """T below 1e-6 is the greedy argmax; a negative or NaN T is refused."""
+    import torch
+    from block_diffusion_speculative_hiddens_gb300.binding import DflashError
+    cfg = get_config("tiny-gains")
+    w = make_weights(cfg)
+    a = GpuRun(cfg, 1, weights_np=w)
+    b = GpuRun(cfg, 1, weights_np=w)
+    a.prefill()
+    b.prefill()
+    da = a.round()["draft"]
+    s = b.state
+    rc = torch.zeros(1, dtype=torch.int32, device=b.dev)
+    s.inject()
+    b.d.draft_block_sample(s.slots, s.bonus, 1e-9, 7, rc, s.draft)
+    assert np.array_equal(to_np(s.draft).astype(np.int64), da)
+    for bad in (-0.5, float("nan")):
+        with pytest.raises(DflashError):
+            b.d.draft_block_sample(s.slots, s.bonus, bad, 7, rc, s.draft)
+    assert b.d.read_status() == 0
+
+
 # inference at blocks smaller than the trained 16: S-1 drafts, acceptance over S
 SMALLER_BLOCKS = ["tiny-b8", "small-batch-b10"]
 
