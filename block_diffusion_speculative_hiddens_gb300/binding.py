@@ -287,10 +287,10 @@ class Drafter:
 
     def plan(self) -> dict:
         """SMs, attention splits and page loop, GEMM cluster size chosen at create."""
-        v = (ctypes.c_int32 * 4)()
+        v = (ctypes.c_int32 * 5)()
         _check("dflash_plan", self.lib.dflash_plan(self.h, v))
         return {"sms": v[0], "attn_splits": v[1], "attn_impl": ["", "warp MMAs", "tcgen05"][v[2]],
-                "gemm_cluster": v[3]}
+                "gemm_cluster": v[3], "attn_merge": ["cluster", "global"][v[4]]}
 
     def harness_verify(self, slots, draft, match, offs, rounds_cap: int, round_ctr, target,
                        feat_stream=None, stream_rows: int = 0, feats_out=None, stream=None):

@@ -88,7 +88,9 @@ struct dflash_handle {
   int max_tok = 0;     // max_batch * block
   int max_pos = 0;     // max_pages_per_slot * page_size
   int attn_splits = 1;
-  bool attn_tc = false;  // tcgen05 attention page loop
+  bool attn_tc = false;      // tcgen05 attention page loop
+  bool attn_global = false;  // splits merged through global memory (no cluster)
+  float* attn_part = nullptr;
   int max_tiles = 0;
   // weights, copied into the workspace at create: matrices packed into
   // 128x64 blocks (f16, except the bf16 fusion projection), gains as fp32
@@ -180,6 +182,19 @@ int pick_attn_splits(const dflash_config& c, int num_sms) {
   return std::max(1, want);
 }
 
+// Split-KV count without a cluster: every CTA of one launch resident at once
+// (one per SM), at least 4 pages per split at full slot capacity, at most 32;
+// the splits' partials are then merged by a second kernel.
+#ifndef DFL_ATTN_GLOBAL
+#define DFL_ATTN_GLOBAL 1
+#endif
+int global_attn_splits(const dflash_config& c, int num_sms) {
+  const int pairs = c.max_batch * c.n_kv_heads;
+  int want = num_sms / pairs;
+  want = std::min(want, std::max(1, c.max_pages_per_slot / 4));
+  return std::max(1, std::min(want, 32));
+}
+
 // Lay out the workspace; with base == nullptr only sizes are computed.
 size_t carve(dflash_handle* h, const dflash_config& c, char* base, int num_sms) {
   Carve w;
@@ -241,6 +256,10 @@ size_t carve(dflash_handle* h, const dflash_config& c, char* base, int num_sms) 
   o->cg = w.take<f16>((size_t)R * H);
   o->ss_c = w.take<float>((size_t)(H / 128) * R);
   o->gemm_ws = w.take<float>((size_t)num_sms * 2 * DFL_BN_MAX * 128);
+  {
+    const int gs = DFL_ATTN_GLOBAL ? global_attn_splits(c, num_sms) : 1;
+    o->attn_part = gs > 1 ? w.take<float>((size_t)c.max_batch * hkv * gs * attn_part_floats(D)) : nullptr;
+  }
   o->tile_ctr = w.take<unsigned>(tiles);
   if (h) {
     h->attn_splits = splits;
@@ -498,6 +517,8 @@ int draft_impl(dflash_handle* h, const int32_t* slots, int32_t batch, const int3
       a.hkv = hkv;
       a.D = D;
       a.n_splits = h->attn_splits;
+      a.merge_global = h->attn_global ? 1 : 0;
+      a.part = h->attn_part;
       a.block = c.block;
       a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
       a.status = h->status;
@@ -669,6 +690,20 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
          attn_max_active_clusters(c.head_dim, c.n_q_heads, c.n_kv_heads, h->attn_splits, h->attn_tc) <
              c.max_batch * c.n_kv_heads)
     --h->attn_splits;
+  // more splits than clusters allow, each still holding 32+ pages at full
+  // slot capacity: merge them through global memory instead (measured on
+  // GB300: 9 splits of ~57 pages beat 6 clusters of ~86 by 83 us per
+  // long-context round; 19 splits of ~8 pages lost 45 us to 12 clusters of
+  // ~12 on the Llama-3.1-8B shape -- the second kernel and the per-CTA set-up
+  // outweigh the shorter page loops)
+  if (!rc && h->attn_part) {
+    const int gs = global_attn_splits(c, sms);
+    if (gs > h->attn_splits && ceil_div(c.max_pages_per_slot, gs) >= 32) {
+      h->attn_global = true;
+      h->attn_splits = gs;
+      h->attn_tc = c.attn_impl == 2 || (c.attn_impl == 0 && ceil_div(c.max_pages_per_slot, gs) >= 8);
+    }
+  }
   if (!rc)
     rc = cuda_err(cudaMemset(h->page_table, 0xFF, (size_t)c.max_slots * c.max_pages_per_slot * sizeof(int)));
   if (!rc) rc = cuda_err(launch_pool_init(h->free_stack, h->free_top, c.max_pages, 0));
@@ -939,12 +974,13 @@ int dflash_marks_read(dflash_handle* h, float* ms_out, int32_t cap, int32_t* n_o
 
 uint64_t dflash_launch_count(dflash_handle* h) { return h ? h->launches : 0; }
 
-int dflash_plan(dflash_handle* h, int32_t* out4) {
-  if (!h || !out4) return DFLASH_ERR_INVALID_ARG;
-  out4[0] = h->num_sms;
-  out4[1] = h->attn_splits;
-  out4[2] = h->attn_tc ? 2 : 1;
-  out4[3] = h->gemm_cl;
+int dflash_plan(dflash_handle* h, int32_t* out5) {
+  if (!h || !out5) return DFLASH_ERR_INVALID_ARG;
+  out5[0] = h->num_sms;
+  out5[1] = h->attn_splits;
+  out5[2] = h->attn_tc ? 2 : 1;
+  out5[3] = h->gemm_cl;
+  out5[4] = h->attn_global ? 1 : 0;
   return DFLASH_OK;
 }
 

@@ -43,6 +43,65 @@ DFL_DEV void atrace(const AttnParams& p, int ev) {
   }
 }
 
+// A split's partial (nf floats from shared memory) to its global slot.
+DFL_DEV void copy_partial(const AttnParams& p, const float* part, int nf, int slot, int D) {
+  float* dst = p.part + (size_t)slot * attn_part_floats(D);
+  for (int i = 4 * (int)threadIdx.x; i < nf; i += 4 * (int)blockDim.x)
+    *reinterpret_cast<float4*>(dst + i) = *reinterpret_cast<const float4*>(part + i);
+}
+
+// Combines the splits' partials of each (request, KV head): one CTA per 16
+// rows (one query head's block tokens), 8 threads per row, each taking D/8
+// output columns; max, sum and weight of every split per row, then the
+// weighted sum of the splits' unnormalised outputs in split order.
+template <int D>
+__global__ void __launch_bounds__(128) k_attn_merge(const AttnParams p) {
+  constexpr int PS = D + 4;
+  constexpr int PF = attn_part_floats(D);
+  constexpr int DC = D / 8;  // columns per thread
+  pdl_launch_dependents();
+  pdl_wait();
+  const int pair = blockIdx.x;
+  const int b = pair / p.hkv, kvh = pair % p.hkv;
+  const int G = p.hq / p.hkv, rows = G * 16;
+  const int r = blockIdx.y * 16 + ((int)threadIdx.x >> 3);
+  const int d0 = ((int)threadIdx.x & 7) * DC;
+  if (r >= rows) return;
+  const int nsp = p.n_splits;
+  const float* base = p.part + (size_t)pair * nsp * PF;
+  float M = -INFINITY;
+  for (int sp = 0; sp < nsp; ++sp) {
+    const float l = base[(size_t)sp * PF + rows * PS + rows + r];
+    if (l > 0.f) M = fmaxf(M, base[(size_t)sp * PF + rows * PS + r]);
+  }
+  float acc[DC];
+#pragma unroll
+  for (int c = 0; c < DC; ++c) acc[c] = 0.f;
+  float L = 0.f;
+  for (int sp = 0; sp < nsp; ++sp) {
+    const float* sb = base + (size_t)sp * PF;
+    const float l = sb[rows * PS + rows + r];
+    const float w = l > 0.f ? exp2f(sb[rows * PS + r] - M) : 0.f;
+    L += w * l;
+#pragma unroll
+    for (int c = 0; c < DC; c += 4) {
+      const float4 v = *reinterpret_cast<const float4*>(sb + r * PS + d0 + c);
+      acc[c] += w * v.x;
+      acc[c + 1] += w * v.y;
+      acc[c + 2] += w * v.z;
+      acc[c + 3] += w * v.w;
+    }
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  const int h = r / 16, t = r % 16;
+  f16* dst = p.out + ((size_t)(b * DFL_BLOCK + t) * p.hq + kvh * G + h) * D + d0;
+#pragma unroll
+  for (int c = 0; c < DC; c += 8)
+    *reinterpret_cast<uint4*>(dst + c) =
+        make_uint4(pack_f16x2(acc[c] * inv, acc[c + 1] * inv), pack_f16x2(acc[c + 2] * inv, acc[c + 3] * inv),
+                   pack_f16x2(acc[c + 4] * inv, acc[c + 5] * inv), pack_f16x2(acc[c + 6] * inv, acc[c + 7] * inv));
+}
+
 // KS warps per query head split every page's 64 keys between them (KS = 2
 // for G <= 4), each with its own online softmax, merged in shared memory at
 // the end: twice the warps in flight and half the dependent MMA chain per
@@ -322,6 +381,12 @@ __global__ void __launch_bounds__(G * KS * 32) k_attn(const AttnParams p) {
     }
   }
   if (threadIdx.x == 0) atrace(p, 4);
+  if (p.merge_global) {  // the partial goes to global memory; k_attn_merge combines the splits
+    __syncthreads();
+    copy_partial(p, part, rows * PS + 2 * rows, (b * hkv + kvh) * p.n_splits + split, D);
+    if (threadIdx.x == 0) atrace(p, 5);
+    return;
+  }
   cluster_sync_all();
 
   const int n = p.n_splits;
@@ -731,6 +796,12 @@ __global__ void __launch_bounds__(320, 1) k_attn_tc(const AttnParams p) {
     }
   }
   if (threadIdx.x == 0) atrace(p, 4);
+  if (p.merge_global) {  // the partial goes to global memory; k_attn_merge combines the splits
+    __syncthreads();
+    copy_partial(p, part, rows * PS + 2 * rows, (b * hkv + kvh) * p.n_splits + split, D);
+    if (threadIdx.x == 0) atrace(p, 5);
+    return;
+  }
   cluster_sync_all();
 
   const int nsp = p.n_splits;
@@ -817,15 +888,30 @@ cudaError_t launch_t(const AttnParams& p, int batch, cudaStream_t s, bool pdl) {
   cfg.dynamicSmemBytes = AttnKernel<D, G, TC>::smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;  // the splits of one KV head
-  attr[0].val.clusterDim.x = (unsigned)p.n_splits;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  int na = 0;
+  if (!p.merge_global) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;  // the splits of one KV head
+    attr[na].val.clusterDim.x = (unsigned)p.n_splits;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, AttnKernel<D, G, TC>::fn, p);
+  cfg.numAttrs = (unsigned)na;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, AttnKernel<D, G, TC>::fn, p);
+  if (e || !p.merge_global || p.n_splits == 1) return e;
+  cudaLaunchConfig_t mc = {};
+  mc.gridDim = dim3((unsigned)(batch * p.hkv), (unsigned)G);  // 16 rows per CTA
+  mc.blockDim = dim3(128);
+  mc.stream = s;
+  mc.attrs = attr + na - (pdl ? 1 : 0);
+  mc.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&mc, k_attn_merge<D>, p);
 }
 
 template <int D, bool TC>

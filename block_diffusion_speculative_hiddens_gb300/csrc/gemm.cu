@@ -35,6 +35,9 @@
 #ifndef DFL_GEMM_L2_HINT
 #define DFL_GEMM_L2_HINT 1
 #endif
+#ifndef DFL_GEMM_SAMPLING  // 0 compiles the lm_head's temperature > 0 draw out
+#define DFL_GEMM_SAMPLING 1
+#endif
 #ifndef DFL_GEMM_RED_MAX  // most split-K part chunks (8 KB) landed at once outside the last segment
 #define DFL_GEMM_RED_MAX 16
 #endif
@@ -85,7 +88,9 @@ DFL_DEV unsigned long long draft_stream_key(unsigned long long seed, int b, int 
   k = sm64_mix(k + SM64_GOLD * (unsigned long long)(rnd + 1));
   return sm64_mix(k + SM64_GOLD * (unsigned long long)(row + 1));
 }
-DFL_DEV float gumbel_at(unsigned long long key, int v) {
+// Out of line: the greedy epilogue, run once per vocabulary tile, keeps its
+// compact code (the instruction cache holds it across tiles).
+__device__ __noinline__ float gumbel_at(unsigned long long key, int v) {
   const unsigned long long bits = sm64_mix(key + SM64_GOLD * (unsigned long long)(v + 1));
   const float u = ((float)(unsigned)(bits >> 41) + 0.5f) * 1.1920928955078125e-7f;  // 2^-23
   return -logf(-logf(u));
@@ -399,34 +404,51 @@ DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, con
       }
     } else if (MODE == GM_ARGMAX) {
       const int n0 = nt * 128;
-      // temperature > 0: each drafting row draws from softmax(logit / T) by
-      // the Gumbel-max rule, on its own stream
-      const float tinv = p.temp_inv;
-      bool smp[EPI_TOK];
-      unsigned long long skey[EPI_TOK];
-#pragma unroll
-      for (int q = 0; q < EPI_TOK; ++q) {
-        const int row = tq[q] % DFL_BLOCK;
-        smp[q] = tinv > 0.f && row >= 1 && row < p.block;
-        skey[q] = smp[q] ? draft_stream_key(p.seed, tq[q] / DFL_BLOCK, rnd, row) : 0ull;
-      }
       unsigned long long best[EPI_TOK];
+      if (DFL_GEMM_SAMPLING && p.temp_inv > 0.f) {
+        // temperature > 0: each drafting row draws from softmax(logit / T) by
+        // the Gumbel-max rule, on its own stream (a separate loop, so the
+        // greedy one below keeps its compact code)
+        const float tinv = p.temp_inv;
 #pragma unroll
-      for (int q = 0; q < EPI_TOK; ++q) {
-        best[q] = 0ull;
+        for (int q = 0; q < EPI_TOK; ++q) {
+          best[q] = 0ull;
+          const int row = tq[q] % DFL_BLOCK;
+          const bool smp = row >= 1 && row < p.block;
+          const unsigned long long skey = smp ? draft_stream_key(p.seed, tq[q] / DFL_BLOCK, rnd, row) : 0ull;
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const int n = n0 + lane + 32 * jj;
-          if (ok[q] && n < p.N) {
-            const float v = x[q][jj] * s[q];
-            if (v != v) {
-              dev_error(p.status, DFLASH_DEV_NAN);
-              continue;
+          for (int jj = 0; jj < 4; ++jj) {
+            const int n = n0 + lane + 32 * jj;
+            if (ok[q] && n < p.N) {
+              const float v = x[q][jj] * s[q];
+              if (v != v) {
+                dev_error(p.status, DFLASH_DEV_NAN);
+                continue;
+              }
+              if (p.logits) p.logits[(size_t)tq[q] * p.N + n] = v;
+              const float sc = smp ? v * tinv + gumbel_at(skey, n) : v;
+              const unsigned long long k = argmax_key(sc, (uint32_t)n);
+              best[q] = k > best[q] ? k : best[q];
             }
-            if (p.logits) p.logits[(size_t)tq[q] * p.N + n] = v;
-            const float sc = smp[q] ? v * tinv + gumbel_at(skey[q], n) : v;
-            const unsigned long long k = argmax_key(sc, (uint32_t)n);
-            best[q] = k > best[q] ? k : best[q];
+          }
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < EPI_TOK; ++q) {
+          best[q] = 0ull;
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            const int n = n0 + lane + 32 * jj;
+            if (ok[q] && n < p.N) {
+              const float v = x[q][jj] * s[q];
+              if (v != v) {
+                dev_error(p.status, DFLASH_DEV_NAN);
+                continue;
+              }
+              if (p.logits) p.logits[(size_t)tq[q] * p.N + n] = v;
+              const unsigned long long k = argmax_key(v, (uint32_t)n);
+              best[q] = k > best[q] ? k : best[q];
+            }
           }
         }
       }

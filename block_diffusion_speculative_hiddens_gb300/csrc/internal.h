@@ -117,7 +117,9 @@ struct AttnParams {
   const int* slots;
   const int* ctx_len;  // keys = ctx_len + block (block K/V already in the cache)
   int hq, hkv, D;
-  int n_splits;        // CTAs per (request, KV head): one cluster, <= 16
+  int n_splits;        // CTAs per (request, KV head): one cluster (<= 16), or any count with merge_global
+  int merge_global;    // 1: splits write partials to `part`, k_attn_merge combines them (no cluster)
+  float* part;         // [batch * hkv][n_splits][attn_part_floats(D)] partials (merge_global)
   int block;           // block size S: keys = context + S (rows S..15 of a request are padding)
   float scale_log2;    // log2(e) / sqrt(D)
   uint32_t* status;
@@ -132,6 +134,10 @@ cudaError_t gemm_launch(const CUtensorMap& B, const GemmParams& p, int grid, cud
 // Clusters of `cl` GEMM CTAs (token tile BN, `stages` ring) the GPU holds at once.
 int gemm_max_clusters(int BN, int stages, int cl);
 cudaError_t gemm_init_attributes();
+
+// Floats of one split's partial: [128 rows][D + 4] unnormalised O, then the
+// rows' running maxima and sums.
+constexpr int attn_part_floats(int D) { return 128 * (D + 4) + 2 * 128; }
 
 // Attention clusters of `splits` CTAs the GPU can hold at once (0: cannot
 // launch); tc selects the tcgen05 page loop, else the warp-MMA one.

@@ -310,10 +310,14 @@ DFLASH_API int dflash_trace_arm(dflash_handle* h, int32_t kernel_id, unsigned lo
 DFLASH_API uint64_t dflash_launch_count(dflash_handle* h);
 
 /* How the handle runs its kernels on this GPU, fixed at dflash_create:
- * out[0] SMs, out[1] attention splits per (request, KV head) (one cluster),
- * out[2] attention page loop (1 warp MMAs, 2 tcgen05), out[3] CTAs per
- * cluster sharing a GEMM token tile of 128+ tokens (1: none).  Host only. */
-DFLASH_API int dflash_plan(dflash_handle* h, int32_t* out4);
+ * out[0] SMs, out[1] attention splits per (request, KV head), out[2]
+ * attention page loop (1 warp MMAs, 2 tcgen05), out[3] CTAs per cluster
+ * sharing a GEMM token tile of 128+ tokens (1: none), out[4] how the
+ * attention splits are merged (0: one thread-block cluster per request and KV
+ * head, over distributed shared memory; 1: through global memory by a second
+ * kernel, when that allows more splits than clusters fit at once).  out:
+ * HOST int32[5].  Host only. */
+DFLASH_API int dflash_plan(dflash_handle* h, int32_t* out5);
 
 /* ---- benchmark harness: stand-in for the target's verify step -----------
  * Not part of the method.  For round r = (*round_ctr)++ it builds the

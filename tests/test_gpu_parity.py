@@ -101,6 +101,26 @@ def test_batch16_round_matches_oracle(lib):
     assert g.d.read_status() == 0
 
 
+@pytest.mark.parametrize("attn_impl", ATTN)
+def test_global_merge_round_matches_oracle(lib, attn_impl):
+    """More attention splits than clusters fit at once: the splits' partials
+    are merged through global memory by a second kernel."""
+    cfg, g, o = _pair("small-long", 2, attn_impl=attn_impl)
+    plan = g.d.plan()
+    if plan["attn_merge"] != "global" and attn_impl == 1:
+        pytest.skip(f"the warp-MMA page loop's clusters all fit at once here: {plan}")
+    assert plan["attn_merge"] == "global" and plan["attn_splits"] > 1, plan
+    for r in range(2):
+        go = g.round(debug=True)
+        oo = o.round(want_logits=True)
+        for j, od in enumerate(oo):
+            assert rel_l2(go["hidden"][j], od["hidden"]) < TOL_REL_L2, (r, j)
+            assert rel_l2(go["logits"][j, 1:], od["logits"]) < TOL_REL_L2, (r, j)
+            check_drafts(go["draft"][j], od)
+            assert (go["tau"][j], go["bonus"][j], go["ctx"][j]) == (od["tau"], od["bonus"], od["ctx"]), (r, j)
+    assert g.d.read_status() == 0
+
+
 @pytest.mark.parametrize("T", [0.7, 1.5])
 @pytest.mark.parametrize("name", ["tiny-gains", "small-batch"])
 def test_sampled_drafts_match_oracle(lib, name, T):

@@ -115,6 +115,13 @@ TEST_CONFIGS = {
         intermediate=768, n_layers=2, vocab=5000, rope_theta=5e5, batch=16, ctx0=None,
         rounds=3, match_p=None, ctx_range=(30, 200), p_range=(0.5, 0.95), gain_std=0.1,
         weight_std=0.05),
+    # 16 (request, KV head) pairs over ~290 pages each: more attention splits
+    # than thread-block clusters fit at once, each holding 32+ pages, so they
+    # merge through global memory.
+    "small-long": DraftConfig(
+        name="small-long", hidden=512, n_q_heads=8, n_kv_heads=4, head_dim=128,
+        intermediate=768, n_layers=2, vocab=5000, rope_theta=1e6, batch=4, ctx0=18500,
+        rounds=3, match_p=0.85, gain_std=0.1, weight_std=0.05),
     # Inference at blocks smaller than the trained 16 (S-1 drafts per round).
     "tiny-b8": CONFIGS["tiny"].with_(name="tiny-b8", block=8, gain_std=0.1, weight_std=0.05),
     "small-batch-b10": DraftConfig(
