@@ -32,7 +32,8 @@ class DflashConfig(ctypes.Structure):
         "n_fused", "block", "mask_id", "page_size", "max_batch", "max_slots", "max_pages",
         "max_pages_per_slot", "max_rows", "device")] + [("rms_eps", ctypes.c_float),
                                                          ("rope_theta", ctypes.c_float),
-                                                         ("attn_impl", ctypes.c_int32)]
+                                                         ("attn_impl", ctypes.c_int32),
+                                                         ("role", ctypes.c_int32)]
 
 
 class DflashWeights(ctypes.Structure):
@@ -77,6 +78,8 @@ _SIGS = {
     "dflash_marks_read": (ctypes.c_int, [_vp, _vp, ctypes.c_int32, _vp]),
     "dflash_launch_count": (ctypes.c_uint64, [_vp]),
     "dflash_plan": (ctypes.c_int, [_vp, _vp]),
+    "dflash_verify_block": (ctypes.c_int, [_vp, _vp, ctypes.c_int32, _vp, _vp, _vp, _vp, _vp]),
+    "dflash_advance": (ctypes.c_int, [_vp, _vp, ctypes.c_int32, _vp, _vp]),
     "dflash_trace_arm": (ctypes.c_int, [_vp, ctypes.c_int32, _vp, ctypes.c_int32]),
     "dflash_harness_verify": (ctypes.c_int, [_vp, _vp, ctypes.c_int32, _vp, _vp, _vp, ctypes.c_int32, _vp,
                                              _vp, _vp, ctypes.c_int32, _vp, _vp]),
@@ -132,25 +135,27 @@ class Drafter:
     """
 
     def __init__(self, cfg, weights: dict, *, max_batch: int, max_slots: int, max_pages: int,
-                 max_pages_per_slot: int, max_rows: int, device: int = 0, attn_impl: int = 0):
+                 max_pages_per_slot: int, max_rows: int, device: int = 0, attn_impl: int = 0, role: int = 0):
         import torch
         self.lib = load()
         self.cfg = cfg
         self.device = device
         self.w = weights
+        self.role = role
+        L = len(weights["layers"]) if role == 1 else cfg.n_layers
+        self.n_layers = L
         c = DflashConfig(hidden=cfg.hidden, n_q_heads=cfg.n_q_heads, n_kv_heads=cfg.n_kv_heads,
-                         head_dim=cfg.head_dim, intermediate=cfg.intermediate, n_layers=cfg.n_layers,
+                         head_dim=cfg.head_dim, intermediate=cfg.intermediate, n_layers=L,
                          vocab=cfg.vocab, n_fused=cfg.n_fused, block=cfg.block, mask_id=cfg.mask_id,
                          page_size=cfg.page_size, max_batch=max_batch, max_slots=max_slots,
                          max_pages=max_pages, max_pages_per_slot=max_pages_per_slot,
                          max_rows=max_rows, device=device, rms_eps=cfg.rms_eps,
-                         rope_theta=cfg.rope_theta, attn_impl=attn_impl)
+                         rope_theta=cfg.rope_theta, attn_impl=attn_impl, role=role)
         self.c = c
         nbytes = self.lib.dflash_workspace_bytes(ctypes.byref(c))
         if nbytes == 0:
             raise DflashError("dflash_workspace_bytes", 2)
         self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=f"cuda:{device}")
-        L = cfg.n_layers
 
         def arr(name):
             a = (_vp * L)(*[weights["layers"][l][name].data_ptr() for l in range(L)])
@@ -158,8 +163,8 @@ class Drafter:
 
         self._arrays = {n: arr(n) for n in ("in_norm", "wqkv", "q_norm", "k_norm", "wo", "post_norm",
                                             "w_gate_up", "w_down")}
-        wts = DflashWeights(embed=weights["embed"].data_ptr(), fc=weights["fc"].data_ptr(),
-                            fc_norm=weights["fc_norm"].data_ptr(),
+        opt = lambda n: weights[n].data_ptr() if n in weights else None  # noqa: E731  (no fusion in a target)
+        wts = DflashWeights(embed=weights["embed"].data_ptr(), fc=opt("fc"), fc_norm=opt("fc_norm"),
                             final_norm=weights["final_norm"].data_ptr(),
                             **{n: ctypes.cast(a, ctypes.POINTER(_vp)) for n, a in self._arrays.items()})
         h = _vp()
@@ -211,6 +216,18 @@ class Drafter:
         _check("dflash_draft_block_sample", self.lib.dflash_draft_block_sample(
             self.h, _ptr(slots), slots.numel(), _ptr(last_tok), float(temperature), int(seed) & ((1 << 64) - 1),
             _ptr(round_ctr), _ptr(draft), _ptr(logits), _stream(stream)))
+
+    # ---- target model (role 1)
+    def verify_block(self, slots, tokens, out_tok, n_valid=None, feats=None, stream=None):
+        """Target forward over block tokens [batch, 16] -> out_tok [batch, 16] (+ feats [batch, 16, 5H])."""
+        _check("dflash_verify_block", self.lib.dflash_verify_block(
+            self.h, _ptr(slots), slots.numel(), _ptr(tokens), _ptr(n_valid), _ptr(out_tok), _ptr(feats),
+            _stream(stream)))
+
+    def advance(self, slots, n, stream=None):
+        """ctx_len[slot] += n[b] (the trim after acceptance / a prefill chunk's step)."""
+        _check("dflash_advance", self.lib.dflash_advance(self.h, _ptr(slots), slots.numel(), _ptr(n),
+                                                          _stream(stream)))
 
     def accept_trim(self, slots, draft, target, accept_len, bonus, ctx_len, stream=None):
         _check("dflash_accept_trim", self.lib.dflash_accept_trim(

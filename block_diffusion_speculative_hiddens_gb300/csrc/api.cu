@@ -163,8 +163,15 @@ bool cfg_valid(const dflash_config* c) {
   if (c->mask_id < 0 || c->mask_id >= c->vocab) return false;
   if (!(c->rms_eps > 0.f) || !(c->rope_theta > 1.f)) return false;
   if (c->attn_impl < 0 || c->attn_impl > 2) return false;
+  if (c->role != 0 && c->role != 1) return false;
+  // a target: full 16-token blocks, and 5 distinct middle layers to tap
+  if (c->role == 1 && (c->block != DFL_BLOCK || c->n_layers < c->n_fused + 2)) return false;
   return true;
 }
+
+// Target layers whose outputs are the drafter's features, shallow to deep:
+// layers 1..L-2 evenly spread (round half up of k(L-3)/(n-1)).
+int tap_layer(int k, int L, int n) { return 1 + (2 * k * (L - 3) + (n - 1)) / (2 * (n - 1)); }
 
 #ifndef DFL_ATTN_MAX_SPLITS
 #define DFL_ATTN_MAX_SPLITS 16
@@ -417,12 +424,21 @@ struct Sampling {
   const int32_t* round = nullptr;
 };
 
+// A target model's verify pass: the block's real tokens, its live rows,
+// the fused-feature taps and every row's token.
+struct Verify {
+  const int32_t* tokens = nullptr;   // [batch][16]
+  const int32_t* n_valid = nullptr;  // [batch] (null: 16)
+  bf16* feats = nullptr;             // [batch][16][n_fused][H] (null: not written)
+};
+
 int draft_impl(dflash_handle* h, const int32_t* slots, int32_t batch, const int32_t* last_tok, int32_t* draft,
                float* hidden, float* logits, void* stream, const void* feats = nullptr, int rows_per_req = 0,
-               const int32_t* n_new = nullptr, Sampling smp = Sampling()) {
+               const int32_t* n_new = nullptr, Sampling smp = Sampling(), Verify vf = Verify()) {
   if (!h || batch < 0 || batch > h->cfg.max_batch) return DFLASH_ERR_INVALID_ARG;
   if (batch == 0) return DFLASH_OK;
-  if (!slots || !last_tok || !draft) return DFLASH_ERR_INVALID_ARG;
+  const bool target = vf.tokens != nullptr;
+  if (!slots || (!last_tok && !target) || !draft) return DFLASH_ERR_INVALID_ARG;
   if (cudaSetDevice(h->cfg.device) != cudaSuccess) return DFLASH_ERR_CUDA;
   cudaStream_t s = (cudaStream_t)stream;
   const dflash_config& c = h->cfg;
@@ -457,6 +473,13 @@ int draft_impl(dflash_handle* h, const int32_t* slots, int32_t batch, const int3
     if (rc) return rc;
   }
 
+  if (target) {  // pages for the block's positions (the context length moves with dflash_advance)
+    h->launches++;
+    rc = cuda_err(launch_page_alloc(slots, batch, DFL_BLOCK, nullptr, DFL_BLOCK, h->ctx_len, h->pos0, h->n_pages,
+                                    h->page_table, c.max_pages_per_slot, h->free_stack, h->free_top, h->n_eff,
+                                    h->slots_ok, c.max_slots, h->status, s));
+    if (rc) return rc;
+  }
   h->launches++;
   BlockCtx bcx;
   bcx.ctx_len = h->ctx_len;
@@ -468,6 +491,8 @@ int draft_impl(dflash_handle* h, const int32_t* slots, int32_t batch, const int3
   bcx.max_pos = h->max_pos;
   bcx.block = c.block;
   bcx.bctx = h->bctx;
+  bcx.tokens = vf.tokens;
+  bcx.n_valid = vf.n_valid;
   bcx.slots_ok = h->slots_ok;
   bcx.max_slots = c.max_slots;
   bcx.brope = h->brope;
@@ -520,6 +545,8 @@ int draft_impl(dflash_handle* h, const int32_t* slots, int32_t batch, const int3
       a.merge_global = h->attn_global ? 1 : 0;
       a.part = h->attn_part;
       a.block = c.block;
+      a.causal = target ? 1 : 0;
+      a.n_valid = vf.n_valid;
       a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
       a.status = h->status;
       if (h->trace.kid == DFLASH_KID_ATTENTION && h->trace.buf &&
@@ -564,6 +591,14 @@ int draft_impl(dflash_handle* h, const int32_t* slots, int32_t batch, const int3
       rc = run_gemm(h, s, GM_RESID, &a, 1, 0, H / 128, I, h->tm_act, M, p, true, 0, DFLASH_KID_DOWN);
       if (rc) return rc;
     }
+    if (vf.feats) {  // this layer's output is one of the drafter's fused features
+      for (int k = 0; k < c.n_fused; ++k)
+        if (tap_layer(k, c.n_layers, c.n_fused) == l) {
+          h->launches++;
+          rc = cuda_err(launch_tap(h->h, M, H, vf.feats, k, c.n_fused, s));
+          if (rc) return rc;
+        }
+    }
   }
   if (hidden) {
     rc = cuda_err(cudaMemcpyAsync(hidden, h->h, (size_t)M * H * sizeof(float), cudaMemcpyDeviceToDevice, s));
@@ -578,6 +613,7 @@ int draft_impl(dflash_handle* h, const int32_t* slots, int32_t batch, const int3
     p.logits = logits;
     p.draft = draft;
     p.block = c.block;
+    p.row0 = target ? 0 : 1;
     p.temp_inv = smp.temp_inv;
     p.seed = smp.seed;
     p.round = smp.round;
@@ -619,8 +655,9 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
   if (!out) return DFLASH_ERR_INVALID_ARG;
   *out = nullptr;
   if (!cfg_valid(cfg)) return DFLASH_ERR_SHAPE;
-  if (!w || !w->embed || !w->fc || !w->fc_norm || !w->final_norm || !w->in_norm || !w->wqkv || !w->q_norm ||
-      !w->k_norm || !w->wo || !w->post_norm || !w->w_gate_up || !w->w_down)
+  const bool drafter = cfg->role == 0;  // a target has no fusion weights
+  if (!w || !w->embed || (drafter && (!w->fc || !w->fc_norm)) || !w->final_norm || !w->in_norm || !w->wqkv ||
+      !w->q_norm || !w->k_norm || !w->wo || !w->post_norm || !w->w_gate_up || !w->w_down)
     return DFLASH_ERR_INVALID_ARG;
   for (int l = 0; l < cfg->n_layers; ++l)
     if (!w->in_norm[l] || !w->wqkv[l] || !w->q_norm[l] || !w->k_norm[l] || !w->wo[l] || !w->post_norm[l] ||
@@ -646,8 +683,8 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
   const int H = c.hidden, D = c.head_dim, hq = c.n_q_heads, hkv = c.n_kv_heads, I = c.intermediate;
   auto B16 = [](const void* p) { return static_cast<const bf16*>(p); };
   cudaError_t e = launch_pack_weight(B16(w->embed), h->embed_pk, c.vocab, H, ceil_div(c.vocab, 128), 0, true, 0);
-  if (!e) e = launch_pack_weight(B16(w->fc), h->fc_pk, H, c.n_fused * H, H / 128, 0, false, 0);
-  if (!e) e = launch_gain_f32(B16(w->fc_norm), h->fc_norm, H, 0);
+  if (!e && drafter) e = launch_pack_weight(B16(w->fc), h->fc_pk, H, c.n_fused * H, H / 128, 0, false, 0);
+  if (!e && drafter) e = launch_gain_f32(B16(w->fc_norm), h->fc_norm, H, 0);
   if (!e) e = launch_gain_f32(B16(w->final_norm), h->final_norm, H, 0);
   for (int l = 0; l < c.n_layers && !e; ++l) {
     e = launch_pack_weight(B16(w->wqkv[l]), h->wqkv_pk[l], (hq + 2 * hkv) * D, H, (hq + 2 * hkv) * D / 128, 0, true,
@@ -805,6 +842,28 @@ int dflash_draft_round(dflash_handle* h, const int32_t* slots, int32_t batch, co
 int dflash_draft_block_debug(dflash_handle* h, const int32_t* slots, int32_t batch, const int32_t* last_tok,
                              int32_t* draft, float* hidden, float* logits, void* stream) {
   return draft_impl(h, slots, batch, last_tok, draft, hidden, logits, stream);
+}
+
+int dflash_verify_block(dflash_handle* h, const int32_t* slots, int32_t batch, const int32_t* tokens,
+                        const int32_t* n_valid, int32_t* out_tok, void* feats, void* stream) {
+  if (!h || h->cfg.role != 1 || !tokens || !out_tok) return DFLASH_ERR_INVALID_ARG;
+  Verify vf;
+  vf.tokens = tokens;
+  vf.n_valid = n_valid;
+  vf.feats = static_cast<bf16*>(feats);
+  return draft_impl(h, slots, batch, nullptr, out_tok, nullptr, nullptr, stream, nullptr, 0, nullptr, Sampling(), vf);
+}
+
+int dflash_advance(dflash_handle* h, const int32_t* slots, int32_t batch, const int32_t* n, void* stream) {
+  if (!h || batch < 0 || batch > h->cfg.max_batch) return DFLASH_ERR_INVALID_ARG;
+  if (batch == 0) return DFLASH_OK;
+  if (!slots || !n) return DFLASH_ERR_INVALID_ARG;
+  if (cudaSetDevice(h->cfg.device) != cudaSuccess) return DFLASH_ERR_CUDA;
+  const dflash_config& c = h->cfg;
+  h->launches++;
+  return cuda_err(launch_page_alloc(slots, batch, DFL_BLOCK, n, DFL_BLOCK, h->ctx_len, h->pos0, h->n_pages,
+                                    h->page_table, c.max_pages_per_slot, h->free_stack, h->free_top, h->n_eff,
+                                    h->slots_ok, c.max_slots, h->status, (cudaStream_t)stream));
 }
 
 int dflash_draft_block_sample(dflash_handle* h, const int32_t* slots, int32_t batch, const int32_t* last_tok,

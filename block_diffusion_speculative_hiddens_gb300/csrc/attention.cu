@@ -134,10 +134,15 @@ __global__ void __launch_bounds__(G * KS * 32) k_attn(const AttnParams p) {
   pdl_wait();
 
   const int slot = p.slots[b];
-  const int nkeys = p.ctx_len[slot] + p.block;  // context + live block rows (0..S-1)
+  const int nv = p.n_valid ? min(max(p.n_valid[b], 1), DFL_BLOCK) : p.block;  // live block rows
+  const int nkeys = p.ctx_len[slot] + nv;             // context + live block rows
   const int npages = (nkeys + 63) >> 6;
   const int pb = (int)((long long)split * npages / p.n_splits);  // balanced page ranges
   const int pe = (int)((long long)(split + 1) * npages / p.n_splits);
+  // keys of rows g and g+8: all, or (causal) the context and block rows up to
+  // the row itself (padding rows: up to the last live row)
+  const int lim0 = p.causal ? nkeys - nv + min(g, nv - 1) + 1 : nkeys;
+  const int lim1 = p.causal ? nkeys - nv + min(g + 8, nv - 1) + 1 : nkeys;
   const f16* kbase = p.kv.k_pool + (size_t)p.layer * p.kv.layer_stride;
   const f16* vbase = p.kv.v_pool + (size_t)p.layer * p.kv.layer_stride;
   const int* pt = p.kv.page_table + (size_t)slot * p.kv.max_pages_per_slot;
@@ -193,7 +198,7 @@ __global__ void __launch_bounds__(G * KS * 32) k_attn(const AttnParams p) {
     const bool ok = mbar_wait(full + s, (uint32_t)((it / C::STAGES) & 1), p.status, &aborted);
     if (it == 0 && threadIdx.x == 0) atrace(p, 2);
     if (ok) {
-      const int valid = min(64, nkeys - pi * 64);
+      const int valid0 = min(64, lim0 - pi * 64), valid1 = min(64, lim1 - pi * 64);
       const uint32_t kb_addr = smem_u32(sm + s * C::STAGE_BYTES);
       const uint32_t vb_addr = kb_addr + C::BLK_BYTES;
       float sc[2 * NKG][4];
@@ -223,7 +228,7 @@ __global__ void __launch_bounds__(G * KS * 32) k_attn(const AttnParams p) {
         for (int e = 0; e < 4; ++e) {
           const int key = half * KPW + nt * 8 + 2 * c4 + (e & 1);
           float v = sc[nt][e] * p.scale_log2;
-          if (key >= valid) v = -INFINITY;
+          if (key >= (e < 2 ? valid0 : valid1)) v = -INFINITY;
           sc[nt][e] = v;
         }
         mx0 = fmaxf(mx0, fmaxf(sc[nt][0], sc[nt][1]));
@@ -541,7 +546,8 @@ __global__ void __launch_bounds__(320, 1) k_attn_tc(const AttnParams p) {
   pdl_wait();
 
   const int slot = p.slots[b];
-  const int nkeys = p.ctx_len[slot] + p.block;  // context + live block rows (0..S-1)
+  const int nv = p.n_valid ? min(max(p.n_valid[b], 1), DFL_BLOCK) : p.block;  // live block rows
+  const int nkeys = p.ctx_len[slot] + nv;             // context + live block rows
   const int npages = (nkeys + 63) >> 6;
   const int pb = (int)((long long)split * npages / p.n_splits);  // balanced page ranges
   const int pe = (int)((long long)(split + 1) * npages / p.n_splits);
@@ -670,6 +676,9 @@ __global__ void __launch_bounds__(320, 1) k_attn_tc(const AttnParams p) {
       mbar_arrive(q_full);
     }
     const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
+    // this row's keys: all, or (causal) the context and block rows up to the
+    // row's own token (padding rows: up to the last live row)
+    const int klim = p.causal ? nkeys - nv + min(r & 15, nv - 1) + 1 : nkeys;
     // P V of page i complete (o_full[i & 1]).  Waited once per page, right
     // after P of the next page is published, so a barrier never runs two
     // phases ahead of its waiter; also frees P buffer i & 1 for page i + 2.
@@ -692,7 +701,7 @@ __global__ void __launch_bounds__(320, 1) k_attn_tc(const AttnParams p) {
         tmem_ld16(lane_base + (uint32_t)(C::S_COL + 64 * bb + 32 * kh + 16 * j), sc + 16 * j);
       tc_fence_before();
       mbar_arrive(s_empty + bb);
-      const int valid = min(64, nkeys - (pb + i) * 64) - 32 * kh;  // this half's unmasked keys
+      const int valid = min(64, klim - (pb + i) * 64) - 32 * kh;  // this half's unmasked keys
       float mx = -INFINITY;
 #pragma unroll
       for (int k = 0; k < 32; ++k) {

@@ -917,9 +917,9 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
     if (*done_flag) {
       __threadfence();
       const int batch = p.M / DFL_BLOCK;
-      const int nd = p.block - 1;  // drafts per request: block rows 1..S-1
+      const int nd = p.block - p.row0;  // tokens per request: block rows row0..S-1
       for (int idx = threadIdx.x; idx < batch * nd; idx += blockDim.x) {
-        const int b = idx / nd, i = idx % nd + 1;
+        const int b = idx / nd, i = idx % nd + p.row0;
         const unsigned long long k = __ldcg(p.keys + b * DFL_BLOCK + i);
         p.draft[idx] = k ? (int)argmax_key_index(k) : 0;
       }

@@ -97,6 +97,7 @@ struct GemmParams {
   float* logits;             // optional [M][N] (N = vocab)
   int* draft;                // [batch][block-1]
   int block;                 // ARGMAX: block size S (drafts from rows 1..S-1); 16 rows per request either way
+  int row0;                  // ARGMAX: first block row whose token is output (1: drafts; 0: target verify)
   float temp_inv;            // ARGMAX: 1/temperature (0: greedy argmax)
   unsigned long long seed;   // ARGMAX sampling: stream seed
   const int* round;          // ARGMAX sampling: round index (device; null: 0)
@@ -121,6 +122,8 @@ struct AttnParams {
   int merge_global;    // 1: splits write partials to `part`, k_attn_merge combines them (no cluster)
   float* part;         // [batch * hkv][n_splits][attn_part_floats(D)] partials (merge_global)
   int block;           // block size S: keys = context + S (rows S..15 of a request are padding)
+  int causal;          // target verify: block row t sees keys < ctx + min(t, n_valid-1) + 1
+  const int* n_valid;  // causal: [batch] live rows (null: block); keys = context + n_valid
   float scale_log2;    // log2(e) / sqrt(D)
   uint32_t* status;
   unsigned long long* trace;  // optional [grid][8] timeline (null: off)
@@ -160,6 +163,8 @@ struct BlockCtx {
   const float2* rope;
   int D, max_pos;
   int block;  // block size S (rows S..15 of each request are padding)
+  const int* tokens;   // target verify: [batch][16] block tokens (null: last_tok + masks)
+  const int* n_valid;  // target verify: [batch] live rows (null: block)
   int max_slots;
   int* slots_ok;  // [batch] out: slots with out-of-range ones replaced by 0
   int2* bctx;
@@ -184,6 +189,9 @@ cudaError_t launch_read_kv(const KVGeom& kv, int layer, int slot, int pos0, int 
                            cudaStream_t s);
 cudaError_t launch_slot_lengths(const int* slots, int batch, const int* ctx_len, int max_slots, int* out,
                                 cudaStream_t s);
+// Rows of the residual stream h [M][H] (fp32) into feats [M][n_fused][H]
+// (bf16) at index `tap` (the target's fused-feature outputs).
+cudaError_t launch_tap(const float* h, int M, int H, bf16* feats, int tap, int n_fused, cudaStream_t s);
 cudaError_t launch_harness_verify(const int* slots, int batch, int S, const int* draft, const int* match,
                                   const int* offs, int rounds_cap, int* round_ctr, int* target, int vocab,
                                   const bf16* feat_stream, int stream_rows, bf16* feats_out, int F,

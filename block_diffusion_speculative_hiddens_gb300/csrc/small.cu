@@ -65,7 +65,12 @@ __global__ void k_embed(const int* __restrict__ slots, const int* __restrict__ l
   pdl_wait();
   const int t = blockIdx.x;
   const int b = t / DFL_BLOCK, i = t % DFL_BLOCK;
-  int tok = i == 0 ? last_tok[b] : mask_id;
+  int nv = bc.n_valid ? bc.n_valid[b] : bc.block;  // live rows of this request
+  if (nv < 1 || nv > DFL_BLOCK) {
+    if (threadIdx.x == 0 && i == 0) dev_error(status, DFLASH_DEV_ARG);
+    nv = nv < 1 ? 1 : DFL_BLOCK;
+  }
+  int tok = bc.tokens ? (i < nv ? bc.tokens[t] : mask_id) : (i == 0 ? last_tok[b] : mask_id);
   if (tok < 0 || tok >= vocab) {
     if (threadIdx.x == 0) dev_error(status, DFLASH_DEV_ARG);
     tok = mask_id;
@@ -101,7 +106,7 @@ __global__ void k_embed(const int* __restrict__ slots, const int* __restrict__ l
     bc.slots_ok[b] = slot;
     if (bad_slot) dev_error(status, DFLASH_DEV_ARG);
   }
-  const bool pad = i >= bc.block || bad_slot;
+  const bool pad = i >= nv || bad_slot;
   const int pos = pad ? min(bc.ctx_len[slot] + i, bc.max_pos - 1) : bc.ctx_len[slot] + i;
   const bool in_range = pos < bc.max_pos;
   if (threadIdx.x == 0) {
@@ -141,7 +146,7 @@ __global__ void k_page_alloc(const int* slots, int batch, int S, const int* n_ne
       continue;
     }
     slots_ok[b] = slot;
-    int n = n_new[b];
+    int n = n_new ? n_new[b] : 0;  // null: only pages for the next block
     if (n < 0 || n > rows_per_req) {
       dev_error(status, DFLASH_DEV_ARG);
       n = 0;
@@ -300,7 +305,22 @@ __global__ void k_harness_verify(const int* slots, int batch, int S, const int* 
   for (int k = threadIdx.x; k < F / 8; k += blockDim.x) dst[k] = src[k];
 }
 
+__global__ void k_tap(const float* __restrict__ h, int H, bf16* __restrict__ feats, int tap, int n_fused) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int row = blockIdx.x;
+  const float* src = h + (size_t)row * H;
+  bf16* dst = feats + ((size_t)row * n_fused + tap) * H;
+  for (int k = threadIdx.x; k < H; k += blockDim.x) dst[k] = __float2bfloat16_rn(src[k]);
+}
+
 }  // namespace
+
+cudaError_t launch_tap(const float* h, int M, int H, bf16* feats, int tap, int n_fused, cudaStream_t s) {
+  cudaLaunchAttribute a[1];
+  cudaLaunchConfig_t c = cfg_of(dim3(M), dim3(256), s, a);
+  return cudaLaunchKernelEx(&c, k_tap, h, H, feats, tap, n_fused);
+}
 
 cudaError_t launch_pack_weight(const bf16* src, void* dst, int N, int K, int n_tiles, int swiglu_I, bool to_f16,
                                cudaStream_t s) {

@@ -102,3 +102,102 @@ def run_round(state: RoundState, verify, stream=None, folded: bool = False):
         state.draft_block(stream)
     verify(stream)
     state.accept(stream)
+
+
+class SpecDecoder:
+    """Greedy speculative generation for one request with a drafter handle and
+    a target handle (role 1) of the same shape family: prefill both models in
+    16-token chunks, then rounds of draft -> verify -> accept -> trim
+    (dflash_draft_block, dflash_verify_block, dflash_accept_trim,
+    dflash_advance, dflash_fuse_inject).  The output equals the target's own
+    greedy decoding.  `draft_override(out, b0)` may supply the drafts instead
+    of the drafter (tests that force long acceptances)."""
+
+    def __init__(self, drafter: Drafter, target: Drafter, slot: int = 0, stream=None):
+        cfg = drafter.cfg
+        dev = torch.device(f"cuda:{drafter.device}")
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.d, self.t, self.stream = drafter, target, stream
+        self.S = cfg.block
+        self.slots = torch.tensor([slot], **i32)
+        self.tokens = torch.zeros(1, 16, **i32)
+        self.out_tok = torch.zeros(1, 16, **i32)
+        self.n_valid = torch.zeros(1, **i32)
+        self.feats = torch.zeros(1, 16, cfg.n_fused * cfg.hidden, dtype=torch.bfloat16, device=dev)
+        self.draft = torch.zeros(1, self.S - 1, **i32)
+        self.accept_len = torch.zeros(1, **i32)
+        self.bonus = torch.zeros(1, **i32)
+        self.ctx = torch.zeros(1, **i32)
+        self.taus = []
+
+    def prefill(self, prompt) -> int:
+        """Both models over the prompt; returns the target's greedy token after it."""
+        prompt = [int(x) for x in prompt]
+        s = self.stream
+        n = 0
+        for p0 in range(0, len(prompt), 16):
+            chunk = prompt[p0:p0 + 16]
+            n = len(chunk)
+            self.tokens.zero_()
+            self.tokens[0, :n] = torch.tensor(chunk, dtype=torch.int32)
+            self.n_valid.fill_(n)
+            self.t.verify_block(self.slots, self.tokens, self.out_tok, self.n_valid, self.feats, s)
+            self.d.fuse_inject(self.slots, self.feats, 16, self.n_valid, s)
+            self.t.advance(self.slots, self.n_valid, s)
+        return int(self.out_tok[0, n - 1].item())
+
+    def generate(self, prompt, n_new: int, draft_override=None):
+        s = self.stream
+        b0 = self.prefill(prompt)
+        out = [b0]
+        self.bonus.fill_(b0)
+        while len(out) < n_new:
+            if draft_override is None:
+                self.d.draft_block(self.slots, self.bonus, self.draft, s)
+            else:
+                self.draft.copy_(torch.as_tensor(draft_override(out, b0), dtype=torch.int32).view(1, -1))
+            self.tokens[:, 0] = self.bonus
+            self.tokens[:, 1:self.S] = self.draft
+            self.t.verify_block(self.slots, self.tokens, self.out_tok, None, self.feats, s)
+            self.d.accept_trim(self.slots, self.draft, self.out_tok[:, :self.S].contiguous(), self.accept_len,
+                               self.bonus, self.ctx, s)
+            self.t.advance(self.slots, self.accept_len, s)
+            self.d.fuse_inject(self.slots, self.feats, 16, self.accept_len, s)
+            tau = int(self.accept_len.item())
+            d = self.draft[0].tolist()
+            b0 = int(self.bonus.item())
+            out.extend(d[:tau - 1])
+            out.append(b0)
+            self.taus.append(tau)
+        return out[:n_new]
+
+
+def greedy_generate(target: Drafter, prompt, n_new: int, slot: int = 0, stream=None):
+    """The target's own greedy decoding through dflash_verify_block with one
+    live row per step (the reference speculative generation must equal)."""
+    dev = torch.device(f"cuda:{target.device}")
+    i32 = dict(dtype=torch.int32, device=dev)
+    slots = torch.tensor([slot], **i32)
+    tokens = torch.zeros(1, 16, **i32)
+    out_tok = torch.zeros(1, 16, **i32)
+    n_valid = torch.zeros(1, **i32)
+    prompt = [int(x) for x in prompt]
+    n = 0
+    for p0 in range(0, len(prompt), 16):
+        chunk = prompt[p0:p0 + 16]
+        n = len(chunk)
+        tokens.zero_()
+        tokens[0, :n] = torch.tensor(chunk, dtype=torch.int32)
+        n_valid.fill_(n)
+        target.verify_block(slots, tokens, out_tok, n_valid, None, stream)
+        target.advance(slots, n_valid, stream)
+    g = int(out_tok[0, n - 1].item())
+    out = [g]
+    n_valid.fill_(1)
+    while len(out) < n_new:
+        tokens[0, 0] = g
+        target.verify_block(slots, tokens, out_tok, n_valid, None, stream)
+        target.advance(slots, n_valid, stream)
+        g = int(out_tok[0, 0].item())
+        out.append(g)
+    return out

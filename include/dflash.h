@@ -93,7 +93,11 @@ typedef struct dflash_config {
   float rms_eps;              /* RMSNorm epsilon (1e-6) */
   float rope_theta;           /* RoPE base */
   int32_t attn_impl;          /* block attention page loop: 0 by capacity (tensor cores from
-                                 16 pages per split up), 1 warp MMAs, 2 tcgen05 */
+                                 8 pages per split up), 1 warp MMAs, 2 tcgen05 */
+  int32_t role;               /* 0: the drafter.  1: a target model of the same layer shape
+                                 for dflash_verify_block / dflash_advance -- causal attention
+                                 over its own paged cache, n_layers >= n_fused + 2, block 16,
+                                 no fusion weights (fc, fc_norm may be null) */
 } dflash_config;
 
 /* Device pointers to the drafter weights, all bf16 and row-major; the arrays
@@ -248,6 +252,33 @@ DFLASH_API int dflash_slot_lengths(dflash_handle* h, const int32_t* slots, int32
 DFLASH_API int dflash_draft_block_debug(dflash_handle* h, const int32_t* slots, int32_t batch,
                              const int32_t* last_tok, int32_t* draft, float* hidden,
                              float* logits, void* stream);
+
+/* ---- target model (role 1): the verify step and the trim -----------------
+ * "DFlash原理深度剖析…", §三 第2步: the target runs one forward over the whole
+ * block and gives, at every block position, its own next token; §三 第3步:
+ * after acceptance both caches are trimmed to the confirmed length; §二.3:
+ * the drafter's features are hidden states of target layers picked evenly
+ * from its middle, and it shares the target's embedding and LM head.
+ *
+ * dflash_verify_block: block tokens [batch, 16] (DEVICE int32; row 0 the
+ * last verified token, rows 1.. the drafts) at positions ctx_len ..
+ * ctx_len+15 of each slot, n_valid [batch] DEVICE int32 live rows (null: 16;
+ * rows >= n_valid are padding: computed, never written to the cache, never
+ * keys), causal attention (row i sees the context and rows 0..i), their K/V
+ * written to the slot's cache; out_tok [batch, 16] DEVICE int32 receives
+ * every row's argmax (ties -> lowest id); feats, when non-null, DEVICE bf16
+ * [batch, 16, n_fused, H] receives the residual stream after target layers
+ * 1 + round(k (L-3) / (n_fused-1)), k = 0..n_fused-1 (the drafter's
+ * dflash_fuse_inject input).  ctx_len does not move.
+ * dflash_advance: ctx_len[slot] += n[b] (DEVICE int32 [batch], 0..16), the
+ * positions beyond it free for the next block -- the trim after acceptance
+ * (n = accept_len) and the step after a prefill chunk (n = its length).
+ * Both: DFLASH_ERR_INVALID_ARG on a drafter handle or null arguments;
+ * out-of-range slots and n are device-side errors (DFLASH_DEV_ARG). */
+DFLASH_API int dflash_verify_block(dflash_handle* h, const int32_t* slots, int32_t batch, const int32_t* tokens,
+                                   const int32_t* n_valid, int32_t* out_tok, void* feats, void* stream);
+DFLASH_API int dflash_advance(dflash_handle* h, const int32_t* slots, int32_t batch, const int32_t* n,
+                              void* stream);
 
 /* a3-a6 at temperature T > 0 ([Paper walkthrough] Results and [News summary]
  * 用例与示例 report DFlash with sampling; [Code walkthrough] §三 第3步: the

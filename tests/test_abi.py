@@ -46,9 +46,15 @@ def test_workspace_sizing_accepts_every_workload(lib, name):
     assert n > 0 and n % 256 == 0
 
 
+def test_target_role_accepted_with_enough_layers(lib):
+    assert lib.dflash_workspace_bytes(ctypes.byref(_cfg(CONFIGS["tiny"], role=1, n_layers=8))) > 0
+    assert lib.dflash_workspace_bytes(ctypes.byref(_cfg(CONFIGS["tiny"], role=1, n_layers=8, block=8))) == 0
+
+
 @pytest.mark.parametrize("bad", [dict(head_dim=96), dict(block=1), dict(block=17), dict(page_size=32), dict(n_layers=9),
                                  dict(n_kv_heads=3), dict(max_batch=65), dict(mask_id=-1),
-                                 dict(hidden=200), dict(rope_theta=0.5), dict(attn_impl=3)])
+                                 dict(hidden=200), dict(rope_theta=0.5), dict(attn_impl=3), dict(role=2),
+                                 dict(role=1)])
 def test_workspace_sizing_rejects_unsupported(lib, bad):
     assert lib.dflash_workspace_bytes(ctypes.byref(_cfg(CONFIGS["tiny"], **bad))) == 0
 
@@ -61,6 +67,8 @@ def test_null_arguments_rejected_without_device(lib):
     assert lib.dflash_fuse_inject(None, None, 1, None, 16, None, None) == 1
     assert lib.dflash_draft_round(None, None, 1, None, 16, None, None, None, None) == 1
     assert lib.dflash_plan(None, None) == 1
+    assert lib.dflash_verify_block(None, None, 1, None, None, None, None, None) == 1
+    assert lib.dflash_advance(None, None, 1, None, None) == 1
     assert lib.dflash_accept_trim(None, None, 1, None, None, None, None, None, None) == 1
     assert lib.dflash_launch_count(None) == 0
     out = ctypes.c_void_p()

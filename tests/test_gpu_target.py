@@ -1,0 +1,104 @@
+"""Target model (verify step) and speculative generation through the C ABI,
+against the float64 oracle (oracle/target_ref.py)."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle as O
+import oracle.target_ref as T
+from tests.gpu_util import MARGIN, TOL_REL_L2, rel_l2, to_np
+from workload import get_config, make_target_weights, make_weights, prompt_tokens
+
+pytestmark = pytest.mark.gpu
+
+NL = 8  # target layers
+
+
+def _handles(cfg, cap=256, attn_impl=0):
+    from block_diffusion_speculative_hiddens_gb300 import Drafter, weights_to_device
+    mpps = math.ceil(cap / 64) + 1
+    tw, dw = make_target_weights(cfg, NL), make_weights(cfg)
+    t = Drafter(cfg, weights_to_device(tw), max_batch=1, max_slots=2, max_pages=2 * mpps, max_pages_per_slot=mpps,
+                max_rows=16, attn_impl=attn_impl, role=1)
+    d = Drafter(cfg, weights_to_device(dw), max_batch=1, max_slots=2, max_pages=2 * mpps, max_pages_per_slot=mpps,
+                max_rows=16, attn_impl=attn_impl)
+    return t, d, O.OracleModel(cfg, tw), O.OracleModel(cfg, dw)
+
+
+@pytest.mark.parametrize("attn_impl", [1, 2], ids=["attn-warp-mma", "attn-tcgen05"])
+@pytest.mark.parametrize("name", ["tiny-gains", "small"])
+def test_verify_block_matches_oracle(lib, name, attn_impl):
+    """Every row's token, the tapped features and the cache, chunk by chunk
+    over a 40-token prompt (causal within each chunk, the last chunk ragged)."""
+    import torch
+    cfg = get_config(name)
+    t, _, tm, _ = _handles(cfg, attn_impl=attn_impl)
+    ot = T.OracleTarget(tm, NL, 256)
+    prompt = prompt_tokens(cfg, 0, 40)
+    dev = torch.device("cuda:0")
+    i32 = dict(dtype=torch.int32, device=dev)
+    slots = torch.tensor([1], **i32)
+    tokens = torch.zeros(1, 16, **i32)
+    out = torch.zeros(1, 16, **i32)
+    nv = torch.zeros(1, **i32)
+    feats = torch.zeros(1, 16, cfg.n_fused * cfg.hidden, dtype=torch.bfloat16, device=dev)
+    for p0 in range(0, len(prompt), 16):
+        chunk = prompt[p0:p0 + 16]
+        n = len(chunk)
+        tokens.zero_()
+        tokens[0, :n] = torch.tensor(chunk, dtype=torch.int32)
+        nv.fill_(n)
+        t.verify_block(slots, tokens, out, nv, feats)
+        t.advance(slots, nv)
+        o = ot.forward(chunk)
+        ot.advance(n)
+        got = to_np(out)[0, :n]
+        strong = o["margin"] > MARGIN
+        assert np.array_equal(got[strong], o["tok"][strong]), (p0, got, o["tok"], o["margin"])
+        f = to_np(feats)[0, :n].reshape(n, cfg.n_fused, cfg.hidden)
+        assert rel_l2(f, o["feats"]) < TOL_REL_L2, p0
+    L = len(prompt)
+    assert int(to_np(t.slot_lengths(slots))[0]) == L
+    for l in (0, NL - 1):
+        k, v = t.read_kv(l, 1, 0, L)
+        assert rel_l2(to_np(k), ot.K[l][:L]) < TOL_REL_L2 and rel_l2(to_np(v), ot.V[l][:L]) < TOL_REL_L2, l
+    assert t.read_status() == 0
+
+
+def _first_weak(margins, thr=MARGIN):
+    weak = np.nonzero(np.asarray(margins) <= thr)[0]
+    return int(weak[0]) if weak.size else len(margins)
+
+
+@pytest.mark.parametrize("mode", ["drafter", "perfect", "corrupt"])
+def test_speculative_generation_is_the_greedy_output(lib, mode):
+    """The speculative output equals the target's own greedy decoding: on the
+    GPU (same kernels, token by token) and against the oracle's greedy tokens
+    up to its first near-tie."""
+    from block_diffusion_speculative_hiddens_gb300.session import SpecDecoder, greedy_generate
+    cfg = get_config("tiny-gains")
+    t, d, tm, _ = _handles(cfg)
+    prompt = prompt_tokens(cfg, 1, 40)
+    n_new = 48
+    og, om = T.greedy_generate(T.OracleTarget(tm, NL, 256), prompt, n_new)
+    gg = greedy_generate(t, prompt, n_new, slot=0)
+    k = _first_weak(om)
+    assert gg[:k] == og[:k].tolist()
+    override = None
+    if mode != "drafter":
+        def override(out, b0, _g=gg):
+            kk = len(out)
+            dd = [_g[kk + i] if kk + i < len(_g) else 0 for i in range(cfg.block - 1)]
+            if mode == "corrupt":
+                j = (kk * 7) % (cfg.block - 1)
+                dd[j] = (dd[j] + 1) % (cfg.vocab - 1)
+            return dd
+    sd = SpecDecoder(d, t, slot=1)
+    got = sd.generate(prompt, n_new, override)
+    assert got == gg, (got, gg, sd.taus)
+    if mode == "perfect":
+        assert all(x == cfg.block for x in sd.taus[:-1])
+    if mode == "corrupt":
+        assert max(sd.taus) > 1
+    assert t.read_status() == 0 and d.read_status() == 0

@@ -15,6 +15,8 @@ from .gen import (  # noqa: F401
 from .configs import DraftConfig, CONFIGS, TEST_CONFIGS, get_config  # noqa: F401
 from .inputs import (  # noqa: F401
     make_weights,
+    make_target_weights,
+    prompt_tokens,
     feature_rows,
     match_stream,
     context_lengths,

@@ -88,6 +88,36 @@ def make_weights(cfg):
     return w
 
 
+SEED_TARGET = 4
+SEED_PROMPT = 5
+
+
+def make_target_weights(cfg, n_layers: int):
+    """Weights of a random target model with the drafter's layer shape: its
+    own n_layers layers and final norm (seed stream 4) and the drafter's
+    embedding table, shared (the drafter reuses the target's embedding and
+    LM head).  Same layout as make_weights; no fusion weights."""
+    def tensor(name, layer=None):
+        shape = _shape(cfg, name)
+        n = int(np.prod(shape))
+        ids = (_GLOBAL_IDS[name],) if layer is None else (1000 + layer, _LAYER_IDS[name])
+        key = stream_key(SEED_TARGET + cfg.seed, *ids)
+        if len(shape) == 1:
+            if cfg.gain_std == 0.0:
+                return np.full(shape, 0x3F80, dtype=np.uint16)
+            return normal_bf16(key, 0, n, scale=cfg.gain_std, shift=1.0).reshape(shape)
+        return normal_bf16(key, 0, n, scale=cfg.weight_std).reshape(shape)
+    w = {"embed": make_weights(cfg)["embed"], "final_norm": tensor("final_norm")}
+    w["layers"] = [{k: tensor(k, l) for k in _LAYER_IDS} for l in range(n_layers)]
+    return w
+
+
+def prompt_tokens(cfg, b: int, n: int) -> np.ndarray:
+    """Prompt of request b: n ids uniform over the vocabulary minus the mask id."""
+    u = uniform(stream_key(SEED_PROMPT + cfg.seed, b), np.arange(n))
+    return np.minimum(np.floor(u * (cfg.vocab - 1)), cfg.vocab - 2).astype(np.int64)
+
+
 def feature_rows(cfg, b: int, p0: int, n: int) -> np.ndarray:
     """Target features of request b at positions p0..p0+n-1: uint16 [n, 5, H]."""
     F = cfg.fused_dim
