@@ -57,6 +57,10 @@ def parse():
     ap.add_argument("--temperature", type=float, default=0.0,
                     help="draft at this temperature (> 0: each draft drawn from softmax(logits / T))")
     ap.add_argument("--seed", type=int, default=1234, help="seed of the drafts' random streams (temperature > 0)")
+    ap.add_argument("--spec-generate", type=int, default=0,
+                    help="instead of the drafting rounds: greedy speculative generation of this many tokens "
+                         "with a random-weight target model (--target-layers) of the workload's layer shape")
+    ap.add_argument("--target-layers", type=int, default=8)
     ap.add_argument("--fold-inject", action="store_true",
                     help="issue dflash_draft_round instead of dflash_fuse_inject + dflash_draft_block")
     return ap.parse_args()
@@ -490,6 +494,59 @@ def run_gpu(args, rank, world, local_rank):
     return res, cfg
 
 
+def run_spec_generate(args):
+    """Greedy speculative generation (draft -> verify -> accept -> trim per
+    round, host loop) with a random-weight target of the drafter's layer
+    shape; times the whole generation and the verify calls."""
+    import numpy as np
+    import torch
+    from block_diffusion_speculative_hiddens_gb300 import Drafter, weights_to_device
+    from block_diffusion_speculative_hiddens_gb300.session import SpecDecoder
+    from workload import get_config, make_target_weights, make_weights, prompt_tokens
+    cfg = get_config(args.config)
+    P = int(cfg.ctx0 or cfg.ctx_range[0])
+    n_new = args.spec_generate
+    cap = P + 16 * (n_new + 2) + 64
+    mpps = math.ceil(cap / 64) + 1
+    kw = dict(max_batch=1, max_slots=1, max_pages=mpps, max_pages_per_slot=mpps, max_rows=16,
+              attn_impl=args.attn_impl)
+    t = Drafter(cfg, weights_to_device(make_target_weights(cfg, args.target_layers)), role=1, **kw)
+    d = Drafter(cfg, weights_to_device(make_weights(cfg)), **kw)
+    prompt = prompt_tokens(cfg, 0, P)
+    times = []
+    ev = []
+    orig = t.verify_block
+
+    def timed_verify(*a, **k):  # CUDA events around every verify call
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        orig(*a, **k)
+        e1.record()
+        ev.append((e0, e1))
+    t.verify_block = timed_verify
+    for rep_ in range(2):  # the first pass warms up; its slot is reset before the timed one
+        for x in (t, d):
+            x.reset_slot(0)
+        ev.clear()
+        sd = SpecDecoder(d, t, slot=0)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        out = sd.generate(prompt, n_new)
+        torch.cuda.synchronize()
+        times.append(time.perf_counter() - t0)
+    n_prefill = math.ceil(P / 16)
+    verify_us = [a.elapsed_time(b) * 1e3 for a, b in ev[n_prefill:]]
+    rounds = len(sd.taus)
+    return {"metric": "greedy speculative generation, random-weight target", "value": round(n_new / times[-1], 1),
+            "unit": "tok/s", "higher_is_better": True, "generated": len(out), "rounds": rounds,
+            "mean_tau": round(float(np.mean(sd.taus)), 3), "wall_s": round(times[-1], 4),
+            "verify_us_median": round(float(np.median(verify_us)), 1) if verify_us else None,
+            "note": "host loop with one host read per round; prefill included; the random drafter rarely matches "
+                    "the random target, so tau is near 1",
+            "config": {"workload": f"{cfg.name} drafter + {args.target_layers}-layer target of the same layer "
+                                   f"shape, prompt {P}, block 16", "target_layers": args.target_layers}}
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -526,6 +583,10 @@ def main():
         return
 
     import torch
+    if args.spec_generate:
+        if rank == 0:
+            print(json.dumps(run_spec_generate(args)), flush=True)
+        return
     if world > 1:
         torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     res, cfg = run_gpu(args, rank, world, local_rank)
