@@ -82,6 +82,10 @@ def argmax_first(x: np.ndarray) -> np.ndarray:
 
 # ----------------------------------------------------------------- model
 
+# matrices held as FP8 E4M3 with per-row scales in the low-precision variant
+# (everything but the fusion projection and the norm gains)
+FP8_WEIGHTS = ("embed", "wqkv", "wo", "w_gate_up", "w_down")
+
 class OracleModel:
     """Drafter weights (bf16 bit patterns) with float64 views on demand.
 
@@ -89,24 +93,32 @@ class OracleModel:
     each matrix when used so full-size drafters fit in host memory.
     """
 
-    def __init__(self, cfg, weights: dict, cache: bool = True):
+    def __init__(self, cfg, weights: dict, cache: bool = True, fp8: bool = False):
         self.cfg = cfg
         self.raw = weights
         self.cache = cache
+        self.fp8 = fp8  # projections and the embedding as per-row-scaled E4M3 (oracle.fp8_ref)
         self._c = {}
+
+    def _widen(self, name: str, src) -> np.ndarray:
+        arr = bf16_to_f64(src)
+        if self.fp8 and name in FP8_WEIGHTS:
+            from .fp8_ref import dequantize_rows
+            arr = dequantize_rows(arr)
+        return arr
 
     def w(self, name: str, layer: int | None = None) -> np.ndarray:
         key = (name, layer)
         if key in self._c:
             return self._c[key]
         src = self.raw[name] if layer is None else self.raw["layers"][layer][name]
-        arr = bf16_to_f64(src)
+        arr = self._widen(name, src)
         if self.cache:
             self._c[key] = arr
         return arr
 
     def embed_rows(self, ids) -> np.ndarray:
-        return bf16_to_f64(self.raw["embed"][np.asarray(ids)])
+        return self._widen("embed", self.raw["embed"][np.asarray(ids)])
 
 
 # ----------------------------------------------------------------- a1, a2
@@ -214,7 +226,7 @@ def lm_head_logits(model: OracleModel, h: np.ndarray, chunk: int = 1 << 14) -> n
     out = np.empty((h.shape[0], V), dtype=np.float64)
     E = model.raw["embed"]
     for v0 in range(0, V, chunk):
-        out[:, v0:v0 + chunk] = hn @ bf16_to_f64(E[v0:v0 + chunk]).T
+        out[:, v0:v0 + chunk] = hn @ model._widen("embed", E[v0:v0 + chunk]).T
     return out
 
 
