@@ -57,6 +57,8 @@ def parse():
     ap.add_argument("--temperature", type=float, default=0.0,
                     help="draft at this temperature (> 0: each draft drawn from softmax(logits / T))")
     ap.add_argument("--seed", type=int, default=1234, help="seed of the drafts' random streams (temperature > 0)")
+    ap.add_argument("--weights", default="bf16", choices=["bf16", "fp8"],
+                    help="drafter weights as given (bf16, held as f16) or FP8 E4M3 with per-row scales")
     ap.add_argument("--spec-generate", type=int, default=0,
                     help="instead of the drafting rounds: greedy speculative generation of this many tokens "
                          "with a random-weight target model (--target-layers) of the workload's layer shape")
@@ -253,7 +255,8 @@ def run_gpu(args, rank, world, local_rank):
 
     chunk = 2048
     d = Drafter(cfg, w_dev, max_batch=B, max_slots=n_slots, max_pages=mpps * n_slots,
-                max_pages_per_slot=mpps, max_rows=max(chunk, S * B), device=local_rank, attn_impl=args.attn_impl)
+                max_pages_per_slot=mpps, max_rows=max(chunk, S * B), device=local_rank, attn_impl=args.attn_impl,
+                weight_fp8=1 if args.weights == "fp8" else 0)
     stream = torch.cuda.Stream(device=dev)
 
     def prefill(g):
@@ -422,7 +425,9 @@ def run_gpu(args, rank, world, local_rank):
     tf_burst, tf_sust = tensor_peaks()
     H, V, D = cfg.hidden, cfg.vocab, cfg.head_dim
     M = S * B                                            # block rows the method computes
-    lm_bytes = V * H * 2 + M * H * 2
+    fp8 = args.weights == "fp8"
+    wb = 1 if fp8 else 2                                 # bytes per projection / embedding weight
+    lm_bytes = V * H * wb + (V * 4 if fp8 else 0) + M * H * 2
     lm_flops = 2.0 * M * V * H
     lm_avg_ms = statistics.mean(lm_ms) if lm_ms else float("nan")
     round_ms_incl = ms / K
@@ -430,14 +435,20 @@ def run_gpu(args, rank, world, local_rank):
     tau = accepted / (K * B)
     avg_ctx = float(ctx.mean()) + tau * (R / 2)
     kv_bytes = B * cfg.n_layers * (avg_ctx + S) * cfg.n_kv_heads * D * 2 * 2
-    round_bytes = cfg.weight_bytes() + kv_bytes + B * tau * F * 2
+    if fp8:  # FP8 projections and embedding (+ a float scale per row); the fusion projection stays 2 bytes
+        fc_bytes = 2 * H * F
+        rows = V + cfg.n_layers * (cfg.qkv_rows + H + 2 * cfg.intermediate + H)
+        w_bytes = (cfg.weight_bytes() - fc_bytes) // 2 + fc_bytes + 4 * rows
+    else:
+        w_bytes = cfg.weight_bytes()
+    round_bytes = w_bytes + kv_bytes + B * tau * F * 2
     layer_params = cfg.qkv_rows * H + H * cfg.n_q_heads * D + 3 * cfg.intermediate * H
     inj_params = H * F + cfg.n_layers * 2 * cfg.n_kv_heads * D * H
     round_flops = 2.0 * M * (cfg.n_layers * layer_params + V * H) + 2.0 * B * tau * inj_params
     if B == 1:
         lm_roof = {"bound": "hbm", "achieved": round(lm_bytes / (lm_avg_ms * 1e-3) / 1e9, 1), "peak": hbm,
                    "unit": "GB/s", "frac": round(lm_bytes / (lm_avg_ms * 1e-3) / 1e9 / hbm, 4),
-                   "traffic": lm_head_traffic(cfg), "peak_source": f"{peak_src} copy bandwidth"}
+                   "traffic": None if fp8 else lm_head_traffic(cfg), "peak_source": f"{peak_src} copy bandwidth"}
     else:
         ach = lm_flops / (lm_avg_ms * 1e-3) / 1e12
         lm_roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": tf_sust, "unit": "TFLOP/s",
@@ -464,7 +475,7 @@ def run_gpu(args, rank, world, local_rank):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f16",
+        "dtype": "f16 activations, fp8 e4m3 weights" if fp8 else "f16",
         "data": f"synthetic (seeded N(0,1) target features from the {feat_src}, N(0,0.02) random-init weights, "
                 "stand-in verify)",
         "config": {"workload": f"{cfg.name} drafter batch {B}: H{H}, {cfg.n_q_heads}q/{cfg.n_kv_heads}kv x"
@@ -472,6 +483,7 @@ def run_gpu(args, rank, world, local_rank):
                                f"{F}->{H}, {ctx_desc}, block {S}, {p_desc}",
                    "batch": B, "prompt_mean": float(ctx.mean()), "rounds_per_slot": R,
                    "attn_impl": ["library choice", "warp MMAs", "tcgen05"][args.attn_impl],
+                   "weights": "fp8 e4m3, per-row scales" if args.weights == "fp8" else "bf16 (held as f16)",
                    "drafting": (f"sampled at temperature {args.temperature} (Gumbel-max, seed {args.seed})"
                                 if args.temperature > 0 else "greedy argmax"),
                    "round_call": "dflash_draft_round" if args.fold_inject

@@ -33,7 +33,8 @@ class DflashConfig(ctypes.Structure):
         "max_pages_per_slot", "max_rows", "device")] + [("rms_eps", ctypes.c_float),
                                                          ("rope_theta", ctypes.c_float),
                                                          ("attn_impl", ctypes.c_int32),
-                                                         ("role", ctypes.c_int32)]
+                                                         ("role", ctypes.c_int32),
+                                                         ("weight_fp8", ctypes.c_int32)]
 
 
 class DflashWeights(ctypes.Structure):
@@ -135,7 +136,8 @@ class Drafter:
     """
 
     def __init__(self, cfg, weights: dict, *, max_batch: int, max_slots: int, max_pages: int,
-                 max_pages_per_slot: int, max_rows: int, device: int = 0, attn_impl: int = 0, role: int = 0):
+                 max_pages_per_slot: int, max_rows: int, device: int = 0, attn_impl: int = 0, role: int = 0,
+                 weight_fp8: int = 0):
         import torch
         self.lib = load()
         self.cfg = cfg
@@ -150,7 +152,7 @@ class Drafter:
                          page_size=cfg.page_size, max_batch=max_batch, max_slots=max_slots,
                          max_pages=max_pages, max_pages_per_slot=max_pages_per_slot,
                          max_rows=max_rows, device=device, rms_eps=cfg.rms_eps,
-                         rope_theta=cfg.rope_theta, attn_impl=attn_impl, role=role)
+                         rope_theta=cfg.rope_theta, attn_impl=attn_impl, role=role, weight_fp8=weight_fp8)
         self.c = c
         nbytes = self.lib.dflash_workspace_bytes(ctypes.byref(c))
         if nbytes == 0:

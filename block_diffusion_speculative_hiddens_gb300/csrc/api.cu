@@ -100,6 +100,11 @@ struct dflash_handle {
   f16* wo_pk[DFL_MAX_LAYERS];
   f16* gu_pk[DFL_MAX_LAYERS];
   f16* down_pk[DFL_MAX_LAYERS];
+  // FP8 weights: the packed blocks above hold E4M3 bytes; per packed row scales
+  bool fp8 = false;
+  float* embed_sc = nullptr;
+  float *wqkv_sc[DFL_MAX_LAYERS] = {}, *wo_sc[DFL_MAX_LAYERS] = {}, *gu_sc[DFL_MAX_LAYERS] = {},
+        *down_sc[DFL_MAX_LAYERS] = {};
   float* fc_norm;
   float* final_norm;
   float* in_norm[DFL_MAX_LAYERS];
@@ -164,6 +169,7 @@ bool cfg_valid(const dflash_config* c) {
   if (!(c->rms_eps > 0.f) || !(c->rope_theta > 1.f)) return false;
   if (c->attn_impl < 0 || c->attn_impl > 2) return false;
   if (c->role != 0 && c->role != 1) return false;
+  if (c->weight_fp8 != 0 && c->weight_fp8 != 1) return false;
   // a target: full 16-token blocks, and 5 distinct middle layers to tap
   if (c->role == 1 && (c->block != DFL_BLOCK || c->n_layers < c->n_fused + 2)) return false;
   return true;
@@ -232,15 +238,26 @@ size_t carve(dflash_handle* h, const dflash_config& c, char* base, int num_sms) 
   o->n_eff = w.take<int>(c.max_batch);
   o->slots_ok = w.take<int>(c.max_batch);
   const size_t KBh = H / 64;
-  o->embed_pk = w.take<f16>((size_t)ceil_div(c.vocab, 128) * KBh * DFL_WBLK_ELEMS);
+  // packed blocks: 16 KB of f16, or 8 KB of FP8 (+ a float scale per packed row)
+  const bool f8 = c.weight_fp8 != 0;
+  auto blocks = [&](size_t n_blk) {
+    return reinterpret_cast<f16*>(w.take<uint8_t>(n_blk * (f8 ? DFL_WBLK8_BYTES : DFL_WBLK_ELEMS * 2)));
+  };
+  auto scales = [&](size_t n_tiles) { return f8 ? w.take<float>(n_tiles * 128) : nullptr; };
+  o->embed_pk = blocks((size_t)ceil_div(c.vocab, 128) * KBh);
+  o->embed_sc = scales((size_t)ceil_div(c.vocab, 128));
   o->fc_pk = w.take<bf16>((size_t)(H / 128) * (c.n_fused * H / 64) * DFL_WBLK_ELEMS);
   o->fc_norm = w.take<float>(H);
   o->final_norm = w.take<float>(H);
   for (int l = 0; l < c.n_layers; ++l) {
-    o->wqkv_pk[l] = w.take<f16>((size_t)((hq + 2 * hkv) * D / 128) * KBh * DFL_WBLK_ELEMS);
-    o->wo_pk[l] = w.take<f16>((size_t)(H / 128) * (hq * D / 64) * DFL_WBLK_ELEMS);
-    o->gu_pk[l] = w.take<f16>((size_t)(I / 64) * KBh * DFL_WBLK_ELEMS);
-    o->down_pk[l] = w.take<f16>((size_t)(H / 128) * (I / 64) * DFL_WBLK_ELEMS);
+    o->wqkv_pk[l] = blocks((size_t)((hq + 2 * hkv) * D / 128) * KBh);
+    o->wo_pk[l] = blocks((size_t)(H / 128) * (hq * D / 64));
+    o->gu_pk[l] = blocks((size_t)(I / 64) * KBh);
+    o->down_pk[l] = blocks((size_t)(H / 128) * (I / 64));
+    o->wqkv_sc[l] = scales((size_t)((hq + 2 * hkv) * D / 128));
+    o->wo_sc[l] = scales((size_t)(H / 128));
+    o->gu_sc[l] = scales((size_t)(I / 64));
+    o->down_sc[l] = scales((size_t)(H / 128));
     o->in_norm[l] = w.take<float>(H);
     o->post_norm[l] = w.take<float>(H);
     o->q_norm[l] = w.take<float>(D);
@@ -337,6 +354,13 @@ GemmShape gemm_shape(const dflash_handle* h, int M) {
   return g;
 }
 
+// FP8 weights: the GEMM streams E4M3 blocks and scales rows by `sc` (group g)
+void fp8_weights(const dflash_handle* h, GemmParams& p, const float* sc, int g = 0) {
+  if (!h->fp8) return;
+  p.a_fp8 = 1;
+  p.a_scale[g] = sc;
+}
+
 // Plan and launch one GEMM over packed A operands a[0..groups-1] (tiles
 // a_tile_off .. a_tile_off+n_tiles-1 of each) and the token operand B.
 int run_gemm(dflash_handle* h, cudaStream_t s, int mode, const void* const* a, int groups, int a_tile_off,
@@ -362,8 +386,8 @@ int run_gemm(dflash_handle* h, cudaStream_t s, int mode, const void* const* a, i
   p.n_tg = ceil_div(n_tiles, gs.cl);
   p.total_ctiles = groups * p.n_tg * t_tiles;
   p.allow_split = allow_split ? 1 : 0;
-  p.stages = gemm_pick_stages(BN, mode);
-  p.red_items = gemm_red_items(BN, p.stages);
+  p.stages = gemm_pick_stages(BN, mode, p.a_fp8);
+  p.red_items = gemm_red_items(BN, p.stages, p.a_fp8);
   int cols = 32;
   while (cols < 2 * BN) cols *= 2;
   p.tmem_cols = cols;
@@ -496,7 +520,7 @@ int draft_impl(dflash_handle* h, const int32_t* slots, int32_t batch, const int3
   bcx.slots_ok = h->slots_ok;
   bcx.max_slots = c.max_slots;
   bcx.brope = h->brope;
-  rc = cuda_err(launch_embed(slots, batch, last_tok, c.mask_id, c.vocab, h->embed_pk, h->in_norm[0], H, h->h,
+  rc = cuda_err(launch_embed(slots, batch, last_tok, c.mask_id, c.vocab, h->embed_pk, h->embed_sc, h->in_norm[0], H, h->h,
                              h->hg, h->ss_a, h->keys, bcx, h->status, s));
   if (rc) return rc;
 
@@ -526,6 +550,7 @@ int draft_impl(dflash_handle* h, const int32_t* slots, int32_t batch, const int3
         p.n_eff = h->n_eff;
       }
       const void* a = h->wqkv_pk[l];
+      fp8_weights(h, p, h->wqkv_sc[l]);
       rc = run_gemm(h, s, GM_QKV, &a, 1, 0, p.N / 128, H, fold ? h->tm_hgx : h->tm_hg, fold ? M + R : M, p, true, 0,
                     DFLASH_KID_QKV);
       if (rc) return rc;
@@ -567,6 +592,7 @@ int draft_impl(dflash_handle* h, const int32_t* slots, int32_t batch, const int3
       p.ss_out = h->ss_a;
       p.N = H;
       const void* a = h->wo_pk[l];
+      fp8_weights(h, p, h->wo_sc[l]);
       rc = run_gemm(h, s, GM_RESID, &a, 1, 0, H / 128, hq * D, h->tm_o, M, p, true, 0, DFLASH_KID_WO);
       if (rc) return rc;
     }
@@ -577,6 +603,7 @@ int draft_impl(dflash_handle* h, const int32_t* slots, int32_t batch, const int3
       p.out = h->act;
       p.N = I;
       const void* a = h->gu_pk[l];
+      fp8_weights(h, p, h->gu_sc[l]);
       rc = run_gemm(h, s, GM_SWIGLU, &a, 1, 0, I / 64, H, h->tm_hg, M, p, true, 0, DFLASH_KID_GATE_UP);
       if (rc) return rc;
     }
@@ -588,6 +615,7 @@ int draft_impl(dflash_handle* h, const int32_t* slots, int32_t batch, const int3
       p.ss_out = h->ss_a;
       p.N = H;
       const void* a = h->down_pk[l];
+      fp8_weights(h, p, h->down_sc[l]);
       rc = run_gemm(h, s, GM_RESID, &a, 1, 0, H / 128, I, h->tm_act, M, p, true, 0, DFLASH_KID_DOWN);
       if (rc) return rc;
     }
@@ -619,6 +647,7 @@ int draft_impl(dflash_handle* h, const int32_t* slots, int32_t batch, const int3
     p.round = smp.round;
     p.done_ctr = h->done_ctr;
     const void* a = h->embed_pk;
+    fp8_weights(h, p, h->embed_sc);
     rc = run_gemm(h, s, GM_ARGMAX, &a, 1, 0, ceil_div(c.vocab, 128), H, h->tm_hg, M, p, true, 0,
                   DFLASH_KID_LM_HEAD);
     if (rc) return rc;
@@ -674,6 +703,7 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
   if (!h) return DFLASH_ERR_CAPACITY;
   h->cfg = *cfg;
   h->num_sms = sms;
+  h->fp8 = cfg->weight_fp8 != 0;
   const size_t need = carve(h, *cfg, static_cast<char*>(workspace), sms);
   if (cuda_err(cudaMemset(workspace, 0, need))) {
     delete h;
@@ -682,16 +712,20 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
   const dflash_config& c = *cfg;
   const int H = c.hidden, D = c.head_dim, hq = c.n_q_heads, hkv = c.n_kv_heads, I = c.intermediate;
   auto B16 = [](const void* p) { return static_cast<const bf16*>(p); };
-  cudaError_t e = launch_pack_weight(B16(w->embed), h->embed_pk, c.vocab, H, ceil_div(c.vocab, 128), 0, true, 0);
+  // f16 packing, or FP8 E4M3 packing with per-row scales
+  auto pack = [&](const void* src, f16* dst, float* sc, int N, int K, int n_tiles, int swiglu_I) {
+    return h->fp8 ? launch_pack_weight_fp8(B16(src), reinterpret_cast<uint8_t*>(dst), sc, N, K, n_tiles, swiglu_I, 0)
+                  : launch_pack_weight(B16(src), dst, N, K, n_tiles, swiglu_I, true, 0);
+  };
+  cudaError_t e = pack(w->embed, h->embed_pk, h->embed_sc, c.vocab, H, ceil_div(c.vocab, 128), 0);
   if (!e && drafter) e = launch_pack_weight(B16(w->fc), h->fc_pk, H, c.n_fused * H, H / 128, 0, false, 0);
   if (!e && drafter) e = launch_gain_f32(B16(w->fc_norm), h->fc_norm, H, 0);
   if (!e) e = launch_gain_f32(B16(w->final_norm), h->final_norm, H, 0);
   for (int l = 0; l < c.n_layers && !e; ++l) {
-    e = launch_pack_weight(B16(w->wqkv[l]), h->wqkv_pk[l], (hq + 2 * hkv) * D, H, (hq + 2 * hkv) * D / 128, 0, true,
-                           0);
-    if (!e) e = launch_pack_weight(B16(w->wo[l]), h->wo_pk[l], H, hq * D, H / 128, 0, true, 0);
-    if (!e) e = launch_pack_weight(B16(w->w_gate_up[l]), h->gu_pk[l], 2 * I, H, I / 64, I, true, 0);
-    if (!e) e = launch_pack_weight(B16(w->w_down[l]), h->down_pk[l], H, I, H / 128, 0, true, 0);
+    e = pack(w->wqkv[l], h->wqkv_pk[l], h->wqkv_sc[l], (hq + 2 * hkv) * D, H, (hq + 2 * hkv) * D / 128, 0);
+    if (!e) e = pack(w->wo[l], h->wo_pk[l], h->wo_sc[l], H, hq * D, H / 128, 0);
+    if (!e) e = pack(w->w_gate_up[l], h->gu_pk[l], h->gu_sc[l], 2 * I, H, I / 64, I);
+    if (!e) e = pack(w->w_down[l], h->down_pk[l], h->down_sc[l], H, I, H / 128, 0);
     if (!e) e = launch_gain_f32(B16(w->in_norm[l]), h->in_norm[l], H, 0);
     if (!e) e = launch_gain_f32(B16(w->post_norm[l]), h->post_norm[l], H, 0);
     if (!e) e = launch_gain_f32(B16(w->q_norm[l]), h->q_norm[l], D, 0);
@@ -704,7 +738,7 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
   // token tiles of 128+ tokens: clusters of 4 CTAs share each tile unless
   // pairs keep clearly more SMs busy (clusters are placed within one GPC)
   if (!rc && DFL_GEMM_MAX_CL > 1) {
-    const int st = gemm_pick_stages(DFL_BN_MAX, GM_QKV);
+    const int st = gemm_pick_stages(DFL_BN_MAX, GM_QKV, 0);
     const int n2 = 2 * gemm_max_clusters(DFL_BN_MAX, st, 2);
     const int n4 = DFL_GEMM_MAX_CL >= 4 ? 4 * gemm_max_clusters(DFL_BN_MAX, st, 4) : 0;
     if (n4 > 0 && 10 * n4 >= 9 * n2) {
@@ -810,7 +844,10 @@ int dflash_fuse_inject(dflash_handle* h, const int32_t* slots, int32_t batch, co
     p.n_eff = h->n_eff;
     p.rows_per_req = rows_per_req;
     const void* a[DFL_MAX_LAYERS];
-    for (int l = 0; l < c.n_layers; ++l) a[l] = h->wqkv_pk[l];
+    for (int l = 0; l < c.n_layers; ++l) {
+      a[l] = h->wqkv_pk[l];
+      fp8_weights(h, p, h->wqkv_sc[l], l);
+    }
     rc = run_gemm(h, s, GM_INJECT, a, c.n_layers, c.n_q_heads * D / 128, p.N / 128, H, h->tm_cg, R, p, true, 0,
                   DFLASH_KID_INJECT);
     if (rc) return rc;
@@ -1133,8 +1170,8 @@ int noalloc_gemm(dflash_handle* h, cudaStream_t s, int mode, const void* const* 
   p.n_tg = n_tiles;
   p.total_ctiles = p.total_tiles;
   p.allow_split = 1;
-  p.stages = gemm_pick_stages(BN, mode);
-  p.red_items = gemm_red_items(BN, p.stages);
+  p.stages = gemm_pick_stages(BN, mode, p.a_fp8);
+  p.red_items = gemm_red_items(BN, p.stages, p.a_fp8);
   int cols = 32;
   while (cols < 2 * BN) cols *= 2;
   p.tmem_cols = cols;
@@ -1215,7 +1252,10 @@ extern "C" int dflash_fuse_inject_noalloc(dflash_handle* h, const int32_t* slots
     p.n_eff = h->n_eff;
     p.rows_per_req = rows_per_req;
     const void* a[DFL_MAX_LAYERS];
-    for (int l = 0; l < c.n_layers; ++l) a[l] = h->wqkv_pk[l];
+    for (int l = 0; l < c.n_layers; ++l) {
+      a[l] = h->wqkv_pk[l];
+      fp8_weights(h, p, h->wqkv_sc[l], l);
+    }
     rc = noalloc_gemm(h, s, GM_INJECT, a, c.n_layers, c.n_q_heads * D / 128, p.N / 128, H, tm_rows, R, p, 0, part,
                       ctr);
   }

@@ -278,6 +278,12 @@ DFL_DEV uint32_t pack_f16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 // float -> f16 activation; values beyond the f16 range set DFLASH_DEV_RANGE.
+// Two FP8 E4M3 values (low byte first) to two f16 (exact: every E4M3 value is an f16).
+DFL_DEV uint32_t e4m3x2_to_f16x2(uint16_t v) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+  return r;
+}
 DFL_DEV f16 to_f16(float x, uint32_t* status) {
   if (fabsf(x) > 65504.f) dev_error(status, DFLASH_DEV_RANGE);
   return __float2half_rn(x);

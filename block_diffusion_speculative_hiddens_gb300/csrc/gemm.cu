@@ -53,6 +53,7 @@ constexpr int RED_PARTS = 4;               // fewest split-K part chunks the red
 constexpr int RED_CHUNK = 16 * 128;        // floats of one part's 16-column chunk (8 KB)
 constexpr int RED_BYTES = RED_PARTS * RED_CHUNK * 4;
 constexpr int EPI_THREADS = 128;
+constexpr int CONV_THREADS = 64;  // warps 6, 7
 
 // Unit arithmetic is 32-bit: the host guarantees units * grid < 2^31.
 DFL_DEV int unit_start(int c, int U, int G) { return c * U / G; }
@@ -326,6 +327,13 @@ DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, con
   const int tt_all = tile / p.t_tiles;       // (group, n-tile)
   const int group = tt_all / p.n_tiles;
   const int nt = tt_all % p.n_tiles;
+  // FP8 weights: the accumulators carry the rows' scales
+  float rs[4] = {1.f, 1.f, 1.f, 1.f};
+  if (p.a_fp8) {
+    const float* sc = p.a_scale[group] + (size_t)(p.a_tile_off + nt) * 128;
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) rs[jj] = sc[lane + 32 * jj];
+  }
   for (int j0 = ew; j0 < ntok; j0 += 4 * EPI_TOK) {
     bool ok[EPI_TOK];
     int tq[EPI_TOK];
@@ -336,7 +344,7 @@ DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, con
       ok[q] = j < ntok;  // warp-uniform
       tq[q] = t_first + j;
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj) x[q][jj] = ok[q] ? stg[j * 128 + lane + 32 * jj] : 0.f;
+      for (int jj = 0; jj < 4; ++jj) x[q][jj] = ok[q] ? stg[j * 128 + lane + 32 * jj] * rs[jj] : 0.f;
     }
 
     if constexpr (MODE == GM_RESID || MODE == GM_FC) {
@@ -531,10 +539,13 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
   const int stage_bytes = A_STAGE_BYTES + BN * 128;
   float* stg = reinterpret_cast<float*>(sm + (size_t)stages * stage_bytes);
   float* red_buf = reinterpret_cast<float*>(sm + (size_t)stages * stage_bytes + STG_BYTES);
-  uint64_t* full =
-      reinterpret_cast<uint64_t*>(sm + (size_t)stages * stage_bytes + STG_BYTES + (size_t)p.red_items * RED_CHUNK * 4);
+  // FP8 weights: each stage's 8 KB block lands here and is converted into the
+  // stage's f16 A area by the converter warps
+  uint8_t* a8 = sm + (size_t)stages * stage_bytes + STG_BYTES + (size_t)p.red_items * RED_CHUNK * 4;
+  uint64_t* full = reinterpret_cast<uint64_t*>(a8 + (p.a_fp8 ? (size_t)stages * DFL_WBLK8_BYTES : 0));
   uint64_t* empty = full + stages;
-  uint64_t* tfull = empty + stages;
+  uint64_t* conv = empty + stages;  // FP8: the stage's A converted (the MMA waits on this instead of full)
+  uint64_t* tfull = conv + stages;
   uint64_t* tempty = tfull + 2;
   uint64_t* mdone = tempty + 2;
   uint64_t* red = mdone + 1;  // split-K parts landed in red_buf
@@ -549,6 +560,7 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
     for (int s = 0; s < stages; ++s) {
       mbar_init(full + s, 1);
       mbar_init(empty + s, p.cl);  // every cluster CTA's MMAs release the stage
+      mbar_init(conv + s, CONV_THREADS);
     }
     mbar_init(tfull + 0, 1);
     mbar_init(tfull + 1, 1);
@@ -601,14 +613,15 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
       const int KBi = p.kblocks;
       const int n_units = (int)(u1 - u0);
       int tile = (int)(u0 / KB), kb = (int)(u0 % KB), tt = 0;
-      const uint16_t* a_ptr = nullptr;
+      const uint8_t* a_ptr = nullptr;
+      const int blk_bytes = p.a_fp8 ? DFL_WBLK8_BYTES : A_STAGE_BYTES;
       auto tile_base = [&]() {  // `tile` counts scheduled tiles here
         const int rest = tile / p.t_tiles;
         const int g = rest / p.n_tg;
         int nt = (rest % p.n_tg) * CL + crank;
         if (nt >= p.n_tiles) nt = p.n_tiles - 1;
         tt = tile % p.t_tiles;
-        a_ptr = static_cast<const uint16_t*>(p.a[g]) + ((size_t)(p.a_tile_off + nt) * KBi + kb) * DFL_WBLK_ELEMS;
+        a_ptr = static_cast<const uint8_t*>(p.a[g]) + ((size_t)(p.a_tile_off + nt) * KBi + kb) * blk_bytes;
       };
       tile_base();
       auto advance = [&]() {
@@ -617,20 +630,21 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
           ++tile;
           tile_base();
         } else {
-          a_ptr += DFL_WBLK_ELEMS;
+          a_ptr += blk_bytes;
         }
       };
       auto load_a = [&](int st) {
-        uint8_t* dst = sm + (size_t)st * stage_bytes;
-        constexpr int CH = A_STAGE_BYTES / DFL_GEMM_A_CHUNKS;
+        uint8_t* dst = p.a_fp8 ? a8 + (size_t)st * DFL_WBLK8_BYTES : sm + (size_t)st * stage_bytes;
+        const int CH = blk_bytes / DFL_GEMM_A_CHUNKS;
 #pragma unroll
         for (int ch = 0; ch < DFL_GEMM_A_CHUNKS; ++ch) {
           if (hint)
-            bulk_load_hint(dst + ch * CH, a_ptr + ch * (CH / 2), CH, full + st, pol);
+            bulk_load_hint(dst + ch * CH, a_ptr + ch * CH, CH, full + st, pol);
           else
-            bulk_load(dst + ch * CH, a_ptr + ch * (CH / 2), CH, full + st);
+            bulk_load(dst + ch * CH, a_ptr + ch * CH, CH, full + st);
         }
       };
+      const uint32_t fill_bytes = (uint32_t)(blk_bytes + BN * 128);  // A (as streamed) + the token tile
       // With a cluster, each CTA loads BN/CL token rows of the tile into every
       // peer's stage (same offsets): the cluster reads each token tile once.
       const int bq = BN / CL;
@@ -646,7 +660,7 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
       const int pre = n_units < stages ? n_units : stages;
       int pkb[DFL_GEMM_MAX_STAGES], ptt[DFL_GEMM_MAX_STAGES];
       for (int i = 0; i < pre; ++i) {
-        mbar_arrive_expect_tx(full + i, stage_bytes);
+        mbar_arrive_expect_tx(full + i, fill_bytes);
         load_a(i);
         pkb[i] = kb;
         ptt[i] = tt;
@@ -659,7 +673,7 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
       int issued = pre;
       for (; issued < n_units; ++issued) {
         if (!mbar_wait(empty + st, phase ^ 1u, p.status, &aborted)) break;
-        mbar_arrive_expect_tx(full + st, stage_bytes);
+        mbar_arrive_expect_tx(full + st, fill_bytes);
         load_a(st);
         load_b(st, kb, tt);
         advance();
@@ -705,7 +719,7 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
               phase ^= 1u;
             }
           }
-          if (!mbar_wait(full + s, phase, p.status, &aborted)) break;
+          if (!mbar_wait((p.a_fp8 ? conv : full) + s, phase, p.status, &aborted)) break;
           if (it == 0) trace_at(p, 2, globaltimer());
           tc_fence_after();
           const uint32_t a_addr = smem_u32(sm + (size_t)s * stage_bytes);
@@ -727,6 +741,49 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
       tc_commit(mdone);
       bool drain_abort = false;
       mbar_wait(mdone, 0, p.status, &drain_abort);
+    }
+  } else if (warp >= 6) {
+    // ------------------------------------------------ FP8 weight converters (warps 6, 7)
+    // Each landed 8 KB E4M3 block (row-major, 64 bytes a row) becomes the
+    // stage's f16 A operand in the 128-byte-swizzle layout the MMA reads.
+    if (p.a_fp8) {
+      const int ct = threadIdx.x - 192;  // 0 .. CONV_THREADS-1
+      int s = 0;
+      uint32_t phase = 0;
+      for (int u = u0, i = 0; u < u1; ++u, ++i) {
+        if (i > 0 && ++s == stages) {
+          s = 0;
+          phase ^= 1u;
+        }
+        if (!mbar_wait(full + s, phase, p.status, &aborted)) break;
+        const uint8_t* src = a8 + (size_t)s * DFL_WBLK8_BYTES;
+        uint8_t* dst = sm + (size_t)s * stage_bytes;
+        // all of this thread's loads first, then the conversions and stores
+        constexpr int NI = 128 * 4 / CONV_THREADS;  // 16-value items per thread
+        uint4 v[NI];
+#pragma unroll
+        for (int k = 0; k < NI; ++k) {
+          const int item = ct + k * CONV_THREADS;
+          v[k] = *reinterpret_cast<const uint4*>(src + (item >> 2) * 64 + (item & 3) * 16);
+        }
+#pragma unroll
+        for (int k = 0; k < NI; ++k) {
+          const int item = ct + k * CONV_THREADS;
+          const int row = item >> 2, c8 = item & 3;  // 16 E4M3 values -> two 16-byte f16 chunks
+          const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+          uint32_t hv[8];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            hv[2 * j] = e4m3x2_to_f16x2((uint16_t)(w[j] & 0xFFFFu));
+            hv[2 * j + 1] = e4m3x2_to_f16x2((uint16_t)(w[j] >> 16));
+          }
+          uint8_t* drow = dst + row * 128;
+          *reinterpret_cast<uint4*>(drow + (((2 * c8) ^ (row & 7)) << 4)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+          *reinterpret_cast<uint4*>(drow + (((2 * c8 + 1) ^ (row & 7)) << 4)) = make_uint4(hv[4], hv[5], hv[6], hv[7]);
+        }
+        fence_proxy_async_smem();  // the generic-proxy writes become visible to the MMA's reads
+        mbar_arrive(conv + s);
+      }
     }
   } else {
     // ------------------------------------------------ epilogue (warps 2..5)
@@ -934,15 +991,16 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
 
 // Split-K part chunks (8 KB) the reduction lands at once while the ring is
 // still in use: whatever shared memory the ring leaves, 4 to 16.
-int gemm_red_items(int BN, int stages) {
-  const long long left = 232448LL - 1024 - (long long)stages * (A_STAGE_BYTES + BN * 128) - STG_BYTES - 512;
+int gemm_red_items(int BN, int stages, int fp8) {
+  const long long left = 232448LL - 1024 - (long long)stages * (A_STAGE_BYTES + BN * 128 + (fp8 ? DFL_WBLK8_BYTES : 0)) -
+                         STG_BYTES - 512;
   const long long n = left / (RED_CHUNK * 4);
   return (int)(n < RED_PARTS ? RED_PARTS : (n > DFL_GEMM_RED_MAX ? DFL_GEMM_RED_MAX : n));
 }
 
-size_t gemm_smem_bytes(int BN, int stages) {
-  return 1024 + (size_t)stages * (A_STAGE_BYTES + BN * 128) + STG_BYTES +
-         (size_t)gemm_red_items(BN, stages) * RED_CHUNK * 4 + (size_t)(2 * stages + 6) * 8 + 16;
+size_t gemm_smem_bytes(int BN, int stages, int fp8) {
+  return 1024 + (size_t)stages * (A_STAGE_BYTES + BN * 128 + (fp8 ? DFL_WBLK8_BYTES : 0)) + STG_BYTES +
+         (size_t)gemm_red_items(BN, stages, fp8) * RED_CHUNK * 4 + (size_t)(3 * stages + 6) * 8 + 16;
 }
 
 // Weight-ring depth.  Six 16 KB stages per SM already keep HBM streaming at
@@ -950,9 +1008,9 @@ size_t gemm_smem_bytes(int BN, int stages) {
 // reduction's L2 round trips wait behind (measured: the Qwen3-8B-shaped round
 // is fastest at 6-7 stages, 2.5% slower at 12).  The lm_head, one long
 // stream with short tails, runs best at 8.
-int gemm_pick_stages(int BN, int mode) {
+int gemm_pick_stages(int BN, int mode, int fp8) {
   const size_t budget = 232448 - 1024 - STG_BYTES - RED_BYTES - 512;
-  int st = (int)(budget / (size_t)(A_STAGE_BYTES + BN * 128));
+  int st = (int)(budget / (size_t)(A_STAGE_BYTES + BN * 128 + (fp8 ? DFL_WBLK8_BYTES : 0)));
   const int cap = mode == GM_ARGMAX ? 8 : 6;
   st = st > cap ? cap : st;
   return st > DFL_GEMM_MAX_STAGES ? DFL_GEMM_MAX_STAGES : st;
@@ -972,7 +1030,7 @@ int gemm_max_clusters(int BN, int stages, int cl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(cl * 64));
   cfg.blockDim = dim3(DFL_GEMM_THREADS);
-  cfg.dynamicSmemBytes = gemm_smem_bytes(BN, stages);
+  cfg.dynamicSmemBytes = gemm_smem_bytes(BN, stages, 0);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)cl;
@@ -991,8 +1049,8 @@ int gemm_max_clusters(int BN, int stages, int cl) {
 cudaError_t gemm_launch(const CUtensorMap& B, const GemmParams& p, int grid, cudaStream_t s, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(DFL_GEMM_THREADS);
-  cfg.dynamicSmemBytes = gemm_smem_bytes(p.BN, p.stages);
+  cfg.blockDim = dim3(p.a_fp8 ? DFL_GEMM_THREADS : DFL_GEMM_THREADS - CONV_THREADS);  // converter warps for FP8 only
+  cfg.dynamicSmemBytes = gemm_smem_bytes(p.BN, p.stages, p.a_fp8);
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   int na = 0;

@@ -15,7 +15,9 @@ typedef __half f16;
 #define DFL_BLOCK 16
 #define DFL_PAGE 64
 #define DFL_BN_MAX 256
-#define DFL_GEMM_THREADS 192
+#define DFL_GEMM_THREADS 256  // producer, MMA, 4 epilogue warps, 2 FP8-weight converter warps
+// One packed FP8 weight block: 128 rows x 64 bytes, row-major (8 KB).
+#define DFL_WBLK8_BYTES (128 * 64)
 // One packed weight block: 128 rows x 64 columns of 16-bit values (16 KB).
 #define DFL_WBLK_ELEMS (128 * 64)
 
@@ -59,6 +61,8 @@ struct GemmParams {
   int tmem_cols;    // power of two >= max(32, 2*BN)
   uint32_t ab_type; // 0: f16 operands, 1: bf16 operands
   const void* a[DFL_MAX_LAYERS];  // packed A blocks [tiles][kblocks][128x64] per group
+  int a_fp8;                      // 1: A blocks are FP8 E4M3 (8 KB, row-major), converted to f16 in the SM
+  const float* a_scale[DFL_MAX_LAYERS];  // a_fp8: per packed row scale [tiles * 128] per group
   int a_tile_off;   // first packed tile of the range (inject: hq*D/128)
   int mode;
   // shapes for epilogues
@@ -130,9 +134,9 @@ struct AttnParams {
 };
 
 // host launchers (gemm.cu / attention.cu / small.cu)
-size_t gemm_smem_bytes(int BN, int stages);
-int gemm_red_items(int BN, int stages);
-int gemm_pick_stages(int BN, int mode);
+size_t gemm_smem_bytes(int BN, int stages, int fp8);
+int gemm_red_items(int BN, int stages, int fp8);
+int gemm_pick_stages(int BN, int mode, int fp8);
 cudaError_t gemm_launch(const CUtensorMap& B, const GemmParams& p, int grid, cudaStream_t s, bool pdl);
 // Clusters of `cl` GEMM CTAs (token tile BN, `stages` ring) the GPU holds at once.
 int gemm_max_clusters(int BN, int stages, int cl);
@@ -152,6 +156,10 @@ cudaError_t attn_init_attributes();
 cudaError_t launch_pack_weight(const bf16* src, void* dst, int N, int K, int n_tiles, int swiglu_I, bool to_f16,
                                cudaStream_t s);
 cudaError_t launch_gain_f32(const bf16* src, float* dst, int n, cudaStream_t s);
+// FP8 E4M3 packing with per-row scales (packed row order): scale = max|row| / 448,
+// q = E4M3(w / scale) rounded to nearest even, saturating.
+cudaError_t launch_pack_weight_fp8(const bf16* src, uint8_t* dst, float* scale, int N, int K, int n_tiles,
+                                   int swiglu_I, cudaStream_t s);
 
 // Positions, pages and RoPE rows of a round's block tokens: the same for
 // every layer, so the embedding kernel writes them once for the layers' QKV
@@ -171,7 +179,8 @@ struct BlockCtx {
   float2* brope;
 };
 cudaError_t launch_embed(const int* slots, int batch, const int* last_tok, int mask_id, int vocab,
-                         const f16* embed_pk, const float* gain, int H, float* h, f16* hg, float* ss,
+                         const void* embed_pk, const float* embed_scale, const float* gain, int H, float* h, f16* hg,
+                         float* ss,
                          unsigned long long* keys, const BlockCtx& bc, uint32_t* status, cudaStream_t s);
 cudaError_t launch_page_alloc(const int* slots, int batch, int S, const int* n_new, int rows_per_req, int* ctx_len,
                               int* pos0, int* n_pages, int* page_table, int max_pages_per_slot,

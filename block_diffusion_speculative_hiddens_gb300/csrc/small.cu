@@ -2,6 +2,8 @@
 // slot reset, RoPE table, cache read-back and the benchmark's stand-in verify.
 #include <algorithm>
 
+#include <cuda_fp8.h>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -49,6 +51,47 @@ __global__ void k_pack_weight(const bf16* __restrict__ src, uint16_t* __restrict
   }
 }
 
+// FP8 packing, pass 1: one warp per packed row -- the row's scale
+// max|w| / 448 (1 for an all-zero or padding row).
+__global__ void k_fp8_scale(const bf16* __restrict__ src, float* __restrict__ scale, int N, int K, int n_rows,
+                            int swiglu_I) {
+  const int pr = (int)((blockIdx.x * (unsigned)blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (pr >= n_rows) return;
+  const int tile = pr >> 7, r = pr & 127;
+  const int row = swiglu_I > 0 ? (r < 64 ? tile * 64 + r : swiglu_I + tile * 64 + (r - 64)) : pr;
+  float m = 0.f;
+  if (row < N)
+    for (int k = lane; k < K; k += 32) m = fmaxf(m, fabsf(__bfloat162float(src[(size_t)row * K + k])));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (lane == 0) scale[pr] = m > 0.f ? __fdiv_rn(m, 448.f) : 1.f;
+}
+
+// FP8 packing, pass 2: 16 weights per thread, w / scale (correctly rounded)
+// to E4M3 (nearest even, saturating), blocks of 128 rows x 64 bytes.
+__global__ void k_pack_fp8(const bf16* __restrict__ src, const float* __restrict__ scale, uint8_t* __restrict__ dst,
+                           int N, int K, int n_tiles, int swiglu_I) {
+  const int KB = K / 64;
+  const long long total = (long long)n_tiles * KB * 128 * 4;  // 16-value chunks
+  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const int c = (int)(idx & 3);
+    const int r = (int)((idx >> 2) & 127);
+    const long long blk = idx >> 9;
+    const int tile = (int)(blk / KB), kb = (int)(blk % KB);
+    const int row = swiglu_I > 0 ? (r < 64 ? tile * 64 + r : swiglu_I + tile * 64 + (r - 64)) : tile * 128 + r;
+    uint8_t q[16];
+    const float sc = scale[tile * 128 + r];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float w = row < N ? __bfloat162float(src[(size_t)row * K + kb * 64 + c * 16 + i]) : 0.f;
+      q[i] = (uint8_t)__nv_cvt_float_to_fp8(__fdiv_rn(w, sc), __NV_SATFINITE, __NV_E4M3);
+    }
+    *reinterpret_cast<uint4*>(dst + blk * DFL_WBLK8_BYTES + r * 64 + c * 16) = *reinterpret_cast<const uint4*>(q);
+  }
+}
+
 __global__ void k_gain_f32(const bf16* __restrict__ src, float* __restrict__ dst, int n) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n) dst[i] = __bfloat162float(src[i]);
@@ -59,8 +102,9 @@ __global__ void k_gain_f32(const bf16* __restrict__ src, float* __restrict__ dst
 // squares of h, the form the first layer's QKV GEMM consumes.  Also clears
 // the argmax keys.
 __global__ void k_embed(const int* __restrict__ slots, const int* __restrict__ last_tok, int mask_id, int vocab,
-                        const f16* __restrict__ E, const float* __restrict__ gain, int H, int M, float* h, f16* hg,
-                        float* ss, unsigned long long* keys, const BlockCtx bc, uint32_t* status) {
+                        const void* __restrict__ Ev, const float* __restrict__ escale, const float* __restrict__ gain,
+                        int H, int M, float* h, f16* hg, float* ss, unsigned long long* keys, const BlockCtx bc,
+                        uint32_t* status) {
   pdl_launch_dependents();
   pdl_wait();
   const int t = blockIdx.x;
@@ -77,14 +121,19 @@ __global__ void k_embed(const int* __restrict__ slots, const int* __restrict__ l
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
   const int KB = H / 64;
-  const f16* tile = E + (size_t)(tok >> 7) * KB * DFL_WBLK_ELEMS;
   const int r = tok & 127;
+  // the tied table: packed f16 blocks, or FP8 blocks (row-major) with a scale per vocabulary row
+  const f16* tile = static_cast<const f16*>(Ev) + (size_t)(tok >> 7) * KB * DFL_WBLK_ELEMS;
+  const uint8_t* tile8 = static_cast<const uint8_t*>(Ev) + (size_t)(tok >> 7) * KB * DFL_WBLK8_BYTES;
+  const float es = escale ? escale[tok] : 1.f;
   for (int part = warp; part < H / 128; part += nw) {
     float sq = 0.f;
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) {
       const int n = part * 128 + lane + 32 * jj;
-      const float v = __half2float(tile[(size_t)(n >> 6) * DFL_WBLK_ELEMS + wpack_off(r, n & 63)]);
+      const float v = escale ? __half2float(__ushort_as_half((unsigned short)(e4m3x2_to_f16x2(
+                                   tile8[(size_t)(n >> 6) * DFL_WBLK8_BYTES + r * 64 + (n & 63)]) & 0xFFFFu))) * es
+                             : __half2float(tile[(size_t)(n >> 6) * DFL_WBLK_ELEMS + wpack_off(r, n & 63)]);
       h[(size_t)t * H + n] = v;
       hg[(size_t)t * H + n] = to_f16(v * gain[n], status);
       sq += v * v;
@@ -331,21 +380,33 @@ cudaError_t launch_pack_weight(const bf16* src, void* dst, int N, int K, int n_t
   return cudaGetLastError();
 }
 
+cudaError_t launch_pack_weight_fp8(const bf16* src, uint8_t* dst, float* scale, int N, int K, int n_tiles,
+                                   int swiglu_I, cudaStream_t s) {
+  const int rows = n_tiles * 128;
+  k_fp8_scale<<<(rows * 32 + 255) / 256, 256, 0, s>>>(src, scale, N, K, rows, swiglu_I);
+  cudaError_t e = cudaGetLastError();
+  if (e) return e;
+  const long long total = (long long)n_tiles * (K / 64) * 128 * 4;
+  const long long blocks = std::min<long long>((total + 255) / 256, 1LL << 20);
+  k_pack_fp8<<<(unsigned)blocks, 256, 0, s>>>(src, scale, dst, N, K, n_tiles, swiglu_I);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_gain_f32(const bf16* src, float* dst, int n, cudaStream_t s) {
   k_gain_f32<<<(n + 255) / 256, 256, 0, s>>>(src, dst, n);
   return cudaGetLastError();
 }
 
 cudaError_t launch_embed(const int* slots, int batch, const int* last_tok, int mask_id, int vocab,
-                         const f16* embed_pk, const float* gain, int H, float* h, f16* hg, float* ss,
-                         unsigned long long* keys, const BlockCtx& bc, uint32_t* status, cudaStream_t s) {
+                         const void* embed_pk, const float* embed_scale, const float* gain, int H, float* h, f16* hg,
+                         float* ss, unsigned long long* keys, const BlockCtx& bc, uint32_t* status, cudaStream_t s) {
   cudaLaunchAttribute a[1];
   const int M = batch * DFL_BLOCK;
   int threads = (H / 128) * 32;
   if (threads > 1024) threads = 1024;
   cudaLaunchConfig_t c = cfg_of(dim3(M), dim3(threads), s, a);
-  return cudaLaunchKernelEx(&c, k_embed, slots, last_tok, mask_id, vocab, embed_pk, gain, H, M, h, hg, ss, keys, bc,
-                            status);
+  return cudaLaunchKernelEx(&c, k_embed, slots, last_tok, mask_id, vocab, embed_pk, embed_scale, gain, H, M, h, hg,
+                            ss, keys, bc, status);
 }
 
 cudaError_t launch_page_alloc(const int* slots, int batch, int S, const int* n_new, int rows_per_req, int* ctx_len,

@@ -98,6 +98,12 @@ typedef struct dflash_config {
                                  for dflash_verify_block / dflash_advance -- causal attention
                                  over its own paged cache, n_layers >= n_fused + 2, block 16,
                                  no fusion weights (fc, fc_norm may be null) */
+  int32_t weight_fp8;         /* 1: every projection and the tied embedding held as FP8 E4M3
+                                 with a float32 scale per output row (max |row| / 448, values
+                                 rounded to nearest even, saturating), converted to f16 in the
+                                 SM before each MMA, the scale applied in the epilogue; the
+                                 fusion projection stays bf16.  Halves the weight bytes a round
+                                 streams.  0: f16 (as below) */
 } dflash_config;
 
 /* Device pointers to the drafter weights, all bf16 and row-major; the arrays

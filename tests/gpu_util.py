@@ -34,7 +34,7 @@ class GpuRun:
     """CUDA-path driver: prefill every request, then rounds with the stand-in verify."""
 
     def __init__(self, cfg, rounds: int, weights_np=None, batch_ids=None, prefill_chunk=4096,
-                 ctx=None, attn_impl: int = 0, temperature: float = 0.0, seed: int = 0):
+                 ctx=None, attn_impl: int = 0, temperature: float = 0.0, seed: int = 0, weight_fp8: int = 0):
         import torch
         from block_diffusion_speculative_hiddens_gb300 import Drafter, weights_to_device
         from block_diffusion_speculative_hiddens_gb300.session import RoundState, SyntheticVerify
@@ -51,7 +51,7 @@ class GpuRun:
         self.chunk = min(prefill_chunk, int(self.ctx0.max()))
         self.d = Drafter(cfg, self.w_dev, max_batch=B, max_slots=B, max_pages=mpps * B,
                          max_pages_per_slot=mpps, max_rows=max(self.chunk, B * cfg.block),
-                         attn_impl=attn_impl)
+                         attn_impl=attn_impl, weight_fp8=weight_fp8)
         dev = torch.device("cuda:0")
         self.dev = dev
         # feature stream: every position a request can reach
@@ -117,14 +117,14 @@ class GpuRun:
 
 class OracleRun:
     def __init__(self, cfg, rounds: int, weights_np=None, batch_ids=None, ctx=None, cache=True,
-                 temperature: float = 0.0, seed: int = 0):
+                 temperature: float = 0.0, seed: int = 0, weight_fp8: int = 0):
         self.temperature = temperature
         self.seed = seed
         self.cfg = cfg
         self.ids = list(range(cfg.batch)) if batch_ids is None else list(batch_ids)
         self.ctx0 = (context_lengths(cfg)[self.ids] if ctx is None else np.asarray(ctx)).astype(int)
         w = make_weights(cfg) if weights_np is None else weights_np
-        self.model = O.OracleModel(cfg, w, cache=cache)
+        self.model = O.OracleModel(cfg, w, cache=cache, fp8=bool(weight_fp8))
         self.dr = O.OracleDrafter(self.model)
         self.reqs = [O.OracleRequest(cfg, int(L) + cfg.block * (rounds + 2)) for L in self.ctx0]
         self.last = [cfg.first_token] * len(self.ids)

@@ -121,6 +121,29 @@ def test_global_merge_round_matches_oracle(lib, attn_impl):
     assert g.d.read_status() == 0
 
 
+@pytest.mark.parametrize("name", ["tiny-gains", "small-batch", "small-b16"])
+def test_fp8_weights_round_matches_oracle(lib, name):
+    """FP8 E4M3 weights with per-row scales (converted to f16 in the SM before
+    each MMA) against the oracle computing with the same dequantised weights:
+    injected K/V, hidden states, logits, drafts and acceptance."""
+    cfg, g, o = _pair(name, 2, weight_fp8=1)
+    for j in range(len(g.ids)):
+        L = int(g.ctx0[j])
+        k, v = g.d.read_kv(0, j, 0, L)
+        ok, ov = o.reqs[j].ctx(0)
+        assert rel_l2(to_np(k), ok) < TOL_REL_L2 and rel_l2(to_np(v), ov) < TOL_REL_L2, j
+    for r in range(2):
+        go = g.round(debug=True)
+        oo = o.round(want_logits=True)
+        for j, od in enumerate(oo):
+            assert rel_l2(go["hidden"][j], od["hidden"]) < TOL_REL_L2, (r, j)
+            assert rel_l2(go["logits"][j, 1:], od["logits"]) < TOL_REL_L2, (r, j)
+            assert np.array_equal(go["draft"][j], np.argmax(go["logits"][j, 1:], -1))
+            check_drafts(go["draft"][j], od)
+            assert (go["tau"][j], go["bonus"][j], go["ctx"][j]) == (od["tau"], od["bonus"], od["ctx"]), (r, j)
+    assert g.d.read_status() == 0
+
+
 @pytest.mark.parametrize("T", [0.7, 1.5])
 @pytest.mark.parametrize("name", ["tiny-gains", "small-batch"])
 def test_sampled_drafts_match_oracle(lib, name, T):
