@@ -53,7 +53,9 @@ constexpr int RED_PARTS = 4;               // fewest split-K part chunks the red
 constexpr int RED_CHUNK = 16 * 128;        // floats of one part's 16-column chunk (8 KB)
 constexpr int RED_BYTES = RED_PARTS * RED_CHUNK * 4;
 constexpr int EPI_THREADS = 128;
-constexpr int CONV_THREADS = 64;  // warps 6, 7
+constexpr int GEMM_THREADS = 192;       // producer, MMA, 4 epilogue warps
+constexpr int CONV_THREADS = 64;        // FP8 kernels: 2 more warps convert the weight blocks
+constexpr int GEMM_THREADS_FP8 = GEMM_THREADS + CONV_THREADS;
 
 // Unit arithmetic is 32-bit: the host guarantees units * grid < 2^31.
 DFL_DEV int unit_start(int c, int U, int G) { return c * U / G; }
@@ -528,8 +530,8 @@ DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, con
   }
 }
 
-template <int MODE>
-__global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
+template <int MODE, bool FP8>
+__global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -746,8 +748,8 @@ __global__ void __launch_bounds__(DFL_GEMM_THREADS, 1)
     // ------------------------------------------------ FP8 weight converters (warps 6, 7)
     // Each landed 8 KB E4M3 block (row-major, 64 bytes a row) becomes the
     // stage's f16 A operand in the 128-byte-swizzle layout the MMA reads.
-    if (p.a_fp8) {
-      const int ct = threadIdx.x - 192;  // 0 .. CONV_THREADS-1
+    if constexpr (FP8) {
+      const int ct = threadIdx.x - GEMM_THREADS;  // 0 .. CONV_THREADS-1
       int s = 0;
       uint32_t phase = 0;
       for (int u = u0, i = 0; u < u1; ++u, ++i) {
@@ -1018,18 +1020,24 @@ int gemm_pick_stages(int BN, int mode, int fp8) {
 
 cudaError_t gemm_init_attributes() {
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(k_gemm<GM_QKV>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448))) return e;
-  if ((e = cudaFuncSetAttribute(k_gemm<GM_INJECT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448))) return e;
-  if ((e = cudaFuncSetAttribute(k_gemm<GM_RESID>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448))) return e;
-  if ((e = cudaFuncSetAttribute(k_gemm<GM_SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448))) return e;
-  if ((e = cudaFuncSetAttribute(k_gemm<GM_FC>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448))) return e;
-  return cudaFuncSetAttribute(k_gemm<GM_ARGMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+  const int A = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  if ((e = cudaFuncSetAttribute(k_gemm<GM_QKV, false>, (cudaFuncAttribute)A, 232448))) return e;
+  if ((e = cudaFuncSetAttribute(k_gemm<GM_INJECT, false>, (cudaFuncAttribute)A, 232448))) return e;
+  if ((e = cudaFuncSetAttribute(k_gemm<GM_RESID, false>, (cudaFuncAttribute)A, 232448))) return e;
+  if ((e = cudaFuncSetAttribute(k_gemm<GM_SWIGLU, false>, (cudaFuncAttribute)A, 232448))) return e;
+  if ((e = cudaFuncSetAttribute(k_gemm<GM_FC, false>, (cudaFuncAttribute)A, 232448))) return e;
+  if ((e = cudaFuncSetAttribute(k_gemm<GM_ARGMAX, false>, (cudaFuncAttribute)A, 232448))) return e;
+  if ((e = cudaFuncSetAttribute(k_gemm<GM_QKV, true>, (cudaFuncAttribute)A, 232448))) return e;
+  if ((e = cudaFuncSetAttribute(k_gemm<GM_INJECT, true>, (cudaFuncAttribute)A, 232448))) return e;
+  if ((e = cudaFuncSetAttribute(k_gemm<GM_RESID, true>, (cudaFuncAttribute)A, 232448))) return e;
+  if ((e = cudaFuncSetAttribute(k_gemm<GM_SWIGLU, true>, (cudaFuncAttribute)A, 232448))) return e;
+  return cudaFuncSetAttribute(k_gemm<GM_ARGMAX, true>, (cudaFuncAttribute)A, 232448);
 }
 
 int gemm_max_clusters(int BN, int stages, int cl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(cl * 64));
-  cfg.blockDim = dim3(DFL_GEMM_THREADS);
+  cfg.blockDim = dim3(GEMM_THREADS);
   cfg.dynamicSmemBytes = gemm_smem_bytes(BN, stages, 0);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1039,7 +1047,7 @@ int gemm_max_clusters(int BN, int stages, int cl) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, k_gemm<GM_ARGMAX>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, k_gemm<GM_ARGMAX, false>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -1049,7 +1057,7 @@ int gemm_max_clusters(int BN, int stages, int cl) {
 cudaError_t gemm_launch(const CUtensorMap& B, const GemmParams& p, int grid, cudaStream_t s, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(p.a_fp8 ? DFL_GEMM_THREADS : DFL_GEMM_THREADS - CONV_THREADS);  // converter warps for FP8 only
+  cfg.blockDim = dim3(p.a_fp8 ? GEMM_THREADS_FP8 : GEMM_THREADS);  // converter warps for FP8 weights only
   cfg.dynamicSmemBytes = gemm_smem_bytes(p.BN, p.stages, p.a_fp8);
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
@@ -1069,12 +1077,17 @@ cudaError_t gemm_launch(const CUtensorMap& B, const GemmParams& p, int grid, cud
   cfg.attrs = attr;
   cfg.numAttrs = (unsigned)na;
   switch (p.mode) {
-    case GM_QKV: return cudaLaunchKernelEx(&cfg, k_gemm<GM_QKV>, B, p);
-    case GM_INJECT: return cudaLaunchKernelEx(&cfg, k_gemm<GM_INJECT>, B, p);
-    case GM_RESID: return cudaLaunchKernelEx(&cfg, k_gemm<GM_RESID>, B, p);
-    case GM_SWIGLU: return cudaLaunchKernelEx(&cfg, k_gemm<GM_SWIGLU>, B, p);
-    case GM_FC: return cudaLaunchKernelEx(&cfg, k_gemm<GM_FC>, B, p);
-    case GM_ARGMAX: return cudaLaunchKernelEx(&cfg, k_gemm<GM_ARGMAX>, B, p);
+    case GM_QKV: return p.a_fp8 ? cudaLaunchKernelEx(&cfg, k_gemm<GM_QKV, true>, B, p)
+                                : cudaLaunchKernelEx(&cfg, k_gemm<GM_QKV, false>, B, p);
+    case GM_INJECT: return p.a_fp8 ? cudaLaunchKernelEx(&cfg, k_gemm<GM_INJECT, true>, B, p)
+                                   : cudaLaunchKernelEx(&cfg, k_gemm<GM_INJECT, false>, B, p);
+    case GM_RESID: return p.a_fp8 ? cudaLaunchKernelEx(&cfg, k_gemm<GM_RESID, true>, B, p)
+                                  : cudaLaunchKernelEx(&cfg, k_gemm<GM_RESID, false>, B, p);
+    case GM_SWIGLU: return p.a_fp8 ? cudaLaunchKernelEx(&cfg, k_gemm<GM_SWIGLU, true>, B, p)
+                                   : cudaLaunchKernelEx(&cfg, k_gemm<GM_SWIGLU, false>, B, p);
+    case GM_FC: return cudaLaunchKernelEx(&cfg, k_gemm<GM_FC, false>, B, p);  // the fusion projection stays bf16
+    case GM_ARGMAX: return p.a_fp8 ? cudaLaunchKernelEx(&cfg, k_gemm<GM_ARGMAX, true>, B, p)
+                                   : cudaLaunchKernelEx(&cfg, k_gemm<GM_ARGMAX, false>, B, p);
   }
   return cudaErrorInvalidValue;
 }

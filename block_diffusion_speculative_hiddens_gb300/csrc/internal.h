@@ -15,7 +15,6 @@ typedef __half f16;
 #define DFL_BLOCK 16
 #define DFL_PAGE 64
 #define DFL_BN_MAX 256
-#define DFL_GEMM_THREADS 256  // producer, MMA, 4 epilogue warps, 2 FP8-weight converter warps
 // One packed FP8 weight block: 128 rows x 64 bytes, row-major (8 KB).
 #define DFL_WBLK8_BYTES (128 * 64)
 // One packed weight block: 128 rows x 64 columns of 16-bit values (16 KB).
