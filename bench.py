@@ -207,6 +207,21 @@ def oracle_round_seconds(cfg, budget_s: float, max_rounds: int):
 
 # ------------------------------------------------------------------ GPU arm
 
+def max_over_ranks(value: float, world: int, device) -> float:
+    """The largest of every rank's value (the job's time is its slowest replica's)."""
+    if world <= 1:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_rate(units_per_rank: float, world: int, seconds: float) -> float:
+    """Whole-job throughput of `world` replicas: all ranks' units over the slowest time."""
+    return units_per_rank * world / seconds
+
+
 def run_gpu(args, rank, world, local_rank):
     import numpy as np
     import torch
@@ -320,10 +335,7 @@ def run_gpu(args, rank, world, local_rank):
     for g in range(n_groups - 1):
         if min(R, K - g * R) > 0:
             accepted += int((states[g].ctx_len.cpu().numpy() - ctx).sum())
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, dev)
 
     # ---- the stand-in verify on its own, and the per-round distribution: one
     # more graph of up to R rounds on a fresh copy of the prompts, with
@@ -411,11 +423,8 @@ def run_gpu(args, rank, world, local_rank):
         h2d = feats_h.numel() * 2 + mu_h.numel() * 4
         d2h = out_h.numel() * 4
         t_e2e = time.perf_counter() - t0
-        if world > 1:
-            t = torch.tensor([t_e2e], dtype=torch.float64, device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            t_e2e = float(t.item())
-        e2e = {"value": round((S - 1) * B * E * world / t_e2e, 1), "unit": "tok/s", "h2d_bytes_per_step": h2d,
+        t_e2e = max_over_ranks(t_e2e, world, dev)
+        e2e = {"value": round(replica_rate((S - 1) * B * E, world, t_e2e), 1), "unit": "tok/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": E,
                "round_us": round(t_e2e / E * 1e6, 1),
                "note": "includes the stand-in verify kernel"}
@@ -460,7 +469,7 @@ def run_gpu(args, rank, world, local_rank):
     p_desc = f"match p {cfg.match_p}" if cfg.match_p is not None else f"match p U[{cfg.p_range[0]}, {cfg.p_range[1]}]"
     res = {
         "metric": METRIC,
-        "value": round((S - 1) * B * world / (round_ms * 1e-3), 1),
+        "value": round(replica_rate((S - 1) * B, world, round_ms * 1e-3), 1),
         "unit": "tok/s",
         "n_gpus": world,
         "steps": K,
