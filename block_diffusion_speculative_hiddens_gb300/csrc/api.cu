@@ -201,9 +201,12 @@ int pick_attn_splits(const dflash_config& c, int num_sms) {
 #ifndef DFL_ATTN_GLOBAL
 #define DFL_ATTN_GLOBAL 1
 #endif
+#ifndef DFL_ATTN_BATCH_SPLITS  // splits per (request, KV head) when the pairs alone fill the SMs
+#define DFL_ATTN_BATCH_SPLITS 1
+#endif
 int global_attn_splits(const dflash_config& c, int num_sms) {
   const int pairs = c.max_batch * c.n_kv_heads;
-  int want = num_sms / pairs;
+  int want = pairs >= num_sms ? DFL_ATTN_BATCH_SPLITS : num_sms / pairs;
   want = std::min(want, std::max(1, c.max_pages_per_slot / 4));
   return std::max(1, std::min(want, 32));
 }
