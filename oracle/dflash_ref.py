@@ -13,7 +13,7 @@ Round structure ([Code walkthrough] §三 第1-3步; [Paper walkthrough] 设计)
   a7 accept    longest matching prefix (cumulative product), bonus = target
                token at the first mismatch, context length += accepted count
 
-Readings where the pages are silent (each listed in the design doc):
+Readings where the pages are silent:
   mask id = vocab-1; the 5 layers concatenate shallow->deep; fusion has no
   bias and its RMSNorm has a learned gain; c enters W_k/W_v without a norm;
   Qwen3-style layer (per-head q/k RMSNorm, SiLU-gated MLP, final norm);
