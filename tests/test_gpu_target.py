@@ -102,3 +102,48 @@ def test_speculative_generation_is_the_greedy_output(lib, mode):
     if mode == "corrupt":
         assert max(sd.taus) > 1
     assert t.read_status() == 0 and d.read_status() == 0
+
+
+def test_verify_block_batch_of_two_with_ragged_chunks(lib):
+    """Two requests verified together, their last chunks of different lengths
+    (37 and 33 prompt tokens): every request matches its own oracle."""
+    import torch
+    from block_diffusion_speculative_hiddens_gb300 import Drafter, weights_to_device
+    cfg = get_config("tiny-gains")
+    tw = make_target_weights(cfg, NL)
+    mpps = 8
+    t = Drafter(cfg, weights_to_device(tw), max_batch=2, max_slots=2, max_pages=2 * mpps, max_pages_per_slot=mpps,
+                max_rows=16, role=1)
+    tm = O.OracleModel(cfg, tw)
+    prompts = [prompt_tokens(cfg, 4, 37), prompt_tokens(cfg, 5, 33)]
+    ots = [T.OracleTarget(tm, NL, 128) for _ in prompts]
+    dev = torch.device("cuda:0")
+    i32 = dict(dtype=torch.int32, device=dev)
+    slots = torch.tensor([0, 1], **i32)
+    tokens = torch.zeros(2, 16, **i32)
+    out = torch.zeros(2, 16, **i32)
+    nv = torch.zeros(2, **i32)
+    feats = torch.zeros(2, 16, cfg.n_fused * cfg.hidden, dtype=torch.bfloat16, device=dev)
+    for p0 in range(0, 37, 16):
+        chunks = [p[p0:p0 + 16] for p in prompts]
+        tokens.zero_()
+        for b, ch in enumerate(chunks):
+            tokens[b, :len(ch)] = torch.tensor(ch, dtype=torch.int32)
+            nv[b] = len(ch)
+        t.verify_block(slots, tokens, out, nv, feats)
+        t.advance(slots, nv)
+        for b, ch in enumerate(chunks):
+            o = ots[b].forward(ch)
+            ots[b].advance(len(ch))
+            n = len(ch)
+            got = to_np(out)[b, :n]
+            strong = o["margin"] > MARGIN
+            assert np.array_equal(got[strong], o["tok"][strong]), (p0, b)
+            f = to_np(feats)[b, :n].reshape(n, cfg.n_fused, cfg.hidden)
+            assert rel_l2(f, o["feats"]) < TOL_REL_L2, (p0, b)
+    lens = to_np(t.slot_lengths(slots))
+    assert lens.tolist() == [37, 33]
+    for b in range(2):
+        k, v = t.read_kv(NL - 1, b, 0, int(lens[b]))
+        assert rel_l2(to_np(k), ots[b].K[NL - 1][:lens[b]]) < TOL_REL_L2, b
+    assert t.read_status() == 0
