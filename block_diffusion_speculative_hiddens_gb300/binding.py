@@ -325,8 +325,10 @@ def weights_to_device(w_np: dict, device: int = 0) -> dict:
     import torch
 
     def t(a):
-        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(
-            f"cuda:{device}")
+        a = np.ascontiguousarray(a)
+        if not a.flags.writeable:  # memory-mapped cache files: copy once instead of aliasing read-only memory
+            a = a.copy()
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(f"cuda:{device}")
 
     out = {k: t(v) for k, v in w_np.items() if k != "layers"}
     out["layers"] = [{k: t(v) for k, v in lw.items()} for lw in w_np["layers"]]
