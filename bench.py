@@ -222,6 +222,12 @@ def replica_rate(units_per_rank: float, world: int, seconds: float) -> float:
     return units_per_rank * world / seconds
 
 
+def roofline_bound(flops: float, nbytes: float, hbm_gbs: float, tflops: float) -> str:
+    """"hbm" when a kernel's arithmetic intensity (flops per algorithmic byte)
+    is below the ridge point of the two peaks, else "tensor"."""
+    return "hbm" if flops / nbytes < tflops * 1e12 / (hbm_gbs * 1e9) else "tensor"
+
+
 def run_gpu(args, rank, world, local_rank):
     import numpy as np
     import torch
@@ -454,7 +460,7 @@ def run_gpu(args, rank, world, local_rank):
     layer_params = cfg.qkv_rows * H + H * cfg.n_q_heads * D + 3 * cfg.intermediate * H
     inj_params = H * F + cfg.n_layers * 2 * cfg.n_kv_heads * D * H
     round_flops = 2.0 * M * (cfg.n_layers * layer_params + V * H) + 2.0 * B * tau * inj_params
-    if B == 1:
+    if roofline_bound(lm_flops, lm_bytes, hbm, tf_sust) == "hbm":
         lm_roof = {"bound": "hbm", "achieved": round(lm_bytes / (lm_avg_ms * 1e-3) / 1e9, 1), "peak": hbm,
                    "unit": "GB/s", "frac": round(lm_bytes / (lm_avg_ms * 1e-3) / 1e9 / hbm, 4),
                    "traffic": None if fp8 else lm_head_traffic(cfg), "peak_source": f"{peak_src} copy bandwidth"}
