@@ -280,14 +280,28 @@ def run_gpu(args, rank, world, local_rank):
                 weight_fp8=1 if args.weights == "fp8" else 0)
     stream = torch.cuda.Stream(device=dev)
 
-    def prefill(g):
+    def prefill(g, timed=False):
+        """Inject every prompt of slot group g in chunks; with timed, returns
+        the device time (ms) of the fuse_inject calls alone."""
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)] if timed else None
         with torch.cuda.stream(stream):
+            calls = []
             for b in range(B):
                 slot = torch.tensor([g * B + b], dtype=torch.int32, device=dev)
                 for p0 in range(0, int(ctx[b]), chunk):
                     n = min(chunk, int(ctx[b]) - p0)
-                    d.fuse_inject(slot, feat_stream[b:b + 1, p0:p0 + n], n,
-                                  torch.tensor([n], dtype=torch.int32, device=dev), stream)
+                    calls.append((slot, b, p0, n, torch.tensor([n], dtype=torch.int32, device=dev)))
+            if timed:
+                stream.synchronize()
+                ev[0].record(stream)
+            for slot, b, p0, n, n_dev in calls:
+                d.fuse_inject(slot, feat_stream[b:b + 1, p0:p0 + n], n, n_dev, stream)
+            if timed:
+                ev[1].record(stream)
+        if timed:
+            ev[1].synchronize()
+            return ev[0].elapsed_time(ev[1])
+        return None
 
     states, verifies = [], []
     for g in range(n_groups):
@@ -352,7 +366,7 @@ def run_gpu(args, rank, world, local_rank):
     gi = n_groups - 1
     for b in range(B):
         d.reset_slot(gi * B + b, stream)
-    prefill(gi)
+    prefill_ms = prefill(gi, timed=True)
     st_i = RoundState(d, B, slots=[gi * B + b for b in range(B)], first_token=cfg.first_token)
     ver_i = SyntheticVerify(st_i, match, offs, feat_stream)
     if args.temperature > 0:
@@ -460,6 +474,7 @@ def run_gpu(args, rank, world, local_rank):
     layer_params = cfg.qkv_rows * H + H * cfg.n_q_heads * D + 3 * cfg.intermediate * H
     inj_params = H * F + cfg.n_layers * 2 * cfg.n_kv_heads * D * H
     round_flops = 2.0 * M * (cfg.n_layers * layer_params + V * H) + 2.0 * B * tau * inj_params
+    prefill_flops = 2.0 * float(ctx.sum()) * inj_params
     if roofline_bound(lm_flops, lm_bytes, hbm, tf_sust) == "hbm":
         lm_roof = {"bound": "hbm", "achieved": round(lm_bytes / (lm_avg_ms * 1e-3) / 1e9, 1), "peak": hbm,
                    "unit": "GB/s", "frac": round(lm_bytes / (lm_avg_ms * 1e-3) / 1e9 / hbm, 4),
@@ -514,6 +529,10 @@ def run_gpu(args, rank, world, local_rank):
         "round_tensor": {"flops_per_round": round_flops, "achieved_tflops": round(
             round_flops / (round_ms * 1e-3) / 1e12, 1), "peak": tf_sust,
             "frac": round(round_flops / (round_ms * 1e-3) / 1e12 / tf_sust, 4)},
+        "prefill": {"tokens": int(ctx.sum()), "us": round(prefill_ms * 1e3, 1),
+                    "tok_s": round(float(ctx.sum()) / (prefill_ms * 1e-3), 1),
+                    "flops": prefill_flops, "tensor_frac": round(prefill_flops / (prefill_ms * 1e-3) / 1e12 / tf_burst, 4),
+                    "call": f"dflash_fuse_inject per request in {chunk}-token chunks (device time, not in the round)"},
         "clocks": clk,
         "status_word": status,
         "e2e": e2e,
