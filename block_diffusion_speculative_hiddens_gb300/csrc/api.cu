@@ -971,6 +971,7 @@ int dflash_graph_end(dflash_handle* h, void* stream, int32_t* n_kernels) {
   if (!rc) rc = cuda_err(cudaGraphInstantiate(&e, g, 0));
   if (!rc) rc = cuda_err(cudaGraphUpload(e, (cudaStream_t)stream));
   if (rc) {
+    if (e) cudaGraphExecDestroy(e);
     if (g) cudaGraphDestroy(g);
     return rc;
   }
