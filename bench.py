@@ -608,21 +608,24 @@ def main():
         if args.block:
             cfg = cfg.with_(block=args.block)
         budget = 150.0
-        times, taus = oracle_round_seconds(cfg, budget, max(1, args.steps or 8))
-        used = times[1:] if len(times) > 1 else times
+        K, W = max(1, args.steps or 8), max(0, args.warmup)
+        times, taus = oracle_round_seconds(cfg, budget, W + K)
+        warm = min(W, len(times) - 1)  # the budget may stop early: keep at least one timed round
+        used = times[warm:]
         rs = statistics.mean(used)
         val = (cfg.block - 1) / rs
+        stopped = len(times) < W + K
         line = {"impl": "reference", "metric": METRIC, "value": round(val, 3), "unit": "tok/s",
-                "n_gpus": args.gpus, "steps": len(used), "warmup": len(times) - len(used),
+                "n_gpus": args.gpus, "steps": len(used), "warmup": warm,
                 "ms_per_step": round(rs * 1e3, 1), "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                 "config": {"workload": f"{cfg.name} drafter, one request of batch {cfg.batch} at a time, "
                                        f"prompt {cfg.ctx0 or cfg.ctx_range[0]}, block {cfg.block}"},
                 "cpu_baseline": {"value": round(val, 3), "unit": "tok/s", "cores": os.cpu_count(),
                                  "kind": "oracle",
-                                 "sample": f"{len(times)} rounds of request 0 after an untimed "
-                                           f"{cfg.ctx0 or cfg.ctx_range[0]}-token "
-                                           f"prefill, stopped after {budget:.0f} s"},
+                                 "sample": f"{len(used)} timed rounds after {warm} warm-up rounds of request 0, "
+                                           f"after an untimed {cfg.ctx0 or cfg.ctx_range[0]}-token prefill"
+                                           + (f"; stopped by the {budget:.0f} s budget" if stopped else "")},
                 "e2e": {"value": round(val, 3), "unit": "tok/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
