@@ -121,6 +121,27 @@ def _ptr(t) -> Optional[int]:
     return None if t is None else t.data_ptr()
 
 
+def _need(t, dtype: str, n: int, what: str, device: int, optional: bool = False):
+    """Refuse a buffer the call would read or write past, before the library
+    sees it: the C ABI gets a bare device pointer.  `n` elements of `dtype`
+    (a torch dtype name), contiguous, on CUDA device `device`; nothing is
+    checked when the call touches no element (n == 0) or an optional buffer
+    is absent."""
+    if n <= 0 or (t is None and optional):
+        return
+    if t is None:
+        raise ValueError(f"{what}: a device tensor is required")
+    dev = t.device
+    if dev.type != "cuda" or dev.index != device:
+        raise ValueError(f"{what}: expected a tensor on cuda:{device}, got {dev}")
+    if str(t.dtype) != "torch." + dtype:
+        raise ValueError(f"{what}: expected {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{what}: expected a contiguous tensor")
+    if t.numel() < n:
+        raise ValueError(f"{what}: {t.numel()} elements, the call needs {n}")
+
+
 def _stream(stream) -> int:
     import torch
     s = torch.cuda.current_stream() if stream is None else stream
@@ -187,27 +208,51 @@ class Drafter:
         except Exception:
             pass
 
+    # ---- argument checks (sizes from include/dflash.h)
+    def _inject_args(self, slots, feats, rows_per_req: int, n_new) -> int:
+        B = slots.numel()
+        _need(slots, "int32", B, "slots", self.device)
+        _need(feats, "bfloat16", B * rows_per_req * self.cfg.n_fused * self.cfg.hidden, "feats", self.device)
+        _need(n_new, "int32", B, "n_new", self.device)
+        return B
+
+    def _draft_args(self, slots, last_tok, draft) -> int:
+        B = slots.numel()
+        _need(slots, "int32", B, "slots", self.device)
+        _need(last_tok, "int32", B, "last_tok", self.device)
+        _need(draft, "int32", B * (self.cfg.block - 1), "draft", self.device)
+        return B
+
     # ---- the three calls of a round
     def fuse_inject(self, slots, feats, rows_per_req: int, n_new, stream=None):
+        self._inject_args(slots, feats, rows_per_req, n_new)
         _check("dflash_fuse_inject", self.lib.dflash_fuse_inject(
             self.h, _ptr(slots), slots.numel(), _ptr(feats), rows_per_req, _ptr(n_new), _stream(stream)))
 
     def fuse_inject_noalloc(self, slots, feats, rows_per_req: int, n_new, stream=None):
         """dflash_fuse_inject with the library's static scratch (at most 64 rows)."""
+        self._inject_args(slots, feats, rows_per_req, n_new)
         _check("dflash_fuse_inject_noalloc", self.lib.dflash_fuse_inject_noalloc(
             self.h, _ptr(slots), slots.numel(), _ptr(feats), rows_per_req, _ptr(n_new), _stream(stream)))
 
     def draft_block(self, slots, last_tok, draft, stream=None):
+        self._draft_args(slots, last_tok, draft)
         _check("dflash_draft_block", self.lib.dflash_draft_block(
             self.h, _ptr(slots), slots.numel(), _ptr(last_tok), _ptr(draft), _stream(stream)))
 
     def draft_round(self, slots, feats, rows_per_req: int, n_new, last_tok, draft, stream=None):
         """fuse_inject + draft_block with the injection folded into the layers' QKV GEMMs."""
+        self._inject_args(slots, feats, rows_per_req, n_new)
+        self._draft_args(slots, last_tok, draft)
         _check("dflash_draft_round", self.lib.dflash_draft_round(
             self.h, _ptr(slots), slots.numel(), _ptr(feats), rows_per_req, _ptr(n_new), _ptr(last_tok),
             _ptr(draft), _stream(stream)))
 
     def draft_block_debug(self, slots, last_tok, draft, hidden=None, logits=None, stream=None):
+        """hidden [batch*16, H] and logits [batch*16, V] float32: all 16 rows of each request."""
+        B = self._draft_args(slots, last_tok, draft)
+        _need(hidden, "float32", B * 16 * self.cfg.hidden, "hidden", self.device, optional=True)
+        _need(logits, "float32", B * 16 * self.cfg.vocab, "logits", self.device, optional=True)
         _check("dflash_draft_block_debug", self.lib.dflash_draft_block_debug(
             self.h, _ptr(slots), slots.numel(), _ptr(last_tok), _ptr(draft), _ptr(hidden),
             _ptr(logits), _stream(stream)))
@@ -215,6 +260,9 @@ class Drafter:
     def draft_block_sample(self, slots, last_tok, temperature: float, seed: int, round_ctr, draft, logits=None,
                            stream=None):
         """dflash_draft_block with each draft drawn from softmax(logits / temperature)."""
+        B = self._draft_args(slots, last_tok, draft)
+        _need(round_ctr, "int32", 1, "round_ctr", self.device, optional=True)
+        _need(logits, "float32", B * 16 * self.cfg.vocab, "logits", self.device, optional=True)
         _check("dflash_draft_block_sample", self.lib.dflash_draft_block_sample(
             self.h, _ptr(slots), slots.numel(), _ptr(last_tok), float(temperature), int(seed) & ((1 << 64) - 1),
             _ptr(round_ctr), _ptr(draft), _ptr(logits), _stream(stream)))
@@ -222,16 +270,31 @@ class Drafter:
     # ---- target model (role 1)
     def verify_block(self, slots, tokens, out_tok, n_valid=None, feats=None, stream=None):
         """Target forward over block tokens [batch, 16] -> out_tok [batch, 16] (+ feats [batch, 16, 5H])."""
+        B = slots.numel()
+        _need(slots, "int32", B, "slots", self.device)
+        _need(tokens, "int32", B * 16, "tokens", self.device)
+        _need(out_tok, "int32", B * 16, "out_tok", self.device)
+        _need(n_valid, "int32", B, "n_valid", self.device, optional=True)
+        _need(feats, "bfloat16", B * 16 * self.cfg.n_fused * self.cfg.hidden, "feats", self.device, optional=True)
         _check("dflash_verify_block", self.lib.dflash_verify_block(
             self.h, _ptr(slots), slots.numel(), _ptr(tokens), _ptr(n_valid), _ptr(out_tok), _ptr(feats),
             _stream(stream)))
 
     def advance(self, slots, n, stream=None):
         """ctx_len[slot] += n[b] (the trim after acceptance / a prefill chunk's step)."""
+        B = slots.numel()
+        _need(slots, "int32", B, "slots", self.device)
+        _need(n, "int32", B, "n", self.device)
         _check("dflash_advance", self.lib.dflash_advance(self.h, _ptr(slots), slots.numel(), _ptr(n),
                                                           _stream(stream)))
 
     def accept_trim(self, slots, draft, target, accept_len, bonus, ctx_len, stream=None):
+        B, S = slots.numel(), self.cfg.block
+        _need(slots, "int32", B, "slots", self.device)
+        _need(draft, "int32", B * (S - 1), "draft", self.device)
+        _need(target, "int32", B * S, "target", self.device)
+        for name, t in (("accept_len", accept_len), ("bonus", bonus), ("ctx_len", ctx_len)):
+            _need(t, "int32", B, name, self.device)
         _check("dflash_accept_trim", self.lib.dflash_accept_trim(
             self.h, _ptr(slots), slots.numel(), _ptr(draft), _ptr(target), _ptr(accept_len),
             _ptr(bonus), _ptr(ctx_len), _stream(stream)))
