@@ -64,10 +64,12 @@ typedef enum {
 #define DFLASH_DEV_RANGE     0x20u /* an f16 activation or cache entry exceeded 65504 (saturated) */
 
 /* Drafter shape and serving limits.
- * Supported: head_dim in {64,128}; hidden, n_fused*hidden, intermediate and
- * n_q_heads*head_dim multiples of 64; n_kv_heads*head_dim a multiple of 128;
- * hidden a multiple of 128 and <= 8192; n_q_heads a multiple of n_kv_heads
- * with n_q_heads/n_kv_heads <= 8; 2 <= block <= 16; page_size == 64; n_layers <= 8. */
+ * Supported: head_dim in {64,128}; intermediate a multiple of 64;
+ * n_q_heads*head_dim and n_kv_heads*head_dim multiples of 128; hidden a
+ * multiple of 128 and <= 8192; n_q_heads/n_kv_heads in {1, 2, 4, 8};
+ * 2 <= block <= 16; page_size == 64; n_layers <= 8; max_batch <= 64.
+ * Anything else makes dflash_workspace_bytes return 0 and dflash_create
+ * return DFLASH_ERR_SHAPE. */
 typedef struct dflash_config {
   int32_t hidden;             /* H */
   int32_t n_q_heads;          /* hq */
