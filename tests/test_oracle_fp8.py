@@ -89,3 +89,19 @@ def test_fp8_model_uses_the_dequantised_weights():
     h = np.random.default_rng(1).normal(size=(3, cfg.hidden))
     ref = O.rmsnorm(h, m8.w("final_norm"), cfg.rms_eps) @ F.dequantize_rows(O.bf16_to_f64(w["embed"])).T
     assert np.allclose(O.lm_head_logits(m8, h), ref, atol=1e-12)
+
+
+def test_rounding_equals_the_library_cast_within_range():
+    """Inside the finite range, rounding onto the E4M3 grid equals PyTorch's own
+    float8_e4m3fn cast (an independent implementation of the same format);
+    beyond 448 the library gives NaN where the reading taken here saturates."""
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("no float8_e4m3fn in this torch")
+    rng = np.random.default_rng(1)
+    g = F.e4m3_grid()
+    mid = ((g[:-1] + g[1:]) / 2).astype(np.float32)
+    for arr in (rng.uniform(-448, 448, 100000).astype(np.float32), mid, -mid,
+                rng.uniform(-2 ** -5, 2 ** -5, 20000).astype(np.float32)):
+        lib = torch.from_numpy(arr).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+        assert np.array_equal(F.round_e4m3(arr.astype(np.float64)), lib)
