@@ -35,3 +35,19 @@ def test_ridge_point():
     ridge = TFLOPS * 1e12 / (HBM_GBS * 1e9)  # about 253 flops per byte
     assert bench.roofline_bound(0.99 * ridge, 1.0, HBM_GBS, TFLOPS) == "hbm"
     assert bench.roofline_bound(1.01 * ridge, 1.0, HBM_GBS, TFLOPS) == "tensor"
+
+
+def test_lm_head_traffic_only_for_the_captured_build_and_workload():
+    """The committed DRAM-traffic figure is reported only while the GEMM's
+    sources hash to the captured build, and only for the workload it scales to."""
+    import re
+    text = open(os.path.join(ROOT, "profiles", "lm_head_traffic_mid.md")).read()
+    want = re.search(r"^source_sha256: ([0-9a-f]{64})$", text, re.M).group(1)
+    traffic = int(re.search(r"^traffic_bytes_per_launch: (\d+)$", text, re.M).group(1))
+    expect = traffic if bench.gemm_source_hash() == want else None
+    assert bench.lm_head_traffic(get_config("qwen3-8b")) == expect
+    assert bench.lm_head_traffic(get_config("long-8layer")) is None
+    # a traffic figure is DRAM bytes of one launch: at least the weights it streams
+    if expect is not None:
+        cfg = get_config("qwen3-8b")
+        assert expect >= cfg.vocab * cfg.hidden * 2
