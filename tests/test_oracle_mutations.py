@@ -159,6 +159,13 @@ def _lm_no_final_norm(model, h, chunk=1 << 14):
     return h @ model.w("embed").T
 
 
+def _lm_untied(model, h, chunk=1 << 14):
+    """lm_head with a table other than the embedding (rows in reverse order)."""
+    cfg = model.cfg
+    hn = R.rmsnorm(h, model.w("final_norm"), cfg.rms_eps)
+    return hn @ model.w("embed")[::-1].T
+
+
 def _argmax_last(x):
     return x.shape[-1] - 1 - np.argmax(x[..., ::-1], axis=-1)
 
@@ -184,9 +191,52 @@ MUTATIONS = [
     ("inject_kv", _inject_v_roped, [P.test_inject_k_norm_and_rope_properties]),
     ("decoder_layer", _layer_post_uses_in_gain, [P.test_decoder_layer_matches_library_assembly]),
     ("decoder_layer", _layer_no_qnorm, [P.test_decoder_layer_matches_library_assembly]),
-    ("lm_head_logits", _lm_no_final_norm, [P.test_lm_head_chunking_is_plain_matmul]),
+    ("lm_head_logits", _lm_no_final_norm, [P.test_lm_head_equals_library_rms_norm_and_linear]),
+    ("lm_head_logits", _lm_untied, [P.test_lm_head_is_tied_to_the_embedding]),
     ("argmax_first", _argmax_last, [P.test_argmax_ties_go_to_lowest_id]),
 ]
+
+
+def _draft_variant(rows_from=1, b0_shift=0, fill=None):
+    """OracleDrafter.draft with one planted slip: drafts from rows
+    rows_from..rows_from+S-2, the block one position later, or the mask rows
+    replaced by another token."""
+    def draft(self, req, last_tok, want_logits=True):
+        cfg = self.cfg
+        S = cfg.block
+        tokens = np.array([last_tok] + [cfg.mask_id if fill is None else fill] * (S - 1))
+        h = self.model.embed_rows(tokens)
+        pos = np.arange(req.ctx_len + b0_shift, req.ctx_len + b0_shift + S)
+        for l in range(cfg.n_layers):
+            ck, cv = req.ctx(l)
+            h = R.decoder_layer(self.model, l, h, pos, ck, cv)
+        logits = R.lm_head_logits(self.model, h[rows_from:rows_from + S - 1])
+        top2 = np.partition(logits, -2, axis=-1)[:, -2:]
+        out = {"draft": R.argmax_first(logits).astype(np.int64), "hidden": h, "margin": top2[:, 1] - top2[:, 0]}
+        if want_logits:
+            out["logits"] = logits
+        return out
+    return draft
+
+
+DRAFT_PINS = [lambda: P.test_draft_block_rows_with_identity_layers(16), P.test_draft_block_positions_closed_form]
+DRAFT_MUTATIONS = [
+    ("rows 0..S-2", _draft_variant(rows_from=0)),
+    ("b0 at L+1", _draft_variant(b0_shift=1)),
+    ("b0 at L-1", _draft_variant(b0_shift=-1)),
+    ("masks dropped", _draft_variant(fill=0)),
+]
+
+
+@pytest.mark.parametrize("label,fn", DRAFT_MUTATIONS, ids=[m[0] for m in DRAFT_MUTATIONS])
+def test_planted_draft_block_mistake_is_caught(monkeypatch, label, fn):
+    monkeypatch.setattr(R.OracleDrafter, "draft", fn)
+    assert _fails(*DRAFT_PINS), f"no pin caught the planted mistake: {label}"
+
+
+def test_unmutated_draft_block_passes_its_pins():
+    for pin in DRAFT_PINS:
+        pin()
 
 
 @pytest.mark.parametrize("name,fn,pins", MUTATIONS,

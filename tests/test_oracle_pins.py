@@ -359,13 +359,126 @@ def test_argmax_ties_go_to_lowest_id():
     assert O.argmax_first(x).tolist() == [1, 0, 0]
 
 
-def test_lm_head_chunking_is_plain_matmul():
+def test_lm_head_equals_library_rms_norm_and_linear():
+    """a6 logits against torch's own RMSNorm and linear layer in float64, the
+    table widened from the bf16 bits by torch (not by the oracle), with
+    non-unit final gains and a chunk size that leaves a ragged last chunk."""
+    cfg = get_config("tiny-gains")
+    w = make_weights(cfg)
+    m = O.OracleModel(cfg, w)
+    h = rng.standard_normal((15, cfg.hidden)) * 3.0
+    got = O.lm_head_logits(m, h, chunk=1000)
+    bits = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).double()
+    E, g = bits(w["embed"]), bits(w["final_norm"])
+    want = F.linear(F.rms_norm(torch.from_numpy(h), (cfg.hidden,), weight=g, eps=cfg.rms_eps), E).numpy()
+    np.testing.assert_allclose(got, want, rtol=1e-10, atol=1e-10)
+
+
+def test_lm_head_is_tied_to_the_embedding():
+    """The lm_head is the embedding table itself ([Code walkthrough] 二.3,
+    [Paper walkthrough] 设计: the drafter reuses the target's embedding and
+    LM head): a hidden state equal to token v's embedding row scores v
+    highest, because a random row's product with itself (|E_v|^2) dwarfs its
+    products with the other rows (about |E_v| |E_u| / sqrt(H))."""
     cfg = get_config("tiny")
-    m = O.OracleModel(cfg, make_weights(cfg))
-    h = rng.standard_normal((15, cfg.hidden))
-    a = O.lm_head_logits(m, h, chunk=1000)
-    b = O.rmsnorm(h, m.w("final_norm"), cfg.rms_eps) @ m.w("embed").T
-    np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-12)
+    w = make_weights(cfg)
+    m = O.OracleModel(cfg, w)
+    ids = np.array([0, 1, 17, 1000, 2048, cfg.vocab - 2, cfg.mask_id])
+    logits = O.lm_head_logits(m, O.bf16_to_f64(w["embed"][ids]))
+    assert O.argmax_first(logits).tolist() == ids.tolist()
+
+
+# ------------------------------------------------------------------ a3-a6 draft block
+
+def _identity_layers(cfg):
+    """Weights whose every layer adds nothing to the residual stream (W_o = 0,
+    W_down = 0), so the block's hidden states stay its embedding rows."""
+    w = make_weights(cfg)
+    w["layers"] = [dict(lw, wo=np.zeros_like(lw["wo"]), w_down=np.zeros_like(lw["w_down"])) for lw in w["layers"]]
+    return w
+
+
+@pytest.mark.parametrize("S", [16, 8])
+def test_draft_block_rows_with_identity_layers(S):
+    """Block = [last verified token, (S-1) x mask] ([Code walkthrough] 二.1:
+    1 known token + 15 masks -> 15 candidates), drafts from rows 1..S-1.
+    With identity layers the hidden state of row 0 is b0's embedding and of
+    every other row the mask's; the drafts are then the lm_head's top id of
+    the mask row (the mask id itself, the table being tied), never b0."""
+    cfg = get_config("tiny").with_(block=S)
+    w = _identity_layers(cfg)
+    m = O.OracleModel(cfg, w)
+    dr = O.OracleDrafter(m)
+    req = O.OracleRequest(cfg, 64 + S)
+    dr.fuse_inject(req, feature_rows(cfg, 0, 0, 64))
+    b0 = 17
+    out = dr.draft(req, b0)
+    E = O.bf16_to_f64(w["embed"])
+    np.testing.assert_array_equal(out["hidden"][0], E[b0])
+    for i in range(1, S):
+        np.testing.assert_array_equal(out["hidden"][i], E[cfg.mask_id])
+    assert out["logits"].shape == (S - 1, cfg.vocab)
+    assert out["draft"].tolist() == [cfg.mask_id] * (S - 1)
+
+
+def _pos2d_model(S, eps):
+    """A hand-built one-layer drafter in two dimensions: hidden 2, one head of
+    dimension 2 (a single RoPE pair rotating by `position` radians), W_q, W_k,
+    W_v, W_o and the fusion projection the identity, the MLP zero, all gains
+    one.  Every weight is exact in bf16."""
+    from workload.configs import DraftConfig
+    cfg = DraftConfig(name="pos2d", hidden=2, n_q_heads=1, n_kv_heads=1, head_dim=2, intermediate=2, n_layers=1,
+                      vocab=4, rope_theta=10000.0, batch=1, ctx0=3, rounds=1, match_p=0.5, n_fused=1, block=S,
+                      rms_eps=eps)
+    b = lambda a: f64_to_bf16_bits(np.asarray(a, dtype=np.float64))
+    eye = np.eye(2)
+    w = {"embed": b([[0.25, -1.0], [1.0, 0.5], [-2.0, 0.75], [-0.5, 1.0]]),
+         "fc": b(eye), "fc_norm": b([1.0, 1.0]), "final_norm": b([1.0, 1.0]),
+         "layers": [{"wqkv": b(np.vstack([eye, eye, eye])), "wo": b(eye), "w_gate_up": b(np.zeros((4, 2))),
+                     "w_down": b(np.zeros((2, 2))), "in_norm": b([1.0, 1.0]), "post_norm": b([1.0, 1.0]),
+                     "q_norm": b([1.0, 1.0]), "k_norm": b([1.0, 1.0])}]}
+    return cfg, w
+
+
+def test_draft_block_positions_closed_form():
+    """Where the block sits: the context's keys at positions 0..L-1 and the
+    block's rows at L..L+S-1, b0 at L (the reading that the block follows
+    the confirmed context), all of them seen by every block row (no mask,
+    [Code walkthrough] 二.2).  On the two-dimensional model every rotation is
+    a plane rotation by the position in radians, so the layer's output is
+    written out here with explicit rotation matrices and the softmax over
+    scalar scores; drafts are the lm_head's choices for rows 1..S-1."""
+    S, L, eps = 4, 3, 1e-6
+    cfg, w = _pos2d_model(S, eps)
+    dr = O.OracleDrafter(O.OracleModel(cfg, w))
+    req = O.OracleRequest(cfg, L + S)
+    x = np.array([[[0.5, 2.0]], [[-1.5, 0.25]], [[1.0, 1.0]]])  # three context features [L, 1, 2]
+    dr.fuse_inject(req, x)
+    b0 = 2
+    out = dr.draft(req, b0)
+
+    n = lambda v: v / np.sqrt(np.mean(v * v) + eps)
+    rot = lambda a: np.array([[np.cos(a), -np.sin(a)], [np.sin(a), np.cos(a)]])
+    E = O.bf16_to_f64(w["embed"])
+    c = [n(x[j, 0]) for j in range(L)]                        # fused context features
+    keys = [rot(j) @ n(c[j]) for j in range(L)]              # k-norm, then RoPE at position j
+    vals = [c[j] for j in range(L)]
+    toks = [b0] + [cfg.mask_id] * (S - 1)
+    h = [E[t] for t in toks]
+    xs = [n(v) for v in h]                                   # input norm
+    keys += [rot(L + i) @ n(xs[i]) for i in range(S)]        # block keys at L..L+S-1
+    vals += [xs[i] for i in range(S)]
+    want = []
+    for i in range(S):
+        q = rot(L + i) @ n(xs[i])
+        s = np.array([q @ k for k in keys]) / np.sqrt(2.0)
+        p = np.exp(s - s.max())
+        p /= p.sum()
+        want.append(h[i] + sum(pj * vj for pj, vj in zip(p, vals)))
+    want = np.array(want)
+    np.testing.assert_allclose(out["hidden"], want, rtol=1e-12, atol=1e-12)
+    drafts = [int(np.argmax(E @ n(want[i]))) for i in range(1, S)]
+    assert out["draft"].tolist() == drafts
 
 
 # ------------------------------------------------------------------ whole round
