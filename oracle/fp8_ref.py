@@ -65,7 +65,25 @@ def quantize_rows(w: np.ndarray):
     return round_e4m3(y.astype(np.float64)), s
 
 
-def dequantize_rows(w: np.ndarray) -> np.ndarray:
-    """The weight the FP8 drafter computes with: q * s per row (float64)."""
+def _dequantize_block(w: np.ndarray) -> np.ndarray:
     q, s = quantize_rows(w)
     return q * s.astype(np.float64)[:, None]
+
+
+def dequantize_rows(w: np.ndarray, rows_per_task: int = 512) -> np.ndarray:
+    """The weight the FP8 drafter computes with: q * s per row (float64).
+    Rows are independent, so large matrices are handled in blocks of rows on
+    a thread pool; every row's arithmetic is the same either way."""
+    w = np.asarray(w)
+    if w.ndim != 2 or w.shape[0] <= rows_per_task:
+        return _dequantize_block(w)
+    from concurrent.futures import ThreadPoolExecutor
+    import os
+    out = np.empty(w.shape, dtype=np.float64)
+
+    def work(r0):
+        out[r0:r0 + rows_per_task] = _dequantize_block(w[r0:r0 + rows_per_task])
+
+    with ThreadPoolExecutor(max(1, min(16, os.cpu_count() or 1))) as ex:
+        list(ex.map(work, range(0, w.shape[0], rows_per_task)))
+    return out
