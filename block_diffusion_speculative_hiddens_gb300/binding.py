@@ -18,7 +18,8 @@ HEADER = os.path.join(os.path.dirname(PKG), "include", "dflash.h")
 
 OK = 0
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported shape", 3: "capacity exceeded",
-          4: "CUDA error", 5: "device-side check failed", 6: "workspace too small or misaligned"}
+          4: "CUDA error", 5: "device-side check failed", 6: "workspace too small or misaligned",
+          7: "a weight exceeds the f16 range"}
 DEV_TIMEOUT, DEV_NAN, DEV_PAGE, DEV_CAPACITY, DEV_ARG, DEV_RANGE = 0x01, 0x02, 0x04, 0x08, 0x10, 0x20
 KID_LM_HEAD, KID_GATE_UP, KID_ATTENTION, KID_DOWN, KID_QKV, KID_WO, KID_FC, KID_INJECT = 1, 2, 3, 4, 5, 6, 7, 8
 
@@ -64,6 +65,7 @@ _SIGS = {
                                                  _vp, _vp, _vp, _vp]),
     "dflash_accept_trim": (ctypes.c_int, [_vp, _vp, ctypes.c_int32, _vp, _vp, _vp, _vp, _vp, _vp]),
     "dflash_reset_slot": (ctypes.c_int, [_vp, ctypes.c_int32, _vp]),
+    "dflash_check_wait_timeout": (ctypes.c_int, [_vp, ctypes.c_uint32, _vp]),
     "dflash_read_status": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_uint32)]),
     "dflash_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "dflash_graph_begin": (ctypes.c_int, [_vp, _vp]),
@@ -214,6 +216,8 @@ class Drafter:
         _need(slots, "int32", B, "slots", self.device)
         _need(feats, "bfloat16", B * rows_per_req * self.cfg.n_fused * self.cfg.hidden, "feats", self.device)
         _need(n_new, "int32", B, "n_new", self.device)
+        if B * rows_per_req > 0 and feats.data_ptr() % 16:
+            raise ValueError("feats: the rows are read by a TMA descriptor and must start 16-byte aligned")
         return B
 
     def _draft_args(self, slots, last_tok, draft) -> int:
@@ -298,6 +302,11 @@ class Drafter:
         _check("dflash_accept_trim", self.lib.dflash_accept_trim(
             self.h, _ptr(slots), slots.numel(), _ptr(draft), _ptr(target), _ptr(accept_len),
             _ptr(bonus), _ptr(ctx_len), _stream(stream)))
+
+    def check_wait_timeout(self, limit_us: int, stream=None):
+        """Make one bounded in-kernel wait run out (nothing arrives at its barrier)."""
+        _check("dflash_check_wait_timeout", self.lib.dflash_check_wait_timeout(self.h, int(limit_us),
+                                                                               _stream(stream)))
 
     def reset_slot(self, slot: int, stream=None):
         _check("dflash_reset_slot", self.lib.dflash_reset_slot(self.h, slot, _stream(stream)))

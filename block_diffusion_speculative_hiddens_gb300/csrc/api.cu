@@ -476,20 +476,22 @@ int draft_impl(dflash_handle* h, const int32_t* slots, int32_t batch, const int3
   const KVGeom kv = kv_geom(h);
   const bool fold = feats != nullptr;
   const int R = fold ? batch * rows_per_req : 0;
+  CUtensorMap tm_feats;
   if (fold) {
+    // every descriptor is encoded (and the caller's feature rows checked)
+    // before anything is queued, so a refused call leaves the slots untouched
+    const int MX = M + R;
+    if (!make_tmap(&tm_feats, feats, R, (uint64_t)c.n_fused * H, gemm_shape(h, R).box(), true))
+      return DFLASH_ERR_INVALID_ARG;
+    if (h->bm_MX != MX) {
+      if (!make_tmap(&h->tm_hgx, h->hg, MX, H, gemm_shape(h, MX).box())) return DFLASH_ERR_CUDA;
+      h->bm_MX = MX;
+    }
     h->launches++;
     rc = cuda_err(launch_page_alloc(slots, batch, h->cfg.block, n_new, rows_per_req, h->ctx_len, h->pos0, h->n_pages,
                                     h->page_table, c.max_pages_per_slot, h->free_stack, h->free_top, h->n_eff, h->slots_ok,
                                     c.max_slots, h->status, s));
     if (rc) return rc;
-    const int MX = M + R;
-    const uint32_t BNr = gemm_shape(h, R).box();
-    CUtensorMap tm_feats;
-    if (!make_tmap(&tm_feats, feats, R, (uint64_t)c.n_fused * H, BNr, true)) return DFLASH_ERR_INVALID_ARG;
-    if (h->bm_MX != MX) {
-      if (!make_tmap(&h->tm_hgx, h->hg, MX, H, gemm_shape(h, MX).box())) return DFLASH_ERR_CUDA;
-      h->bm_MX = MX;
-    }
     GemmParams p = {};
     p.out = h->hg + (size_t)M * H;  // fused-feature rows right below the block rows
     p.gain = h->fc_norm;
@@ -671,6 +673,7 @@ const char* dflash_status_string(int st) {
     case DFLASH_ERR_CUDA: return "CUDA error";
     case DFLASH_ERR_DEVICE: return "device-side check failed";
     case DFLASH_ERR_WORKSPACE: return "workspace too small or misaligned";
+    case DFLASH_ERR_RANGE: return "a weight exceeds the f16 range";
   }
   return "unknown status";
 }
@@ -718,10 +721,10 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
   // f16 packing, or FP8 E4M3 packing with per-row scales
   auto pack = [&](const void* src, f16* dst, float* sc, int N, int K, int n_tiles, int swiglu_I) {
     return h->fp8 ? launch_pack_weight_fp8(B16(src), reinterpret_cast<uint8_t*>(dst), sc, N, K, n_tiles, swiglu_I, 0)
-                  : launch_pack_weight(B16(src), dst, N, K, n_tiles, swiglu_I, true, 0);
+                  : launch_pack_weight(B16(src), dst, N, K, n_tiles, swiglu_I, true, h->status, 0);
   };
   cudaError_t e = pack(w->embed, h->embed_pk, h->embed_sc, c.vocab, H, ceil_div(c.vocab, 128), 0);
-  if (!e && drafter) e = launch_pack_weight(B16(w->fc), h->fc_pk, H, c.n_fused * H, H / 128, 0, false, 0);
+  if (!e && drafter) e = launch_pack_weight(B16(w->fc), h->fc_pk, H, c.n_fused * H, H / 128, 0, false, h->status, 0);
   if (!e && drafter) e = launch_gain_f32(B16(w->fc_norm), h->fc_norm, H, 0);
   if (!e) e = launch_gain_f32(B16(w->final_norm), h->final_norm, H, 0);
   for (int l = 0; l < c.n_layers && !e; ++l) {
@@ -783,6 +786,15 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
   if (!rc) rc = cuda_err(launch_pool_init(h->free_stack, h->free_top, c.max_pages, 0));
   if (!rc) rc = cuda_err(launch_rope_table(h->rope, h->max_pos, D, c.rope_theta, 0));
   if (!rc) rc = cuda_err(cudaDeviceSynchronize());
+  if (!rc) {  // a weight the f16 copies cannot hold (the packing saturated it): refuse the handle
+    uint32_t st = 0;
+    rc = cuda_err(cudaMemcpy(&st, h->status, sizeof(st), cudaMemcpyDeviceToHost));
+    if (!rc && (st & DFLASH_DEV_RANGE)) {
+      fprintf(stderr, "[dflash] dflash_create: a weight exceeds the f16 range (|w| > 65504); "
+                      "create the handle with weight_fp8 = 1 (per-row scales) instead\n");
+      rc = DFLASH_ERR_RANGE;
+    }
+  }
   if (rc) {
     delete h;
     return rc;
@@ -803,7 +815,8 @@ int dflash_destroy(dflash_handle* h) {
 
 int dflash_fuse_inject(dflash_handle* h, const int32_t* slots, int32_t batch, const void* feats,
                        int32_t rows_per_req, const int32_t* n_new, void* stream) {
-  if (!h || batch < 0 || batch > h->cfg.max_batch || rows_per_req < 0) return DFLASH_ERR_INVALID_ARG;
+  if (!h || h->cfg.role != 0 || batch < 0 || batch > h->cfg.max_batch || rows_per_req < 0)
+    return DFLASH_ERR_INVALID_ARG;
   if ((long long)batch * rows_per_req > h->cfg.max_rows) return DFLASH_ERR_CAPACITY;
   if (batch == 0) return DFLASH_OK;
   if (!slots || !n_new) return DFLASH_ERR_INVALID_ARG;
@@ -812,19 +825,24 @@ int dflash_fuse_inject(dflash_handle* h, const int32_t* slots, int32_t batch, co
   cudaStream_t s = (cudaStream_t)stream;
   const dflash_config& c = h->cfg;
   const int H = c.hidden, D = c.head_dim, hkv = c.n_kv_heads;
+  const int R = batch * rows_per_req;
+  // every descriptor is encoded (and the caller's feature rows checked:
+  // 16-byte aligned) before anything is queued, so a refused call leaves the
+  // slots' lengths and pages untouched
+  CUtensorMap tm_feats;
+  if (R > 0) {
+    const uint32_t BN = gemm_shape(h, R).box();
+    if (!make_tmap(&tm_feats, feats, R, (uint64_t)c.n_fused * H, BN, true)) return DFLASH_ERR_INVALID_ARG;
+    if (h->bm_rows != R) {
+      if (!make_tmap(&h->tm_cg, h->cg, R, H, BN)) return DFLASH_ERR_CUDA;
+      h->bm_rows = R;
+    }
+  }
   h->launches++;
   int rc = cuda_err(launch_page_alloc(slots, batch, h->cfg.block, n_new, rows_per_req, h->ctx_len, h->pos0, h->n_pages,
                                       h->page_table, c.max_pages_per_slot, h->free_stack, h->free_top, h->n_eff, h->slots_ok,
                                       c.max_slots, h->status, s));
-  if (rc || rows_per_req == 0) return rc;
-  const int R = batch * rows_per_req;
-  const uint32_t BN = gemm_shape(h, R).box();
-  CUtensorMap tm_feats;
-  if (!make_tmap(&tm_feats, feats, R, (uint64_t)c.n_fused * H, BN, true)) return DFLASH_ERR_INVALID_ARG;
-  if (h->bm_rows != R) {
-    if (!make_tmap(&h->tm_cg, h->cg, R, H, BN)) return DFLASH_ERR_CUDA;
-    h->bm_rows = R;
-  }
+  if (rc || R == 0) return rc;
   {  // fusion projection; RMSNorm gain folded in, its scale deferred to the consumer
     GemmParams p = {};
     p.out = h->cg;
@@ -866,7 +884,8 @@ int dflash_draft_block(dflash_handle* h, const int32_t* slots, int32_t batch, co
 int dflash_draft_round(dflash_handle* h, const int32_t* slots, int32_t batch, const void* feats,
                        int32_t rows_per_req, const int32_t* n_new, const int32_t* last_tok, int32_t* draft,
                        void* stream) {
-  if (!h || batch < 0 || batch > h->cfg.max_batch || rows_per_req < 0) return DFLASH_ERR_INVALID_ARG;
+  if (!h || h->cfg.role != 0 || batch < 0 || batch > h->cfg.max_batch || rows_per_req < 0)
+    return DFLASH_ERR_INVALID_ARG;
   if (batch == 0) return DFLASH_OK;
   // folding needs the feature rows to fit below the block rows in one token tile
   const long long R = (long long)batch * rows_per_req;
@@ -927,6 +946,13 @@ int dflash_accept_trim(dflash_handle* h, const int32_t* slots, int32_t batch, co
   h->launches++;
   return cuda_err(launch_accept(slots, batch, h->cfg.block, draft, target, accept_len, bonus, ctx_len, h->ctx_len,
                                 h->cfg.max_slots, h->status, (cudaStream_t)stream));
+}
+
+int dflash_check_wait_timeout(dflash_handle* h, uint32_t limit_us, void* stream) {
+  if (!h || limit_us < 1 || limit_us > 100000) return DFLASH_ERR_INVALID_ARG;
+  if (cudaSetDevice(h->cfg.device) != cudaSuccess) return DFLASH_ERR_CUDA;
+  h->launches++;
+  return cuda_err(launch_wait_check(h->status, (unsigned long long)limit_us * 1000ull, (cudaStream_t)stream));
 }
 
 int dflash_reset_slot(dflash_handle* h, int32_t slot, void* stream) {
@@ -1200,7 +1226,8 @@ int noalloc_gemm(dflash_handle* h, cudaStream_t s, int mode, const void* const* 
 
 extern "C" int dflash_fuse_inject_noalloc(dflash_handle* h, const int32_t* slots, int32_t batch, const void* feats,
                                           int32_t rows_per_req, const int32_t* n_new, void* stream) {
-  if (!h || batch < 0 || batch > h->cfg.max_batch || rows_per_req < 0) return DFLASH_ERR_INVALID_ARG;
+  if (!h || h->cfg.role != 0 || batch < 0 || batch > h->cfg.max_batch || rows_per_req < 0)
+    return DFLASH_ERR_INVALID_ARG;
   if ((long long)batch * rows_per_req > NA_MAX_ROWS) {
     fprintf(stderr, "[dflash] dflash_fuse_inject_noalloc: %lld rows exceed its static scratch limit of %d\n",
             (long long)batch * rows_per_req, NA_MAX_ROWS);
@@ -1221,6 +1248,15 @@ extern "C" int dflash_fuse_inject_noalloc(dflash_handle* h, const int32_t* slots
   cudaStream_t s = (cudaStream_t)stream;
   const dflash_config& c = h->cfg;
   const int H = c.hidden, D = c.head_dim, hkv = c.n_kv_heads;
+  const int R = batch * rows_per_req;
+  // descriptors first (and the caller's feature rows checked), so a refused
+  // call queues nothing
+  const uint32_t BN = (uint32_t)(((R + 15) / 16) * 16);
+  CUtensorMap tm_feats, tm_rows;
+  if (R > 0) {
+    if (!make_tmap(&tm_feats, feats, R, (uint64_t)c.n_fused * H, BN, true)) return DFLASH_ERR_INVALID_ARG;
+    if (!make_tmap(&tm_rows, rows, R, H, BN)) return DFLASH_ERR_CUDA;
+  }
   // tile counters must start at zero (the kernels also leave them at zero)
   rc = cuda_err(cudaMemsetAsync(ctr, 0, NA_CTR_BYTES, s));
   if (rc) return rc;
@@ -1228,12 +1264,7 @@ extern "C" int dflash_fuse_inject_noalloc(dflash_handle* h, const int32_t* slots
   rc = cuda_err(launch_page_alloc(slots, batch, h->cfg.block, n_new, rows_per_req, h->ctx_len, h->pos0, h->n_pages,
                                   h->page_table, c.max_pages_per_slot, h->free_stack, h->free_top, h->n_eff, h->slots_ok,
                                   c.max_slots, h->status, s));
-  if (rc || rows_per_req == 0) return rc;
-  const int R = batch * rows_per_req;
-  const uint32_t BN = (uint32_t)(((R + 15) / 16) * 16);
-  CUtensorMap tm_feats, tm_rows;
-  if (!make_tmap(&tm_feats, feats, R, (uint64_t)c.n_fused * H, BN, true)) return DFLASH_ERR_INVALID_ARG;
-  if (!make_tmap(&tm_rows, rows, R, H, BN)) return DFLASH_ERR_CUDA;
+  if (rc || R == 0) return rc;
   {
     GemmParams p = {};
     p.out = rows;

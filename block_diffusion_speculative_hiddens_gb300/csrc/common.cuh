@@ -66,21 +66,24 @@ DFL_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 // Wait for the phase with the given parity to complete.  Gives up after
-// DFL_WAIT_NS, sets DFLASH_DEV_TIMEOUT and returns false; once `*aborted` is
-// set (by this thread or earlier) it returns false immediately so every role
-// drains to the kernel's exit instead of waiting again.
-DFL_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status, bool* aborted) {
+// limit_ns of %globaltimer, sets DFLASH_DEV_TIMEOUT and returns false; once
+// `*aborted` is set (by this thread or earlier) it returns false immediately
+// so every role drains to the kernel's exit instead of waiting again.
+DFL_DEV bool mbar_wait_for(uint64_t* bar, uint32_t parity, uint32_t* status, bool* aborted, uint64_t limit_ns) {
   if (*aborted) return false;
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer() - t0 > DFL_WAIT_NS) {
+    if (globaltimer() - t0 > limit_ns) {
       dev_error(status, DFLASH_DEV_TIMEOUT);
       *aborted = true;
       return false;
     }
   }
+}
+DFL_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status, bool* aborted) {
+  return mbar_wait_for(bar, parity, status, aborted, DFL_WAIT_NS);
 }
 
 // ------------------------------------------------------------------ TMA
@@ -277,15 +280,19 @@ DFL_DEV uint32_t pack_f16x2(float lo, float hi) {
   __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
-// float -> f16 activation; values beyond the f16 range set DFLASH_DEV_RANGE.
 // Two FP8 E4M3 values (low byte first) to two f16 (exact: every E4M3 value is an f16).
 DFL_DEV uint32_t e4m3x2_to_f16x2(uint16_t v) {
   uint32_t r;
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
   return r;
 }
+// float -> f16 activation, saturating: a value beyond the f16 range becomes
+// +-65504 (the largest finite f16) and sets DFLASH_DEV_RANGE; NaN stays NaN.
 DFL_DEV f16 to_f16(float x, uint32_t* status) {
-  if (fabsf(x) > 65504.f) dev_error(status, DFLASH_DEV_RANGE);
+  if (fabsf(x) > 65504.f) {
+    dev_error(status, DFLASH_DEV_RANGE);
+    x = copysignf(65504.f, x);
+  }
   return __float2half_rn(x);
 }
 

@@ -153,7 +153,7 @@ cudaError_t attn_init_attributes();
 
 // weight preparation (dflash_create)
 cudaError_t launch_pack_weight(const bf16* src, void* dst, int N, int K, int n_tiles, int swiglu_I, bool to_f16,
-                               cudaStream_t s);
+                               uint32_t* status, cudaStream_t s);
 cudaError_t launch_gain_f32(const bf16* src, float* dst, int n, cudaStream_t s);
 // FP8 E4M3 packing with per-row scales (packed row order): scale = max|row| / 448,
 // q = E4M3(w / scale) rounded to nearest even, saturating.
@@ -199,6 +199,7 @@ cudaError_t launch_slot_lengths(const int* slots, int batch, const int* ctx_len,
                                 cudaStream_t s);
 // Rows of the residual stream h [M][H] (fp32) into feats [M][n_fused][H]
 // (bf16) at index `tap` (the target's fused-feature outputs).
+cudaError_t launch_wait_check(uint32_t* status, unsigned long long limit_ns, cudaStream_t s);
 cudaError_t launch_tap(const float* h, int M, int H, bf16* feats, int tap, int n_fused, cudaStream_t s);
 cudaError_t launch_harness_verify(const int* slots, int batch, int S, const int* draft, const int* match,
                                   const int* offs, int rounds_cap, int* round_ctr, int* target, int vocab,

@@ -25,9 +25,11 @@ cudaLaunchConfig_t cfg_of(dim3 grid, dim3 block, cudaStream_t s, cudaLaunchAttri
 // columns ([tile][k-block]), each in the 128-byte-swizzle image, converted to
 // f16 (exact for every bf16 value in the f16 normal range) or kept bf16.
 // swiglu_I > 0 packs a [2I, K] gate/up matrix so that tile t holds gate rows
-// t*64..t*64+63 then up rows I+t*64..I+t*64+63.  Rows past N are zero.
+// t*64..t*64+63 then up rows I+t*64..I+t*64+63.  Rows past N are zero.  A
+// weight beyond the f16 range (|w| > 65504) is saturated and sets
+// DFLASH_DEV_RANGE, which dflash_create turns into DFLASH_ERR_RANGE.
 __global__ void k_pack_weight(const bf16* __restrict__ src, uint16_t* __restrict__ dst, int N, int K, int n_tiles,
-                              int swiglu_I, int to_f16) {
+                              int swiglu_I, int conv, uint32_t* status) {
   const int KB = K / 64;
   const long long total = (long long)n_tiles * KB * 128 * 8;  // 16-byte chunks
   for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
@@ -39,12 +41,15 @@ __global__ void k_pack_weight(const bf16* __restrict__ src, uint16_t* __restrict
     const int row = swiglu_I > 0 ? (r < 64 ? tile * 64 + r : swiglu_I + tile * 64 + (r - 64)) : tile * 128 + r;
     uint4 v = make_uint4(0, 0, 0, 0);
     if (row < N) v = *reinterpret_cast<const uint4*>(src + (size_t)row * K + kb * 64 + c * 8);
-    if (to_f16) {
+    if (conv) {
       const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&v);
       uint4 o;
       __half2* h2 = reinterpret_cast<__half2*>(&o);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) h2[i] = __float22half2_rn(__bfloat1622float2(b2[i]));
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(b2[i]);
+        h2[i] = __halves2half2(to_f16(f.x, status), to_f16(f.y, status));
+      }
       v = o;
     }
     *reinterpret_cast<uint4*>(dst + blk * DFL_WBLK_ELEMS + r * 64 + ((c ^ (r & 7)) << 3)) = v;
@@ -354,6 +359,24 @@ __global__ void k_harness_verify(const int* slots, int batch, int S, const int* 
   for (int k = threadIdx.x; k < F / 8; k += blockDim.x) dst[k] = src[k];
 }
 
+// Failure-detection check: thread 0 waits on an mbarrier nothing arrives at,
+// with a short limit, through the pipelines' own bounded wait; it gives up,
+// sets DFLASH_DEV_TIMEOUT and returns.  A second wait after the give-up
+// returns at once (the aborted flag), as the pipelines' drain paths rely on.
+__global__ void k_wait_check(uint32_t* status, unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    bool aborted = false;
+    mbar_wait_for(&bar, 0, status, &aborted, limit_ns);
+    mbar_wait_for(&bar, 0, status, &aborted, limit_ns);
+  }
+}
+
 __global__ void k_tap(const float* __restrict__ h, int H, bf16* __restrict__ feats, int tap, int n_fused) {
   pdl_launch_dependents();
   pdl_wait();
@@ -365,6 +388,11 @@ __global__ void k_tap(const float* __restrict__ h, int H, bf16* __restrict__ fea
 
 }  // namespace
 
+cudaError_t launch_wait_check(uint32_t* status, unsigned long long limit_ns, cudaStream_t s) {
+  k_wait_check<<<1, 32, 0, s>>>(status, limit_ns);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_tap(const float* h, int M, int H, bf16* feats, int tap, int n_fused, cudaStream_t s) {
   cudaLaunchAttribute a[1];
   cudaLaunchConfig_t c = cfg_of(dim3(M), dim3(256), s, a);
@@ -372,11 +400,11 @@ cudaError_t launch_tap(const float* h, int M, int H, bf16* feats, int tap, int n
 }
 
 cudaError_t launch_pack_weight(const bf16* src, void* dst, int N, int K, int n_tiles, int swiglu_I, bool to_f16,
-                               cudaStream_t s) {
+                               uint32_t* status, cudaStream_t s) {
   const long long total = (long long)n_tiles * (K / 64) * 128 * 8;
   const long long blocks = std::min<long long>((total + 255) / 256, 1LL << 20);
   k_pack_weight<<<(unsigned)blocks, 256, 0, s>>>(src, static_cast<uint16_t*>(dst), N, K, n_tiles, swiglu_I,
-                                                 to_f16 ? 1 : 0);
+                                                 to_f16 ? 1 : 0, status);
   return cudaGetLastError();
 }
 

@@ -51,17 +51,20 @@ typedef enum {
   DFLASH_ERR_CAPACITY = 3,    /* rows > max_rows, or the page pool is exhausted (device) */
   DFLASH_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
   DFLASH_ERR_DEVICE = 5,      /* a device-side check tripped; see dflash_read_status */
-  DFLASH_ERR_WORKSPACE = 6    /* workspace null, too small or not 256-byte aligned */
+  DFLASH_ERR_WORKSPACE = 6,   /* workspace null, too small or not 256-byte aligned */
+  DFLASH_ERR_RANGE = 7        /* dflash_create: a weight exceeds the f16 range (|w| > 65504) */
 } dflash_status;
 
 /* Device status word bits (dflash_read_status). */
-#define DFLASH_DEV_TIMEOUT   0x01u /* a bounded wait inside a kernel gave up */
+#define DFLASH_DEV_TIMEOUT   0x01u /* a bounded wait inside a kernel gave up (2 s; the kernel then
+                                       drains its copies in flight, frees its TMEM and returns) */
 #define DFLASH_DEV_NAN       0x02u /* a NaN logit was skipped by the argmax */
 #define DFLASH_DEV_PAGE      0x04u /* a page-table entry was out of range */
 #define DFLASH_DEV_CAPACITY  0x08u /* page pool or per-slot page table full */
 #define DFLASH_DEV_ARG       0x10u /* slot id or n_new out of range (the request is skipped: no
                                        cache entry written; its outputs are unspecified) */
-#define DFLASH_DEV_RANGE     0x20u /* an f16 activation or cache entry exceeded 65504 (saturated) */
+#define DFLASH_DEV_RANGE     0x20u /* an f16 activation or cache entry exceeded 65504 (stored as
+                                       +-65504, the largest finite f16; NaN stays NaN) */
 
 /* Drafter shape and serving limits.
  * Supported: head_dim in {64,128}; intermediate a multiple of 64;
@@ -116,8 +119,10 @@ typedef struct dflash_config {
  * to within 2^-25; the fusion projection stays bf16) and gains as float32.
  * The caller may free its buffers once dflash_create returns.  Activations,
  * the KV cache and the argmax logits are computed with f16 tensor-core
- * operands and fp32 accumulation; an activation beyond the f16 range sets
- * DFLASH_DEV_RANGE. */
+ * operands and fp32 accumulation; an activation beyond the f16 range is
+ * saturated and sets DFLASH_DEV_RANGE.  With weight_fp8 = 0, a weight beyond
+ * the f16 range makes dflash_create return DFLASH_ERR_RANGE (no handle is
+ * created; weight_fp8 = 1 holds any finite weight through its row scale). */
 typedef struct dflash_weights {
   const void* embed;             /* [V, H]  tied embedding and lm_head */
   const void* fc;                /* [H, n_fused*H] fusion projection (no bias) */
@@ -161,7 +166,11 @@ DFLASH_API int dflash_destroy(dflash_handle* h);
  * Prefill is one call with rows_per_req = prompt length.  In a round,
  * n_new is the previous round's accept_len (the same device buffer), which
  * keeps a captured round loop free of host reads.  Requires
- * batch*rows_per_req <= max_rows. */
+ * batch*rows_per_req <= max_rows (else DFLASH_ERR_CAPACITY) and feats
+ * 16-byte aligned (else DFLASH_ERR_INVALID_ARG); a target handle (role 1)
+ * is refused with DFLASH_ERR_INVALID_ARG.  Every host-side refusal happens
+ * before anything is enqueued: the slots' lengths and pages stay as they
+ * were. */
 DFLASH_API int dflash_fuse_inject(dflash_handle* h, const int32_t* slots, int32_t batch, const void* feats,
                        int32_t rows_per_req, const int32_t* n_new, void* stream);
 
@@ -180,7 +189,8 @@ DFLASH_API int dflash_draft_block(dflash_handle* h, const int32_t* slots, int32_
  * layer's own QKV projection (the rows ride along as extra tokens of that
  * GEMM), so every layer's K/V weights are read once per round instead of
  * twice.  Used when rows_per_req <= 16 and batch*(16 + rows_per_req) <= 256;
- * otherwise it runs the two calls. */
+ * otherwise it runs the two calls.  A drafter call: DFLASH_ERR_INVALID_ARG
+ * on a target handle. */
 DFLASH_API int dflash_draft_round(dflash_handle* h, const int32_t* slots, int32_t batch, const void* feats,
                                   int32_t rows_per_req, const int32_t* n_new, const int32_t* last_tok,
                                   int32_t* draft, void* stream);
@@ -220,6 +230,15 @@ DFLASH_API int dflash_accept_trim(dflash_handle* h, const int32_t* slots, int32_
  *   the caller.  The tile counters are cleared at the start of every call. */
 DFLASH_API int dflash_fuse_inject_noalloc(dflash_handle* h, const int32_t* slots, int32_t batch, const void* feats,
                                           int32_t rows_per_req, const int32_t* n_new, void* stream);
+
+/* Failure-detection check (no counterpart on the pages): one thread of a
+ * one-warp kernel waits, through the same bounded wait the GEMM and
+ * attention pipelines use, on an mbarrier that nothing ever arrives at, with
+ * a limit of limit_us microseconds (1 .. 100000); it gives up, sets
+ * DFLASH_DEV_TIMEOUT in the handle's status word and returns, leaving the
+ * CUDA context usable.  dflash_read_status then reports (and clears) the bit.
+ * The pipelines' own waits give up after 2 s the same way. */
+DFLASH_API int dflash_check_wait_timeout(dflash_handle* h, uint32_t limit_us, void* stream);
 
 /* Free a slot's pages and set its length to 0 (stream-ordered). */
 DFLASH_API int dflash_reset_slot(dflash_handle* h, int32_t slot, void* stream);

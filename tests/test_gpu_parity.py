@@ -416,3 +416,97 @@ def test_edge_cases_and_errors(lib):
     assert d.read_status() & DEV_ARG
     after = [to_np(t) for t in d.read_kv(0, 0, 0, 64)]
     assert all(np.array_equal(x, y, equal_nan=True) for x, y in zip(before, after))
+
+
+# attention shapes beyond the workloads': one query head per KV head, head_dim 64 with G = 4 and 8
+ATTN_SHAPES = ["small-g1", "small-d64-g4", "small-d64-g8"]
+
+
+@pytest.mark.parametrize("attn_impl", ATTN)
+@pytest.mark.parametrize("name", ATTN_SHAPES)
+def test_attention_shapes_round_matches_oracle(lib, name, attn_impl):
+    cfg, g, o = _pair(name, 2, attn_impl=attn_impl)
+    for j in range(len(g.ids)):
+        L = int(g.ctx0[j])
+        k, v = g.d.read_kv(1, j, 0, L)
+        ok, ov = o.reqs[j].ctx(1)
+        assert rel_l2(to_np(k), ok) < TOL_REL_L2 and rel_l2(to_np(v), ov) < TOL_REL_L2, j
+    for r in range(2):
+        go = g.round(debug=True)
+        oo = o.round(want_logits=True)
+        for j, od in enumerate(oo):
+            assert rel_l2(go["hidden"][j], od["hidden"]) < TOL_REL_L2, (r, j)
+            assert rel_l2(go["logits"][j, 1:], od["logits"]) < TOL_REL_L2, (r, j)
+            assert np.array_equal(go["draft"][j], np.argmax(go["logits"][j, 1:], -1))
+            strong, _ = check_drafts(go["draft"][j], od)
+            assert strong >= 5, (r, j, strong)
+            assert (go["tau"][j], go["bonus"][j], go["ctx"][j]) == (od["tau"], od["bonus"], od["ctx"]), (r, j)
+    assert g.d.read_status() == 0
+
+
+def test_misaligned_features_refused_before_anything_is_queued(lib):
+    """Feature rows the TMA descriptor cannot address (not 16-byte aligned)
+    are refused by the host-side check before the page allocation is queued:
+    the slot's length and pages stay as they were."""
+    import torch
+    from block_diffusion_speculative_hiddens_gb300 import Drafter, weights_to_device
+    cfg = get_config("tiny")
+    d = Drafter(cfg, weights_to_device(make_weights(cfg)), max_batch=1, max_slots=1, max_pages=8,
+                max_pages_per_slot=8, max_rows=64)
+    dev = torch.device("cuda:0")
+    i32 = dict(dtype=torch.int32, device=dev)
+    slot = torch.tensor([0], **i32)
+    buf = torch.zeros(1, 9, cfg.fused_dim, dtype=torch.bfloat16, device=dev)
+    d.fuse_inject(slot, buf[:, :8].contiguous(), 8, torch.tensor([8], **i32))
+    torch.cuda.synchronize()
+    before = to_np(d.slot_lengths(slot))[0]
+    n_new = torch.tensor([4], **i32)
+    rc = d.lib.dflash_fuse_inject(d.h, slot.data_ptr(), 1, buf.data_ptr() + 2, 4, n_new.data_ptr(),
+                                  torch.cuda.current_stream().cuda_stream)
+    assert rc == 1  # DFLASH_ERR_INVALID_ARG
+    rc = d.lib.dflash_fuse_inject_noalloc(d.h, slot.data_ptr(), 1, buf.data_ptr() + 2, 4, n_new.data_ptr(),
+                                          torch.cuda.current_stream().cuda_stream)
+    assert rc == 1
+    torch.cuda.synchronize()
+    assert to_np(d.slot_lengths(slot))[0] == before == 8
+    with pytest.raises(ValueError):  # the binding refuses it before the library sees it
+        d.fuse_inject(slot, buf.view(-1)[1:1 + 4 * cfg.fused_dim].view(1, 4, cfg.fused_dim), 4, n_new)
+    assert d.read_status() == 0
+
+
+def test_bounded_wait_gives_up_and_reports(lib):
+    """A bounded in-kernel wait on a barrier nothing arrives at gives up after
+    its limit, sets DFLASH_DEV_TIMEOUT and returns; the context stays usable
+    and a round afterwards matches the oracle."""
+    import time
+    from block_diffusion_speculative_hiddens_gb300.binding import DEV_TIMEOUT
+    cfg, g, o = _pair("tiny-gains", 1)
+    t0 = time.perf_counter()
+    g.d.check_wait_timeout(2000)  # 2 ms
+    st = g.d.read_status()
+    dt = time.perf_counter() - t0
+    assert st & DEV_TIMEOUT and dt < 5.0
+    assert g.d.read_status() == 0  # cleared by the read
+    go = g.round()
+    od = o.round(want_logits=False)[0]
+    assert (go["tau"][0], go["bonus"][0], go["ctx"][0]) == (od["tau"], od["bonus"], od["ctx"])
+    check_drafts(go["draft"][0], od)
+    assert g.d.read_status() == 0
+
+
+def test_create_refuses_weights_beyond_f16(lib):
+    """A weight the f16 copies cannot hold makes dflash_create fail with
+    DFLASH_ERR_RANGE instead of silently holding inf; FP8 weights (per-row
+    scales) take the same matrix."""
+    import torch
+    from block_diffusion_speculative_hiddens_gb300 import Drafter, weights_to_device
+    from block_diffusion_speculative_hiddens_gb300.binding import DflashError
+    cfg = get_config("tiny")
+    w = weights_to_device(make_weights(cfg))
+    w["layers"][1]["wo"][3, 7] = 1.0e5
+    kw = dict(max_batch=1, max_slots=1, max_pages=4, max_pages_per_slot=4, max_rows=16)
+    with pytest.raises(DflashError) as e:
+        Drafter(cfg, w, **kw)
+    assert e.value.code == 7
+    d = Drafter(cfg, w, weight_fp8=1, **kw)
+    assert d.read_status() == 0

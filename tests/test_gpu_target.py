@@ -147,3 +147,26 @@ def test_verify_block_batch_of_two_with_ragged_chunks(lib):
         k, v = t.read_kv(NL - 1, b, 0, int(lens[b]))
         assert rel_l2(to_np(k), ots[b].K[NL - 1][:lens[b]]) < TOL_REL_L2, b
     assert t.read_status() == 0
+
+
+def test_drafter_calls_refused_on_a_target_handle(lib):
+    """A target handle has no fusion weights: the injection and folded-round
+    calls refuse it (DFLASH_ERR_INVALID_ARG) instead of reading an unpacked
+    fusion block, and nothing is queued."""
+    import torch
+    from block_diffusion_speculative_hiddens_gb300.binding import DflashError
+    cfg = get_config("tiny-gains")
+    t, _, _, _ = _handles(cfg)
+    dev = torch.device("cuda:0")
+    i32 = dict(dtype=torch.int32, device=dev)
+    slots = torch.tensor([0], **i32)
+    feats = torch.zeros(1, 16, cfg.n_fused * cfg.hidden, dtype=torch.bfloat16, device=dev)
+    n_new = torch.tensor([4], **i32)
+    for call in (lambda: t.fuse_inject(slots, feats, 16, n_new),
+                 lambda: t.fuse_inject_noalloc(slots, feats, 16, n_new),
+                 lambda: t.draft_round(slots, feats, 16, n_new, torch.ones(1, **i32), torch.zeros(1, 15, **i32))):
+        with pytest.raises(DflashError) as e:
+            call()
+        assert e.value.code == 1
+    assert to_np(t.slot_lengths(slots))[0] == 0
+    assert t.read_status() == 0

@@ -129,6 +129,28 @@ TEST_CONFIGS = {
         intermediate=768, n_layers=2, vocab=5000, rope_theta=5e5, batch=3, ctx0=None,
         rounds=4, match_p=None, ctx_range=(30, 300), p_range=(0.5, 0.95), gain_std=0.1,
         weight_std=0.05, block=10),
+    # Attention shapes beyond the workloads': one query head per KV head, and
+    # head_dim 64 with 4 and 8 query heads per KV head.
+    "small-g1": DraftConfig(
+        name="small-g1", hidden=512, n_q_heads=4, n_kv_heads=4, head_dim=128, intermediate=768,
+        n_layers=2, vocab=5000, rope_theta=1e6, batch=2, ctx0=None, rounds=3, match_p=None,
+        ctx_range=(30, 300), p_range=(0.5, 0.95), gain_std=0.1, weight_std=0.05),
+    "small-d64-g4": DraftConfig(
+        name="small-d64-g4", hidden=512, n_q_heads=8, n_kv_heads=2, head_dim=64, intermediate=768,
+        n_layers=2, vocab=5000, rope_theta=1e6, batch=2, ctx0=None, rounds=3, match_p=None,
+        ctx_range=(30, 300), p_range=(0.5, 0.95), gain_std=0.1, weight_std=0.05),
+    "small-d64-g8": DraftConfig(
+        name="small-d64-g8", hidden=1024, n_q_heads=16, n_kv_heads=2, head_dim=64, intermediate=768,
+        n_layers=2, vocab=5000, rope_theta=1e6, batch=2, ctx0=None, rounds=3, match_p=None,
+        ctx_range=(30, 300), p_range=(0.5, 0.95), gain_std=0.1, weight_std=0.05),
+    # Wide hidden sizes (the fusion projection 5H -> H at H = 4096 and 8192)
+    # with a small vocabulary and few layers, for the static-scratch injection.
+    "wide-4096": DraftConfig(
+        name="wide-4096", hidden=4096, n_q_heads=32, n_kv_heads=8, head_dim=128, intermediate=1024,
+        n_layers=2, vocab=4096, rope_theta=1e6, batch=1, ctx0=64, rounds=2, match_p=0.9),
+    "wide-8192": DraftConfig(
+        name="wide-8192", hidden=8192, n_q_heads=32, n_kv_heads=8, head_dim=128, intermediate=1024,
+        n_layers=1, vocab=2048, rope_theta=1e6, batch=1, ctx0=64, rounds=2, match_p=0.9),
 }
 
 
