@@ -14,12 +14,19 @@ from workload import get_config, make_weights
 pytestmark = pytest.mark.gpu
 
 
+# At these shapes about 15-20 % of the 15 draft positions fall within the
+# oracle's 0.05 margin of a tie; a round must still compare most of them.
+MIN_STRONG = 6
+
+
 def _check_round(go, oo, ids):
     for j, od in zip(ids, oo):
         assert rel_l2(go["hidden"][j], od["hidden"]) < TOL_REL_L2
         assert rel_l2(go["logits"][j, 1:], od["logits"]) < TOL_REL_L2
         assert np.array_equal(go["draft"][j], np.argmax(go["logits"][j, 1:], -1))
-        check_drafts(go["draft"][j], od)
+        strong, total = check_drafts(go["draft"][j], od)
+        assert strong >= MIN_STRONG, (j, strong, total)
+        assert len(set(od["draft"].tolist())) >= 2  # the comparison is not over one repeated id
         assert (go["tau"][j], go["bonus"][j], go["ctx"][j]) == (od["tau"], od["bonus"], od["ctx"])
 
 
@@ -80,4 +87,22 @@ def test_long_context_workload_sampled_request(lib):
     go = g.round(debug=True)
     oo = o.round(want_logits=True)
     _check_round(go, oo, [2])
+    assert g.d.read_status() == 0
+
+
+def test_fp8_weights_full_size_round(lib):
+    """FP8 E4M3 weights at the Qwen3-8B shape, batch 1: injected K/V at
+    sampled positions, then one round's hidden states, logits, drafts and
+    acceptance against the oracle computing with the same dequantised weights."""
+    cfg = get_config("qwen3-8b")
+    w = make_weights(cfg)
+    g = GpuRun(cfg, 1, weights_np=w, prefill_chunk=2048, weight_fp8=1)
+    g.prefill()
+    o = OracleRun(cfg, 1, weights_np=w, cache=False, weight_fp8=1)
+    o.prefill()
+    L = cfg.ctx0
+    _check_kv(g, o, 0, 0, [0, 63, L // 2 + 5, L - 1], [0, cfg.n_layers - 1])
+    go = g.round(debug=True)
+    oo = o.round(want_logits=True)
+    _check_round(go, oo, [0])
     assert g.d.read_status() == 0
