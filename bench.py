@@ -1,22 +1,28 @@
 #!/usr/bin/env python
-"""Benchmark: one DFlash drafting-plus-acceptance round per step on GB300.
+"""Benchmark: one DFlash drafting-plus-acceptance round per step on one GB300.
 
-Workload (default): the Qwen3-8B-shaped drafter at batch 1 -- hidden 4096,
-32/8 heads x 128, SwiGLU 12288, 5 layers, vocabulary 151936, fusion
-20480 -> 4096 -- with a 2048-token prompt, block 16 and a stand-in verify
-that copies each draft with probability 0.9.  One step = fuse+inject the
-previous round's accepted features, draft one block, stand-in verify,
-accept/trim, all captured in one CUDA graph.  Synthetic seeded data and
-random-init weights of that architecture.
+Headline workload (default): the Qwen3-8B-shaped drafter at batch 1 -- hidden
+4096, 32/8 heads x 128, SwiGLU 12288, 5 layers, vocabulary 151936, fusion
+20480 -> 4096 -- with a 2048-token prompt, block 16 and a stand-in verify that
+copies each draft with probability 0.9.  One step = accept/trim the previous
+round, fuse+inject its accepted features, draft one block; the stand-in
+verify runs between rounds and is timed apart, in the same CUDA graph.
+Synthetic seeded data and random-init weights of that architecture.
 
 Every scenario pass is the workload's round count from its prompts; timed
 steps cycle through identically prefilled groups of request slots, one pass
-per group, so K steps always run rounds of the stated scenario.  Other
-workloads (`--config llama3.1-8b | batched-qwen3-8b | long-8layer`) run the
-same way at their own batch; large feature streams are drawn on the GPU.
+per group, so K steps always run rounds of the stated scenario.  After the
+headline, the default run measures the other drafting workloads (tiny,
+Llama-3.1-8B shape, batched Qwen3-8B shape, long-context 8-layer) with a
+short run each and reports them under "workloads" (`--workloads none` skips
+them; `--config NAME` makes another workload the headline).
 
-Prints one JSON line (rank 0).  `--impl reference` times the float64 CPU
-oracle on the host cores instead.
+The library drives one GPU; `--gpus N` with N > 1 prints a one-line record
+saying so and exits (replicas are independent processes, one per GPU, each
+running this benchmark on its own).
+
+Prints one JSON line.  `--impl reference` times the float64 CPU oracle on the
+host cores instead.
 """
 from __future__ import annotations
 
@@ -46,7 +52,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="qwen3-8b")
-    ap.add_argument("--rounds-per-slot", type=int, default=None)
+    ap.add_argument("--rounds-per-slot", type=int, default=None,
+                    help="rounds of the scenario per slot group (default: the workload's round count)")
     ap.add_argument("--e2e-steps", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=25.0)
@@ -65,6 +72,9 @@ def parse():
     ap.add_argument("--target-layers", type=int, default=8)
     ap.add_argument("--fold-inject", action="store_true",
                     help="issue dflash_draft_round instead of dflash_fuse_inject + dflash_draft_block")
+    ap.add_argument("--workloads", default="all",
+                    help="after the headline, also measure: all (tiny, llama3.1-8b, batched-qwen3-8b, "
+                         "long-8layer), none, or a comma-separated list")
     return ap.parse_args()
 
 
@@ -175,12 +185,12 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ oracle timing
 
-def oracle_round_seconds(cfg, budget_s: float, max_rounds: int):
+def oracle_round_seconds(cfg, budget_s: float, max_rounds: int, weights=None):
     """Time the float64 CPU oracle on rounds of `cfg` (request 0) after an untimed prefill."""
     import numpy as np
     import oracle as O
     from workload import feature_rows, make_weights, match_stream
-    w = make_weights(cfg)
+    w = make_weights(cfg) if weights is None else weights
     model = O.OracleModel(cfg, w, cache=False)
     dr = O.OracleDrafter(model)
     L0 = int(cfg.ctx0 or cfg.ctx_range[0])
@@ -207,67 +217,90 @@ def oracle_round_seconds(cfg, budget_s: float, max_rounds: int):
 
 # ------------------------------------------------------------------ GPU arm
 
-def max_over_ranks(value: float, world: int, device) -> float:
-    """The largest of every rank's value (the job's time is its slowest replica's)."""
-    if world <= 1:
-        return value
-    import torch
-    t = torch.tensor([value], dtype=torch.float64, device=device)
-    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    return float(t.item())
-
-
-def replica_rate(units_per_rank: float, world: int, seconds: float) -> float:
-    """Whole-job throughput of `world` replicas: all ranks' units over the slowest time."""
-    return units_per_rank * world / seconds
-
-
 def roofline_bound(flops: float, nbytes: float, hbm_gbs: float, tflops: float) -> str:
     """"hbm" when a kernel's arithmetic intensity (flops per algorithmic byte)
     is below the ridge point of the two peaks, else "tensor"."""
     return "hbm" if flops / nbytes < tflops * 1e12 / (hbm_gbs * 1e9) else "tensor"
 
 
-def run_gpu(args, rank, world, local_rank):
+# The workloads every default run measures after the headline one, each with
+# a short run of timed rounds (the batched round is ~6 ms, the others < 2 ms).
+EXTRA_WORKLOADS = ("tiny", "llama3.1-8b", "batched-qwen3-8b", "long-8layer")
+EXTRA_STEPS = {"tiny": 64, "llama3.1-8b": 32, "batched-qwen3-8b": 16, "long-8layer": 32}
+FEATS_ON_HOST_MAX = 4e8  # feature-stream elements drawn by the workload generator; larger: on the device
+
+
+def device_weights(cfg, dev, seed: int) -> dict:
+    """Random-init weights of cfg's architecture drawn on the device: every
+    projection N(0, weight_std) in bf16, RMSNorm gains 1 -- the distribution
+    and layout of workload.make_weights, from a seeded torch generator."""
+    import torch
+    from workload.inputs import WEIGHT_NAMES, _shape
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+
+    def t(name):
+        shape = _shape(cfg, name)
+        if len(shape) == 1:
+            return torch.ones(shape, dtype=torch.bfloat16, device=dev)
+        x = torch.empty(shape, dtype=torch.float32, device=dev)
+        x.normal_(0.0, cfg.weight_std, generator=g)
+        return x.to(torch.bfloat16)
+
+    glob = [n for n in WEIGHT_NAMES if n in ("embed", "fc", "fc_norm", "final_norm")]
+    out = {n: t(n) for n in glob}
+    out["layers"] = [{n: t(n) for n in WEIGHT_NAMES if n not in glob} for _ in range(cfg.n_layers)]
+    return out
+
+
+def feature_stream(cfg, B, cap, dev):
+    """Target features of every position [B, cap, F] bf16 on the device: the
+    workload's position-keyed stream when small, else N(0,1) drawn on the
+    device from a per-request seeded generator (same distribution and shape).
+    Returns (tensor, host numpy bits or None, description)."""
     import numpy as np
     import torch
-    from block_diffusion_speculative_hiddens_gb300 import Drafter, binding, weights_to_device
-    from block_diffusion_speculative_hiddens_gb300.session import RoundState, SyntheticVerify, run_round
-    from workload import context_lengths, feature_rows, get_config, make_weights, match_stream
+    from block_diffusion_speculative_hiddens_gb300 import binding
+    from workload import feature_rows
+    F = cfg.fused_dim
+    if B * cap * F <= FEATS_ON_HOST_MAX:
+        fs = np.stack([feature_rows(cfg, b, 0, cap).reshape(cap, F) for b in range(B)])
+        return binding.bf16_host(fs).to(dev), fs, "workload generator"
+    out = torch.empty(B, cap, F, dtype=torch.bfloat16, device=dev)
+    for b in range(B):
+        g = torch.Generator(device=dev)
+        g.manual_seed(1_000_003 * (cfg.seed + 1) + b)
+        out[b].normal_(generator=g)
+    return out, None, "device generator (torch.normal_, seeded per request)"
 
-    torch.cuda.set_device(local_rank)
-    dev = torch.device(f"cuda:{local_rank}")
-    cfg = get_config(args.config)
-    if args.block:
-        cfg = cfg.with_(block=args.block)
-    S = cfg.block                                        # S-1 drafts per request per round
-    B = cfg.batch
-    ctx = context_lengths(cfg).astype(int)               # prompt length per request
-    R = args.rounds_per_slot or cfg.rounds
-    K = args.steps if args.steps is not None else (512 if B == 1 else R)
-    W = args.warmup
+
+def measure(cfg, w_dev, dev, K, W, *, attn_impl=0, weight_fp8=0, temperature=0.0, seed=0, fold=False,
+            e2e_steps=0, weights_desc="workload generator", rounds_per_slot=None):
+    """Run K timed drafting rounds of `cfg` (after W warm-up rounds) as one
+    CUDA graph and return the measurements.
+
+    Timed graph: [mark] then per round fuse_inject + draft_block, [mark],
+    stand-in verify, [mark], accept_trim, and a final [mark].  The intervals
+    between marks split the graph into the drafter's work (accept of the
+    previous round + inject + draft of this one) and the stand-in verify, so
+    the round time, its percentiles and the verify's time all come from the
+    same replay; the lm_head launches carry CUDA-event probes in the same
+    graph (its end probe coincides with the verify's first mark)."""
+    import numpy as np
+    import torch
+    from block_diffusion_speculative_hiddens_gb300 import Drafter, binding
+    from block_diffusion_speculative_hiddens_gb300.session import RoundState, SyntheticVerify, run_round
+    from workload import context_lengths, match_stream
+
+    S, B = cfg.block, cfg.batch
+    ctx = context_lengths(cfg).astype(int)
+    R = rounds_per_slot or cfg.rounds
     n_groups = math.ceil(K / R) + 1                      # + one group of B slots for warm-up
     n_slots = n_groups * B
-    cap = int(ctx.max()) + cfg.block * (max(R, W) + 2) + 64
+    cap = int(ctx.max()) + S * (max(R, W) + 2) + 64
     mpps = math.ceil(cap / 64) + 1
     F = cfg.fused_dim
-
-    w_dev = weights_to_device(make_weights(cfg), local_rank)
-    # target features of every position a request reaches: the workload's
-    # position-keyed stream when it is small, else N(0,1) drawn on the device
-    # from a per-request seeded generator (same distribution, same shapes)
-    if B * cap * F <= 4e8:
-        fs = np.stack([feature_rows(cfg, b, 0, cap).reshape(cap, F) for b in range(B)])
-        feat_stream = binding.bf16_host(fs).to(dev)
-        feat_src = "workload generator"
-    else:
-        fs = None
-        feat_stream = torch.empty(B, cap, F, dtype=torch.bfloat16, device=dev)
-        for b in range(B):
-            g = torch.Generator(device=dev)
-            g.manual_seed(1_000_003 * (cfg.seed + 1) + b)
-            feat_stream[b].normal_(generator=g)
-        feat_src = "device generator (torch.normal_, seeded per request)"
+    feat_stream, fs, feat_src = feature_stream(cfg, B, cap, dev)
     m = np.empty((max(R, W), B, S), dtype=np.int32)
     u = np.empty_like(m)
     for r in range(max(R, W)):
@@ -275,14 +308,13 @@ def run_gpu(args, rank, world, local_rank):
     match, offs = torch.from_numpy(m).to(dev), torch.from_numpy(u).to(dev)
 
     chunk = 2048
-    d = Drafter(cfg, w_dev, max_batch=B, max_slots=n_slots, max_pages=mpps * n_slots,
-                max_pages_per_slot=mpps, max_rows=max(chunk, S * B), device=local_rank, attn_impl=args.attn_impl,
-                weight_fp8=1 if args.weights == "fp8" else 0)
+    d = Drafter(cfg, w_dev, max_batch=B, max_slots=n_slots, max_pages=mpps * n_slots, max_pages_per_slot=mpps,
+                max_rows=max(chunk, S * B), device=dev.index, attn_impl=attn_impl, weight_fp8=weight_fp8)
     stream = torch.cuda.Stream(device=dev)
 
     def prefill(g, timed=False):
-        """Inject every prompt of slot group g in chunks; with timed, returns
-        the device time (ms) of the fuse_inject calls alone."""
+        """Inject every prompt of slot group g in chunks; with timed, the
+        device time (ms) of the fuse_inject calls alone."""
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)] if timed else None
         with torch.cuda.stream(stream):
             calls = []
@@ -303,38 +335,53 @@ def run_gpu(args, rank, world, local_rank):
             return ev[0].elapsed_time(ev[1])
         return None
 
-    states, verifies = [], []
-    for g in range(n_groups):
-        prefill(g)
+    def new_state(g, verify_feats=True):
         st = RoundState(d, B, slots=[g * B + b for b in range(B)], first_token=cfg.first_token)
+        ver = SyntheticVerify(st, match, offs, feat_stream if verify_feats else None)
+        if temperature > 0:
+            st.set_sampling(temperature, seed, ver.round_ctr)
+        return st, ver
+
+    states, verifies = [], []
+    for g in range(n_groups - 1):
+        prefill(g)
+        st, ver = new_state(g)
         states.append(st)
-        verifies.append(SyntheticVerify(st, match, offs, feat_stream))
-        if args.temperature > 0:
-            st.set_sampling(args.temperature, args.seed, verifies[-1].round_ctr)
+        verifies.append(ver)
+    gw = n_groups - 1
+    prefill_ms = prefill(gw, timed=True)                 # the warm-up group's prefill, timed on its own
+    wst, wv = new_state(gw)
     stream.synchronize()
 
     # warm-up: W rounds on the spare group, as one graph
-    wst, wv = states[-1], verifies[-1]
     d.graph_begin(stream)
     for _ in range(W):
-        run_round(wst, wv, stream, folded=args.fold_inject)
+        run_round(wst, wv, stream, folded=fold)
     d.graph_end(stream)
     d.graph_launch(stream)
     stream.synchronize()
 
-    # timed: K rounds, R per group, one graph; lm_head bracketed by event probes
+    # timed: K rounds, R per slot group, one graph with marks around each verify
+    n_marks = 2 * K + 2
+    d.marks_arm(n_marks)
     d.probe_arm(binding.KID_LM_HEAD, K)
     n0 = d.launch_count()
     d.graph_begin(stream)
+    d.mark(stream)
     for i in range(K):
-        run_round(states[i // R], verifies[i // R], stream, folded=args.fold_inject)
+        ver = verifies[i // R]
+
+        def marked(s_=None, ver=ver):
+            d.mark(s_)
+            ver(s_)
+            d.mark(s_)
+        run_round(states[i // R], marked, stream, folded=fold)
+    d.mark(stream)
     n_kernels = d.graph_end(stream)
-    launches_captured = d.launch_count() - n0
+    launches = d.launch_count() - n0
     stream.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
     torch.cuda.synchronize()
-    clocks = ClockSampler(local_rank)
+    clocks = ClockSampler(dev.index)
     time.sleep(0.3)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
@@ -345,122 +392,32 @@ def run_gpu(args, rank, world, local_rank):
     e1.synchronize()
     t_wall1 = time.time()
     torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
     clk = clocks.stop(t_wall0, t_wall1)
-    ms = e0.elapsed_time(e1)
+    total_ms = e0.elapsed_time(e1)
+    iv = d.marks_read(n_marks - 1)
     lm_ms = d.probe_read(K)
     status = d.read_status()
     accepted = 0
     for g in range(n_groups - 1):
         if min(R, K - g * R) > 0:
             accepted += int((states[g].ctx_len.cpu().numpy() - ctx).sum())
-    ms = max_over_ranks(ms, world, dev)
 
-    # ---- the stand-in verify on its own, and the per-round distribution: one
-    # more graph of up to R rounds on a fresh copy of the prompts, with
-    # timeline marks at every round start and around the verify (the marks'
-    # event nodes cost a little overlap, so the headline mean stays the
-    # unmarked graph's, minus the verify's mean)
-    Ki = min(R, K)
-    gi = n_groups - 1
-    for b in range(B):
-        d.reset_slot(gi * B + b, stream)
-    prefill_ms = prefill(gi, timed=True)
-    st_i = RoundState(d, B, slots=[gi * B + b for b in range(B)], first_token=cfg.first_token)
-    ver_i = SyntheticVerify(st_i, match, offs, feat_stream)
-    if args.temperature > 0:
-        st_i.set_sampling(args.temperature, args.seed, ver_i.round_ctr)
-
-    def marked_verify(s_=None):
-        d.mark(s_)
-        ver_i(s_)
-        d.mark(s_)
-
-    d.marks_arm(3 * Ki + 1)
-    d.graph_begin(stream)
-    for _ in range(Ki):
-        d.mark(stream)
-        run_round(st_i, marked_verify, stream, folded=args.fold_inject)
-    d.mark(stream)
-    d.graph_end(stream)
-    d.graph_launch(stream)
-    stream.synchronize()
-    iv = d.marks_read(3 * Ki)
-    verify_ms = statistics.mean(iv[1::3])
-    per_round_ms = sorted(a + c for a, c in zip(iv[0::3], iv[2::3]))
-    pct = lambda q: per_round_ms[min(len(per_round_ms) - 1, int(q * len(per_round_ms)))]
-
-    # ---- end to end through the C ABI with host buffers: per step H2D of the
-    # block's target features and verify streams, one round, D2H of the result
-    e2e = None
-    E = min(args.e2e_steps, R)
-    if E > 0:
-        for b in range(B):
-            d.reset_slot(gi * B + b, stream)
-        prefill(gi)
-        st = RoundState(d, B, slots=[gi * B + b for b in range(B)], first_token=cfg.first_token)
-        m_dev = torch.zeros(1, B, S, dtype=torch.int32, device=dev)
-        u_dev = torch.zeros_like(m_dev)
-        ver = SyntheticVerify(st, m_dev, u_dev, None)
-        if args.temperature > 0:
-            st.set_sampling(args.temperature, args.seed, ver.round_ctr)
-        d.graph_begin(stream)
-        run_round(st, ver, stream, folded=args.fold_inject)
-        d.graph_end(stream)
-        feats_h = torch.empty(B, S, F, dtype=torch.bfloat16).pin_memory()
-        mu_h = torch.empty(2, B, S, dtype=torch.int32).pin_memory()
-        out_h = torch.empty(B, S - 1 + 3, dtype=torch.int32).pin_memory()
-        if fs is not None:
-            fs_host = binding.bf16_host(fs)
-        else:  # the device-drawn stream's first rows stand in on the host
-            fs_host = feat_stream[:, :S].cpu()
-        stream.synchronize()
-        # the round's inject consumes the previous round's block features
-        # (positions prev_L .. prev_L+S-1 of each request, the first accept_len)
-        prev_L = ctx.copy()
-        cur_L = ctx.copy()
-        t0 = time.perf_counter()
-        for r in range(E):
-            for b in range(B):
-                if fs is not None:
-                    feats_h[b].copy_(fs_host[b, prev_L[b]:prev_L[b] + S])
-                else:
-                    feats_h[b].copy_(fs_host[b])
-            mu_h[0].copy_(torch.from_numpy(m[r % len(m)]))
-            mu_h[1].copy_(torch.from_numpy(u[r % len(u)]))
-            with torch.cuda.stream(stream):
-                st.feats.copy_(feats_h, non_blocking=True)
-                m_dev[0].copy_(mu_h[0], non_blocking=True)
-                u_dev[0].copy_(mu_h[1], non_blocking=True)
-                d.graph_launch(stream)
-                out_h[:, :S - 1].copy_(st.draft, non_blocking=True)
-                out_h[:, S - 1].copy_(st.accept_len, non_blocking=True)
-                out_h[:, S].copy_(st.bonus, non_blocking=True)
-                out_h[:, S + 1].copy_(st.ctx_len, non_blocking=True)
-            stream.synchronize()
-            prev_L, cur_L = cur_L, out_h[:, S + 1].numpy().astype(int)
-        h2d = feats_h.numel() * 2 + mu_h.numel() * 4
-        d2h = out_h.numel() * 4
-        t_e2e = time.perf_counter() - t0
-        t_e2e = max_over_ranks(t_e2e, world, dev)
-        e2e = {"value": round(replica_rate((S - 1) * B * E, world, t_e2e), 1), "unit": "tok/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "steps": E,
-               "round_us": round(t_e2e / E * 1e6, 1),
-               "note": "includes the stand-in verify kernel"}
+    drafter_ms = iv[0::2]                                # accept(prev) + inject + draft, per round
+    verify_ms = iv[1::2]
+    round_ms = sum(drafter_ms) / K                       # every kernel of the K rounds but the verify
+    full = sorted(drafter_ms[1:K])                       # rounds 1..K-1: one accept + inject + draft each
+    pct = (lambda q: full[min(len(full) - 1, int(q * len(full)))]) if full else (lambda q: round_ms)
 
     # ---- rooflines: the dominant kernel (lm_head + argmax) and the round
     hbm, _, peak_src = peaks()
     tf_burst, tf_sust = tensor_peaks()
     H, V, D = cfg.hidden, cfg.vocab, cfg.head_dim
     M = S * B                                            # block rows the method computes
-    fp8 = args.weights == "fp8"
+    fp8 = bool(weight_fp8)
     wb = 1 if fp8 else 2                                 # bytes per projection / embedding weight
     lm_bytes = V * H * wb + (V * 4 if fp8 else 0) + M * H * 2
     lm_flops = 2.0 * M * V * H
     lm_avg_ms = statistics.mean(lm_ms) if lm_ms else float("nan")
-    round_ms_incl = ms / K
-    round_ms = round_ms_incl - verify_ms  # the stand-in verify is not part of the round
     tau = accepted / (K * B)
     avg_ctx = float(ctx.mean()) + tau * (R / 2)
     kv_bytes = B * cfg.n_layers * (avg_ctx + S) * cfg.n_kv_heads * D * 2 * 2
@@ -476,9 +433,14 @@ def run_gpu(args, rank, world, local_rank):
     round_flops = 2.0 * M * (cfg.n_layers * layer_params + V * H) + 2.0 * B * tau * inj_params
     prefill_flops = 2.0 * float(ctx.sum()) * inj_params
     if roofline_bound(lm_flops, lm_bytes, hbm, tf_sust) == "hbm":
-        lm_roof = {"bound": "hbm", "achieved": round(lm_bytes / (lm_avg_ms * 1e-3) / 1e9, 1), "peak": hbm,
-                   "unit": "GB/s", "frac": round(lm_bytes / (lm_avg_ms * 1e-3) / 1e9 / hbm, 4),
-                   "traffic": None if fp8 else lm_head_traffic(cfg), "peak_source": f"{peak_src} copy bandwidth"}
+        ach = lm_bytes / (lm_avg_ms * 1e-3) / 1e9
+        lm_roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
+                   "frac": round(ach / hbm, 4), "frac_of_8000": round(ach / 8000.0, 4),
+                   "traffic": None if fp8 else lm_head_traffic(cfg),
+                   "peak_source": f"{peak_src} copy bandwidth"}
+        if lm_roof["traffic"] is not None:
+            lm_roof["traffic_source"] = ("ncu capture on the mid shape, scaled to this launch by the weight "
+                                         "bytes it streams (profiles/lm_head_traffic_mid.md)")
     else:
         ach = lm_flops / (lm_avg_ms * 1e-3) / 1e12
         lm_roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": tf_sust, "unit": "TFLOP/s",
@@ -486,58 +448,204 @@ def run_gpu(args, rank, world, local_rank):
                    "peak_source": "measured bf16 sustained (f16 dense rate equals bf16 on this part)"}
     lm_roof.update({"kernel": "lm_head+argmax (tcgen05 GEMM)", "bytes_per_launch": lm_bytes,
                     "flops_per_launch": lm_flops, "avg_launch_us": round(lm_avg_ms * 1e3, 2)})
-    ctx_desc = f"prompt {int(ctx[0])}" if cfg.ctx0 else f"prompts U[{cfg.ctx_range[0]}, {cfg.ctx_range[1]}]"
-    p_desc = f"match p {cfg.match_p}" if cfg.match_p is not None else f"match p U[{cfg.p_range[0]}, {cfg.p_range[1]}]"
+    gbs = round_bytes / (round_ms * 1e-3) / 1e9
     res = {
-        "metric": METRIC,
-        "value": round(replica_rate((S - 1) * B, world, round_ms * 1e-3), 1),
-        "unit": "tok/s",
-        "n_gpus": world,
-        "steps": K,
-        "warmup": W,
-        "ms_per_step": round(round_ms, 4),
+        "value": round((S - 1) * B / (round_ms * 1e-3), 1),
         "round_us": round(round_ms * 1e3, 1),
         "round_us_p10_p50_p90": [round(pct(0.1) * 1e3, 1), round(pct(0.5) * 1e3, 1), round(pct(0.9) * 1e3, 1)],
-        "round_us_with_stand_in_verify": round(round_ms_incl * 1e3, 1),
-        "stand_in_verify_us": round(verify_ms * 1e3, 1),
-        "accepted_tok_s": round(accepted * world / (round_ms * K * 1e-3), 1),
+        "round_samples": len(full),
+        "stand_in_verify_us": round(statistics.mean(verify_ms) * 1e3, 1),
+        "round_us_with_stand_in_verify": round(total_ms / K * 1e3, 1),
+        "accepted_tok_s": round(accepted / (round_ms * K * 1e-3), 1),
         "mean_tau": round(tau, 3),
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "f16 activations, fp8 e4m3 weights" if fp8 else "f16",
-        "data": f"synthetic (seeded N(0,1) target features from the {feat_src}, N(0,0.02) random-init weights, "
-                "stand-in verify)",
-        "config": {"workload": f"{cfg.name} drafter batch {B}: H{H}, {cfg.n_q_heads}q/{cfg.n_kv_heads}kv x"
-                               f"{D}, I{cfg.intermediate}, {cfg.n_layers} layers, V{V}, fusion "
-                               f"{F}->{H}, {ctx_desc}, block {S}, {p_desc}",
-                   "batch": B, "prompt_mean": float(ctx.mean()), "rounds_per_slot": R,
-                   "attn_impl": ["library choice", "warp MMAs", "tcgen05"][args.attn_impl],
-                   "weights": "fp8 e4m3, per-row scales" if args.weights == "fp8" else "bf16 (held as f16)",
-                   "drafting": (f"sampled at temperature {args.temperature} (Gumbel-max, seed {args.seed})"
-                                if args.temperature > 0 else "greedy argmax"),
-                   "round_call": "dflash_draft_round" if args.fold_inject
-                   else "dflash_fuse_inject+dflash_draft_block", "slot_groups": n_groups - 1,
-                   "l2": "inputs larger than L2 (the drafter's weights stream every round)",
-                   "parallelism": f"replicas x{world}"},
-        "gpu_launches": launches_captured,
-        "plan": d.plan(),
-        "graph_kernel_nodes": n_kernels,
         "roofline": lm_roof,
-        "round_roofline": {"bytes_per_round": int(round_bytes), "achieved_gbs": round(
-            round_bytes / (round_ms * 1e-3) / 1e9, 1), "frac": round(round_bytes / (round_ms * 1e-3) / 1e9 / hbm, 4)},
+        "round_roofline": {"bytes_per_round": int(round_bytes), "achieved_gbs": round(gbs, 1),
+                           "frac": round(gbs / hbm, 4), "frac_of_8000": round(gbs / 8000.0, 4)},
         "round_tensor": {"flops_per_round": round_flops, "achieved_tflops": round(
             round_flops / (round_ms * 1e-3) / 1e12, 1), "peak": tf_sust,
             "frac": round(round_flops / (round_ms * 1e-3) / 1e12 / tf_sust, 4)},
         "prefill": {"tokens": int(ctx.sum()), "us": round(prefill_ms * 1e3, 1),
                     "tok_s": round(float(ctx.sum()) / (prefill_ms * 1e-3), 1),
-                    "flops": prefill_flops, "tensor_frac": round(prefill_flops / (prefill_ms * 1e-3) / 1e12 / tf_burst, 4),
+                    "flops": prefill_flops,
+                    "tensor_frac": round(prefill_flops / (prefill_ms * 1e-3) / 1e12 / tf_burst, 4),
                     "call": f"dflash_fuse_inject per request in {chunk}-token chunks (device time, not in the round)"},
         "clocks": clk,
         "status_word": status,
-        "e2e": e2e,
+        "gpu_launches": launches,
+        "graph_kernel_nodes": n_kernels,
+        "plan": d.plan(),
+        "steps": K,
+        "warmup": W,
+        "rounds_per_slot": R,
+        "slot_groups": n_groups - 1,
+        "feature_source": feat_src,
+        "weights_source": weights_desc,
     }
-    return res, cfg
+
+    # ---- end to end through the C ABI with host buffers: per round the
+    # block's target features and verify streams go host -> device from
+    # pinned memory and the round's result comes back; the host prepares
+    # round r+1's inputs while round r runs (double-buffered staging)
+    if e2e_steps > 0:
+        E = min(e2e_steps, R)
+        for b in range(B):
+            d.reset_slot(gw * B + b, stream)
+        prefill(gw)
+        st = RoundState(d, B, slots=[gw * B + b for b in range(B)], first_token=cfg.first_token)
+        m_dev = torch.zeros(1, B, S, dtype=torch.int32, device=dev)
+        u_dev = torch.zeros_like(m_dev)
+        ver = SyntheticVerify(st, m_dev, u_dev, None)
+        if temperature > 0:
+            st.set_sampling(temperature, seed, ver.round_ctr)
+        d.graph_begin(stream)
+        run_round(st, ver, stream, folded=fold)
+        d.graph_end(stream)
+        feats_h = [torch.empty(B, S, F, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+        mu_h = [torch.empty(2, B, S, dtype=torch.int32).pin_memory() for _ in range(2)]
+        out_h = [torch.empty(B, S + 2, dtype=torch.int32).pin_memory() for _ in range(2)]
+        done = [torch.cuda.Event() for _ in range(2)]
+        fs_host = binding.bf16_host(fs) if fs is not None else feat_stream[:, :S].cpu()
+        m_t, u_t = torch.from_numpy(m), torch.from_numpy(u)
+        stream.synchronize()
+
+        def prepare(buf, r, pos):
+            """Inputs of round r: the features of the block positions of round
+            r-1 (pos = that round's first position), the verify streams."""
+            for b in range(B):
+                if fs is not None:
+                    feats_h[buf][b].copy_(fs_host[b, pos[b]:pos[b] + S])
+                else:  # the device-drawn stream's first rows stand in on the host
+                    feats_h[buf][b].copy_(fs_host[b])
+            mu_h[buf][0].copy_(m_t[r % len(m_t)])
+            mu_h[buf][1].copy_(u_t[r % len(u_t)])
+
+        t0 = time.perf_counter()
+        prepare(0, 0, ctx)
+        for r in range(E):
+            buf = r & 1
+            with torch.cuda.stream(stream):
+                st.feats.copy_(feats_h[buf], non_blocking=True)
+                m_dev[0].copy_(mu_h[buf][0], non_blocking=True)
+                u_dev[0].copy_(mu_h[buf][1], non_blocking=True)
+                d.graph_launch(stream)
+                out_h[buf][:, :S - 1].copy_(st.draft, non_blocking=True)
+                out_h[buf][:, S - 1].copy_(st.accept_len, non_blocking=True)
+                out_h[buf][:, S].copy_(st.ctx_len, non_blocking=True)
+                done[buf].record(stream)
+            if r + 1 < E:
+                if r >= 1:  # round r+1 injects round r's block features: round r starts at r-1's confirmed length
+                    done[buf ^ 1].synchronize()
+                    pos = out_h[buf ^ 1][:, S].numpy().astype(int)
+                else:
+                    pos = ctx
+                prepare(buf ^ 1, r + 1, pos)
+        done[(E - 1) & 1].synchronize()
+        t_e2e = time.perf_counter() - t0
+        h2d = feats_h[0].numel() * 2 + mu_h[0].numel() * 4
+        d2h = out_h[0].numel() * 4
+        res["e2e"] = {"value": round((S - 1) * B * E / t_e2e, 1), "unit": "tok/s", "h2d_bytes_per_step": h2d,
+                      "d2h_bytes_per_step": d2h, "steps": E, "round_us": round(t_e2e / E * 1e6, 1),
+                      "note": "dflash_graph_launch of one round per step with pinned host staging, double-buffered; "
+                              "includes the stand-in verify kernel"}
+    d.close()
+    del d, states, verifies, feat_stream, match, offs
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
+
+
+def workload_desc(cfg, ctx_mean):
+    B, H, D, F = cfg.batch, cfg.hidden, cfg.head_dim, cfg.fused_dim
+    ctx_desc = f"prompt {cfg.ctx0}" if cfg.ctx0 else f"prompts U[{cfg.ctx_range[0]}, {cfg.ctx_range[1]}]"
+    p_desc = f"match p {cfg.match_p}" if cfg.match_p is not None else f"match p U[{cfg.p_range[0]}, {cfg.p_range[1]}]"
+    return (f"{cfg.name} drafter batch {B}: H{H}, {cfg.n_q_heads}q/{cfg.n_kv_heads}kv x{D}, I{cfg.intermediate}, "
+            f"{cfg.n_layers} layers, V{cfg.vocab}, fusion {F}->{H}, {ctx_desc}, block {cfg.block}, {p_desc}")
+
+
+SUMMARY_KEYS = ("value", "round_us", "round_us_p10_p50_p90", "round_samples", "stand_in_verify_us", "mean_tau",
+                "accepted_tok_s", "roofline", "round_roofline", "round_tensor", "prefill", "clocks", "steps",
+                "warmup", "gpu_launches", "plan", "status_word", "weights_source", "feature_source")
+
+
+def run_gpu(args):
+    import torch
+    from block_diffusion_speculative_hiddens_gb300 import weights_to_device
+    from workload import context_lengths, get_config, make_weights
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda:0")
+    cfg = get_config(args.config)
+    if args.block:
+        cfg = cfg.with_(block=args.block)
+    B = cfg.batch
+    K = args.steps if args.steps is not None else (512 if B == 1 else (args.rounds_per_slot or cfg.rounds))
+    W = args.warmup
+    w_np = make_weights(cfg)
+    w_dev = weights_to_device(w_np, 0)
+    head = measure(cfg, w_dev, dev, K, W, attn_impl=args.attn_impl, weight_fp8=1 if args.weights == "fp8" else 0,
+                   temperature=args.temperature, seed=args.seed, fold=args.fold_inject, e2e_steps=args.e2e_steps,
+                   rounds_per_slot=args.rounds_per_slot)
+    ctx = context_lengths(cfg)
+    res = {
+        "metric": METRIC,
+        "value": head["value"],
+        "unit": "tok/s",
+        "n_gpus": 1,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": round(head["round_us"] * 1e-3, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16 activations, fp8 e4m3 weights" if args.weights == "fp8" else "f16",
+        "data": f"synthetic (seeded N(0,1) target features from the {head['feature_source']}, N(0,0.02) "
+                "random-init weights from the workload generator, stand-in verify)",
+        "config": {"workload": workload_desc(cfg, float(ctx.mean())), "batch": B, "prompt_mean": float(ctx.mean()),
+                   "rounds_per_slot": head["rounds_per_slot"], "slot_groups": head["slot_groups"],
+                   "attn_impl": ["library choice", "warp MMAs", "tcgen05"][args.attn_impl],
+                   "weights": "fp8 e4m3, per-row scales" if args.weights == "fp8" else "bf16 (held as f16)",
+                   "drafting": (f"sampled at temperature {args.temperature} (Gumbel-max, seed {args.seed})"
+                                if args.temperature > 0 else "greedy argmax"),
+                   "round_call": "dflash_draft_round" if args.fold_inject
+                   else "dflash_fuse_inject+dflash_draft_block",
+                   "l2": "inputs larger than L2 (the drafter's weights stream every round)",
+                   "parallelism": "single GPU"},
+        "timing": "one CUDA graph of the K timed rounds with event marks around every stand-in verify: ms_per_step "
+                  "is the graph's time outside the verify intervals / K (each round's accept, fuse_inject and "
+                  "draft_block); the percentiles are the same graph's per-round intervals",
+    }
+    res.update({k: head[k] for k in ("round_us", "round_us_p10_p50_p90", "round_samples", "stand_in_verify_us",
+                                     "round_us_with_stand_in_verify", "accepted_tok_s", "mean_tau", "gpu_launches",
+                                     "plan", "graph_kernel_nodes", "roofline", "round_roofline", "round_tensor",
+                                     "prefill", "clocks", "status_word")})
+    if "e2e" in head:
+        res["e2e"] = head["e2e"]
+
+    names = [] if args.workloads == "none" else (
+        list(EXTRA_WORKLOADS) if args.workloads == "all" else [n for n in args.workloads.split(",") if n])
+    workloads = {cfg.name: {k: head[k] for k in SUMMARY_KEYS}} if names else {}
+    for name in names:
+        if name == cfg.name:
+            continue
+        wc = get_config(name)
+        if name == "tiny":
+            wd, src = weights_to_device(make_weights(wc), 0), "workload generator"
+        elif (wc.hidden, wc.n_q_heads, wc.n_kv_heads, wc.intermediate, wc.n_layers, wc.vocab, wc.seed) == \
+                (cfg.hidden, cfg.n_q_heads, cfg.n_kv_heads, cfg.intermediate, cfg.n_layers, cfg.vocab, cfg.seed) \
+                and args.weights == "bf16":
+            wd, src = w_dev, "workload generator (the headline drafter's weights)"
+        else:
+            wd, src = device_weights(wc, dev, 7919 + len(workloads)), \
+                "device generator (torch.normal_ N(0,0.02), seeded; gains 1)"
+        r = measure(wc, wd, dev, EXTRA_STEPS.get(name, 16), min(W, 3), attn_impl=args.attn_impl, weights_desc=src)
+        if wd is not w_dev:
+            del wd
+        s = {k: r[k] for k in SUMMARY_KEYS}
+        s["workload"] = workload_desc(wc, 0.0)
+        workloads[name] = s
+    if workloads:
+        res["workloads"] = workloads
+    return res, cfg, w_np
 
 
 def run_spec_generate(args):
@@ -593,11 +701,45 @@ def run_spec_generate(args):
                                    f"shape, prompt {P}, block 16", "target_layers": args.target_layers}}
 
 
+ONE_THREAD_ENV = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS")
+
+
+def oracle_one_thread(name: str, rounds: int, budget_s: float):
+    """The oracle's round time on one host thread (a child process whose BLAS
+    runs single-threaded), or None if it could not run."""
+    env = dict(os.environ, **{k: "1" for k in ONE_THREAD_ENV})
+    code = ("import json, statistics, sys; sys.path.insert(0, %r); import bench; from workload import get_config; "
+            "t, _ = bench.oracle_round_seconds(get_config(%r), %r, %d); print(json.dumps(t))"
+            % (ROOT, name, budget_s, rounds))
+    try:
+        r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                           timeout=budget_s * 4 + 60)
+        times = json.loads(r.stdout.strip().splitlines()[-1])
+    except Exception:
+        return None
+    return times
+
+
+def cpu_baseline_line(cfg, weights, budget_s):
+    times, _ = oracle_round_seconds(cfg, budget_s, 4, weights=weights)
+    rs = statistics.mean(times)
+    out = {"value": round((cfg.block - 1) / rs, 3), "unit": "tok/s", "cores": os.cpu_count(), "kind": "oracle",
+           "sample": f"{len(times)} round(s) of the same workload (request 0) after an untimed "
+                     f"{cfg.ctx0 or cfg.ctx_range[0]}-token prefill, float64 NumPy, BLAS on every host core"}
+    one = oracle_one_thread("tiny", 8, 20.0)
+    if one:
+        rs1 = statistics.mean(one)
+        out["tiny_one_thread"] = {"value": round(15 / rs1, 3), "unit": "tok/s", "cores": 1,
+                                  "ms_per_round": round(rs1 * 1e3, 2),
+                                  "sample": f"{len(one)} rounds of the tiny workload after its 128-token prefill, "
+                                            "one host thread"}
+    return out
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
-    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
 
     if args.impl == "reference":
         # the CPU oracle on the host cores; rank 0 alone, other ranks exit
@@ -631,25 +773,23 @@ def main():
         print(json.dumps(line), flush=True)
         return
 
+    if args.gpus > 1 or world > 1:
+        # one GPU per process: there is no multi-GPU path to run or time
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "n_gpus": max(args.gpus, world), "value": None,
+                              "unavailable": "single-GPU library: a replica per GPU is an independent process "
+                                             "running this benchmark with --gpus 1; nothing is shared or "
+                                             "exchanged between GPUs, so no multi-GPU run is made"}), flush=True)
+        return
+
     import torch
     if args.spec_generate:
-        if rank == 0:
-            print(json.dumps(run_spec_generate(args)), flush=True)
+        print(json.dumps(run_spec_generate(args)), flush=True)
         return
-    if world > 1:
-        torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-    res, cfg = run_gpu(args, rank, world, local_rank)
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        times, taus = oracle_round_seconds(cfg, args.cpu_budget_s, 4)
-        rs = statistics.mean(times)
-        res["cpu_baseline"] = {"value": round((cfg.block - 1) / rs, 3), "unit": "tok/s", "cores": os.cpu_count(),
-                               "kind": "oracle",
-                               "sample": f"{len(times)} round(s) of the same workload (request 0) after an "
-                                         f"untimed {cfg.ctx0 or cfg.ctx_range[0]}-token prefill, float64 NumPy"}
-    if world > 1:
-        torch.distributed.destroy_process_group()
-    if rank == 0:
-        print(json.dumps(res), flush=True)
+    res, cfg, w_np = run_gpu(args)
+    if not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline_line(cfg, w_np, args.cpu_budget_s)
+    print(json.dumps(res), flush=True)
 
 
 if __name__ == "__main__":
