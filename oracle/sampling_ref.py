@@ -29,7 +29,8 @@ from __future__ import annotations
 
 import numpy as np
 
-DRAFT = 1  # purpose id of the drafter's Gumbel streams
+DRAFT = 1   # purpose id of the drafter's Gumbel streams
+TARGET = 2  # purpose id of the target's Gumbel streams
 
 _MASK = (1 << 64) - 1
 _GOLD = 0x9E3779B97F4A7C15
@@ -91,6 +92,21 @@ def sample_drafts(z: np.ndarray, temperature: float, seed: int, b: int, rnd: int
     d, mg = [], []
     for k in range(z.shape[0]):
         idx, m = sample_row(z[k], temperature, stream_key(seed, DRAFT, b, rnd, k + 1))
+        d.append(idx)
+        mg.append(m)
+    return np.array(d, dtype=np.int64), np.array(mg)
+
+
+def sample_target_rows(z: np.ndarray, temperature: float, seed: int, slot: int, pos0: int):
+    """The target's sampled tokens for block rows at positions pos0, pos0+1, ..
+    of request `slot` (the verify step at temperature T > 0): row i's token
+    -- the one that follows position pos0+i -- is drawn from softmax(z_i / T)
+    with the stream (seed, TARGET, slot, pos0+i).  Keyed by position, not by
+    round, so the speculative loop and the target's own sampled decoding draw
+    the same numbers for the same position.  Returns (tokens, margins)."""
+    d, mg = [], []
+    for i in range(z.shape[0]):
+        idx, m = sample_row(z[i], temperature, stream_key(seed, TARGET, slot, pos0 + i))
         d.append(idx)
         mg.append(m)
     return np.array(d, dtype=np.int64), np.array(mg)

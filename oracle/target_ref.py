@@ -24,7 +24,14 @@ Readings taken where the pages are silent:
     spread, first and last excluded), rounded to bf16 at the interface (the
     drafter's feature input is bf16);
   * generation starts from the target's greedy token at the last prompt
-    position.
+    position;
+  * at temperature T > 0 the target samples its own token at every block
+    position ([Code walkthrough] §三 第3步 compares the block with the
+    target's sampled tokens; [Paper walkthrough] Results reports sampling at
+    T = 1) by the Gumbel-max rule on a stream keyed by the position
+    (sampling_ref.sample_target_rows), so a position's draw does not depend
+    on which round or block it falls in -- the speculative loop then emits
+    exactly the target's own sampled decoding.
 """
 from __future__ import annotations
 
@@ -95,11 +102,12 @@ class OracleTarget:
         self.V = [np.zeros((capacity, hkv, D)) for _ in range(n_layers)]
         self.ctx_len = 0
 
-    def forward(self, tokens) -> dict:
+    def forward(self, tokens, temperature: float = 0.0, seed: int = 0, slot: int = 0) -> dict:
         """The block's tokens at positions ctx_len.. (their K/V are written to
         the cache; ctx_len moves only with advance()).  Returns the logits of
-        every row, their argmax and top-2 margin, and the 5 tap features
-        (float64 and bf16 bits) of every row."""
+        every row, its token -- the argmax, or at temperature > 0 the draw of
+        sampling_ref.sample_target_rows -- with the top-2 margin of the
+        (perturbed) scores, and the 5 tap features (float64 and bf16 bits)."""
         tokens = np.asarray(tokens)
         L = self.ctx_len
         S = len(tokens)
@@ -112,34 +120,40 @@ class OracleTarget:
             if l in self.taps:
                 feats[:, self.taps.index(l)] = h
         logits = lm_head_logits(self.model, h)
-        top2 = np.partition(logits, -2, axis=-1)[:, -2:]
-        return dict(logits=logits, tok=np.argmax(logits, -1).astype(np.int64), margin=top2[:, 1] - top2[:, 0],
-                    feats=feats, feats_bf16=f64_to_bf16_bits(feats))
+        if temperature > 0:
+            from .sampling_ref import sample_target_rows
+            tok, margin = sample_target_rows(logits, temperature, seed, slot, L)
+        else:
+            top2 = np.partition(logits, -2, axis=-1)[:, -2:]
+            tok, margin = np.argmax(logits, -1).astype(np.int64), top2[:, 1] - top2[:, 0]
+        return dict(logits=logits, tok=tok, margin=margin, feats=feats, feats_bf16=f64_to_bf16_bits(feats))
 
     def advance(self, n: int):
         self.ctx_len += int(n)
 
-    def prefill(self, prompt, chunk: int = 16) -> dict:
+    def prefill(self, prompt, chunk: int = 16, temperature: float = 0.0, seed: int = 0, slot: int = 0) -> dict:
         """Run the prompt in chunks; returns the last chunk's outputs and the
         bf16 features of every prompt position."""
         prompt = np.asarray(prompt)
         feats = []
         out = None
         for p0 in range(0, len(prompt), chunk):
-            out = self.forward(prompt[p0:p0 + chunk])
+            out = self.forward(prompt[p0:p0 + chunk], temperature, seed, slot)
             self.advance(min(chunk, len(prompt) - p0))
             feats.append(out["feats_bf16"])
         return dict(last=out, feats_bf16=np.concatenate(feats, 0))
 
 
-def greedy_generate(target: OracleTarget, prompt, n_new: int):
-    """The target's own greedy decoding: n_new tokens after the prompt, with
-    each token's top-2 margin."""
-    pf = target.prefill(prompt)
+def greedy_generate(target: OracleTarget, prompt, n_new: int, temperature: float = 0.0, seed: int = 0,
+                    slot: int = 0):
+    """The target's own decoding: n_new tokens after the prompt, greedy, or
+    at temperature > 0 each drawn as in sampling_ref.sample_target_rows;
+    with each token's top-2 margin."""
+    pf = target.prefill(prompt, temperature=temperature, seed=seed, slot=slot)
     g = int(pf["last"]["tok"][-1])
     out, margins = [g], [float(pf["last"]["margin"][-1])]
     while len(out) < n_new:
-        o = target.forward([g])
+        o = target.forward([g], temperature, seed, slot)
         target.advance(1)
         g = int(o["tok"][0])
         out.append(g)
@@ -147,19 +161,31 @@ def greedy_generate(target: OracleTarget, prompt, n_new: int):
     return np.array(out, dtype=np.int64), np.array(margins)
 
 
-def spec_generate(drafter, draft_req, target: OracleTarget, prompt, n_new: int, block: int, draft_fn=None):
+def spec_generate(drafter, draft_req, target: OracleTarget, prompt, n_new: int, block: int, draft_fn=None,
+                  temperature: float = 0.0, seed: int = 0, slot: int = 0):
     """Speculative generation: prefill both models, then rounds of draft ->
     verify -> accept -> trim until n_new tokens are out.  draft_fn(out, b0)
-    may replace the drafter's tokens (tests that force long acceptances)."""
-    pf = target.prefill(prompt)
+    may replace the drafter's tokens (tests that force long acceptances).
+    At temperature > 0 the drafter draws each draft from its own softmax
+    (sampling_ref.sample_drafts, request 0, round index of the generation)
+    and the target samples its tokens by position; acceptance is unchanged."""
+    from .sampling_ref import sample_drafts
+    pf = target.prefill(prompt, temperature=temperature, seed=seed, slot=slot)
     drafter.fuse_inject(draft_req, pf["feats_bf16"])
     b0 = int(pf["last"]["tok"][-1])
     out = [b0]
     taus = []
+    rnd = 0
     while len(out) < n_new:
-        d = drafter.draft(draft_req, b0, want_logits=False)["draft"] if draft_fn is None else draft_fn(out, b0)
+        if draft_fn is not None:
+            d = draft_fn(out, b0)
+        elif temperature > 0:
+            d, _ = sample_drafts(drafter.draft(draft_req, b0)["logits"], temperature, seed, 0, rnd)
+        else:
+            d = drafter.draft(draft_req, b0, want_logits=False)["draft"]
+        rnd += 1
         d = np.asarray(d, dtype=np.int64)[:block - 1]
-        v = target.forward(np.concatenate([[b0], d]))
+        v = target.forward(np.concatenate([[b0], d]), temperature, seed, slot)
         tau, bonus = accept_longest_prefix(d, v["tok"])
         target.advance(tau)
         drafter.fuse_inject(draft_req, v["feats_bf16"][:tau])

@@ -126,3 +126,72 @@ def test_planted_mistake_breaks_losslessness(models, monkeypatch):
     got, _ = T.spec_generate(O.OracleDrafter(dm), O.OracleRequest(CFG, 120), T.OracleTarget(tm, NL, 120),
                              prompt, 20, CFG.block)
     assert not np.array_equal(got, greedy)
+
+
+TEMP = 1.0
+
+
+@pytest.mark.parametrize("mode", ["drafter", "perfect", "corrupt"])
+def test_sampled_speculative_output_is_the_targets_sampled_output(models, mode):
+    """At temperature 1 the verify step compares the block with the target's
+    sampled tokens ([Code walkthrough] §三 第3步).  With the target's draws
+    keyed by position, every emitted token is the target's own draw for its
+    position given the same prefix, so speculative sampling emits exactly the
+    target's own sampled decoding for the same seed, whatever the drafts."""
+    tm, dm = models
+    prompt = prompt_tokens(CFG, 4, 33)
+    n_new, seed = 48, 77
+    plain, _ = T.greedy_generate(T.OracleTarget(tm, NL, 160), prompt, n_new, TEMP, seed, slot=3)
+    greedy, _ = T.greedy_generate(T.OracleTarget(tm, NL, 160), prompt, n_new)
+    assert not np.array_equal(plain, greedy)  # the draws are not the argmax
+    draft_fn = None
+    if mode != "drafter":
+        def draft_fn(out, b0, _g=plain):
+            k = len(out)
+            d = np.array([_g[k + i] if k + i < len(_g) else 0 for i in range(CFG.block - 1)])
+            if mode == "corrupt":
+                j = (k * 5) % (CFG.block - 1)
+                d[j] = (d[j] + 1) % (CFG.vocab - 1)
+            return d
+    got, taus = T.spec_generate(O.OracleDrafter(dm), O.OracleRequest(CFG, 160), T.OracleTarget(tm, NL, 160), prompt,
+                                n_new, CFG.block, draft_fn, temperature=TEMP, seed=seed, slot=3)
+    assert np.array_equal(got, plain)
+    if mode == "perfect":
+        assert all(t == CFG.block for t in taus[:-1])
+    if mode == "corrupt":
+        assert max(taus) > 1 and min(taus) < CFG.block
+
+
+def test_sampled_decoding_tends_to_greedy_as_temperature_vanishes(models):
+    tm, _ = models
+    prompt = prompt_tokens(CFG, 5, 20)
+    cold, _ = T.greedy_generate(T.OracleTarget(tm, NL, 80), prompt, 24, 1e-9, 5)
+    greedy, _ = T.greedy_generate(T.OracleTarget(tm, NL, 80), prompt, 24)
+    assert np.array_equal(cold, greedy)
+
+
+def test_target_draws_keyed_by_round_break_losslessness(models, monkeypatch):
+    """Planted mistake: the target's stream keyed by the row within the block
+    (as the drafter's is) instead of the position -- then a position's draw
+    depends on where the block starts, and speculative sampling no longer
+    reproduces the target's own sampled decoding."""
+    import oracle.sampling_ref as SR
+    tm, dm = models
+
+    def by_row(z, temperature, seed, slot, pos0):
+        d, mg = [], []
+        for i in range(z.shape[0]):
+            idx, m = SR.sample_row(z[i], temperature, SR.stream_key(seed, SR.TARGET, slot, i))
+            d.append(idx)
+            mg.append(m)
+        return np.array(d, dtype=np.int64), np.array(mg)
+    monkeypatch.setattr(SR, "sample_target_rows", by_row)
+    prompt = prompt_tokens(CFG, 4, 33)
+    plain, _ = T.greedy_generate(T.OracleTarget(tm, NL, 160), prompt, 40, TEMP, 77, slot=3)
+
+    def draft_fn(out, b0):  # the plain sampled continuation, so blocks are accepted past row 0
+        k = len(out)
+        return np.array([plain[k + i] if k + i < len(plain) else 0 for i in range(CFG.block - 1)])
+    got, _ = T.spec_generate(O.OracleDrafter(dm), O.OracleRequest(CFG, 160), T.OracleTarget(tm, NL, 160), prompt,
+                             40, CFG.block, draft_fn, temperature=TEMP, seed=77, slot=3)
+    assert not np.array_equal(got, plain)
