@@ -279,13 +279,15 @@ def measure(cfg, w_dev, dev, K, W, *, attn_impl=0, weight_fp8=0, temperature=0.0
     """Run K timed drafting rounds of `cfg` (after W warm-up rounds) as one
     CUDA graph and return the measurements.
 
-    Timed graph: [mark] then per round fuse_inject + draft_block, [mark],
-    stand-in verify, [mark], accept_trim, and a final [mark].  The intervals
-    between marks split the graph into the drafter's work (accept of the
-    previous round + inject + draft of this one) and the stand-in verify, so
-    the round time, its percentiles and the verify's time all come from the
-    same replay; the lm_head launches carry CUDA-event probes in the same
-    graph (its end probe coincides with the verify's first mark)."""
+    Timed graph: per round fuse_inject + draft_block, the stand-in verify,
+    accept_trim.  The graph is timed with CUDA events on its stream; the
+    stand-in verify writes device timestamps (%globaltimer) when it may
+    start (the drafter's kernels before it complete) and when its last block
+    is done, so the drafter's time -- the graph's time outside the verify
+    windows -- and its per-round intervals (accept of the previous round +
+    inject + draft of this one) come from the same replay, with no extra
+    node in the graph; the lm_head launches carry CUDA-event probes in the
+    same graph."""
     import numpy as np
     import torch
     from block_diffusion_speculative_hiddens_gb300 import Drafter, binding
@@ -361,23 +363,16 @@ def measure(cfg, w_dev, dev, K, W, *, attn_impl=0, weight_fp8=0, temperature=0.0
     d.graph_launch(stream)
     stream.synchronize()
 
-    # timed: K rounds, R per slot group, one graph with marks around each verify
-    n_marks = 2 * K + 2
-    d.marks_arm(n_marks)
+    # timed: K rounds, R per slot group, one graph; the verify windows stamped on the device
+    stamps = torch.zeros(K, 2, dtype=torch.int64, device=dev)
+    d.stamps_arm(stamps, K)
     d.probe_arm(binding.KID_LM_HEAD, K)
     n0 = d.launch_count()
     d.graph_begin(stream)
-    d.mark(stream)
     for i in range(K):
-        ver = verifies[i // R]
-
-        def marked(s_=None, ver=ver):
-            d.mark(s_)
-            ver(s_)
-            d.mark(s_)
-        run_round(states[i // R], marked, stream, folded=fold)
-    d.mark(stream)
+        run_round(states[i // R], verifies[i // R], stream, folded=fold)
     n_kernels = d.graph_end(stream)
+    d.stamps_arm(None, 0)
     launches = d.launch_count() - n0
     stream.synchronize()
     torch.cuda.synchronize()
@@ -394,7 +389,7 @@ def measure(cfg, w_dev, dev, K, W, *, attn_impl=0, weight_fp8=0, temperature=0.0
     torch.cuda.synchronize()
     clk = clocks.stop(t_wall0, t_wall1)
     total_ms = e0.elapsed_time(e1)
-    iv = d.marks_read(n_marks - 1)
+    st_ns = stamps.cpu().numpy().astype(np.int64)
     lm_ms = d.probe_read(K)
     status = d.read_status()
     accepted = 0
@@ -402,10 +397,9 @@ def measure(cfg, w_dev, dev, K, W, *, attn_impl=0, weight_fp8=0, temperature=0.0
         if min(R, K - g * R) > 0:
             accepted += int((states[g].ctx_len.cpu().numpy() - ctx).sum())
 
-    drafter_ms = iv[0::2]                                # accept(prev) + inject + draft, per round
-    verify_ms = iv[1::2]
-    round_ms = sum(drafter_ms) / K                       # every kernel of the K rounds but the verify
-    full = sorted(drafter_ms[1:K])                       # rounds 1..K-1: one accept + inject + draft each
+    verify_ms = [(int(e) - int(s)) * 1e-6 for s, e in st_ns]         # the stand-in verify windows
+    round_ms = (total_ms - sum(verify_ms)) / K           # every kernel of the K rounds but the verify
+    full = sorted((int(st_ns[r][0]) - int(st_ns[r - 1][1])) * 1e-6 for r in range(1, K))  # accept + inject + draft
     pct = (lambda q: full[min(len(full) - 1, int(q * len(full)))]) if full else (lambda q: round_ms)
 
     # ---- rooflines: the dominant kernel (lm_head + argmax) and the round
@@ -610,9 +604,10 @@ def run_gpu(args):
                    else "dflash_fuse_inject+dflash_draft_block",
                    "l2": "inputs larger than L2 (the drafter's weights stream every round)",
                    "parallelism": "single GPU"},
-        "timing": "one CUDA graph of the K timed rounds with event marks around every stand-in verify: ms_per_step "
-                  "is the graph's time outside the verify intervals / K (each round's accept, fuse_inject and "
-                  "draft_block); the percentiles are the same graph's per-round intervals",
+        "timing": "one CUDA graph of the K timed rounds, timed with CUDA events on its stream; the stand-in verify "
+                  "stamps its window on the device (%globaltimer): ms_per_step is the graph's time outside the "
+                  "verify windows / K, the percentiles are the same replay's per-round intervals between verify "
+                  "windows (each an accept, a fuse_inject and a draft_block)",
     }
     res.update({k: head[k] for k in ("round_us", "round_us_p10_p50_p90", "round_samples", "stand_in_verify_us",
                                      "round_us_with_stand_in_verify", "accepted_tok_s", "mean_tau", "gpu_launches",

@@ -22,6 +22,7 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported shape", 3: "capacity e
           7: "a weight exceeds the f16 range"}
 DEV_TIMEOUT, DEV_NAN, DEV_PAGE, DEV_CAPACITY, DEV_ARG, DEV_RANGE = 0x01, 0x02, 0x04, 0x08, 0x10, 0x20
 KID_LM_HEAD, KID_GATE_UP, KID_ATTENTION, KID_DOWN, KID_QKV, KID_WO, KID_FC, KID_INJECT = 1, 2, 3, 4, 5, 6, 7, 8
+KID_ALL = 255  # trace_arm: every GEMM and attention launch in turn
 
 _c_int_p = ctypes.POINTER(ctypes.c_int32)
 _vp = ctypes.c_void_p
@@ -83,7 +84,10 @@ _SIGS = {
     "dflash_plan": (ctypes.c_int, [_vp, _vp]),
     "dflash_verify_block": (ctypes.c_int, [_vp, _vp, ctypes.c_int32, _vp, _vp, _vp, _vp, _vp]),
     "dflash_advance": (ctypes.c_int, [_vp, _vp, ctypes.c_int32, _vp, _vp]),
+    "dflash_verify_block_sample": (ctypes.c_int, [_vp, _vp, ctypes.c_int32, _vp, _vp, ctypes.c_float,
+                                                  ctypes.c_uint64, _vp, _vp, _vp]),
     "dflash_trace_arm": (ctypes.c_int, [_vp, ctypes.c_int32, _vp, ctypes.c_int32]),
+    "dflash_stamps_arm": (ctypes.c_int, [_vp, _vp, ctypes.c_int32]),
     "dflash_harness_verify": (ctypes.c_int, [_vp, _vp, ctypes.c_int32, _vp, _vp, _vp, ctypes.c_int32, _vp,
                                              _vp, _vp, ctypes.c_int32, _vp, _vp]),
 }
@@ -284,6 +288,20 @@ class Drafter:
             self.h, _ptr(slots), slots.numel(), _ptr(tokens), _ptr(n_valid), _ptr(out_tok), _ptr(feats),
             _stream(stream)))
 
+    def verify_block_sample(self, slots, tokens, out_tok, temperature: float, seed: int, n_valid=None, feats=None,
+                            stream=None):
+        """verify_block with every row's token drawn from softmax(logits / temperature),
+        keyed by (seed, slot, position)."""
+        B = slots.numel()
+        _need(slots, "int32", B, "slots", self.device)
+        _need(tokens, "int32", B * 16, "tokens", self.device)
+        _need(out_tok, "int32", B * 16, "out_tok", self.device)
+        _need(n_valid, "int32", B, "n_valid", self.device, optional=True)
+        _need(feats, "bfloat16", B * 16 * self.cfg.n_fused * self.cfg.hidden, "feats", self.device, optional=True)
+        _check("dflash_verify_block_sample", self.lib.dflash_verify_block_sample(
+            self.h, _ptr(slots), slots.numel(), _ptr(tokens), _ptr(n_valid), float(temperature),
+            int(seed) & ((1 << 64) - 1), _ptr(out_tok), _ptr(feats), _stream(stream)))
+
     def advance(self, slots, n, stream=None):
         """ctx_len[slot] += n[b] (the trim after acceptance / a prefill chunk's step)."""
         B = slots.numel()
@@ -372,6 +390,13 @@ class Drafter:
         """Arm a per-CTA timeline of the next launch of a GEMM kernel; buf is an
         int64 device tensor [cap_ctas, 8]."""
         _check("dflash_trace_arm", self.lib.dflash_trace_arm(self.h, kernel_id, _ptr(buf), cap_ctas))
+
+    def stamps_arm(self, buf=None, n: int = 0):
+        """Device timestamps of the next n stand-in verify calls into buf
+        (int64 device tensor [n, 2]: start, end in ns)."""
+        if n > 0:
+            _need(buf, "int64", 2 * n, "stamps", self.device)
+        _check("dflash_stamps_arm", self.lib.dflash_stamps_arm(self.h, _ptr(buf) if n > 0 else None, n))
 
     def launch_count(self) -> int:
         return int(self.lib.dflash_launch_count(self.h))

@@ -73,9 +73,23 @@ struct Probe {
 };
 
 struct Trace {
-  int kid = 0;
+  int kid = 0;  // DFLASH_KID_*, or DFLASH_KID_ALL: every GEMM and attention launch in turn
   unsigned long long* buf = nullptr;
   int cap = 0;  // CTAs the buffer holds
+  int used = 0; // DFLASH_KID_ALL: rows taken by the launches so far
+  // Rows of buf for the next launch of kernel `kid` (null: not traced).
+  unsigned long long* take(int k, long long ctas) {
+    if (!buf || !k) return nullptr;
+    if (kid == DFLASH_KID_ALL) {
+      if (used + ctas > cap) return nullptr;
+      unsigned long long* r = buf + (size_t)used * 8;
+      used += (int)ctas;
+      return r;
+    }
+    if (kid != k || ctas > cap) return nullptr;
+    kid = 0;  // one launch only
+    return buf;
+  }
 };
 
 }  // namespace
@@ -140,6 +154,8 @@ struct dflash_handle {
   Probe probe;
   Probe marks;  // timeline marks: ev[i] = mark i, n = capacity, next = recorded
   Trace trace;
+  unsigned long long* stamps = nullptr;  // harness verify stamps [stamp_cap][2] (null: off)
+  int stamp_cap = 0, stamp_next = 0;
   cudaGraph_t graph = nullptr;
   cudaGraphExec_t exec = nullptr;
 };
@@ -287,7 +303,7 @@ size_t carve(dflash_handle* h, const dflash_config& c, char* base, int num_sms) 
     const int gs = DFL_ATTN_GLOBAL ? global_attn_splits(c, num_sms) : 1;
     o->attn_part = gs > 1 ? w.take<float>((size_t)c.max_batch * hkv * gs * attn_part_floats(D)) : nullptr;
   }
-  o->tile_ctr = w.take<unsigned>(tiles);
+  o->tile_ctr = w.take<unsigned>(2 * (size_t)tiles);  // arrivals, then finalisers done
   if (h) {
     h->attn_splits = splits;
     h->max_tiles = tiles;
@@ -397,6 +413,7 @@ int run_gemm(dflash_handle* h, cudaStream_t s, int mode, const void* const* a, i
   p.status = h->status;
   p.ws = h->gemm_ws;
   p.tile_ctr = h->tile_ctr;
+  p.tile_fin = h->tile_ctr + h->max_tiles;
   p.eps = h->cfg.rms_eps;
   p.H = h->cfg.hidden;
   p.hq = h->cfg.n_q_heads;
@@ -409,10 +426,7 @@ int run_gemm(dflash_handle* h, cudaStream_t s, int mode, const void* const* a, i
   const int clusters = (int)std::min<long long>(units, gs.cl > 1 ? h->gemm_cl_ctas / gs.cl : h->num_sms);
   const int grid = clusters * gs.cl;
   if (units * (clusters + 1) >= (1LL << 31)) return DFLASH_ERR_SHAPE;  // the kernel's unit math is 32-bit
-  if (kid && h->trace.kid == kid && h->trace.buf && grid <= h->trace.cap) {
-    p.trace = h->trace.buf;  // one launch only
-    h->trace.kid = 0;
-  }
+  if (unsigned long long* tb = h->trace.take(kid, grid)) p.trace = tb;
   ProbeScope ps(h, kid, s);
   h->launches++;
   return cuda_err(gemm_launch(B, p, grid, s, h->pdl));
@@ -579,11 +593,8 @@ int draft_impl(dflash_handle* h, const int32_t* slots, int32_t batch, const int3
       a.n_valid = vf.n_valid;
       a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
       a.status = h->status;
-      if (h->trace.kid == DFLASH_KID_ATTENTION && h->trace.buf &&
-          (long long)a.n_splits * hkv * batch <= h->trace.cap) {
-        a.trace = h->trace.buf;  // one launch only
-        h->trace.kid = 0;
-      }
+      if (unsigned long long* tb = h->trace.take(DFLASH_KID_ATTENTION, (long long)a.n_splits * hkv * batch))
+        a.trace = tb;
       ProbeScope ps(h, DFLASH_KID_ATTENTION, s);
       h->launches++;
       rc = cuda_err(attn_launch(a, batch, s, h->pdl, h->attn_tc));
@@ -650,6 +661,8 @@ int draft_impl(dflash_handle* h, const int32_t* slots, int32_t batch, const int3
     p.temp_inv = smp.temp_inv;
     p.seed = smp.seed;
     p.round = smp.round;
+    p.slots = h->slots_ok;  // a target's draws are keyed by slot and position
+    p.bctx = h->bctx;
     p.done_ctr = h->done_ctr;
     const void* a = h->embed_pk;
     fp8_weights(h, p, h->embed_sc);
@@ -913,6 +926,21 @@ int dflash_verify_block(dflash_handle* h, const int32_t* slots, int32_t batch, c
   return draft_impl(h, slots, batch, nullptr, out_tok, nullptr, nullptr, stream, nullptr, 0, nullptr, Sampling(), vf);
 }
 
+int dflash_verify_block_sample(dflash_handle* h, const int32_t* slots, int32_t batch, const int32_t* tokens,
+                               const int32_t* n_valid, float temperature, uint64_t seed, int32_t* out_tok, void* feats,
+                               void* stream) {
+  if (!h || h->cfg.role != 1 || !tokens || !out_tok) return DFLASH_ERR_INVALID_ARG;
+  if (!(temperature == temperature) || temperature < 0.f) return DFLASH_ERR_INVALID_ARG;
+  Verify vf;
+  vf.tokens = tokens;
+  vf.n_valid = n_valid;
+  vf.feats = static_cast<bf16*>(feats);
+  Sampling smp;
+  smp.temp_inv = temperature >= 1e-6f ? 1.f / temperature : 0.f;  // below: the draw is the argmax
+  smp.seed = seed;
+  return draft_impl(h, slots, batch, nullptr, out_tok, nullptr, nullptr, stream, nullptr, 0, nullptr, smp, vf);
+}
+
 int dflash_advance(dflash_handle* h, const int32_t* slots, int32_t batch, const int32_t* n, void* stream) {
   if (!h || batch < 0 || batch > h->cfg.max_batch) return DFLASH_ERR_INVALID_ARG;
   if (batch == 0) return DFLASH_OK;
@@ -1115,6 +1143,7 @@ int dflash_trace_arm(dflash_handle* h, int32_t kernel_id, unsigned long long* bu
   h->trace.kid = kernel_id;
   h->trace.buf = buf;
   h->trace.cap = cap_ctas;
+  h->trace.used = 0;
   return DFLASH_OK;
 }
 
@@ -1130,10 +1159,20 @@ int dflash_harness_verify(dflash_handle* h, const int32_t* slots, int32_t batch,
   if (feat_stream && (!feats_out || stream_rows <= 0)) return DFLASH_ERR_INVALID_ARG;
   if (cudaSetDevice(h->cfg.device) != cudaSuccess) return DFLASH_ERR_CUDA;
   h->launches++;
+  unsigned long long* stamp = nullptr;
+  if (h->stamps && h->stamp_next < h->stamp_cap) stamp = h->stamps + 2 * (size_t)h->stamp_next++;
   return cuda_err(launch_harness_verify(slots, batch, h->cfg.block, draft, match, offs, rounds_cap, round_ctr, target,
                                         h->cfg.vocab, static_cast<const bf16*>(feat_stream), stream_rows,
                                         static_cast<bf16*>(feats_out), h->cfg.n_fused * h->cfg.hidden,
-                                        h->ctx_len, h->cfg.max_slots, (cudaStream_t)stream));
+                                        h->ctx_len, h->cfg.max_slots, stamp, h->done_ctr + 8, (cudaStream_t)stream));
+}
+
+int dflash_stamps_arm(dflash_handle* h, unsigned long long* buf, int32_t n) {
+  if (!h || n < 0 || (n > 0 && !buf)) return DFLASH_ERR_INVALID_ARG;
+  h->stamps = n > 0 ? buf : nullptr;
+  h->stamp_cap = n;
+  h->stamp_next = 0;
+  return DFLASH_OK;
 }
 
 }  // extern "C"
@@ -1146,8 +1185,8 @@ int dflash_harness_verify(dflash_handle* h, const int32_t* slots, int32_t batch,
 // squares, and the split-K partial sums and tile counters of the two GEMMs.
 // Limits: batch * rows_per_req <= 64 rows; the GEMMs run on at most 16 CTAs.
 // Size: 16*2*256*128*4 (partials) + 64*8192*2 (rows) + 64*64*4 (sums) +
-// 4096*4 (counters) bytes, about 5.1 MB, held by every device that loads the
-// library until the process exits.
+// 2*4096*4 (counters) bytes, about 5.1 MB, held by every device that loads
+// the library until the process exits.
 namespace {
 constexpr int NA_MAX_ROWS = 64;
 constexpr int NA_MAX_CTAS = 16;
@@ -1155,7 +1194,7 @@ constexpr size_t NA_PART_BYTES = (size_t)NA_MAX_CTAS * 2 * DFL_BN_MAX * 128 * si
 constexpr size_t NA_ROWS_BYTES = (size_t)NA_MAX_ROWS * 8192 * sizeof(f16);
 constexpr size_t NA_SS_BYTES = (size_t)(8192 / 128) * NA_MAX_ROWS * sizeof(float);
 constexpr int NA_MAX_TILES = 4096;
-constexpr size_t NA_CTR_BYTES = (size_t)NA_MAX_TILES * sizeof(unsigned);
+constexpr size_t NA_CTR_BYTES = 2 * (size_t)NA_MAX_TILES * sizeof(unsigned);  // arrivals, finalisers done
 constexpr size_t NA_BYTES = NA_PART_BYTES + NA_ROWS_BYTES + NA_SS_BYTES + NA_CTR_BYTES;
 }  // namespace
 
@@ -1208,6 +1247,7 @@ int noalloc_gemm(dflash_handle* h, cudaStream_t s, int mode, const void* const* 
   p.status = h->status;
   p.ws = part;
   p.tile_ctr = ctr;
+  p.tile_fin = ctr + NA_MAX_TILES;
   p.eps = h->cfg.rms_eps;
   p.H = h->cfg.hidden;
   p.hq = h->cfg.n_q_heads;

@@ -43,6 +43,35 @@ DFL_DEV void atrace(const AttnParams& p, int ev) {
   }
 }
 
+#ifndef DFL_ATTN_L2_PF  // 1: a CTA's K/V pages are prefetched into L2 before the dependency wait
+#define DFL_ATTN_L2_PF 0
+#endif
+
+// This CTA's K and V page blocks into L2, issued before the wait on the
+// previous kernel (the QKV projection) -- the context pages were written in
+// earlier rounds.  The slot, length and page ids read here may still be a
+// previous round's (the kernels that update them need not have finished):
+// a prefetch of another page only costs bandwidth, every address is checked
+// to lie inside the pool, and L2 stays coherent with later writes.
+DFL_DEV void attn_l2_prefetch(const AttnParams& p, int b, int split, int kvh, int D) {
+  const int slot = p.slots[b];
+  int npages = (p.ctx_len[slot] + p.block + 63) >> 6;
+  if (npages > p.kv.max_pages_per_slot) npages = p.kv.max_pages_per_slot;
+  if (npages <= 0) return;
+  const int pb = (int)((long long)split * npages / p.n_splits);
+  const int pe = (int)((long long)(split + 1) * npages / p.n_splits);
+  const int* pt = p.kv.page_table + (size_t)slot * p.kv.max_pages_per_slot;
+  const f16* kb = p.kv.k_pool + (size_t)p.layer * p.kv.layer_stride;
+  const f16* vb = p.kv.v_pool + (size_t)p.layer * p.kv.layer_stride;
+  for (int pi = pb; pi < pe; ++pi) {
+    const int pg = pt[pi];
+    if (pg < 0 || pg >= p.kv.max_pages) continue;
+    const size_t off = ((size_t)pg * p.kv.hkv + kvh) * (64 * D);
+    prefetch_l2_bulk(kb + off, (uint32_t)(64 * D * 2));
+    prefetch_l2_bulk(vb + off, (uint32_t)(64 * D * 2));
+  }
+}
+
 // A split's partial (nf floats from shared memory) to its global slot.
 DFL_DEV void copy_partial(const AttnParams& p, const float* part, int nf, int slot, int D) {
   float* dst = p.part + (size_t)slot * attn_part_floats(D);
@@ -129,6 +158,7 @@ __global__ void __launch_bounds__(G * KS * 32) k_attn(const AttnParams p) {
     atrace(p, 0);
     for (int s = 0; s < C::STAGES; ++s) mbar_init(full + s, 1);
     fence_mbar_init();
+    if (DFL_ATTN_L2_PF) attn_l2_prefetch(p, b, split, kvh, D);
   }
   pdl_launch_dependents();
   pdl_wait();
@@ -533,6 +563,7 @@ __global__ void __launch_bounds__(320, 1) k_attn_tc(const AttnParams p) {
     mbar_init(q_full, 256);
     mbar_init(mdone, 1);
     fence_mbar_init();
+    if (DFL_ATTN_L2_PF) attn_l2_prefetch(p, b, split, kvh, D);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::TMEM_COLS);

@@ -44,6 +44,9 @@
 #ifndef DFL_GEMM_A_CHUNKS  // bulk copies per 16 KB weight block
 #define DFL_GEMM_A_CHUNKS 1
 #endif
+#ifndef DFL_GEMM_L2_PF  // weight blocks past the ring prefetched into L2 while the previous kernel drains
+#define DFL_GEMM_L2_PF 0
+#endif
 
 namespace {
 
@@ -91,12 +94,40 @@ DFL_DEV unsigned long long draft_stream_key(unsigned long long seed, int b, int 
   k = sm64_mix(k + SM64_GOLD * (unsigned long long)(rnd + 1));
   return sm64_mix(k + SM64_GOLD * (unsigned long long)(row + 1));
 }
+// The target's draws at temperature > 0 (its verify step): the stream of
+// (seed, purpose 2 = target, request slot, position of the block row), so a
+// position's numbers do not depend on the block or round it falls in.
+DFL_DEV unsigned long long target_stream_key(unsigned long long seed, int slot, int pos) {
+  unsigned long long k = sm64_mix(seed + SM64_GOLD);
+  k = sm64_mix(k + SM64_GOLD * 3ull);  // purpose id 2
+  k = sm64_mix(k + SM64_GOLD * (unsigned long long)(slot + 1));
+  return sm64_mix(k + SM64_GOLD * (unsigned long long)(pos + 1));
+}
 // Out of line: the greedy epilogue, run once per vocabulary tile, keeps its
 // compact code (the instruction cache holds it across tiles).
 __device__ __noinline__ float gumbel_at(unsigned long long key, int v) {
   const unsigned long long bits = sm64_mix(key + SM64_GOLD * (unsigned long long)(v + 1));
   const float u = ((float)(unsigned)(bits >> 41) + 0.5f) * 1.1920928955078125e-7f;  // 2^-23
   return -logf(-logf(u));
+}
+
+// Wait (bounded) until the tile counter at `addr` reaches `target`: the
+// acquire load makes every arriver's part visible.  False after DFL_WAIT_NS
+// (DFLASH_DEV_TIMEOUT set).
+DFL_DEV bool wait_count(const unsigned* addr, unsigned target, uint32_t* status) {
+  uint64_t t0 = 0;
+  while (true) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
+    if (v >= target) return true;
+    const uint64_t t = globaltimer();
+    if (t0 == 0) {
+      t0 = t;
+    } else if (t - t0 > DFL_WAIT_NS) {
+      dev_error(status, DFLASH_DEV_TIMEOUT);
+      return false;
+    }
+  }
 }
 
 // Timeline stamps (p.trace non-null): 0 entry, 1 set-up done, 2 first weight
@@ -325,7 +356,7 @@ DFL_DEV void gather_ctx(const GemmParams& p, int t_first, int j0, int ntok, int 
 template <int MODE>
 DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, const float* stg, int ew, int lane,
                        bool use_pre, const TokCtx& pre0, const TokCtx& pre1, const float* gq, const float* gk,
-                       bool use_hpre, const float (&hpre)[EPI_TOK][4], int rnd) {
+                       bool use_hpre, const float (&hpre)[EPI_TOK][4], const float (&gpre)[4], int rnd) {
   const int tt_all = tile / p.t_tiles;       // (group, n-tile)
   const int group = tt_all / p.n_tiles;
   const int nt = tt_all % p.n_tiles;
@@ -360,10 +391,10 @@ DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, con
           hv[q][jj] = (MODE == GM_RESID && ok[q])
                           ? (hp ? hpre[q][jj] : p.h[(size_t)tq[q] * p.N + n0 + lane + 32 * jj])
                           : 0.f;
-      // the gain is read once, before any store (stores to h/out could alias it)
+      // the tile's gains: read when the tile started (one token tile), else now
       float gn[4];
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj) gn[jj] = p.gain[n0 + lane + 32 * jj];
+      for (int jj = 0; jj < 4; ++jj) gn[jj] = use_hpre ? gpre[jj] : p.gain[n0 + lane + 32 * jj];
       float sq[EPI_TOK];
 #pragma unroll
       for (int q = 0; q < EPI_TOK; ++q) {
@@ -393,8 +424,9 @@ DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, con
     // per-token inputs: gathered at kernel start for the first 16 tokens of a
     // single token tile, otherwise now
     TokCtx ctx;
-    if (use_pre && t_first == 0 && j0 - ew < 32)
-      ctx = j0 == ew ? pre0 : pre1;
+    const int jg = t_first + j0 - ew;  // this token group's offset in the tile (0, 16, 32, ...)
+    if (use_pre && jg < 32)
+      ctx = jg == 0 ? pre0 : pre1;
     else
       gather_ctx<MODE>(p, t_first, j0, ntok, lane, ctx);
     const TokCtx* tc = &ctx;
@@ -416,16 +448,21 @@ DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, con
       const int n0 = nt * 128;
       unsigned long long best[EPI_TOK];
       if (DFL_GEMM_SAMPLING && p.temp_inv > 0.f) {
-        // temperature > 0: each drafting row draws from softmax(logit / T) by
-        // the Gumbel-max rule, on its own stream (a separate loop, so the
-        // greedy one below keeps its compact code)
+        // temperature > 0: each drafting row (or, for a target's verify,
+        // every row) draws from softmax(logit / T) by the Gumbel-max rule, on
+        // its own stream (a separate loop, so the greedy one below keeps its
+        // compact code)
         const float tinv = p.temp_inv;
+        const bool tgt = p.row0 == 0;
 #pragma unroll
         for (int q = 0; q < EPI_TOK; ++q) {
           best[q] = 0ull;
           const int row = tq[q] % DFL_BLOCK;
-          const bool smp = row >= 1 && row < p.block;
-          const unsigned long long skey = smp ? draft_stream_key(p.seed, tq[q] / DFL_BLOCK, rnd, row) : 0ull;
+          const bool smp = ok[q] && (tgt || (row >= 1 && row < p.block));
+          unsigned long long skey = 0ull;
+          if (smp)
+            skey = tgt ? target_stream_key(p.seed, p.slots[tq[q] / DFL_BLOCK], p.bctx[tq[q]].x)
+                       : draft_stream_key(p.seed, tq[q] / DFL_BLOCK, rnd, row);
 #pragma unroll
           for (int jj = 0; jj < 4; ++jj) {
             const int n = n0 + lane + 32 * jj;
@@ -668,6 +705,27 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
         ptt[i] = tt;
         advance();
       }
+      if (DFL_GEMM_L2_PF > 0) {
+        // the weight blocks that follow the ring's first fill, into L2, while
+        // the previous kernel still runs (weights do not depend on it): the
+        // main loop then reads them at L2 speed
+        int t2 = tile, k2 = kb;
+        const uint8_t* ap = a_ptr;
+        const int end = n_units < pre + DFL_GEMM_L2_PF ? n_units : pre + DFL_GEMM_L2_PF;
+        for (int i = pre; i < end; ++i) {
+          prefetch_l2_bulk(ap, (uint32_t)blk_bytes);
+          if (++k2 == KBi) {
+            k2 = 0;
+            ++t2;
+            const int rest = t2 / p.t_tiles;
+            int nt = (rest % p.n_tg) * CL + crank;
+            if (nt >= p.n_tiles) nt = p.n_tiles - 1;
+            ap = static_cast<const uint8_t*>(p.a[rest / p.n_tg]) + (size_t)(p.a_tile_off + nt) * KBi * blk_bytes;
+          } else {
+            ap += blk_bytes;
+          }
+        }
+      }
       pdl_wait();
       for (int i = 0; i < pre; ++i) load_b(i, pkb[i], ptt[i]);
       int st = pre == stages ? 0 : pre;
@@ -823,16 +881,18 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
       const int tile = tile_of(p, tile_s, crank);
       // RESID, one token tile: this tile's residual inputs for the first 16
       // tokens, loaded while the accumulators and the split reduction finish
-      float hpre[EPI_TOK][4];
-      const bool use_hpre = MODE == GM_RESID && p.t_tiles == 1 && tile >= 0;
+      float hpre[EPI_TOK][4], gpre[4];
+      const bool use_hpre = (MODE == GM_RESID || MODE == GM_FC) && p.t_tiles == 1 && tile >= 0;
       if (use_hpre) {
         const int n0 = (int)(tile % p.n_tiles) * 128;
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) gpre[jj] = p.gain[n0 + lane + 32 * jj];
 #pragma unroll
         for (int q4 = 0; q4 < EPI_TOK; ++q4)
 #pragma unroll
           for (int jj = 0; jj < 4; ++jj) {
             const int j = ew + 4 * q4;
-            hpre[q4][jj] = j < p.M ? p.h[(size_t)j * p.N + n0 + lane + 32 * jj] : 0.f;
+            hpre[q4][jj] = (MODE == GM_RESID && j < p.M) ? p.h[(size_t)j * p.N + n0 + lane + 32 * jj] : 0.f;
           }
       }
       if (!mbar_wait(tfull + abuf, use & 1u, p.status, &aborted)) break;
@@ -852,6 +912,8 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
         c_last = cta_of_unit(tile_s * KB + KB - 1, U, G);
       }
       const bool split = c_first != c_last;
+      const int nsl = (mt + 15) >> 4;  // 16-token slices of the tile
+      int rank = 0, npar = 1, ct = 16;  // finalisers; tokens per chunk a finaliser takes at once
       if (split) {
         const int my_slot = tile_s == first_tile ? 0 : 1;
         float* w = p.ws + (size_t)((c * CL + crank) * 2 + my_slot) * (DFL_BN_MAX * 128);
@@ -865,37 +927,60 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
         tc_fence_before();
         mbar_arrive(tempty + abuf);
         named_bar_sync(1, EPI_THREADS);
+        // One 16-token slice: the last arriver finalises it at once.  More:
+        // the contributors whose unit ranges end in this tile (all but a last
+        // one that goes on to the next tile) share the slices, contributor j
+        // taking slices j, j+npar, ..., each after a bounded wait for the
+        // remaining parts; having no main-loop work left, they hold nothing
+        // another CTA waits for.
+        const unsigned cnt = (unsigned)(c_last - c_first + 1);
+        if (nsl > 1) {
+          const int n_end = (int)cnt - (unit_start(c_last + 1, U, G) > (tile_s + 1) * KB ? 1 : 0);
+          ct = nsl >= 2 * n_end ? 32 : 16;  // two slices per landing batch when each finaliser has several
+          const int nch = (mt + ct - 1) / ct;
+          npar = nch < n_end ? nch : n_end;
+        }
         if (et == 0) {
-          const unsigned cnt = (unsigned)(c_last - c_first + 1);
           const unsigned old = atomic_add_acq_rel(p.tile_ctr + tile, 1u);
-          const int last = old == cnt - 1;
-          if (last) p.tile_ctr[tile] = 0;
-          *flag = last;
+          int go;
+          if (nsl == 1) {
+            go = old == cnt - 1u ? 0 : -1;
+            if (go == 0) p.tile_ctr[tile] = 0;
+          } else {
+            const int j = c - c_first;
+            go = j < npar ? j : -1;
+            if (go >= 0 && old != cnt - 1u && !wait_count(p.tile_ctr + tile, cnt, p.status))
+              go = -2;  // gave up: skip the slices, still sign off
+          }
+          *flag = go;
         }
         named_bar_sync(1, EPI_THREADS);
-        const int last = *flag;
+        rank = *flag;
         named_bar_sync(1, EPI_THREADS);
-        if (!last) continue;
+        if (rank == -1) continue;
+        if (rank == -2) aborted = true;
       }
-      for (int tc0 = 0; tc0 < mt; tc0 += 32) {
-        float v0[16], v1[16];
-        const bool two = tc0 + 16 < BN;  // a second 16-column chunk in this 32-token chunk
-        if (split) {
+      if (split) {
+        // The parts' 16-token chunks land in shared memory by bulk copies
+        // (one issuing thread, one barrier per batch) and are added in k
+        // order by a compact loop -- this code runs cold once per tile.  On
+        // the CTA's last segment every weight stage has been consumed, so
+        // the whole ring takes a batch; otherwise the p.red_items-chunk buffer.
+        // Every part after the first opens its CTA's range (slot 0); the
+        // first part is slot 1 unless the tile also opens c_first's.
+        const int sl_first = unit_start(c_first, U, G) == tile_s * KB ? 0 : 1;
+        const bool ring_free = u == u1;
+        float* land = ring_free ? reinterpret_cast<float*>(sm) : red_buf;
+        const int cap_items = ring_free ? (stages * stage_bytes) / (RED_CHUNK * 4) : p.red_items;
+        const int nparts = c_last - c_first + 1;
+        const int nch = (mt + ct - 1) / ct;
+        for (int ch = rank; ch < nch && !aborted; ch += npar) {
+          const int tc0 = ch * ct;
+          const int subs = (mt - tc0) > 16 && ct == 32 ? 2 : 1;  // 16-token slices in this chunk
+          float v0[16], v1[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) v0[i] = v1[i] = 0.f;
-          // The parts' 16-column chunks land in shared memory by bulk copies
-          // (one issuing thread, one barrier per batch) and are added in k
-          // order by a compact loop -- this code runs cold once per tile.  On
-          // the CTA's last segment every weight stage has been consumed, so
-          // the whole ring takes a batch; otherwise the p.red_items-chunk buffer.
-          // Every part after the first opens its CTA's range (slot 0); the
-          // first part is slot 1 unless the tile also opens c_first's.
-          const int sl_first = unit_start(c_first, U, G) == tile_s * KB ? 0 : 1;
-          const bool ring_free = u == u1;
-          float* land = ring_free ? reinterpret_cast<float*>(sm) : red_buf;
-          const int cap_items = ring_free ? (stages * stage_bytes) / (RED_CHUNK * 4) : p.red_items;
-          const int nparts = c_last - c_first + 1;
-          const int nitems = nparts * (two ? 2 : 1);  // (sub, part), part fastest
+          const int nitems = nparts * subs;  // (sub, part), part fastest
           for (int it0 = 0; it0 < nitems && !aborted; it0 += cap_items) {
             const int nb = (nitems - it0) < cap_items ? (nitems - it0) : cap_items;
             if (et == 0) {
@@ -908,7 +993,7 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
                 const int cc = c_first + item - sub * nparts;
                 const int sl = cc == c_first ? sl_first : 0;
                 bulk_load(land + k * RED_CHUNK,
-                          p.ws + (size_t)((cc * CL + crank) * 2 + sl) * (DFL_BN_MAX * 128) + (tc0 + 16 * sub) * 128,
+                          p.ws + (size_t)((cc * CL + crank) * 2 + sl) * (DFL_BN_MAX * 128) + (size_t)(tc0 + 16 * sub) * 128,
                           RED_CHUNK * 4, red);
               }
             }
@@ -927,20 +1012,41 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
             }
             named_bar_sync(1, EPI_THREADS);  // landing area free for the next batch
           }
-        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) stg[i * 128 + r] = v0[i];
+          if (subs == 2) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) stg[(16 + i) * 128 + r] = v1[i];
+          }
+          named_bar_sync(1, EPI_THREADS);
+          epi_final<MODE>(p, (int)tile, t_base + tc0, (mt - tc0) < ct ? (mt - tc0) : ct, stg, ew, lane, use_pre,
+                          pre0, pre1, gq, gk, use_hpre, hpre, gpre, rnd);
+          named_bar_sync(1, EPI_THREADS);
+        }
+        // several slices: the last finaliser to finish clears the tile's counters
+        if (nsl > 1 && et == 0) {
+          if (atomicAdd(p.tile_fin + tile, 1u) == (unsigned)(npar - 1)) {
+            p.tile_ctr[tile] = 0;
+            p.tile_fin[tile] = 0;
+          }
+        }
+      } else {
+        for (int tc0 = 0; tc0 < mt; tc0 += 32) {
+          float v0[16], v1[16];
+          const bool two = tc0 + 16 < BN;  // a second 16-column chunk in this 32-token chunk
           tmem_ld16(taddr + (uint32_t)tc0, v0);
           if (two) tmem_ld16(taddr + (uint32_t)(tc0 + 16), v1);
-        }
 #pragma unroll
-        for (int i = 0; i < 16; ++i) stg[i * 128 + r] = v0[i];
-        if (two) {
+          for (int i = 0; i < 16; ++i) stg[i * 128 + r] = v0[i];
+          if (two) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) stg[(16 + i) * 128 + r] = v1[i];
+            for (int i = 0; i < 16; ++i) stg[(16 + i) * 128 + r] = v1[i];
+          }
+          named_bar_sync(1, EPI_THREADS);
+          epi_final<MODE>(p, (int)tile, t_base + tc0, (mt - tc0) < 32 ? (mt - tc0) : 32, stg, ew, lane, use_pre,
+                          pre0, pre1, gq, gk, use_hpre, hpre, gpre, rnd);
+          named_bar_sync(1, EPI_THREADS);
         }
-        named_bar_sync(1, EPI_THREADS);
-        epi_final<MODE>(p, (int)tile, t_base + tc0, (mt - tc0) < 32 ? (mt - tc0) : 32, stg, ew, lane, use_pre,
-                        pre0, pre1, gq, gk, use_hpre, hpre, rnd);
-        named_bar_sync(1, EPI_THREADS);
       }
       if (!split) {
         tc_fence_before();

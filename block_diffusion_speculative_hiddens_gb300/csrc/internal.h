@@ -109,7 +109,8 @@ struct GemmParams {
   unsigned long long* trace;
   // split-K scratch
   float* ws;            // [grid][2][BN_MAX*128]
-  unsigned* tile_ctr;   // [total_tiles]
+  unsigned* tile_ctr;   // [total_tiles] parts arrived (self-resetting)
+  unsigned* tile_fin;   // [total_tiles] finalisers done, when several share a tile (self-resetting)
   uint32_t* status;
 };
 
@@ -204,4 +205,5 @@ cudaError_t launch_tap(const float* h, int M, int H, bf16* feats, int tap, int n
 cudaError_t launch_harness_verify(const int* slots, int batch, int S, const int* draft, const int* match,
                                   const int* offs, int rounds_cap, int* round_ctr, int* target, int vocab,
                                   const bf16* feat_stream, int stream_rows, bf16* feats_out, int F,
-                                  const int* ctx_len, int max_slots, cudaStream_t s);
+                                  const int* ctx_len, int max_slots, unsigned long long* stamp,
+                                  unsigned* blocks_done, cudaStream_t s);

@@ -319,15 +319,10 @@ __global__ void k_slot_lengths(const int* slots, int batch, const int* ctx_len, 
   out[b] = (s >= 0 && s < max_slots) ? ctx_len[s] : -1;
 }
 
-// Benchmark stand-in for the target's verify (not part of the method).
-// Block 0 builds the target tokens of round (*round_ctr)++; blocks 1.. copy
-// the target features of the S block positions from a position-indexed stream.
-__global__ void k_harness_verify(const int* slots, int batch, int S, const int* draft, const int* match, const int* offs,
-                                 int rounds_cap, int* round_ctr, int* target, int vocab,
-                                 const bf16* feat_stream, int stream_rows, bf16* feats_out, int F,
-                                 const int* ctx_len, int max_slots) {
-  pdl_launch_dependents();
-  pdl_wait();
+// The stand-in verify's work (see k_harness_verify).
+DFL_DEV void verify_body(const int* slots, int batch, int S, const int* draft, const int* match, const int* offs,
+                         int rounds_cap, int* round_ctr, int* target, int vocab, const bf16* feat_stream,
+                         int stream_rows, bf16* feats_out, int F, const int* ctx_len, int max_slots) {
   if (blockIdx.x == 0) {
     const int r = *round_ctr;
     const int rr = r % rounds_cap;
@@ -357,6 +352,34 @@ __global__ void k_harness_verify(const int* slots, int batch, int S, const int* 
   const uint4* src = reinterpret_cast<const uint4*>(feat_stream + ((size_t)b * stream_rows + pos) * F);
   uint4* dst = reinterpret_cast<uint4*>(feats_out + (size_t)row * F);
   for (int k = threadIdx.x; k < F / 8; k += blockDim.x) dst[k] = src[k];
+}
+
+// Benchmark stand-in for the target's verify (not part of the method).
+// Block 0 builds the target tokens of round (*round_ctr)++; blocks 1.. copy
+// the target features of the S block positions from a position-indexed stream.
+// With `stamp` non-null, stamp[0] receives %globaltimer when the kernel may
+// start its work (the drafter's last kernel complete) and stamp[1] when its
+// last block is done (counted on blocks_done, left at zero).
+__global__ void k_harness_verify(const int* slots, int batch, int S, const int* draft, const int* match, const int* offs,
+                                 int rounds_cap, int* round_ctr, int* target, int vocab,
+                                 const bf16* feat_stream, int stream_rows, bf16* feats_out, int F,
+                                 const int* ctx_len, int max_slots, unsigned long long* stamp,
+                                 unsigned* blocks_done) {
+  pdl_launch_dependents();
+  pdl_wait();
+  if (stamp && blockIdx.x == 0 && threadIdx.x == 0) stamp[0] = globaltimer();
+  verify_body(slots, batch, S, draft, match, offs, rounds_cap, round_ctr, target, vocab, feat_stream, stream_rows,
+              feats_out, F, ctx_len, max_slots);
+  if (stamp) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      __threadfence();
+      if (atomicAdd(blocks_done, 1u) == gridDim.x - 1) {
+        stamp[1] = globaltimer();
+        *blocks_done = 0u;
+      }
+    }
+  }
 }
 
 // Failure-detection check: thread 0 waits on an mbarrier nothing arrives at,
@@ -490,10 +513,10 @@ cudaError_t launch_slot_lengths(const int* slots, int batch, const int* ctx_len,
 cudaError_t launch_harness_verify(const int* slots, int batch, int S, const int* draft, const int* match,
                                   const int* offs, int rounds_cap, int* round_ctr, int* target, int vocab,
                                   const bf16* feat_stream, int stream_rows, bf16* feats_out, int F, const int* ctx_len,
-                                  int max_slots, cudaStream_t s) {
+                                  int max_slots, unsigned long long* stamp, unsigned* blocks_done, cudaStream_t s) {
   cudaLaunchAttribute a[1];
   const int blocks = 1 + (feat_stream ? batch * S : 0);
   cudaLaunchConfig_t c = cfg_of(dim3(blocks), dim3(256), s, a);
   return cudaLaunchKernelEx(&c, k_harness_verify, slots, batch, S, draft, match, offs, rounds_cap, round_ctr, target,
-                            vocab, feat_stream, stream_rows, feats_out, F, ctx_len, max_slots);
+                            vocab, feat_stream, stream_rows, feats_out, F, ctx_len, max_slots, stamp, blocks_done);
 }

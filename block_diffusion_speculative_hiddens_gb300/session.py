@@ -105,15 +105,19 @@ def run_round(state: RoundState, verify, stream=None, folded: bool = False):
 
 
 class SpecDecoder:
-    """Greedy speculative generation for one request with a drafter handle and
-    a target handle (role 1) of the same shape family: prefill both models in
+    """Speculative generation for one request with a drafter handle and a
+    target handle (role 1) of the same shape family: prefill both models in
     16-token chunks, then rounds of draft -> verify -> accept -> trim
     (dflash_draft_block, dflash_verify_block, dflash_accept_trim,
     dflash_advance, dflash_fuse_inject).  The output equals the target's own
-    greedy decoding.  `draft_override(out, b0)` may supply the drafts instead
-    of the drafter (tests that force long acceptances)."""
+    greedy decoding, or at temperature > 0 (drafts drawn from the drafter's
+    softmax, the target's tokens sampled by position with
+    dflash_verify_block_sample) the target's own sampled decoding for the same
+    seed.  `draft_override(out, b0)` may supply the drafts instead of the
+    drafter (tests that force long acceptances)."""
 
-    def __init__(self, drafter: Drafter, target: Drafter, slot: int = 0, stream=None):
+    def __init__(self, drafter: Drafter, target: Drafter, slot: int = 0, stream=None, temperature: float = 0.0,
+                 seed: int = 0):
         cfg = drafter.cfg
         dev = torch.device(f"cuda:{drafter.device}")
         i32 = dict(dtype=torch.int32, device=dev)
@@ -128,7 +132,16 @@ class SpecDecoder:
         self.accept_len = torch.zeros(1, **i32)
         self.bonus = torch.zeros(1, **i32)
         self.ctx = torch.zeros(1, **i32)
+        self.rnd = torch.zeros(1, **i32)  # the drafter's round index (its draws' stream)
+        self.temperature, self.seed = float(temperature), int(seed)
         self.taus = []
+
+    def _verify(self, n_valid=None):
+        if self.temperature > 0:
+            self.t.verify_block_sample(self.slots, self.tokens, self.out_tok, self.temperature, self.seed, n_valid,
+                                       self.feats, self.stream)
+        else:
+            self.t.verify_block(self.slots, self.tokens, self.out_tok, n_valid, self.feats, self.stream)
 
     def prefill(self, prompt) -> int:
         """Both models over the prompt; returns the target's greedy token after it."""
@@ -141,7 +154,7 @@ class SpecDecoder:
             self.tokens.zero_()
             self.tokens[0, :n] = torch.tensor(chunk, dtype=torch.int32)
             self.n_valid.fill_(n)
-            self.t.verify_block(self.slots, self.tokens, self.out_tok, self.n_valid, self.feats, s)
+            self._verify(self.n_valid)
             self.d.fuse_inject(self.slots, self.feats, 16, self.n_valid, s)
             self.t.advance(self.slots, self.n_valid, s)
         return int(self.out_tok[0, n - 1].item())
@@ -152,13 +165,17 @@ class SpecDecoder:
         out = [b0]
         self.bonus.fill_(b0)
         while len(out) < n_new:
-            if draft_override is None:
-                self.d.draft_block(self.slots, self.bonus, self.draft, s)
-            else:
+            if draft_override is not None:
                 self.draft.copy_(torch.as_tensor(draft_override(out, b0), dtype=torch.int32).view(1, -1))
+            elif self.temperature > 0:
+                self.rnd.fill_(len(self.taus))
+                self.d.draft_block_sample(self.slots, self.bonus, self.temperature, self.seed, self.rnd, self.draft,
+                                          None, s)
+            else:
+                self.d.draft_block(self.slots, self.bonus, self.draft, s)
             self.tokens[:, 0] = self.bonus
             self.tokens[:, 1:self.S] = self.draft
-            self.t.verify_block(self.slots, self.tokens, self.out_tok, None, self.feats, s)
+            self._verify()
             self.d.accept_trim(self.slots, self.draft, self.out_tok[:, :self.S].contiguous(), self.accept_len,
                                self.bonus, self.ctx, s)
             self.t.advance(self.slots, self.accept_len, s)
@@ -172,9 +189,11 @@ class SpecDecoder:
         return out[:n_new]
 
 
-def greedy_generate(target: Drafter, prompt, n_new: int, slot: int = 0, stream=None):
-    """The target's own greedy decoding through dflash_verify_block with one
-    live row per step (the reference speculative generation must equal)."""
+def greedy_generate(target: Drafter, prompt, n_new: int, slot: int = 0, stream=None, temperature: float = 0.0,
+                    seed: int = 0):
+    """The target's own decoding through dflash_verify_block with one live
+    row per step (what speculative generation must equal): greedy, or at
+    temperature > 0 sampled by position (dflash_verify_block_sample)."""
     dev = torch.device(f"cuda:{target.device}")
     i32 = dict(dtype=torch.int32, device=dev)
     slots = torch.tensor([slot], **i32)
@@ -182,6 +201,12 @@ def greedy_generate(target: Drafter, prompt, n_new: int, slot: int = 0, stream=N
     out_tok = torch.zeros(1, 16, **i32)
     n_valid = torch.zeros(1, **i32)
     prompt = [int(x) for x in prompt]
+
+    def verify(sl, tk, ot, nv):
+        if temperature > 0:
+            target.verify_block_sample(sl, tk, ot, temperature, seed, nv, None, stream)
+        else:
+            target.verify_block(sl, tk, ot, nv, None, stream)
     n = 0
     for p0 in range(0, len(prompt), 16):
         chunk = prompt[p0:p0 + 16]
@@ -189,14 +214,14 @@ def greedy_generate(target: Drafter, prompt, n_new: int, slot: int = 0, stream=N
         tokens.zero_()
         tokens[0, :n] = torch.tensor(chunk, dtype=torch.int32)
         n_valid.fill_(n)
-        target.verify_block(slots, tokens, out_tok, n_valid, None, stream)
+        verify(slots, tokens, out_tok, n_valid)
         target.advance(slots, n_valid, stream)
     g = int(out_tok[0, n - 1].item())
     out = [g]
     n_valid.fill_(1)
     while len(out) < n_new:
         tokens[0, 0] = g
-        target.verify_block(slots, tokens, out_tok, n_valid, None, stream)
+        verify(slots, tokens, out_tok, n_valid)
         target.advance(slots, n_valid, stream)
         g = int(out_tok[0, 0].item())
         out.append(g)

@@ -307,6 +307,22 @@ DFLASH_API int dflash_verify_block(dflash_handle* h, const int32_t* slots, int32
 DFLASH_API int dflash_advance(dflash_handle* h, const int32_t* slots, int32_t batch, const int32_t* n,
                               void* stream);
 
+/* dflash_verify_block at temperature T > 0: the target samples its own token
+ * at every block position ("DFlash原理深度剖析…", §三 第3步: the block is
+ * checked against the target's sampled tokens; "DFlash：drafter 的答案…",
+ * Results: sampling at T = 1).  Row i of request b (position
+ * p = ctx_len + i of slot s = slots[b]) outputs argmax_v(logit_v / T + g_v),
+ * g_v = -ln(-ln u_v), u_v from the SplitMix64 stream (seed, 2, s, p) built as
+ * for dflash_draft_block_sample.  Keyed by position, a position's draw is the
+ * same whichever block or round it falls in, so speculative decoding with
+ * dflash_accept_trim emits exactly the target's own sampled decoding (one
+ * live row per call) for the same seed.  temperature < 1e-6 (or 0) is the
+ * argmax; negative or NaN is DFLASH_ERR_INVALID_ARG; otherwise as
+ * dflash_verify_block. */
+DFLASH_API int dflash_verify_block_sample(dflash_handle* h, const int32_t* slots, int32_t batch,
+                                          const int32_t* tokens, const int32_t* n_valid, float temperature,
+                                          uint64_t seed, int32_t* out_tok, void* feats, void* stream);
+
 /* a3-a6 at temperature T > 0 ([Paper walkthrough] Results and [News summary]
  * 用例与示例 report DFlash with sampling; [Code walkthrough] §三 第3步: the
  * block is checked against the target's sampled tokens with the same
@@ -339,6 +355,7 @@ DFLASH_API int dflash_draft_block_sample(dflash_handle* h, const int32_t* slots,
 #define DFLASH_KID_WO 6
 #define DFLASH_KID_FC 7
 #define DFLASH_KID_INJECT 8
+#define DFLASH_KID_ALL 255 /* dflash_trace_arm only: every GEMM and attention launch */
 DFLASH_API int dflash_probe_arm(dflash_handle* h, int32_t kernel_id, int32_t n);
 DFLASH_API int dflash_probe_read(dflash_handle* h, float* ms_out, int32_t cap, int32_t* n_out);
 
@@ -356,7 +373,9 @@ DFLASH_API int dflash_marks_read(dflash_handle* h, float* ms_out, int32_t cap, i
 
 /* Device timeline of one launch: the next launch of kernel `kernel_id`
  * (DFLASH_KID_*) writes, per CTA, 8 uint64 values into the DEVICE buffer
- * buf[cap_ctas][8].  GEMMs: %globaltimer (ns) at entry, end of set-up, first
+ * buf[cap_ctas][8]; with DFLASH_KID_ALL every following GEMM and attention
+ * launch takes the next rows (its grid's CTAs, in launch order) until the
+ * buffer is full.  GEMMs: %globaltimer (ns) at entry, end of set-up, first
  * weight stage landed, last MMA issued, epilogue done and exit, then the
  * CTA's unit count and its SM id.  Attention (CTAs in split-fastest order):
  * entry, context length known, first page landed, pages done, partial
@@ -386,6 +405,15 @@ DFLASH_API int dflash_plan(dflash_handle* h, int32_t* out5);
  * and, when feat_stream is non-null, copies the target features of the S
  * block positions ctx_len .. ctx_len+S-1 from feat_stream
  * [batch, stream_rows, n_fused*H] into feats_out [batch, S, n_fused*H]. */
+/* Device timestamps of the stand-in verify (measurement only): after
+ * dflash_stamps_arm(h, buf, n), the next n dflash_harness_verify calls
+ * enqueued (or captured) write %globaltimer (ns) into the DEVICE buffer
+ * buf[2i] when call i may start its work (the kernels before it are
+ * complete) and buf[2i+1] when its last block is done.  n = 0 disarms.
+ * The drafter's time in a replayed round loop is then the time outside these
+ * windows, with no event-record node in the graph. */
+DFLASH_API int dflash_stamps_arm(dflash_handle* h, unsigned long long* buf, int32_t n);
+
 DFLASH_API int dflash_harness_verify(dflash_handle* h, const int32_t* slots, int32_t batch,
                           const int32_t* draft, const int32_t* match, const int32_t* offs,
                           int32_t rounds_cap, int32_t* round_ctr, int32_t* target,

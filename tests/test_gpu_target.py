@@ -104,6 +104,65 @@ def test_speculative_generation_is_the_greedy_output(lib, mode):
     assert t.read_status() == 0 and d.read_status() == 0
 
 
+@pytest.mark.parametrize("mode", ["drafter", "perfect", "corrupt"])
+def test_sampled_speculative_generation_is_the_targets_sampled_output(lib, mode):
+    """At temperature 1 (drafts drawn from the drafter's softmax, the target's
+    tokens sampled by position with dflash_verify_block_sample) the
+    speculative output equals the target's own sampled decoding for the same
+    seed and slot: on the GPU token by token, and against the oracle's
+    sampled tokens up to its first near-tie of the perturbed scores."""
+    from block_diffusion_speculative_hiddens_gb300.session import SpecDecoder, greedy_generate
+    cfg = get_config("tiny-gains")
+    t, d, tm, _ = _handles(cfg)
+    prompt = prompt_tokens(cfg, 1, 40)
+    n_new, temp, seed = 48, 1.0, 99
+    gs = greedy_generate(t, prompt, n_new, slot=1, temperature=temp, seed=seed)
+    t.reset_slot(1)
+    gg = greedy_generate(t, prompt, n_new, slot=1)
+    t.reset_slot(1)
+    assert gs != gg  # the draws are not the argmax
+    os_, om = T.greedy_generate(T.OracleTarget(tm, NL, 256), prompt, n_new, temp, seed, slot=1)
+    k = _first_weak(om, MARGIN / temp)
+    assert k > 0 and gs[:k] == os_[:k].tolist()
+    override = None
+    if mode != "drafter":
+        def override(out, b0, _g=gs):
+            kk = len(out)
+            dd = [_g[kk + i] if kk + i < len(_g) else 0 for i in range(cfg.block - 1)]
+            if mode == "corrupt":
+                j = (kk * 5) % (cfg.block - 1)
+                dd[j] = (dd[j] + 1) % (cfg.vocab - 1)
+            return dd
+    sd = SpecDecoder(d, t, slot=1, temperature=temp, seed=seed)
+    got = sd.generate(prompt, n_new, override)
+    assert got == gs, (got, gs, sd.taus)
+    if mode == "perfect":
+        assert all(x == cfg.block for x in sd.taus[:-1])
+    if mode == "corrupt":
+        assert max(sd.taus) > 1
+    assert t.read_status() == 0 and d.read_status() == 0
+
+
+def test_verify_sample_temperature_edges(lib):
+    """T below 1e-6 is the argmax; a negative or NaN T is refused."""
+    import torch
+    from block_diffusion_speculative_hiddens_gb300.binding import DflashError
+    cfg = get_config("tiny-gains")
+    t, _, _, _ = _handles(cfg)
+    dev = torch.device("cuda:0")
+    i32 = dict(dtype=torch.int32, device=dev)
+    slots = torch.tensor([0], **i32)
+    tokens = torch.tensor([prompt_tokens(cfg, 2, 16).tolist()], **i32)
+    a, b = torch.zeros(1, 16, **i32), torch.zeros(1, 16, **i32)
+    t.verify_block(slots, tokens, a)
+    t.verify_block_sample(slots, tokens, b, 1e-9, 5)
+    assert np.array_equal(to_np(a), to_np(b))
+    for bad in (-1.0, float("nan")):
+        with pytest.raises(DflashError):
+            t.verify_block_sample(slots, tokens, b, bad, 5)
+    assert t.read_status() == 0
+
+
 def test_verify_block_batch_of_two_with_ragged_chunks(lib):
     """Two requests verified together, their last chunks of different lengths
     (37 and 33 prompt tokens): every request matches its own oracle."""
