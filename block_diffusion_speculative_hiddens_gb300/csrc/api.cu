@@ -132,6 +132,14 @@ struct dflash_handle {
   CUtensorMap tm_hgx;  // hg plus the fused-feature rows below it
   int bm_rows = -1;
   CUtensorMap tm_cg;
+  // round injections of more rows than one token tile: the appended rows
+  // gathered densely (compact), their source rows and count
+  bf16* cstage = nullptr;  // [max_batch * 16][n_fused * H]
+  int* row_map = nullptr;  // [max_batch * 16]
+  int* row_off = nullptr;  // [max_batch]
+  int* n_live = nullptr;   // [1]
+  int bm_cstage = -1;
+  CUtensorMap tm_cstage;
   // workspace
   uint32_t* status;
   int *ctx_len, *pos0, *n_pages, *page_table, *free_stack, *free_top, *n_eff;
@@ -216,6 +224,9 @@ int pick_attn_splits(const dflash_config& c, int num_sms) {
 // the splits' partials are then merged by a second kernel.
 #ifndef DFL_ATTN_GLOBAL
 #define DFL_ATTN_GLOBAL 1
+#endif
+#ifndef DFL_ATTN_GLOBAL_MIN_PAGES  // pages per split (at full slot capacity) from which splits merge through memory
+#define DFL_ATTN_GLOBAL_MIN_PAGES 32
 #endif
 #ifndef DFL_ATTN_BATCH_SPLITS  // splits per (request, KV head) when the pairs alone fill the SMs
 #define DFL_ATTN_BATCH_SPLITS 1
@@ -304,6 +315,15 @@ size_t carve(dflash_handle* h, const dflash_config& c, char* base, int num_sms) 
     o->attn_part = gs > 1 ? w.take<float>((size_t)c.max_batch * hkv * gs * attn_part_floats(D)) : nullptr;
   }
   o->tile_ctr = w.take<unsigned>(2 * (size_t)tiles);  // arrivals, then finalisers done
+  if (M > DFL_BN_MAX && c.role == 0) {  // a round's injection can span several token tiles: compaction buffers
+    o->cstage = w.take<bf16>((size_t)M * c.n_fused * H);
+    o->row_map = w.take<int>(M);
+    o->row_off = w.take<int>(c.max_batch);
+    o->n_live = w.take<int>(1);
+  } else {
+    o->cstage = nullptr;
+    o->row_map = o->row_off = o->n_live = nullptr;
+  }
   if (h) {
     h->attn_splits = splits;
     h->max_tiles = tiles;
@@ -788,7 +808,7 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
   // outweigh the shorter page loops)
   if (!rc && h->attn_part) {
     const int gs = global_attn_splits(c, sms);
-    if (gs > h->attn_splits && ceil_div(c.max_pages_per_slot, gs) >= 32) {
+    if (gs > h->attn_splits && ceil_div(c.max_pages_per_slot, gs) >= DFL_ATTN_GLOBAL_MIN_PAGES) {
       h->attn_global = true;
       h->attn_splits = gs;
       h->attn_tc = c.attn_impl == 2 || (c.attn_impl == 0 && ceil_div(c.max_pages_per_slot, gs) >= 8);
@@ -839,6 +859,10 @@ int dflash_fuse_inject(dflash_handle* h, const int32_t* slots, int32_t batch, co
   const dflash_config& c = h->cfg;
   const int H = c.hidden, D = c.head_dim, hkv = c.n_kv_heads;
   const int R = batch * rows_per_req;
+  // A round's injection over more rows than one token tile holds computes
+  // only the appended rows: they are gathered densely first, and the GEMMs
+  // read their count on the device.
+  const bool compact = R > DFL_BN_MAX && rows_per_req <= DFL_BLOCK && h->cstage;
   // every descriptor is encoded (and the caller's feature rows checked:
   // 16-byte aligned) before anything is queued, so a refused call leaves the
   // slots' lengths and pages untouched
@@ -850,20 +874,33 @@ int dflash_fuse_inject(dflash_handle* h, const int32_t* slots, int32_t batch, co
       if (!make_tmap(&h->tm_cg, h->cg, R, H, BN)) return DFLASH_ERR_CUDA;
       h->bm_rows = R;
     }
+    if (compact && h->bm_cstage != R) {
+      if (!make_tmap(&h->tm_cstage, h->cstage, R, (uint64_t)c.n_fused * H, BN, true)) return DFLASH_ERR_CUDA;
+      h->bm_cstage = R;
+    }
   }
   h->launches++;
   int rc = cuda_err(launch_page_alloc(slots, batch, h->cfg.block, n_new, rows_per_req, h->ctx_len, h->pos0, h->n_pages,
                                       h->page_table, c.max_pages_per_slot, h->free_stack, h->free_top, h->n_eff, h->slots_ok,
-                                      c.max_slots, h->status, s));
+                                      c.max_slots, h->status, s, compact ? h->row_off : nullptr,
+                                      compact ? h->n_live : nullptr));
   if (rc || R == 0) return rc;
+  if (compact) {
+    h->launches++;
+    rc = cuda_err(launch_compact_rows(static_cast<const bf16*>(feats), batch, rows_per_req, c.n_fused * H, h->n_eff,
+                                      h->row_off, h->cstage, h->row_map, s));
+    if (rc) return rc;
+  }
   {  // fusion projection; RMSNorm gain folded in, its scale deferred to the consumer
     GemmParams p = {};
     p.out = h->cg;
     p.gain = h->fc_norm;
     p.ss_out = h->ss_c;
     p.N = H;
+    if (compact) p.m_dyn = h->n_live;
     const void* a = h->fc_pk;
-    rc = run_gemm(h, s, GM_FC, &a, 1, 0, H / 128, c.n_fused * H, tm_feats, R, p, true, 1, DFLASH_KID_FC);
+    rc = run_gemm(h, s, GM_FC, &a, 1, 0, H / 128, c.n_fused * H, compact ? h->tm_cstage : tm_feats, R, p, true, 1,
+                  DFLASH_KID_FC);
     if (rc) return rc;
   }
   {  // every layer's K/V projection of the fused feature, k-norm, RoPE, paged append
@@ -877,6 +914,10 @@ int dflash_fuse_inject(dflash_handle* h, const int32_t* slots, int32_t batch, co
     p.pos0 = h->pos0;
     p.n_eff = h->n_eff;
     p.rows_per_req = rows_per_req;
+    if (compact) {
+      p.m_dyn = h->n_live;
+      p.row_map = h->row_map;
+    }
     const void* a[DFL_MAX_LAYERS];
     for (int l = 0; l < c.n_layers; ++l) {
       a[l] = h->wqkv_pk[l];

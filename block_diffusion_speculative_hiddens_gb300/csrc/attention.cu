@@ -46,6 +46,15 @@ DFL_DEV void atrace(const AttnParams& p, int ev) {
 #ifndef DFL_ATTN_L2_PF  // 1: a CTA's K/V pages are prefetched into L2 before the dependency wait
 #define DFL_ATTN_L2_PF 0
 #endif
+#ifndef DFL_ATTN_EARLY  // 1: context-only pages are loaded before the wait on the QKV projection
+#define DFL_ATTN_EARLY 0
+#endif
+// With DFL_ATTN_EARLY the QKV projection before this kernel lets it launch
+// only after that projection's own dependency wait, so every earlier kernel
+// (page allocation, injection, embedding) is complete when this one starts:
+// the slot, its length, its page table and its context pages may be read at
+// once.  The block's own K/V and its queries, written by the projection,
+// are read only after this kernel's wait.
 
 // This CTA's K and V page blocks into L2, issued before the wait on the
 // previous kernel (the QKV projection) -- the context pages were written in
@@ -80,61 +89,85 @@ DFL_DEV void copy_partial(const AttnParams& p, const float* part, int nf, int sl
 }
 
 // Combines the splits' partials of each (request, KV head): one CTA per 16
-// rows (one query head's block tokens), 8 threads per row, each taking D/8
-// output columns; max, sum and weight of every split per row, then the
-// weighted sum of the splits' unnormalised outputs in split order.
+// rows (one query head's block tokens), 16 threads per row, each taking D/16
+// output columns.  Every split's max and sum are loaded at once, then the
+// splits' unnormalised outputs in groups of 8 (all loads of a group issued
+// before any is used), and summed in split order.
+constexpr int MERGE_TPR = 16;      // threads per row
+constexpr int MERGE_MAX_SPLITS = 32;
+constexpr int MERGE_GROUP = 8;     // splits whose outputs are loaded at once
+
 template <int D>
-__global__ void __launch_bounds__(128) k_attn_merge(const AttnParams p) {
+__global__ void __launch_bounds__(16 * MERGE_TPR) k_attn_merge(const AttnParams p) {
   constexpr int PS = D + 4;
   constexpr int PF = attn_part_floats(D);
-  constexpr int DC = D / 8;  // columns per thread
+  constexpr int DC = D / MERGE_TPR;  // columns per thread (8 or 4)
+  constexpr int NV = DC / 4;         // float4 per split
   pdl_launch_dependents();
   pdl_wait();
   const int pair = blockIdx.x;
   const int b = pair / p.hkv, kvh = pair % p.hkv;
   const int G = p.hq / p.hkv, rows = G * 16;
-  const int r = blockIdx.y * 16 + ((int)threadIdx.x >> 3);
-  const int d0 = ((int)threadIdx.x & 7) * DC;
+  const int r = blockIdx.y * 16 + ((int)threadIdx.x / MERGE_TPR);
+  const int d0 = ((int)threadIdx.x % MERGE_TPR) * DC;
   if (r >= rows) return;
   const int nsp = p.n_splits;
   const float* base = p.part + (size_t)pair * nsp * PF;
+  float mv[MERGE_MAX_SPLITS], lv[MERGE_MAX_SPLITS];
+#pragma unroll
+  for (int sp = 0; sp < MERGE_MAX_SPLITS; ++sp) {
+    mv[sp] = -INFINITY;
+    lv[sp] = 0.f;
+    if (sp < nsp) {
+      lv[sp] = base[(size_t)sp * PF + rows * PS + rows + r];
+      mv[sp] = base[(size_t)sp * PF + rows * PS + r];
+    }
+  }
   float M = -INFINITY;
-  for (int sp = 0; sp < nsp; ++sp) {
-    const float l = base[(size_t)sp * PF + rows * PS + rows + r];
-    if (l > 0.f) M = fmaxf(M, base[(size_t)sp * PF + rows * PS + r]);
+#pragma unroll
+  for (int sp = 0; sp < MERGE_MAX_SPLITS; ++sp)
+    if (lv[sp] > 0.f) M = fmaxf(M, mv[sp]);
+  float L = 0.f;
+#pragma unroll
+  for (int sp = 0; sp < MERGE_MAX_SPLITS; ++sp) {
+    const float w = lv[sp] > 0.f ? exp2f(mv[sp] - M) : 0.f;
+    mv[sp] = w;  // now the split's weight
+    L += w * lv[sp];
   }
   float acc[DC];
 #pragma unroll
   for (int c = 0; c < DC; ++c) acc[c] = 0.f;
-  float L = 0.f;
-  for (int sp = 0; sp < nsp; ++sp) {
-    const float* sb = base + (size_t)sp * PF;
-    const float l = sb[rows * PS + rows + r];
-    const float w = l > 0.f ? exp2f(sb[rows * PS + r] - M) : 0.f;
-    L += w * l;
 #pragma unroll
-    for (int c = 0; c < DC; c += 4) {
-      const float4 v = *reinterpret_cast<const float4*>(sb + r * PS + d0 + c);
-      acc[c] += w * v.x;
-      acc[c + 1] += w * v.y;
-      acc[c + 2] += w * v.z;
-      acc[c + 3] += w * v.w;
+  for (int g = 0; g < MERGE_MAX_SPLITS; g += MERGE_GROUP) {
+    if (g >= nsp) break;
+    float4 v[MERGE_GROUP][NV];
+#pragma unroll
+    for (int k = 0; k < MERGE_GROUP; ++k)
+#pragma unroll
+      for (int c4 = 0; c4 < NV; ++c4)
+        v[k][c4] = g + k < nsp ? *reinterpret_cast<const float4*>(base + (size_t)(g + k) * PF + r * PS + d0 + 4 * c4)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < MERGE_GROUP; ++k) {
+      const float w = mv[g + k];  // 0 past the last split
+#pragma unroll
+      for (int c4 = 0; c4 < NV; ++c4) {
+        acc[4 * c4] += w * v[k][c4].x;
+        acc[4 * c4 + 1] += w * v[k][c4].y;
+        acc[4 * c4 + 2] += w * v[k][c4].z;
+        acc[4 * c4 + 3] += w * v[k][c4].w;
+      }
     }
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;
   const int h = r / 16, t = r % 16;
   f16* dst = p.out + ((size_t)(b * DFL_BLOCK + t) * p.hq + kvh * G + h) * D + d0;
 #pragma unroll
-  for (int c = 0; c < DC; c += 8)
-    *reinterpret_cast<uint4*>(dst + c) =
-        make_uint4(pack_f16x2(acc[c] * inv, acc[c + 1] * inv), pack_f16x2(acc[c + 2] * inv, acc[c + 3] * inv),
-                   pack_f16x2(acc[c + 4] * inv, acc[c + 5] * inv), pack_f16x2(acc[c + 6] * inv, acc[c + 7] * inv));
+  for (int c = 0; c < DC; c += 4)
+    *reinterpret_cast<uint2*>(dst + c) =
+        make_uint2(pack_f16x2(acc[c] * inv, acc[c + 1] * inv), pack_f16x2(acc[c + 2] * inv, acc[c + 3] * inv));
 }
 
-// KS warps per query head split every page's 64 keys between them (KS = 2
-// for G <= 4), each with its own online softmax, merged in shared memory at
-// the end: twice the warps in flight and half the dependent MMA chain per
-// page for the common GQA group sizes.
 template <int D, int G, int KS>
 __global__ void __launch_bounds__(G * KS * 32) k_attn(const AttnParams p) {
   using C = AttnCfg<D>;
@@ -161,7 +194,7 @@ __global__ void __launch_bounds__(G * KS * 32) k_attn(const AttnParams p) {
     if (DFL_ATTN_L2_PF) attn_l2_prefetch(p, b, split, kvh, D);
   }
   pdl_launch_dependents();
-  pdl_wait();
+  if (!DFL_ATTN_EARLY) pdl_wait();
 
   const int slot = p.slots[b];
   const int nv = p.n_valid ? min(max(p.n_valid[b], 1), DFL_BLOCK) : p.block;  // live block rows
@@ -169,6 +202,7 @@ __global__ void __launch_bounds__(G * KS * 32) k_attn(const AttnParams p) {
   const int npages = (nkeys + 63) >> 6;
   const int pb = (int)((long long)split * npages / p.n_splits);  // balanced page ranges
   const int pe = (int)((long long)(split + 1) * npages / p.n_splits);
+  const int ctx_pages = (nkeys - nv) >> 6;            // pages holding no block row
   // keys of rows g and g+8: all, or (causal) the context and block rows up to
   // the row itself (padding rows: up to the last live row)
   const int lim0 = p.causal ? nkeys - nv + min(g, nv - 1) + 1 : nkeys;
@@ -196,8 +230,13 @@ __global__ void __launch_bounds__(G * KS * 32) k_attn(const AttnParams p) {
     bulk_load(dst + C::BLK_BYTES, vbase + off, C::BLK_BYTES, full + s);
   };
   int issued = 0;  // meaningful in thread 0 only
+  if (DFL_ATTN_EARLY) {
+    if (threadIdx.x == 0)  // context pages first, then (after the wait) the block's
+      for (; issued < C::STAGES && pb + issued < pe && pb + issued < ctx_pages; ++issued) issue(issued, pb + issued);
+    pdl_wait();
+  }
   if (threadIdx.x == 0)
-    for (int i = 0; i < C::STAGES && pb + i < pe; ++i, ++issued) issue(i, pb + i);
+    for (; issued < C::STAGES && pb + issued < pe; ++issued) issue(issued, pb + issued);
 
   // Q fragments of this warp's query head (16 block rows x D) in registers.
   const int j = head0 + hw;
@@ -574,11 +613,12 @@ __global__ void __launch_bounds__(320, 1) k_attn_tc(const AttnParams p) {
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   pdl_launch_dependents();
-  pdl_wait();
+  if (!DFL_ATTN_EARLY) pdl_wait();
 
   const int slot = p.slots[b];
   const int nv = p.n_valid ? min(max(p.n_valid[b], 1), DFL_BLOCK) : p.block;  // live block rows
   const int nkeys = p.ctx_len[slot] + nv;             // context + live block rows
+  const int ctx_pages = (nkeys - nv) >> 6;            // pages holding no block row
   const int npages = (nkeys + 63) >> 6;
   const int pb = (int)((long long)split * npages / p.n_splits);  // balanced page ranges
   const int pe = (int)((long long)(split + 1) * npages / p.n_splits);
@@ -609,9 +649,14 @@ __global__ void __launch_bounds__(320, 1) k_attn_tc(const AttnParams p) {
         return (pg < 0 || pg >= p.kv.max_pages) ? -1 : pg;
       };
       int i = 0;
+      bool waited = !DFL_ATTN_EARLY;
       for (; i < n; ++i) {
         const int s = i % C::STAGES;
         if (i >= C::STAGES && !mbar_wait(empty + s, (uint32_t)((i / C::STAGES - 1) & 1), p.status, &aborted)) break;
+        if (!waited && pb + i >= ctx_pages) {  // the block's pages: written by the QKV projection
+          pdl_wait();
+          waited = true;
+        }
         int pg = page_of_idx(i);
         if (pg < 0) {
           dev_error(p.status, DFLASH_DEV_PAGE);
@@ -692,6 +737,7 @@ __global__ void __launch_bounds__(320, 1) k_attn_tc(const AttnParams p) {
         }
       }
     };
+    if (DFL_ATTN_EARLY) pdl_wait();  // the queries come from the QKV projection
     {  // this row's query (half of its chunks per thread), zero-padded to 128 rows
       const int h = r >> 4, t = r & 15;
       const f16* src = p.q + ((size_t)(b * DFL_BLOCK + t) * hq + kvh * G + h) * D;
@@ -947,7 +993,7 @@ cudaError_t launch_t(const AttnParams& p, int batch, cudaStream_t s, bool pdl) {
   if (e || !p.merge_global || p.n_splits == 1) return e;
   cudaLaunchConfig_t mc = {};
   mc.gridDim = dim3((unsigned)(batch * p.hkv), (unsigned)G);  // 16 rows per CTA
-  mc.blockDim = dim3(128);
+  mc.blockDim = dim3(16 * MERGE_TPR);
   mc.stream = s;
   mc.attrs = attr + na - (pdl ? 1 : 0);
   mc.numAttrs = pdl ? 1 : 0;

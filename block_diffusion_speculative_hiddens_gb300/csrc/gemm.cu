@@ -47,6 +47,12 @@
 #ifndef DFL_GEMM_L2_PF  // weight blocks past the ring prefetched into L2 while the previous kernel drains
 #define DFL_GEMM_L2_PF 0
 #endif
+#ifndef DFL_GEMM_WARM  // 1: the epilogue warps run the fused epilogue once, storing nothing, during the main loop
+#define DFL_GEMM_WARM 0
+#endif
+#ifndef DFL_ATTN_EARLY  // 1: the QKV GEMM lets its dependent (the attention) launch only after its own dependency wait
+#define DFL_ATTN_EARLY 0
+#endif
 
 namespace {
 
@@ -70,10 +76,12 @@ DFL_DEV int cta_of_unit(int u, int U, int G) { return ((u + 1) * G + U - 1) / U 
 // -> the tile this CTA computes, or -1 for a rank past its group's last
 // n-tile (it streams a copy of the last weight tile and finalises nothing).
 // With cl = 1 the two numberings coincide.
-DFL_DEV int tile_of(const GemmParams& p, int ct, int cr) {
-  const int rest = ct / p.t_tiles;
+// tl: token tiles scheduled (p.t_tiles, or fewer for a launch whose live
+// token rows are counted on the device); tile ids keep the p.t_tiles layout.
+DFL_DEV int tile_of(const GemmParams& p, int ct, int cr, int tl) {
+  const int rest = ct / tl;
   const int nt = (rest % p.n_tg) * p.cl + cr;
-  return nt < p.n_tiles ? ((rest / p.n_tg) * p.n_tiles + nt) * p.t_tiles + ct % p.t_tiles : -1;
+  return nt < p.n_tiles ? ((rest / p.n_tg) * p.n_tiles + nt) * p.t_tiles + ct % tl : -1;
 }
 
 // Counter-based random numbers for drafting at temperature > 0: SplitMix64
@@ -273,7 +281,8 @@ DFL_DEV void gather_ctx(const GemmParams& p, int t_first, int j0, int ntok, int 
     for (int q = 0; q < EPI_TOK; ++q) {
       const bool in = ok[q] && c.inj[q];
       any_inj |= in;
-      const int tl = MODE == GM_QKV ? tq[q] - p.inj_m0 : tq[q];
+      int tl = MODE == GM_QKV ? tq[q] - p.inj_m0 : tq[q];
+      if (MODE == GM_INJECT && p.row_map) tl = p.row_map[tl];  // a compacted row: its request and row
       const int b = tl / p.rows_per_req;
       ii[q] = tl % p.rows_per_req;
       slot[q] = in ? p.slots[b] : 0;
@@ -356,7 +365,8 @@ DFL_DEV void gather_ctx(const GemmParams& p, int t_first, int j0, int ntok, int 
 template <int MODE>
 DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, const float* stg, int ew, int lane,
                        bool use_pre, const TokCtx& pre0, const TokCtx& pre1, const float* gq, const float* gk,
-                       bool use_hpre, const float (&hpre)[EPI_TOK][4], const float (&gpre)[4], int rnd) {
+                       bool use_hpre, const float (&hpre)[EPI_TOK][4], const float (&gpre)[4], int rnd,
+                       bool dry = false) {
   const int tt_all = tile / p.t_tiles;       // (group, n-tile)
   const int group = tt_all / p.n_tiles;
   const int nt = tt_all % p.n_tiles;
@@ -411,7 +421,7 @@ DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, con
         for (int q = 0; q < EPI_TOK; ++q) sq[q] += __shfl_xor_sync(0xffffffffu, sq[q], o);
 #pragma unroll
       for (int q = 0; q < EPI_TOK; ++q) {
-        if (!ok[q]) continue;
+        if (!ok[q] || dry) continue;
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
           const size_t o = (size_t)tq[q] * p.N + n0 + lane + 32 * jj;
@@ -436,7 +446,7 @@ DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, con
       const int f0 = nt * 64;
 #pragma unroll
       for (int q = 0; q < EPI_TOK; ++q) {
-        if (!ok[q]) continue;
+        if (!ok[q] || dry) continue;
 #pragma unroll
         for (int jj = 0; jj < 2; ++jj) {
           const float g = x[q][jj] * s[q], u = x[q][jj + 2] * s[q];
@@ -469,10 +479,10 @@ DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, con
             if (ok[q] && n < p.N) {
               const float v = x[q][jj] * s[q];
               if (v != v) {
-                dev_error(p.status, DFLASH_DEV_NAN);
+                if (!dry) dev_error(p.status, DFLASH_DEV_NAN);
                 continue;
               }
-              if (p.logits) p.logits[(size_t)tq[q] * p.N + n] = v;
+              if (p.logits && !dry) p.logits[(size_t)tq[q] * p.N + n] = v;
               const float sc = smp ? v * tinv + gumbel_at(skey, n) : v;
               const unsigned long long k = argmax_key(sc, (uint32_t)n);
               best[q] = k > best[q] ? k : best[q];
@@ -489,10 +499,10 @@ DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, con
             if (ok[q] && n < p.N) {
               const float v = x[q][jj] * s[q];
               if (v != v) {
-                dev_error(p.status, DFLASH_DEV_NAN);
+                if (!dry) dev_error(p.status, DFLASH_DEV_NAN);
                 continue;
               }
-              if (p.logits) p.logits[(size_t)tq[q] * p.N + n] = v;
+              if (p.logits && !dry) p.logits[(size_t)tq[q] * p.N + n] = v;
               const unsigned long long k = argmax_key(v, (uint32_t)n);
               best[q] = k > best[q] ? k : best[q];
             }
@@ -508,7 +518,7 @@ DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, con
         }
 #pragma unroll
       for (int q = 0; q < EPI_TOK; ++q)
-        if (ok[q] && lane == 0 && best[q]) atomicMax(p.keys + tq[q], best[q]);
+        if (ok[q] && lane == 0 && best[q] && !dry) atomicMax(p.keys + tq[q], best[q]);
     } else if (MODE == GM_QKV || MODE == GM_INJECT) {
       const int D = p.D;
       int n0, kind, layer;
@@ -538,7 +548,7 @@ DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, con
       if (kind < 2) head_norm_rope4(x, g, c0, c1, D, p.eps);
 #pragma unroll
       for (int q = 0; q < EPI_TOK; ++q) {
-        if (!live[q]) continue;  // warp-uniform
+        if (!live[q] || dry) continue;  // warp-uniform
         if (kind == 0 && inj[q]) continue;  // fused-feature rows only append K/V
         const float* xv = x[q];
         if (kind == 0) {
@@ -619,8 +629,22 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
   // cluster peers write into this CTA's stages and signal its barriers
   if (p.cl > 1) cluster_sync_all();
   const uint32_t tmem = *tmem_slot;
-  pdl_launch_dependents();
+  // The QKV projection's dependent, the block attention, reads the page
+  // tables and context pages before its own wait: it may launch only once
+  // this grid's wait has returned, i.e. once every kernel before it is done.
+  if (!(DFL_ATTN_EARLY && MODE == GM_QKV)) pdl_launch_dependents();
   if (threadIdx.x == 0) trace_at(p, 1, globaltimer());
+  // Token rows of this launch: p.M, or the device count p.m_dyn (the live
+  // rows of a compacted injection), read after the wait on the kernel that
+  // writes it; only the token tiles holding them are scheduled.
+  int Mx = p.M, tl = p.t_tiles;
+  if (p.m_dyn) {
+    pdl_wait();
+    const int m = *p.m_dyn;
+    Mx = m < 0 ? 0 : (m > p.M ? p.M : m);
+    tl = (Mx + BN - 1) / BN;
+  }
+  const int total_ct = p.groups * p.n_tg * tl;
 
   // Units (scheduled tile, k-block) are divided over the clusters; the CTAs
   // of a cluster run the same units in lockstep, each on its own n-tile.
@@ -628,16 +652,24 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
   const int CL = p.cl;
   const int crank = CL > 1 ? (int)cluster_ctarank() : 0;
   const uint16_t cmask = (uint16_t)((1u << CL) - 1u);
-  const int G = gridDim.x / CL, c = blockIdx.x / CL;
-  int U, u0, u1;
-  if (p.allow_split) {
-    U = p.total_ctiles * KB;
-    u0 = unit_start(c, U, G);
-    u1 = unit_start(c + 1, U, G);
-  } else {
-    U = p.total_ctiles * KB;
-    u0 = unit_start(c, p.total_ctiles, G) * KB;
-    u1 = unit_start(c + 1, p.total_ctiles, G) * KB;
+  // Clusters taking part: the grid holds at most one per unit (tile without
+  // split) for the launch's rows; with fewer live rows than it was sized
+  // for, the clusters past the units present sit out, so every
+  // participating cluster has work (split tiles count on every cluster from
+  // the first to the last of their units).
+  const int c = blockIdx.x / CL;
+  int G = gridDim.x / CL;
+  const int units_avail = p.allow_split ? total_ct * KB : total_ct;
+  if (G > units_avail) G = units_avail;
+  int U = total_ct * KB, u0 = 0, u1 = 0;
+  if (c < G) {
+    if (p.allow_split) {
+      u0 = unit_start(c, U, G);
+      u1 = unit_start(c + 1, U, G);
+    } else {
+      u0 = unit_start(c, total_ct, G) * KB;
+      u1 = unit_start(c + 1, total_ct, G) * KB;
+    }
   }
   bool aborted = false;
 
@@ -655,11 +687,11 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
       const uint8_t* a_ptr = nullptr;
       const int blk_bytes = p.a_fp8 ? DFL_WBLK8_BYTES : A_STAGE_BYTES;
       auto tile_base = [&]() {  // `tile` counts scheduled tiles here
-        const int rest = tile / p.t_tiles;
+        const int rest = tile / tl;
         const int g = rest / p.n_tg;
         int nt = (rest % p.n_tg) * CL + crank;
         if (nt >= p.n_tiles) nt = p.n_tiles - 1;
-        tt = tile % p.t_tiles;
+        tt = tile % tl;
         a_ptr = static_cast<const uint8_t*>(p.a[g]) + ((size_t)(p.a_tile_off + nt) * KBi + kb) * blk_bytes;
       };
       tile_base();
@@ -717,7 +749,7 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
           if (++k2 == KBi) {
             k2 = 0;
             ++t2;
-            const int rest = t2 / p.t_tiles;
+            const int rest = t2 / tl;
             int nt = (rest % p.n_tg) * CL + crank;
             if (nt >= p.n_tiles) nt = p.n_tiles - 1;
             ap = static_cast<const uint8_t*>(p.a[rest / p.n_tg]) + (size_t)(p.a_tile_off + nt) * KBi * blk_bytes;
@@ -848,6 +880,7 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
   } else {
     // ------------------------------------------------ epilogue (warps 2..5)
     pdl_wait();
+    if (DFL_ATTN_EARLY && MODE == GM_QKV) pdl_launch_dependents();
     const int q = warp & 3;
     const int r = q * 32 + lane;  // TMEM lane = tile row
     const int et = threadIdx.x - 64;
@@ -869,6 +902,21 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
         pre1 = pre0;
       use_pre = true;
     }
+    if (DFL_GEMM_WARM && u0 < u1) {
+      // The fused epilogue's code runs once here, on zeroed staging and
+      // storing nothing, while the main loop streams: the tile finalisation
+      // at the end of the launch then runs from a warm instruction cache.
+      const int tile0 = tile_of(p, u0 / KB, crank, tl);
+      const int tb0 = tile0 >= 0 ? (int)(tile0 % p.t_tiles) * BN : 0;
+      const int nw = (Mx - tb0) < 16 ? (Mx - tb0) : 16;
+      if (tile0 >= 0 && nw > 0) {
+        for (int i = et; i < 32 * 128; i += EPI_THREADS) stg[i] = 0.f;
+        named_bar_sync(1, EPI_THREADS);
+        float hz[EPI_TOK][4] = {}, gz[4] = {};
+        epi_final<MODE>(p, tile0, tb0, nw, stg, ew, lane, use_pre, pre0, pre1, gq, gk, false, hz, gz, rnd, true);
+        named_bar_sync(1, EPI_THREADS);
+      }
+    }
     int seg = 0;
     const int first_tile = u0 / KB;  // this CTA's first segment's scheduled tile
     uint32_t red_phase = 0;
@@ -878,7 +926,7 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
       u = seg_end;
       const int abuf = seg & 1;
       const uint32_t use = (uint32_t)(seg >> 1);
-      const int tile = tile_of(p, tile_s, crank);
+      const int tile = tile_of(p, tile_s, crank, tl);
       // RESID, one token tile: this tile's residual inputs for the first 16
       // tokens, loaded while the accumulators and the split reduction finish
       float hpre[EPI_TOK][4], gpre[4];
@@ -905,7 +953,7 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(abuf * BN);
       const int tt = (int)(tile % p.t_tiles);
       const int t_base = tt * BN;
-      const int mt = (p.M - t_base) < BN ? (p.M - t_base) : BN;
+      const int mt = (Mx - t_base) < BN ? (Mx - t_base) : BN;
       int c_first = c, c_last = c;
       if (p.allow_split) {
         c_first = cta_of_unit(tile_s * KB, U, G);

@@ -64,6 +64,8 @@ struct GemmParams {
   const float* a_scale[DFL_MAX_LAYERS];  // a_fp8: per packed row scale [tiles * 128] per group
   int a_tile_off;   // first packed tile of the range (inject: hq*D/128)
   int mode;
+  const int* m_dyn;     // non-null: the launch computes the first *m_dyn (<= M) token rows (device count)
+  const int* row_map;   // INJECT over compacted rows: row j's source row b * rows_per_req + i
   // shapes for epilogues
   int H;            // hidden (norm width for ss partial consumers)
   int hq, hkv, D;
@@ -185,8 +187,12 @@ cudaError_t launch_embed(const int* slots, int batch, const int* last_tok, int m
 cudaError_t launch_page_alloc(const int* slots, int batch, int S, const int* n_new, int rows_per_req, int* ctx_len,
                               int* pos0, int* n_pages, int* page_table, int max_pages_per_slot,
                               int* free_stack, int* free_top, int* n_eff, int* slots_ok, int max_slots,
-                              uint32_t* status,
-                              cudaStream_t s);
+                              uint32_t* status, cudaStream_t s, int* row_off = nullptr, int* n_live = nullptr);
+// The appended feature rows of a round gathered densely: request b's first
+// n_eff[b] rows of feats [batch][rows_per_req][F] to rows row_off[b].. of
+// dst [*, F], row_map[j] = source row of dst row j.
+cudaError_t launch_compact_rows(const bf16* feats, int batch, int rows_per_req, int F, const int* n_eff,
+                                const int* row_off, bf16* dst, int* row_map, cudaStream_t s);
 cudaError_t launch_accept(const int* slots, int batch, int S, const int* draft, const int* target, int* accept_len,
                           int* bonus, int* ctx_out, int* ctx_len, int max_slots, uint32_t* status,
                           cudaStream_t s);

@@ -183,13 +183,18 @@ __global__ void k_embed(const int* __restrict__ slots, const int* __restrict__ l
 // the page assignment is deterministic).  Grows each slot's page table to
 // cover ctx_len + n_new + block positions, records the first new position
 // (pos0, per request) and the effective row count, and advances ctx_len.
+// With row_off non-null it also gives each request's first row among the
+// appended rows of all requests (row_off[b]) and their total (*n_live), for
+// an injection over the appended rows alone.
 __global__ void k_page_alloc(const int* slots, int batch, int S, const int* n_new, int rows_per_req, int* ctx_len,
                              int* pos0, int* n_pages, int* page_table, int mpps, int* free_stack, int* free_top,
-                             int* n_eff, int* slots_ok, int max_slots, uint32_t* status) {
+                             int* n_eff, int* slots_ok, int max_slots, uint32_t* status, int* row_off,
+                             int* n_live) {
   pdl_launch_dependents();
   pdl_wait();
   if (threadIdx.x != 0) return;
   int top = *free_top;
+  int live = 0;
   for (int b = 0; b < batch; ++b) {
     const int slot = slots[b];
     if (slot < 0 || slot >= max_slots) {
@@ -197,6 +202,7 @@ __global__ void k_page_alloc(const int* slots, int batch, int S, const int* n_ne
       n_eff[b] = 0;
       pos0[b] = 0;
       slots_ok[b] = 0;  // in bounds for the later kernels; no row of it is live
+      if (row_off) row_off[b] = live;
       continue;
     }
     slots_ok[b] = slot;
@@ -226,8 +232,26 @@ __global__ void k_page_alloc(const int* slots, int batch, int S, const int* n_ne
     pos0[b] = L;
     ctx_len[slot] = L + n;
     n_eff[b] = n;
+    if (row_off) row_off[b] = live;
+    live += n;
   }
   *free_top = top;
+  if (n_live) *n_live = live;
+}
+
+// One block per (row i, request b): the row is copied when it is appended.
+__global__ void k_compact_rows(const bf16* __restrict__ feats, int rows_per_req, int F, const int* n_eff,
+                               const int* row_off, bf16* __restrict__ dst, int* row_map) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int i = blockIdx.x, b = blockIdx.y;
+  if (i >= n_eff[b]) return;
+  const int j = row_off[b] + i;
+  const int src_row = b * rows_per_req + i;
+  if (threadIdx.x == 0) row_map[j] = src_row;
+  const uint4* s = reinterpret_cast<const uint4*>(feats + (size_t)src_row * F);
+  uint4* d = reinterpret_cast<uint4*>(dst + (size_t)j * F);
+  for (int k = threadIdx.x; k < F / 8; k += blockDim.x) d[k] = s[k];
 }
 
 // a7: one warp per request.  Lane i compares draft d_{i+1} with target t_i;
@@ -462,11 +486,20 @@ cudaError_t launch_embed(const int* slots, int batch, const int* last_tok, int m
 
 cudaError_t launch_page_alloc(const int* slots, int batch, int S, const int* n_new, int rows_per_req, int* ctx_len,
                               int* pos0, int* n_pages, int* page_table, int mpps, int* free_stack, int* free_top,
-                              int* n_eff, int* slots_ok, int max_slots, uint32_t* status, cudaStream_t s) {
+                              int* n_eff, int* slots_ok, int max_slots, uint32_t* status, cudaStream_t s,
+                              int* row_off, int* n_live) {
   cudaLaunchAttribute a[1];
   cudaLaunchConfig_t c = cfg_of(dim3(1), dim3(32), s, a);
   return cudaLaunchKernelEx(&c, k_page_alloc, slots, batch, S, n_new, rows_per_req, ctx_len, pos0, n_pages,
-                            page_table, mpps, free_stack, free_top, n_eff, slots_ok, max_slots, status);
+                            page_table, mpps, free_stack, free_top, n_eff, slots_ok, max_slots, status, row_off,
+                            n_live);
+}
+
+cudaError_t launch_compact_rows(const bf16* feats, int batch, int rows_per_req, int F, const int* n_eff,
+                                const int* row_off, bf16* dst, int* row_map, cudaStream_t s) {
+  cudaLaunchAttribute a[1];
+  cudaLaunchConfig_t c = cfg_of(dim3((unsigned)rows_per_req, (unsigned)batch), dim3(256), s, a);
+  return cudaLaunchKernelEx(&c, k_compact_rows, feats, rows_per_req, F, n_eff, row_off, dst, row_map);
 }
 
 cudaError_t launch_accept(const int* slots, int batch, int S, const int* draft, const int* target, int* accept_len,

@@ -510,3 +510,30 @@ def test_create_refuses_weights_beyond_f16(lib):
     assert e.value.code == 7
     d = Drafter(cfg, w, weight_fp8=1, **kw)
     assert d.read_status() == 0
+
+
+def test_batch32_rounds_inject_only_the_appended_rows(lib):
+    """Batch 32: a round's injection covers 512 feature rows, more than one
+    token tile, so the library gathers the appended rows (each request's
+    accept_len first rows) and the fusion and injection GEMMs compute those
+    alone.  Acceptance bit-exact over three rounds, hidden states and logits
+    against the oracle, and afterwards every request's cache equal to the
+    oracle's context K/V."""
+    cfg, g, o = _pair("small-b32", 3)
+    for r in range(3):
+        go = g.round(debug=True)
+        oo = o.round(want_logits=True)
+        for j, od in enumerate(oo):
+            assert rel_l2(go["hidden"][j], od["hidden"]) < TOL_REL_L2, (r, j)
+            assert rel_l2(go["logits"][j, 1:], od["logits"]) < TOL_REL_L2, (r, j)
+            check_drafts(go["draft"][j], od)
+            assert (go["tau"][j], go["bonus"][j], go["ctx"][j]) == (od["tau"], od["bonus"], od["ctx"]), (r, j)
+    assert len(set(int(t) for t in go["tau"])) > 3  # ragged acceptance: the gather matters
+    lens = to_np(g.d.slot_lengths(g.state.slots))
+    for j in range(len(g.ids)):
+        L = int(lens[j])
+        for l in range(cfg.n_layers):
+            k, v = g.d.read_kv(l, j, 0, L)
+            ok, ov = o.reqs[j].ctx(l)
+            assert rel_l2(to_np(k), ok[:L]) < TOL_REL_L2 and rel_l2(to_np(v), ov[:L]) < TOL_REL_L2, (j, l)
+    assert g.d.read_status() == 0

@@ -129,6 +129,12 @@ TEST_CONFIGS = {
         intermediate=768, n_layers=2, vocab=5000, rope_theta=5e5, batch=3, ctx0=None,
         rounds=4, match_p=None, ctx_range=(30, 300), p_range=(0.5, 0.95), gain_std=0.1,
         weight_std=0.05, block=10),
+    # Batch 32: a round appends up to 512 feature rows, more than one token
+    # tile, so the injection gathers the appended rows and computes only them.
+    "small-b32": DraftConfig(
+        name="small-b32", hidden=512, n_q_heads=8, n_kv_heads=2, head_dim=128, intermediate=768,
+        n_layers=2, vocab=5000, rope_theta=1e6, batch=32, ctx0=None, rounds=3, match_p=None,
+        ctx_range=(30, 200), p_range=(0.3, 0.95), gain_std=0.1, weight_std=0.05),
     # Attention shapes beyond the workloads': one query head per KV head, and
     # head_dim 64 with 4 and 8 query heads per KV head.
     "small-g1": DraftConfig(
