@@ -611,6 +611,7 @@ int draft_impl(dflash_handle* h, const int32_t* slots, int32_t batch, const int3
       a.block = c.block;
       a.causal = target ? 1 : 0;
       a.n_valid = vf.n_valid;
+      a.early = fold ? 0 : 1;  // a folded QKV projection appends context rows itself
       a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
       a.status = h->status;
       if (unsigned long long* tb = h->trace.take(DFLASH_KID_ATTENTION, (long long)a.n_splits * hkv * batch))

@@ -35,26 +35,26 @@ struct AttnCfg {
 };
 
 // Timeline stamps (p.trace non-null), per CTA in grid order: 0 entry, 1 context
-// length known, 2 first page landed, 3 pages done, 4 partial published, 5 exit.
+// length known, 2 first page landed, 3 pages done, 4 partial published, 5 exit;
+// with the entry, 6 = the launch's CTA count in the high 32 bits (low bits 0).
 DFL_DEV void atrace(const AttnParams& p, int ev) {
   if (p.trace) {
     const size_t cta = ((size_t)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
     p.trace[cta * 8 + ev] = globaltimer();
+    if (ev == 0) p.trace[cta * 8 + 6] = (unsigned long long)gridDim.x * gridDim.y * gridDim.z << 32;
   }
 }
 
 #ifndef DFL_ATTN_L2_PF  // 1: a CTA's K/V pages are prefetched into L2 before the dependency wait
 #define DFL_ATTN_L2_PF 0
 #endif
-#ifndef DFL_ATTN_EARLY  // 1: context-only pages are loaded before the wait on the QKV projection
-#define DFL_ATTN_EARLY 0
-#endif
-// With DFL_ATTN_EARLY the QKV projection before this kernel lets it launch
-// only after that projection's own dependency wait, so every earlier kernel
-// (page allocation, injection, embedding) is complete when this one starts:
-// the slot, its length, its page table and its context pages may be read at
-// once.  The block's own K/V and its queries, written by the projection,
-// are read only after this kernel's wait.
+// The QKV projection before this kernel lets it launch only after that
+// projection's own dependency wait, so every earlier kernel (page
+// allocation, injection, embedding) is complete when this one starts: with
+// p.early the slot, its length, its page table and the pages holding no
+// block row are read at once, and the block's own K/V and its queries,
+// written by the projection, only after this kernel's wait.  A folded round
+// (the projection also appends the new context rows) clears p.early.
 
 // This CTA's K and V page blocks into L2, issued before the wait on the
 // previous kernel (the QKV projection) -- the context pages were written in
@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(G * KS * 32) k_attn(const AttnParams p) {
     if (DFL_ATTN_L2_PF) attn_l2_prefetch(p, b, split, kvh, D);
   }
   pdl_launch_dependents();
-  if (!DFL_ATTN_EARLY) pdl_wait();
+  if (!p.early) pdl_wait();
 
   const int slot = p.slots[b];
   const int nv = p.n_valid ? min(max(p.n_valid[b], 1), DFL_BLOCK) : p.block;  // live block rows
@@ -230,7 +230,7 @@ __global__ void __launch_bounds__(G * KS * 32) k_attn(const AttnParams p) {
     bulk_load(dst + C::BLK_BYTES, vbase + off, C::BLK_BYTES, full + s);
   };
   int issued = 0;  // meaningful in thread 0 only
-  if (DFL_ATTN_EARLY) {
+  if (p.early) {
     if (threadIdx.x == 0)  // context pages first, then (after the wait) the block's
       for (; issued < C::STAGES && pb + issued < pe && pb + issued < ctx_pages; ++issued) issue(issued, pb + issued);
     pdl_wait();
@@ -613,7 +613,7 @@ __global__ void __launch_bounds__(320, 1) k_attn_tc(const AttnParams p) {
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   pdl_launch_dependents();
-  if (!DFL_ATTN_EARLY) pdl_wait();
+  if (!p.early) pdl_wait();
 
   const int slot = p.slots[b];
   const int nv = p.n_valid ? min(max(p.n_valid[b], 1), DFL_BLOCK) : p.block;  // live block rows
@@ -649,7 +649,7 @@ __global__ void __launch_bounds__(320, 1) k_attn_tc(const AttnParams p) {
         return (pg < 0 || pg >= p.kv.max_pages) ? -1 : pg;
       };
       int i = 0;
-      bool waited = !DFL_ATTN_EARLY;
+      bool waited = !p.early;
       for (; i < n; ++i) {
         const int s = i % C::STAGES;
         if (i >= C::STAGES && !mbar_wait(empty + s, (uint32_t)((i / C::STAGES - 1) & 1), p.status, &aborted)) break;
@@ -737,7 +737,7 @@ __global__ void __launch_bounds__(320, 1) k_attn_tc(const AttnParams p) {
         }
       }
     };
-    if (DFL_ATTN_EARLY) pdl_wait();  // the queries come from the QKV projection
+    if (p.early) pdl_wait();  // the queries come from the QKV projection
     {  // this row's query (half of its chunks per thread), zero-padded to 128 rows
       const int h = r >> 4, t = r & 15;
       const f16* src = p.q + ((size_t)(b * DFL_BLOCK + t) * hq + kvh * G + h) * D;

@@ -50,9 +50,7 @@
 #ifndef DFL_GEMM_WARM  // 1: the epilogue warps run the fused epilogue once, storing nothing, during the main loop
 #define DFL_GEMM_WARM 0
 #endif
-#ifndef DFL_ATTN_EARLY  // 1: the QKV GEMM lets its dependent (the attention) launch only after its own dependency wait
-#define DFL_ATTN_EARLY 0
-#endif
+
 
 namespace {
 
@@ -139,7 +137,8 @@ DFL_DEV bool wait_count(const unsigned* addr, unsigned target, uint32_t* status)
 }
 
 // Timeline stamps (p.trace non-null): 0 entry, 1 set-up done, 2 first weight
-// stage landed, 3 last MMA issued, 4 epilogue done, 5 exit, 6 units, 7 SM id.
+// stage landed, 3 last MMA issued, 4 epilogue done, 5 exit, 6 units (low 32
+// bits) and the launch's CTA count (high 32 bits), 7 SM id.
 DFL_DEV void trace_at(const GemmParams& p, int ev, unsigned long long v) {
   if (p.trace) p.trace[(size_t)blockIdx.x * 8 + ev] = v;
 }
@@ -632,7 +631,7 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
   // The QKV projection's dependent, the block attention, reads the page
   // tables and context pages before its own wait: it may launch only once
   // this grid's wait has returned, i.e. once every kernel before it is done.
-  if (!(DFL_ATTN_EARLY && MODE == GM_QKV)) pdl_launch_dependents();
+  if (MODE != GM_QKV) pdl_launch_dependents();
   if (threadIdx.x == 0) trace_at(p, 1, globaltimer());
   // Token rows of this launch: p.M, or the device count p.m_dyn (the live
   // rows of a compacted injection), read after the wait on the kernel that
@@ -829,7 +828,7 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
         tc_commit(tfull + abuf);
       }
       trace_at(p, 3, globaltimer());
-      trace_at(p, 6, (unsigned long long)(u1 - u0));
+      trace_at(p, 6, (unsigned long long)(u1 - u0) | ((unsigned long long)gridDim.x << 32));
       tc_commit(mdone);
       bool drain_abort = false;
       mbar_wait(mdone, 0, p.status, &drain_abort);
@@ -880,7 +879,7 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
   } else {
     // ------------------------------------------------ epilogue (warps 2..5)
     pdl_wait();
-    if (DFL_ATTN_EARLY && MODE == GM_QKV) pdl_launch_dependents();
+    if (MODE == GM_QKV) pdl_launch_dependents();
     const int q = warp & 3;
     const int r = q * 32 + lane;  // TMEM lane = tile row
     const int et = threadIdx.x - 64;

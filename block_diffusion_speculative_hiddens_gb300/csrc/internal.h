@@ -129,6 +129,8 @@ struct AttnParams {
   float* part;         // [batch * hkv][n_splits][attn_part_floats(D)] partials (merge_global)
   int block;           // block size S: keys = context + S (rows S..15 of a request are padding)
   int causal;          // target verify: block row t sees keys < ctx + min(t, n_valid-1) + 1
+  int early;           // 1: the page list and the pages holding no block row are read before the wait on
+                       // the QKV projection (which then wrote no context row: not a folded injection)
   const int* n_valid;  // causal: [batch] live rows (null: block); keys = context + n_valid
   float scale_log2;    // log2(e) / sqrt(D)
   uint32_t* status;
