@@ -47,9 +47,6 @@
 #ifndef DFL_GEMM_L2_PF  // weight blocks past the ring prefetched into L2 while the previous kernel drains
 #define DFL_GEMM_L2_PF 0
 #endif
-#ifndef DFL_GEMM_WARM  // 1: the epilogue warps run the fused epilogue once, storing nothing, during the main loop
-#define DFL_GEMM_WARM 0
-#endif
 
 
 namespace {
@@ -219,153 +216,125 @@ DFL_DEV int page_of(const GemmParams& p, int slot, int pos) {
 }
 
 
-// Per-token epilogue inputs of one warp's EPI_TOK tokens (j0, j0+4, ...):
-// the RMSNorm scale of the GEMM's input and, for QKV/INJECT, whether the row
-// is appended, its position, RoPE (cos, sin) of frequencies lane and lane+32,
-// and the page holding it.  None depends on the accumulators, so a batch-1
-// CTA gathers them once while its main loop streams.
+// Per-token inputs of a token tile, built once per token tile in shared
+// memory by the epilogue warps while the main loop streams (so the tile's
+// finalisation finds them there instead of waiting on dependent global
+// loads): the RMSNorm scale of the GEMM's input and, for QKV/INJECT, the
+// row's position, the page holding it (-1: none, -2: a padding row of a
+// smaller block) and flags (bit 0: the row is written, bit 1: a fused-feature
+// row -- QKV's folded injection rows, every INJECT row).
+struct TokTab {
+  float* s;
+  int* pos;
+  int* pg;
+  int* flag;
+};
+constexpr int TOKTAB_BYTES = DFL_BN_MAX * 16;
+
+template <int MODE>
+DFL_DEV void build_toktab(const GemmParams& p, int t_base, int mt, const TokTab& tb, int et) {
+  for (int j = et; j < mt; j += EPI_THREADS) {
+    const int t = t_base + j;
+    const bool inj = MODE == GM_INJECT || (MODE == GM_QKV && p.inj_m0 > 0 && t >= p.inj_m0);
+    float s = 1.f;
+    if (MODE != GM_RESID && MODE != GM_FC) {  // every partial sum of squares at once (H <= 8192: <= 64 parts)
+      const bool fold = MODE == GM_QKV && inj;
+      const float* src = fold ? p.ss_inj : p.ss_in;
+      const int ld = fold ? p.inj_ld : p.ss_ld;
+      const int row = fold ? t - p.inj_m0 : t;
+      float part[64];
+#pragma unroll
+      for (int i = 0; i < 64; ++i) part[i] = i < p.ss_parts ? src[(size_t)i * ld + row] : 0.f;
+      float acc = 0.f;
+#pragma unroll
+      for (int i = 0; i < 64; ++i) acc += part[i];
+      s = rsqrtf(acc / (float)p.H + p.eps);
+    }
+    int pos = 0, pg = -1, flag = 0;
+    if (MODE == GM_QKV && !inj) {  // block rows: position and page written by the embedding
+      const int2 bc = p.bctx[t];
+      pos = bc.x;
+      pg = bc.y;
+      flag = bc.x < p.max_pos ? 1 : 0;  // out-of-range positions were reported by the embedding
+    } else if (MODE == GM_QKV || MODE == GM_INJECT) {  // fused-feature rows: the request's slot and position
+      int tl = MODE == GM_QKV ? t - p.inj_m0 : t;
+      if (MODE == GM_INJECT && p.row_map) tl = p.row_map[tl];  // a compacted row: its request and row
+      const int b = tl / p.rows_per_req, ii = tl % p.rows_per_req;
+      const int slot = p.slots[b], ne = p.n_eff[b];
+      bool live = ii < ne;
+      pos = p.pos0[b] + ii;
+      if (live && pos >= p.max_pos) {
+        dev_error(p.status, DFLASH_DEV_CAPACITY);
+        live = false;
+      }
+      pg = live ? page_of(p, slot, pos) : -1;
+      flag = (live ? 1 : 0) | 2;
+    }
+    tb.s[j] = s;
+    tb.pos[j] = pos;
+    tb.pg[j] = pg;
+    tb.flag[j] = flag;
+  }
+}
+
+// One warp's EPI_TOK tokens (j0, j0+4, ...) of a chunk: the table's values
+// and, for QKV/INJECT, RoPE (cos, sin) of frequencies lane and lane+32 --
+// the embedding's per-token rows for block rows, the table at the position
+// for fused-feature rows.
 struct TokCtx {
   float s[EPI_TOK];
   bool live[EPI_TOK];
-  bool inj[EPI_TOK];  // QKV: a fused-feature row (K/V appended, no Q)
+  bool inj[EPI_TOK];
   int pos[EPI_TOK], pg[EPI_TOK];
   float2 c0[EPI_TOK], c1[EPI_TOK];
 };
 
 template <int MODE>
-DFL_DEV void gather_ctx(const GemmParams& p, int t_first, int j0, int ntok, int lane, TokCtx& c) {
-  bool ok[EPI_TOK];
-  int tq[EPI_TOK];
+DFL_DEV void fill_ctx(const GemmParams& p, const TokTab& tb, int tab_t0, int t_first, int j0, int ntok, int lane,
+                      TokCtx& c) {
 #pragma unroll
   for (int q = 0; q < EPI_TOK; ++q) {
     const int j = j0 + 4 * q;
-    ok[q] = j < ntok;  // warp-uniform
-    tq[q] = ok[q] ? t_first + j : t_first;
-  }
-#pragma unroll
-  for (int q = 0; q < EPI_TOK; ++q) c.inj[q] = MODE == GM_INJECT || (MODE == GM_QKV && p.inj_m0 > 0 && tq[q] >= p.inj_m0);
-  // Every load that depends only on the token index is issued before any
-  // value is used, so the tokens' inputs arrive in one round trip (two for
-  // fused-feature rows, whose RoPE row and page follow from their position).
-  float sv[EPI_TOK][2];
-#pragma unroll
-  for (int q = 0; q < EPI_TOK; ++q) {
-    const bool fold = MODE == GM_QKV && c.inj[q];
-    const float* src = fold ? p.ss_inj : p.ss_in;
-    const int ld = fold ? p.inj_ld : p.ss_ld;
-    const int row = fold ? tq[q] - p.inj_m0 : tq[q];
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const int i = lane + 32 * k;
-      sv[q][k] = (ok[q] && i < p.ss_parts) ? src[(size_t)i * ld + row] : 0.f;
-    }
-  }
-  int2 bc[EPI_TOK];
-  float2 r0[EPI_TOK], r1[EPI_TOK];
-  if (MODE == GM_QKV) {  // block rows: position, page and RoPE row written by the embedding
-    const int D = p.D;
-#pragma unroll
-    for (int q = 0; q < EPI_TOK; ++q) {
-      const bool blk = ok[q] && !c.inj[q];
-      const float2* row = p.brope + (size_t)tq[q] * (D / 2);
-      bc[q] = blk ? p.bctx[tq[q]] : make_int2(0, -1);
-      r0[q] = blk ? row[lane] : make_float2(1.f, 0.f);
-      r1[q] = (blk && D == 128) ? row[lane + 32] : make_float2(1.f, 0.f);
-    }
-  }
-  int slot[EPI_TOK], ne[EPI_TOK], ii[EPI_TOK], p0[EPI_TOK];
-  bool any_inj = false;
-  if (MODE == GM_QKV || MODE == GM_INJECT) {  // fused-feature rows: the request's slot and first position
-#pragma unroll
-    for (int q = 0; q < EPI_TOK; ++q) {
-      const bool in = ok[q] && c.inj[q];
-      any_inj |= in;
-      int tl = MODE == GM_QKV ? tq[q] - p.inj_m0 : tq[q];
-      if (MODE == GM_INJECT && p.row_map) tl = p.row_map[tl];  // a compacted row: its request and row
-      const int b = tl / p.rows_per_req;
-      ii[q] = tl % p.rows_per_req;
-      slot[q] = in ? p.slots[b] : 0;
-      ne[q] = in ? p.n_eff[b] : 0;
-      p0[q] = in ? p.pos0[b] : 0;
-    }
-  }
-  {
-    float ssq[EPI_TOK];
-#pragma unroll
-    for (int q = 0; q < EPI_TOK; ++q) ssq[q] = sv[q][0] + sv[q][1];
-    for (int i = lane + 64; i < p.ss_parts; i += 32)  // hidden sizes above 8192 only
-#pragma unroll
-      for (int q = 0; q < EPI_TOK; ++q) {
-        const bool fold = MODE == GM_QKV && c.inj[q];
-        if (ok[q]) ssq[q] += (fold ? p.ss_inj : p.ss_in)[(size_t)i * (fold ? p.inj_ld : p.ss_ld) + (fold ? tq[q] - p.inj_m0 : tq[q])];
-      }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-      for (int q = 0; q < EPI_TOK; ++q) ssq[q] += __shfl_xor_sync(0xffffffffu, ssq[q], o);
-#pragma unroll
-    for (int q = 0; q < EPI_TOK; ++q) c.s[q] = rsqrtf(ssq[q] / (float)p.H + p.eps);
+    const bool ok = j < ntok;  // warp-uniform
+    const int k = t_first + (ok ? j : 0) - tab_t0;
+    c.s[q] = tb.s[k];
+    const int f = ok ? tb.flag[k] : 0;
+    c.live[q] = (f & 1) != 0;
+    c.inj[q] = (f & 2) != 0;
+    c.pos[q] = tb.pos[k];
+    c.pg[q] = tb.pg[k];
   }
   if (MODE == GM_QKV || MODE == GM_INJECT) {
     const int D = p.D;
 #pragma unroll
     for (int q = 0; q < EPI_TOK; ++q) {
-      c.c0[q] = c.c1[q] = make_float2(1.f, 0.f);
-      c.pg[q] = -1;
-      c.pos[q] = 0;
-      c.live[q] = false;
-    }
-    if (MODE == GM_QKV) {
-#pragma unroll
-      for (int q = 0; q < EPI_TOK; ++q) {
-        if (ok[q] && !c.inj[q]) {
-          c.pos[q] = bc[q].x;
-          c.pg[q] = bc[q].y;
-          c.live[q] = bc[q].x < p.max_pos;  // out-of-range positions were reported by the embedding
-          c.c0[q] = r0[q];
-          c.c1[q] = r1[q];
-        }
-      }
-    }
-    if (any_inj) {
-#pragma unroll
-      for (int q = 0; q < EPI_TOK; ++q) {
-        if (!(ok[q] && c.inj[q])) continue;
-        c.live[q] = ii[q] < ne[q];
-        c.pos[q] = p0[q] + ii[q];
-        if (c.live[q] && c.pos[q] >= p.max_pos) {
-          dev_error(p.status, DFLASH_DEV_CAPACITY);
-          c.live[q] = false;
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < EPI_TOK; ++q) {
-        if (ok[q] && c.inj[q] && c.live[q]) {
-          const float2* row = p.rope + (size_t)c.pos[q] * (D / 2);
-          c.c0[q] = row[lane];
-          if (D == 128) c.c1[q] = row[lane + 32];
-          c.pg[q] = page_of(p, slot[q], c.pos[q]);
-        }
-      }
+      const bool blk = MODE == GM_QKV && !c.inj[q];
+      const float2* row = blk ? p.brope + (size_t)(t_first + j0 + 4 * q) * (D / 2) : p.rope + (size_t)c.pos[q] * (D / 2);
+      c.c0[q] = c.live[q] ? row[lane] : make_float2(1.f, 0.f);
+      c.c1[q] = (c.live[q] && D == 128) ? row[lane + 32] : make_float2(1.f, 0.f);
     }
   }
 }
 
-// Final epilogue for tokens t_first .. t_first+ntok-1 of `tile`; staging
-// stg[j][r] holds the fully reduced fp32 accumulators.  Epilogue warp ew
-// handles tokens j = ew, ew+4, ...; lane holds rows lane + 32*jj.  Every
-// global input of a warp's next EPI_TOK tokens is loaded before any is used,
-// so the dependent-load chain costs a few round trips per tile, not per token.
-// pre0/pre1 (use_pre): the contexts of tokens ew+4q and ew+16+4q of a chunk
-// starting at token 0, gathered at kernel start; gq/gk: QKV's q/k head-norm
-// gains (load_head_gain); hpre (use_hpre, RESID): residual values of tokens
-// ew+4q, rows lane+32jj of this tile, loaded when the tile started.  All are
-// selected by value so they stay in registers.
+// Final epilogue for tokens t_first .. t_first+ntok-1 (ntok <= 32) of
+// `tile`; staging stg[j][r] holds the fully reduced fp32 accumulators.
+// Epilogue warp ew handles tokens j = ew, ew+4, ... (two groups of EPI_TOK
+// tokens, ew and ew+16); lane holds rows lane + 32*jj.  The groups run as a
+// loop, not unrolled: this code runs cold once per tile, and a second copy
+// of it costs more in instruction fetch than the loop does (measured).
+// cx holds the contexts of the chunk of cx_key = t_first * 64 + ntok (-1:
+// none), both groups' RoPE rows loaded in one round trip: a chunk's contexts
+// depend on its tokens only, so every n-tile finalised for the same chunk
+// reuses them, and with a single token tile the first chunk's are filled
+// while the main loop streams; otherwise they are filled here from the
+// shared-memory table tab (its first token tab_t0).  gq/gk: QKV's q/k
+// head-norm gains (load_head_gain); hpre (use_hpre, RESID): residual values
+// of tokens ew+4q of a single token tile, loaded when the tile started;
+// gpre: the tile's gains (RESID/FC).
 template <int MODE>
 DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, const float* stg, int ew, int lane,
-                       bool use_pre, const TokCtx& pre0, const TokCtx& pre1, const float* gq, const float* gk,
-                       bool use_hpre, const float (&hpre)[EPI_TOK][4], const float (&gpre)[4], int rnd,
-                       bool dry = false) {
+                       const TokTab& tab, int tab_t0, TokCtx (&cx)[2], int& cx_key, const float* gq, const float* gk,
+                       bool use_hpre, const float (&hpre)[EPI_TOK][4], const float (&gpre)[4], int rnd) {
   const int tt_all = tile / p.t_tiles;       // (group, n-tile)
   const int group = tt_all / p.n_tiles;
   const int nt = tt_all % p.n_tiles;
@@ -376,7 +345,18 @@ DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, con
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) rs[jj] = sc[lane + 32 * jj];
   }
-  for (int j0 = ew; j0 < ntok; j0 += 4 * EPI_TOK) {
+  if constexpr (MODE != GM_FC && MODE != GM_RESID) {
+    if (cx_key != t_first * 64 + ntok) {
+#pragma unroll
+      for (int gi = 0; gi < 2; ++gi)
+        if (ew + 16 * gi < ntok) fill_ctx<MODE>(p, tab, tab_t0, t_first, ew + 16 * gi, ntok, lane, cx[gi]);
+      cx_key = t_first * 64 + ntok;
+    }
+  }
+#pragma unroll 1
+  for (int gi = 0; gi < 2; ++gi) {
+    const int j0 = ew + 16 * gi;
+    if (j0 >= ntok) break;
     bool ok[EPI_TOK];
     int tq[EPI_TOK];
     float x[EPI_TOK][4];
@@ -391,26 +371,21 @@ DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, con
 
     if constexpr (MODE == GM_RESID || MODE == GM_FC) {
       const int n0 = nt * 128;
+      const float(&gn)[4] = gpre;  // the tile's gains, read when the tile started
       float hv[EPI_TOK][4];
-      const bool hp = use_hpre && t_first == 0 && j0 == ew;
+      const bool hp = use_hpre && t_first == 0 && gi == 0;
 #pragma unroll
       for (int q = 0; q < EPI_TOK; ++q)
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj)
-          hv[q][jj] = (MODE == GM_RESID && ok[q])
-                          ? (hp ? hpre[q][jj] : p.h[(size_t)tq[q] * p.N + n0 + lane + 32 * jj])
-                          : 0.f;
-      // the tile's gains: read when the tile started (one token tile), else now
-      float gn[4];
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj) gn[jj] = use_hpre ? gpre[jj] : p.gain[n0 + lane + 32 * jj];
+          hv[q][jj] = (MODE == GM_RESID && ok[q]) ? (hp ? hpre[q][jj] : p.h[(size_t)tq[q] * p.N + n0 + lane + 32 * jj]) : 0.f;
       float sq[EPI_TOK];
 #pragma unroll
       for (int q = 0; q < EPI_TOK; ++q) {
         sq[q] = 0.f;
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
-          x[q][jj] += hv[q][jj];
+          if (MODE == GM_RESID) x[q][jj] += hv[q][jj];
           sq[q] += x[q][jj] * x[q][jj];
         }
       }
@@ -420,7 +395,7 @@ DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, con
         for (int q = 0; q < EPI_TOK; ++q) sq[q] += __shfl_xor_sync(0xffffffffu, sq[q], o);
 #pragma unroll
       for (int q = 0; q < EPI_TOK; ++q) {
-        if (!ok[q] || dry) continue;
+        if (!ok[q]) continue;
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
           const size_t o = (size_t)tq[q] * p.N + n0 + lane + 32 * jj;
@@ -430,22 +405,16 @@ DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, con
         if (lane == 0) p.ss_out[(size_t)nt * p.M + tq[q]] = sq[q];
       }
     } else {
-    // per-token inputs: gathered at kernel start for the first 16 tokens of a
-    // single token tile, otherwise now
-    TokCtx ctx;
-    const int jg = t_first + j0 - ew;  // this token group's offset in the tile (0, 16, 32, ...)
-    if (use_pre && jg < 32)
-      ctx = jg == 0 ? pre0 : pre1;
-    else
-      gather_ctx<MODE>(p, t_first, j0, ntok, lane, ctx);
-    const TokCtx* tc = &ctx;
+    TokCtx tcv;
+    if constexpr (MODE != GM_RESID && MODE != GM_FC) tcv = gi ? cx[1] : cx[0];
+    const TokCtx* tc = &tcv;
     const float* s = tc->s;
 
     if (MODE == GM_SWIGLU) {
       const int f0 = nt * 64;
 #pragma unroll
       for (int q = 0; q < EPI_TOK; ++q) {
-        if (!ok[q] || dry) continue;
+        if (!ok[q]) continue;
 #pragma unroll
         for (int jj = 0; jj < 2; ++jj) {
           const float g = x[q][jj] * s[q], u = x[q][jj + 2] * s[q];
@@ -478,10 +447,10 @@ DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, con
             if (ok[q] && n < p.N) {
               const float v = x[q][jj] * s[q];
               if (v != v) {
-                if (!dry) dev_error(p.status, DFLASH_DEV_NAN);
+                dev_error(p.status, DFLASH_DEV_NAN);
                 continue;
               }
-              if (p.logits && !dry) p.logits[(size_t)tq[q] * p.N + n] = v;
+              if (p.logits) p.logits[(size_t)tq[q] * p.N + n] = v;
               const float sc = smp ? v * tinv + gumbel_at(skey, n) : v;
               const unsigned long long k = argmax_key(sc, (uint32_t)n);
               best[q] = k > best[q] ? k : best[q];
@@ -498,10 +467,10 @@ DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, con
             if (ok[q] && n < p.N) {
               const float v = x[q][jj] * s[q];
               if (v != v) {
-                if (!dry) dev_error(p.status, DFLASH_DEV_NAN);
+                dev_error(p.status, DFLASH_DEV_NAN);
                 continue;
               }
-              if (p.logits && !dry) p.logits[(size_t)tq[q] * p.N + n] = v;
+              if (p.logits) p.logits[(size_t)tq[q] * p.N + n] = v;
               const unsigned long long k = argmax_key(v, (uint32_t)n);
               best[q] = k > best[q] ? k : best[q];
             }
@@ -517,7 +486,7 @@ DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, con
         }
 #pragma unroll
       for (int q = 0; q < EPI_TOK; ++q)
-        if (ok[q] && lane == 0 && best[q] && !dry) atomicMax(p.keys + tq[q], best[q]);
+        if (ok[q] && lane == 0 && best[q]) atomicMax(p.keys + tq[q], best[q]);
     } else if (MODE == GM_QKV || MODE == GM_INJECT) {
       const int D = p.D;
       int n0, kind, layer;
@@ -547,7 +516,7 @@ DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, con
       if (kind < 2) head_norm_rope4(x, g, c0, c1, D, p.eps);
 #pragma unroll
       for (int q = 0; q < EPI_TOK; ++q) {
-        if (!live[q] || dry) continue;  // warp-uniform
+        if (!live[q]) continue;  // warp-uniform
         if (kind == 0 && inj[q]) continue;  // fused-feature rows only append K/V
         const float* xv = x[q];
         if (kind == 0) {
@@ -587,9 +556,10 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
   const int stage_bytes = A_STAGE_BYTES + BN * 128;
   float* stg = reinterpret_cast<float*>(sm + (size_t)stages * stage_bytes);
   float* red_buf = reinterpret_cast<float*>(sm + (size_t)stages * stage_bytes + STG_BYTES);
+  float* tokf = red_buf + (size_t)p.red_items * RED_CHUNK;  // the token table (TOKTAB_BYTES)
   // FP8 weights: each stage's 8 KB block lands here and is converted into the
   // stage's f16 A area by the converter warps
-  uint8_t* a8 = sm + (size_t)stages * stage_bytes + STG_BYTES + (size_t)p.red_items * RED_CHUNK * 4;
+  uint8_t* a8 = sm + (size_t)stages * stage_bytes + STG_BYTES + (size_t)p.red_items * RED_CHUNK * 4 + TOKTAB_BYTES;
   uint64_t* full = reinterpret_cast<uint64_t*>(a8 + (p.a_fp8 ? (size_t)stages * DFL_WBLK8_BYTES : 0));
   uint64_t* empty = full + stages;
   uint64_t* conv = empty + stages;  // FP8: the stage's A converted (the MMA waits on this instead of full)
@@ -884,38 +854,25 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
     const int r = q * 32 + lane;  // TMEM lane = tile row
     const int et = threadIdx.x - 64;
     const int ew = et >> 5;
-    TokCtx pre0, pre1;
-    bool use_pre = false;
     float gq[4], gk[4];
     if (MODE == GM_QKV) {
       load_head_gain(p.qn_gain, p.D, lane, gq);
       load_head_gain(p.kn_gain[0], p.D, lane, gk);
     }
     const int rnd = (MODE == GM_ARGMAX && p.temp_inv > 0.f && p.round) ? *p.round : 0;
-    if (MODE != GM_RESID && MODE != GM_FC && p.t_tiles == 1) {
-      const int nt0 = p.M < 32 ? p.M : 32;  // the first chunk's tokens
-      gather_ctx<MODE>(p, 0, ew, nt0, lane, pre0);
-      if (nt0 > 16)
-        gather_ctx<MODE>(p, 0, ew + 16, nt0, lane, pre1);
-      else
-        pre1 = pre0;
-      use_pre = true;
-    }
-    if (DFL_GEMM_WARM && u0 < u1) {
-      // The fused epilogue's code runs once here, on zeroed staging and
-      // storing nothing, while the main loop streams: the tile finalisation
-      // at the end of the launch then runs from a warm instruction cache.
-      const int tile0 = tile_of(p, u0 / KB, crank, tl);
-      const int tb0 = tile0 >= 0 ? (int)(tile0 % p.t_tiles) * BN : 0;
-      const int nw = (Mx - tb0) < 16 ? (Mx - tb0) : 16;
-      if (tile0 >= 0 && nw > 0) {
-        for (int i = et; i < 32 * 128; i += EPI_THREADS) stg[i] = 0.f;
-        named_bar_sync(1, EPI_THREADS);
-        float hz[EPI_TOK][4] = {}, gz[4] = {};
-        epi_final<MODE>(p, tile0, tb0, nw, stg, ew, lane, use_pre, pre0, pre1, gq, gk, false, hz, gz, rnd, true);
-        named_bar_sync(1, EPI_THREADS);
-      }
-    }
+    // per-token inputs of the token tile being finalised (not RESID/FC), in
+    // shared memory, rebuilt when the token tile changes
+    TokTab tab;
+    tab.s = tokf;
+    tab.pos = reinterpret_cast<int*>(tokf + DFL_BN_MAX);
+    tab.pg = tab.pos + DFL_BN_MAX;
+    tab.flag = tab.pg + DFL_BN_MAX;
+    int tab_tt = -1;
+    TokCtx cx[2];  // the contexts of the chunk of cx_key (its first token * 64 + its token count)
+    int cx_key = -1;
+    // with a single token tile, the contexts of its first 32 tokens (the
+    // table's values and their RoPE rows) are filled in registers once, while
+    // the main loop streams: the finalisation then issues no load for them
     int seg = 0;
     const int first_tile = u0 / KB;  // this CTA's first segment's scheduled tile
     uint32_t red_phase = 0;
@@ -926,21 +883,43 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
       const int abuf = seg & 1;
       const uint32_t use = (uint32_t)(seg >> 1);
       const int tile = tile_of(p, tile_s, crank, tl);
-      // RESID, one token tile: this tile's residual inputs for the first 16
-      // tokens, loaded while the accumulators and the split reduction finish
+      // RESID/FC: the tile's gains and, with one token tile, the residual
+      // inputs of its first 16 tokens, loaded while the accumulators and the
+      // split reduction finish
       float hpre[EPI_TOK][4], gpre[4];
-      const bool use_hpre = (MODE == GM_RESID || MODE == GM_FC) && p.t_tiles == 1 && tile >= 0;
-      if (use_hpre) {
-        const int n0 = (int)(tile % p.n_tiles) * 128;
+      const bool use_hpre = MODE == GM_RESID && p.t_tiles == 1 && tile >= 0;
+      if ((MODE == GM_RESID || MODE == GM_FC) && tile >= 0) {
+        const int n0 = (int)((tile / p.t_tiles) % p.n_tiles) * 128;
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) gpre[jj] = p.gain[n0 + lane + 32 * jj];
+      }
+      if (use_hpre) {
+        const int n0 = (int)(tile % p.n_tiles) * 128;
 #pragma unroll
         for (int q4 = 0; q4 < EPI_TOK; ++q4)
 #pragma unroll
           for (int jj = 0; jj < 4; ++jj) {
             const int j = ew + 4 * q4;
-            hpre[q4][jj] = (MODE == GM_RESID && j < p.M) ? p.h[(size_t)j * p.N + n0 + lane + 32 * jj] : 0.f;
+            hpre[q4][jj] = j < p.M ? p.h[(size_t)j * p.N + n0 + lane + 32 * jj] : 0.f;
           }
+      }
+      // the token table of this tile's token rows, built while its main loop streams
+      if (MODE != GM_RESID && MODE != GM_FC && tile >= 0 && (int)(tile % p.t_tiles) != tab_tt) {
+        const int ttb = (int)(tile % p.t_tiles);
+        const int tb0 = ttb * BN;
+        named_bar_sync(1, EPI_THREADS);  // every thread is done with the previous token tile's table
+        const int mtt = (Mx - tb0) < BN ? (Mx - tb0) : BN;
+        build_toktab<MODE>(p, tb0, mtt, tab, et);
+        named_bar_sync(1, EPI_THREADS);
+        tab_tt = ttb;
+        cx_key = -1;
+        if (p.t_tiles == 1) {  // the first 32-token chunk's contexts, while the main loop streams
+          const int n32 = mtt < 32 ? mtt : 32;
+#pragma unroll
+          for (int gi = 0; gi < 2; ++gi)
+            if (ew + 16 * gi < n32) fill_ctx<MODE>(p, tab, tb0, tb0, ew + 16 * gi, n32, lane, cx[gi]);
+          cx_key = tb0 * 64 + n32;
+        }
       }
       if (!mbar_wait(tfull + abuf, use & 1u, p.status, &aborted)) break;
       tc_fence_after();
@@ -1066,8 +1045,8 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
             for (int i = 0; i < 16; ++i) stg[(16 + i) * 128 + r] = v1[i];
           }
           named_bar_sync(1, EPI_THREADS);
-          epi_final<MODE>(p, (int)tile, t_base + tc0, (mt - tc0) < ct ? (mt - tc0) : ct, stg, ew, lane, use_pre,
-                          pre0, pre1, gq, gk, use_hpre, hpre, gpre, rnd);
+          epi_final<MODE>(p, (int)tile, t_base + tc0, (mt - tc0) < ct ? (mt - tc0) : ct, stg, ew, lane, tab,
+                          t_base, cx, cx_key, gq, gk, use_hpre, hpre, gpre, rnd);
           named_bar_sync(1, EPI_THREADS);
         }
         // several slices: the last finaliser to finish clears the tile's counters
@@ -1090,8 +1069,8 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
             for (int i = 0; i < 16; ++i) stg[(16 + i) * 128 + r] = v1[i];
           }
           named_bar_sync(1, EPI_THREADS);
-          epi_final<MODE>(p, (int)tile, t_base + tc0, (mt - tc0) < 32 ? (mt - tc0) : 32, stg, ew, lane, use_pre,
-                          pre0, pre1, gq, gk, use_hpre, hpre, gpre, rnd);
+          epi_final<MODE>(p, (int)tile, t_base + tc0, (mt - tc0) < 32 ? (mt - tc0) : 32, stg, ew, lane, tab,
+                          t_base, cx, cx_key, gq, gk, use_hpre, hpre, gpre, rnd);
           named_bar_sync(1, EPI_THREADS);
         }
       }
@@ -1148,14 +1127,14 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
 // still in use: whatever shared memory the ring leaves, 4 to 16.
 int gemm_red_items(int BN, int stages, int fp8) {
   const long long left = 232448LL - 1024 - (long long)stages * (A_STAGE_BYTES + BN * 128 + (fp8 ? DFL_WBLK8_BYTES : 0)) -
-                         STG_BYTES - 512;
+                         STG_BYTES - TOKTAB_BYTES - 512;
   const long long n = left / (RED_CHUNK * 4);
   return (int)(n < RED_PARTS ? RED_PARTS : (n > DFL_GEMM_RED_MAX ? DFL_GEMM_RED_MAX : n));
 }
 
 size_t gemm_smem_bytes(int BN, int stages, int fp8) {
   return 1024 + (size_t)stages * (A_STAGE_BYTES + BN * 128 + (fp8 ? DFL_WBLK8_BYTES : 0)) + STG_BYTES +
-         (size_t)gemm_red_items(BN, stages, fp8) * RED_CHUNK * 4 + (size_t)(3 * stages + 6) * 8 + 16;
+         (size_t)gemm_red_items(BN, stages, fp8) * RED_CHUNK * 4 + TOKTAB_BYTES + (size_t)(3 * stages + 6) * 8 + 16;
 }
 
 // Weight-ring depth.  Six 16 KB stages per SM already keep HBM streaming at
@@ -1164,7 +1143,7 @@ size_t gemm_smem_bytes(int BN, int stages, int fp8) {
 // is fastest at 6-7 stages, 2.5% slower at 12).  The lm_head, one long
 // stream with short tails, runs best at 8.
 int gemm_pick_stages(int BN, int mode, int fp8) {
-  const size_t budget = 232448 - 1024 - STG_BYTES - RED_BYTES - 512;
+  const size_t budget = 232448 - 1024 - STG_BYTES - RED_BYTES - TOKTAB_BYTES - 512;
   int st = (int)(budget / (size_t)(A_STAGE_BYTES + BN * 128 + (fp8 ? DFL_WBLK8_BYTES : 0)));
   const int cap = mode == GM_ARGMAX ? 8 : 6;
   st = st > cap ? cap : st;
