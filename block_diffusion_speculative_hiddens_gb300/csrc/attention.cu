@@ -529,23 +529,29 @@ __global__ void __launch_bounds__(G * KS * 32) k_attn(const AttnParams p) {
 // once), so P stays within f16 and O is read from TMEM only at the end; the
 // result is the same softmax up to rounding.
 // The K page is already the K-major B operand of the first MMA and the V^T
-// page the K-major B operand of the second (pre-swizzled in HBM).  S and P
-// are double-buffered, and the next page's Q K^T is issued before this page's
-// P V, so the MMAs overlap the softmax.
+// page the K-major B operand of the second (pre-swizzled in HBM).  S is
+// double-buffered, and the next page's Q K^T is issued before this page's
+// P V, so the MMAs overlap the softmax.  A stage is refilled only once the
+// P V of its page is done, so a CTA streams (stages) pages per (HBM round
+// trip + page latency); measured per page on a 32K context: ~1.7 us from a
+// load's issue to its landing, ~1.6 us from landing to the end of its P V.
+// Five stages of 32 KB therefore stream ~40 % more than four, and to make
+// room P has a single buffer: a page's P is written once the previous page's
+// P V is done (by then long since, as P V is issued the moment P lands).
 // Warps: 0 page loads (one thread), 1 TMEM allocation and MMA issue (one
 // thread), 2-9 softmax: two threads per query row (TMEM lane), each taking 32
 // of a page's 64 keys and half of the output columns; the pair trades its
 // half-row maxima through shared memory once per page.
 template <int D>
 struct TcCfg {
-  static constexpr int STAGES = 4;                  // pages in flight
+  static constexpr int STAGES = 5;                  // pages in flight
   static constexpr int BLK = 64 * D * 2;            // one K (or V^T) page block
   static constexpr int STAGE = 2 * BLK;
   static constexpr int QB = 128 * D * 2;            // Q: 128 rows x D, D/64 panels of 16 KB
   static constexpr int PB = 128 * 64 * 2;           // P: 128 rows x 64 keys, one 16 KB panel
   static constexpr int OFF_Q = STAGES * STAGE;
-  static constexpr int OFF_P = OFF_Q + QB;          // two P buffers
-  static constexpr int OFF_BAR = OFF_P + 2 * PB;
+  static constexpr int OFF_P = OFF_Q + QB;          // one P buffer
+  static constexpr int OFF_BAR = OFF_P + PB;
   static constexpr int MAX_PIDS = 512;
   static constexpr int OFF_PIDS = OFF_BAR + 256;
   static constexpr int OFF_X = OFF_PIDS + MAX_PIDS * 4;  // half-row exchange: [2 parities][2 halves][128] u64
@@ -567,7 +573,7 @@ __global__ void __launch_bounds__(320, 1) k_attn_tc(const AttnParams p) {
   uint64_t* empty = full + C::STAGES;       // [STAGES] page's MMAs done
   uint64_t* s_full = empty + C::STAGES;     // [2] S in TMEM
   uint64_t* s_empty = s_full + 2;           // [2] S read by the softmax warps
-  uint64_t* p_full = s_empty + 2;           // [2] P in shared memory
+  uint64_t* p_full = s_empty + 2;           // P of page i (phase i & 1) in shared memory
   uint64_t* o_full = p_full + 2;            // [2] P V of page i (barrier i & 1) complete
   uint64_t* q_full = o_full + 2;            // Q in shared memory
   uint64_t* mdone = q_full + 1;             // every issued MMA complete
@@ -698,9 +704,9 @@ __global__ void __launch_bounds__(320, 1) k_attn_tc(const AttnParams p) {
       for (int i = 0; i < n && ok; ++i) {
         if (i + 1 < n && !issue_s(i + 1)) break;
         const int s = i % C::STAGES, bb = i & 1;
-        if (!mbar_wait(p_full + bb, (uint32_t)((i / 2) & 1), p.status, &aborted)) break;
+        if (!mbar_wait(p_full, (uint32_t)(i & 1), p.status, &aborted)) break;
         tc_fence_after();
-        const uint32_t p_addr = smem_u32(sm + C::OFF_P + bb * C::PB);
+        const uint32_t p_addr = smem_u32(sm + C::OFF_P);
         const uint32_t v_addr = smem_u32(sm + s * C::STAGE + C::BLK);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
@@ -756,9 +762,9 @@ __global__ void __launch_bounds__(320, 1) k_attn_tc(const AttnParams p) {
     // this row's keys: all, or (causal) the context and block rows up to the
     // row's own token (padding rows: up to the last live row)
     const int klim = p.causal ? nkeys - nv + min(r & 15, nv - 1) + 1 : nkeys;
-    // P V of page i complete (o_full[i & 1]).  Waited once per page, right
-    // after P of the next page is published, so a barrier never runs two
-    // phases ahead of its waiter; also frees P buffer i & 1 for page i + 2.
+    // P V of page i complete (o_full[i & 1]).  Waited once per page, before
+    // P of the next page is written (one P buffer), so a barrier never runs
+    // two phases ahead of its waiter.
     int o_seen = -1;  // pages whose P V this thread has seen complete
     auto wait_o = [&](int i) {
       if (i <= o_seen) return true;
@@ -819,16 +825,16 @@ __global__ void __launch_bounds__(320, 1) k_attn_tc(const AttnParams p) {
         pk[k] = pack_f16x2(a, c);
       }
       l_run += rs;
+      if (i > 0 && !wait_o(i - 1)) break;  // the previous page's P V has read the P buffer
       {  // this half of P row r: 32 keys = 4 chunks of 16 bytes, swizzled like the K page rows
-        uint8_t* prow = sm + C::OFF_P + bb * C::PB + r * 128;
+        uint8_t* prow = sm + C::OFF_P + r * 128;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
           *reinterpret_cast<uint4*>(prow + ((((4 * kh + c) ^ (r & 7))) << 4)) =
               make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
       }
       fence_proxy_async_smem();
-      mbar_arrive(p_full + bb);
-      if (i > 0) ok = wait_o(i - 1);
+      mbar_arrive(p_full);
     }
     // the row's output half, once every P V is done
     if (ok && n > 0 && !aborted && wait_o(n - 1)) {

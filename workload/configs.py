@@ -108,6 +108,18 @@ TEST_CONFIGS = {
     "mid": DraftConfig(
         name="mid", hidden=2048, n_q_heads=16, n_kv_heads=4, head_dim=128, intermediate=6144,
         n_layers=2, vocab=32768, rope_theta=1e6, batch=1, ctx0=1024, rounds=8, match_p=0.9),
+    # The mid shape at batch 64 (1,024 block rows, as the batched workload):
+    # the batched GEMMs' hardware counters with a device footprint of ~1 GB.
+    "mid-b64": DraftConfig(
+        name="mid-b64", hidden=2048, n_q_heads=16, n_kv_heads=4, head_dim=128, intermediate=6144,
+        n_layers=2, vocab=32768, rope_theta=1e6, batch=64, ctx0=None, rounds=4, match_p=None,
+        ctx_range=(256, 1024), p_range=(0.6, 0.95)),
+    # The long-context attention (32 query / 4 KV heads x 128, 4 requests at
+    # 32K) with two layers and a small vocabulary: its hardware counters with
+    # a device footprint of ~1.5 GB.
+    "mid-long": DraftConfig(
+        name="mid-long", hidden=2048, n_q_heads=32, n_kv_heads=4, head_dim=128, intermediate=6144,
+        n_layers=2, vocab=32768, rope_theta=1e6, batch=4, ctx0=32768, rounds=4, match_p=0.9),
     # Batch 16: 256 block tokens, so every GEMM of the round runs with a full
     # 256-token tile shared by a cluster of CTAs.
     "small-b16": DraftConfig(
