@@ -542,12 +542,15 @@ __global__ void __launch_bounds__(G * KS * 32) k_attn(const AttnParams p) {
 // thread), 2-9 softmax: two threads per query row (TMEM lane), each taking 32
 // of a page's 64 keys and half of the output columns; the pair trades its
 // half-row maxima through shared memory once per page.
+#ifndef DFL_ATTN_Q_TMEM  // 1: Q is the S MMA's A operand in tensor memory (else in shared memory)
+#define DFL_ATTN_Q_TMEM 1
+#endif
 template <int D>
 struct TcCfg {
-  static constexpr int STAGES = 5;                  // pages in flight
+  static constexpr int STAGES = DFL_ATTN_Q_TMEM ? 6 : 5;  // pages in flight
   static constexpr int BLK = 64 * D * 2;            // one K (or V^T) page block
   static constexpr int STAGE = 2 * BLK;
-  static constexpr int QB = 128 * D * 2;            // Q: 128 rows x D, D/64 panels of 16 KB
+  static constexpr int QB = DFL_ATTN_Q_TMEM ? 0 : 128 * D * 2;  // Q: 128 rows x D, D/64 panels of 16 KB
   static constexpr int PB = 128 * 64 * 2;           // P: 128 rows x 64 keys, one 16 KB panel
   static constexpr int OFF_Q = STAGES * STAGE;
   static constexpr int OFF_P = OFF_Q + QB;          // one P buffer
@@ -558,10 +561,14 @@ struct TcCfg {
   static constexpr int SMEM = 1024 + OFF_X + 2 * 2 * 128 * 8;  // + 1024 for aligning the base
   static constexpr int S_COL = 0;                   // S buffers: columns [0, 128)
   static constexpr int O_COL = 128;                 // O accumulator: columns [128, 128 + D)
+  static constexpr int Q_COL = 256;                 // Q (tensor-memory A operand): columns [256, 256 + D/2)
   // columns allocated: a power of two covering the buffers, so two CTAs that
   // might share an SM never wait on each other's columns
-  static constexpr uint32_t TMEM_COLS = 256;
+  static constexpr uint32_t TMEM_COLS = DFL_ATTN_Q_TMEM ? 512 : 256;
 };
+
+// TMEM address of lane quarter q4 (lanes 32*q4 ..) at column 0.
+DFL_DEV uint32_t lane_base_q(uint32_t tmem, int q4) { return tmem + ((uint32_t)(q4 * 32) << 16); }
 
 template <int D, int G>
 __global__ void __launch_bounds__(320, 1) k_attn_tc(const AttnParams p) {
@@ -693,9 +700,14 @@ __global__ void __launch_bounds__(320, 1) k_attn_tc(const AttnParams p) {
         const uint32_t k_addr = smem_u32(sm + s * C::STAGE);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t ad = sdesc_sw128(q_addr + (uint32_t)((kk >> 2) * 16384)) + (uint64_t)(2 * (kk & 3));
           const uint64_t bd = sdesc_sw128(k_addr + (uint32_t)((kk >> 2) * 8192)) + (uint64_t)(2 * (kk & 3));
-          tc_mma_f16(tmem + (uint32_t)(C::S_COL + 64 * bb), ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+          if (DFL_ATTN_Q_TMEM) {
+            tc_mma_f16_ts(tmem + (uint32_t)(C::S_COL + 64 * bb), tmem + (uint32_t)(C::Q_COL + 8 * kk), bd, idesc_s,
+                          kk > 0 ? 1u : 0u);
+          } else {
+            const uint64_t ad = sdesc_sw128(q_addr + (uint32_t)((kk >> 2) * 16384)) + (uint64_t)(2 * (kk & 3));
+            tc_mma_f16(tmem + (uint32_t)(C::S_COL + 64 * bb), ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+          }
         }
         tc_commit(s_full + bb);
         return true;
@@ -747,15 +759,27 @@ __global__ void __launch_bounds__(320, 1) k_attn_tc(const AttnParams p) {
     {  // this row's query (half of its chunks per thread), zero-padded to 128 rows
       const int h = r >> 4, t = r & 15;
       const f16* src = p.q + ((size_t)(b * DFL_BLOCK + t) * hq + kvh * G + h) * D;
+      if (DFL_ATTN_Q_TMEM) {  // TMEM lane r, columns Q_COL + kh*D/4 ...: two f16 per column
+        uint4 v[D / 16];
 #pragma unroll
-      for (int cc = 0; cc < D / 16; ++cc) {
-        const int c = kh * (D / 16) + cc;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (r < rows) v = *reinterpret_cast<const uint4*>(src + c * 8);
-        uint8_t* dst = sm + C::OFF_Q + (c >> 3) * 16384 + r * 128 + (((c & 7) ^ (r & 7)) << 4);
-        *reinterpret_cast<uint4*>(dst) = v;
+        for (int cc = 0; cc < D / 16; ++cc)
+          v[cc] = r < rows ? *reinterpret_cast<const uint4*>(src + (kh * (D / 16) + cc) * 8) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int j = 0; j < D / 64; ++j)
+          tmem_st16(lane_base_q(tmem, q4) + (uint32_t)(C::Q_COL + kh * (D / 4) + 16 * j),
+                    reinterpret_cast<const float*>(&v[4 * j]));
+        tc_fence_before();
+      } else {
+#pragma unroll
+        for (int cc = 0; cc < D / 16; ++cc) {
+          const int c = kh * (D / 16) + cc;
+          uint4 v = make_uint4(0u, 0u, 0u, 0u);
+          if (r < rows) v = *reinterpret_cast<const uint4*>(src + c * 8);
+          uint8_t* dst = sm + C::OFF_Q + (c >> 3) * 16384 + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+          *reinterpret_cast<uint4*>(dst) = v;
+        }
+        fence_proxy_async_smem();
       }
-      fence_proxy_async_smem();
       mbar_arrive(q_full);
     }
     const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
@@ -779,9 +803,15 @@ __global__ void __launch_bounds__(320, 1) k_attn_tc(const AttnParams p) {
       if (i == 0 && threadIdx.x == 64) atrace(p, 2);
       tc_fence_after();
       float sc[32];
+      {
+        uint32_t u[32];
 #pragma unroll
-      for (int j = 0; j < 2; ++j)
-        tmem_ld16(lane_base + (uint32_t)(C::S_COL + 64 * bb + 32 * kh + 16 * j), sc + 16 * j);
+        for (int j = 0; j < 2; ++j)
+          tmem_ld16_nowait(lane_base + (uint32_t)(C::S_COL + 64 * bb + 32 * kh + 16 * j), u + 16 * j);
+        tmem_wait_ld();
+#pragma unroll
+        for (int k = 0; k < 32; ++k) sc[k] = __uint_as_float(u[k]);
+      }
       tc_fence_before();
       mbar_arrive(s_empty + bb);
       const int valid = min(64, klim - (pb + i) * 64) - 32 * kh;  // this half's unmasked keys
