@@ -299,7 +299,7 @@ def measure(cfg, w_dev, dev, K, W, *, attn_impl=0, weight_fp8=0, temperature=0.0
     R = rounds_per_slot or cfg.rounds
     n_groups = math.ceil(K / R) + 1                      # + one group of B slots for warm-up
     n_slots = n_groups * B
-    cap = int(ctx.max()) + S * (max(R, W) + 2) + 64
+    cap = int(ctx.max()) + S * (max(R, W) + 2 + TRACED_ROUNDS) + 64
     mpps = math.ceil(cap / 64) + 1
     F = cfg.fused_dim
     feat_stream, fs, feat_src = feature_stream(cfg, B, cap, dev)
@@ -476,6 +476,25 @@ def measure(cfg, w_dev, dev, K, W, *, attn_impl=0, weight_fp8=0, temperature=0.0
         "weights_source": weights_desc,
     }
 
+    # ---- where the round's time goes: one more round of the warm-up group,
+    # captured with every GEMM and attention launch writing per-CTA
+    # %globaltimer stamps, replayed TRACED_ROUNDS - 1 times; each launch's
+    # time runs from the previous traced launch's end to its own (the small
+    # kernels between them count with the launch after them)
+    if not fold:
+        kt = kernel_times(d, binding, run_round, wst, wv, stream, cfg)
+        if kt is not None:
+            status |= d.read_status()
+            res["status_word"] = status
+            g_us, a_us = kt["gemm_us"], kt["attention_us"]
+            res["kernel_time"] = kt
+            res["gemm_tensor"] = {"flops_per_round": round_flops, "us_per_round": round(g_us, 1),
+                                  "achieved_tflops": round(round_flops / (g_us * 1e-6) / 1e12, 1), "peak": tf_sust,
+                                  "frac": round(round_flops / (g_us * 1e-6) / 1e12 / tf_sust, 4)}
+            res["attention_hbm"] = {"kv_bytes_per_round": int(kv_bytes), "us_per_round": round(a_us, 1),
+                                    "achieved_gbs": round(kv_bytes / (a_us * 1e-6) / 1e9, 1),
+                                    "frac": round(kv_bytes / (a_us * 1e-6) / 1e9 / hbm, 4)}
+
     # ---- end to end through the C ABI with host buffers: per round the
     # block's target features and verify streams go host -> device from
     # pinned memory and the round's result comes back; the host prepares
@@ -548,6 +567,49 @@ def measure(cfg, w_dev, dev, K, W, *, attn_impl=0, weight_fp8=0, temperature=0.0
     return res
 
 
+TRACED_ROUNDS = 4  # rounds the kernel-time pass adds to the warm-up group (capture + replays)
+
+
+def kernel_times(d, binding, run_round, st, ver, stream, cfg):
+    """GEMM and attention time of one live round (us), from a traced replay;
+    None when the launches cannot be attributed."""
+    import numpy as np
+    import torch
+    cap = 16384
+    buf = torch.zeros(cap, 8, dtype=torch.int64, device=stream.device)
+    d.trace_arm(binding.KID_ALL, buf, cap)
+    d.graph_begin(stream)
+    run_round(st, ver, stream)
+    d.graph_end(stream)
+    d.trace_arm(0)
+    for _ in range(TRACED_ROUNDS - 1):
+        d.graph_launch(stream)
+    stream.synchronize()
+    rows = buf.cpu().numpy().astype(np.int64)
+    names = ["fc", "inject"] + ["qkv", "attention", "wo", "gate_up", "down"] * cfg.n_layers + ["lm_head"]
+    segs, pos = [], 0
+    while pos < cap and rows[pos, 0] > 0 and len(segs) < len(names):
+        grid = int(rows[pos, 6]) >> 32
+        if grid <= 0 or pos + grid > cap:
+            return None
+        seg = rows[pos:pos + grid]
+        segs.append((int(seg[:, 0][seg[:, 0] > 0].min()), int(seg[:, 5].max())))
+        pos += grid
+    if len(segs) != len(names):
+        return None
+    own = {}
+    prev_end = segs[0][0]
+    for (start, end), nm in zip(segs, names):
+        own[nm] = own.get(nm, 0.0) + (end - prev_end) * 1e-3
+        prev_end = end
+    gemm = sum(v for k, v in own.items() if k != "attention")
+    return {"gemm_us": round(gemm, 1), "attention_us": round(own["attention"], 1),
+            "per_kind_us": {k: round(v, 1) for k, v in own.items()},
+            "traced_us": round((segs[-1][1] - segs[0][0]) * 1e-3, 1),
+            "source": "one traced replay of a round (per-CTA %globaltimer stamps); a launch's time runs from the "
+                      "previous traced launch's end to its own, the small kernels between counting with the next"}
+
+
 def workload_desc(cfg, ctx_mean):
     B, H, D, F = cfg.batch, cfg.hidden, cfg.head_dim, cfg.fused_dim
     ctx_desc = f"prompt {cfg.ctx0}" if cfg.ctx0 else f"prompts U[{cfg.ctx_range[0]}, {cfg.ctx_range[1]}]"
@@ -558,7 +620,8 @@ def workload_desc(cfg, ctx_mean):
 
 SUMMARY_KEYS = ("value", "round_us", "round_us_p10_p50_p90", "round_samples", "stand_in_verify_us", "mean_tau",
                 "accepted_tok_s", "roofline", "round_roofline", "round_tensor", "prefill", "clocks", "steps",
-                "warmup", "gpu_launches", "plan", "status_word", "weights_source", "feature_source")
+                "warmup", "gpu_launches", "plan", "status_word", "weights_source", "feature_source", "gemm_tensor",
+                "attention_hbm", "kernel_time")
 
 
 def run_gpu(args):
@@ -618,7 +681,7 @@ def run_gpu(args):
 
     names = [] if args.workloads == "none" else (
         list(EXTRA_WORKLOADS) if args.workloads == "all" else [n for n in args.workloads.split(",") if n])
-    workloads = {cfg.name: {k: head[k] for k in SUMMARY_KEYS}} if names else {}
+    workloads = {cfg.name: {k: head[k] for k in SUMMARY_KEYS if k in head}} if names else {}
     for name in names:
         if name == cfg.name:
             continue
@@ -635,7 +698,7 @@ def run_gpu(args):
         r = measure(wc, wd, dev, EXTRA_STEPS.get(name, 16), min(W, 3), attn_impl=args.attn_impl, weights_desc=src)
         if wd is not w_dev:
             del wd
-        s = {k: r[k] for k in SUMMARY_KEYS}
+        s = {k: r[k] for k in SUMMARY_KEYS if k in r}
         s["workload"] = workload_desc(wc, 0.0)
         workloads[name] = s
     if workloads:
