@@ -73,10 +73,31 @@ DFL_DEV int cta_of_unit(int u, int U, int G) { return ((u + 1) * G + U - 1) / U 
 // With cl = 1 the two numberings coincide.
 // tl: token tiles scheduled (p.t_tiles, or fewer for a launch whose live
 // token rows are counted on the device); tile ids keep the p.t_tiles layout.
+//
+// The token tile is the slowest index of the scheduled order: the clusters'
+// contiguous unit ranges then put the token tiles of one n-tile group on
+// clusters a quarter (for four token tiles) of the grid apart, which stream
+// the same weight blocks at about the same time, so DRAM serves each once
+// and L2 the rest (with the token tile fastest, one cluster ran the token
+// tiles of a group back to back and re-read its weights from DRAM for each).
+#ifndef DFL_GEMM_TT_SLOW
+#define DFL_GEMM_TT_SLOW 1
+#endif
+DFL_DEV void sched_decode(const GemmParams& p, int ct, int tl, int& rest, int& tt) {
+  if (DFL_GEMM_TT_SLOW) {
+    const int ngr = p.groups * p.n_tg;
+    rest = ct % ngr;
+    tt = ct / ngr;
+  } else {
+    rest = ct / tl;
+    tt = ct % tl;
+  }
+}
 DFL_DEV int tile_of(const GemmParams& p, int ct, int cr, int tl) {
-  const int rest = ct / tl;
+  int rest, tt;
+  sched_decode(p, ct, tl, rest, tt);
   const int nt = (rest % p.n_tg) * p.cl + cr;
-  return nt < p.n_tiles ? ((rest / p.n_tg) * p.n_tiles + nt) * p.t_tiles + ct % tl : -1;
+  return nt < p.n_tiles ? ((rest / p.n_tg) * p.n_tiles + nt) * p.t_tiles + tt : -1;
 }
 
 // Counter-based random numbers for drafting at temperature > 0: SplitMix64
@@ -656,11 +677,11 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
       const uint8_t* a_ptr = nullptr;
       const int blk_bytes = p.a_fp8 ? DFL_WBLK8_BYTES : A_STAGE_BYTES;
       auto tile_base = [&]() {  // `tile` counts scheduled tiles here
-        const int rest = tile / tl;
+        int rest;
+        sched_decode(p, tile, tl, rest, tt);
         const int g = rest / p.n_tg;
         int nt = (rest % p.n_tg) * CL + crank;
         if (nt >= p.n_tiles) nt = p.n_tiles - 1;
-        tt = tile % tl;
         a_ptr = static_cast<const uint8_t*>(p.a[g]) + ((size_t)(p.a_tile_off + nt) * KBi + kb) * blk_bytes;
       };
       tile_base();
@@ -718,7 +739,8 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
           if (++k2 == KBi) {
             k2 = 0;
             ++t2;
-            const int rest = t2 / tl;
+            int rest, tt2;
+            sched_decode(p, t2, tl, rest, tt2);
             int nt = (rest % p.n_tg) * CL + crank;
             if (nt >= p.n_tiles) nt = p.n_tiles - 1;
             ap = static_cast<const uint8_t*>(p.a[rest / p.n_tg]) + (size_t)(p.a_tile_off + nt) * KBi * blk_bytes;
