@@ -676,6 +676,7 @@ def run_gpu(args):
                                      "round_us_with_stand_in_verify", "accepted_tok_s", "mean_tau", "gpu_launches",
                                      "plan", "graph_kernel_nodes", "roofline", "round_roofline", "round_tensor",
                                      "prefill", "clocks", "status_word")})
+    res.update({k: head[k] for k in ("gemm_tensor", "attention_hbm", "kernel_time") if k in head})
     if "e2e" in head:
         res["e2e"] = head["e2e"]
 
