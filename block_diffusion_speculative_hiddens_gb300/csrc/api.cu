@@ -128,6 +128,7 @@ struct dflash_handle {
   // cached B operand descriptors for the current token count
   int bm_M = -1;
   CUtensorMap tm_hg, tm_o, tm_act;
+  CUtensorMap tm_hg_s;  // hg in DFL_BN_SMALL-row token tiles (the QKV projection)
   int bm_MX = -1;
   CUtensorMap tm_hgx;  // hg plus the fused-feature rows below it
   int bm_rows = -1;
@@ -225,6 +226,21 @@ int pick_attn_splits(const dflash_config& c, int num_sms) {
 #ifndef DFL_ATTN_GLOBAL
 #define DFL_ATTN_GLOBAL 1
 #endif
+// Token tiles of at most DFL_BN_SMALL rows for the GEMMs with few n-tiles
+// and heavy epilogues (QKV, fusion, injection) over at most
+// DFL_BN_SMALL_ROWS rows: at a round's 1,024 rows twice the token tiles give
+// their CTAs whole tiles instead of shares of a few split ones (measured on
+// GB300, batched round 4,411 -> 4,313 us: QKV 534 -> 487 us, injection 128
+// -> 80 us; the lm_head and gate/up lose with it, their tiles being
+// plentiful, and so does a 2,048-row prefill chunk: 44.2 -> 48.0 ms).
+#ifndef DFL_BN_SMALL
+#define DFL_BN_SMALL 128
+#endif
+#ifndef DFL_BN_SMALL_ROWS
+#define DFL_BN_SMALL_ROWS 1024
+#endif
+int bn_small(int M) { return M <= DFL_BN_SMALL_ROWS ? DFL_BN_SMALL : DFL_BN_MAX; }
+
 #ifndef DFL_ATTN_GLOBAL_MIN_PAGES  // pages per split (at full slot capacity) from which splits merge through memory
 #define DFL_ATTN_GLOBAL_MIN_PAGES 32
 #endif
@@ -255,6 +271,9 @@ size_t carve(dflash_handle* h, const dflash_config& c, char* base, int num_sms) 
   int tiles = std::max({(c.n_q_heads + 2 * hkv) * D / 128, H / 128, I / 64, c.n_layers * 2 * hkv * D / 128,
                         ceil_div(c.vocab, 128)});
   tiles *= t_tiles_max;
+  // the GEMMs on DFL_BN_SMALL-row token tiles: QKV, fusion, injection
+  tiles = std::max(tiles, std::max({(c.n_q_heads + 2 * hkv) * D / 128, H / 128, c.n_layers * 2 * hkv * D / 128}) *
+                              ceil_div(std::min(std::max(M, R), DFL_BN_SMALL_ROWS), DFL_BN_SMALL));
 
   dflash_handle tmp;
   dflash_handle* o = h ? h : &tmp;
@@ -377,16 +396,16 @@ struct ProbeScope {
 #define DFL_GEMM_MAX_CL 4
 #endif
 
-// Token tiling of an M-row GEMM operand: t_tiles tiles of BN rows; for tiles
-// of 128 tokens or more, cl CTAs of a cluster share each token tile (each
-// loads BN/cl rows into all of them), so its box is BN/cl rows.
+// Token tiling of an M-row GEMM operand: t_tiles tiles of BN <= bn_max rows;
+// for tiles of 128 tokens or more, cl CTAs of a cluster share each token
+// tile (each loads BN/cl rows into all of them), so its box is BN/cl rows.
 struct GemmShape {
   int t_tiles, BN, cl;
   uint32_t box() const { return (uint32_t)(BN / cl); }
 };
-GemmShape gemm_shape(const dflash_handle* h, int M) {
+GemmShape gemm_shape(const dflash_handle* h, int M, int bn_max = DFL_BN_MAX) {
   GemmShape g;
-  g.t_tiles = ceil_div(std::max(M, 1), DFL_BN_MAX);
+  g.t_tiles = ceil_div(std::max(M, 1), bn_max);
   g.BN = ((ceil_div(std::max(M, 1), g.t_tiles) + 15) / 16) * 16;
   g.cl = (g.BN >= 128 && h->gemm_cl > 1) ? h->gemm_cl : 1;
   if (g.cl == 4) g.BN = (g.BN + 31) / 32 * 32;  // each quarter whole 8-row swizzle atoms
@@ -404,9 +423,9 @@ void fp8_weights(const dflash_handle* h, GemmParams& p, const float* sc, int g =
 // a_tile_off .. a_tile_off+n_tiles-1 of each) and the token operand B.
 int run_gemm(dflash_handle* h, cudaStream_t s, int mode, const void* const* a, int groups, int a_tile_off,
              int n_tiles, int K, const CUtensorMap& B, int M, GemmParams p, bool allow_split, uint32_t ab_type,
-             int kid = 0) {
+             int kid = 0, int bn_max = DFL_BN_MAX) {
   if (M <= 0) return DFLASH_OK;
-  const GemmShape gs = gemm_shape(h, M);
+  const GemmShape gs = gemm_shape(h, M, bn_max);
   const int t_tiles = gs.t_tiles;
   const int BN = gs.BN;
   p.mode = mode;
@@ -470,6 +489,7 @@ int ensure_bmaps(dflash_handle* h, int M) {
   const dflash_config& c = h->cfg;
   const uint32_t BN = gemm_shape(h, M).box();
   if (!make_tmap(&h->tm_hg, h->hg, M, c.hidden, BN)) return DFLASH_ERR_CUDA;
+  if (!make_tmap(&h->tm_hg_s, h->hg, M, c.hidden, gemm_shape(h, M, bn_small(M)).box())) return DFLASH_ERR_CUDA;
   if (!make_tmap(&h->tm_o, h->obuf, M, (uint64_t)c.n_q_heads * c.head_dim, BN)) return DFLASH_ERR_CUDA;
   if (!make_tmap(&h->tm_act, h->act, M, c.intermediate, BN)) return DFLASH_ERR_CUDA;
   h->bm_M = M;
@@ -590,8 +610,8 @@ int draft_impl(dflash_handle* h, const int32_t* slots, int32_t batch, const int3
       }
       const void* a = h->wqkv_pk[l];
       fp8_weights(h, p, h->wqkv_sc[l]);
-      rc = run_gemm(h, s, GM_QKV, &a, 1, 0, p.N / 128, H, fold ? h->tm_hgx : h->tm_hg, fold ? M + R : M, p, true, 0,
-                    DFLASH_KID_QKV);
+      rc = run_gemm(h, s, GM_QKV, &a, 1, 0, p.N / 128, H, fold ? h->tm_hgx : h->tm_hg_s, fold ? M + R : M, p, true, 0,
+                    DFLASH_KID_QKV, fold ? DFL_BN_MAX : bn_small(M));
       if (rc) return rc;
     }
     {  // block attention
@@ -869,7 +889,7 @@ int dflash_fuse_inject(dflash_handle* h, const int32_t* slots, int32_t batch, co
   // slots' lengths and pages untouched
   CUtensorMap tm_feats;
   if (R > 0) {
-    const uint32_t BN = gemm_shape(h, R).box();
+    const uint32_t BN = gemm_shape(h, R, bn_small(R)).box();
     if (!make_tmap(&tm_feats, feats, R, (uint64_t)c.n_fused * H, BN, true)) return DFLASH_ERR_INVALID_ARG;
     if (h->bm_rows != R) {
       if (!make_tmap(&h->tm_cg, h->cg, R, H, BN)) return DFLASH_ERR_CUDA;
@@ -901,7 +921,7 @@ int dflash_fuse_inject(dflash_handle* h, const int32_t* slots, int32_t batch, co
     if (compact) p.m_dyn = h->n_live;
     const void* a = h->fc_pk;
     rc = run_gemm(h, s, GM_FC, &a, 1, 0, H / 128, c.n_fused * H, compact ? h->tm_cstage : tm_feats, R, p, true, 1,
-                  DFLASH_KID_FC);
+                  DFLASH_KID_FC, bn_small(R));
     if (rc) return rc;
   }
   {  // every layer's K/V projection of the fused feature, k-norm, RoPE, paged append
@@ -925,7 +945,7 @@ int dflash_fuse_inject(dflash_handle* h, const int32_t* slots, int32_t batch, co
       fp8_weights(h, p, h->wqkv_sc[l], l);
     }
     rc = run_gemm(h, s, GM_INJECT, a, c.n_layers, c.n_q_heads * D / 128, p.N / 128, H, h->tm_cg, R, p, true, 0,
-                  DFLASH_KID_INJECT);
+                  DFLASH_KID_INJECT, bn_small(R));
     if (rc) return rc;
   }
   return DFLASH_OK;

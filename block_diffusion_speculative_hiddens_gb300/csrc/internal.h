@@ -14,7 +14,9 @@ typedef __half f16;
 #define DFL_MAX_LAYERS 8
 #define DFL_BLOCK 16
 #define DFL_PAGE 64
+#ifndef DFL_BN_MAX
 #define DFL_BN_MAX 256
+#endif
 // One packed FP8 weight block: 128 rows x 64 bytes, row-major (8 KB).
 #define DFL_WBLK8_BYTES (128 * 64)
 // One packed weight block: 128 rows x 64 columns of 16-bit values (16 KB).
