@@ -80,6 +80,9 @@ DFL_DEV int cta_of_unit(int u, int U, int G) { return ((u + 1) * G + U - 1) / U 
 // the same weight blocks at about the same time, so DRAM serves each once
 // and L2 the rest (with the token tile fastest, one cluster ran the token
 // tiles of a group back to back and re-read its weights from DRAM for each).
+#ifndef DFL_GEMM_LAND_PIPE  // 1: a finaliser's next chunk of split-K parts lands during the current one
+#define DFL_GEMM_LAND_PIPE 1
+#endif
 #ifndef DFL_GEMM_TT_SLOW
 #define DFL_GEMM_TT_SLOW 1
 #endif
@@ -566,7 +569,11 @@ DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, con
   }
 }
 
-template <int MODE, bool FP8>
+// BIG: token tiles of 128+ rows (batched rounds, prefill), whose split tiles
+// are finalised in several chunks by one CTA; only this instance carries the
+// pipelined landing of a finaliser's next chunk (its code slowed the
+// small-tile instance by ~1 % even where it never ran).
+template <int MODE, bool FP8, bool BIG>
 __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -587,8 +594,8 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
   uint64_t* tfull = conv + stages;
   uint64_t* tempty = tfull + 2;
   uint64_t* mdone = tempty + 2;
-  uint64_t* red = mdone + 1;  // split-K parts landed in red_buf
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red + 1);
+  uint64_t* red = mdone + 1;  // [2] split-K parts landed (one barrier per landing buffer)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red + 2);
   int* flag = reinterpret_cast<int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -607,6 +614,7 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
     mbar_init(tempty + 1, EPI_THREADS);
     mbar_init(mdone, 1);
     mbar_init(red, 1);
+    mbar_init(red + 1, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -897,7 +905,7 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
     // the main loop streams: the finalisation then issues no load for them
     int seg = 0;
     const int first_tile = u0 / KB;  // this CTA's first segment's scheduled tile
-    uint32_t red_phase = 0;
+    uint32_t red_phase = 0;  // bit b: the parity of landing barrier red[b]'s next phase
     for (int u = u0; u < u1; ++seg) {
       const int tile_s = u / KB;  // scheduled tile
       const int seg_end = (tile_s + 1) * KB < u1 ? (tile_s + 1) * KB : u1;
@@ -1022,6 +1030,34 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
         const int cap_items = ring_free ? (stages * stage_bytes) / (RED_CHUNK * 4) : p.red_items;
         const int nparts = c_last - c_first + 1;
         const int nch = (mt + ct - 1) / ct;
+        // With room for two chunks' parts (the ring free), the parts of this
+        // finaliser's next chunk land while the current one is reduced and
+        // run through the epilogue.
+        const int half = cap_items / 2;
+        const bool pipe = BIG && DFL_GEMM_LAND_PIPE && ring_free && 2 * nparts <= half && rank + npar < nch;
+        auto issue_chunk = [&](int ch, int buf) {  // thread et == 0
+          const int tc0 = ch * ct;
+          const int subs = (mt - tc0) > 16 && ct == 32 ? 2 : 1;
+          const int nitems = nparts * subs;
+          float* dst = land + (size_t)buf * half * RED_CHUNK;
+          fence_proxy_async_global();  // parts acquired through the tile counter
+          mbar_arrive_expect_tx(red + buf, (uint32_t)(nitems * RED_CHUNK * 4));
+#pragma unroll 1
+          for (int k = 0; k < nitems; ++k) {
+            const int sub = k >= nparts ? 1 : 0;
+            const int cc = c_first + k - sub * nparts;
+            const int sl = cc == c_first ? sl_first : 0;
+            bulk_load(dst + k * RED_CHUNK,
+                      p.ws + (size_t)((cc * CL + crank) * 2 + sl) * (DFL_BN_MAX * 128) + (size_t)(tc0 + 16 * sub) * 128,
+                      RED_CHUNK * 4, red + buf);
+          }
+        };
+        int pbuf = 0;           // pipelined: the buffer of the current chunk
+        unsigned in_flight = 0; // pipelined: bit b set while buffer b's copies are issued and not waited for
+        if (pipe) {
+          if (et == 0) issue_chunk(rank, 0);
+          in_flight = 1u;
+        }
         for (int ch = rank; ch < nch && !aborted; ch += npar) {
           const int tc0 = ch * ct;
           const int subs = (mt - tc0) > 16 && ct == 32 ? 2 : 1;  // 16-token slices in this chunk
@@ -1029,28 +1065,19 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
 #pragma unroll
           for (int i = 0; i < 16; ++i) v0[i] = v1[i] = 0.f;
           const int nitems = nparts * subs;  // (sub, part), part fastest
-          for (int it0 = 0; it0 < nitems && !aborted; it0 += cap_items) {
-            const int nb = (nitems - it0) < cap_items ? (nitems - it0) : cap_items;
-            if (et == 0) {
-              fence_proxy_async_global();  // parts acquired through the tile counter
-              mbar_arrive_expect_tx(red, (uint32_t)(nb * RED_CHUNK * 4));
-#pragma unroll 1
-              for (int k = 0; k < nb; ++k) {
-                const int item = it0 + k;
-                const int sub = item >= nparts ? 1 : 0;
-                const int cc = c_first + item - sub * nparts;
-                const int sl = cc == c_first ? sl_first : 0;
-                bulk_load(land + k * RED_CHUNK,
-                          p.ws + (size_t)((cc * CL + crank) * 2 + sl) * (DFL_BN_MAX * 128) + (size_t)(tc0 + 16 * sub) * 128,
-                          RED_CHUNK * 4, red);
-              }
+          if (pipe) {
+            if (ch + npar < nch) {
+              if (et == 0) issue_chunk(ch + npar, pbuf ^ 1);
+              in_flight |= 1u << (pbuf ^ 1);
             }
-            if (!mbar_wait(red, red_phase, p.status, &aborted)) break;
-            red_phase ^= 1u;
+            if (!mbar_wait(red + pbuf, (red_phase >> pbuf) & 1u, p.status, &aborted)) break;
+            red_phase ^= 1u << pbuf;
+            in_flight &= ~(1u << pbuf);
+            const float* lb = land + (size_t)pbuf * half * RED_CHUNK + r;
 #pragma unroll 1
-            for (int k = 0; k < nb; ++k) {
-              const float* src = land + k * RED_CHUNK + r;
-              if (it0 + k < nparts) {
+            for (int k = 0; k < nitems; ++k) {
+              const float* src = lb + k * RED_CHUNK;
+              if (k < nparts) {
 #pragma unroll
                 for (int i = 0; i < 16; ++i) v0[i] += src[i * 128];
               } else {
@@ -1058,7 +1085,38 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
                 for (int i = 0; i < 16; ++i) v1[i] += src[i * 128];
               }
             }
-            named_bar_sync(1, EPI_THREADS);  // landing area free for the next batch
+          } else {
+            for (int it0 = 0; it0 < nitems && !aborted; it0 += cap_items) {
+              const int nb = (nitems - it0) < cap_items ? (nitems - it0) : cap_items;
+              if (et == 0) {
+                fence_proxy_async_global();  // parts acquired through the tile counter
+                mbar_arrive_expect_tx(red, (uint32_t)(nb * RED_CHUNK * 4));
+#pragma unroll 1
+                for (int k = 0; k < nb; ++k) {
+                  const int item = it0 + k;
+                  const int sub = item >= nparts ? 1 : 0;
+                  const int cc = c_first + item - sub * nparts;
+                  const int sl = cc == c_first ? sl_first : 0;
+                  bulk_load(land + k * RED_CHUNK,
+                            p.ws + (size_t)((cc * CL + crank) * 2 + sl) * (DFL_BN_MAX * 128) + (size_t)(tc0 + 16 * sub) * 128,
+                            RED_CHUNK * 4, red);
+                }
+              }
+              if (!mbar_wait(red, red_phase & 1u, p.status, &aborted)) break;
+              red_phase ^= 1u;
+#pragma unroll 1
+              for (int k = 0; k < nb; ++k) {
+                const float* src = land + k * RED_CHUNK + r;
+                if (it0 + k < nparts) {
+#pragma unroll
+                  for (int i = 0; i < 16; ++i) v0[i] += src[i * 128];
+                } else {
+#pragma unroll
+                  for (int i = 0; i < 16; ++i) v1[i] += src[i * 128];
+                }
+              }
+              named_bar_sync(1, EPI_THREADS);  // landing area free for the next batch
+            }
           }
 #pragma unroll
           for (int i = 0; i < 16; ++i) stg[i * 128 + r] = v0[i];
@@ -1069,8 +1127,15 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
           named_bar_sync(1, EPI_THREADS);
           epi_final<MODE>(p, (int)tile, t_base + tc0, (mt - tc0) < ct ? (mt - tc0) : ct, stg, ew, lane, tab,
                           t_base, cx, cx_key, gq, gk, use_hpre, hpre, gpre, rnd);
-          named_bar_sync(1, EPI_THREADS);
+          named_bar_sync(1, EPI_THREADS);  // staging (and, pipelined, this chunk's landing buffer) free
+          pbuf ^= 1;
         }
+        // gave up while copies were in flight: they land before the CTA moves on
+        for (int b = 0; b < 2; ++b)
+          if (in_flight & (1u << b)) {
+            bool drain_abort = false;
+            mbar_wait(red + b, (red_phase >> b) & 1u, p.status, &drain_abort);
+          }
         // several slices: the last finaliser to finish clears the tile's counters
         if (nsl > 1 && et == 0) {
           if (atomicAdd(p.tile_fin + tile, 1u) == (unsigned)(npar - 1)) {
@@ -1156,7 +1221,7 @@ int gemm_red_items(int BN, int stages, int fp8) {
 
 size_t gemm_smem_bytes(int BN, int stages, int fp8) {
   return 1024 + (size_t)stages * (A_STAGE_BYTES + BN * 128 + (fp8 ? DFL_WBLK8_BYTES : 0)) + STG_BYTES +
-         (size_t)gemm_red_items(BN, stages, fp8) * RED_CHUNK * 4 + TOKTAB_BYTES + (size_t)(3 * stages + 6) * 8 + 16;
+         (size_t)gemm_red_items(BN, stages, fp8) * RED_CHUNK * 4 + TOKTAB_BYTES + (size_t)(3 * stages + 7) * 8 + 16;
 }
 
 // Weight-ring depth.  Six 16 KB stages per SM already keep HBM streaming at
@@ -1172,20 +1237,35 @@ int gemm_pick_stages(int BN, int mode, int fp8) {
   return st > DFL_GEMM_MAX_STAGES ? DFL_GEMM_MAX_STAGES : st;
 }
 
+template <int MODE, bool FP8>
+cudaError_t set_smem_attr(int big) {
+  const cudaFuncAttribute A = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  return big ? cudaFuncSetAttribute(k_gemm<MODE, FP8, true>, A, 232448)
+             : cudaFuncSetAttribute(k_gemm<MODE, FP8, false>, A, 232448);
+}
+
+template <int MODE, bool FP8>
+cudaError_t launch_inst(cudaLaunchConfig_t* cfg, const CUtensorMap& B, const GemmParams& p) {
+  return p.BN >= 128 ? cudaLaunchKernelEx(cfg, k_gemm<MODE, FP8, true>, B, p)
+                     : cudaLaunchKernelEx(cfg, k_gemm<MODE, FP8, false>, B, p);
+}
+
 cudaError_t gemm_init_attributes() {
   cudaError_t e;
-  const int A = cudaFuncAttributeMaxDynamicSharedMemorySize;
-  if ((e = cudaFuncSetAttribute(k_gemm<GM_QKV, false>, (cudaFuncAttribute)A, 232448))) return e;
-  if ((e = cudaFuncSetAttribute(k_gemm<GM_INJECT, false>, (cudaFuncAttribute)A, 232448))) return e;
-  if ((e = cudaFuncSetAttribute(k_gemm<GM_RESID, false>, (cudaFuncAttribute)A, 232448))) return e;
-  if ((e = cudaFuncSetAttribute(k_gemm<GM_SWIGLU, false>, (cudaFuncAttribute)A, 232448))) return e;
-  if ((e = cudaFuncSetAttribute(k_gemm<GM_FC, false>, (cudaFuncAttribute)A, 232448))) return e;
-  if ((e = cudaFuncSetAttribute(k_gemm<GM_ARGMAX, false>, (cudaFuncAttribute)A, 232448))) return e;
-  if ((e = cudaFuncSetAttribute(k_gemm<GM_QKV, true>, (cudaFuncAttribute)A, 232448))) return e;
-  if ((e = cudaFuncSetAttribute(k_gemm<GM_INJECT, true>, (cudaFuncAttribute)A, 232448))) return e;
-  if ((e = cudaFuncSetAttribute(k_gemm<GM_RESID, true>, (cudaFuncAttribute)A, 232448))) return e;
-  if ((e = cudaFuncSetAttribute(k_gemm<GM_SWIGLU, true>, (cudaFuncAttribute)A, 232448))) return e;
-  return cudaFuncSetAttribute(k_gemm<GM_ARGMAX, true>, (cudaFuncAttribute)A, 232448);
+  for (int big = 0; big < 2; ++big) {
+    if ((e = set_smem_attr<GM_QKV, false>(big))) return e;
+    if ((e = set_smem_attr<GM_INJECT, false>(big))) return e;
+    if ((e = set_smem_attr<GM_RESID, false>(big))) return e;
+    if ((e = set_smem_attr<GM_SWIGLU, false>(big))) return e;
+    if ((e = set_smem_attr<GM_FC, false>(big))) return e;
+    if ((e = set_smem_attr<GM_ARGMAX, false>(big))) return e;
+    if ((e = set_smem_attr<GM_QKV, true>(big))) return e;
+    if ((e = set_smem_attr<GM_INJECT, true>(big))) return e;
+    if ((e = set_smem_attr<GM_RESID, true>(big))) return e;
+    if ((e = set_smem_attr<GM_SWIGLU, true>(big))) return e;
+    if ((e = set_smem_attr<GM_ARGMAX, true>(big))) return e;
+  }
+  return cudaSuccess;
 }
 
 int gemm_max_clusters(int BN, int stages, int cl) {
@@ -1201,7 +1281,7 @@ int gemm_max_clusters(int BN, int stages, int cl) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, k_gemm<GM_ARGMAX, false>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, k_gemm<GM_ARGMAX, false, true>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -1231,17 +1311,12 @@ cudaError_t gemm_launch(const CUtensorMap& B, const GemmParams& p, int grid, cud
   cfg.attrs = attr;
   cfg.numAttrs = (unsigned)na;
   switch (p.mode) {
-    case GM_QKV: return p.a_fp8 ? cudaLaunchKernelEx(&cfg, k_gemm<GM_QKV, true>, B, p)
-                                : cudaLaunchKernelEx(&cfg, k_gemm<GM_QKV, false>, B, p);
-    case GM_INJECT: return p.a_fp8 ? cudaLaunchKernelEx(&cfg, k_gemm<GM_INJECT, true>, B, p)
-                                   : cudaLaunchKernelEx(&cfg, k_gemm<GM_INJECT, false>, B, p);
-    case GM_RESID: return p.a_fp8 ? cudaLaunchKernelEx(&cfg, k_gemm<GM_RESID, true>, B, p)
-                                  : cudaLaunchKernelEx(&cfg, k_gemm<GM_RESID, false>, B, p);
-    case GM_SWIGLU: return p.a_fp8 ? cudaLaunchKernelEx(&cfg, k_gemm<GM_SWIGLU, true>, B, p)
-                                   : cudaLaunchKernelEx(&cfg, k_gemm<GM_SWIGLU, false>, B, p);
-    case GM_FC: return cudaLaunchKernelEx(&cfg, k_gemm<GM_FC, false>, B, p);  // the fusion projection stays bf16
-    case GM_ARGMAX: return p.a_fp8 ? cudaLaunchKernelEx(&cfg, k_gemm<GM_ARGMAX, true>, B, p)
-                                   : cudaLaunchKernelEx(&cfg, k_gemm<GM_ARGMAX, false>, B, p);
+    case GM_QKV: return p.a_fp8 ? launch_inst<GM_QKV, true>(&cfg, B, p) : launch_inst<GM_QKV, false>(&cfg, B, p);
+    case GM_INJECT: return p.a_fp8 ? launch_inst<GM_INJECT, true>(&cfg, B, p) : launch_inst<GM_INJECT, false>(&cfg, B, p);
+    case GM_RESID: return p.a_fp8 ? launch_inst<GM_RESID, true>(&cfg, B, p) : launch_inst<GM_RESID, false>(&cfg, B, p);
+    case GM_SWIGLU: return p.a_fp8 ? launch_inst<GM_SWIGLU, true>(&cfg, B, p) : launch_inst<GM_SWIGLU, false>(&cfg, B, p);
+    case GM_FC: return launch_inst<GM_FC, false>(&cfg, B, p);  // the fusion projection stays bf16
+    case GM_ARGMAX: return p.a_fp8 ? launch_inst<GM_ARGMAX, true>(&cfg, B, p) : launch_inst<GM_ARGMAX, false>(&cfg, B, p);
   }
   return cudaErrorInvalidValue;
 }
