@@ -569,10 +569,11 @@ DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, con
   }
 }
 
-// BIG: token tiles of 128+ rows (batched rounds, prefill), whose split tiles
-// are finalised in several chunks by one CTA; only this instance carries the
-// pipelined landing of a finaliser's next chunk (its code slowed the
-// small-tile instance by ~1 % even where it never ran).
+// BIG: token tiles of 128+ rows (batched rounds, prefill), shared by a
+// cluster, whose split tiles are finalised in several chunks by one CTA;
+// only this instance carries the clusters and the pipelined landing of a
+// finaliser's next chunk (that code slowed the small-tile instance by ~1 %
+// even where it never ran).
 template <int MODE, bool FP8, bool BIG>
 __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
@@ -625,7 +626,7 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   // cluster peers write into this CTA's stages and signal its barriers
-  if (p.cl > 1) cluster_sync_all();
+  if (BIG && p.cl > 1) cluster_sync_all();
   const uint32_t tmem = *tmem_slot;
   // The QKV projection's dependent, the block attention, reads the page
   // tables and context pages before its own wait: it may launch only once
@@ -647,7 +648,7 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
   // Units (scheduled tile, k-block) are divided over the clusters; the CTAs
   // of a cluster run the same units in lockstep, each on its own n-tile.
   const int KB = p.kblocks;
-  const int CL = p.cl;
+  const int CL = BIG ? p.cl : 1;  // clusters share token tiles of 128+ rows only
   const int crank = CL > 1 ? (int)cluster_ctarank() : 0;
   const uint16_t cmask = (uint16_t)((1u << CL) - 1u);
   // Clusters taking part: the grid holds at most one per unit (tile without
@@ -1171,7 +1172,7 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
 
   __syncthreads();
   // no CTA leaves while a peer may still write into it or signal its barriers
-  if (p.cl > 1) cluster_sync_all();
+  if (BIG && p.cl > 1) cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, ncols);
