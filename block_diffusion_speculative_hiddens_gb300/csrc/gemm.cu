@@ -569,12 +569,14 @@ DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, con
   }
 }
 
-// BIG: token tiles of 128+ rows (batched rounds, prefill), shared by a
+// TIER 2: token tiles of 128+ rows (batched rounds, prefill), shared by a
 // cluster, whose split tiles are finalised in several chunks by one CTA;
 // only this instance carries the clusters and the pipelined landing of a
-// finaliser's next chunk (that code slowed the small-tile instance by ~1 %
-// even where it never ran).
-template <int MODE, bool FP8, bool BIG>
+// finaliser's next chunk (that code slowed the small-tile instances by ~1 %
+// even where it never ran).  TIER 0: one tile of at most 16 tokens (a
+// batch-1 round), finalised whole by its last arriving part: no slices.
+// TIER 1: the rest.
+template <int MODE, bool FP8, int TIER>
 __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -626,7 +628,7 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   // cluster peers write into this CTA's stages and signal its barriers
-  if (BIG && p.cl > 1) cluster_sync_all();
+  if (TIER == 2 && p.cl > 1) cluster_sync_all();
   const uint32_t tmem = *tmem_slot;
   // The QKV projection's dependent, the block attention, reads the page
   // tables and context pages before its own wait: it may launch only once
@@ -648,7 +650,7 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
   // Units (scheduled tile, k-block) are divided over the clusters; the CTAs
   // of a cluster run the same units in lockstep, each on its own n-tile.
   const int KB = p.kblocks;
-  const int CL = BIG ? p.cl : 1;  // clusters share token tiles of 128+ rows only
+  const int CL = TIER == 2 ? p.cl : 1;  // clusters share token tiles of 128+ rows only
   const int crank = CL > 1 ? (int)cluster_ctarank() : 0;
   const uint16_t cmask = (uint16_t)((1u << CL) - 1u);
   // Clusters taking part: the grid holds at most one per unit (tile without
@@ -969,7 +971,7 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
         c_last = cta_of_unit(tile_s * KB + KB - 1, U, G);
       }
       const bool split = c_first != c_last;
-      const int nsl = (mt + 15) >> 4;  // 16-token slices of the tile
+      const int nsl = TIER == 0 ? 1 : (mt + 15) >> 4;  // 16-token slices of the tile
       int rank = 0, npar = 1, ct = 16;  // finalisers; tokens per chunk a finaliser takes at once
       if (split) {
         const int my_slot = tile_s == first_tile ? 0 : 1;
@@ -1035,7 +1037,7 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
         // finaliser's next chunk land while the current one is reduced and
         // run through the epilogue.
         const int half = cap_items / 2;
-        const bool pipe = BIG && DFL_GEMM_LAND_PIPE && ring_free && 2 * nparts <= half && rank + npar < nch;
+        const bool pipe = TIER == 2 && DFL_GEMM_LAND_PIPE && ring_free && 2 * nparts <= half && rank + npar < nch;
         auto issue_chunk = [&](int ch, int buf) {  // thread et == 0
           const int tc0 = ch * ct;
           const int subs = (mt - tc0) > 16 && ct == 32 ? 2 : 1;
@@ -1172,7 +1174,7 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
 
   __syncthreads();
   // no CTA leaves while a peer may still write into it or signal its barriers
-  if (BIG && p.cl > 1) cluster_sync_all();
+  if (TIER == 2 && p.cl > 1) cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, ncols);
@@ -1239,21 +1241,23 @@ int gemm_pick_stages(int BN, int mode, int fp8) {
 }
 
 template <int MODE, bool FP8>
-cudaError_t set_smem_attr(int big) {
+cudaError_t set_smem_attr(int tier) {
   const cudaFuncAttribute A = cudaFuncAttributeMaxDynamicSharedMemorySize;
-  return big ? cudaFuncSetAttribute(k_gemm<MODE, FP8, true>, A, 232448)
-             : cudaFuncSetAttribute(k_gemm<MODE, FP8, false>, A, 232448);
+  return tier == 2   ? cudaFuncSetAttribute(k_gemm<MODE, FP8, 2>, A, 232448)
+         : tier == 1 ? cudaFuncSetAttribute(k_gemm<MODE, FP8, 1>, A, 232448)
+                     : cudaFuncSetAttribute(k_gemm<MODE, FP8, 0>, A, 232448);
 }
 
 template <int MODE, bool FP8>
 cudaError_t launch_inst(cudaLaunchConfig_t* cfg, const CUtensorMap& B, const GemmParams& p) {
-  return p.BN >= 128 ? cudaLaunchKernelEx(cfg, k_gemm<MODE, FP8, true>, B, p)
-                     : cudaLaunchKernelEx(cfg, k_gemm<MODE, FP8, false>, B, p);
+  if (p.BN >= 128) return cudaLaunchKernelEx(cfg, k_gemm<MODE, FP8, 2>, B, p);
+  if (p.M <= 16 && p.t_tiles == 1 && !p.m_dyn) return cudaLaunchKernelEx(cfg, k_gemm<MODE, FP8, 0>, B, p);
+  return cudaLaunchKernelEx(cfg, k_gemm<MODE, FP8, 1>, B, p);
 }
 
 cudaError_t gemm_init_attributes() {
   cudaError_t e;
-  for (int big = 0; big < 2; ++big) {
+  for (int big = 0; big < 3; ++big) {
     if ((e = set_smem_attr<GM_QKV, false>(big))) return e;
     if ((e = set_smem_attr<GM_INJECT, false>(big))) return e;
     if ((e = set_smem_attr<GM_RESID, false>(big))) return e;
@@ -1282,7 +1286,7 @@ int gemm_max_clusters(int BN, int stages, int cl) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, k_gemm<GM_ARGMAX, false, true>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, k_gemm<GM_ARGMAX, false, 2>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
