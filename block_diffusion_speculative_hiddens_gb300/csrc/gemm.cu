@@ -354,8 +354,9 @@ DFL_DEV void fill_ctx(const GemmParams& p, const TokTab& tb, int tab_t0, int t_f
 // shared-memory table tab (its first token tab_t0).  gq/gk: QKV's q/k
 // head-norm gains (load_head_gain); hpre (use_hpre, RESID): residual values
 // of tokens ew+4q of a single token tile, loaded when the tile started;
-// gpre: the tile's gains (RESID/FC).
-template <int MODE>
+// gpre: the tile's gains (RESID/FC).  TIER 0 (one tile of at most 16
+// tokens): one token group, its contexts always those filled with the table.
+template <int MODE, int TIER>
 DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, const float* stg, int ew, int lane,
                        const TokTab& tab, int tab_t0, TokCtx (&cx)[2], int& cx_key, const float* gq, const float* gk,
                        bool use_hpre, const float (&hpre)[EPI_TOK][4], const float (&gpre)[4], int rnd) {
@@ -369,7 +370,7 @@ DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, con
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) rs[jj] = sc[lane + 32 * jj];
   }
-  if constexpr (MODE != GM_FC && MODE != GM_RESID) {
+  if constexpr (MODE != GM_FC && MODE != GM_RESID && TIER != 0) {
     if (cx_key != t_first * 64 + ntok) {
 #pragma unroll
       for (int gi = 0; gi < 2; ++gi)
@@ -378,7 +379,7 @@ DFL_DEV void epi_final(const GemmParams& p, int tile, int t_first, int ntok, con
     }
   }
 #pragma unroll 1
-  for (int gi = 0; gi < 2; ++gi) {
+  for (int gi = 0; gi < (TIER == 0 ? 1 : 2); ++gi) {
     const int j0 = ew + 16 * gi;
     if (j0 >= ntok) break;
     bool ok[EPI_TOK];
@@ -1063,7 +1064,7 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
         }
         for (int ch = rank; ch < nch && !aborted; ch += npar) {
           const int tc0 = ch * ct;
-          const int subs = (mt - tc0) > 16 && ct == 32 ? 2 : 1;  // 16-token slices in this chunk
+          const int subs = TIER != 0 && (mt - tc0) > 16 && ct == 32 ? 2 : 1;  // 16-token slices in this chunk
           float v0[16], v1[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) v0[i] = v1[i] = 0.f;
@@ -1128,7 +1129,7 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
             for (int i = 0; i < 16; ++i) stg[(16 + i) * 128 + r] = v1[i];
           }
           named_bar_sync(1, EPI_THREADS);
-          epi_final<MODE>(p, (int)tile, t_base + tc0, (mt - tc0) < ct ? (mt - tc0) : ct, stg, ew, lane, tab,
+          epi_final<MODE, TIER>(p, (int)tile, t_base + tc0, (mt - tc0) < ct ? (mt - tc0) : ct, stg, ew, lane, tab,
                           t_base, cx, cx_key, gq, gk, use_hpre, hpre, gpre, rnd);
           named_bar_sync(1, EPI_THREADS);  // staging (and, pipelined, this chunk's landing buffer) free
           pbuf ^= 1;
@@ -1149,7 +1150,7 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
       } else {
         for (int tc0 = 0; tc0 < mt; tc0 += 32) {
           float v0[16], v1[16];
-          const bool two = tc0 + 16 < BN;  // a second 16-column chunk in this 32-token chunk
+          const bool two = TIER != 0 && tc0 + 16 < BN;  // a second 16-column chunk in this 32-token chunk
           tmem_ld16(taddr + (uint32_t)tc0, v0);
           if (two) tmem_ld16(taddr + (uint32_t)(tc0 + 16), v1);
 #pragma unroll
@@ -1159,7 +1160,7 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
             for (int i = 0; i < 16; ++i) stg[(16 + i) * 128 + r] = v1[i];
           }
           named_bar_sync(1, EPI_THREADS);
-          epi_final<MODE>(p, (int)tile, t_base + tc0, (mt - tc0) < 32 ? (mt - tc0) : 32, stg, ew, lane, tab,
+          epi_final<MODE, TIER>(p, (int)tile, t_base + tc0, (mt - tc0) < 32 ? (mt - tc0) : 32, stg, ew, lane, tab,
                           t_base, cx, cx_key, gq, gk, use_hpre, hpre, gpre, rnd);
           named_bar_sync(1, EPI_THREADS);
         }
