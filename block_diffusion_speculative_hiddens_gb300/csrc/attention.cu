@@ -535,9 +535,10 @@ __global__ void __launch_bounds__(G * KS * 32) k_attn(const AttnParams p) {
 // P V of its page is done, so a CTA streams (stages) pages per (HBM round
 // trip + page latency); measured per page on a 32K context: ~1.7 us from a
 // load's issue to its landing, ~1.6 us from landing to the end of its P V.
-// Five stages of 32 KB therefore stream ~40 % more than four, and to make
-// room P has a single buffer: a page's P is written once the previous page's
-// P V is done (by then long since, as P V is issued the moment P lands).
+// Q therefore lives in tensor memory (the S MMA's A operand) and P has a
+// single buffer -- a page's P is written once the previous page's P V is
+// done, by then long since, as P V is issued the moment P lands -- leaving
+// shared memory to six 32 KB page stages.
 // Warps: 0 page loads (one thread), 1 TMEM allocation and MMA issue (one
 // thread), 2-9 softmax: two threads per query row (TMEM lane), each taking 32
 // of a page's 64 keys and half of the output columns; the pair trades its
