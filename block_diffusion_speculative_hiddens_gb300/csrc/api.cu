@@ -105,6 +105,7 @@ struct dflash_handle {
   bool attn_tc = false;      // tcgen05 attention page loop
   bool attn_global = false;  // splits merged through global memory (no cluster)
   float* attn_part = nullptr;
+  int* attn_order = nullptr;  // [max_batch] the attention grid's request order (longest first)
   int max_tiles = 0;
   // weights, copied into the workspace at create: matrices packed into
   // 128x64 blocks (f16, except the bf16 fusion projection), gains as fp32
@@ -324,6 +325,7 @@ size_t carve(dflash_handle* h, const dflash_config& c, char* base, int num_sms) 
   o->act = w.take<f16>((size_t)M * I);
   o->keys = w.take<unsigned long long>(M);
   o->bctx = w.take<int2>(M);
+  o->attn_order = w.take<int>(c.max_batch);
   o->brope = w.take<float2>((size_t)M * (D / 2));
   o->done_ctr = w.take<unsigned>(64);
   o->cg = w.take<f16>((size_t)R * H);
@@ -579,6 +581,9 @@ int draft_impl(dflash_handle* h, const int32_t* slots, int32_t batch, const int3
   bcx.slots_ok = h->slots_ok;
   bcx.max_slots = c.max_slots;
   bcx.brope = h->brope;
+  // with several requests, the attention grid takes them longest first: its
+  // CTAs start in grid order, so the short requests fill the last wave
+  bcx.order = batch > 1 ? h->attn_order : nullptr;
   rc = cuda_err(launch_embed(slots, batch, last_tok, c.mask_id, c.vocab, h->embed_pk, h->embed_sc, h->in_norm[0], H, h->h,
                              h->hg, h->ss_a, h->keys, bcx, h->status, s));
   if (rc) return rc;
@@ -631,6 +636,7 @@ int draft_impl(dflash_handle* h, const int32_t* slots, int32_t batch, const int3
       a.block = c.block;
       a.causal = target ? 1 : 0;
       a.n_valid = vf.n_valid;
+      a.order = batch > 1 ? h->attn_order : nullptr;
       a.early = fold ? 0 : 1;  // a folded QKV projection appends context rows itself
       a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
       a.status = h->status;

@@ -178,7 +178,7 @@ __global__ void __launch_bounds__(G * KS * 32) k_attn(const AttnParams p) {
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + C::STAGES * C::STAGE_BYTES);
   int* pids = reinterpret_cast<int*>(sm + C::STAGES * C::STAGE_BYTES + 128);
 
-  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int split = blockIdx.x, kvh = blockIdx.y, b = p.order ? p.order[blockIdx.z] : (int)blockIdx.z;
   const int head0 = kvh * G;  // first query head
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hw = warp % G;    // query head of this warp within the group
@@ -593,7 +593,7 @@ __global__ void __launch_bounds__(320, 1) k_attn_tc(const AttnParams p) {
   // trade waits for the partner's same tag), so two parity slots suffice.
   volatile unsigned long long* xch = reinterpret_cast<volatile unsigned long long*>(sm + C::OFF_X);
 
-  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int split = blockIdx.x, kvh = blockIdx.y, b = p.order ? p.order[blockIdx.z] : (int)blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rows = G * 16;
   for (int i = threadIdx.x; i < 512; i += blockDim.x) xch[i] = 0xFFFFFFFF00000000ull;  // no tag yet

@@ -134,6 +134,8 @@ struct AttnParams {
   int early;           // 1: the page list and the pages holding no block row are read before the wait on
                        // the QKV projection (which then wrote no context row: not a folded injection)
   const int* n_valid;  // causal: [batch] live rows (null: block); keys = context + n_valid
+  const int* order;    // [batch] request of grid row z (null: z itself): longest first, so the CTAs of
+                       // the longest requests start first and the short ones fill the last wave
   float scale_log2;    // log2(e) / sqrt(D)
   uint32_t* status;
   unsigned long long* trace;  // optional [grid][8] timeline (null: off)
@@ -183,6 +185,7 @@ struct BlockCtx {
   int* slots_ok;  // [batch] out: slots with out-of-range ones replaced by 0
   int2* bctx;
   float2* brope;
+  int* order;  // [batch] out (null: not written): the requests by descending key count, for the attention grid
 };
 cudaError_t launch_embed(const int* slots, int batch, const int* last_tok, int mask_id, int vocab,
                          const void* embed_pk, const float* embed_scale, const float* gain, int H, float* h, f16* hg,

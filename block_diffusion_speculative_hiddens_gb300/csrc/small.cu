@@ -147,6 +147,23 @@ __global__ void k_embed(const int* __restrict__ slots, const int* __restrict__ l
     if (lane == 0) ss[(size_t)part * M + t] = sq;
   }
   if (threadIdx.x == 0) keys[t] = 0ull;
+  if (bc.order && t == 0) {
+    // the requests by descending context length (ties: request order), for
+    // the attention grid: request j's rank is the count of requests that
+    // come before it
+    const int batch = M / DFL_BLOCK;
+    for (int j = threadIdx.x; j < batch; j += blockDim.x) {
+      const int sj = slots[j];
+      const int lj = (sj >= 0 && sj < bc.max_slots) ? bc.ctx_len[sj] : 0;
+      int rank = 0;
+      for (int k = 0; k < batch; ++k) {
+        const int sk = slots[k];
+        const int lk = (sk >= 0 && sk < bc.max_slots) ? bc.ctx_len[sk] : 0;
+        rank += (lk > lj || (lk == lj && k < j)) ? 1 : 0;
+      }
+      bc.order[rank] = j;
+    }
+  }
   // this token's position (block rows follow the slot's context), page and
   // RoPE row, for every layer's QKV epilogue
   // rows block..15 of a request pad a smaller block: page -2 (computed like
