@@ -90,12 +90,12 @@ DFL_DEV void copy_partial(const AttnParams& p, const float* part, int nf, int sl
 
 // Combines the splits' partials of each (request, KV head): one CTA per 16
 // rows (one query head's block tokens), 16 threads per row, each taking D/16
-// output columns.  Every split's max and sum are loaded at once, then the
-// splits' unnormalised outputs in groups of 8 (all loads of a group issued
-// before any is used), and summed in split order.
+// output columns.  Every split's max and sum and the first 16 splits'
+// unnormalised outputs are loaded at once (one round trip), any further
+// splits' outputs in groups of 16, and summed in split order.
 constexpr int MERGE_TPR = 16;      // threads per row
 constexpr int MERGE_MAX_SPLITS = 32;
-constexpr int MERGE_GROUP = 8;     // splits whose outputs are loaded at once
+constexpr int MERGE_GROUP = 16;    // splits whose outputs are loaded at once
 
 template <int D>
 __global__ void __launch_bounds__(16 * MERGE_TPR) k_attn_merge(const AttnParams p) {
@@ -114,6 +114,7 @@ __global__ void __launch_bounds__(16 * MERGE_TPR) k_attn_merge(const AttnParams 
   const int nsp = p.n_splits;
   const float* base = p.part + (size_t)pair * nsp * PF;
   float mv[MERGE_MAX_SPLITS], lv[MERGE_MAX_SPLITS];
+  float4 v0[MERGE_GROUP][NV];  // the first group's outputs, loaded with the maxima and sums
 #pragma unroll
   for (int sp = 0; sp < MERGE_MAX_SPLITS; ++sp) {
     mv[sp] = -INFINITY;
@@ -123,6 +124,12 @@ __global__ void __launch_bounds__(16 * MERGE_TPR) k_attn_merge(const AttnParams 
       mv[sp] = base[(size_t)sp * PF + rows * PS + r];
     }
   }
+#pragma unroll
+  for (int k = 0; k < MERGE_GROUP; ++k)
+#pragma unroll
+    for (int c4 = 0; c4 < NV; ++c4)
+      v0[k][c4] = k < nsp ? *reinterpret_cast<const float4*>(base + (size_t)k * PF + r * PS + d0 + 4 * c4)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
   float M = -INFINITY;
 #pragma unroll
   for (int sp = 0; sp < MERGE_MAX_SPLITS; ++sp)
@@ -145,8 +152,9 @@ __global__ void __launch_bounds__(16 * MERGE_TPR) k_attn_merge(const AttnParams 
     for (int k = 0; k < MERGE_GROUP; ++k)
 #pragma unroll
       for (int c4 = 0; c4 < NV; ++c4)
-        v[k][c4] = g + k < nsp ? *reinterpret_cast<const float4*>(base + (size_t)(g + k) * PF + r * PS + d0 + 4 * c4)
-                               : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[k][c4] = g == 0 ? v0[k][c4]
+                          : (g + k < nsp ? *reinterpret_cast<const float4*>(base + (size_t)(g + k) * PF + r * PS + d0 + 4 * c4)
+                                         : make_float4(0.f, 0.f, 0.f, 0.f));
 #pragma unroll
     for (int k = 0; k < MERGE_GROUP; ++k) {
       const float w = mv[g + k];  // 0 past the last split
