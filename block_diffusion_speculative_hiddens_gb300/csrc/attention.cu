@@ -45,9 +45,6 @@ DFL_DEV void atrace(const AttnParams& p, int ev) {
   }
 }
 
-#ifndef DFL_ATTN_L2_PF  // 1: a CTA's K/V pages are prefetched into L2 before the dependency wait
-#define DFL_ATTN_L2_PF 0
-#endif
 // The QKV projection before this kernel lets it launch only after that
 // projection's own dependency wait, so every earlier kernel (page
 // allocation, injection, embedding) is complete when this one starts: with
@@ -55,31 +52,6 @@ DFL_DEV void atrace(const AttnParams& p, int ev) {
 // block row are read at once, and the block's own K/V and its queries,
 // written by the projection, only after this kernel's wait.  A folded round
 // (the projection also appends the new context rows) clears p.early.
-
-// This CTA's K and V page blocks into L2, issued before the wait on the
-// previous kernel (the QKV projection) -- the context pages were written in
-// earlier rounds.  The slot, length and page ids read here may still be a
-// previous round's (the kernels that update them need not have finished):
-// a prefetch of another page only costs bandwidth, every address is checked
-// to lie inside the pool, and L2 stays coherent with later writes.
-DFL_DEV void attn_l2_prefetch(const AttnParams& p, int b, int split, int kvh, int D) {
-  const int slot = p.slots[b];
-  int npages = (p.ctx_len[slot] + p.block + 63) >> 6;
-  if (npages > p.kv.max_pages_per_slot) npages = p.kv.max_pages_per_slot;
-  if (npages <= 0) return;
-  const int pb = (int)((long long)split * npages / p.n_splits);
-  const int pe = (int)((long long)(split + 1) * npages / p.n_splits);
-  const int* pt = p.kv.page_table + (size_t)slot * p.kv.max_pages_per_slot;
-  const f16* kb = p.kv.k_pool + (size_t)p.layer * p.kv.layer_stride;
-  const f16* vb = p.kv.v_pool + (size_t)p.layer * p.kv.layer_stride;
-  for (int pi = pb; pi < pe; ++pi) {
-    const int pg = pt[pi];
-    if (pg < 0 || pg >= p.kv.max_pages) continue;
-    const size_t off = ((size_t)pg * p.kv.hkv + kvh) * (64 * D);
-    prefetch_l2_bulk(kb + off, (uint32_t)(64 * D * 2));
-    prefetch_l2_bulk(vb + off, (uint32_t)(64 * D * 2));
-  }
-}
 
 // A split's partial (nf floats from shared memory) to its global slot.
 DFL_DEV void copy_partial(const AttnParams& p, const float* part, int nf, int slot, int D) {
@@ -199,7 +171,6 @@ __global__ void __launch_bounds__(G * KS * 32) k_attn(const AttnParams p) {
     atrace(p, 0);
     for (int s = 0; s < C::STAGES; ++s) mbar_init(full + s, 1);
     fence_mbar_init();
-    if (DFL_ATTN_L2_PF) attn_l2_prefetch(p, b, split, kvh, D);
   }
   pdl_launch_dependents();
   if (!p.early) pdl_wait();
@@ -551,18 +522,13 @@ __global__ void __launch_bounds__(G * KS * 32) k_attn(const AttnParams p) {
 // thread), 2-9 softmax: two threads per query row (TMEM lane), each taking 32
 // of a page's 64 keys and half of the output columns; the pair trades its
 // half-row maxima through shared memory once per page.
-#ifndef DFL_ATTN_Q_TMEM  // 1: Q is the S MMA's A operand in tensor memory (else in shared memory)
-#define DFL_ATTN_Q_TMEM 1
-#endif
 template <int D>
 struct TcCfg {
-  static constexpr int STAGES = DFL_ATTN_Q_TMEM ? 6 : 5;  // pages in flight
+  static constexpr int STAGES = 6;                  // pages in flight
   static constexpr int BLK = 64 * D * 2;            // one K (or V^T) page block
   static constexpr int STAGE = 2 * BLK;
-  static constexpr int QB = DFL_ATTN_Q_TMEM ? 0 : 128 * D * 2;  // Q: 128 rows x D, D/64 panels of 16 KB
   static constexpr int PB = 128 * 64 * 2;           // P: 128 rows x 64 keys, one 16 KB panel
-  static constexpr int OFF_Q = STAGES * STAGE;
-  static constexpr int OFF_P = OFF_Q + QB;          // one P buffer
+  static constexpr int OFF_P = STAGES * STAGE;     // one P buffer (Q lives in tensor memory)
   static constexpr int OFF_BAR = OFF_P + PB;
   static constexpr int MAX_PIDS = 512;
   static constexpr int OFF_PIDS = OFF_BAR + 256;
@@ -573,7 +539,7 @@ struct TcCfg {
   static constexpr int Q_COL = 256;                 // Q (tensor-memory A operand): columns [256, 256 + D/2)
   // columns allocated: a power of two covering the buffers, so two CTAs that
   // might share an SM never wait on each other's columns
-  static constexpr uint32_t TMEM_COLS = DFL_ATTN_Q_TMEM ? 512 : 256;
+  static constexpr uint32_t TMEM_COLS = 512;
 };
 
 // TMEM address of lane quarter q4 (lanes 32*q4 ..) at column 0.
@@ -591,7 +557,7 @@ __global__ void __launch_bounds__(320, 1) k_attn_tc(const AttnParams p) {
   uint64_t* s_empty = s_full + 2;           // [2] S read by the softmax warps
   uint64_t* p_full = s_empty + 2;           // P of page i (phase i & 1) in shared memory
   uint64_t* o_full = p_full + 2;            // [2] P V of page i (barrier i & 1) complete
-  uint64_t* q_full = o_full + 2;            // Q in shared memory
+  uint64_t* q_full = o_full + 2;            // Q in tensor memory
   uint64_t* mdone = q_full + 1;             // every issued MMA complete
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mdone + 1);
   int* pids = reinterpret_cast<int*>(sm + C::OFF_PIDS);
@@ -624,7 +590,6 @@ __global__ void __launch_bounds__(320, 1) k_attn_tc(const AttnParams p) {
     mbar_init(q_full, 256);
     mbar_init(mdone, 1);
     fence_mbar_init();
-    if (DFL_ATTN_L2_PF) attn_l2_prefetch(p, b, split, kvh, D);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::TMEM_COLS);
@@ -700,7 +665,6 @@ __global__ void __launch_bounds__(320, 1) k_attn_tc(const AttnParams p) {
     // ------------------------------------------------ MMA issue
     if (lane == 0 && mbar_wait(q_full, 0, p.status, &aborted)) {
       tc_fence_after();
-      const uint32_t q_addr = smem_u32(sm + C::OFF_Q);
       auto issue_s = [&](int i) {
         const int s = i % C::STAGES, bb = i & 1;
         if (!mbar_wait(full + s, (uint32_t)((i / C::STAGES) & 1), p.status, &aborted)) return false;
@@ -710,13 +674,8 @@ __global__ void __launch_bounds__(320, 1) k_attn_tc(const AttnParams p) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t bd = sdesc_sw128(k_addr + (uint32_t)((kk >> 2) * 8192)) + (uint64_t)(2 * (kk & 3));
-          if (DFL_ATTN_Q_TMEM) {
-            tc_mma_f16_ts(tmem + (uint32_t)(C::S_COL + 64 * bb), tmem + (uint32_t)(C::Q_COL + 8 * kk), bd, idesc_s,
-                          kk > 0 ? 1u : 0u);
-          } else {
-            const uint64_t ad = sdesc_sw128(q_addr + (uint32_t)((kk >> 2) * 16384)) + (uint64_t)(2 * (kk & 3));
-            tc_mma_f16(tmem + (uint32_t)(C::S_COL + 64 * bb), ad, bd, idesc_s, kk > 0 ? 1u : 0u);
-          }
+          tc_mma_f16_ts(tmem + (uint32_t)(C::S_COL + 64 * bb), tmem + (uint32_t)(C::Q_COL + 8 * kk), bd, idesc_s,
+                        kk > 0 ? 1u : 0u);
         }
         tc_commit(s_full + bb);
         return true;
@@ -768,27 +727,16 @@ __global__ void __launch_bounds__(320, 1) k_attn_tc(const AttnParams p) {
     {  // this row's query (half of its chunks per thread), zero-padded to 128 rows
       const int h = r >> 4, t = r & 15;
       const f16* src = p.q + ((size_t)(b * DFL_BLOCK + t) * hq + kvh * G + h) * D;
-      if (DFL_ATTN_Q_TMEM) {  // TMEM lane r, columns Q_COL + kh*D/4 ...: two f16 per column
-        uint4 v[D / 16];
+      // TMEM lane r, columns Q_COL + kh*D/4 ...: two f16 per column
+      uint4 v[D / 16];
 #pragma unroll
-        for (int cc = 0; cc < D / 16; ++cc)
-          v[cc] = r < rows ? *reinterpret_cast<const uint4*>(src + (kh * (D / 16) + cc) * 8) : make_uint4(0u, 0u, 0u, 0u);
+      for (int cc = 0; cc < D / 16; ++cc)
+        v[cc] = r < rows ? *reinterpret_cast<const uint4*>(src + (kh * (D / 16) + cc) * 8) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-        for (int j = 0; j < D / 64; ++j)
-          tmem_st16(lane_base_q(tmem, q4) + (uint32_t)(C::Q_COL + kh * (D / 4) + 16 * j),
-                    reinterpret_cast<const float*>(&v[4 * j]));
-        tc_fence_before();
-      } else {
-#pragma unroll
-        for (int cc = 0; cc < D / 16; ++cc) {
-          const int c = kh * (D / 16) + cc;
-          uint4 v = make_uint4(0u, 0u, 0u, 0u);
-          if (r < rows) v = *reinterpret_cast<const uint4*>(src + c * 8);
-          uint8_t* dst = sm + C::OFF_Q + (c >> 3) * 16384 + r * 128 + (((c & 7) ^ (r & 7)) << 4);
-          *reinterpret_cast<uint4*>(dst) = v;
-        }
-        fence_proxy_async_smem();
-      }
+      for (int j = 0; j < D / 64; ++j)
+        tmem_st16(lane_base_q(tmem, q4) + (uint32_t)(C::Q_COL + kh * (D / 4) + 16 * j),
+                  reinterpret_cast<const float*>(&v[4 * j]));
+      tc_fence_before();
       mbar_arrive(q_full);
     }
     const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);

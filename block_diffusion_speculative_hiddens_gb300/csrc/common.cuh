@@ -131,11 +131,7 @@ DFL_DEV void bulk_load_hint(void* dst, const void* src, uint32_t bytes, uint64_t
       "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
-// Bring `bytes` (multiple of 16) at a 16-byte-aligned global address into
-// L2; a hint that completes on its own (no barrier, no destination).
-DFL_DEV void prefetch_l2_bulk(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
+// Bring a tensor map's descriptor on chip before its first use.
 DFL_DEV void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }

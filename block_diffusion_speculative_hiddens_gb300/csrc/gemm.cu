@@ -44,9 +44,6 @@
 #ifndef DFL_GEMM_A_CHUNKS  // bulk copies per 16 KB weight block
 #define DFL_GEMM_A_CHUNKS 1
 #endif
-#ifndef DFL_GEMM_L2_PF  // weight blocks past the ring prefetched into L2 while the previous kernel drains
-#define DFL_GEMM_L2_PF 0
-#endif
 
 
 namespace {
@@ -738,28 +735,6 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
         pkb[i] = kb;
         ptt[i] = tt;
         advance();
-      }
-      if (DFL_GEMM_L2_PF > 0) {
-        // the weight blocks that follow the ring's first fill, into L2, while
-        // the previous kernel still runs (weights do not depend on it): the
-        // main loop then reads them at L2 speed
-        int t2 = tile, k2 = kb;
-        const uint8_t* ap = a_ptr;
-        const int end = n_units < pre + DFL_GEMM_L2_PF ? n_units : pre + DFL_GEMM_L2_PF;
-        for (int i = pre; i < end; ++i) {
-          prefetch_l2_bulk(ap, (uint32_t)blk_bytes);
-          if (++k2 == KBi) {
-            k2 = 0;
-            ++t2;
-            int rest, tt2;
-            sched_decode(p, t2, tl, rest, tt2);
-            int nt = (rest % p.n_tg) * CL + crank;
-            if (nt >= p.n_tiles) nt = p.n_tiles - 1;
-            ap = static_cast<const uint8_t*>(p.a[rest / p.n_tg]) + (size_t)(p.a_tile_off + nt) * KBi * blk_bytes;
-          } else {
-            ap += blk_bytes;
-          }
-        }
       }
       pdl_wait();
       for (int i = 0; i < pre; ++i) load_b(i, pkb[i], ptt[i]);
