@@ -663,28 +663,35 @@ __global__ void __launch_bounds__(320, 1) k_attn_tc(const AttnParams p) {
     }
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issue
-    if (lane == 0 && mbar_wait(q_full, 0, p.status, &aborted)) {
+    // The whole warp runs the loop, converged (waits made warp-uniform), and
+    // one elected lane issues each MMA and commit.
+    auto wait_all = [&](uint64_t* bar, uint32_t par) {
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(bar, par, p.status, &aborted));
+      if (!ok) aborted = true;
+      return ok;
+    };
+    if (wait_all(q_full, 0)) {
       tc_fence_after();
       auto issue_s = [&](int i) {
         const int s = i % C::STAGES, bb = i & 1;
-        if (!mbar_wait(full + s, (uint32_t)((i / C::STAGES) & 1), p.status, &aborted)) return false;
-        if (i >= 2 && !mbar_wait(s_empty + bb, (uint32_t)((i / 2 - 1) & 1), p.status, &aborted)) return false;
+        if (!wait_all(full + s, (uint32_t)((i / C::STAGES) & 1))) return false;
+        if (i >= 2 && !wait_all(s_empty + bb, (uint32_t)((i / 2 - 1) & 1))) return false;
         tc_fence_after();
         const uint32_t k_addr = smem_u32(sm + s * C::STAGE);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t bd = sdesc_sw128(k_addr + (uint32_t)((kk >> 2) * 8192)) + (uint64_t)(2 * (kk & 3));
-          tc_mma_f16_ts(tmem + (uint32_t)(C::S_COL + 64 * bb), tmem + (uint32_t)(C::Q_COL + 8 * kk), bd, idesc_s,
-                        kk > 0 ? 1u : 0u);
+          tc_mma_f16_ts_elect(tmem + (uint32_t)(C::S_COL + 64 * bb), tmem + (uint32_t)(C::Q_COL + 8 * kk), bd, idesc_s,
+                              kk > 0 ? 1u : 0u);
         }
-        tc_commit(s_full + bb);
+        tc_commit_elect(s_full + bb);
         return true;
       };
       bool ok = n == 0 || issue_s(0);
       for (int i = 0; i < n && ok; ++i) {
         if (i + 1 < n && !issue_s(i + 1)) break;
         const int s = i % C::STAGES, bb = i & 1;
-        if (!mbar_wait(p_full, (uint32_t)(i & 1), p.status, &aborted)) break;
+        if (!wait_all(p_full, (uint32_t)(i & 1))) break;
         tc_fence_after();
         const uint32_t p_addr = smem_u32(sm + C::OFF_P);
         const uint32_t v_addr = smem_u32(sm + s * C::STAGE + C::BLK);
@@ -692,13 +699,13 @@ __global__ void __launch_bounds__(320, 1) k_attn_tc(const AttnParams p) {
         for (int kk = 0; kk < 4; ++kk) {
           const uint64_t ad = sdesc_sw128(p_addr) + (uint64_t)(2 * kk);
           const uint64_t bd = sdesc_sw128(v_addr) + (uint64_t)(2 * kk);
-          tc_mma_f16(tmem + (uint32_t)C::O_COL, ad, bd, idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_f16_elect(tmem + (uint32_t)C::O_COL, ad, bd, idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
         }
-        tc_commit(o_full + bb);
-        tc_commit(empty + s);
+        tc_commit_elect(o_full + bb);
+        tc_commit_elect(empty + s);
       }
-      // every MMA this thread issued completes before the columns are freed
-      tc_commit(mdone);
+      // every MMA this warp issued completes before the columns are freed
+      tc_commit_elect(mdone);
       bool drain_abort = false;
       mbar_wait(mdone, 0, p.status, &drain_abort);
     }

@@ -160,23 +160,12 @@ DFL_DEV void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
       : "memory");
 }
-// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16: A's rows are TMEM lanes, each
-// 32-bit column holding two consecutive K elements (the lower in the low half).
-DFL_DEV void tc_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc, uint32_t accum) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accum)
-      : "memory");
-}
 // Arrive once on `bar` when all previously issued tcgen05.mma of this thread complete.
 DFL_DEV void tc_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    smem_u32(bar))
                : "memory");
 }
-// 32 lanes x 16 consecutive 32-bit columns; thread i of the warp gets lane (base+i).
 // Arrive on the barrier at the same offset in every CTA of `mask` once the
 // issuing thread's tensor-core operations so far have completed.
 DFL_DEV void tc_commit_mc(uint64_t* bar, uint16_t mask) {
@@ -184,6 +173,38 @@ DFL_DEV void tc_commit_mc(uint64_t* bar, uint16_t mask) {
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
           smem_u32(bar)),
       "h"(mask)
+      : "memory");
+}
+// tc_mma_f16, its TMEM-operand form and tc_commit issued by the one lane that
+// elect.sync picks from the full, converged warp: the instruction is
+// predicated, not branched around.  An MMA loop run this way by a whole warp
+// (waits included) issues a k-block of four M=128 N=16 MMAs in about half the
+// cycles of the same loop run by one lane.
+DFL_DEV void tc_mma_f16_elect(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accum) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
+      : "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16: A's rows are TMEM lanes, each
+// 32-bit column holding two consecutive K elements (the lower in the low half).
+DFL_DEV void tc_mma_f16_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc, uint32_t accum) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accum)
+      : "memory");
+}
+DFL_DEV void tc_commit_elect(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
       : "memory");
 }
 // Store 16 consecutive columns of this thread's TMEM lane (the warp's lane

@@ -768,8 +768,65 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // Tiles of up to 64 tokens: the whole warp runs the loop, converged
+    // (every wait's outcome made warp-uniform), and one elected lane issues
+    // each MMA and commit -- issued by one lane of an otherwise idle warp, a
+    // k-block's wait, fence and four narrow MMAs took about twice as long.
+    // Tiles of 128+ tokens are bound by the MMAs themselves: one lane issues
+    // (the spinning lanes only cost there), in a loop of its own: the issue
+    // rate of one lane's MMAs depends on the exact code around them.
+    if constexpr (TIER == 2) {
+      if (lane == 0) {
+        const uint32_t idesc = idesc_f16_f32(128, BN, p.ab_type);
+        int it = 0;
+        int seg = 0;
+        int s = 0;
+        uint32_t phase = 0;
+        for (int u = u0; u < u1 && !aborted; ++seg) {
+          const int tile = u / KB;
+          const int seg_end = (tile + 1) * KB < u1 ? (tile + 1) * KB : u1;
+          const int abuf = seg & 1;
+          const uint32_t use = (uint32_t)(seg >> 1);
+          if (!mbar_wait(tempty + abuf, (use & 1u) ^ 1u, p.status, &aborted)) break;
+          tc_fence_after();
+          const uint32_t d = tmem + (uint32_t)(abuf * BN);
+          for (int k = 0; u < seg_end; ++u, ++k, ++it) {
+            if (k > 0 || it > 0) {
+              if (++s == stages) {
+                s = 0;
+                phase ^= 1u;
+              }
+            }
+            if (!mbar_wait((p.a_fp8 ? conv : full) + s, phase, p.status, &aborted)) break;
+            if (it == 0) trace_at(p, 2, globaltimer());
+            tc_fence_after();
+            const uint32_t a_addr = smem_u32(sm + (size_t)s * stage_bytes);
+            const uint64_t adesc = sdesc_sw128(a_addr);
+            const uint64_t bdesc = sdesc_sw128(a_addr + A_STAGE_BYTES);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              tc_mma_f16(d, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk), idesc,
+                          (k > 0 || kk > 0) ? 1u : 0u);
+            if (CL > 1)
+              tc_commit_mc(empty + s, cmask);
+            else
+              tc_commit(empty + s);
+          }
+          tc_commit(tfull + abuf);
+        }
+        trace_at(p, 3, globaltimer());
+        trace_at(p, 6, (unsigned long long)(u1 - u0) | ((unsigned long long)gridDim.x << 32));
+        tc_commit(mdone);
+        bool drain_abort = false;
+        mbar_wait(mdone, 0, p.status, &drain_abort);
+      }
+    } else {
       const uint32_t idesc = idesc_f16_f32(128, BN, p.ab_type);
+      auto wait_all = [&](uint64_t* bar, uint32_t par) {
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(bar, par, p.status, &aborted));
+        if (!ok) aborted = true;
+        return ok;
+      };
       int it = 0;
       int seg = 0;
       int s = 0;
@@ -779,7 +836,7 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
         const int seg_end = (tile + 1) * KB < u1 ? (tile + 1) * KB : u1;
         const int abuf = seg & 1;
         const uint32_t use = (uint32_t)(seg >> 1);
-        if (!mbar_wait(tempty + abuf, (use & 1u) ^ 1u, p.status, &aborted)) break;
+        if (!wait_all(tempty + abuf, (use & 1u) ^ 1u)) break;
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(abuf * BN);
         for (int k = 0; u < seg_end; ++u, ++k, ++it) {
@@ -789,26 +846,25 @@ __global__ void __launch_bounds__(FP8 ? GEMM_THREADS_FP8 : GEMM_THREADS, 1)
               phase ^= 1u;
             }
           }
-          if (!mbar_wait((p.a_fp8 ? conv : full) + s, phase, p.status, &aborted)) break;
-          if (it == 0) trace_at(p, 2, globaltimer());
+          if (!wait_all((FP8 ? conv : full) + s, phase)) break;
+          if (it == 0 && lane == 0) trace_at(p, 2, globaltimer());
           tc_fence_after();
           const uint32_t a_addr = smem_u32(sm + (size_t)s * stage_bytes);
           const uint64_t adesc = sdesc_sw128(a_addr);
           const uint64_t bdesc = sdesc_sw128(a_addr + A_STAGE_BYTES);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            tc_mma_f16(d, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk), idesc,
-                        (k > 0 || kk > 0) ? 1u : 0u);
-          if (CL > 1)
-            tc_commit_mc(empty + s, cmask);
-          else
-            tc_commit(empty + s);
+            tc_mma_f16_elect(d, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk), idesc,
+                             (k > 0 || kk > 0) ? 1u : 0u);
+          tc_commit_elect(empty + s);  // one CTA per cluster below 128 tokens
         }
-        tc_commit(tfull + abuf);
+        tc_commit_elect(tfull + abuf);
       }
-      trace_at(p, 3, globaltimer());
-      trace_at(p, 6, (unsigned long long)(u1 - u0) | ((unsigned long long)gridDim.x << 32));
-      tc_commit(mdone);
+      if (lane == 0) {
+        trace_at(p, 3, globaltimer());
+        trace_at(p, 6, (unsigned long long)(u1 - u0) | ((unsigned long long)gridDim.x << 32));
+      }
+      tc_commit_elect(mdone);
       bool drain_abort = false;
       mbar_wait(mdone, 0, p.status, &drain_abort);
     }
